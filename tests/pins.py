@@ -1,0 +1,336 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics fix.
+
+Each ``check_*`` takes the oracle module(s) as arguments and raises
+AssertionError on a mismatch, so the same check can be run on the oracle
+(``test_oracle_*.py``: must pass) and on copies of it with a planted mistake
+(``test_oracle_mutants.py``: must fail).  None of these checks re-types the
+oracle's own formula: each compares against an independent route (a library
+routine, a brute force, a closed form, an invariant or a worked example from
+the pages).
+"""
+
+from __future__ import annotations
+
+import itertools
+import json
+import math
+from pathlib import Path
+
+import numpy as np
+
+GOLDEN = Path(__file__).resolve().parent / "golden"
+
+
+def golden(name: str) -> dict:
+    return json.loads((GOLDEN / name).read_text())
+
+
+# ----------------------------------------------------------------------------- router
+
+def check_softmax_library(router) -> None:
+    """softmax equals scipy.special.softmax and is shift invariant."""
+    from scipy.special import softmax as sp_softmax
+    rng = np.random.default_rng(11)
+    z = rng.standard_normal((40, 13)) * 3.0
+    p = router.softmax(z)
+    np.testing.assert_allclose(p, sp_softmax(z, axis=1), rtol=1e-13, atol=0)
+    np.testing.assert_allclose(router.softmax(z + 7.25), p, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, rtol=1e-14)
+
+
+def _brute_topk_row(z: np.ndarray, k: int) -> list[int]:
+    """The unique k-subset whose members all precede every non-member under
+    (larger logit first, then lower index), listed in that order."""
+    E = len(z)
+
+    def before(i: int, j: int) -> bool:
+        return z[i] > z[j] or (z[i] == z[j] and i < j)
+
+    winners = [S for S in itertools.combinations(range(E), k)
+               if all(before(i, j) for i in S for j in range(E) if j not in S)]
+    assert len(winners) == 1
+    return sorted(winners[0], key=lambda i: (-z[i], i))
+
+
+def check_topk_bruteforce(router) -> None:
+    """top_k equals brute-force enumeration of k-subsets, with many ties."""
+    rng = np.random.default_rng(12)
+    for E in range(1, 8):
+        for k in range(1, min(E, 3) + 1):
+            z = rng.integers(0, 3, size=(25, E)).astype(np.float64)   # ties everywhere
+            z[:3] = rng.standard_normal((3, E))                        # and a few without
+            got = router.top_k(z, k)
+            for t in range(z.shape[0]):
+                assert list(got[t]) == _brute_topk_row(z[t], k), (E, k, t, z[t], got[t])
+
+
+def check_top1_argmax(router) -> None:
+    """k = 1 reduces to numpy.argmax (first maximum on ties)."""
+    rng = np.random.default_rng(13)
+    z = rng.integers(0, 4, size=(200, 9)).astype(np.float64)
+    np.testing.assert_array_equal(router.top_k(z, 1)[:, 0], np.argmax(z, axis=1))
+
+
+def check_gate_hand_example(router) -> None:
+    """z = [0, ln 3] gives p = [1/4, 3/4]: the top-1 gate is 3/4; a top-2
+    renormalised gate is [3/4, 1/4] (the picks already hold all the mass)."""
+    z = np.array([[0.0, math.log(3.0)]])
+    p = router.softmax(z)
+    idx1 = router.top_k(z, 1)
+    assert idx1[0, 0] == 1
+    np.testing.assert_allclose(router.gates(p, idx1, renorm=False), [[0.75]], rtol=1e-15)
+    idx2 = router.top_k(z, 2)
+    np.testing.assert_allclose(router.gates(p, idx2, renorm=True), [[0.75, 0.25]], rtol=1e-15)
+    z3 = np.array([[math.log(2.0), 0.0, math.log(6.0)]])      # p = [2, 1, 6] / 9
+    p3 = router.softmax(z3)
+    np.testing.assert_allclose(router.gates(p3, router.top_k(z3, 2), renorm=True), [[0.75, 0.25]], rtol=1e-14)
+    np.testing.assert_allclose(router.gates(p3, router.top_k(z3, 2), renorm=False), [[6 / 9, 2 / 9]], rtol=1e-14)
+
+
+def check_counts_bruteforce(router) -> None:
+    """bincount with minlength equals a plain loop; unused experts report 0."""
+    rng = np.random.default_rng(14)
+    idx = rng.integers(0, 5, size=(30, 2))
+    E = 9
+    want = [0] * E
+    for e in idx.ravel():
+        want[int(e)] += 1
+    got = router.expert_counts(idx, E)
+    assert list(got) == want and got[5:].sum() == 0
+
+
+def check_fp_sums(router, synth) -> None:
+    """sum_i f_i = 1 and sum_i P_i = 1 ([P1] §5.3) on every workload recipe."""
+    for w in synth.ROUTER_WORKLOADS.values():
+        small = w.with_tokens(257)
+        out = router.router_forward(synth.router_logits(small), small.dtype, small.k, small.alpha,
+                                    n_ranks=small.n_ranks)
+        assert out["counts"].sum() == small.T * small.k
+        assert abs(out["f"].sum() - 1.0) < 1e-12, out["f"].sum()
+        assert abs(out["P"].sum() - 1.0) < 1e-12, out["P"].sum()
+
+
+def check_balance_uniform_P(router) -> None:
+    """Equal logits in every row: P_i = 1/N, so N * sum f_i P_i = 1 for any f ([P2] §2.2)."""
+    rng = np.random.default_rng(15)
+    T, E, k = 64, 6, 2
+    z = np.repeat(rng.standard_normal((T, 1)), E, axis=1)
+    out = router.router_forward(z.astype(np.float32), "fp32", k, alpha=0.01)
+    np.testing.assert_allclose(out["P"], 1.0 / E, rtol=1e-14)
+    assert abs(out["balance"] - 1.0) < 1e-13 and abs(out["l_aux"] - 0.01) < 1e-15
+
+
+def check_balance_uniform_f(router) -> None:
+    """Token t forced to expert t mod N (top-1): f_i = 1/N, so the balance is 1 for any P."""
+    rng = np.random.default_rng(16)
+    T, E = 96, 8
+    z = rng.standard_normal((T, E))
+    z[np.arange(T), np.arange(T) % E] += 20.0
+    out = router.router_forward(z.astype(np.float32), "fp32", 1, alpha=0.5)
+    np.testing.assert_allclose(out["f"], 1.0 / E, rtol=0)
+    assert abs(out["balance"] - 1.0) < 1e-13 and abs(out["l_aux"] - 0.5) < 1e-13
+
+
+def check_switch_hand_example(router) -> None:
+    """Two tokens, two experts, top-1, worked by hand.
+
+    z0 = [ln 3, 0] -> p0 = [3/4, 1/4], expert 0; z1 = [0, 0] -> p1 = [1/2, 1/2],
+    a tie, expert 0.  counts = [2, 0], f = [1, 0], P = [5/8, 3/8];
+    N * sum f P = 2 * 5/8 = 5/4; with alpha = 0.01, L_aux = 0.0125.
+    """
+    z = np.array([[math.log(3.0), 0.0], [0.0, 0.0]])
+    out = router.router_forward(z, "fp32", 1, alpha=0.01)  # ln 3 rounds to fp32 first
+    z32 = z.astype(np.float32).astype(np.float64)
+    p00 = math.exp(z32[0, 0]) / (math.exp(z32[0, 0]) + 1.0)
+    assert list(out["idx"][:, 0]) == [0, 0] and list(out["counts"]) == [2, 0]
+    np.testing.assert_allclose(out["P"], [(p00 + 0.5) / 2, (1 - p00 + 0.5) / 2], rtol=1e-15)
+    assert abs(out["balance"] - 2 * (p00 + 0.5) / 2) < 1e-15
+    assert abs(out["balance"] - 1.25) < 1e-7 and abs(out["l_aux"] - 0.0125) < 1e-9
+
+
+def check_cv_closed_forms(router) -> None:
+    """Population CV on crafted load vectors."""
+    assert router.load_cv(np.array([1, 3])) == 0.5                       # mean 2, std 1
+    assert router.load_cv(np.array([4, 4, 4, 4])) == 0.0
+    assert abs(router.load_cv(np.array([0, 0, 0, 4])) - math.sqrt(3.0)) < 1e-15   # mean 1, var 3
+    assert abs(router.load_cv(np.array([2, 4, 4, 4, 5, 5, 7, 9])) - 2.0 / 5.0) < 1e-15  # std 2, mean 5
+
+
+def check_log_example(router) -> None:
+    """[P1] §5.3's log line: 8192 tokens over 8 experts, one expert receiving
+    4320; [P1] §5.4 calls max/mean above 2 imbalanced."""
+    g = golden("p1_s5_3_tokens_per_expert_log.json")
+    mean = g["total_tokens"] / g["num_experts"]
+    ratio = g["max_expert_tokens"] / mean
+    assert abs(ratio - g["max_over_mean"]) < 1e-12
+    assert router.is_ratio_imbalanced(ratio)
+    assert not router.is_ratio_imbalanced(1.9)
+
+
+def check_cv_grades(router) -> None:
+    """The CV bands of [P3] §5.1."""
+    g = golden("p3_s5_1_cv_bands.json")
+    for cv, label in g["cases"]:
+        assert router.cv_grade(cv) == label, (cv, label)
+
+
+def check_grad_finite_difference(router) -> None:
+    """Central differences of g * L_aux(z) with f frozen match the closed form."""
+    rng = np.random.default_rng(17)
+    T, E, alpha, g = 5, 6, 0.3, 1.7
+    z32 = rng.standard_normal((T, E)).astype(np.float32)
+    z = z32.astype(np.float64)
+    f = rng.random(E)
+    f /= f.sum()
+    grad = router.aux_loss_grad(z32, "fp32", f, alpha, grad_scale=g)
+    h = 1e-6
+    fd = np.zeros_like(z)
+    for t in range(T):
+        for j in range(E):
+            zp, zm = z.copy(), z.copy()
+            zp[t, j] += h
+            zm[t, j] -= h
+            fd[t, j] = (router.aux_loss_of_logits(zp, f, alpha, g) - router.aux_loss_of_logits(zm, f, alpha, g)) / (2 * h)
+    scale = np.abs(grad).max()
+    assert np.abs(grad - fd).max() <= 1e-7 * scale, np.abs(grad - fd).max() / scale
+
+
+def check_grad_structure(router) -> None:
+    """Rows of dL/dz sum to 0 (softmax shift invariance); equal logits give
+    g * (alpha / T) * (f_j - 1/N)."""
+    rng = np.random.default_rng(18)
+    T, E, alpha = 7, 5, 0.2
+    z = rng.standard_normal((T, E)).astype(np.float32)
+    f = rng.random(E)
+    f /= f.sum()
+    grad = router.aux_loss_grad(z, "fp32", f, alpha)
+    assert np.abs(grad.sum(axis=1)).max() < 1e-15
+    zu = np.zeros((T, E), dtype=np.float32)
+    gu = router.aux_loss_grad(zu, "fp32", f, alpha, grad_scale=3.0)
+    np.testing.assert_allclose(gu, np.broadcast_to(3.0 * (alpha / T) * (f - 1.0 / E), (T, E)), rtol=1e-12, atol=1e-17)
+
+
+# ----------------------------------------------------------------------------- dispatch
+
+def check_capacity_example(dispatch) -> None:
+    """[P1] §4.5: 1024 tokens, 8 experts, capacity factor 1.25 -> 160 tokens per expert."""
+    g = golden("p1_s4_5_capacity_example.json")
+    assert dispatch.capacity(g["tokens"], 1, g["num_experts"], g["capacity_factor"]) == g["capacity"]
+
+
+def _brute_dispatch(idx: np.ndarray, E: int, C: int):
+    flat = [int(e) for e in np.asarray(idx).ravel()]
+    n = len(flat)
+    rank = [sum(1 for b in range(a) if flat[b] == flat[a]) for a in range(n)]
+    counts = [flat.count(e) for e in range(E)]
+    offsets = [sum(counts[:e]) for e in range(E + 1)]
+    perm = [-1] * n
+    for a in range(n):
+        perm[offsets[flat[a]] + rank[a]] = a
+    slot = [r if r < C else -1 for r in rank]
+    kept = [min(c, C) for c in counts]
+    return perm, slot, offsets, counts, kept, n - sum(kept)
+
+
+def check_dispatch_bruteforce(dispatch, router) -> None:
+    """The stable dispatch equals an O((T*k)^2) count of earlier same-expert assignments."""
+    rng = np.random.default_rng(19)
+    for trial in range(30):
+        T = int(rng.integers(1, 30))
+        E = int(rng.integers(1, 7))
+        k = int(rng.integers(1, min(E, 3) + 1))
+        z = rng.integers(0, 3, size=(T, E)).astype(np.float64)
+        idx = router.top_k(z, k)
+        C = int(rng.integers(0, T + 2))
+        got = dispatch.dispatch(idx, E, C)
+        perm, slot, offsets, counts, kept, nd = _brute_dispatch(idx, E, C)
+        assert list(got["perm"]) == perm, trial
+        assert list(got["slot"]) == slot, trial
+        assert list(got["offsets"]) == offsets and list(got["counts"]) == counts
+        assert list(got["kept"]) == kept and got["n_dropped"] == nd
+
+
+def check_dispatch_identities(dispatch, router, synth) -> None:
+    """Counting identities on a workload-shaped batch with drops."""
+    w = synth.ROUTER_WORKLOADS["zipf-hot-top8-T131072-E256"].with_tokens(2048)
+    z = router.widen(synth.router_logits(w), w.dtype)
+    idx = router.top_k(z, w.k)
+    C = dispatch.capacity(w.T, w.k, w.E, w.capacity_factor)
+    d = dispatch.dispatch(idx, w.E, C)
+    n = w.T * w.k
+    assert d["offsets"][-1] == n and d["kept"].sum() + d["n_dropped"] == n
+    assert d["n_dropped"] > 0                                  # capacity factor 1.0 with hot experts drops
+    assert sorted(d["perm"]) == list(range(n))
+    flat = idx.ravel()
+    for e in range(w.E):
+        seg = d["perm"][d["offsets"][e]:d["offsets"][e + 1]]
+        assert np.all(flat[seg] == e) and np.all(np.diff(seg) > 0)
+        assert np.all(d["slot"][seg[:d["kept"][e]]] == np.arange(d["kept"][e]))
+        assert np.all(d["slot"][seg[d["kept"][e]:]] == -1)
+
+
+# ----------------------------------------------------------------------------- Sinkhorn
+
+def check_sinkhorn_two_rank(sinkhorn) -> None:
+    """Two ranks, one overloaded: all the mass flows 0 -> 1, whatever the cost."""
+    out = sinkhorn.taot_phase1(np.array([[3.0, 1.0]]), ranks_per_node=1, lam=10.0, iters=5)
+    np.testing.assert_allclose(out["plan"][0], [[0.0, 1.0], [0.0, 0.0]], atol=1e-15)
+    assert out["status"][0] == 0
+
+
+def check_sinkhorn_dual(sinkhorn) -> None:
+    """On a small non-symmetric problem, Sinkhorn-Knopp matches an independent
+    solve of the entropic transport dual (scipy L-BFGS):
+    max_{f,g} <f,a> + <g,b> - eps * sum_ij exp((f_i + g_j - W_ij)/eps)."""
+    from scipy.optimize import minimize
+    rng = np.random.default_rng(20)
+    R, S, eps = 5, 5, 0.7
+    W = rng.random((R, S)) * 2.0                  # not symmetric
+    a = rng.random(R) + 0.1
+    a /= a.sum()
+    b = rng.random(S) + 0.1
+    b /= b.sum()
+    M = np.exp(-W / eps)
+
+    def negdual(x):
+        f, g = x[:R], x[R:]
+        Tm = np.exp((f[:, None] + g[None, :] - W) / eps)
+        val = f @ a + g @ b - eps * Tm.sum()
+        grad = np.concatenate([a - Tm.sum(axis=1), b - Tm.sum(axis=0)])
+        return -val, -grad
+
+    res = minimize(negdual, np.zeros(R + S), jac=True, method="L-BFGS-B",
+                   options={"gtol": 1e-14, "ftol": 1e-16, "maxiter": 10000})
+    f, g = res.x[:R], res.x[R:]
+    plan_dual = np.exp((f[:, None] + g[None, :] - W) / eps)
+    u, v = sinkhorn.sinkhorn_knopp(a, b, M, 3000)
+    plan = sinkhorn.transport_plan(u, M, v)
+    np.testing.assert_allclose(plan, plan_dual, rtol=1e-6, atol=1e-9)
+
+
+def check_sinkhorn_marginals(sinkhorn, loads: np.ndarray) -> None:
+    """Column sums equal b after every v update; row sums reach a in 50 iterations;
+    the plan has the diag(u) M diag(v) form and no negative entry."""
+    out = sinkhorn.taot_phase1(loads, ranks_per_node=8, lam=10.0, iters=50)
+    for m in range(loads.shape[0]):
+        over = loads[m] - loads[m].mean()            # overload (+) / idle capacity (-)
+        ok = (over > 0).any()
+        a = np.clip(over, 0, None) / max(np.clip(over, 0, None).sum(), 1e-300)
+        b = np.clip(-over, 0, None) / max(np.clip(-over, 0, None).sum(), 1e-300)
+        if not ok:
+            assert out["status"][m] == 1 and not out["plan"][m].any()
+            continue
+        plan = out["plan"][m]
+        assert (plan >= 0).all()
+        np.testing.assert_allclose(plan.sum(axis=0), b, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(plan.sum(axis=1), a, rtol=1e-9, atol=1e-15)
+        np.testing.assert_allclose(plan, out["u"][m][:, None] * out["M"] * out["v"][m][None, :], rtol=1e-14)
+
+
+def check_sinkhorn_topology_kernel(sinkhorn) -> None:
+    """With eps = lambda = 10 the intra-node / cross-node kernel ratio is
+    exp(-1/10) / exp(-10/10) = e^0.9 > 1 ([P4] §2, soft topology preference)."""
+    W = sinkhorn.topology_cost(16, 8, 10.0)
+    M = sinkhorn.gibbs_kernel(W, 10.0)
+    assert M[0, 0] == 1.0 and abs(M[0, 1] / M[0, 8] - math.exp(0.9)) < 1e-14
+    assert (W == W.T).all() and W[3, 3] == 0 and W[3, 5] == 1 and W[3, 12] == 10

@@ -1,0 +1,138 @@
+"""Plausible mistakes planted in the oracle (on the CPU) must fail a pin.
+
+Each case monkeypatches one oracle function with a wrong variant and checks
+that at least one of the pins raises.  This is what makes the pins worth
+trusting: a dropped term, a wrong sign, a transposed operand or a changed
+tie rule cannot slip through.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import pins
+import synth
+
+R, D, S = oracle.router, oracle.dispatch, oracle.sinkhorn
+
+
+def _masked_forward(logits, dtype, k, alpha, renorm=None, n_ranks=0):
+    # [P2]'s masked P_i: only the selected experts' probabilities, over T*k
+    out = _orig_forward(logits, dtype, k, alpha, renorm, n_ranks)
+    z = R.widen(logits, dtype)
+    p = R.softmax(z)
+    mask = np.zeros_like(p)
+    np.put_along_axis(mask, out["idx"], 1.0, axis=1)
+    out["P"] = (p * mask).sum(axis=0) / (z.shape[0] * k)
+    out["balance"] = R.balance(out["f"], out["P"])
+    out["l_aux"] = alpha * out["balance"]
+    return out
+
+
+_orig_forward = R.router_forward
+
+MUTANTS = {
+    "P masked to the selected experts": (
+        [(R, "router_forward", _masked_forward)],
+        [lambda: pins.check_fp_sums(R, synth), lambda: pins.check_balance_uniform_P(R)]),
+    "f divided by T instead of T*k": (
+        [(R, "token_fraction", lambda counts, T, k: counts / float(T))],
+        [lambda: pins.check_fp_sums(R, synth)]),
+    "top-k ties to the higher index": (
+        [(R, "top_k", lambda z, k: (z.shape[1] - 1 - np.argsort(-z[:, ::-1], axis=1, kind="stable"))[:, :k])],
+        [lambda: pins.check_topk_bruteforce(R), lambda: pins.check_top1_argmax(R)]),
+    "top-k picks the smallest logits": (
+        [(R, "top_k", lambda z, k: np.argsort(z, axis=1, kind="stable")[:, :k])],
+        [lambda: pins.check_topk_bruteforce(R)]),
+    "softmax normalised over the token axis": (
+        [(R, "softmax", lambda z: np.exp(z) / np.exp(z).sum(axis=0, keepdims=True))],
+        [lambda: pins.check_softmax_library(R)]),
+    "balance without the factor N": (
+        [(R, "balance", lambda f, P: float(np.sum(f * P)))],
+        [lambda: pins.check_balance_uniform_P(R), lambda: pins.check_switch_hand_example(R)]),
+    "gradient with the wrong sign": (
+        [(R, "aux_loss_grad", lambda *a, **kw: -_orig_grad(*a, **kw))],
+        [lambda: pins.check_grad_finite_difference(R)]),
+    "gradient without the sum_i p_i f_i term": (
+        [(R, "aux_loss_grad", lambda logits, dtype, f, alpha, grad_scale=1.0:
+          grad_scale * (alpha * len(f) / R.widen(logits, dtype).shape[0]) * R.softmax(R.widen(logits, dtype)) * f[None, :])],
+        [lambda: pins.check_grad_finite_difference(R), lambda: pins.check_grad_structure(R)]),
+    "CV with the sample (n-1) deviation": (
+        [(R, "load_cv", lambda x: float(np.std(np.asarray(x, float), ddof=1) / np.mean(x)))],
+        [lambda: pins.check_cv_closed_forms(R)]),
+    "dispatch keeps the last C instead of the first": (
+        [(D, "dispatch", lambda idx, E, C: _reverse_dispatch(idx, E, C))],
+        [lambda: pins.check_dispatch_bruteforce(D, R)]),
+    "dispatch keeps C + 1": (
+        [(D, "dispatch", lambda idx, E, C: _orig_dispatch(idx, E, C + 1))],
+        [lambda: pins.check_dispatch_bruteforce(D, R)]),
+    "capacity floors the per-expert share": (
+        [(D, "capacity", lambda T, k, E, cf: int(math.ceil((T * k // E) * cf)))],
+        [lambda: pins.check_dispatch_bruteforce(D, R), lambda: _capacity_ragged()]),
+    "Sinkhorn uses M^T where M belongs": (
+        [(S, "sinkhorn_knopp", lambda a, b, M, iters: _orig_sk(a, b, M.T.copy(), iters))],
+        [lambda: pins.check_sinkhorn_dual(S)]),
+    "Sinkhorn kernel exp(-W * eps)": (
+        [(S, "gibbs_kernel", lambda W, eps: np.exp(-W * float(eps)))],
+        [lambda: pins.check_sinkhorn_topology_kernel(S)]),
+    "supply and demand swapped": (
+        [(S, "supply_demand", lambda load: _orig_sd(load)[1::-1] + (_orig_sd(load)[2],))],
+        [lambda: pins.check_sinkhorn_marginals(S, _loads()), lambda: pins.check_sinkhorn_two_rank(S)]),
+    "cross-node cost and intra-node cost swapped": (
+        [(S, "topology_cost", lambda R_, rpn, lam: np.where(_orig_tc(R_, rpn, lam) == 1.0, lam, np.where(_orig_tc(R_, rpn, lam) == lam, 1.0, 0.0)))],
+        [lambda: pins.check_sinkhorn_topology_kernel(S)]),
+}
+
+_orig_grad = R.aux_loss_grad
+_orig_dispatch = D.dispatch
+_orig_sk = S.sinkhorn_knopp
+_orig_sd = S.supply_demand
+_orig_tc = S.topology_cost
+
+
+def _reverse_dispatch(idx, E, C):
+    out = _orig_dispatch(idx, E, C)
+    counts = out["counts"]
+    slot = np.full_like(out["slot"], -1)
+    for e in range(E):
+        seg = out["perm"][out["offsets"][e]:out["offsets"][e + 1]]
+        for r, a in enumerate(seg[::-1]):
+            slot[a] = r if r < C else -1
+        out["perm"][out["offsets"][e]:out["offsets"][e + 1]] = seg[::-1]
+    out["slot"] = slot
+    out["counts"] = counts
+    return out
+
+
+def _capacity_ragged():
+    # T*k/E not an integer: 10 tokens, 4 experts, k=1, factor 1.0 -> ceil(2.5) = 3
+    assert D.capacity(10, 1, 4, 1.0) == 3
+
+
+def _loads():
+    rng = np.random.default_rng(3)
+    loads = rng.poisson(384, size=(6, 64)).astype(np.float64)
+    loads[1, :8] += 600.0
+    return loads
+
+
+@pytest.mark.parametrize("name", list(MUTANTS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    patches, checks = MUTANTS[name]
+    for mod, attr, fn in patches:
+        monkeypatch.setattr(mod, attr, fn)
+    caught = 0
+    for check in checks:
+        try:
+            check()
+        except AssertionError:
+            caught += 1
+    assert caught > 0, f"no pin caught the planted mistake: {name}"
+
+
+def test_unmutated_oracle_passes_the_same_checks():
+    for _, checks in MUTANTS.values():
+        for check in checks:
+            check()
