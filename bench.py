@@ -1,0 +1,476 @@
+"""Benchmark of the MoE router hot path on GB300: one step = router forward +
+dispatch + backward over one batch (one launch of moe_router_step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extra]
+
+Prints one JSON line on rank 0.  With --gpus N > 1 (under torchrun) every rank
+routes its own batch (independent replicas, weak scaling); the timed region
+is bracketed by a barrier and the slowest rank's time is reported.
+
+`--impl reference` times the CPU oracle (fp64 numpy, the only other use of
+``oracle/`` outside the tests) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import threading  # noqa: E402
+import time  # noqa: E402
+from pathlib import Path  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import synth  # noqa: E402
+
+METRIC = "router fwd+bwd+dispatch tokens/s; achieved HBM GB/s vs GB300 peak"
+DEFAULT_WORKLOAD = "zipf-top2-T65536-E64"
+EXTRA_WORKLOADS = ("zipf-hot-top8-T131072-E256", "zipf-ep64-top6-T262144-E384")
+SINKHORN_WORKLOAD = "taot-sinkhorn-B1024-R64"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FP32_FMA_TFLOPS_NOMINAL = 152 * 128 * 2 * 2.07e9 / 1e12      # SMs x FMA lanes x 2 flops x max clock
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------- sizes
+
+def algorithmic_bytes(w: synth.RouterWorkload) -> int:
+    """Bytes the step must move: logits read once, dlogits written in fp32, and
+    idx, gate, perm, slot (4 bytes each) per assignment."""
+    esize = 2 if w.dtype == "bf16" else 4
+    return w.T * (w.E * (esize + 4) + 16 * w.k)
+
+
+def peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json hbm_gbs)"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback 6.8 TB/s"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def to_device(logits: np.ndarray, dtype: str, torch, device):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(logits).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32)).to(device)
+
+
+def out_buffers(w, torch, device) -> dict:
+    T, E, k = w.T, w.E, w.k
+    i32, f32 = torch.int32, torch.float32
+    return {
+        "idx": torch.empty((T, k), dtype=i32, device=device), "gate": torch.empty((T, k), dtype=f32, device=device),
+        "counts": torch.empty(E, dtype=i32, device=device), "f": torch.empty(E, dtype=f32, device=device),
+        "P": torch.empty(E, dtype=f32, device=device), "scalars": torch.empty(7, dtype=f32, device=device),
+        "rank_load": torch.empty(max(w.n_ranks, 0), dtype=i32, device=device),
+        "perm": torch.empty(T * k, dtype=i32, device=device), "slot": torch.empty(T * k, dtype=i32, device=device),
+        "offsets": torch.empty(E + 1, dtype=i32, device=device), "kept": torch.empty(E, dtype=i32, device=device),
+        "n_dropped": torch.empty(1, dtype=i32, device=device),
+        "dlogits": torch.empty((T, E), dtype=f32, device=device),
+    }
+
+
+def time_router(w, steps: int, warmup: int, torch, device, dist_ctx, soak_s: float = 0.0, sampler=None) -> dict:
+    """Device-timed steps of moe_router_step with buffers rotated so that the
+    working set of consecutive steps exceeds L2 several times over."""
+    import moe_expert_routing_router_gb300 as mr
+    logits = synth.router_logits(w)
+    step_bytes = algorithmic_bytes(w)
+    n_sets = max(2, math.ceil(3 * L2_BYTES / step_bytes))
+    x0 = to_device(logits, w.dtype, torch, device)
+    xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
+    outs = [out_buffers(w, torch, device) for _ in range(n_sets)]
+    ws = mr.Workspace(device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(i):
+        mr.moe_router_step(xs[i % n_sets], w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm),
+                           n_ranks=w.n_ranks, grad_scale=1.0, ws=ws, out=outs[i % n_sets])
+
+    for i in range(max(warmup, 3)):
+        step(i)
+    torch.cuda.synchronize(device)
+    # The K timed steps are captured once into a CUDA graph so that the device
+    # time is measured, not the Python-side launch rate.
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for s in range(steps):
+                step(s)
+        graph = g
+    except Exception as e:  # capture unsupported: time eager launches instead
+        log(f"CUDA graph capture failed ({e!r}); timing eager launches")
+        torch.cuda.synchronize(device)
+
+    def run_steps():
+        if graph is not None:
+            graph.replay()
+        else:
+            for s in range(steps):
+                step(s)
+
+    run_steps()
+    torch.cuda.synchronize(device)
+    if sampler is not None:
+        sampler.start()
+    t_end = time.time() + soak_s
+    while time.time() < t_end:                      # loaded window for the clock samples
+        run_steps()
+        torch.cuda.synchronize(device)
+    dist_ctx.barrier()
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    run_steps()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    dist_ctx.barrier()
+    clocks = sampler.stop() if sampler is not None else None
+    total_ms = t0.elapsed_time(t1)
+    flags = mr.moe_get_device_status(ws)
+    if flags:
+        raise RuntimeError(f"device wait expired during the benchmark (flags {flags})")
+    # one kernel per step: its mean launch duration is the device time per step
+    return {"total_ms": dist_ctx.max(total_ms), "launch_ms_mean": total_ms / steps, "n_sets": n_sets,
+            "clocks": clocks, "step_bytes": step_bytes,
+            "timing": ("CUDA graph of the timed steps replayed once between two CUDA events" if graph is not None
+                       else "eager launches between two CUDA events")}
+
+
+def time_e2e(w, steps: int, warmup: int, torch, device, dist_ctx) -> dict:
+    """The same step with the logits in pinned HOST memory and every output
+    copied back to pinned host memory, copies inside the timed region."""
+    import moe_expert_routing_router_gb300 as mr
+    logits = synth.router_logits(w)
+    host_x = to_device(logits, w.dtype, torch, "cpu").pin_memory()
+    dev_x = torch.empty_like(host_x, device=device)
+    outs = out_buffers(w, torch, device)
+    host_outs = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+    ws = mr.Workspace(device)
+    stream = torch.cuda.current_stream(device)
+    h2d = host_x.numel() * host_x.element_size()
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+
+    def step():
+        dev_x.copy_(host_x, non_blocking=True)
+        mr.moe_router_step(dev_x, w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks,
+                           grad_scale=1.0, ws=ws, out=outs)
+        for k2, v in outs.items():
+            host_outs[k2].copy_(v, non_blocking=True)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize(device)
+    dist_ctx.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    dist_ctx.barrier()
+    ms = dist_ctx.max(t0.elapsed_time(t1)) / steps
+    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h}
+
+
+def time_sinkhorn(torch, device, reps: int = 20) -> dict:
+    import moe_expert_routing_router_gb300 as mr
+    s = synth.SINKHORN_WORKLOADS[SINKHORN_WORKLOAD]
+    loads_path = ROOT / "tests" / "golden" / "taot_sinkhorn_B1024_R64_loads.npy"
+    loads = torch.from_numpy(np.load(loads_path).astype(np.float32)).to(device)
+    out = {"u": torch.empty_like(loads), "v": torch.empty_like(loads),
+           "plan": torch.empty((s.B, s.R, s.R), dtype=torch.float32, device=device),
+           "status": torch.empty(s.B, dtype=torch.int32, device=device)}
+    for _ in range(3):
+        mr.taot_sinkhorn_batched(loads, s.ranks_per_node, s.lam, s.eps, s.iters, out=out)
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        mr.taot_sinkhorn_batched(loads, s.ranks_per_node, s.lam, s.eps, s.iters, out=out)
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        ms.append(a.elapsed_time(b))
+    us = statistics.median(ms) * 1e3
+    flops = s.B * s.iters * 2 * 2 * s.R * s.R           # two R x R matrix-vector products per iteration
+    return {"workload": SINKHORN_WORKLOAD, "us_per_call": round(us, 2),
+            "gflop_per_call": round(flops / 1e9, 4), "achieved_tflops": round(flops / (us * 1e-6) / 1e12, 2),
+            "fp32_fma_peak_tflops_nominal": round(FP32_FMA_TFLOPS_NOMINAL, 1),
+            "frac_of_fp32_peak": round(flops / (us * 1e-6) / 1e12 / FP32_FMA_TFLOPS_NOMINAL, 4),
+            "bound": "alu"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_step(w, logits: np.ndarray) -> None:
+    """One pass of the oracle over a batch: forward, dispatch, backward."""
+    import oracle
+    fw = oracle.router.router_forward(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks)
+    T = logits.shape[0]
+    oracle.dispatch.dispatch(fw["idx"], w.E, oracle.dispatch.capacity(T, w.k, w.E, w.capacity_factor))
+    oracle.router.aux_loss_grad(logits, w.dtype, fw["f"], w.alpha, 1.0)
+
+
+def time_oracle(w, budget_s: float, min_steps: int = 1, rows: int | None = None) -> dict:
+    """The oracle on a sample of `rows` tokens of the workload (default: sized
+    so that about `budget_s` seconds of CPU work are done)."""
+    if rows is None:
+        probe = w.with_tokens(min(w.T, 2048))
+        lg = synth.router_logits(probe)
+        t0 = time.perf_counter()
+        oracle_step(probe, lg)
+        per_row = (time.perf_counter() - t0) / probe.T
+        rows = int(min(w.T, max(256, budget_s / max(min_steps, 1) / per_row)))
+    sample = w if rows == w.T else w.with_tokens(rows)
+    lg = synth.router_logits(sample)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < min_steps or time.perf_counter() < t_end:
+        t0 = time.perf_counter()
+        oracle_step(sample, lg)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.median(times)
+    return {"value": rows / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {w.T} tokens of {w.name} (same E, k, recipe); median of {len(times)} "
+                      f"oracle steps (fwd + dispatch + bwd, fp64 numpy, single thread)",
+            "sec_per_step": sec, "rows": rows}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+class DistCtx:
+    def __init__(self, torch):
+        self.torch = torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.dist = dist
+            self.backend = backend
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        dev = f"cuda:{self.local}" if self.backend == "nccl" else "cpu"
+        t = self.torch.tensor([x], dtype=self.torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            self.dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- main
+
+def config_of(w, extra: dict | None = None) -> dict:
+    c = {"workload": w.name, "T": w.T, "E": w.E, "k": w.k, "logits": w.dtype, "alpha": w.alpha,
+         "capacity_factor": w.capacity_factor, "gate_renorm": w.renorm}
+    if w.n_ranks:
+        c["ep_ranks"] = w.n_ranks
+        c["ranks_per_node"] = w.ranks_per_node
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_reference(args) -> dict:
+    w = synth.ROUTER_WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return {}
+    budget = 120.0 / max(args.steps + args.warmup, 1)       # whole run within ~2 minutes
+    probe = time_oracle(w, budget_s=0.0, min_steps=1, rows=min(w.T, 2048))
+    per_row = 1.0 / probe["value"]
+    rows = int(min(w.T, max(256, budget / per_row)))
+    sample = w if rows == w.T else w.with_tokens(rows)
+    lg = synth.router_logits(sample)
+    for _ in range(args.warmup):
+        oracle_step(sample, lg)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sample, lg)
+    sec = (time.perf_counter() - t0) / args.steps
+    value = rows / sec
+    desc = (f"{rows} of {w.T} tokens of {w.name} per step; oracle fwd + dispatch + bwd "
+            f"(fp64 numpy, single thread)")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, {"sample_tokens": rows}),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args) -> dict:
+    import torch
+    dist_ctx = DistCtx(torch)
+    device = torch.device("cuda", dist_ctx.local)
+    torch.cuda.set_device(device)
+    pk = peaks()
+    w = synth.ROUTER_WORKLOADS[args.workload]
+    sampler = ClockSampler(dist_ctx.local)
+    r = time_router(w, args.steps, args.warmup, torch, device, dist_ctx, soak_s=1.0, sampler=sampler)
+    ms_step = r["total_ms"] / args.steps
+    value = dist_ctx.world * w.T / (ms_step * 1e-3)
+    achieved = r["step_bytes"] / (r["launch_ms_mean"] * 1e-3) / 1e9
+    e2e = time_e2e(w, max(5, min(args.steps, 50)), args.warmup, torch, device, dist_ctx)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist_ctx.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w, {"l2": f"inputs and outputs rotated over {r['n_sets']} buffer sets "
+                                      f"(>= 3x the 129 MB L2 between reuses)",
+                                "parallelism": f"replicas x{dist_ctx.world}", "timing": r["timing"]}),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "router_persistent_kernel (moe_router_step, one launch per step)",
+                     "algorithmic_bytes_per_launch": r["step_bytes"],
+                     "launch_us_mean": round(r["launch_ms_mean"] * 1e3, 2), "peak_source": pk["source"]},
+        "e2e": {"value": dist_ctx.world * w.T / (e2e["ms_per_step"] * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": args.steps,
+        "clocks": r["clocks"],
+    }
+    if dist_ctx.rank == 0 and not args.no_extra:
+        also = {}
+        for name in EXTRA_WORKLOADS:
+            wx = synth.ROUTER_WORKLOADS[name]
+            rx = time_router(wx, max(10, min(args.steps, 50)), args.warmup, torch, device, _Solo())
+            msx = rx["total_ms"] / max(10, min(args.steps, 50))
+            ach = rx["step_bytes"] / (rx["launch_ms_mean"] * 1e-3) / 1e9
+            also[name] = {"value": wx.T / (msx * 1e-3), "unit": "tokens/s", "ms_per_step": msx,
+                          "launch_us_mean": round(rx["launch_ms_mean"] * 1e3, 2),
+                          "roofline_frac": round(ach / pk["hbm_gbs"], 4), "achieved_gbs": round(ach, 1),
+                          "algorithmic_bytes_per_launch": rx["step_bytes"]}
+        line["also"] = also
+        line["sinkhorn"] = time_sinkhorn(torch, device)
+    if dist_ctx.rank == 0:
+        cb = time_oracle(w, budget_s=args.cpu_seconds, min_steps=2)
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    dist_ctx.close()
+    return line if dist_ctx.rank == 0 else {}
+
+
+class _Solo:
+    def barrier(self):
+        pass
+
+    def max(self, x):
+        return x
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.ROUTER_WORKLOADS))
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads and the Sinkhorn line")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("warmup raised to 3")
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

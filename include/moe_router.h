@@ -1,0 +1,236 @@
+/*
+ * moe_router.h -- C ABI of the GB300 (sm_103a) MoE expert-routing library.
+ *
+ * The hot path of MoE expert routing with equal-cost load balancing: router
+ * softmax and top-k, the Switch auxiliary balance loss and its closed-form
+ * gradient, a capacity-limited stable token->expert dispatch, and the batched
+ * topology-aware Sinkhorn-Knopp flow plan of TAOT Phase 1.
+ *
+ * Sources (cited by title and section):
+ *   [P1] the three-layer load-balancing article (LVS, NIC Teaming, MoE
+ *        equal-cost balancing), mhpq.cn/news/998159
+ *   [P2] "MoE大模型训练中的等开销负载均衡：原理、代码实现与调参实战" (codechina.net)
+ *   [P3] large-model load-balancing survey printed as "企业官网建设流程全解析"
+ *        (cnvsn.com/news/335486)
+ *   [P4] "MoE 训练端到端加速 1.43 倍：LoongForge 基于拓扑感知最优传输重新定义 EP
+ *        专家负载均衡" (LoongForge blog, TAOT)
+ *
+ * Conventions for every entry point:
+ *   - Array arguments are DEVICE pointers owned by the caller, dense and
+ *     row-major, unless a comment says otherwise.  The library never
+ *     allocates device memory; scratch lives in a caller-allocated workspace.
+ *   - Work is enqueued on `stream` (0 = the legacy default stream) and the
+ *     call returns without synchronising.  Results are valid once the stream
+ *     reaches that point.  Calls that share a workspace must be ordered on one
+ *     stream; concurrent calls need separate workspaces.
+ *   - Errors are returned as moe_status; no exception crosses the ABI.
+ *     Argument errors are found on the host before anything is enqueued.
+ *     moe_last_error() gives a one-line description of the last failure on
+ *     the calling thread.
+ *   - Inputs are assumed finite: NaN or Inf logits give unspecified results.
+ *   - Indices are int32; T*k must stay below 2^31.
+ */
+#ifndef MOE_ROUTER_H
+#define MOE_ROUTER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ROUTER_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,     /* bad argument: null pointer, size out of range, misaligned workspace */
+  MOE_ERR_UNSUPPORTED = 2, /* unknown dtype */
+  MOE_ERR_CUDA = 3,        /* a CUDA launch or query failed (moe_last_error has the CUDA message) */
+  MOE_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (see moe_get_device_status) */
+  MOE_ERR_WORKSPACE = 5    /* workspace smaller than the *_workspace_size query asked for */
+} moe_status;
+
+typedef enum { MOE_DTYPE_FP32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+/* Indices into the `scalars` output of moe_router_fwd / moe_router_step. */
+enum {
+  MOE_SCALAR_L_AUX = 0,              /* alpha * E * sum_i f_i P_i                        */
+  MOE_SCALAR_BALANCE = 1,            /* E * sum_i f_i P_i (1 under uniform routing)      */
+  MOE_SCALAR_CV = 2,                 /* std/mean of the per-expert counts (population)   */
+  MOE_SCALAR_MAX_OVER_MEAN = 3,      /* max count / mean count                           */
+  MOE_SCALAR_MIN_OVER_MEAN = 4,      /* min count / mean count                           */
+  MOE_SCALAR_RANK_CV = 5,            /* std/mean of the per-rank loads (0 if n_ranks==0) */
+  MOE_SCALAR_RANK_MAX_OVER_MEAN = 6, /* max rank load / mean rank load (0 if none)       */
+  MOE_NUM_SCALARS = 7
+};
+
+/* Limits checked by every entry point (MOE_ERR_INVALID otherwise). */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 8
+#define MOE_MAX_RANKS 64
+
+/* ------------------------------------------------------------------------ */
+/* Workspace                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device scratch that moe_router_fwd, moe_dispatch and
+ * moe_router_step need for a batch of T tokens over E experts with top-k.
+ * Returns 0 for arguments that those calls would reject. */
+MOE_API size_t moe_router_workspace_size(int64_t T, int32_t E, int32_t k);
+
+/* Zero-fills a workspace (an async memset on `stream`).  A workspace must be
+ * zero-filled once before its first use; every call that completes leaves it
+ * ready for the next one.  After a call reported MOE_ERR_TIMEOUT, initialise
+ * it again.  `ws` must be 256-byte aligned. */
+MOE_API moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Reads and clears the device error flags of a workspace (synchronises
+ * `stream`).  *flags = 0 when every bounded wait completed; otherwise
+ * returns MOE_ERR_TIMEOUT and sets bits: 1 = grid barrier wait expired. */
+MOE_API moe_status moe_get_device_status(void* ws, moe_stream_t stream, int32_t* flags);
+
+/* ------------------------------------------------------------------------ */
+/* Router forward                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Router softmax, top-k and the Switch balance statistics of one batch.
+ *
+ * Computes, in fp32 from fp32 or bf16 logits:
+ *   p[t,e]  = softmax(logits[t,:])[e]                        [P1] §4.2; [P2] §3.1
+ *   idx[t,j]: the k experts with the largest logits, largest first, ties to
+ *             the lower expert index                        [P1] §4.4; [P2] §3.1
+ *   gate[t,j] = p[t, idx[t,j]], divided by sum_j p[t, idx[t,j]] when renorm
+ *   counts[e] = #assignments to e (before capacity drops)    [P2] §3.1 (bincount, minlength=E)
+ *   f[e]      = counts[e] / (T*k)                            [P1] §4.4
+ *   P[e]      = (1/T) * sum_t p[t,e]  (all tokens, unmasked) [P1] §4.2
+ *   scalars   = MOE_SCALAR_*: L_aux = alpha*E*sum f*P ([P2] §2.2), the
+ *               balance E*sum f*P, CV and max/min over mean of the counts
+ *               ([P3] §5.1), and the same over ranks
+ *   rank_load[r] = sum of counts over experts [r*E/n_ranks, (r+1)*E/n_ranks)
+ *
+ * logits     [T,E] fp32 or bf16 (dt).
+ * k          1..min(E, 8).     E in 1..1024.     T >= 1, T*k < 2^31.
+ * alpha      >= 0, the aux-loss weight applied inside L_aux.
+ * renorm     1: renormalise the gate over the picks; 0: raw p; -1: auto (k > 1).
+ * n_ranks    0 for none, else 1..64 dividing E (experts mapped contiguously).
+ * idx [T,k] int32, gate [T,k] fp32, counts [E] int32, f [E] fp32, P [E] fp32,
+ * scalars [MOE_NUM_SCALARS] fp32, rank_load [n_ranks] int32 (may be NULL
+ * when n_ranks == 0).  ws: >= moe_router_workspace_size(T,E,k) bytes,
+ * 256-byte aligned, zero-filled before first use.
+ * The per-expert results are reduced in a fixed order: repeated calls give
+ * bit-identical outputs. */
+MOE_API moe_status moe_router_fwd(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                          float alpha, int32_t renorm, int32_t n_ranks,
+                          int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                          float* scalars, int32_t* rank_load,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Router backward (aux loss only)                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Gradient of grad_scale * L_aux with respect to the logits, f held constant
+ * (f comes from the hard top-k selection and carries no gradient, [P1] §4.2):
+ *
+ *   dlogits[t,j] = grad_scale * (alpha*E/T) * p[t,j] * (f[j] - sum_i p[t,i] f[i])
+ *
+ * logits [T,E] fp32/bf16, f [E] fp32 (as written by moe_router_fwd),
+ * dlogits [T,E] fp32 (written, not accumulated).  No workspace. */
+MOE_API moe_status moe_router_bwd(const void* logits, moe_dtype dt, int64_t T, int32_t E, float alpha,
+                          const float* f, float grad_scale, float* dlogits, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Capacity-limited dispatch                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Expert capacity C = ceil(ceil(T*k/E) * capacity_factor), the product in
+ * double ([P1] §4.5: 1024 tokens, 8 experts, factor 1.25 -> 160).  Host-only.
+ * Returns -1 for invalid arguments (T < 1, E < 1, k < 1, factor <= 0). */
+MOE_API int64_t moe_dispatch_capacity(int64_t T, int32_t E, int32_t k, double capacity_factor);
+
+/* Stable counting-sort dispatch of the T*k assignments a = t*k + j by expert
+ * with capacity C = moe_dispatch_capacity(T,E,k,capacity_factor) ([P1] §4.5:
+ * assignments beyond an expert's capacity are dropped):
+ *   offsets [E+1] int32: exclusive prefix of the per-expert counts, offsets[E] = T*k
+ *   perm    [T*k] int32: assignment ids grouped by expert, ascending within an expert
+ *   slot    [T*k] int32: rank of assignment a within its expert, -1 if >= C (dropped)
+ *   kept    [E]   int32: min(count, C)
+ *   n_dropped [1] int32: T*k - sum(kept)
+ * The kept assignments of expert e are perm[offsets[e] .. offsets[e]+kept[e]).
+ * idx [T,k] int32 with values in [0,E) (out-of-range values give unspecified
+ * results but stay in bounds).  capacity_out: HOST pointer, may be NULL.
+ * ws as for moe_router_fwd. */
+MOE_API moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_t k, double capacity_factor,
+                        int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                        int32_t* n_dropped, int64_t* capacity_out,
+                        void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Fused step: forward + dispatch + backward in one launch                  */
+/* ------------------------------------------------------------------------ */
+
+/* One pass of the whole hot path over a batch: exactly the outputs of
+ * moe_router_fwd, then moe_dispatch on the idx it produced, then
+ * moe_router_bwd with its f, computed by one persistent cooperative kernel
+ * (grid-wide barriers separate the global reductions).  Outputs are
+ * bit-identical to the three separate calls.  Arguments as above. */
+MOE_API moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                           float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
+                           float grad_scale,
+                           int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                           float* scalars, int32_t* rank_load,
+                           int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                           int32_t* n_dropped, float* dlogits,
+                           void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* TAOT Phase 1: batched topology-aware Sinkhorn flow plan                  */
+/* ------------------------------------------------------------------------ */
+
+/* [P4] §2 Phase 1 and §3: per microbatch m, the overloaded ranks' excess load
+ * is a supply and the idle ranks' spare capacity a demand:
+ *   a_r = max(load_r - mean, 0) / sum,  b_r = max(mean - load_r, 0) / sum
+ * The cost is W[r,s] = 0 (same rank), 1 (same node), lambda (across nodes),
+ * rank r on node r / ranks_per_node; the Gibbs kernel M = exp(-W/eps).
+ * Starting from v = 1, `iters` times: u = a / max(M v, 1e-30), then
+ * v = b / max(M^T u, 1e-30).  The plan is diag(u) M diag(v).
+ *
+ * loads [B,R] fp32; R in 1..64; ranks_per_node in 1..R dividing R;
+ * lambda > 0; eps <= 0 means eps = lambda; iters >= 0.
+ * u, v [B,R] fp32; plan [B,R,R] fp32 or NULL; status [B] int32:
+ * 0 = planned, 1 = nothing to move (no rank above the mean; u = v = plan = 0).
+ * One CTA per microbatch; no workspace. */
+MOE_API moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t R, int32_t ranks_per_node,
+                                 float lambda, float eps, int32_t iters,
+                                 float* u, float* v, float* plan, int32_t* status,
+                                 moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Misc                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Limit of every device-side wait (the grid barriers of the persistent
+ * kernels), process-wide, in nanoseconds; 0 restores the default of 2 s.
+ * When a wait expires, the kernel stops writing and returns, and the next
+ * moe_get_device_status reports MOE_ERR_TIMEOUT.  Tests shorten the limit to
+ * exercise that path; the library has no other use for it. */
+MOE_API void moe_set_wait_timeout_ns(uint64_t ns);
+
+MOE_API const char* moe_status_string(moe_status s);
+MOE_API const char* moe_last_error(void);
+MOE_API int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTER_H */

@@ -1,0 +1,225 @@
+"""Python binding of the C ABI (include/moe_router.h): argument marshalling only.
+
+Every function takes CUDA tensors, allocates outputs with torch (device memory
+is the only thing torch provides here), passes raw pointers and the current
+torch stream to the library, and checks the returned status.  All arithmetic
+runs in the library's CUDA kernels; nothing here computes on the host.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _native
+from ._native import MOE_DTYPE_BF16, MOE_DTYPE_FP32, MOE_NUM_SCALARS, SCALAR_NAMES, check, lib
+
+__all__ = [
+    "Workspace", "moe_router_fwd", "moe_router_bwd", "moe_dispatch", "moe_dispatch_capacity",
+    "moe_router_step", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
+]
+
+_DTYPES = {torch.float32: MOE_DTYPE_FP32, torch.bfloat16: MOE_DTYPE_BF16}
+
+
+def _stream_handle(stream: torch.cuda.Stream | None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype: torch.dtype | None = None) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+class Workspace:
+    """Device scratch of the persistent kernels, zero-filled once at creation.
+
+    One workspace serves calls ordered on one stream; it grows on demand.
+    """
+
+    def __init__(self, device: torch.device | int | None = None):
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
+                                   (device.index if isinstance(device, torch.device) else device))
+        self.buf: torch.Tensor | None = None
+
+    def ensure(self, T: int, E: int, k: int, stream: torch.cuda.Stream | None = None) -> tuple[int, int]:
+        need = int(lib().moe_router_workspace_size(T, E, k))
+        if need == 0:
+            raise ValueError(f"invalid sizes for a workspace: T={T}, E={E}, k={k}")
+        if self.buf is None or self.buf.numel() < need:
+            self.buf = torch.empty(need, dtype=torch.uint8, device=self.device)
+            check(lib().moe_workspace_init(_ptr(self.buf), need, _stream_handle(stream)), "moe_workspace_init")
+        return _ptr(self.buf), int(self.buf.numel())
+
+
+_workspaces: dict[tuple[int, int], Workspace] = {}
+
+
+def _default_ws(device: torch.device, stream: torch.cuda.Stream | None) -> Workspace:
+    key = (device.index, _stream_handle(stream))
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = _workspaces[key] = Workspace(device)
+    return ws
+
+
+def _out(out: dict | None, name: str, shape, dtype, device) -> torch.Tensor:
+    if out is not None and name in out and out[name] is not None:
+        t = out[name]
+        if tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device or not t.is_contiguous():
+            raise ValueError(f"out[{name!r}] must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+        return t
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def _fwd_outputs(T: int, E: int, k: int, n_ranks: int, device, out: dict | None) -> dict:
+    return {
+        "idx": _out(out, "idx", (T, k), torch.int32, device),
+        "gate": _out(out, "gate", (T, k), torch.float32, device),
+        "counts": _out(out, "counts", (E,), torch.int32, device),
+        "f": _out(out, "f", (E,), torch.float32, device),
+        "P": _out(out, "P", (E,), torch.float32, device),
+        "scalars": _out(out, "scalars", (MOE_NUM_SCALARS,), torch.float32, device),
+        "rank_load": _out(out, "rank_load", (max(n_ranks, 0),), torch.int32, device),
+    }
+
+
+def _dispatch_outputs(T: int, E: int, k: int, device, out: dict | None) -> dict:
+    return {
+        "perm": _out(out, "perm", (T * k,), torch.int32, device),
+        "slot": _out(out, "slot", (T * k,), torch.int32, device),
+        "offsets": _out(out, "offsets", (E + 1,), torch.int32, device),
+        "kept": _out(out, "kept", (E,), torch.int32, device),
+        "n_dropped": _out(out, "n_dropped", (1,), torch.int32, device),
+    }
+
+
+def moe_router_fwd(logits: torch.Tensor, k: int, alpha: float, renorm: int = -1, n_ranks: int = 0,
+                   ws: Workspace | None = None, out: dict | None = None,
+                   stream: torch.cuda.Stream | None = None) -> dict:
+    """Router softmax, top-k, gates, counts, f, P, scalars and rank loads (C: moe_router_fwd)."""
+    _need_cuda("logits", logits)
+    if logits.dtype not in _DTYPES or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 or bfloat16 tensor")
+    T, E = logits.shape
+    o = _fwd_outputs(T, E, k, n_ranks, logits.device, out)
+    ws = ws or _default_ws(logits.device, stream)
+    wp, wn = ws.ensure(T, E, k, stream)
+    st = lib().moe_router_fwd(_ptr(logits), _DTYPES[logits.dtype], T, E, k, float(alpha), int(renorm), int(n_ranks),
+                              _ptr(o["idx"]), _ptr(o["gate"]), _ptr(o["counts"]), _ptr(o["f"]), _ptr(o["P"]),
+                              _ptr(o["scalars"]), _ptr(o["rank_load"]) if n_ranks > 0 else None,
+                              wp, wn, _stream_handle(stream))
+    check(st, "moe_router_fwd")
+    return o
+
+
+def moe_router_bwd(logits: torch.Tensor, f: torch.Tensor, alpha: float, grad_scale: float = 1.0,
+                   dlogits: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """dL_aux/dlogits with f held constant (C: moe_router_bwd)."""
+    _need_cuda("logits", logits)
+    _need_cuda("f", f, torch.float32)
+    if logits.dtype not in _DTYPES or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 or bfloat16 tensor")
+    T, E = logits.shape
+    if f.numel() != E:
+        raise ValueError("f must have E elements")
+    dl = _out({"dlogits": dlogits}, "dlogits", (T, E), torch.float32, logits.device)
+    st = lib().moe_router_bwd(_ptr(logits), _DTYPES[logits.dtype], T, E, float(alpha), _ptr(f), float(grad_scale),
+                              _ptr(dl), _stream_handle(stream))
+    check(st, "moe_router_bwd")
+    return dl
+
+
+def moe_dispatch_capacity(T: int, E: int, k: int, capacity_factor: float) -> int:
+    """Expert capacity ceil(ceil(T*k/E) * capacity_factor) (C: moe_dispatch_capacity)."""
+    c = int(lib().moe_dispatch_capacity(T, E, k, float(capacity_factor)))
+    if c < 0:
+        raise ValueError("invalid capacity arguments")
+    return c
+
+
+def moe_dispatch(idx: torch.Tensor, E: int, capacity_factor: float, ws: Workspace | None = None,
+                 out: dict | None = None, stream: torch.cuda.Stream | None = None) -> dict:
+    """Stable capacity-limited dispatch of idx [T, k] (C: moe_dispatch)."""
+    _need_cuda("idx", idx, torch.int32)
+    if idx.dim() != 2:
+        raise ValueError("idx must be [T, k]")
+    T, k = idx.shape
+    o = _dispatch_outputs(T, E, k, idx.device, out)
+    ws = ws or _default_ws(idx.device, stream)
+    wp, wn = ws.ensure(T, E, k, stream)
+    cap = C.c_int64(0)
+    st = lib().moe_dispatch(_ptr(idx), T, E, k, float(capacity_factor), _ptr(o["perm"]), _ptr(o["slot"]),
+                            _ptr(o["offsets"]), _ptr(o["kept"]), _ptr(o["n_dropped"]), C.byref(cap),
+                            wp, wn, _stream_handle(stream))
+    check(st, "moe_dispatch")
+    o["capacity"] = int(cap.value)
+    return o
+
+
+def moe_router_step(logits: torch.Tensor, k: int, alpha: float, capacity_factor: float, renorm: int = -1,
+                    n_ranks: int = 0, grad_scale: float = 1.0, ws: Workspace | None = None,
+                    out: dict | None = None, stream: torch.cuda.Stream | None = None) -> dict:
+    """Forward + dispatch + backward in one launch (C: moe_router_step)."""
+    _need_cuda("logits", logits)
+    if logits.dtype not in _DTYPES or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 or bfloat16 tensor")
+    T, E = logits.shape
+    dev = logits.device
+    o = _fwd_outputs(T, E, k, n_ranks, dev, out)
+    o.update(_dispatch_outputs(T, E, k, dev, out))
+    o["dlogits"] = _out(out, "dlogits", (T, E), torch.float32, dev)
+    ws = ws or _default_ws(dev, stream)
+    wp, wn = ws.ensure(T, E, k, stream)
+    st = lib().moe_router_step(_ptr(logits), _DTYPES[logits.dtype], T, E, k, float(alpha), int(renorm), int(n_ranks),
+                               float(capacity_factor), float(grad_scale),
+                               _ptr(o["idx"]), _ptr(o["gate"]), _ptr(o["counts"]), _ptr(o["f"]), _ptr(o["P"]),
+                               _ptr(o["scalars"]), _ptr(o["rank_load"]) if n_ranks > 0 else None,
+                               _ptr(o["perm"]), _ptr(o["slot"]), _ptr(o["offsets"]), _ptr(o["kept"]),
+                               _ptr(o["n_dropped"]), _ptr(o["dlogits"]), wp, wn, _stream_handle(stream))
+    check(st, "moe_router_step")
+    o["capacity"] = moe_dispatch_capacity(T, E, k, capacity_factor)
+    return o
+
+
+def taot_sinkhorn_batched(loads: torch.Tensor, ranks_per_node: int, lam: float, eps: float = 0.0,
+                          iters: int = 50, with_plan: bool = True, out: dict | None = None,
+                          stream: torch.cuda.Stream | None = None) -> dict:
+    """TAOT Phase 1 topology-aware Sinkhorn plan per microbatch (C: taot_sinkhorn_batched)."""
+    _need_cuda("loads", loads, torch.float32)
+    if loads.dim() != 2:
+        raise ValueError("loads must be [B, R]")
+    B, R = loads.shape
+    dev = loads.device
+    o = {
+        "u": _out(out, "u", (B, R), torch.float32, dev),
+        "v": _out(out, "v", (B, R), torch.float32, dev),
+        "plan": _out(out, "plan", (B, R, R), torch.float32, dev) if with_plan else None,
+        "status": _out(out, "status", (B,), torch.int32, dev),
+    }
+    st = lib().taot_sinkhorn_batched(_ptr(loads), B, R, ranks_per_node, float(lam), float(eps), int(iters),
+                                     _ptr(o["u"]), _ptr(o["v"]), _ptr(o["plan"]), _ptr(o["status"]),
+                                     _stream_handle(stream))
+    check(st, "taot_sinkhorn_batched")
+    return o
+
+
+def moe_get_device_status(ws: Workspace, stream: torch.cuda.Stream | None = None) -> int:
+    """Reads and clears the device error flags of a workspace (synchronises)."""
+    if ws.buf is None:
+        return 0
+    flags = C.c_int32(0)
+    st = lib().moe_get_device_status(_ptr(ws.buf), _stream_handle(stream), C.byref(flags))
+    if st not in (_native.MOE_OK, _native.MOE_ERR_TIMEOUT):
+        check(st, "moe_get_device_status")
+    return int(flags.value)

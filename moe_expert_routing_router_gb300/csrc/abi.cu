@@ -1,0 +1,431 @@
+// Host side of the C ABI declared in include/moe_router.h: argument checks,
+// workspace layout, choice of the kernel variant, grid sizing and launches.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+
+#include "moe_router.h"
+#include "router_kernels.cuh"
+#include "router_table.h"
+#include "sinkhorn.h"
+
+namespace {
+
+using moe::RouterParams;
+using moe::RouterVariant;
+
+constexpr int kGridMax = 1024;                       // CTAs of the persistent kernel
+constexpr size_t kAlign = 256;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+moe_status fail(moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Workspace: [Ctrl][tile_hist E x kGridMax][P_part E x kGridMax][counts E]
+struct WsLayout {
+  size_t ctrl = 0, tile_hist = 0, p_part = 0, counts = 0, total = 0;
+};
+
+WsLayout ws_layout(int E) {
+  WsLayout w;
+  w.ctrl = 0;
+  w.tile_hist = align_up(sizeof(moe::Ctrl));
+  w.p_part = w.tile_hist + align_up(size_t(E) * kGridMax * sizeof(int32_t));
+  w.counts = w.p_part + align_up(size_t(E) * kGridMax * sizeof(float));
+  w.total = w.counts + align_up(size_t(E) * sizeof(int32_t));
+  return w;
+}
+
+// Per-device, per-kernel occupancy (blocks per SM) and SM count.
+struct DeviceInfo {
+  int sms = 0;
+};
+
+std::mutex g_mu;
+std::unordered_map<int, DeviceInfo> g_devices;
+std::unordered_map<std::string, int> g_occupancy;
+
+moe_status device_info(DeviceInfo* out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_devices.find(dev);
+  if (it == g_devices.end()) {
+    DeviceInfo d;
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    it = g_devices.emplace(dev, d).first;
+  }
+  *out = it->second;
+  *dev_out = dev;
+  return MOE_OK;
+}
+
+moe_status occupancy(const void* func, int threads, size_t smem, int dev, int* blocks) {
+  char key[96];
+  snprintf(key, sizeof(key), "%d:%p:%d:%zu", dev, func, threads, smem);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_occupancy.find(key);
+    if (it != g_occupancy.end()) {
+      *blocks = it->second;
+      return MOE_OK;
+    }
+  }
+  cudaError_t e = cudaSuccess;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  }
+  int b = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, func, threads, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (b < 1) return fail(MOE_ERR_CUDA, "kernel does not fit on an SM (smem %zu bytes)", smem);
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_occupancy[key] = b;
+  *blocks = b;
+  return MOE_OK;
+}
+
+// Picks the compiled variant for (dtype, E): the vector variant with the
+// smallest coverage when E % VW == 0 and the arrays are 16-byte aligned, else
+// the smallest scalar (VW == 1) variant.
+const RouterVariant* pick_variant(moe_dtype dt, int E, bool vec_ok) {
+  int n = 0;
+  const RouterVariant* tab = dt == MOE_DTYPE_BF16 ? moe::router_variants_bf16(&n) : moe::router_variants_fp32(&n);
+  const RouterVariant* best = nullptr;
+  for (int pass = 0; pass < 2 && !best; ++pass) {
+    for (int i = 0; i < n; ++i) {
+      const RouterVariant& v = tab[i];
+      const bool vec = v.VW > 1;
+      if (pass == 0 && (!vec || !vec_ok || E % v.VW != 0)) continue;
+      if (pass == 1 && vec) continue;
+      const int cover = v.LPR * v.VW * v.NV;
+      if (cover < E) continue;
+      if (!best || cover < best->LPR * best->VW * best->NV) best = &v;
+    }
+  }
+  return best;
+}
+
+moe_status check_router_args(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k) {
+  if (dt != MOE_DTYPE_FP32 && dt != MOE_DTYPE_BF16) return fail(MOE_ERR_UNSUPPORTED, "dtype %d is not fp32 (0) or bf16 (1)", int(dt));
+  if (!logits) return fail(MOE_ERR_INVALID, "logits is NULL");
+  if (T < 1 || T >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T = %lld outside [1, 2^31)", (long long)T);
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_INVALID, "E = %d outside [1, %d]", E, MOE_MAX_EXPERTS);
+  if (k < 1 || k > MOE_MAX_TOPK || k > E) return fail(MOE_ERR_INVALID, "k = %d outside [1, min(E, %d)]", k, MOE_MAX_TOPK);
+  if (T * (int64_t)k >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T*k = %lld does not fit int32", (long long)(T * k));
+  if (!aligned(logits, dt == MOE_DTYPE_BF16 ? 2 : 4)) return fail(MOE_ERR_INVALID, "logits is not element aligned");
+  return MOE_OK;
+}
+
+moe_status check_ws(void* ws, size_t ws_bytes, int E) {
+  if (!ws) return fail(MOE_ERR_INVALID, "workspace is NULL");
+  if (!aligned(ws, kAlign)) return fail(MOE_ERR_INVALID, "workspace is not 256-byte aligned");
+  const size_t need = ws_layout(E).total;
+  if (ws_bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return MOE_OK;
+}
+
+void bind_ws(RouterParams& p, void* ws, int E) {
+  const WsLayout w = ws_layout(E);
+  char* base = static_cast<char*>(ws);
+  p.ctrl = reinterpret_cast<moe::Ctrl*>(base + w.ctrl);
+  p.tile_hist = reinterpret_cast<int32_t*>(base + w.tile_hist);
+  p.P_part = reinterpret_cast<float*>(base + w.p_part);
+  p.counts_ws = reinterpret_cast<int32_t*>(base + w.counts);
+  p.G_stride = kGridMax;
+  p.timeout_ns = g_wait_ns.load(std::memory_order_relaxed);
+}
+
+int64_t capacity_of(int64_t T, int32_t E, int32_t k, double cf) {
+  const int64_t per_expert = (T * k + E - 1) / E;
+  return (int64_t)std::ceil(double(per_expert) * cf);
+}
+
+// Grid of the persistent kernel: every CTA resident (cooperative launch), at
+// least one full step of rows per CTA, at most kGridMax CTAs.
+moe_status persistent_grid(const RouterVariant* v, int64_t T, int E, int* G) {
+  DeviceInfo d;
+  int dev = 0;
+  moe_status s = device_info(&d, &dev);
+  if (s != MOE_OK) return s;
+  const size_t smem = moe::router_smem_bytes(E);
+  int bf = 0, bs = 0;
+  if ((s = occupancy(v->fwd, moe::kThreads, smem, dev, &bf)) != MOE_OK) return s;
+  if ((s = occupancy(v->step, moe::kThreads, smem, dev, &bs)) != MOE_OK) return s;
+  const int64_t cap = std::min<int64_t>(int64_t(std::min(bf, bs)) * d.sms, kGridMax);
+  const int64_t rows_per_step = int64_t(moe::kWarps) * (moe::kWarp / v->LPR);
+  const int64_t want = (T + rows_per_step - 1) / rows_per_step;
+  *G = int(std::max<int64_t>(1, std::min(cap, want)));
+  return MOE_OK;
+}
+
+moe_status launch_persistent(const void* func, const RouterParams& p, cudaStream_t stream) {
+  const size_t smem = moe::router_smem_bytes(p.E);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  }
+  void* args[] = {const_cast<RouterParams*>(&p)};
+  cudaError_t e = cudaLaunchCooperativeKernel(func, dim3(p.G), dim3(moe::kThreads), args, smem, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");
+  return MOE_OK;
+}
+
+RouterParams base_params(const void* logits, int64_t T, int32_t E, int32_t k) {
+  RouterParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.logits = logits;
+  p.T = T;
+  p.E = E;
+  p.k = k;
+  return p;
+}
+
+moe_status check_fwd_outputs(int32_t k, float alpha, int32_t renorm, int32_t n_ranks, int32_t E,
+                             const void* idx, const void* gate, const void* counts, const void* f,
+                             const void* P, const void* scalars, const void* rank_load) {
+  if (!(alpha >= 0.f) || !std::isfinite(alpha)) return fail(MOE_ERR_INVALID, "alpha must be finite and >= 0");
+  if (renorm < -1 || renorm > 1) return fail(MOE_ERR_INVALID, "renorm must be -1, 0 or 1");
+  if (n_ranks < 0 || n_ranks > MOE_MAX_RANKS || (n_ranks > 0 && E % n_ranks != 0))
+    return fail(MOE_ERR_INVALID, "n_ranks = %d must be 0 or a divisor of E in [1, %d]", n_ranks, MOE_MAX_RANKS);
+  if (!idx || !gate || !counts || !f || !P || !scalars) return fail(MOE_ERR_INVALID, "a forward output is NULL");
+  if (n_ranks > 0 && !rank_load) return fail(MOE_ERR_INVALID, "rank_load is NULL with n_ranks > 0");
+  (void)k;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_router_workspace_size(int64_t T, int32_t E, int32_t k) {
+  if (T < 1 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_TOPK || k > E) return 0;
+  return ws_layout(E).total;
+}
+
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || !aligned(ws, kAlign)) return fail(MOE_ERR_INVALID, "workspace is NULL or not 256-byte aligned");
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(void* ws, moe_stream_t stream, int32_t* flags) {
+  if (!ws || !flags) return fail(MOE_ERR_INVALID, "NULL argument");
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  moe::Ctrl* c = static_cast<moe::Ctrl*>(ws);
+  int32_t v = 0;
+  e = cudaMemcpy(&v, &c->error, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+  *flags = v;
+  if (v != 0) {
+    // Clear the flags and the barrier state for the next call.
+    e = cudaMemset(ws, 0, sizeof(moe::Ctrl));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    return fail(MOE_ERR_TIMEOUT, "device wait expired (flags 0x%x)", unsigned(v));
+  }
+  return MOE_OK;
+}
+
+int64_t moe_dispatch_capacity(int64_t T, int32_t E, int32_t k, double capacity_factor) {
+  if (T < 1 || T >= (int64_t(1) << 40) || E < 1 || k < 1 || !(capacity_factor > 0.0) || !std::isfinite(capacity_factor)) return -1;
+  return capacity_of(T, E, k, capacity_factor);
+}
+
+moe_status moe_router_fwd(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                          float alpha, int32_t renorm, int32_t n_ranks,
+                          int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                          float* scalars, int32_t* rank_load,
+                          void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_router_args(logits, dt, T, E, k);
+  if (s != MOE_OK) return s;
+  if ((s = check_fwd_outputs(k, alpha, renorm, n_ranks, E, idx, gate, counts, f, P, scalars, rank_load)) != MOE_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, E)) != MOE_OK) return s;
+  const RouterVariant* v = pick_variant(dt, E, aligned(logits, 16));
+  if (!v) return fail(MOE_ERR_INVALID, "no kernel variant for E = %d", E);
+  RouterParams p = base_params(logits, T, E, k);
+  p.alpha = alpha;
+  p.renorm = renorm < 0 ? (k > 1) : renorm;
+  p.n_ranks = n_ranks;
+  p.idx = idx; p.gate = gate; p.counts = counts; p.f = f; p.P = P; p.scalars = scalars; p.rank_load = rank_load;
+  bind_ws(p, ws, E);
+  if ((s = persistent_grid(v, T, E, &p.G)) != MOE_OK) return s;
+  return launch_persistent(v->fwd, p, stream);
+}
+
+moe_status moe_router_bwd(const void* logits, moe_dtype dt, int64_t T, int32_t E, float alpha,
+                          const float* f, float grad_scale, float* dlogits, moe_stream_t stream) {
+  moe_status s = check_router_args(logits, dt, T, E, 1);
+  if (s != MOE_OK) return s;
+  if (!(alpha >= 0.f) || !std::isfinite(alpha)) return fail(MOE_ERR_INVALID, "alpha must be finite and >= 0");
+  if (!std::isfinite(grad_scale)) return fail(MOE_ERR_INVALID, "grad_scale must be finite");
+  if (!f || !dlogits) return fail(MOE_ERR_INVALID, "f or dlogits is NULL");
+  if (!aligned(dlogits, 4) || !aligned(f, 4)) return fail(MOE_ERR_INVALID, "f or dlogits is not 4-byte aligned");
+  const RouterVariant* v = pick_variant(dt, E, aligned(logits, 16) && aligned(dlogits, 16));
+  if (!v) return fail(MOE_ERR_INVALID, "no kernel variant for E = %d", E);
+  DeviceInfo d;
+  int dev = 0;
+  if ((s = device_info(&d, &dev)) != MOE_OK) return s;
+  int blocks = 0;
+  if ((s = occupancy(v->bwd, moe::kThreads, 0, dev, &blocks)) != MOE_OK) return s;
+  const int64_t rows_per_block = int64_t(moe::kWarps) * (moe::kWarp / v->LPR);
+  const int64_t want = (T + rows_per_block - 1) / rows_per_block;
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(blocks) * d.sms)));
+  moe::BwdParams p;
+  p.logits = logits;
+  p.T = T;
+  p.E = E;
+  p.f = f;
+  p.coef = grad_scale * alpha * float(E) / float(T);
+  p.dlogits = dlogits;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernel(v->bwd, dim3(grid), dim3(moe::kThreads), args, 0, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
+  return MOE_OK;
+}
+
+moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_t k, double capacity_factor,
+                        int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                        int32_t* n_dropped, int64_t* capacity_out,
+                        void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!idx) return fail(MOE_ERR_INVALID, "idx is NULL");
+  if (T < 1 || T >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T = %lld outside [1, 2^31)", (long long)T);
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_INVALID, "E = %d outside [1, %d]", E, MOE_MAX_EXPERTS);
+  if (k < 1 || k > MOE_MAX_TOPK || k > E) return fail(MOE_ERR_INVALID, "k = %d outside [1, min(E, %d)]", k, MOE_MAX_TOPK);
+  if (T * (int64_t)k >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T*k does not fit int32");
+  if (!(capacity_factor > 0.0) || !std::isfinite(capacity_factor)) return fail(MOE_ERR_INVALID, "capacity_factor must be > 0");
+  if (!perm || !slot || !offsets || !kept || !n_dropped) return fail(MOE_ERR_INVALID, "a dispatch output is NULL");
+  moe_status s = check_ws(ws, ws_bytes, E);
+  if (s != MOE_OK) return s;
+  const int64_t C = capacity_of(T, E, k, capacity_factor);
+  if (capacity_out) *capacity_out = C;
+  RouterParams p = base_params(nullptr, T, E, k);
+  p.idx_in = idx;
+  p.C = int(std::min<int64_t>(C, INT32_MAX));
+  p.perm = perm; p.slot = slot; p.offsets = offsets; p.kept = kept; p.n_dropped = n_dropped;
+  bind_ws(p, ws, E);
+  DeviceInfo d;
+  int dev = 0;
+  if ((s = device_info(&d, &dev)) != MOE_OK) return s;
+  const void* func = moe::dispatch_kernel();
+  int blocks = 0;
+  if ((s = occupancy(func, moe::kThreads, moe::router_smem_bytes(E), dev, &blocks)) != MOE_OK) return s;
+  const int64_t cap = std::min<int64_t>(int64_t(blocks) * d.sms, kGridMax);
+  const int64_t want = (T * k + 2047) / 2048;
+  p.G = int(std::max<int64_t>(1, std::min(cap, want)));
+  return launch_persistent(func, p, stream);
+}
+
+moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                           float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
+                           float grad_scale,
+                           int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                           float* scalars, int32_t* rank_load,
+                           int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                           int32_t* n_dropped, float* dlogits,
+                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_router_args(logits, dt, T, E, k);
+  if (s != MOE_OK) return s;
+  if ((s = check_fwd_outputs(k, alpha, renorm, n_ranks, E, idx, gate, counts, f, P, scalars, rank_load)) != MOE_OK) return s;
+  if (!(capacity_factor > 0.0) || !std::isfinite(capacity_factor)) return fail(MOE_ERR_INVALID, "capacity_factor must be > 0");
+  if (!std::isfinite(grad_scale)) return fail(MOE_ERR_INVALID, "grad_scale must be finite");
+  if (!perm || !slot || !offsets || !kept || !n_dropped || !dlogits) return fail(MOE_ERR_INVALID, "a dispatch or backward output is NULL");
+  if (!aligned(dlogits, 4)) return fail(MOE_ERR_INVALID, "dlogits is not 4-byte aligned");
+  if ((s = check_ws(ws, ws_bytes, E)) != MOE_OK) return s;
+  const RouterVariant* v = pick_variant(dt, E, aligned(logits, 16) && aligned(dlogits, 16));
+  if (!v) return fail(MOE_ERR_INVALID, "no kernel variant for E = %d", E);
+  RouterParams p = base_params(logits, T, E, k);
+  p.alpha = alpha;
+  p.renorm = renorm < 0 ? (k > 1) : renorm;
+  p.n_ranks = n_ranks;
+  p.grad_scale = grad_scale;
+  p.C = int(std::min<int64_t>(capacity_of(T, E, k, capacity_factor), INT32_MAX));
+  p.idx = idx; p.gate = gate; p.counts = counts; p.f = f; p.P = P; p.scalars = scalars; p.rank_load = rank_load;
+  p.perm = perm; p.slot = slot; p.offsets = offsets; p.kept = kept; p.n_dropped = n_dropped;
+  p.dlogits = dlogits;
+  bind_ws(p, ws, E);
+  if ((s = persistent_grid(v, T, E, &p.G)) != MOE_OK) return s;
+  return launch_persistent(v->step, p, stream);
+}
+
+moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t R, int32_t ranks_per_node,
+                                 float lambda, float eps, int32_t iters,
+                                 float* u, float* v, float* plan, int32_t* status,
+                                 moe_stream_t stream) {
+  if (!loads || !u || !v || !status) return fail(MOE_ERR_INVALID, "a Sinkhorn argument is NULL");
+  if (B < 1) return fail(MOE_ERR_INVALID, "B = %d must be >= 1", B);
+  if (R < 1 || R > MOE_MAX_RANKS) return fail(MOE_ERR_INVALID, "R = %d outside [1, %d]", R, MOE_MAX_RANKS);
+  if (ranks_per_node < 1 || ranks_per_node > R || R % ranks_per_node != 0)
+    return fail(MOE_ERR_INVALID, "ranks_per_node = %d must divide R = %d", ranks_per_node, R);
+  if (!(lambda > 0.f) || !std::isfinite(lambda)) return fail(MOE_ERR_INVALID, "lambda must be > 0");
+  if (!std::isfinite(eps)) return fail(MOE_ERR_INVALID, "eps must be finite");
+  if (iters < 0) return fail(MOE_ERR_INVALID, "iters must be >= 0");
+  const double e = eps > 0.f ? double(eps) : double(lambda);
+  moe::SinkhornParams p;
+  p.loads = loads;
+  p.B = B;
+  p.R = R;
+  p.ranks_per_node = ranks_per_node;
+  p.iters = iters;
+  p.m_node = float(std::exp(-1.0 / e));
+  p.m_cross = float(std::exp(-double(lambda) / e));
+  p.u = u;
+  p.v = v;
+  p.plan = plan;
+  p.status = status;
+  cudaError_t err = moe::launch_taot_sinkhorn(p, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "taot_sinkhorn launch");
+  return MOE_OK;
+}
+
+void moe_set_wait_timeout_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs, std::memory_order_relaxed); }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dtype";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+int32_t moe_abi_version(void) { return MOE_ROUTER_ABI_VERSION; }
+
+}  // extern "C"

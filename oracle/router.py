@@ -115,6 +115,27 @@ def rank_loads(counts: np.ndarray, n_ranks: int) -> np.ndarray:
     return np.asarray(counts).reshape(n_ranks, E // n_ranks).sum(axis=1)
 
 
+def batch_statistics(counts: np.ndarray, P: np.ndarray, T: int, k: int, alpha: float,
+                     n_ranks: int = 0) -> dict:
+    """f and the batch scalars from the expert counts and P of a whole batch."""
+    E = len(counts)
+    f = token_fraction(counts, T, k)
+    mean = T * k / E
+    out = {
+        "counts": counts, "f": f, "P": P,
+        "l_aux": aux_loss(f, P, alpha), "balance": balance(f, P),
+        "cv": load_cv(counts), "max_over_mean": counts.max() / mean,
+        "min_over_mean": counts.min() / mean,
+        "rank_cv": 0.0, "rank_max_over_mean": 0.0, "rank_load": np.zeros(0, np.int64),
+    }
+    if n_ranks > 0:
+        rl = rank_loads(counts, n_ranks)
+        out["rank_load"] = rl
+        out["rank_cv"] = load_cv(rl)
+        out["rank_max_over_mean"] = rl.max() / (T * k / n_ranks)
+    return out
+
+
 def router_forward(logits: np.ndarray, dtype: str, k: int, alpha: float,
                    renorm: bool | None = None, n_ranks: int = 0) -> dict:
     """The whole forward of the router on one batch, in float64.
@@ -129,23 +150,9 @@ def router_forward(logits: np.ndarray, dtype: str, k: int, alpha: float,
         renorm = k > 1
     p = softmax(z)
     idx = top_k(z, k)
-    g = gates(p, idx, renorm)
-    counts = expert_counts(idx, E)
-    f = token_fraction(counts, T, k)
-    P = mean_router_prob(p)
-    mean = T * k / E
-    out = {
-        "idx": idx, "gate": g, "counts": counts, "f": f, "P": P,
-        "l_aux": aux_loss(f, P, alpha), "balance": balance(f, P),
-        "cv": load_cv(counts), "max_over_mean": counts.max() / mean,
-        "min_over_mean": counts.min() / mean,
-        "rank_cv": 0.0, "rank_max_over_mean": 0.0, "rank_load": np.zeros(0, np.int64),
-    }
-    if n_ranks > 0:
-        rl = rank_loads(counts, n_ranks)
-        out["rank_load"] = rl
-        out["rank_cv"] = load_cv(rl)
-        out["rank_max_over_mean"] = rl.max() / (T * k / n_ranks)
+    out = batch_statistics(expert_counts(idx, E), mean_router_prob(p), T, k, alpha, n_ranks)
+    out["idx"] = idx
+    out["gate"] = gates(p, idx, renorm)
     return out
 
 
@@ -156,16 +163,18 @@ def aux_loss_of_logits(z: np.ndarray, f: np.ndarray, alpha: float, grad_scale: f
 
 
 def aux_loss_grad(logits: np.ndarray, dtype: str, f: np.ndarray, alpha: float,
-                  grad_scale: float = 1.0) -> np.ndarray:
+                  grad_scale: float = 1.0, T: int | None = None) -> np.ndarray:
     """dL_aux/dz[t, j] = g * (alpha * N / T) * p[t, j] * (f_j - sum_i p[t, i] f_i).
 
     Differentiating alpha*N*sum_i f_i*(1/T)*sum_t p[t,i] through the softmax
     Jacobian dp_i/dz_j = p_i (delta_ij - p_j), with f constant.
+    ``T`` is the batch size when ``logits`` holds only some of its rows.
     Pinned by: central finite differences of ``aux_loss_of_logits``; rows sum
     to zero; the uniform-p special case (alpha/T)*(f_j - 1/N).
     """
     z = widen(logits, dtype)
-    T, E = z.shape
+    E = z.shape[1]
+    T = z.shape[0] if T is None else T
     p = softmax(z)
     s = (p * np.asarray(f, dtype=np.float64)[None, :]).sum(axis=1)
     return grad_scale * (alpha * E / T) * p * (f[None, :] - s[:, None])

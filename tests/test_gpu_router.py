@@ -1,0 +1,179 @@
+"""GPU parity of the router path through the C ABI against the CPU oracle.
+
+Small sizes span many CTAs and a ragged tail; full sizes are the four router
+workloads as benchmarked, compared on every element.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import (assert_equal, check_backward, check_dispatch, check_forward, oracle_forward,
+                    to_device, workload_inputs)
+
+pytestmark = pytest.mark.gpu
+
+WORKLOADS = list(synth.ROUTER_WORKLOADS)
+SMALL_T = {"switch-top1-T4096-E8": 1001, "zipf-top2-T65536-E64": 3001,
+           "zipf-hot-top8-T131072-E256": 2999, "zipf-ep64-top6-T262144-E384": 3007}
+
+
+@pytest.fixture(scope="module")
+def mr(native_lib):
+    import moe_expert_routing_router_gb300 as m
+    return m
+
+
+def _run_fwd(mr, w, logits):
+    x = to_device(logits, w.dtype)
+    got = mr.moe_router_fwd(x, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks)
+    torch.cuda.synchronize()
+    return x, got
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+@pytest.mark.parametrize("size", ["small", "full"])
+def test_forward_parity(mr, name, size):
+    w, logits = workload_inputs(name, SMALL_T[name] if size == "small" else None)
+    _, got = _run_fwd(mr, w, logits)
+    want = oracle_forward(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks)
+    check_forward(got, want, w.n_ranks)
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+@pytest.mark.parametrize("size", ["small", "full"])
+def test_backward_parity(mr, name, size):
+    w, logits = workload_inputs(name, SMALL_T[name] if size == "small" else None)
+    x = to_device(logits, w.dtype)
+    rng = np.random.default_rng(5)
+    f = rng.random(w.E).astype(np.float32)
+    f /= f.sum()
+    dl = mr.moe_router_bwd(x, torch.from_numpy(f).cuda(), w.alpha, grad_scale=1.5)
+    torch.cuda.synchronize()
+    check_backward(dl, logits, w.dtype, f.astype(np.float64), w.alpha, 1.5)
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+@pytest.mark.parametrize("size", ["small", "full"])
+def test_dispatch_parity(mr, name, size):
+    w, logits = workload_inputs(name, SMALL_T[name] if size == "small" else None)
+    z = logits
+    idx = np.concatenate([oracle.router.top_k(oracle.router.widen(z[r:r + 16384], w.dtype), w.k)
+                          for r in range(0, w.T, 16384)])
+    C = oracle.dispatch.capacity(w.T, w.k, w.E, w.capacity_factor)
+    got = mr.moe_dispatch(torch.from_numpy(idx.astype(np.int32)).cuda(), w.E, w.capacity_factor)
+    torch.cuda.synchronize()
+    assert got["capacity"] == C
+    check_dispatch(got, idx, w.E, C)
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+@pytest.mark.parametrize("size", ["small", "full"])
+def test_step_parity_and_equals_separate_calls(mr, name, size):
+    w, logits = workload_inputs(name, SMALL_T[name] if size == "small" else None)
+    x = to_device(logits, w.dtype)
+    st = mr.moe_router_step(x, w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks,
+                            grad_scale=1.0)
+    torch.cuda.synchronize()
+    want = oracle_forward(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks)
+    check_forward(st, want, w.n_ranks)
+    C = oracle.dispatch.capacity(w.T, w.k, w.E, w.capacity_factor)
+    check_dispatch(st, want["idx"], w.E, C)
+    check_backward(st["dlogits"], logits, w.dtype, want["f"], w.alpha, 1.0)
+    # the three separate calls give the same bits
+    fw = mr.moe_router_fwd(x, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks)
+    dp = mr.moe_dispatch(fw["idx"], w.E, w.capacity_factor)
+    dl = mr.moe_router_bwd(x, fw["f"], w.alpha, 1.0)
+    torch.cuda.synchronize()
+    for key in ("idx", "gate", "counts", "f", "P", "scalars", "rank_load"):
+        assert torch.equal(st[key], fw[key]), key
+    for key in ("perm", "slot", "offsets", "kept", "n_dropped"):
+        assert torch.equal(st[key], dp[key]), key
+    assert torch.equal(st["dlogits"], dl)
+
+
+def test_repeated_calls_are_bit_identical(mr):
+    w, logits = workload_inputs("zipf-ep64-top6-T262144-E384", 20011)
+    x = to_device(logits, w.dtype)
+    a = mr.moe_router_step(x, w.k, w.alpha, w.capacity_factor, n_ranks=w.n_ranks)
+    b = mr.moe_router_step(x, w.k, w.alpha, w.capacity_factor, n_ranks=w.n_ranks)
+    torch.cuda.synchronize()
+    for key in a:
+        if isinstance(a[key], torch.Tensor):
+            assert torch.equal(a[key], b[key]), key
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+EDGE = [
+    # (T, E, k, dtype, renorm, n_ranks, cf, levels)   levels > 0: integer logits (ties)
+    (1, 1, 1, "fp32", -1, 0, 1.0, 0),
+    (1, 1, 1, "bf16", -1, 1, 1.0, 0),
+    (5, 8, 8, "bf16", -1, 2, 1.0, 0),          # k = E
+    (777, 64, 4, "bf16", -1, 8, 1.0, 3),       # heavy ties, vector path
+    (513, 7, 3, "fp32", -1, 7, 0.5, 2),        # odd E, scalar path, ties, drops
+    (1000, 33, 2, "bf16", 0, 0, 2.0, 0),       # odd E, raw gates for k = 2
+    (300, 100, 1, "bf16", 1, 10, 1.0, 0),      # renormalised top-1 gate (= 1)
+    (4099, 1024, 8, "bf16", -1, 64, 1.25, 0),  # largest E and k
+    (2050, 1000, 5, "fp32", -1, 8, 1.0, 4),    # E not a multiple of the vector width
+    (100003, 64, 2, "bf16", -1, 0, 1.25, 0),   # long ragged batch
+    (4096, 8, 1, "fp32", -1, 0, 1.25, 0),      # Switch top-1, E = 8
+    (3000, 384, 6, "fp32", -1, 64, 1.0, 0),    # fp32 vector path at E = 384
+    (2000, 16, 2, "bf16", -1, 4, 0.25, 0),     # capacity below the mean: most tokens dropped
+]
+
+
+@pytest.mark.parametrize("T,E,k,dtype,renorm,n_ranks,cf,levels", EDGE)
+def test_edge_cases(mr, T, E, k, dtype, renorm, n_ranks, cf, levels):
+    logits = synth.random_logits(T, E, dtype, seed=T * 7 + E, scale=2.0, integer_levels=levels)
+    x = to_device(logits, dtype)
+    st = mr.moe_router_step(x, k, 0.01, cf, renorm=renorm, n_ranks=n_ranks, grad_scale=0.5)
+    torch.cuda.synchronize()
+    rn = None if renorm < 0 else bool(renorm)
+    want = oracle_forward(logits, dtype, k, 0.01, rn, n_ranks)
+    check_forward(st, want, n_ranks)
+    check_dispatch(st, want["idx"], E, oracle.dispatch.capacity(T, k, E, cf))
+    check_backward(st["dlogits"], logits, dtype, want["f"], 0.01, 0.5)
+
+
+def test_misaligned_views_take_the_scalar_path(mr):
+    T, E, k = 1500, 64, 2
+    base = synth.random_logits(T + 1, E, "bf16", seed=3)
+    flat = to_device(base, "bf16").reshape(-1)
+    x = flat[3:3 + T * E].view(T, E)             # 6-byte offset: not 16-byte aligned
+    logits = base.reshape(-1)[3:3 + T * E].reshape(T, E)
+    fw = mr.moe_router_fwd(x, k, 0.01)
+    dl_buf = torch.empty(T * E + 1, dtype=torch.float32, device="cuda")
+    dl = mr.moe_router_bwd(x, fw["f"], 0.01, 1.0, dlogits=dl_buf[1:].view(T, E))
+    torch.cuda.synchronize()
+    want = oracle_forward(logits, "bf16", k, 0.01, None, 0)
+    check_forward(fw, want, 0)
+    check_backward(dl, logits, "bf16", want["f"], 0.01, 1.0)
+
+
+def test_dispatch_of_arbitrary_assignments(mr):
+    # user-supplied idx may repeat an expert within a token; the sort stays stable
+    rng = np.random.default_rng(9)
+    T, k, E = 5000, 3, 37
+    idx = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    idx[:50] = 5                                    # a burst on one expert
+    got = mr.moe_dispatch(torch.from_numpy(idx).cuda(), E, 0.8)
+    torch.cuda.synchronize()
+    C = oracle.dispatch.capacity(T, k, E, 0.8)
+    check_dispatch(got, idx, E, C)
+
+
+def test_uniform_routing_gives_unit_balance(mr):
+    # [P2] §2.2: uniform routing makes E * sum f P equal to 1
+    T, E = 4096, 16
+    z = np.zeros((T, E), dtype=np.float32)
+    z[np.arange(T), np.arange(T) % E] = 5.0
+    fw = mr.moe_router_fwd(to_device(z, "fp32"), 1, 0.01)
+    torch.cuda.synchronize()
+    assert_equal("counts", fw["counts"].cpu().numpy(), np.full(E, T // E))
+    sc = fw["scalars"].cpu().numpy()
+    want = oracle_forward(z, "fp32", 1, 0.01, None, 0)
+    assert abs(sc[1] - want["balance"]) <= 1e-5 * want["balance"]
+    assert sc[2] == 0.0                             # CV of equal counts
