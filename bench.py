@@ -403,7 +403,7 @@ def run_ours(args) -> dict:
     pk = peaks()
     w = synth.ROUTER_WORKLOADS[args.workload]
     sampler = ClockSampler(dist_ctx.local)
-    r = time_router(w, args.steps, args.warmup, torch, device, dist_ctx, soak_s=1.0, sampler=sampler)
+    r = time_router(w, args.steps, args.warmup, torch, device, dist_ctx, soak_s=args.soak_seconds, sampler=sampler)
     ms_step = r["total_ms"] / args.steps
     value = dist_ctx.world * w.T / (ms_step * 1e-3)
     achieved = r["step_bytes"] / (r["launch_ms_mean"] * 1e-3) / 1e9
@@ -462,6 +462,8 @@ def main() -> int:
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.ROUTER_WORKLOADS))
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads and the Sinkhorn line")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--soak-seconds", type=float, default=1.0,
+                    help="loaded window before the timed region, for the clock samples")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warmup raised to 3")

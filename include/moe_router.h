@@ -225,6 +225,29 @@ MOE_API moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t 
  * exercise that path; the library has no other use for it. */
 MOE_API void moe_set_wait_timeout_ns(uint64_t ns);
 
+/* Test hook for the timeout path, process-wide: with enable != 0 the grid
+ * barriers of later launches wait for one CTA more than the grid holds, so no
+ * barrier is ever released and every wait runs to its limit (shorten it with
+ * moe_set_wait_timeout_ns first).  The kernels then stop writing after the
+ * forward and return; moe_get_device_status reports MOE_ERR_TIMEOUT.  Nothing
+ * faults or hangs.  0 restores normal barriers. */
+MOE_API void moe_set_unreachable_barriers(int32_t enable);
+
+/* Phase tracing of the persistent kernels (moe_router_fwd, moe_dispatch,
+ * moe_router_step), process-wide.  With a non-NULL DEVICE buffer of
+ * max_ctas * MOE_TRACE_POINTS uint64 values, every launch has CTA c write
+ * %globaltimer (ns) to device_buf[c * MOE_TRACE_POINTS + i] at phase boundary
+ * i (points a launch does not pass are left as they were):
+ *   0 entry, 1 first forward ring stage landed, 2 forward rows done (warp 0),
+ *   3 per-CTA partials published, 4 after grid barrier 1, 5 per-expert scans
+ *   done, 6 after grid barrier 2, 7 first backward stage available, 8 backward
+ *   rows done (warp 0), 9 dispatch and E-sized outputs done (dispatch warp),
+ *   10 all warps joined, 11 exit.
+ * A launch with more than max_ctas CTAs fails with MOE_ERR_INVALID.  NULL
+ * turns tracing off. */
+#define MOE_TRACE_POINTS 16
+MOE_API void moe_set_trace_buffer(uint64_t* device_buf, int32_t max_ctas);
+
 MOE_API const char* moe_status_string(moe_status s);
 MOE_API const char* moe_last_error(void);
 MOE_API int32_t moe_abi_version(void);

@@ -33,6 +33,8 @@ SIGNATURES = {
                                _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "taot_sinkhorn_batched": (_i32, [_p, _i32, _i32, _i32, _f32, _f32, _i32, _p, _p, _p, _p, _p]),
     "moe_set_wait_timeout_ns": (None, [C.c_uint64]),
+    "moe_set_unreachable_barriers": (None, [_i32]),
+    "moe_set_trace_buffer": (None, [_p, _i32]),
     "moe_status_string": (C.c_char_p, [_i32]),
     "moe_last_error": (C.c_char_p, []),
     "moe_abi_version": (_i32, []),

@@ -23,7 +23,8 @@ LIBDIR = PKG / "_lib"
 LIBNAME = "libmoerouter.so"
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
-SOURCES = ["router_bf16.cu", "router_fp32.cu", "router_dispatch.cu", "sinkhorn.cu", "abi.cu"]
+SOURCES = ["router_bf16_staged.cu", "router_bf16_direct.cu", "router_fp32_staged.cu", "router_fp32_direct.cu",
+           "router_dispatch.cu", "sinkhorn.cu", "abi.cu"]
 
 
 def nvcc() -> str:

@@ -27,6 +27,9 @@ constexpr int kGridMax = 1024;                       // CTAs of the persistent k
 constexpr size_t kAlign = 256;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<unsigned long long*> g_trace{nullptr};
+std::atomic<unsigned> g_barrier_extra{0};
+std::atomic<int> g_trace_ctas{0};
 
 thread_local std::string g_last_error;
 
@@ -116,24 +119,24 @@ moe_status occupancy(const void* func, int threads, size_t smem, int dev, int* b
   return MOE_OK;
 }
 
-// Picks the compiled variant for (dtype, E): the vector variant with the
-// smallest coverage when E % VW == 0 and the arrays are 16-byte aligned, else
-// the smallest scalar (VW == 1) variant.
-const RouterVariant* pick_variant(moe_dtype dt, int E, bool vec_ok) {
-  int n = 0;
-  const RouterVariant* tab = dt == MOE_DTYPE_BF16 ? moe::router_variants_bf16(&n) : moe::router_variants_fp32(&n);
+// Picks the compiled variant for (dtype, E): a staged variant (rows streamed
+// through the shared-memory ring) with the smallest coverage when a row is a
+// multiple of 16 bytes and the arrays are 16-byte aligned, else the smallest
+// direct variant (one element per load, any E).
+const RouterVariant* pick_variant(moe_dtype dt, int E, bool aligned16) {
+  const int esize = dt == MOE_DTYPE_BF16 ? 2 : 4;
+  const bool staged_ok = aligned16 && (E * esize) % 16 == 0;
+  int ns = 0, nd = 0;
+  const RouterVariant* st = dt == MOE_DTYPE_BF16 ? moe::router_variants_bf16_staged(&ns) : moe::router_variants_fp32_staged(&ns);
+  const RouterVariant* di = dt == MOE_DTYPE_BF16 ? moe::router_variants_bf16_direct(&nd) : moe::router_variants_fp32_direct(&nd);
   const RouterVariant* best = nullptr;
-  for (int pass = 0; pass < 2 && !best; ++pass) {
-    for (int i = 0; i < n; ++i) {
-      const RouterVariant& v = tab[i];
-      const bool vec = v.VW > 1;
-      if (pass == 0 && (!vec || !vec_ok || E % v.VW != 0)) continue;
-      if (pass == 1 && vec) continue;
-      const int cover = v.LPR * v.VW * v.NV;
-      if (cover < E) continue;
-      if (!best || cover < best->LPR * best->VW * best->NV) best = &v;
-    }
-  }
+  auto cover = [](const RouterVariant* v) { return v->LPR * v->VW * v->NV; };
+  if (staged_ok)
+    for (int i = 0; i < ns; ++i)
+      if (cover(&st[i]) >= E && E % st[i].VW == 0 && (!best || cover(&st[i]) < cover(best))) best = &st[i];
+  if (!best)
+    for (int i = 0; i < nd; ++i)
+      if (cover(&di[i]) >= E && (!best || cover(&di[i]) < cover(best))) best = &di[i];
   return best;
 }
 
@@ -165,6 +168,8 @@ void bind_ws(RouterParams& p, void* ws, int E) {
   p.counts_ws = reinterpret_cast<int32_t*>(base + w.counts);
   p.G_stride = kGridMax;
   p.timeout_ns = g_wait_ns.load(std::memory_order_relaxed);
+  p.trace = g_trace.load(std::memory_order_relaxed);
+  p.barrier_extra = g_barrier_extra.load(std::memory_order_relaxed);
 }
 
 int64_t capacity_of(int64_t T, int32_t E, int32_t k, double cf) {
@@ -172,26 +177,55 @@ int64_t capacity_of(int64_t T, int32_t E, int32_t k, double cf) {
   return (int64_t)std::ceil(double(per_expert) * cf);
 }
 
-// Grid of the persistent kernel: every CTA resident (cooperative launch), at
-// least one full step of rows per CTA, at most kGridMax CTAs.
-moe_status persistent_grid(const RouterVariant* v, int64_t T, int E, int* G) {
+// Launch geometry of the persistent kernel: every CTA resident (cooperative
+// launch), at least one row group per consumer warp, at most kGridMax CTAs;
+// for staged variants, ring stages of about 16 KB and as many slots as fit in
+// the shared memory left per CTA (or as the chunk needs).
+struct Geometry {
+  int G = 1, rows_per_stage = 0, n_slots = 0;
+  size_t smem = 0;
+};
+
+constexpr size_t kSmemPerSm = 228 * 1024;      // GB300 shared memory per SM
+constexpr size_t kSmemReservedPerCta = 1024;
+
+moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, int E, Geometry* out) {
   DeviceInfo d;
   int dev = 0;
   moe_status s = device_info(&d, &dev);
   if (s != MOE_OK) return s;
-  const size_t smem = moe::router_smem_bytes(E);
+  const int esize = dt == MOE_DTYPE_BF16 ? 2 : 4;
+  const int group_rows = moe::kConsumerWarps * (moe::kWarp / v->LPR) * v->NR;
+  Geometry g;
+  const size_t fixed = moe::router_smem_layout(E, 0, 0).total;
+  if (v->staged) {
+    const int row_bytes = E * esize;
+    g.rows_per_stage = std::max(group_rows, (16384 / row_bytes) / group_rows * group_rows);
+    const size_t stage_bytes = size_t(g.rows_per_stage) * row_bytes;
+    const size_t budget = kSmemPerSm / size_t(v->min_blocks) - kSmemReservedPerCta;
+    g.n_slots = int(std::max<size_t>(1, std::min<size_t>(moe::kMaxSlots, (budget - fixed) / stage_bytes)));
+  }
+  size_t smem = moe::router_smem_layout(E, g.n_slots, g.rows_per_stage * E * esize).total;
   int bf = 0, bs = 0;
   if ((s = occupancy(v->fwd, moe::kThreads, smem, dev, &bf)) != MOE_OK) return s;
   if ((s = occupancy(v->step, moe::kThreads, smem, dev, &bs)) != MOE_OK) return s;
   const int64_t cap = std::min<int64_t>(int64_t(std::min(bf, bs)) * d.sms, kGridMax);
-  const int64_t rows_per_step = int64_t(moe::kWarps) * (moe::kWarp / v->LPR);
-  const int64_t want = (T + rows_per_step - 1) / rows_per_step;
-  *G = int(std::max<int64_t>(1, std::min(cap, want)));
+  const int64_t want = (T + group_rows - 1) / group_rows;
+  g.G = int(std::max<int64_t>(1, std::min(cap, want)));
+  if (v->staged) {   // no more slots than the largest chunk has stages
+    const int64_t chunk = (T + g.G - 1) / g.G;
+    const int64_t stages = (chunk + g.rows_per_stage - 1) / g.rows_per_stage;
+    g.n_slots = int(std::max<int64_t>(1, std::min<int64_t>(g.n_slots, stages)));
+    smem = moe::router_smem_layout(E, g.n_slots, g.rows_per_stage * E * esize).total;
+  }
+  g.smem = smem;
+  *out = g;
   return MOE_OK;
 }
 
-moe_status launch_persistent(const void* func, const RouterParams& p, cudaStream_t stream) {
-  const size_t smem = moe::router_smem_bytes(p.E);
+moe_status launch_persistent(const void* func, const RouterParams& p, size_t smem, cudaStream_t stream) {
+  if (p.trace != nullptr && p.G > g_trace_ctas.load(std::memory_order_relaxed))
+    return fail(MOE_ERR_INVALID, "trace buffer holds %d CTAs, the launch has %d", g_trace_ctas.load(), p.G);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
@@ -281,8 +315,12 @@ moe_status moe_router_fwd(const void* logits, moe_dtype dt, int64_t T, int32_t E
   p.n_ranks = n_ranks;
   p.idx = idx; p.gate = gate; p.counts = counts; p.f = f; p.P = P; p.scalars = scalars; p.rank_load = rank_load;
   bind_ws(p, ws, E);
-  if ((s = persistent_grid(v, T, E, &p.G)) != MOE_OK) return s;
-  return launch_persistent(v->fwd, p, stream);
+  Geometry geo;
+  if ((s = persistent_geometry(v, dt, T, E, &geo)) != MOE_OK) return s;
+  p.G = geo.G;
+  p.rows_per_stage = geo.rows_per_stage;
+  p.n_slots = geo.n_slots;
+  return launch_persistent(v->fwd, p, geo.smem, stream);
 }
 
 moe_status moe_router_bwd(const void* logits, moe_dtype dt, int64_t T, int32_t E, float alpha,
@@ -298,9 +336,10 @@ moe_status moe_router_bwd(const void* logits, moe_dtype dt, int64_t T, int32_t E
   DeviceInfo d;
   int dev = 0;
   if ((s = device_info(&d, &dev)) != MOE_OK) return s;
+  constexpr int kBwdThreads = 256;
   int blocks = 0;
-  if ((s = occupancy(v->bwd, moe::kThreads, 0, dev, &blocks)) != MOE_OK) return s;
-  const int64_t rows_per_block = int64_t(moe::kWarps) * (moe::kWarp / v->LPR);
+  if ((s = occupancy(v->bwd, kBwdThreads, 0, dev, &blocks)) != MOE_OK) return s;
+  const int64_t rows_per_block = int64_t(kBwdThreads / moe::kWarp) * (moe::kWarp / v->LPR);
   const int64_t want = (T + rows_per_block - 1) / rows_per_block;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(blocks) * d.sms)));
   moe::BwdParams p;
@@ -311,7 +350,7 @@ moe_status moe_router_bwd(const void* logits, moe_dtype dt, int64_t T, int32_t E
   p.coef = grad_scale * alpha * float(E) / float(T);
   p.dlogits = dlogits;
   void* args[] = {&p};
-  cudaError_t e = cudaLaunchKernel(v->bwd, dim3(grid), dim3(moe::kThreads), args, 0, stream);
+  cudaError_t e = cudaLaunchKernel(v->bwd, dim3(grid), dim3(kBwdThreads), args, 0, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
   return MOE_OK;
 }
@@ -340,12 +379,13 @@ moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_t k, dou
   int dev = 0;
   if ((s = device_info(&d, &dev)) != MOE_OK) return s;
   const void* func = moe::dispatch_kernel();
+  const size_t smem = moe::router_smem_layout(E, 0, 0).total;
   int blocks = 0;
-  if ((s = occupancy(func, moe::kThreads, moe::router_smem_bytes(E), dev, &blocks)) != MOE_OK) return s;
+  if ((s = occupancy(func, moe::kThreads, smem, dev, &blocks)) != MOE_OK) return s;
   const int64_t cap = std::min<int64_t>(int64_t(blocks) * d.sms, kGridMax);
   const int64_t want = (T * k + 2047) / 2048;
   p.G = int(std::max<int64_t>(1, std::min(cap, want)));
-  return launch_persistent(func, p, stream);
+  return launch_persistent(func, p, smem, stream);
 }
 
 moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
@@ -376,8 +416,12 @@ moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t 
   p.perm = perm; p.slot = slot; p.offsets = offsets; p.kept = kept; p.n_dropped = n_dropped;
   p.dlogits = dlogits;
   bind_ws(p, ws, E);
-  if ((s = persistent_grid(v, T, E, &p.G)) != MOE_OK) return s;
-  return launch_persistent(v->step, p, stream);
+  Geometry geo;
+  if ((s = persistent_geometry(v, dt, T, E, &geo)) != MOE_OK) return s;
+  p.G = geo.G;
+  p.rows_per_stage = geo.rows_per_stage;
+  p.n_slots = geo.n_slots;
+  return launch_persistent(v->step, p, geo.smem, stream);
 }
 
 moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t R, int32_t ranks_per_node,
@@ -409,6 +453,13 @@ moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t R, int32
   if (err != cudaSuccess) return cuda_fail(err, "taot_sinkhorn launch");
   return MOE_OK;
 }
+
+void moe_set_trace_buffer(uint64_t* device_buf, int32_t max_ctas) {
+  g_trace_ctas.store(device_buf ? max_ctas : 0, std::memory_order_relaxed);
+  g_trace.store(reinterpret_cast<unsigned long long*>(device_buf), std::memory_order_relaxed);
+}
+
+void moe_set_unreachable_barriers(int32_t enable) { g_barrier_extra.store(enable ? 1u : 0u, std::memory_order_relaxed); }
 
 void moe_set_wait_timeout_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs, std::memory_order_relaxed); }
 

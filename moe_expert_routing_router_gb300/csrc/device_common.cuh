@@ -1,5 +1,6 @@
-// Device helpers shared by the router kernels: order-preserving top-k keys,
-// lane-group reductions, the bounded grid barrier and exp2.
+// Device helpers shared by the router kernels: the bounded grid barrier,
+// mbarrier / bulk-copy (TMA) primitives, order-preserving top-k keys, exp2
+// and lane-group reductions.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -11,21 +12,25 @@ constexpr int kWarp = 32;
 constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
 
 // ---------------------------------------------------------------------------
-// Workspace control block (first 256 bytes of the caller's workspace).
+// Workspace control block (first 512 bytes of the caller's workspace).  The
+// fields that many CTAs touch at once sit on separate 128-byte lines.
 // ---------------------------------------------------------------------------
 struct Ctrl {
   unsigned bar_count;   // CTAs arrived at the current grid barrier (0 between barriers)
+  unsigned pad0[31];
   unsigned bar_gen;     // barrier generation, bumped by the last arriver
+  unsigned pad1[31];
   int error;            // sticky error bits, read and cleared by the host
-  int pad[61];
+  int pad2[31];
+  unsigned pad3[32];
 };
-static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
+static_assert(sizeof(Ctrl) == 512, "control block is 512 bytes");
 
-enum : int { kErrBarrierTimeout = 1 };
+enum : int { kErrBarrierTimeout = 1, kErrPipelineTimeout = 2 };
 
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t) :: "memory");
   return t;
 }
 
@@ -35,41 +40,121 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ int ld_volatile_i32(const int* p) {
   return *reinterpret_cast<const volatile int*>(p);
 }
 
-// Grid-wide barrier for a cooperative launch (all CTAs co-resident).  The wait
-// is bounded by `timeout_ns`; on expiry the CTA records kErrBarrierTimeout.
+// Grid-wide barrier for a cooperative launch (all CTAs co-resident): the CTA
+// that brings the arrivals to nblocks + extra releases it (extra is 0 except in
+// tests of the timeout path, where it makes the release unreachable).  The
+// wait is bounded by `timeout_ns`; on expiry the CTA records kErrBarrierTimeout.
 // Returns false (uniformly across the CTA) once any CTA of the launch has
 // recorded an error: the caller must then stop writing and return, and later
 // barriers stop waiting because the flag is already set.
-__device__ __forceinline__ bool grid_barrier(Ctrl* c, unsigned nblocks, uint64_t timeout_ns, int* s_flag) {
-  __syncthreads();
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// Called by the `nthreads` threads (whole warps, including thread 0) that
+// synchronise on named barrier `bar_id` within the CTA.
+__device__ __forceinline__ bool grid_barrier(Ctrl* c, unsigned nblocks, unsigned extra, uint64_t timeout_ns,
+                                             int* s_flag, int bar_id, int nthreads) {
+  named_barrier(bar_id, nthreads);               // the group's writes happen before thread 0's arrival
   if (threadIdx.x == 0) {
     const unsigned gen = ld_acquire_u32(&c->bar_gen);
-    __threadfence();
-    const unsigned arrived = atomicAdd(&c->bar_count, 1u);
-    if (arrived == nblocks - 1) {
-      atomicExch(&c->bar_count, 0u);
-      __threadfence();
-      atomicAdd(&c->bar_gen, 1u);
+    unsigned arrived;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(arrived) : "l"(&c->bar_count) : "memory");
+    if (arrived == nblocks + extra - 1) {
+      c->bar_count = 0u;
+      st_release_u32(&c->bar_gen, gen + 1u);   // orders the reset (and every arrival seen) before the release
     } else {
-      const uint64_t t0 = global_ns();
-      while (ld_acquire_u32(&c->bar_gen) == gen) {
-        if (ld_volatile_i32(&c->error) != 0) break;
-        if (global_ns() - t0 > timeout_ns) {
-          atomicOr(&c->error, kErrBarrierTimeout);
-          break;
+      uint64_t t0 = 0;
+      for (unsigned spin = 0;; ++spin) {
+        if (ld_acquire_u32(&c->bar_gen) != gen) break;
+        if ((spin & 15u) == 15u) {
+          if (ld_volatile_i32(&c->error) != 0) break;
+          const uint64_t now = global_ns();
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > timeout_ns) {
+            atomicOr(&c->error, kErrBarrierTimeout);
+            break;
+          }
         }
-        __nanosleep(32);
+        if (spin > 8) __nanosleep(64);
       }
     }
-    __threadfence();
     *s_flag = ld_volatile_i32(&c->error);
   }
-  __syncthreads();
+  named_barrier(bar_id, nthreads);
   return *s_flag == 0;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier and bulk asynchronous copy (TMA, non-tensor form).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Waits until the barrier phase of parity `parity` has completed; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_ns() - t0 > timeout_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global to shared memory; completion is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -81,43 +166,55 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Reciprocal on the special-function unit (the hardware instruction).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------------------
-// Element types.  Raw is the storage word of one element.
+// Element types.  Raw is the storage word of one element; bits() gives its
+// fp32 bit pattern.  key_from_bits() is an order-preserving signed integer: a
+// larger logit gives a larger key, and of equal logits (-0.0 equals +0.0) the
+// lower column gets the larger key.
 // ---------------------------------------------------------------------------
 struct Bf16 {
   using Raw = uint16_t;
-  using Key = int;          // 32-bit: 16 value bits + 16 index bits
-  static __device__ __forceinline__ float to_float(Raw r) { return __uint_as_float(uint32_t(r) << 16); }
-  // Order-preserving signed key: larger logit -> larger key; equal logits ->
-  // the lower column has the larger key.  -0.0 and +0.0 map to the same value.
-  static __device__ __forceinline__ Key key(Raw r, int col) {
-    const int s = int(uint32_t(r) << 16);
-    const int v = s < 0 ? -(s & 0x7fffffff) : s;   // sign-magnitude -> two's complement
-    return v | (0xffff - col);                        // low 16 bits of v are zero
+  using Key = int;          // 16 value bits above 16 column bits
+  static constexpr Raw kNegInf = 0xff80u;
+  static __device__ __forceinline__ uint32_t bits(Raw r) { return uint32_t(r) << 16; }
+  static __device__ __forceinline__ Key key_from_bits(uint32_t b, int col) {
+    const int v = int(b);
+    const int s = v >> 31;                        // 0, or -1 for a negative value
+    const int t = v ^ (s & 0x7fffffff);           // one's complement of negative magnitudes
+    return t - s + (0xffff - col);                // two's complement; the low 16 bits of v are zero
   }
   static __device__ __forceinline__ int key_col(Key k) { return 0xffff - (k & 0xffff); }
   static __device__ __forceinline__ float key_value(Key k) {
     const int v = k & int(0xffff0000u);
-    const uint32_t bits = v < 0 ? (0x80000000u | uint32_t(-v)) : uint32_t(v);
-    return __uint_as_float(bits);
+    const uint32_t b = v < 0 ? (0x80000000u | uint32_t(-v)) : uint32_t(v);
+    return __uint_as_float(b);
   }
   static constexpr Key kKeyMin = int(0x80000000u);
 };
 
 struct Fp32 {
   using Raw = uint32_t;
-  using Key = long long;    // 64-bit: 32 value bits + 32 index bits
-  static __device__ __forceinline__ float to_float(Raw r) { return __uint_as_float(r); }
-  static __device__ __forceinline__ Key key(Raw r, int col) {
-    const int s = int(r);
-    const long long v = s < 0 ? -(long long)(s & 0x7fffffff) : (long long)s;
-    return (long long)((unsigned long long)v << 32) | (long long)(0xffffffffu - uint32_t(col));
+  using Key = long long;    // 32 value bits above 32 column bits
+  static constexpr Raw kNegInf = 0xff800000u;
+  static __device__ __forceinline__ uint32_t bits(Raw r) { return r; }
+  static __device__ __forceinline__ Key key_from_bits(uint32_t b, int col) {
+    const int v = int(b);
+    const int s = v >> 31;
+    const long long m = (long long)((v ^ (s & 0x7fffffff)) - s);   // two's complement of the magnitude
+    return (long long)((unsigned long long)m << 32) | (long long)(0xffffffffu - uint32_t(col));
   }
   static __device__ __forceinline__ int key_col(Key k) { return int(0xffffffffu - uint32_t(k & 0xffffffffll)); }
   static __device__ __forceinline__ float key_value(Key k) {
-    const long long v = k >> 32;    // arithmetic shift: the signed magnitude
-    const uint32_t bits = v < 0 ? (0x80000000u | uint32_t(-v)) : uint32_t(v);
-    return __uint_as_float(bits);
+    const long long v = k >> 32;
+    const uint32_t b = v < 0 ? (0x80000000u | uint32_t(-v)) : uint32_t(v);
+    return __uint_as_float(b);
   }
   static constexpr Key kKeyMin = (long long)0x8000000000000000ull;
 };
@@ -161,19 +258,10 @@ __device__ __forceinline__ long long group_max_key(long long x) {
   return x;
 }
 
-// Deterministic block-wide sum (fixed order) of one float per thread.
-template <int NT>
-__device__ __forceinline__ float block_sum(float x, float* scratch /* >= NT/32 floats */) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+__device__ __forceinline__ double warp_sum_d(double x) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  __syncthreads();
-  if (lane == 0) scratch[w] = x;
-  __syncthreads();
-  float t = 0.f;
-#pragma unroll
-  for (int i = 0; i < NT / 32; ++i) t += scratch[i];
-  return t;
+  return x;
 }
 
 }  // namespace moe

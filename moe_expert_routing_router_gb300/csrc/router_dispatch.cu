@@ -4,7 +4,8 @@
 namespace moe {
 
 const void* dispatch_kernel() {
-  return reinterpret_cast<const void*>(&router_persistent_kernel<Bf16, 32, 1, 1, kModeDispatch>);
+  return reinterpret_cast<const void*>(
+      &router_persistent_kernel<Bf16, 32, 1, 1, 1, kModeDispatch, false, kDispatchMinBlocks>);
 }
 
 }  // namespace moe

@@ -3,12 +3,23 @@
 // stable dispatch, as one persistent cooperative kernel with grid barriers
 // between the phases, plus a plain streaming kernel for the backward alone.
 //
+// CTA organisation (kThreads = 320):
+//   warps 0..7  consumers: the per-row forward and backward math
+//   warp  8     producer: streams this CTA's contiguous chunk of logit rows
+//               into a shared-memory ring with bulk asynchronous copies (TMA)
+//   warp  9     dispatcher: stable ranks and the scatter of the dispatch, and
+//               (CTA 0) the E-sized outputs, concurrently with the backward
+//
 // Row layout.  A row of E logits is held by a group of LPR consecutive lanes
 // (LPR in {8, 16, 32}; a warp holds 32/LPR rows).  Lane l of the group owns
 // NV vectors of VW consecutive columns: column(v, l, i) = v*LPR*VW + l*VW + i,
-// so one vector index across the group is one contiguous LPR*VW-column span
-// (coalesced loads and stores).  LPR >= 8 >= k lets lane j of the group own
-// the row's j-th pick.
+// so one vector index across the group is one contiguous LPR*VW-column span.
+// LPR >= 8 >= k lets lane j of the group own the row's j-th pick.
+//
+// Ring.  Stage s of the chunk (rows_per_stage rows) goes to slot s % n_slots.
+// The backward walks the stages in reverse: the last n_slots stages of the
+// forward are still in the ring and are used without reloading; older stages
+// are reloaded into the slot freed by the stage n_slots above them.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -18,9 +29,23 @@
 
 namespace moe {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / kWarp;
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kDispatchWarp = kConsumerWarps + 1;
+constexpr int kThreads = (kConsumerWarps + 2) * kWarp;
+constexpr int kConsumerThreads = kConsumerWarps * kWarp;
+// Warps 0..8 (consumers + producer): the CTA-level syncs from the end of the
+// forward to the start of phase C exclude the dispatch warp, whose in-CTA
+// ranking runs on through the grid barriers and the per-expert scans.
+constexpr int kMainThreads = (kConsumerWarps + 1) * kWarp;
+constexpr int kBarMain = 2;       // named barrier of the main group
+constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
 constexpr int kMaxK = 8;
+constexpr int kMaxSlots = 16;
+constexpr int kNumScalars = 7;
+// Limit of the wait for this CTA's own bulk copies before it exits; it does not
+// follow RouterParams::timeout_ns, which tests shorten.
+constexpr unsigned long long kDrainNs = 1000000000ull;
 
 enum : int { kModeFwd = 1, kModeDispatch = 2, kModeBwd = 4, kModeStep = kModeFwd | kModeDispatch | kModeBwd };
 
@@ -56,9 +81,36 @@ struct RouterParams {
   int G;                       // CTAs in the grid
   int G_stride;
   unsigned long long timeout_ns;
+  unsigned barrier_extra;      // 0; 1 makes every grid barrier unreachable (timeout tests)
+  unsigned long long* trace;   // [G][kTracePoints] phase timestamps (ns), or null
+  // staging ring (staged variants)
+  int rows_per_stage;
+  int n_slots;
 };
 
-constexpr int kNumScalars = 7;
+// Phase boundaries recorded in RouterParams::trace (lane 0 of the warp named).
+enum : int {
+  kTrStart = 0,        // warp 0: kernel entry
+  kTrFirstStage,       // warp 0: first ring stage of the forward has landed
+  kTrFwdRows,          // warp 0: its forward rows are done
+  kTrFwdDone,          // warp 0: per-CTA counts and sums of p published
+  kTrBarrier1,         // warp 0: first grid barrier passed
+  kTrScanDone,         // warp 0: per-expert scans done
+  kTrBarrier2,         // warp 0: second grid barrier passed
+  kTrBwdFirst,         // warp 0: first backward stage available
+  kTrBwdRows,          // warp 0: its backward rows are done
+  kTrDispatchDone,     // warp 9: dispatch (and CTA 0's E-sized outputs) done
+  kTrJoined,           // warp 0: all warps joined
+  kTrEnd,              // warp 0: kernel exit
+  kTracePoints = 16
+};
+
+__device__ __forceinline__ void trace_point(const RouterParams& p, int point) {
+  if (p.trace != nullptr && (threadIdx.x & 31) == 0) {
+    if (point == kTrDispatchDone ? threadIdx.x == kDispatchWarp * kWarp : threadIdx.x == 0)
+      p.trace[blockIdx.x * kTracePoints + point] = global_ns();
+  }
+}
 
 struct BwdParams {
   const void* logits;
@@ -70,14 +122,25 @@ struct BwdParams {
 };
 
 // ---------------------------------------------------------------------------
-// Shared-memory layout of the persistent kernel (ints/floats, 4 bytes each):
-//   s_red  [64]        reduction scratch (also 32 doubles; first, so 8-byte aligned)
-//   s_hist [E]         per-CTA expert counts (phase A)
-//   s_off  [E + 1]     expert offsets (phase C)
-//   s_w    [kWarps*E]  per-warp P partials (phase A), per-warp ranks (phase C)
+// Shared-memory layout of the persistent kernel (byte offsets).
 // ---------------------------------------------------------------------------
-__host__ __device__ inline size_t router_smem_bytes(int E) {
-  return sizeof(int) * (size_t(E) + size_t(E + 1) + size_t(kWarps) * E + 64);
+struct SmemLayout {
+  unsigned red, hist, off, rank, w, bars, ring, total;
+};
+
+__host__ __device__ inline unsigned align_to(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline SmemLayout router_smem_layout(int E, int n_slots, int stage_bytes) {
+  SmemLayout L;
+  L.red = 0;                                                  // 64 ints (32 doubles)
+  L.hist = 256;                                               // E ints
+  L.off = L.hist + 4u * E;                                    // E + 1 ints
+  L.rank = L.off + 4u * (E + 1);                              // E ints
+  L.w = align_to(L.rank + 4u * E, 16);                        // kConsumerWarps * E words
+  L.bars = align_to(L.w + 4u * kConsumerWarps * E, 16);       // 2 * kMaxSlots mbarriers
+  L.ring = align_to(L.bars + 16u * kMaxSlots, 128);
+  L.total = L.ring + unsigned(n_slots) * unsigned(stage_bytes);
+  return L;
 }
 
 // ---------------------------------------------------------------------------
@@ -89,13 +152,14 @@ template <> struct VecT<4> { using T = uint32_t; };
 template <> struct VecT<8> { using T = uint2; };
 template <> struct VecT<16> { using T = uint4; };
 
-template <class Raw, int VW>
+template <class Raw, int VW, bool GLOBAL>
 __device__ __forceinline__ void load_vec(const Raw* src, Raw (&dst)[VW]) {
   constexpr int BYTES = int(sizeof(Raw)) * VW;
   if constexpr (BYTES <= 16) {
     using V = typename VecT<BYTES>::T;
     union { V v; Raw r[VW]; } u;
-    u.v = __ldg(reinterpret_cast<const V*>(src));
+    if constexpr (GLOBAL) u.v = __ldg(reinterpret_cast<const V*>(src));
+    else u.v = *reinterpret_cast<const V*>(src);
 #pragma unroll
     for (int i = 0; i < VW; ++i) dst[i] = u.r[i];
   } else {
@@ -104,7 +168,8 @@ __device__ __forceinline__ void load_vec(const Raw* src, Raw (&dst)[VW]) {
 #pragma unroll
     for (int h = 0; h < VW / H; ++h) {
       union { uint4 v; Raw r[H]; } u;
-      u.v = __ldg(reinterpret_cast<const uint4*>(src + h * H));
+      if constexpr (GLOBAL) u.v = __ldg(reinterpret_cast<const uint4*>(src + h * H));
+      else u.v = *reinterpret_cast<const uint4*>(src + h * H);
 #pragma unroll
       for (int i = 0; i < H; ++i) dst[h * H + i] = u.r[i];
     }
@@ -124,217 +189,267 @@ __device__ __forceinline__ void store_vec_f32(float* dst, const float* src) {
   }
 }
 
-// Loads lane l's EPL elements of row t (zeros for invalid rows / columns).
-template <class DT, int LPR, int VW, int NV>
-__device__ __forceinline__ void load_row(const typename DT::Raw* X, long long t, int E, int l, bool valid,
-                                         typename DT::Raw (&raw)[VW * NV]) {
+template <int LPR, int VW>
+__device__ __forceinline__ int col_of(int v, int l, int i) { return v * LPR * VW + l * VW + i; }
+
+// Lane l's EPL elements of one row.  Columns past E read as -inf (their key is
+// below every logit and their exp is 0, so the math needs no column checks);
+// an invalid row reads as zeros.  `row` points at the row in global memory
+// (GLOBAL) or in a ring stage.
+template <class DT, int LPR, int VW, int NV, bool GLOBAL>
+__device__ __forceinline__ void load_lane(const typename DT::Raw* row, int E, int l, bool valid,
+                                          typename DT::Raw (&raw)[VW * NV]) {
   using Raw = typename DT::Raw;
-  constexpr int SPAN = LPR * VW;
-  const Raw* row = X + t * (long long)E;
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    const int c0 = v * SPAN + l * VW;
+    const int c0 = col_of<LPR, VW>(v, l, 0);
     Raw tmp[VW];
     if (valid && c0 < E) {   // E % VW == 0 for VW > 1: the whole vector is in the row
-      if constexpr (VW == 1) tmp[0] = __ldg(row + c0);
-      else load_vec<Raw, VW>(row + c0, tmp);
+      load_vec<Raw, VW, GLOBAL>(row + c0, tmp);
     } else {
 #pragma unroll
-      for (int i = 0; i < VW; ++i) tmp[i] = Raw(0);
+      for (int i = 0; i < VW; ++i) tmp[i] = valid ? DT::kNegInf : Raw(0);
     }
 #pragma unroll
     for (int i = 0; i < VW; ++i) raw[v * VW + i] = tmp[i];
   }
 }
 
-template <int LPR, int VW>
-__device__ __forceinline__ int col_of(int v, int l, int i) { return v * LPR * VW + l * VW + i; }
+// ---------------------------------------------------------------------------
+// Forward of one row group: top-k on order-preserving keys, softmax against the
+// row max, gates; idx/gate stores, pick counts into s_hist, p into pacc.
+//
+// Top-k.  Each lane keeps the two largest of its keys; k rounds take the group
+// max of the lanes' heads, and the winning lane moves its second key up (a lane
+// that has won twice is exhausted).  The rounds are exact unless some lane has
+// a third key above the k-th pick; a count per lane detects that (rare) case
+// and the row is then redone by exact_topk, which rescans.
+// ---------------------------------------------------------------------------
+template <class DT, int LPR, int VW, int NV, bool GLOBAL>
+__device__ __noinline__ void exact_topk(const typename DT::Raw* row, int E, int k, int l, bool valid,
+                                        typename DT::Key* top_out, typename DT::Key* mine_out) {
+  using Key = typename DT::Key;
+  constexpr int EPL = VW * NV;
+  typename DT::Raw raw[EPL];
+  load_lane<DT, LPR, VW, NV, GLOBAL>(row, E, l, valid, raw);
+  Key key[EPL];
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < VW; ++i) key[v * VW + i] = DT::key_from_bits(DT::bits(raw[v * VW + i]), col_of<LPR, VW>(v, l, i));
+  Key prev = DT::kKeyMin, top = DT::kKeyMin, mine = DT::kKeyMin;
+  for (int j = 0; j < k; ++j) {
+    Key local = DT::kKeyMin;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) local = ((j == 0 || key[i] < prev) && key[i] > local) ? key[i] : local;
+    const Key w = group_max_key<LPR>(local);
+    if (j == 0) top = w;
+    if (l == j) mine = w;
+    prev = w;
+  }
+  *top_out = top;
+  *mine_out = mine;
+}
 
-// ---------------------------------------------------------------------------
-// Phase A: forward over rows [r0, r1).  Writes idx and gate, counts picks into
-// s_hist (shared atomics) and leaves this warp's sums of p in s_w[warp][:].
-// ---------------------------------------------------------------------------
+// Lane-local two largest keys of one row, as a pairwise tree (short dependency
+// chains): merging sorted pairs (h1, l1) and (h2, l2) gives
+// (max(h1, h2), max(min(h1, h2), max(l1, l2))).
 template <class DT, int LPR, int VW, int NV>
-__device__ __forceinline__ void fwd_rows(const RouterParams& p, long long r0, long long r1,
-                                         int* s_hist, float* s_w) {
+__device__ __forceinline__ void lane_top2(const typename DT::Raw (&raw)[VW * NV], int l, typename DT::Key& m1,
+                                          typename DT::Key& m2) {
+  using Key = typename DT::Key;
+  constexpr int EPL = VW * NV;
+  Key hi[EPL], lo[EPL];
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < VW; ++i) {
+      hi[v * VW + i] = DT::key_from_bits(DT::bits(raw[v * VW + i]), col_of<LPR, VW>(v, l, i));
+      lo[v * VW + i] = DT::kKeyMin;
+    }
+#pragma unroll
+  for (int n = EPL; n > 1; n = (n + 1) / 2) {
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const Key a = hi[2 * i], b = hi[2 * i + 1];
+      const Key la = lo[2 * i], lb = lo[2 * i + 1];
+      hi[i] = a > b ? a : b;
+      const Key mn = a < b ? a : b;
+      const Key ml = la > lb ? la : lb;
+      lo[i] = mn > ml ? mn : ml;
+    }
+    if (n & 1) {
+      hi[n / 2] = hi[n - 1];
+      lo[n / 2] = lo[n - 1];
+    }
+  }
+  m1 = hi[0];
+  m2 = lo[0];
+}
+
+template <int N>
+__device__ __forceinline__ float tree_sum(const float (&x)[N]) {
+  float t[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) t[i] = x[i];
+#pragma unroll
+  for (int n = N; n > 1; n = (n + 1) / 2) {
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) t[i] = t[2 * i] + t[2 * i + 1];
+    if (n & 1) t[n / 2] = t[n - 1];
+  }
+  return t[0];
+}
+
+// Forward of NR row groups of one warp at once (independent dependency chains
+// interleave): top-k rounds, softmax against the row max (the first pick),
+// gates; idx/gate stores, pick counts into s_hist, p into pacc.
+template <class DT, int LPR, int VW, int NV, int NR, bool GLOBAL>
+__device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename DT::Raw* const (&row)[NR],
+                                           const long long (&t)[NR], const bool (&valid)[NR], int l, int* s_hist,
+                                           float (&pacc)[VW * NV]) {
   using Raw = typename DT::Raw;
   using Key = typename DT::Key;
   constexpr int EPL = VW * NV;
-  constexpr int RPW = kWarp / LPR;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane / LPR, l = lane % LPR;
-  const int E = p.E, k = p.k;
-  const Raw* X = static_cast<const Raw*>(p.logits);
+  const int k = p.k;
 
-  float pacc[EPL];
+  Raw raw[NR][EPL];
+  Key m1[NR], m2[NR], top[NR], mine[NR], w[NR];
+  int wins[NR];
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) pacc[i] = 0.f;
-
-  for (long long base = r0 + (long long)warp * RPW; base < r1; base += (long long)kWarps * RPW) {
-    const long long t = base + g;
-    const bool valid = t < r1;
-    Raw raw[EPL];
-    load_row<DT, LPR, VW, NV>(X, t, E, l, valid, raw);
-
-    Key key[EPL];
+  for (int r = 0; r < NR; ++r) {
+    load_lane<DT, LPR, VW, NV, GLOBAL>(row[r], p.E, l, valid[r], raw[r]);
+    lane_top2<DT, LPR, VW, NV>(raw[r], l, m1[r], m2[r]);
+    top[r] = mine[r] = w[r] = DT::kKeyMin;
+    wins[r] = 0;
+  }
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
 #pragma unroll
-    for (int v = 0; v < NV; ++v)
+    for (int r = 0; r < NR; ++r) w[r] = group_max_key<LPR>(m1[r]);
 #pragma unroll
-      for (int i = 0; i < VW; ++i) {
-        const int c = col_of<LPR, VW>(v, l, i);
-        key[v * VW + i] = c < E ? DT::key(raw[v * VW + i], c) : DT::kKeyMin;
-      }
-
-    // Top-k: k rounds of "largest key below the previous winner".
-    Key win[kMaxK];
-    Key prev = DT::kKeyMin;
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      win[j] = DT::kKeyMin;
-      if (j < k) {
-        Key local = DT::kKeyMin;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-          const bool below = (j == 0) || (key[i] < prev);
-          local = (below && key[i] > local) ? key[i] : local;
-        }
-        win[j] = group_max_key<LPR>(local);
-        prev = win[j];
-      }
+    for (int r = 0; r < NR; ++r) {
+      top[r] = j == 0 ? w[r] : top[r];
+      mine[r] = l == j ? w[r] : mine[r];
+      const bool won = m1[r] == w[r];
+      m1[r] = won ? m2[r] : m1[r];
+      m2[r] = won ? DT::kKeyMin : m2[r];
+      wins[r] += won ? 1 : 0;
     }
-
-    // Softmax against the row max (= the value of the first pick).
-    const float mL = DT::key_value(win[0]) * kLog2e;
-    float e[EPL];
-    float s = 0.f;
+  }
+  // A lane that won twice ran out of cached keys: the picks are exact unless
+  // it holds a third key above the k-th pick w (then the row is redone).
+  bool twice = false;
 #pragma unroll
-    for (int v = 0; v < NV; ++v)
+  for (int r = 0; r < NR; ++r) twice = twice || wins[r] >= 2;
+  if (__any_sync(0xffffffffu, twice)) {
 #pragma unroll
-      for (int i = 0; i < VW; ++i) {
-        const int c = col_of<LPR, VW>(v, l, i);
-        const float x = DT::to_float(raw[v * VW + i]);
-        e[v * VW + i] = c < E ? ex2_approx(fmaf(x, kLog2e, -mL)) : 0.f;
-        s += e[v * VW + i];
-      }
-    s = group_sum<LPR>(s);
-    const float inv_s = valid ? 1.f / s : 0.f;
+    for (int r = 0; r < NR; ++r) {
+      int above = 0;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) pacc[i] = fmaf(e[i], inv_s, pacc[i]);
-
-    // Lane j of the group owns pick j.
-    Key mine = DT::kKeyMin;
+      for (int v = 0; v < NV; ++v)
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) mine = (j == l) ? win[j] : mine;
-    const bool owner = l < k;
-    const float ej = owner ? ex2_approx(fmaf(DT::key_value(mine), kLog2e, -mL)) : 0.f;
-    const float denom = p.renorm ? group_sum<LPR>(ej) : s;
-    if (valid && owner) {
-      const int col = DT::key_col(mine);
-      const long long a = t * k + l;
-      p.idx[a] = col;
-      p.gate[a] = ej / denom;
-      atomicAdd(&s_hist[col], 1);
+        for (int i = 0; i < VW; ++i)
+          above += DT::key_from_bits(DT::bits(raw[r][v * VW + i]), col_of<LPR, VW>(v, l, i)) > w[r] ? 1 : 0;
+      if (__any_sync(0xffffffffu, above > wins[r]))
+        exact_topk<DT, LPR, VW, NV, GLOBAL>(row[r], p.E, k, l, valid[r], &top[r], &mine[r]);
     }
   }
 
-  // Sum the row groups of the warp, then group 0 stores the warp's partials.
 #pragma unroll
-  for (int i = 0; i < EPL; ++i)
+  for (int r = 0; r < NR; ++r) {
+    const float mL = DT::key_value(top[r]) * kLog2e;
+    float e[EPL];
 #pragma unroll
-    for (int off = LPR; off < kWarp; off <<= 1) pacc[i] += __shfl_xor_sync(0xffffffffu, pacc[i], off);
-  if (g == 0) {
+    for (int i = 0; i < EPL; ++i) e[i] = ex2_approx(fmaf(__uint_as_float(DT::bits(raw[r][i])), kLog2e, -mL));
+    const float s = group_sum<LPR>(tree_sum(e));
+    const float inv_s = valid[r] ? rcp_approx(s) : 0.f;
 #pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-      for (int i = 0; i < VW; ++i) {
-        const int c = col_of<LPR, VW>(v, l, i);
-        if (c < E) s_w[warp * E + c] = pacc[v * VW + i];
-      }
+    for (int i = 0; i < EPL; ++i) pacc[i] = fmaf(e[i], inv_s, pacc[i]);
+    const bool owner = l < k;
+    const float ej = owner ? ex2_approx(fmaf(DT::key_value(mine[r]), kLog2e, -mL)) : 0.f;
+    const float denom = p.renorm ? group_sum<LPR>(ej) : s;
+    if (valid[r] && owner) {
+      const int col = DT::key_col(mine[r]);
+      const long long a = t[r] * k + l;
+      p.idx[a] = col;
+      p.gate[a] = ej * rcp_approx(denom);
+      atomicAdd(&s_hist[col], 1);
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Backward over rows [r0, r1) with row groups striding by `stride` rows:
+// Backward of one row group:
 //   dlogits[t,j] = coef * p[t,j] * (f[j] - sum_i p[t,i] f[i])
-// `f` is read through L2 (it may have been written earlier in this launch).
 // ---------------------------------------------------------------------------
 template <class DT, int LPR, int VW, int NV>
-__device__ __forceinline__ void bwd_rows(const void* logits, int E, const float* f, float coef, float* dlogits,
-                                         long long first, long long r1, long long stride) {
-  using Raw = typename DT::Raw;
+__device__ __forceinline__ void bwd_group(const typename DT::Raw (&raw)[VW * NV], const float (&fr)[VW * NV], long long t,
+                                          bool valid, int l, int E, float coef, float* dlogits) {
   constexpr int EPL = VW * NV;
-  const int lane = threadIdx.x & 31;
-  const int g = lane / LPR, l = lane % LPR;
-  const Raw* X = static_cast<const Raw*>(logits);
+  float x[EPL];
+  float m = -3.402823466e38f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    x[i] = __uint_as_float(DT::bits(raw[i]));
+    m = fmaxf(m, x[i]);
+  }
+  m = group_max<LPR>(m);
+  const float mL = m * kLog2e;
+  float e[EPL];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    e[i] = ex2_approx(fmaf(x[i], kLog2e, -mL));
+    s += e[i];
+  }
+  s = group_sum<LPR>(s);
+  const float inv_s = rcp_approx(s);
+  float dot = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    e[i] *= inv_s;                       // p
+    dot = fmaf(e[i], fr[i], dot);
+  }
+  dot = group_sum<LPR>(dot);
+  if (valid) {
+    float* out = dlogits + t * (long long)E;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int c0 = col_of<LPR, VW>(v, l, 0);
+      if (c0 < E) {
+        float d[VW];
+#pragma unroll
+        for (int i = 0; i < VW; ++i) d[i] = coef * e[v * VW + i] * (fr[v * VW + i] - dot);
+        store_vec_f32<VW>(out + c0, d);
+      }
+    }
+  }
+}
 
-  float fr[EPL];
+// Lane l's f values (zero past E) from a shared-memory copy of f.
+template <int LPR, int VW, int NV>
+__device__ __forceinline__ void load_f(const float* s_f, int E, int l, float (&fr)[VW * NV]) {
 #pragma unroll
   for (int v = 0; v < NV; ++v)
 #pragma unroll
     for (int i = 0; i < VW; ++i) {
       const int c = col_of<LPR, VW>(v, l, i);
-      fr[v * VW + i] = c < E ? __ldcg(f + c) : 0.f;
+      fr[v * VW + i] = c < E ? s_f[c] : 0.f;
     }
+}
 
-  for (long long base = first; base < r1; base += stride) {
-    const long long t = base + g;
-    const bool valid = t < r1;
-    Raw raw[EPL];
-    load_row<DT, LPR, VW, NV>(X, t, E, l, valid, raw);
-    float x[EPL];
-    float m = -3.402823466e38f;
-#pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-      for (int i = 0; i < VW; ++i) {
-        const int c = col_of<LPR, VW>(v, l, i);
-        x[v * VW + i] = DT::to_float(raw[v * VW + i]);
-        if (c < E) m = fmaxf(m, x[v * VW + i]);
-      }
-    m = group_max<LPR>(m);
-    const float mL = m * kLog2e;
-    float e[EPL];
-    float s = 0.f;
-#pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-      for (int i = 0; i < VW; ++i) {
-        const int c = col_of<LPR, VW>(v, l, i);
-        e[v * VW + i] = c < E ? ex2_approx(fmaf(x[v * VW + i], kLog2e, -mL)) : 0.f;
-        s += e[v * VW + i];
-      }
-    s = group_sum<LPR>(s);
-    const float inv_s = 1.f / s;
-    float dot = 0.f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      e[i] *= inv_s;                       // p
-      dot = fmaf(e[i], fr[i], dot);
-    }
-    dot = group_sum<LPR>(dot);
-    if (valid) {
-      float* out = dlogits + t * (long long)E;
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const int c0 = col_of<LPR, VW>(v, l, 0);
-        if (c0 < E) {
-          float d[VW];
-#pragma unroll
-          for (int i = 0; i < VW; ++i) d[i] = coef * e[v * VW + i] * (fr[v * VW + i] - dot);
-          store_vec_f32<VW>(out + c0, d);
-        }
-      }
-    }
-  }
+__device__ __forceinline__ void sync_main() {
+  asm volatile("bar.sync %0, %1;" :: "n"(kBarMain), "n"(kMainThreads) : "memory");
 }
 
 // ---------------------------------------------------------------------------
-// Block-wide helpers (kThreads threads).
+// Exclusive scan of n ints in place over the main group (n <= 4 * kMainThreads);
+// returns the total.  All kMainThreads threads must call it.
 // ---------------------------------------------------------------------------
-
-// Exclusive scan of n ints in place (n <= 4 * kThreads); returns the total.
 __device__ __forceinline__ int block_exclusive_scan(int* data, int n, int* s_red, bool global_src) {
   constexpr int PER = 4;
+  constexpr int NW = kMainThreads / kWarp;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int v[PER];
   int sum = 0;
@@ -350,12 +465,12 @@ __device__ __forceinline__ int block_exclusive_scan(int* data, int n, int* s_red
     const int y = __shfl_up_sync(0xffffffffu, incl, off);
     if (lane >= off) incl += y;
   }
-  __syncthreads();
+  sync_main();
   if (lane == 31) s_red[warp] = incl;
-  __syncthreads();
+  sync_main();
   int warp_base = 0, total = 0;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < NW; ++w) {
     const int t = s_red[w];
     warp_base += w < warp ? t : 0;
     total += t;
@@ -367,100 +482,266 @@ __device__ __forceinline__ int block_exclusive_scan(int* data, int n, int* s_red
     if (j < n) data[j] = run;
     run += v[i];
   }
-  __syncthreads();
+  sync_main();
   return total;
 }
 
-__device__ __forceinline__ double block_sum_d(double x, double* s_red) {
+// Fixed-order sum of one float per thread over the main group (all call it).
+__device__ __forceinline__ float block_sum_f(float x, float* s_red) {
+  constexpr int NW = kMainThreads / kWarp;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  __syncthreads();
+  sync_main();
   if (lane == 0) s_red[warp] = x;
-  __syncthreads();
-  double t = 0.0;
+  sync_main();
+  float t = 0.f;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) t += s_red[w];
-  __syncthreads();
-  return t;
-}
-
-__device__ __forceinline__ int block_max_i(int x, int* s_red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  x = __reduce_max_sync(0xffffffffu, x);
-  __syncthreads();
-  if (lane == 0) s_red[warp] = x;
-  __syncthreads();
-  int t = s_red[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) t = max(t, s_red[w]);
-  __syncthreads();
-  return t;
-}
-
-__device__ __forceinline__ int block_min_i(int x, int* s_red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  x = __reduce_min_sync(0xffffffffu, x);
-  __syncthreads();
-  if (lane == 0) s_red[warp] = x;
-  __syncthreads();
-  int t = s_red[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) t = min(t, s_red[w]);
-  __syncthreads();
+  for (int w = 0; w < NW; ++w) t += s_red[w];
+  sync_main();
   return t;
 }
 
 // ---------------------------------------------------------------------------
-// Phase C dispatch: stable ranks of this CTA's assignments [a0, a1).
-// tile_hist[e][cta] holds the exclusive prefix of expert e's count over the
-// CTAs before this one; s_off the expert offsets.
+// Dispatch.  The stable rank of assignment a = t*k + j among the assignments
+// to its expert e is  (count of e in the CTAs before this one)  +  (count of e
+// among this CTA's assignments before a).  One warp walks this CTA's
+// assignments in order, 32 at a time: lanes holding the same expert are found
+// with one ballot per bit of e, and a per-expert running count in shared
+// memory gives the in-CTA rank.  With the rows streamed through the ring this
+// runs during the forward, a stage behind the consumer warps, and parks the
+// in-CTA ranks in slot[]; after the global prefix is known a sync-free pass
+// turns them into final ranks and writes perm and slot.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void dispatch_scatter(const RouterParams& p, const int32_t* idx_src, int cta,
-                                                 long long a0, long long a1, const int* s_off, int* s_w) {
-  const int E = p.E, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const long long n = a1 - a0;
-  const long long w_lo = a0 + n * warp / kWarps, w_hi = a0 + n * (warp + 1) / kWarps;
-  int* wh = s_w + warp * E;
-  for (int e = lane; e < E; e += kWarp) wh[e] = 0;
-  __syncwarp();
-  for (long long a = w_lo + lane; a < w_hi; a += kWarp) {
-    const int e = min(max(__ldcg(idx_src + a), 0), E - 1);
-    atomicAdd(&wh[e], 1);
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += kThreads) {
-    int run = __ldcg(p.tile_hist + (size_t)e * p.G_stride + cta);
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const int c = s_w[w * E + e];
-      s_w[w * E + e] = run;
-      run += c;
-    }
-  }
-  __syncthreads();
+constexpr int kDispChunks = 8;
+
+// How idx is read: a read-only input, data this CTA is writing during the
+// forward (volatile loads, coherent within the SM), or data published before a
+// grid barrier (L2 loads).
+enum : int { kLoadInput = 0, kLoadOwn = 1, kLoadPublished = 2 };
+
+// In-CTA ranks of assignments [a_lo, a_hi), written to out[a].
+template <int LOAD>
+__device__ __forceinline__ void local_ranks(const int32_t* idx_src, long long a_lo, long long a_hi, int E, int* rank,
+                                            int32_t* out) {
+  const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
-  for (long long base = w_lo; base < w_hi; base += kWarp) {
-    const long long a = base + lane;
-    const bool act = a < w_hi;
-    const unsigned mask = __ballot_sync(0xffffffffu, act);
-    int e = 0, r = 0, lower = 0;
-    unsigned peers = 0;
-    if (act) {
-      e = min(max(__ldcg(idx_src + a), 0), E - 1);
-      peers = __match_any_sync(mask, e);
-      lower = __popc(peers & lt);
-      r = wh[e] + lower;
+  for (long long base = a_lo; base < a_hi; base += kDispChunks * kWarp) {
+    int e_[kDispChunks], r_[kDispChunks];
+#pragma unroll
+    for (int j = 0; j < kDispChunks; ++j) {
+      const long long a = base + j * kWarp + lane;
+      int v = 0;
+      if (a < a_hi) {
+        if constexpr (LOAD == kLoadOwn) v = *reinterpret_cast<const volatile int32_t*>(idx_src + a);
+        else if constexpr (LOAD == kLoadPublished) v = __ldcg(idx_src + a);
+        else v = __ldg(idx_src + a);
+      }
+      e_[j] = min(max(v, 0), E - 1);
     }
-    __syncwarp();
-    if (act && lower == 0) wh[e] += __popc(peers);
-    __syncwarp();
-    if (act) {
-      p.perm[s_off[e] + r] = int(a);
+#pragma unroll
+    for (int j = 0; j < kDispChunks; ++j) {
+      r_[j] = 0;
+      if (base + j * kWarp >= a_hi) continue;             // warp-uniform
+      const bool act = base + j * kWarp + lane < a_hi;
+      const int e = e_[j];
+      unsigned peers = __ballot_sync(0xffffffffu, act);  // lanes holding the same expert
+      for (int bit = 0; (1 << bit) < E; ++bit) {
+        const unsigned ones = __ballot_sync(0xffffffffu, (e >> bit) & 1);
+        peers &= ((e >> bit) & 1) ? ones : ~ones;
+      }
+      const int lower = __popc(peers & lt);
+      r_[j] = act ? rank[e] + lower : 0;
+      __syncwarp();
+      if (act && lower == 0) rank[e] += __popc(peers);
+      __syncwarp();
+    }
+#pragma unroll
+    for (int j = 0; j < kDispChunks; ++j) {
+      const long long a = base + j * kWarp + lane;
+      if (a < a_hi) out[a] = r_[j];
+    }
+  }
+}
+
+// Final ranks from the parked in-CTA ranks: r = base[e] + local; perm and slot.
+__device__ __forceinline__ void dispatch_fixup(const RouterParams& p, const int32_t* idx_src, long long a0, long long a1,
+                                               const int* off, const int* base) {
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+  for (long long b = a0; b < a1; b += 4 * kWarp) {
+    int e_[4], l_[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long a = b + j * kWarp + lane;
+      e_[j] = a < a1 ? min(max(__ldcg(idx_src + a), 0), E - 1) : 0;
+      l_[j] = a < a1 ? __ldcg(p.slot + a) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long a = b + j * kWarp + lane;
+      const int e = e_[j];
+      const int r = base[e] + l_[j];
+      if (a < a1 && r >= 0 && r < off[e + 1] - off[e]) {   // always true for consistent ranks
+        p.perm[off[e] + r] = int(a);
+        p.slot[a] = r < p.C ? r : -1;
+      }
+    }
+  }
+}
+
+// Final ranks directly (rank[e] starts at the CTA's prefix), for the variants
+// that read rows straight from global memory: used after the global prefix.
+__device__ __forceinline__ void dispatch_direct(const RouterParams& p, const int32_t* idx_src, long long a0, long long a1,
+                                                const int* off, int* rank) {
+  const int E = p.E;
+  const int lane = threadIdx.x & 31;
+  local_ranks<kLoadPublished>(idx_src, a0, a1, E, rank, p.slot);   // slot[a] = final rank
+  __syncwarp();
+  for (long long a = a0 + lane; a < a1; a += kWarp) {
+    const int e = min(max(__ldcg(idx_src + a), 0), E - 1);
+    const int r = p.slot[a];
+    if (r >= 0 && r < off[e + 1] - off[e]) {                // always true for consistent ranks
+      p.perm[off[e] + r] = int(a);
       p.slot[a] = r < p.C ? r : -1;
     }
   }
 }
+
+// Exclusive scan of counts[0..E) into off[0..E] (shared or global) by one warp.
+__device__ __forceinline__ void warp_offsets(const int32_t* counts, int E, int* off) {
+  const int lane = threadIdx.x & 31;
+  const int per = (E + 31) / 32;
+  const int lo = min(lane * per, E), hi = min(lo + per, E);
+  int sum = 0;
+  for (int e = lo; e < hi; ++e) sum += __ldcg(counts + e);
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int run = incl - sum;
+  for (int e = lo; e < hi; ++e) {
+    off[e] = run;
+    run += __ldcg(counts + e);
+  }
+  if (lane == 31) off[E] = incl;
+  __syncwarp();
+}
+
+// The E-sized outputs, by one warp of CTA 0.
+template <int MODE>
+__device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32_t* counts) {
+  const int lane = threadIdx.x & 31;
+  const int E = p.E, k = p.k;
+  if constexpr ((MODE & kModeDispatch) != 0) {
+    warp_offsets(counts, E, p.offsets);
+    int dropped = 0;
+    for (int e = lane; e < E; e += kWarp) {
+      const int c = __ldcg(counts + e);
+      p.kept[e] = min(c, p.C);
+      dropped += max(c - p.C, 0);
+    }
+    dropped = __reduce_add_sync(0xffffffffu, dropped);
+    if (lane == 0) *p.n_dropped = dropped;
+  }
+  if constexpr ((MODE & kModeFwd) != 0) {
+    const double mean = double(p.T) * k / E;
+    double fp = 0.0, dev = 0.0;
+    int cmax = 0, cmin = 0x7fffffff;
+    for (int e = lane; e < E; e += kWarp) {
+      const int c = __ldcg(p.counts + e);
+      fp += double(__ldcg(p.f + e)) * double(__ldcg(p.P + e));
+      dev += (double(c) - mean) * (double(c) - mean);
+      cmax = max(cmax, c);
+      cmin = min(cmin, c);
+    }
+    fp = warp_sum_d(fp);
+    dev = warp_sum_d(dev);
+    cmax = __reduce_max_sync(0xffffffffu, cmax);
+    cmin = __reduce_min_sync(0xffffffffu, cmin);
+    const int R = p.n_ranks;
+    double rdev = 0.0;
+    int rmax = 0;
+    if (R > 0) {
+      const int per = E / R;
+      const double rmean = double(p.T) * k / R;
+      for (int r = lane; r < R; r += kWarp) {
+        int load = 0;
+        for (int j = 0; j < per; ++j) load += __ldcg(p.counts + r * per + j);
+        p.rank_load[r] = load;
+        rdev += (double(load) - rmean) * (double(load) - rmean);
+        rmax = max(rmax, load);
+      }
+      rdev = warp_sum_d(rdev);
+      rmax = __reduce_max_sync(0xffffffffu, rmax);
+    }
+    if (lane == 0) {
+      const double balance = double(E) * fp;
+      p.scalars[0] = float(double(p.alpha) * balance);
+      p.scalars[1] = float(balance);
+      p.scalars[2] = float(sqrt(dev / E) / mean);
+      p.scalars[3] = float(cmax / mean);
+      p.scalars[4] = float(cmin / mean);
+      if (R > 0) {
+        const double rmean = double(p.T) * k / R;
+        p.scalars[5] = float(sqrt(rdev / R) / rmean);
+        p.scalars[6] = float(rmax / rmean);
+      } else {
+        p.scalars[5] = 0.f;
+        p.scalars[6] = 0.f;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The dispatch warp after the forward: waits (bounded) until grid barrier 2 has
+// passed for this CTA, then turns the in-CTA ranks into final positions and,
+// in CTA 0 when the producer warp is busy with refills, writes the E-sized
+// outputs.
+// ---------------------------------------------------------------------------
+template <int MODE, bool STAGED>
+__device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta, long long a0, long long a1, int* s_off,
+                                                 int* s_rank, int* s_phase, const int32_t* counts, bool finalize_here,
+                                                 bool ranked) {
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+  int ph = 0;
+  uint64_t t0 = 0;
+  for (unsigned spin = 0; (ph = *reinterpret_cast<volatile int*>(s_phase)) == 0; ++spin) {
+    if ((spin & 15u) == 15u) {
+      const uint64_t now = global_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > p.timeout_ns) break;
+    }
+    __nanosleep(64);
+  }
+  if (ph != 1 || !ranked) return;                        // an error (or a lost signal): write nothing
+  __threadfence();
+  if constexpr ((MODE & kModeDispatch) != 0) {
+    warp_offsets(counts, E, s_off);
+    for (int e = lane; e < E; e += kWarp) s_rank[e] = __ldcg(p.tile_hist + (size_t)e * p.G_stride + cta);
+    __syncwarp();
+    constexpr bool kRanked = STAGED || (MODE & kModeFwd) == 0;   // in-CTA ranks already parked in slot[]
+    if constexpr (kRanked) dispatch_fixup(p, (MODE & kModeFwd) ? p.idx : p.idx_in, a0, a1, s_off, s_rank);
+    else dispatch_direct(p, p.idx, a0, a1, s_off, s_rank);
+  }
+  if (finalize_here) finalize_warp<MODE>(p, counts);
+  trace_point(p, kTrDispatchDone);
+}
+
+// ---------------------------------------------------------------------------
+// Ring bookkeeping.  With n stages and NS slots, slot q holds the stages
+// s = q (mod NS); count_a(q) of them pass through it in the forward, whose fill
+// of stage s is the slot's full-barrier completion s / NS.  In the backward the
+// stage rel >= 1 slot-rounds below the slot's last stage is its refill rel - 1:
+// full-barrier completion count_a(q) + rel - 1, issued after the consumption
+// of the previous occupant, empty-barrier completion count_a(q) + rel - 1.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int ring_count_a(int q, int n, int NS) { return q < n ? (n - 1 - q) / NS + 1 : 0; }
+__device__ __forceinline__ int ring_last(int q, int n, int NS) { return q + (ring_count_a(q, n, NS) - 1) * NS; }
 
 // ---------------------------------------------------------------------------
 // The persistent kernel.  MODE selects the phases:
@@ -468,154 +749,333 @@ __device__ __forceinline__ void dispatch_scatter(const RouterParams& p, const in
 //   B: per-expert totals, exclusive prefixes over CTAs, f and P
 //   C: dispatch scatter (kModeDispatch), backward (kModeBwd), and the E-sized
 //      outputs written by CTA 0 (scalars, rank loads, offsets, kept, drops).
+// STAGED: logit rows are 16-byte multiples and the producer warp streams them
+// through the ring; otherwise the consumers read global memory directly.
 // Launched cooperatively with p.G CTAs of kThreads threads.
 // ---------------------------------------------------------------------------
-template <class DT, int LPR, int VW, int NV, int MODE>
-__global__ void __launch_bounds__(kThreads) router_persistent_kernel(const RouterParams p) {
-  extern __shared__ int smem[];
+template <class DT, int LPR, int VW, int NV, int NR, int MODE, bool STAGED, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const RouterParams p) {
+  using Raw = typename DT::Raw;
+  constexpr int EPL = VW * NV;
+  constexpr int RPW = kWarp / LPR;
+  extern __shared__ __align__(128) unsigned char smem[];
   const int E = p.E, k = p.k, G = p.G, cta = blockIdx.x, tid = threadIdx.x;
-  int* s_red = smem;
-  int* s_hist = s_red + 64;
-  int* s_off = s_hist + E;
-  int* s_w = s_off + E + 1;
-  float* s_wf = reinterpret_cast<float*>(s_w);
-  double* s_red_d = reinterpret_cast<double*>(s_red);
+  const int lane = tid & 31, warp = tid >> 5;
+  const int g = lane / LPR, l = lane % LPR;
+  const int S = STAGED ? p.rows_per_stage : 1;
+  const int NS = STAGED ? p.n_slots : 1;
+  const int stage_elems = S * E;
+  const SmemLayout L = router_smem_layout(E, STAGED ? NS : 0, stage_elems * int(sizeof(Raw)));
+  int* s_red = reinterpret_cast<int*>(smem + L.red);
+  int* s_prog = s_red + 40;       // stages finished per consumer warp (forward)
+  int* s_phase = s_red + 48;      // 1 once grid barrier 2 has passed, -1 after an error
+  int* s_hist = reinterpret_cast<int*>(smem + L.hist);
+  int* s_off = reinterpret_cast<int*>(smem + L.off);
+  int* s_rank = reinterpret_cast<int*>(smem + L.rank);
+  float* s_wf = reinterpret_cast<float*>(smem + L.w);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + kMaxSlots;
+  Raw* ring = reinterpret_cast<Raw*>(smem + L.ring);
 
   const long long r0 = p.T * cta / G, r1 = p.T * (cta + 1) / G;
   const long long a0 = r0 * k, a1 = r1 * k;
+  const int n_rows = int(r1 - r0);
+  const int n_st = STAGED ? (n_rows + S - 1) / S : 0;
+  const Raw* X = static_cast<const Raw*>(p.logits);
   int32_t* counts_dst = (MODE & kModeFwd) ? p.counts : p.counts_ws;
+  const bool is_producer = STAGED && warp == kProducerWarp && lane == 0;
+  int fills[kMaxSlots];          // copies issued per slot (producer thread), drained on an error exit
+  bool ranked = true;            // dispatch warp: every in-CTA rank of this CTA has been written
+#pragma unroll
+  for (int q = 0; q < kMaxSlots; ++q) fills[q] = 0;
 
-  // ---- phase A
-  for (int e = tid; e < E; e += kThreads) s_hist[e] = 0;
-  for (int i = tid; i < kWarps * E; i += kThreads) s_w[i] = 0;
-  __syncthreads();
-  if constexpr ((MODE & kModeFwd) != 0) {
-    fwd_rows<DT, LPR, VW, NV>(p, r0, r1, s_hist, s_wf);
-  } else {
-    for (long long a = a0 + tid; a < a1; a += kThreads) {
-      const int e = min(max(__ldg(p.idx_in + a), 0), E - 1);
-      atomicAdd(&s_hist[e], 1);
+  trace_point(p, kTrStart);
+  for (int e = tid; e < E; e += kThreads) {
+    s_hist[e] = 0;
+    s_rank[e] = 0;
+  }
+  if (tid < kConsumerWarps) s_prog[tid] = 0;
+  if (tid == 0) *s_phase = 0;
+  if (STAGED && tid == 0) {
+    for (int q = 0; q < NS; ++q) {
+      mbar_init(&full[q], 1);
+      mbar_init(&empty[q], kConsumerWarps);
     }
+    mbar_fence_init();
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kThreads) {
+
+  // ---- phase A
+  if constexpr ((MODE & kModeFwd) != 0) {
+    if (warp < kConsumerWarps) {
+      float pacc[EPL];
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) pacc[i] = 0.f;
+      if constexpr (STAGED) {
+        for (int s = 0; s < n_st; ++s) {
+          const int q = s % NS;
+          if (!mbar_wait(&full[q], (s / NS) & 1, p.timeout_ns)) {
+            atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+            break;
+          }
+          if (s == 0) trace_point(p, kTrFirstStage);
+          const Raw* st = ring + q * stage_elems;
+          const int rows_here = min(S, n_rows - s * S);
+          for (int sg = warp; sg * NR * RPW < rows_here; sg += kConsumerWarps) {
+            const Raw* rows[NR];
+            long long ts[NR];
+            bool valids[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+              const int ri = (sg * NR + r) * RPW + g;
+              valids[r] = ri < rows_here;
+              rows[r] = st + (valids[r] ? ri : 0) * E;
+              ts[r] = r0 + (long long)s * S + ri;
+            }
+            fwd_groups<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&empty[q]);
+            if constexpr ((MODE & kModeDispatch) != 0) {
+              __threadfence_block();                        // idx stores before the progress mark
+              *reinterpret_cast<volatile int*>(&s_prog[warp]) = s + 1;
+            }
+          }
+        }
+      } else {
+        for (long long base = r0 + (long long)warp * NR * RPW; base < r1; base += (long long)kConsumerWarps * NR * RPW) {
+          const Raw* rows[NR];
+          long long ts[NR];
+          bool valids[NR];
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            ts[r] = base + r * RPW + g;
+            valids[r] = ts[r] < r1;
+            rows[r] = X + (valids[r] ? ts[r] : r0) * (long long)E;
+          }
+          fwd_groups<DT, LPR, VW, NV, NR, true>(p, rows, ts, valids, l, s_hist, pacc);
+        }
+      }
+      trace_point(p, kTrFwdRows);
+      // Sum the row groups of the warp; group 0 stores the warp's partials.
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+#pragma unroll
+        for (int off = LPR; off < kWarp; off <<= 1) pacc[i] += __shfl_xor_sync(0xffffffffu, pacc[i], off);
+      if (g == 0) {
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int i = 0; i < VW; ++i) {
+            const int c = col_of<LPR, VW>(v, l, i);
+            if (c < E) s_wf[warp * E + c] = pacc[v * VW + i];
+          }
+      }
+    } else if (is_producer) {
+      const uint64_t pol = l2_policy_evict_last();
+      const uint32_t row_bytes = uint32_t(E) * uint32_t(sizeof(Raw));
+      for (int s = 0; s < n_st; ++s) {
+        const int q = s % NS;
+        if (s >= NS && !mbar_wait(&empty[q], ((s / NS) - 1) & 1, p.timeout_ns)) {
+          atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+          break;
+        }
+        const int rows_here = min(S, n_rows - s * S);
+        const uint32_t bytes = uint32_t(rows_here) * row_bytes;
+        mbar_arrive_expect_tx(&full[q], bytes);
+        bulk_g2s(ring + q * stage_elems, X + (r0 + (long long)s * S) * E, bytes, &full[q], pol);
+        ++fills[q];
+      }
+    } else if (STAGED && (MODE & kModeDispatch) != 0 && warp == kDispatchWarp) {
+      // in-CTA dispatch ranks, one stage behind the consumer warps
+      ranked = false;
+      for (int s = 0; s < n_st; ++s) {
+        bool ready = false;
+        uint64_t t0 = 0;
+        for (unsigned spin = 0; !ready; ++spin) {
+          const int pr = lane < kConsumerWarps ? *reinterpret_cast<volatile int*>(&s_prog[lane]) : s + 1;
+          ready = __all_sync(0xffffffffu, pr > s);
+          if (!ready) {
+            __nanosleep(256);                     // leave the issue slots to the consumer warps
+            if ((spin & 15u) == 15u) {
+              const uint64_t now = global_ns();
+              if (t0 == 0) t0 = now;
+              else if (now - t0 > p.timeout_ns) break;
+            }
+          }
+        }
+        if (!ready) {
+          if (lane == 0) atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+          break;
+        }
+        __threadfence_block();
+        const long long lo = (r0 + (long long)s * S) * k;
+        const long long hi = min(r0 + (long long)(s + 1) * S, r1) * k;
+        local_ranks<kLoadOwn>(p.idx, lo, hi, E, s_rank, p.slot);
+        if (s == n_st - 1) ranked = true;
+      }
+      if (n_st == 0) ranked = true;
+    }
+  } else {
+    if (warp == kDispatchWarp) {
+      local_ranks<kLoadInput>(p.idx_in, a0, a1, E, s_rank, p.slot);
+    } else {
+      for (long long a = a0 + tid; a < a1; a += kMainThreads) {
+        const int e = min(max(__ldg(p.idx_in + a), 0), E - 1);
+        atomicAdd(&s_hist[e], 1);
+      }
+    }
+  }
+  // The producer warp is idle in phase C unless it refills the ring for the
+  // backward; CTA 0's E-sized outputs go to whichever of warps 8 and 9 is idle.
+  const bool refills = STAGED && (MODE & kModeBwd) != 0 && n_st > NS;
+  if (warp == kDispatchWarp) {
+    dispatch_phase_c<MODE, STAGED>(p, cta, a0, a1, s_off, s_rank, s_phase, counts_dst, cta == 0 && refills, ranked);
+    return;
+  }
+  sync_main();
+  for (int e = tid; e < E; e += kMainThreads) {
     p.tile_hist[(size_t)e * p.G_stride + cta] = s_hist[e];
     if constexpr ((MODE & kModeFwd) != 0) {
       float t = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) t += s_wf[w * E + e];
+      for (int w = 0; w < kConsumerWarps; ++w) t += s_wf[w * E + e];
       p.P_part[(size_t)e * p.G_stride + cta] = t;
     }
   }
-  if (!grid_barrier(p.ctrl, G, p.timeout_ns, s_red + 63)) return;
+  trace_point(p, kTrFwdDone);
+  if (!grid_barrier(p.ctrl, G, p.barrier_extra, p.timeout_ns, s_red + 63, kBarMain, kMainThreads)) {
+    if (tid == 0) *reinterpret_cast<volatile int*>(s_phase) = -1;
+    if (is_producer)   // let every issued copy land before the CTA exits
+      for (int q = 0; q < NS; ++q)
+        if (fills[q] > 0) mbar_wait(&full[q], (fills[q] - 1) & 1, kDrainNs);
+    return;
+  }
+  trace_point(p, kTrBarrier1);
 
   // ---- phase B: experts cta, cta + G, ...
   for (int e = cta; e < E; e += G) {
+    float t = 0.f;
+    if constexpr ((MODE & kModeFwd) != 0)
+      for (int j = tid; j < G; j += kMainThreads) t += __ldcg(p.P_part + (size_t)e * p.G_stride + j);
     const int total = block_exclusive_scan(p.tile_hist + (size_t)e * p.G_stride, G, s_red, true);
     if constexpr ((MODE & kModeFwd) != 0) {
-      float t = 0.f;
-      for (int j = tid; j < G; j += kThreads) t += __ldcg(p.P_part + (size_t)e * p.G_stride + j);
-      const double Ps = block_sum_d(double(t), s_red_d);
+      const float Ps = block_sum_f(t, reinterpret_cast<float*>(s_red + 16));
       if (tid == 0) {
         p.counts[e] = total;
         p.f[e] = float(double(total) / double(p.T * k));
-        p.P[e] = float(Ps / double(p.T));
+        p.P[e] = float(double(Ps) / double(p.T));
       }
     } else {
       if (tid == 0) counts_dst[e] = total;
     }
-    __syncthreads();
   }
-  if (!grid_barrier(p.ctrl, G, p.timeout_ns, s_red + 63)) return;
+  trace_point(p, kTrScanDone);
+  if (!grid_barrier(p.ctrl, G, p.barrier_extra, p.timeout_ns, s_red + 63, kBarMain, kMainThreads)) {
+    if (tid == 0) *reinterpret_cast<volatile int*>(s_phase) = -1;
+    return;
+  }
+  if (tid == 0) {
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(s_phase) = 1;
+  }
+  trace_point(p, kTrBarrier2);
 
   // ---- phase C
-  if constexpr ((MODE & kModeDispatch) != 0) {
-    for (int e = tid; e < E; e += kThreads) s_off[e] = __ldcg(counts_dst + e);
-    __syncthreads();
-    const int total = block_exclusive_scan(s_off, E, s_red, false);
-    if (tid == 0) s_off[E] = total;
-    __syncthreads();
-    dispatch_scatter(p, (MODE & kModeFwd) ? p.idx : p.idx_in, cta, a0, a1, s_off, s_w);
-  }
+  if (warp == kProducerWarp && cta == 0 && !refills) finalize_warp<MODE>(p, counts_dst);
   if constexpr ((MODE & kModeBwd) != 0) {
-    constexpr int RPW = kWarp / LPR;
     const float coef = p.grad_scale * p.alpha * float(E) / float(p.T);
-    bwd_rows<DT, LPR, VW, NV>(p.logits, E, p.f, coef, p.dlogits, r0 + (long long)(tid >> 5) * RPW, r1,
-                              (long long)kWarps * RPW);
-  }
-  if (cta == 0) {
-    if constexpr ((MODE & kModeDispatch) != 0) {
-      __syncthreads();
-      int dropped = 0;
-      for (int e = tid; e <= E; e += kThreads) {
-        p.offsets[e] = s_off[e];
-        if (e < E) {
-          const int c = __ldcg(counts_dst + e);
-          p.kept[e] = min(c, p.C);
-          dropped += max(c - p.C, 0);
+    float* s_f = s_wf;            // f, staged once per CTA (the per-warp partials are spent)
+    if (warp < kConsumerWarps)
+      for (int e = tid; e < E; e += kConsumerThreads) s_f[e] = __ldcg(p.f + e);
+    if (warp < kConsumerWarps) named_barrier(kBarConsumers, kConsumerThreads);
+    if (warp < kConsumerWarps) {
+      float fr[EPL];
+      load_f<LPR, VW, NV>(s_f, E, l, fr);
+      if constexpr (STAGED) {
+        for (int s = n_st - 1; s >= 0; --s) {
+          const int q = s % NS;
+          const int rel = (ring_last(q, n_st, NS) - s) / NS;     // 0: still in the ring from the forward
+          if (rel > 0 && !mbar_wait(&full[q], (ring_count_a(q, n_st, NS) + rel - 1) & 1, p.timeout_ns)) {
+            atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+            break;
+          }
+          if (s == n_st - 1) trace_point(p, kTrBwdFirst);
+          const Raw* st = ring + q * stage_elems;
+          const int rows_here = min(S, n_rows - s * S);
+          for (int gi = warp; gi * RPW < rows_here; gi += kConsumerWarps) {
+            const int ri = gi * RPW + g;
+            const bool valid = ri < rows_here;
+            Raw raw[EPL];
+            load_lane<DT, LPR, VW, NV, false>(st + (valid ? ri : 0) * E, E, l, valid, raw);
+            bwd_group<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, coef, p.dlogits);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[q]);
+        }
+      } else {
+        const long long n_groups = (r1 - r0 + RPW - 1) / RPW;
+        for (long long gi = n_groups - 1 - warp; gi >= 0; gi -= kConsumerWarps) {
+          const long long t = r0 + gi * RPW + g;
+          const bool valid = t < r1;
+          Raw raw[EPL];
+          load_lane<DT, LPR, VW, NV, true>(X + (valid ? t : r0) * (long long)E, E, l, valid, raw);
+          bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, E, coef, p.dlogits);
         }
       }
-      const double d = block_sum_d(double(dropped), s_red_d);
-      if (tid == 0) *p.n_dropped = int(d);
-    }
-    if constexpr ((MODE & kModeFwd) != 0) {
-      const double mean = double(p.T) * k / E;
-      double fp = 0.0, dev = 0.0;
-      int cmax = 0, cmin = 0x7fffffff;
-      for (int e = tid; e < E; e += kThreads) {
-        const int c = __ldcg(p.counts + e);
-        fp += double(__ldcg(p.f + e)) * double(__ldcg(p.P + e));
-        dev += (double(c) - mean) * (double(c) - mean);
-        cmax = max(cmax, c);
-        cmin = min(cmin, c);
-      }
-      fp = block_sum_d(fp, s_red_d);
-      dev = block_sum_d(dev, s_red_d);
-      cmax = block_max_i(cmax, s_red);
-      cmin = block_min_i(cmin, s_red);
-      double rdev = 0.0;
-      int rmax = 0;
-      const int R = p.n_ranks;
-      if (R > 0) {
-        const int per = E / R;
-        const double rmean = double(p.T) * k / R;
-        for (int r = tid; r < R; r += kThreads) {
-          int load = 0;
-          for (int j = 0; j < per; ++j) load += __ldcg(p.counts + r * per + j);
-          p.rank_load[r] = load;
-          rdev += (double(load) - rmean) * (double(load) - rmean);
-          rmax = max(rmax, load);
+      trace_point(p, kTrBwdRows);
+    } else if (is_producer) {
+      const uint64_t pol = l2_policy_evict_first();
+      const uint32_t row_bytes = uint32_t(E) * uint32_t(sizeof(Raw));
+      for (int s = n_st - NS - 1; s >= 0; --s) {
+        const int q = s % NS;
+        const int rel = (ring_last(q, n_st, NS) - s) / NS;       // >= 1 here
+        if (!mbar_wait(&empty[q], (ring_count_a(q, n_st, NS) + rel - 1) & 1, p.timeout_ns)) {
+          atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+          break;
         }
-        rdev = block_sum_d(rdev, s_red_d);
-        rmax = block_max_i(rmax, s_red);
-      }
-      if (tid == 0) {
-        const double balance = double(E) * fp;
-        p.scalars[0] = float(double(p.alpha) * balance);
-        p.scalars[1] = float(balance);
-        p.scalars[2] = float(sqrt(dev / E) / mean);
-        p.scalars[3] = float(cmax / mean);
-        p.scalars[4] = float(cmin / mean);
-        if (R > 0) {
-          const double rmean = double(p.T) * k / R;
-          p.scalars[5] = float(sqrt(rdev / R) / rmean);
-          p.scalars[6] = float(rmax / rmean);
-        } else {
-          p.scalars[5] = 0.f;
-          p.scalars[6] = 0.f;
-        }
+        const int rows_here = min(S, n_rows - s * S);
+        const uint32_t bytes = uint32_t(rows_here) * row_bytes;
+        mbar_arrive_expect_tx(&full[q], bytes);
+        bulk_g2s(ring + q * stage_elems, X + (r0 + (long long)s * S) * E, bytes, &full[q], pol);
+        ++fills[q];
       }
     }
   }
+  sync_main();
+  trace_point(p, kTrJoined);
+  // Every copy was waited on by the consumers in a normal run (these tests then
+  // pass at once); after an expired wait this keeps the CTA until its copies land.
+  if (is_producer)
+    for (int q = 0; q < NS; ++q)
+      if (fills[q] > 0) mbar_wait(&full[q], (fills[q] - 1) & 1, kDrainNs);
+  trace_point(p, kTrEnd);
 }
 
-// Backward alone: a plain grid-stride streaming kernel.
+// Backward alone: a plain grid-stride streaming kernel (8 warps per CTA).
 template <class DT, int LPR, int VW, int NV>
-__global__ void __launch_bounds__(kThreads) router_bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(256) router_bwd_kernel(const BwdParams p) {
+  using Raw = typename DT::Raw;
+  constexpr int EPL = VW * NV;
   constexpr int RPW = kWarp / LPR;
-  const long long gw = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const long long nw = (long long)gridDim.x * kWarps;
-  bwd_rows<DT, LPR, VW, NV>(p.logits, p.E, p.f, p.coef, p.dlogits, gw * RPW, p.T, nw * RPW);
+  __shared__ float s_f[1024];
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) s_f[e] = __ldg(p.f + e);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int g = lane / LPR, l = lane % LPR;
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long nw = (long long)gridDim.x * 8;
+  const Raw* X = static_cast<const Raw*>(p.logits);
+  float fr[EPL];
+  load_f<LPR, VW, NV>(s_f, p.E, l, fr);
+  for (long long base = gw * RPW; base < p.T; base += nw * RPW) {
+    const long long t = base + g;
+    const bool valid = t < p.T;
+    Raw raw[EPL];
+    load_lane<DT, LPR, VW, NV, true>(X + (valid ? t : 0) * (long long)p.E, p.E, l, valid, raw);
+    bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, p.E, p.coef, p.dlogits);
+  }
 }
 
 }  // namespace moe

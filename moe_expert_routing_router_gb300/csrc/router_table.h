@@ -7,15 +7,21 @@ namespace moe {
 
 struct RouterVariant {
   int LPR, VW, NV;         // lanes per row, elements per vector, vectors per lane
+  int NR;                  // row groups a consumer warp works on at once in the forward
+  int staged;              // rows streamed through the shared-memory ring (16-byte rows)
+  int min_blocks;          // CTAs per SM the persistent kernels are compiled for
   const void* fwd;         // persistent kernel, forward phases
   const void* step;        // persistent kernel, forward + dispatch + backward
   const void* bwd;         // streaming backward kernel
 };
 
 // Variants compiled for bf16 / fp32 logits; *n receives the count.
-const RouterVariant* router_variants_bf16(int* n);
-const RouterVariant* router_variants_fp32(int* n);
-// The dispatch-only persistent kernel.
+const RouterVariant* router_variants_bf16_staged(int* n);
+const RouterVariant* router_variants_bf16_direct(int* n);
+const RouterVariant* router_variants_fp32_staged(int* n);
+const RouterVariant* router_variants_fp32_direct(int* n);
+// The dispatch-only persistent kernel (compiled for kDispatchMinBlocks CTAs per SM).
 const void* dispatch_kernel();
+constexpr int kDispatchMinBlocks = 2;
 
 }  // namespace moe
