@@ -192,6 +192,34 @@ MOE_API moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, 
                            int32_t* n_dropped, float* dlogits,
                            void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_router_step for callers that cannot allocate device memory.
+ *
+ * Not a step of the method: the source pages have no counterpart.  It exists
+ * for callers that can pass inputs and outputs but cannot allocate or lend
+ * scratch memory: code running where allocation is not allowed or not safe,
+ * plugins with a device-memory budget fixed at load time, or runtimes that
+ * keep all device memory in their own pool.  Its scratch is a fixed array
+ * inside the library image (4 MiB + 64 KiB, held by every GPU that loads the
+ * library until the process exits); the call allocates nothing and frees
+ * nothing.
+ *   - Arguments and outputs are exactly those of moe_router_step, minus the
+ *     workspace; the results are the same.
+ *   - E must be <= 512 (MOE_ERR_INVALID otherwise, with a message naming the
+ *     limit).
+ *   - The first call on a device looks up the array's device address (a
+ *     cudaGetSymbolAddress, with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - All calls on a device share the one array: calls that may overlap on the
+ *     GPU (different streams, or different host threads) race.  Each call
+ *     clears the array's control block on `stream` before its kernel. */
+MOE_API moe_status moe_router_step_static(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                                          float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
+                                          float grad_scale,
+                                          int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                                          float* scalars, int32_t* rank_load,
+                                          int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                                          int32_t* n_dropped, float* dlogits, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* TAOT Phase 1: batched topology-aware Sinkhorn flow plan                  */
 /* ------------------------------------------------------------------------ */

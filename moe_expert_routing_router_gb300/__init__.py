@@ -14,10 +14,11 @@ from .api import (  # noqa: F401
     moe_router_bwd,
     moe_router_fwd,
     moe_router_step,
+    moe_router_step_static,
     taot_sinkhorn_batched,
 )
 
 __all__ = [
     "SCALAR_NAMES", "Workspace", "moe_dispatch", "moe_dispatch_capacity", "moe_get_device_status",
-    "moe_router_bwd", "moe_router_fwd", "moe_router_step", "taot_sinkhorn_batched",
+    "moe_router_bwd", "moe_router_fwd", "moe_router_step", "moe_router_step_static", "taot_sinkhorn_batched",
 ]

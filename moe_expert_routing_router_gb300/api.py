@@ -17,7 +17,7 @@ from ._native import MOE_DTYPE_BF16, MOE_DTYPE_FP32, MOE_NUM_SCALARS, SCALAR_NAM
 
 __all__ = [
     "Workspace", "moe_router_fwd", "moe_router_bwd", "moe_dispatch", "moe_dispatch_capacity",
-    "moe_router_step", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
+    "moe_router_step", "moe_router_step_static", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
 ]
 
 _DTYPES = {torch.float32: MOE_DTYPE_FP32, torch.bfloat16: MOE_DTYPE_BF16}
@@ -189,6 +189,29 @@ def moe_router_step(logits: torch.Tensor, k: int, alpha: float, capacity_factor:
                                _ptr(o["n_dropped"]), _ptr(o["dlogits"]), wp, wn, _stream_handle(stream))
     check(st, "moe_router_step")
     o["capacity"] = moe_dispatch_capacity(T, E, k, capacity_factor)
+    return o
+
+
+def moe_router_step_static(logits: torch.Tensor, k: int, alpha: float, capacity_factor: float, renorm: int = -1,
+                           n_ranks: int = 0, grad_scale: float = 1.0, out: dict | None = None,
+                           stream: torch.cuda.Stream | None = None) -> dict:
+    """moe_router_step without a workspace, for callers that cannot allocate device
+    scratch (C: moe_router_step_static; E <= 512; calls that overlap on the GPU race)."""
+    _need_cuda("logits", logits)
+    if logits.dtype not in _DTYPES or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 or bfloat16 tensor")
+    T, E = logits.shape
+    dev = logits.device
+    o = _fwd_outputs(T, E, k, n_ranks, dev, out)
+    o.update(_dispatch_outputs(T, E, k, dev, out))
+    o["dlogits"] = _out(out, "dlogits", (T, E), torch.float32, dev)
+    st = lib().moe_router_step_static(_ptr(logits), _DTYPES[logits.dtype], T, E, k, float(alpha), int(renorm),
+                                      int(n_ranks), float(capacity_factor), float(grad_scale),
+                                      _ptr(o["idx"]), _ptr(o["gate"]), _ptr(o["counts"]), _ptr(o["f"]), _ptr(o["P"]),
+                                      _ptr(o["scalars"]), _ptr(o["rank_load"]) if n_ranks > 0 else None,
+                                      _ptr(o["perm"]), _ptr(o["slot"]), _ptr(o["offsets"]), _ptr(o["kept"]),
+                                      _ptr(o["n_dropped"]), _ptr(o["dlogits"]), _stream_handle(stream))
+    check(st, "moe_router_step_static")
     return o
 
 

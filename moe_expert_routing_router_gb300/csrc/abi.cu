@@ -480,3 +480,72 @@ const char* moe_last_error(void) { return g_last_error.c_str(); }
 int32_t moe_abi_version(void) { return MOE_ROUTER_ABI_VERSION; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moe_router_step_static: moe_router_step without a caller workspace.
+//
+// Some callers cannot hand the library any device memory of their own: code
+// that runs where allocating is not allowed or not safe (for instance while a
+// host thread must not block on the allocator, inside plugins whose memory
+// budget is fixed when they are loaded, or from runtimes that own every byte
+// of device memory through their own pool and expose no allocator to native
+// code).  For them this entry point keeps its scratch in a fixed array that is
+// part of the library image: every GPU that loads the library holds it, all
+// kStaticScratchBytes of it, until the process exits, and the call itself
+// allocates nothing.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t(4) << 20) + (size_t(64) << 10);   // 4 MiB + 64 KiB
+constexpr int kStaticMaxExperts = 512;      // ws_layout(512).total fits in kStaticScratchBytes
+static_assert(kStaticScratchBytes >= 4096 + size_t(kStaticMaxExperts) * 4 * (2 * 1024 + 1), "scratch size");
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device.  In host code the
+// array's name only stands in for the symbol, so the address is looked up once
+// per device (with that device current) and cached.
+moe_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_INVALID, "device %d is beyond the %d this entry point serves", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    g_static_ptr[dev] = ptr;
+  }
+  *out = g_static_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_router_step_static(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                                             float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
+                                             float grad_scale,
+                                             int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                                             float* scalars, int32_t* rank_load,
+                                             int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                                             int32_t* n_dropped, float* dlogits, moe_stream_t stream) {
+  if (E > kStaticMaxExperts)
+    return fail(MOE_ERR_INVALID, "moe_router_step_static serves at most %d experts (E = %d); use moe_router_step",
+                kStaticMaxExperts, E);
+  void* ws = nullptr;
+  moe_status s = static_scratch(&ws);
+  if (s != MOE_OK) return s;
+  const size_t need = ws_layout(E).total;
+  if (need > kStaticScratchBytes) return fail(MOE_ERR_INVALID, "E = %d needs %zu bytes of scratch", E, need);
+  // The array keeps the previous call's contents; the control block (barrier
+  // state, error flags) must start at zero, the rest is written before it is read.
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(moe::Ctrl), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return moe_router_step(logits, dt, T, E, k, alpha, renorm, n_ranks, capacity_factor, grad_scale, idx, gate, counts,
+                         f, P, scalars, rank_load, perm, slot, offsets, kept, n_dropped, dlogits, ws, need, stream);
+}
