@@ -58,6 +58,32 @@ def algorithmic_bytes(w: synth.RouterWorkload) -> int:
     return w.T * (w.E * (esize + 4) + 16 * w.k)
 
 
+def kernel_source_hash() -> str:
+    """Hash of the CUDA/C++ sources of the library (changes whenever a kernel does)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = ROOT / "moe_expert_routing_router_gb300" / "csrc"
+    for f in sorted(csrc.iterdir()):
+        if f.suffix in (".cu", ".cuh", ".h"):
+            h.update(f.name.encode())
+            h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str) -> dict | None:
+    """DRAM bytes per launch of the step kernel from the committed ncu summary,
+    only while the kernel sources are the ones that summary was taken with."""
+    p = ROOT / "profiles" / "router_step_dram_traffic.txt"
+    if not p.exists():
+        return None
+    cur = kernel_source_hash()
+    for ln in p.read_text().splitlines():
+        f = ln.split()
+        if len(f) >= 8 and f[0] == "workload" and f[1] == workload and f[6] == "source_hash" and f[7] == cur:
+            return {"read": int(f[3]), "write": int(f[5])}
+    return None
+
+
 def peaks() -> dict:
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -416,7 +442,8 @@ def run_ours(args) -> dict:
                                       f"(>= 3x the 129 MB L2 between reuses)",
                                 "parallelism": f"replicas x{dist_ctx.world}", "timing": r["timing"]}),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "traffic": (lambda t: None if t is None else t["read"] + t["write"])(measured_traffic(w.name)),
                      "kernel": "router_persistent_kernel (moe_router_step, one launch per step)",
                      "algorithmic_bytes_per_launch": r["step_bytes"],
                      "launch_us_mean": round(r["launch_ms_mean"] * 1e3, 2), "peak_source": pk["source"]},

@@ -182,14 +182,15 @@ int64_t capacity_of(int64_t T, int32_t E, int32_t k, double cf) {
 // for staged variants, ring stages of about 16 KB and as many slots as fit in
 // the shared memory left per CTA (or as the chunk needs).
 struct Geometry {
-  int G = 1, rows_per_stage = 0, n_slots = 0;
+  int G = 1, rows_per_stage = 0, n_slots = 0, asg_cap = 0;
   size_t smem = 0;
 };
 
 constexpr size_t kSmemPerSm = 228 * 1024;      // GB300 shared memory per SM
 constexpr size_t kSmemReservedPerCta = 1024;
+constexpr int kMaxAsgSmem = 12288;             // assignments per CTA kept in shared memory for the dispatch
 
-moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, int E, Geometry* out) {
+moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, int E, int k, Geometry* out) {
   DeviceInfo d;
   int dev = 0;
   moe_status s = device_info(&d, &dev);
@@ -198,25 +199,36 @@ moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, 
   const int group_rows = moe::kConsumerWarps * (moe::kWarp / v->LPR) * v->NR;
   Geometry g;
   const size_t fixed = moe::router_smem_layout(E, 0, 0).total;
+  const size_t budget = kSmemPerSm / size_t(v->min_blocks) - kSmemReservedPerCta;
+  size_t stage_bytes = 0;
   if (v->staged) {
     const int row_bytes = E * esize;
     g.rows_per_stage = std::max(group_rows, (16384 / row_bytes) / group_rows * group_rows);
-    const size_t stage_bytes = size_t(g.rows_per_stage) * row_bytes;
-    const size_t budget = kSmemPerSm / size_t(v->min_blocks) - kSmemReservedPerCta;
+    stage_bytes = size_t(g.rows_per_stage) * row_bytes;
     g.n_slots = int(std::max<size_t>(1, std::min<size_t>(moe::kMaxSlots, (budget - fixed) / stage_bytes)));
   }
-  size_t smem = moe::router_smem_layout(E, g.n_slots, g.rows_per_stage * E * esize).total;
+  size_t smem = moe::router_smem_layout(E, g.n_slots, int(stage_bytes)).total;
   int bf = 0, bs = 0;
   if ((s = occupancy(v->fwd, moe::kThreads, smem, dev, &bf)) != MOE_OK) return s;
   if ((s = occupancy(v->step, moe::kThreads, smem, dev, &bs)) != MOE_OK) return s;
   const int64_t cap = std::min<int64_t>(int64_t(std::min(bf, bs)) * d.sms, kGridMax);
   const int64_t want = (T + group_rows - 1) / group_rows;
   g.G = int(std::max<int64_t>(1, std::min(cap, want)));
-  if (v->staged) {   // no more slots than the largest chunk has stages
+  if (v->staged) {
     const int64_t chunk = (T + g.G - 1) / g.G;
-    const int64_t stages = (chunk + g.rows_per_stage - 1) / g.rows_per_stage;
+    // Keep each CTA's assignments (expert id, in-CTA rank) in shared memory when
+    // they fit beside at least two ring slots.
+    const int64_t asg = (chunk * k + 7) / 8 * 8;
+    if (asg <= kMaxAsgSmem) {
+      const size_t with = moe::router_smem_layout(E, 0, 0, int(asg)).total;
+      if (with + 2 * stage_bytes <= budget) {
+        g.asg_cap = int(asg);
+        g.n_slots = int(std::max<size_t>(1, std::min<size_t>(moe::kMaxSlots, (budget - with) / stage_bytes)));
+      }
+    }
+    const int64_t stages = (chunk + g.rows_per_stage - 1) / g.rows_per_stage;   // no more slots than stages
     g.n_slots = int(std::max<int64_t>(1, std::min<int64_t>(g.n_slots, stages)));
-    smem = moe::router_smem_layout(E, g.n_slots, g.rows_per_stage * E * esize).total;
+    smem = moe::router_smem_layout(E, g.n_slots, int(stage_bytes), g.asg_cap).total;
   }
   g.smem = smem;
   *out = g;
@@ -316,10 +328,11 @@ moe_status moe_router_fwd(const void* logits, moe_dtype dt, int64_t T, int32_t E
   p.idx = idx; p.gate = gate; p.counts = counts; p.f = f; p.P = P; p.scalars = scalars; p.rank_load = rank_load;
   bind_ws(p, ws, E);
   Geometry geo;
-  if ((s = persistent_geometry(v, dt, T, E, &geo)) != MOE_OK) return s;
+  if ((s = persistent_geometry(v, dt, T, E, k, &geo)) != MOE_OK) return s;
   p.G = geo.G;
   p.rows_per_stage = geo.rows_per_stage;
   p.n_slots = geo.n_slots;
+  p.asg_cap = geo.asg_cap;
   return launch_persistent(v->fwd, p, geo.smem, stream);
 }
 
@@ -417,10 +430,11 @@ moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t 
   p.dlogits = dlogits;
   bind_ws(p, ws, E);
   Geometry geo;
-  if ((s = persistent_geometry(v, dt, T, E, &geo)) != MOE_OK) return s;
+  if ((s = persistent_geometry(v, dt, T, E, k, &geo)) != MOE_OK) return s;
   p.G = geo.G;
   p.rows_per_stage = geo.rows_per_stage;
   p.n_slots = geo.n_slots;
+  p.asg_cap = geo.asg_cap;
   return launch_persistent(v->step, p, geo.smem, stream);
 }
 

@@ -127,11 +127,23 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Like mbar_test, but the thread may be suspended in hardware for up to
+// `hint_ns` until the phase completes (no issue slots spent while waiting).
+__device__ __forceinline__ bool mbar_test_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns) : "memory");
+  return ok != 0;
+}
+
 // Waits until the barrier phase of parity `parity` has completed; false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_test(bar, parity)) {
+  while (!mbar_test_suspend(bar, parity, 20000u)) {
     if (global_ns() - t0 > timeout_ns) return false;
   }
   return true;

@@ -86,6 +86,7 @@ struct RouterParams {
   // staging ring (staged variants)
   int rows_per_stage;
   int n_slots;
+  int asg_cap;                 // assignments per CTA the shared-memory dispatch buffers hold (0: none)
 };
 
 // Phase boundaries recorded in RouterParams::trace (lane 0 of the warp named).
@@ -102,12 +103,13 @@ enum : int {
   kTrDispatchDone,     // warp 9: dispatch (and CTA 0's E-sized outputs) done
   kTrJoined,           // warp 0: all warps joined
   kTrEnd,              // warp 0: kernel exit
+  kTrRanked,           // warp 9: in-CTA dispatch ranks done
   kTracePoints = 16
 };
 
 __device__ __forceinline__ void trace_point(const RouterParams& p, int point) {
   if (p.trace != nullptr && (threadIdx.x & 31) == 0) {
-    if (point == kTrDispatchDone ? threadIdx.x == kDispatchWarp * kWarp : threadIdx.x == 0)
+    if ((point == kTrDispatchDone || point == kTrRanked) ? threadIdx.x == kDispatchWarp * kWarp : threadIdx.x == 0)
       p.trace[blockIdx.x * kTracePoints + point] = global_ns();
   }
 }
@@ -125,12 +127,14 @@ struct BwdParams {
 // Shared-memory layout of the persistent kernel (byte offsets).
 // ---------------------------------------------------------------------------
 struct SmemLayout {
-  unsigned red, hist, off, rank, w, bars, ring, total;
+  unsigned red, hist, off, rank, w, bars, asg, ring, total;
 };
 
 __host__ __device__ inline unsigned align_to(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout router_smem_layout(int E, int n_slots, int stage_bytes) {
+// asg_cap: capacity of the two uint16 arrays (expert id and in-CTA rank of each
+// of the CTA's assignments) that keep the dispatch in shared memory.
+__host__ __device__ inline SmemLayout router_smem_layout(int E, int n_slots, int stage_bytes, int asg_cap = 0) {
   SmemLayout L;
   L.red = 0;                                                  // 64 ints (32 doubles)
   L.hist = 256;                                               // E ints
@@ -138,7 +142,8 @@ __host__ __device__ inline SmemLayout router_smem_layout(int E, int n_slots, int
   L.rank = L.off + 4u * (E + 1);                              // E ints
   L.w = align_to(L.rank + 4u * E, 16);                        // kConsumerWarps * E words
   L.bars = align_to(L.w + 4u * kConsumerWarps * E, 16);       // 2 * kMaxSlots mbarriers
-  L.ring = align_to(L.bars + 16u * kMaxSlots, 128);
+  L.asg = L.bars + 16u * kMaxSlots;                           // 2 * asg_cap uint16
+  L.ring = align_to(L.asg + 4u * unsigned(asg_cap), 128);
   L.total = L.ring + unsigned(n_slots) * unsigned(stage_bytes);
   return L;
 }
@@ -307,7 +312,7 @@ __device__ __forceinline__ float tree_sum(const float (&x)[N]) {
 template <class DT, int LPR, int VW, int NV, int NR, bool GLOBAL>
 __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename DT::Raw* const (&row)[NR],
                                            const long long (&t)[NR], const bool (&valid)[NR], int l, int* s_hist,
-                                           float (&pacc)[VW * NV]) {
+                                           float (&pacc)[VW * NV], uint16_t* s_aidx, long long a_base) {
   using Raw = typename DT::Raw;
   using Key = typename DT::Key;
   constexpr int EPL = VW * NV;
@@ -375,6 +380,7 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
       p.idx[a] = col;
       p.gate[a] = ej * rcp_approx(denom);
       atomicAdd(&s_hist[col], 1);
+      if (s_aidx != nullptr) s_aidx[a - a_base] = uint16_t(col);
     }
   }
 }
@@ -590,6 +596,46 @@ __device__ __forceinline__ void dispatch_fixup(const RouterParams& p, const int3
   }
 }
 
+// In-CTA ranks from the shared-memory copy of this CTA's expert ids: for local
+// assignment indices [lo, hi), rank[lo..hi) = rank among this CTA's assignments
+// to the same expert.
+__device__ __forceinline__ void local_ranks_smem(const uint16_t* aidx, int lo, int hi, int* rank, uint16_t* out) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += kWarp) {
+    const int a = base + lane;
+    const bool act = a < hi;
+    const int e = act ? aidx[a] : 0;
+    unsigned peers = __ballot_sync(0xffffffffu, act);   // lanes holding the same expert
+#pragma unroll
+    for (int bit = 0; bit < 10; ++bit) {
+      const unsigned ones = __ballot_sync(0xffffffffu, (e >> bit) & 1);
+      peers &= ((e >> bit) & 1) ? ones : ~ones;
+    }
+    const int lower = __popc(peers & lt);
+    const int r = act ? rank[e] + lower : 0;
+    __syncwarp();
+    if (act && lower == 0) rank[e] += __popc(peers);
+    __syncwarp();
+    if (act) out[a] = uint16_t(r);
+  }
+}
+
+// Final positions from the shared-memory expert ids and in-CTA ranks.
+__device__ __forceinline__ void dispatch_fixup_smem(const RouterParams& p, long long a0, int n, const uint16_t* aidx,
+                                                    const uint16_t* arank, const int* off, const int* base) {
+  const int lane = threadIdx.x & 31;
+  for (int i = lane; i < n; i += kWarp) {
+    const int e = aidx[i];
+    const int r = base[e] + arank[i];
+    const long long a = a0 + i;
+    if (r >= 0 && r < off[e + 1] - off[e]) {                // always true for consistent ranks
+      p.perm[off[e] + r] = int(a);
+      p.slot[a] = r < p.C ? r : -1;
+    }
+  }
+}
+
 // Final ranks directly (rank[e] starts at the CTA's prefix), for the variants
 // that read rows straight from global memory: used after the global prefix.
 __device__ __forceinline__ void dispatch_direct(const RouterParams& p, const int32_t* idx_src, long long a0, long long a1,
@@ -705,7 +751,7 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
 template <int MODE, bool STAGED>
 __device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta, long long a0, long long a1, int* s_off,
                                                  int* s_rank, int* s_phase, const int32_t* counts, bool finalize_here,
-                                                 bool ranked) {
+                                                 bool ranked, const uint16_t* s_aidx, const uint16_t* s_arank) {
   const int lane = threadIdx.x & 31;
   const int E = p.E;
   int ph = 0;
@@ -724,8 +770,9 @@ __device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta,
     warp_offsets(counts, E, s_off);
     for (int e = lane; e < E; e += kWarp) s_rank[e] = __ldcg(p.tile_hist + (size_t)e * p.G_stride + cta);
     __syncwarp();
-    constexpr bool kRanked = STAGED || (MODE & kModeFwd) == 0;   // in-CTA ranks already parked in slot[]
-    if constexpr (kRanked) dispatch_fixup(p, (MODE & kModeFwd) ? p.idx : p.idx_in, a0, a1, s_off, s_rank);
+    constexpr bool kRanked = STAGED || (MODE & kModeFwd) == 0;   // in-CTA ranks already computed
+    if (s_aidx != nullptr) dispatch_fixup_smem(p, a0, int(a1 - a0), s_aidx, s_arank, s_off, s_rank);
+    else if constexpr (kRanked) dispatch_fixup(p, (MODE & kModeFwd) ? p.idx : p.idx_in, a0, a1, s_off, s_rank);
     else dispatch_direct(p, p.idx, a0, a1, s_off, s_rank);
   }
   if (finalize_here) finalize_warp<MODE>(p, counts);
@@ -765,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   const int S = STAGED ? p.rows_per_stage : 1;
   const int NS = STAGED ? p.n_slots : 1;
   const int stage_elems = S * E;
-  const SmemLayout L = router_smem_layout(E, STAGED ? NS : 0, stage_elems * int(sizeof(Raw)));
+  const SmemLayout L = router_smem_layout(E, STAGED ? NS : 0, stage_elems * int(sizeof(Raw)), p.asg_cap);
   int* s_red = reinterpret_cast<int*>(smem + L.red);
   int* s_prog = s_red + 40;       // stages finished per consumer warp (forward)
   int* s_phase = s_red + 48;      // 1 once grid barrier 2 has passed, -1 after an error
@@ -783,6 +830,10 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   const int n_st = STAGED ? (n_rows + S - 1) / S : 0;
   const Raw* X = static_cast<const Raw*>(p.logits);
   int32_t* counts_dst = (MODE & kModeFwd) ? p.counts : p.counts_ws;
+  // the CTA's dispatch in shared memory when its assignments fit
+  const bool asg_smem = STAGED && (MODE & kModeFwd) != 0 && (MODE & kModeDispatch) != 0 && a1 - a0 <= p.asg_cap;
+  uint16_t* s_aidx = asg_smem ? reinterpret_cast<uint16_t*>(smem + L.asg) : nullptr;
+  uint16_t* s_arank = asg_smem ? s_aidx + p.asg_cap : nullptr;
   const bool is_producer = STAGED && warp == kProducerWarp && lane == 0;
   int fills[kMaxSlots];          // copies issued per slot (producer thread), drained on an error exit
   bool ranked = true;            // dispatch warp: every in-CTA rank of this CTA has been written
@@ -832,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
               rows[r] = st + (valids[r] ? ri : 0) * E;
               ts[r] = r0 + (long long)s * S + ri;
             }
-            fwd_groups<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc);
+            fwd_groups<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc, s_aidx, a0);
           }
           __syncwarp();
           if (lane == 0) {
@@ -854,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
             valids[r] = ts[r] < r1;
             rows[r] = X + (valids[r] ? ts[r] : r0) * (long long)E;
           }
-          fwd_groups<DT, LPR, VW, NV, NR, true>(p, rows, ts, valids, l, s_hist, pacc);
+          fwd_groups<DT, LPR, VW, NV, NR, true>(p, rows, ts, valids, l, s_hist, pacc, nullptr, 0);
         }
       }
       trace_point(p, kTrFwdRows);
@@ -912,10 +963,12 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
         __threadfence_block();
         const long long lo = (r0 + (long long)s * S) * k;
         const long long hi = min(r0 + (long long)(s + 1) * S, r1) * k;
-        local_ranks<kLoadOwn>(p.idx, lo, hi, E, s_rank, p.slot);
+        if (s_aidx != nullptr) local_ranks_smem(s_aidx, int(lo - a0), int(hi - a0), s_rank, s_arank);
+        else local_ranks<kLoadOwn>(p.idx, lo, hi, E, s_rank, p.slot);
         if (s == n_st - 1) ranked = true;
       }
       if (n_st == 0) ranked = true;
+      trace_point(p, kTrRanked);
     }
   } else {
     if (warp == kDispatchWarp) {
@@ -931,7 +984,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   // backward; CTA 0's E-sized outputs go to whichever of warps 8 and 9 is idle.
   const bool refills = STAGED && (MODE & kModeBwd) != 0 && n_st > NS;
   if (warp == kDispatchWarp) {
-    dispatch_phase_c<MODE, STAGED>(p, cta, a0, a1, s_off, s_rank, s_phase, counts_dst, cta == 0 && refills, ranked);
+    dispatch_phase_c<MODE, STAGED>(p, cta, a0, a1, s_off, s_rank, s_phase, counts_dst, cta == 0 && refills, ranked,
+                                   s_aidx, s_arank);
     return;
   }
   sync_main();

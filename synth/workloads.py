@@ -4,7 +4,8 @@ Every workload is a token-by-expert matrix of router logits z[T, E]:
 
   * ``switch-top1-T4096-E8``: fp32 logits drawn i.i.d. N(0, 1); Switch top-1
     routing over 8 experts (the 8-expert setting of the MoE article's
-    capacity example, section 4.5 of "负载均衡在高性能计算中的三层实践").
+    capacity example, section 4.5 of the untitled HPC load-balancing article at
+    mhpq.cn/news/998159).
   * ``zipf-top2-T65536-E64``: 16 sequences x 4096 tokens, 64 experts, top-2 with
     the gate renormalised over the two picks.  Logits are N(0, 1) plus a
     per-expert bias b_e = 1.5 * ln(w_e), where w is a Zipf(s=1.1) law laid over
