@@ -270,7 +270,9 @@ MOE_API void moe_set_unreachable_barriers(int32_t enable);
  *   3 per-CTA partials published, 4 after grid barrier 1, 5 per-expert scans
  *   done, 6 after grid barrier 2, 7 first backward stage available, 8 backward
  *   rows done (warp 0), 9 dispatch and E-sized outputs done (dispatch warp),
- *   10 all warps joined, 11 exit, 12 in-CTA dispatch ranks done (dispatch warp).
+ *   10 all warps joined, 11 exit, 12 in-CTA dispatch ranks done (dispatch warp),
+ *   13 the SM the CTA ran on (an SM id, not a time), 14 and 15 the time the
+ *   last consumer warp finished its forward / backward rows. 
  * A launch with more than max_ctas CTAs fails with MOE_ERR_INVALID.  NULL
  * turns tracing off. */
 #define MOE_TRACE_POINTS 16

@@ -182,32 +182,39 @@ int64_t capacity_of(int64_t T, int32_t E, int32_t k, double cf) {
 // for staged variants, ring stages of about 16 KB and as many slots as fit in
 // the shared memory left per CTA (or as the chunk needs).
 struct Geometry {
-  int G = 1, rows_per_stage = 0, n_slots = 0, asg_cap = 0;
+  int G = 1, rows_per_stage = 0, n_slots = 0, asg_cap = 0, rstat_cap = 0;
   size_t smem = 0;
 };
 
 constexpr size_t kSmemPerSm = 228 * 1024;      // GB300 shared memory per SM
 constexpr size_t kSmemReservedPerCta = 1024;
+constexpr int kStageBytes = 24576;             // target size of one ring stage
 constexpr int kMaxAsgSmem = 12288;             // assignments per CTA kept in shared memory for the dispatch
+constexpr int kMaxRowStats = 4096;             // rows per CTA whose softmax statistics stay in shared memory
 
-moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, int E, int k, Geometry* out) {
+// fused: the launch runs the fused step (forward, dispatch and backward), whose
+// CTAs keep their dispatch and the rows' softmax statistics in shared memory
+// when these fit beside at least two ring slots.
+moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, int E, int k, bool fused,
+                               Geometry* out) {
   DeviceInfo d;
   int dev = 0;
   moe_status s = device_info(&d, &dev);
   if (s != MOE_OK) return s;
   const int esize = dt == MOE_DTYPE_BF16 ? 2 : 4;
+  const int kb = dt == MOE_DTYPE_BF16 ? int(sizeof(moe::Bf16::Key)) : int(sizeof(moe::Fp32::Key));
   const int group_rows = moe::kConsumerWarps * (moe::kWarp / v->LPR) * v->NR;
   Geometry g;
-  const size_t fixed = moe::router_smem_layout(E, 0, 0).total;
+  const size_t fixed = moe::router_smem_layout(E, kb, 0, 0).total;
   const size_t budget = kSmemPerSm / size_t(v->min_blocks) - kSmemReservedPerCta;
   size_t stage_bytes = 0;
   if (v->staged) {
     const int row_bytes = E * esize;
-    g.rows_per_stage = std::max(group_rows, (16384 / row_bytes) / group_rows * group_rows);
+    g.rows_per_stage = std::max(group_rows, (kStageBytes / row_bytes) / group_rows * group_rows);
     stage_bytes = size_t(g.rows_per_stage) * row_bytes;
     g.n_slots = int(std::max<size_t>(1, std::min<size_t>(moe::kMaxSlots, (budget - fixed) / stage_bytes)));
   }
-  size_t smem = moe::router_smem_layout(E, g.n_slots, int(stage_bytes)).total;
+  size_t smem = moe::router_smem_layout(E, kb, g.n_slots, int(stage_bytes)).total;
   int bf = 0, bs = 0;
   if ((s = occupancy(v->fwd, moe::kThreads, smem, dev, &bf)) != MOE_OK) return s;
   if ((s = occupancy(v->step, moe::kThreads, smem, dev, &bs)) != MOE_OK) return s;
@@ -216,19 +223,21 @@ moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, 
   g.G = int(std::max<int64_t>(1, std::min(cap, want)));
   if (v->staged) {
     const int64_t chunk = (T + g.G - 1) / g.G;
-    // Keep each CTA's assignments (expert id, in-CTA rank) in shared memory when
-    // they fit beside at least two ring slots.
-    const int64_t asg = (chunk * k + 7) / 8 * 8;
-    if (asg <= kMaxAsgSmem) {
-      const size_t with = moe::router_smem_layout(E, 0, 0, int(asg)).total;
-      if (with + 2 * stage_bytes <= budget) {
+    if (fused) {
+      const int64_t rows = (chunk + 15) / 16 * 16;
+      if (rows <= kMaxRowStats &&
+          moe::router_smem_layout(E, kb, 0, 0, 0, int(rows)).total + 2 * stage_bytes <= budget)
+        g.rstat_cap = int(rows);
+      const int64_t asg = (chunk * k + 7) / 8 * 8;
+      if (asg <= kMaxAsgSmem &&
+          moe::router_smem_layout(E, kb, 0, 0, int(asg), g.rstat_cap).total + 2 * stage_bytes <= budget)
         g.asg_cap = int(asg);
-        g.n_slots = int(std::max<size_t>(1, std::min<size_t>(moe::kMaxSlots, (budget - with) / stage_bytes)));
-      }
+      const size_t with = moe::router_smem_layout(E, kb, 0, 0, g.asg_cap, g.rstat_cap).total;
+      g.n_slots = int(std::max<size_t>(1, std::min<size_t>(moe::kMaxSlots, (budget - with) / stage_bytes)));
     }
     const int64_t stages = (chunk + g.rows_per_stage - 1) / g.rows_per_stage;   // no more slots than stages
     g.n_slots = int(std::max<int64_t>(1, std::min<int64_t>(g.n_slots, stages)));
-    smem = moe::router_smem_layout(E, g.n_slots, int(stage_bytes), g.asg_cap).total;
+    smem = moe::router_smem_layout(E, kb, g.n_slots, int(stage_bytes), g.asg_cap, g.rstat_cap).total;
   }
   g.smem = smem;
   *out = g;
@@ -292,9 +301,10 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream, int32_t* flags) 
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   moe::Ctrl* c = static_cast<moe::Ctrl*>(ws);
-  int32_t v = 0;
-  e = cudaMemcpy(&v, &c->error, sizeof(v), cudaMemcpyDeviceToHost);
+  unsigned long long word = 0;
+  e = cudaMemcpy(&word, &c->sync, sizeof(word), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+  const int32_t v = int32_t(word >> 32);
   *flags = v;
   if (v != 0) {
     // Clear the flags and the barrier state for the next call.
@@ -328,11 +338,12 @@ moe_status moe_router_fwd(const void* logits, moe_dtype dt, int64_t T, int32_t E
   p.idx = idx; p.gate = gate; p.counts = counts; p.f = f; p.P = P; p.scalars = scalars; p.rank_load = rank_load;
   bind_ws(p, ws, E);
   Geometry geo;
-  if ((s = persistent_geometry(v, dt, T, E, k, &geo)) != MOE_OK) return s;
+  if ((s = persistent_geometry(v, dt, T, E, k, false, &geo)) != MOE_OK) return s;
   p.G = geo.G;
   p.rows_per_stage = geo.rows_per_stage;
   p.n_slots = geo.n_slots;
   p.asg_cap = geo.asg_cap;
+  p.rstat_cap = geo.rstat_cap;
   return launch_persistent(v->fwd, p, geo.smem, stream);
 }
 
@@ -392,7 +403,7 @@ moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_t k, dou
   int dev = 0;
   if ((s = device_info(&d, &dev)) != MOE_OK) return s;
   const void* func = moe::dispatch_kernel();
-  const size_t smem = moe::router_smem_layout(E, 0, 0).total;
+  const size_t smem = moe::router_smem_layout(E, int(sizeof(moe::Bf16::Key)), 0, 0).total;   // a bf16 instance
   int blocks = 0;
   if ((s = occupancy(func, moe::kThreads, smem, dev, &blocks)) != MOE_OK) return s;
   const int64_t cap = std::min<int64_t>(int64_t(blocks) * d.sms, kGridMax);
@@ -430,11 +441,12 @@ moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t 
   p.dlogits = dlogits;
   bind_ws(p, ws, E);
   Geometry geo;
-  if ((s = persistent_geometry(v, dt, T, E, k, &geo)) != MOE_OK) return s;
+  if ((s = persistent_geometry(v, dt, T, E, k, true, &geo)) != MOE_OK) return s;
   p.G = geo.G;
   p.rows_per_stage = geo.rows_per_stage;
   p.n_slots = geo.n_slots;
   p.asg_cap = geo.asg_cap;
+  p.rstat_cap = geo.rstat_cap;
   return launch_persistent(v->step, p, geo.smem, stream);
 }
 

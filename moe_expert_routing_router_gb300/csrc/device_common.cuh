@@ -12,17 +12,20 @@ constexpr int kWarp = 32;
 constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
 
 // ---------------------------------------------------------------------------
-// Workspace control block (first 512 bytes of the caller's workspace).  The
-// fields that many CTAs touch at once sit on separate 128-byte lines.
+// Workspace control block (first 512 bytes of the caller's workspace).
+//
+// One 64-bit word carries the grid-barrier arrival count (low half) and the
+// sticky error bits (high half), so that an arrival is a single atomic and a
+// waiter learns both "everyone is here" and "someone failed" from one load.
+// The count grows by one per CTA and barrier during a launch; the last CTA to
+// arrive at the launch's final barrier takes it back to 0.  A failed launch
+// leaves the count wherever it stopped and the error bits set; the host reads
+// and clears both (moe_get_device_status), and until then every later launch
+// sees the error at its first barrier and writes nothing.
 // ---------------------------------------------------------------------------
 struct Ctrl {
-  unsigned bar_count;   // CTAs arrived at the current grid barrier (0 between barriers)
-  unsigned pad0[31];
-  unsigned bar_gen;     // barrier generation, bumped by the last arriver
-  unsigned pad1[31];
-  int error;            // sticky error bits, read and cleared by the host
-  int pad2[31];
-  unsigned pad3[32];
+  unsigned long long sync;   // [31:0] arrivals, [63:32] error bits
+  unsigned long long pad[63];
 };
 static_assert(sizeof(Ctrl) == 512, "control block is 512 bytes");
 
@@ -34,61 +37,69 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_u64(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
 }
 
-__device__ __forceinline__ int ld_volatile_i32(const int* p) {
-  return *reinterpret_cast<const volatile int*>(p);
+__device__ __forceinline__ void ctrl_set_error(Ctrl* c, int bits) {
+  atomicOr(&c->sync, (unsigned long long)(unsigned)bits << 32);
 }
 
-// Grid-wide barrier for a cooperative launch (all CTAs co-resident): the CTA
-// that brings the arrivals to nblocks + extra releases it (extra is 0 except in
-// tests of the timeout path, where it makes the release unreachable).  The
-// wait is bounded by `timeout_ns`; on expiry the CTA records kErrBarrierTimeout.
-// Returns false (uniformly across the CTA) once any CTA of the launch has
-// recorded an error: the caller must then stop writing and return, and later
-// barriers stop waiting because the flag is already set.
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
+// Grid-wide barrier number `round` (1, 2, ...) of a cooperative launch (all
+// CTAs co-resident).  It passes once the arrival count reaches
+// round * (nblocks + extra); extra is 0 except in tests of the timeout path,
+// where it makes the barrier unreachable.  On the launch's final barrier
+// (`last`) the CTA that completes it subtracts the launch's arrivals again, and
+// its waiters accept a count of 0 as passed.  Every wait is bounded by
+// `timeout_ns`; on expiry the CTA records kErrBarrierTimeout.  Returns false
+// (uniformly across the CTA) once any CTA of the launch, or of an earlier
+// launch not yet cleared by the host, has recorded an error: the caller must
+// then stop writing and return.
+//
 // Called by the `nthreads` threads (whole warps, including thread 0) that
 // synchronise on named barrier `bar_id` within the CTA.
-__device__ __forceinline__ bool grid_barrier(Ctrl* c, unsigned nblocks, unsigned extra, uint64_t timeout_ns,
-                                             int* s_flag, int bar_id, int nthreads) {
+__device__ __forceinline__ bool grid_barrier(Ctrl* c, unsigned nblocks, unsigned extra, unsigned round, bool last,
+                                             uint64_t timeout_ns, int* s_flag, int bar_id, int nthreads) {
   named_barrier(bar_id, nthreads);               // the group's writes happen before thread 0's arrival
   if (threadIdx.x == 0) {
-    const unsigned gen = ld_acquire_u32(&c->bar_gen);
-    unsigned arrived;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(arrived) : "l"(&c->bar_count) : "memory");
-    if (arrived == nblocks + extra - 1) {
-      c->bar_count = 0u;
-      st_release_u32(&c->bar_gen, gen + 1u);   // orders the reset (and every arrival seen) before the release
-    } else {
+    const unsigned target = (nblocks + extra) * round;
+    const unsigned long long old = atom_add_acq_rel_u64(&c->sync, 1ull);
+    unsigned err = unsigned(old >> 32);
+    if (err == 0 && unsigned(old) + 1u == target) {
+      if (last) atomicAdd(&c->sync, 0ull - (unsigned long long)target);   // back to 0 for the next launch
+    } else if (err == 0) {
       uint64_t t0 = 0;
       for (unsigned spin = 0;; ++spin) {
-        if (ld_acquire_u32(&c->bar_gen) != gen) break;
+        const unsigned long long v = ld_acquire_u64(&c->sync);
+        err = unsigned(v >> 32);
+        const unsigned n = unsigned(v);
+        if (err != 0 || n >= target || (last && n == 0)) break;
         if ((spin & 15u) == 15u) {
-          if (ld_volatile_i32(&c->error) != 0) break;
           const uint64_t now = global_ns();
           if (t0 == 0) {
             t0 = now;
           } else if (now - t0 > timeout_ns) {
-            atomicOr(&c->error, kErrBarrierTimeout);
+            ctrl_set_error(c, kErrBarrierTimeout);
+            err = kErrBarrierTimeout;
             break;
           }
         }
-        if (spin > 8) __nanosleep(64);
+        if (spin > 8) __nanosleep(32);
       }
     }
-    *s_flag = ld_volatile_i32(&c->error);
+    *s_flag = int(err);
   }
   named_barrier(bar_id, nthreads);
   return *s_flag == 0;
@@ -270,7 +281,7 @@ __device__ __forceinline__ long long group_max_key(long long x) {
   return x;
 }
 
-__device__ __forceinline__ double warp_sum_d(double x) {
+__device__ __forceinline__ float warp_sum_f(float x) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
   return x;

@@ -4,10 +4,10 @@
 namespace moe {
 
 static const RouterVariant kVariants[] = {
-    MOE_ROUTER_VARIANT(Fp32, 8, 1, 1, 1, false, 2),    // E <= 8
-    MOE_ROUTER_VARIANT(Fp32, 32, 1, 1, 1, false, 2),   // E <= 32
-    MOE_ROUTER_VARIANT(Fp32, 32, 1, 2, 1, false, 2),
-    MOE_ROUTER_VARIANT(Fp32, 32, 1, 4, 1, false, 2),
+    MOE_ROUTER_VARIANT(Fp32, 8, 1, 1, 1, false, 1),    // E <= 8
+    MOE_ROUTER_VARIANT(Fp32, 32, 1, 1, 1, false, 1),   // E <= 32
+    MOE_ROUTER_VARIANT(Fp32, 32, 1, 2, 1, false, 1),
+    MOE_ROUTER_VARIANT(Fp32, 32, 1, 4, 1, false, 1),
     MOE_ROUTER_VARIANT(Fp32, 32, 1, 8, 1, false, 1),
     MOE_ROUTER_VARIANT(Fp32, 32, 1, 16, 1, false, 1),
     MOE_ROUTER_VARIANT(Fp32, 32, 1, 32, 1, false, 1),  // E <= 1024

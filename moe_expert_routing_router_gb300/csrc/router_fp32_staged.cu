@@ -4,11 +4,11 @@
 namespace moe {
 
 static const RouterVariant kVariants[] = {
-    MOE_ROUTER_VARIANT(Fp32, 8, 1, 1, 2, true, 2),     // E <= 8
-    MOE_ROUTER_VARIANT(Fp32, 8, 4, 1, 2, true, 2),     // E <= 32
-    MOE_ROUTER_VARIANT(Fp32, 8, 4, 2, 2, true, 2),     // E <= 64
-    MOE_ROUTER_VARIANT(Fp32, 16, 4, 2, 2, true, 2),    // E <= 128
-    MOE_ROUTER_VARIANT(Fp32, 32, 4, 2, 2, true, 2),    // E <= 256
+    MOE_ROUTER_VARIANT(Fp32, 8, 1, 1, 2, true, 1),     // E <= 8
+    MOE_ROUTER_VARIANT(Fp32, 8, 4, 1, 2, true, 1),     // E <= 32
+    MOE_ROUTER_VARIANT(Fp32, 8, 4, 2, 2, true, 1),     // E <= 64
+    MOE_ROUTER_VARIANT(Fp32, 16, 4, 2, 2, true, 1),    // E <= 128
+    MOE_ROUTER_VARIANT(Fp32, 32, 4, 2, 2, true, 1),    // E <= 256
     MOE_ROUTER_VARIANT(Fp32, 32, 4, 3, 1, true, 1),    // E <= 384
     MOE_ROUTER_VARIANT(Fp32, 32, 4, 4, 1, true, 1),    // E <= 512
     MOE_ROUTER_VARIANT(Fp32, 32, 4, 8, 1, true, 1),    // E <= 1024

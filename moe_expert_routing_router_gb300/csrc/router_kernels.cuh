@@ -29,15 +29,28 @@
 
 namespace moe {
 
-constexpr int kConsumerWarps = 8;
+// One CTA per SM: 18 consumer warps, one producer (TMA) warp, one dispatch
+// warp -- five warps on each of the SM's four schedulers.  The consumers share
+// one ring, so a warp the scheduler favours cannot run more than the ring's
+// depth ahead of the others.  (Five warps per scheduler cap a thread at 96
+// registers.)
+constexpr int kConsumerWarps = 18;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kDispatchWarp = kConsumerWarps + 1;
 constexpr int kThreads = (kConsumerWarps + 2) * kWarp;
 constexpr int kConsumerThreads = kConsumerWarps * kWarp;
-// Warps 0..8 (consumers + producer): the CTA-level syncs from the end of the
-// forward to the start of phase C exclude the dispatch warp, whose in-CTA
-// ranking runs on through the grid barriers and the per-expert scans.
+// Consumers + producer: the CTA-level syncs from the end of the forward to the
+// start of phase C exclude the dispatch warp, whose in-CTA ranking runs on
+// through the grid barriers and the per-expert scans.
 constexpr int kMainThreads = (kConsumerWarps + 1) * kWarp;
+static_assert(kMainThreads / kWarp <= 32, "block scans hold one value per warp in 32 slots");
+// Slots of the 128-int scratch area at the start of shared memory.
+constexpr int kRedScan = 0;      // block_exclusive_scan, one int per warp
+constexpr int kRedSum = 32;      // block_sum_f, one float per warp
+constexpr int kRedProg = 64;     // forward stages finished, per consumer warp
+constexpr int kRedPhase = 96;    // 1 once grid barrier 2 has passed, -1 after an error
+constexpr int kRedFlag = 127;    // grid barrier result
+static_assert(kConsumerWarps <= 32, "progress slots");
 constexpr int kBarMain = 2;       // named barrier of the main group
 constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
 constexpr int kMaxK = 8;
@@ -87,6 +100,7 @@ struct RouterParams {
   int rows_per_stage;
   int n_slots;
   int asg_cap;                 // assignments per CTA the shared-memory dispatch buffers hold (0: none)
+  int rstat_cap;               // rows per CTA whose softmax statistics shared memory holds (0: none)
 };
 
 // Phase boundaries recorded in RouterParams::trace (lane 0 of the warp named).
@@ -104,14 +118,28 @@ enum : int {
   kTrJoined,           // warp 0: all warps joined
   kTrEnd,              // warp 0: kernel exit
   kTrRanked,           // warp 9: in-CTA dispatch ranks done
+  kTrSmId,             // the SM the CTA runs on (an id, not a time)
+  kTrFwdRowsAll,       // the last consumer warp's forward rows are done
+  kTrBwdRowsAll,       // the last consumer warp's backward rows are done
   kTracePoints = 16
 };
 
 __device__ __forceinline__ void trace_point(const RouterParams& p, int point) {
   if (p.trace != nullptr && (threadIdx.x & 31) == 0) {
-    if ((point == kTrDispatchDone || point == kTrRanked) ? threadIdx.x == kDispatchWarp * kWarp : threadIdx.x == 0)
+    if ((point == kTrDispatchDone || point == kTrRanked) ? threadIdx.x == kDispatchWarp * kWarp : threadIdx.x == 0) {
       p.trace[blockIdx.x * kTracePoints + point] = global_ns();
+      if (point == kTrStart) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        p.trace[blockIdx.x * kTracePoints + kTrSmId] = smid;
+      }
+    }
   }
+}
+
+// Latest time over the calling warps (lane 0 of each) at `point`.
+__device__ __forceinline__ void trace_last(const RouterParams& p, int point) {
+  if (p.trace != nullptr && (threadIdx.x & 31) == 0) atomicMax(&p.trace[blockIdx.x * kTracePoints + point], global_ns());
 }
 
 struct BwdParams {
@@ -127,22 +155,27 @@ struct BwdParams {
 // Shared-memory layout of the persistent kernel (byte offsets).
 // ---------------------------------------------------------------------------
 struct SmemLayout {
-  unsigned red, hist, off, rank, w, bars, asg, ring, total;
+  unsigned red, hist, off, rank, w, bars, pick, rstat, asg, ring, total;
 };
 
 __host__ __device__ inline unsigned align_to(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
 // asg_cap: capacity of the two uint16 arrays (expert id and in-CTA rank of each
 // of the CTA's assignments) that keep the dispatch in shared memory.
-__host__ __device__ inline SmemLayout router_smem_layout(int E, int n_slots, int stage_bytes, int asg_cap = 0) {
+// rstat_cap: rows of (max * log2e, 1 / sum) kept from the forward for the backward.
+// key_bytes: size of a top-k key (4 for bf16 logits, 8 for fp32).
+__host__ __device__ inline SmemLayout router_smem_layout(int E, int key_bytes, int n_slots, int stage_bytes,
+                                                         int asg_cap = 0, int rstat_cap = 0) {
   SmemLayout L;
-  L.red = 0;                                                  // 64 ints (32 doubles)
-  L.hist = 256;                                               // E ints
+  L.red = 0;                                                  // 128 ints
+  L.hist = 512;                                               // E ints
   L.off = L.hist + 4u * E;                                    // E + 1 ints
   L.rank = L.off + 4u * (E + 1);                              // E ints
   L.w = align_to(L.rank + 4u * E, 16);                        // kConsumerWarps * E words
   L.bars = align_to(L.w + 4u * kConsumerWarps * E, 16);       // 2 * kMaxSlots mbarriers
-  L.asg = L.bars + 16u * kMaxSlots;                           // 2 * asg_cap uint16
+  L.pick = L.bars + 16u * kMaxSlots;                          // kConsumerWarps * 64 keys
+  L.rstat = L.pick + unsigned(key_bytes) * 64u * kConsumerWarps;   // rstat_cap float2
+  L.asg = L.rstat + 8u * unsigned(rstat_cap);                 // 2 * asg_cap uint16
   L.ring = align_to(L.asg + 4u * unsigned(asg_cap), 128);
   L.total = L.ring + unsigned(n_slots) * unsigned(stage_bytes);
   return L;
@@ -258,38 +291,55 @@ __device__ __noinline__ void exact_topk(const typename DT::Raw* row, int E, int 
 
 // Lane-local two largest keys of one row, as a pairwise tree (short dependency
 // chains): merging sorted pairs (h1, l1) and (h2, l2) gives
-// (max(h1, h2), max(min(h1, h2), max(l1, l2))).
+// (max(h1, h2), max(min(h1, h2), l1, l2)).
+__device__ __forceinline__ int max3_key(int a, int b, int c) { return __vimax3_s32(a, b, c); }
+__device__ __forceinline__ long long max3_key(long long a, long long b, long long c) {
+  const long long m = a > b ? a : b;
+  return m > c ? m : c;
+}
+
 template <class DT, int LPR, int VW, int NV>
 __device__ __forceinline__ void lane_top2(const typename DT::Raw (&raw)[VW * NV], int l, typename DT::Key& m1,
                                           typename DT::Key& m2) {
   using Key = typename DT::Key;
   constexpr int EPL = VW * NV;
-  Key hi[EPL], lo[EPL];
+  Key key[EPL];
 #pragma unroll
   for (int v = 0; v < NV; ++v)
 #pragma unroll
-    for (int i = 0; i < VW; ++i) {
-      hi[v * VW + i] = DT::key_from_bits(DT::bits(raw[v * VW + i]), col_of<LPR, VW>(v, l, i));
-      lo[v * VW + i] = DT::kKeyMin;
-    }
+    for (int i = 0; i < VW; ++i) key[v * VW + i] = DT::key_from_bits(DT::bits(raw[v * VW + i]), col_of<LPR, VW>(v, l, i));
+  if constexpr (EPL == 1) {
+    m1 = key[0];
+    m2 = DT::kKeyMin;
+  } else {
+    constexpr int N0 = (EPL + 1) / 2;
+    Key hi[N0], lo[N0];
 #pragma unroll
-  for (int n = EPL; n > 1; n = (n + 1) / 2) {
-#pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const Key a = hi[2 * i], b = hi[2 * i + 1];
-      const Key la = lo[2 * i], lb = lo[2 * i + 1];
+    for (int i = 0; i < EPL / 2; ++i) {
+      const Key a = key[2 * i], b = key[2 * i + 1];
       hi[i] = a > b ? a : b;
-      const Key mn = a < b ? a : b;
-      const Key ml = la > lb ? la : lb;
-      lo[i] = mn > ml ? mn : ml;
+      lo[i] = a < b ? a : b;
     }
-    if (n & 1) {
-      hi[n / 2] = hi[n - 1];
-      lo[n / 2] = lo[n - 1];
+    if constexpr (EPL & 1) {
+      hi[N0 - 1] = key[EPL - 1];
+      lo[N0 - 1] = DT::kKeyMin;
     }
+#pragma unroll
+    for (int n = N0; n > 1; n = (n + 1) / 2) {
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const Key a = hi[2 * i], b = hi[2 * i + 1];
+        hi[i] = a > b ? a : b;
+        lo[i] = max3_key(a < b ? a : b, lo[2 * i], lo[2 * i + 1]);
+      }
+      if (n & 1) {
+        hi[n / 2] = hi[n - 1];
+        lo[n / 2] = lo[n - 1];
+      }
+    }
+    m1 = hi[0];
+    m2 = lo[0];
   }
-  m1 = hi[0];
-  m2 = lo[0];
 }
 
 template <int N>
@@ -306,74 +356,134 @@ __device__ __forceinline__ float tree_sum(const float (&x)[N]) {
   return t[0];
 }
 
+// Sum over the first min(LPR, 8) lanes of each row group (the owners of the k
+// <= 8 picks; every other lane passes 0).
+template <int LPR>
+__device__ __forceinline__ float owners_sum(float x) {
+#pragma unroll
+  for (int off = 1; off < (LPR < 8 ? LPR : 8); off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// Softmax statistics of one row from lane l's share: e[i] = 2^(x log2e - mL)
+// and the row sum s of e (a fixed tree per lane, then across the group).  The
+// forward and both backward paths use this one definition, so a row's p is the
+// same bits wherever it is recomputed.
+template <class DT, int LPR, int EPL>
+__device__ __forceinline__ void row_exp(const typename DT::Raw (&raw)[EPL], float mL, float (&e)[EPL]) {
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) e[i] = ex2_approx(fmaf(__uint_as_float(DT::bits(raw[i])), kLog2e, -mL));
+}
+
+// d = a * b + c, clamped to [0, 1].
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Shared-memory slots for one warp's picks: NR rows x (32 / LPR) groups x kMaxK.
+constexpr int kPickSlotsPerWarp = 64;
+
 // Forward of NR row groups of one warp at once (independent dependency chains
 // interleave): top-k rounds, softmax against the row max (the first pick),
-// gates; idx/gate stores, pick counts into s_hist, p into pacc.
+// gates; idx/gate stores, pick counts into s_hist, p into pacc.  s_pick is the
+// warp's kPickSlotsPerWarp slots.  With s_aidx the expert ids also go to this
+// CTA's shared-memory dispatch buffer (index a - a_base); with s_rstat each
+// row's (max * log2e, 1 / sum) goes to s_rstat[t - r_base] for the backward.
 template <class DT, int LPR, int VW, int NV, int NR, bool GLOBAL>
 __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename DT::Raw* const (&row)[NR],
                                            const long long (&t)[NR], const bool (&valid)[NR], int l, int* s_hist,
-                                           float (&pacc)[VW * NV], uint16_t* s_aidx, long long a_base) {
+                                           float (&pacc)[VW * NV], typename DT::Key* s_pick, uint16_t* s_aidx,
+                                           long long a_base, float2* s_rstat, long long r_base) {
   using Raw = typename DT::Raw;
   using Key = typename DT::Key;
   constexpr int EPL = VW * NV;
+  constexpr int GPW = kWarp / LPR;
+  static_assert(NR * GPW * kMaxK <= kPickSlotsPerWarp, "pick slots");
   const int k = p.k;
+  const int g = (threadIdx.x & 31) / LPR;
 
   Raw raw[NR][EPL];
   Key m1[NR], m2[NR], top[NR], mine[NR], w[NR];
-  int wins[NR];
+  float mL[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     load_lane<DT, LPR, VW, NV, GLOBAL>(row[r], p.E, l, valid[r], raw[r]);
     lane_top2<DT, LPR, VW, NV>(raw[r], l, m1[r], m2[r]);
-    top[r] = mine[r] = w[r] = DT::kKeyMin;
-    wins[r] = 0;
   }
-#pragma unroll 1
-  for (int j = 0; j < k; ++j) {
+  // Round 0 gives the row max; the exponentials are issued before the other
+  // rounds so that their latency hides behind them.  Round j's pick goes to
+  // slot j of the row group; lane l takes pick l afterwards.
+  float e[NR][EPL];
+  __syncwarp();                                    // the previous rows' picks have been read
 #pragma unroll
-    for (int r = 0; r < NR; ++r) w[r] = group_max_key<LPR>(m1[r]);
+  for (int r = 0; r < NR; ++r) {
+    w[r] = group_max_key<LPR>(m1[r]);
+    top[r] = w[r];
+    s_pick[(r * GPW + g) * kMaxK] = w[r];
+    const bool won = m1[r] == w[r];
+    m1[r] = won ? m2[r] : m1[r];
+    m2[r] = won ? DT::kKeyMin : m2[r];
+    mL[r] = DT::key_value(top[r]) * kLog2e;
+    row_exp<DT, LPR, EPL>(raw[r], mL[r], e[r]);
+  }
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      top[r] = j == 0 ? w[r] : top[r];
-      mine[r] = l == j ? w[r] : mine[r];
-      const bool won = m1[r] == w[r];
-      m1[r] = won ? m2[r] : m1[r];
-      m2[r] = won ? DT::kKeyMin : m2[r];
-      wins[r] += won ? 1 : 0;
+  for (int j = 1; j < kMaxK; ++j) {
+    if (j < k) {                                   // uniform across the warp
+#pragma unroll
+      for (int r = 0; r < NR; ++r) w[r] = group_max_key<LPR>(m1[r]);
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        s_pick[(r * GPW + g) * kMaxK + j] = w[r];
+        const bool won = m1[r] == w[r];
+        m1[r] = won ? m2[r] : m1[r];
+        m2[r] = won ? DT::kKeyMin : m2[r];
+      }
     }
   }
-  // A lane that won twice ran out of cached keys: the picks are exact unless
-  // it holds a third key above the k-th pick w (then the row is redone).
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < NR; ++r) mine[r] = l < k ? s_pick[(r * GPW + g) * kMaxK + l] : DT::kKeyMin;
+
+  // Only a lane that won twice (its cache is spent: m1 == kKeyMin) can hide an
+  // unpicked key above the k-th pick w; it does iff more than two of its keys
+  // exceed w (its picks account for at most two).  A count on the FMA pipe
+  // screens for that: every key above w has e >= e(w) and adds 1, others add
+  // at most 1, so a lane whose count stays at 2 hides nothing.  Rows that fail
+  // the screen get the exact count, and exact_topk if needed.
   bool twice = false;
 #pragma unroll
-  for (int r = 0; r < NR; ++r) twice = twice || wins[r] >= 2;
+  for (int r = 0; r < NR; ++r) twice = twice || m1[r] == DT::kKeyMin;
   if (__any_sync(0xffffffffu, twice)) {
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      int above = 0;
+      const float ew = ex2_approx(fmaf(DT::key_value(w[r]), kLog2e, -mL[r]));
+      float est = 0.f;
 #pragma unroll
-      for (int v = 0; v < NV; ++v)
+      for (int i = 0; i < EPL; ++i) est += fma_sat(e[r][i] - ew, 0x1p100f, 1.f);
+      if (__any_sync(0xffffffffu, m1[r] == DT::kKeyMin && est > 2.f)) {
+        int above = 0;
 #pragma unroll
-        for (int i = 0; i < VW; ++i)
-          above += DT::key_from_bits(DT::bits(raw[r][v * VW + i]), col_of<LPR, VW>(v, l, i)) > w[r] ? 1 : 0;
-      if (__any_sync(0xffffffffu, above > wins[r]))
-        exact_topk<DT, LPR, VW, NV, GLOBAL>(row[r], p.E, k, l, valid[r], &top[r], &mine[r]);
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int i = 0; i < VW; ++i)
+            above += DT::key_from_bits(DT::bits(raw[r][v * VW + i]), col_of<LPR, VW>(v, l, i)) > w[r] ? 1 : 0;
+        if (__any_sync(0xffffffffu, m1[r] == DT::kKeyMin && above > 2))
+          exact_topk<DT, LPR, VW, NV, GLOBAL>(row[r], p.E, k, l, valid[r], &top[r], &mine[r]);
+      }
     }
   }
 
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
-    const float mL = DT::key_value(top[r]) * kLog2e;
-    float e[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) e[i] = ex2_approx(fmaf(__uint_as_float(DT::bits(raw[r][i])), kLog2e, -mL));
-    const float s = group_sum<LPR>(tree_sum(e));
+    const float s = group_sum<LPR>(tree_sum(e[r]));
     const float inv_s = valid[r] ? rcp_approx(s) : 0.f;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) pacc[i] = fmaf(e[i], inv_s, pacc[i]);
+    for (int i = 0; i < EPL; ++i) pacc[i] = fmaf(e[r][i], inv_s, pacc[i]);
     const bool owner = l < k;
-    const float ej = owner ? ex2_approx(fmaf(DT::key_value(mine[r]), kLog2e, -mL)) : 0.f;
-    const float denom = p.renorm ? group_sum<LPR>(ej) : s;
+    const float ej = owner ? ex2_approx(fmaf(DT::key_value(mine[r]), kLog2e, -mL[r])) : 0.f;
+    const float denom = p.renorm ? owners_sum<LPR>(ej) : s;
     if (valid[r] && owner) {
       const int col = DT::key_col(mine[r]);
       const long long a = t[r] * k + l;
@@ -382,42 +492,39 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
       atomicAdd(&s_hist[col], 1);
       if (s_aidx != nullptr) s_aidx[a - a_base] = uint16_t(col);
     }
+    if (s_rstat != nullptr && valid[r] && l == 0) s_rstat[t[r] - r_base] = make_float2(mL[r], inv_s);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Backward of one row group:
 //   dlogits[t,j] = coef * p[t,j] * (f[j] - sum_i p[t,i] f[i])
+// With F = coef * f (held per lane), p = e / s and w = (1/s)^2 * sum_i e_i F_i:
+//   dlogits[t,j] = e_j * ((1/s) * F_j - w).
+// mL (max * log2e) and inv_s come from the forward (bwd_row_stats otherwise).
 // ---------------------------------------------------------------------------
 template <class DT, int LPR, int VW, int NV>
-__device__ __forceinline__ void bwd_group(const typename DT::Raw (&raw)[VW * NV], const float (&fr)[VW * NV], long long t,
-                                          bool valid, int l, int E, float coef, float* dlogits) {
+__device__ __forceinline__ void bwd_row_stats(const typename DT::Raw (&raw)[VW * NV], float& mL, float& inv_s) {
   constexpr int EPL = VW * NV;
-  float x[EPL];
   float m = -3.402823466e38f;
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    x[i] = __uint_as_float(DT::bits(raw[i]));
-    m = fmaxf(m, x[i]);
-  }
-  m = group_max<LPR>(m);
-  const float mL = m * kLog2e;
+  for (int i = 0; i < EPL; ++i) m = fmaxf(m, __uint_as_float(DT::bits(raw[i])));
+  mL = group_max<LPR>(m) * kLog2e;
   float e[EPL];
-  float s = 0.f;
+  row_exp<DT, LPR, EPL>(raw, mL, e);
+  inv_s = rcp_approx(group_sum<LPR>(tree_sum(e)));
+}
+
+template <class DT, int LPR, int VW, int NV>
+__device__ __forceinline__ void bwd_group(const typename DT::Raw (&raw)[VW * NV], const float (&Fr)[VW * NV], long long t,
+                                          bool valid, int l, int E, float mL, float inv_s, float* dlogits) {
+  constexpr int EPL = VW * NV;
+  float e[EPL];
+  row_exp<DT, LPR, EPL>(raw, mL, e);
+  float dot[EPL];
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    e[i] = ex2_approx(fmaf(x[i], kLog2e, -mL));
-    s += e[i];
-  }
-  s = group_sum<LPR>(s);
-  const float inv_s = rcp_approx(s);
-  float dot = 0.f;
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    e[i] *= inv_s;                       // p
-    dot = fmaf(e[i], fr[i], dot);
-  }
-  dot = group_sum<LPR>(dot);
+  for (int i = 0; i < EPL; ++i) dot[i] = e[i] * Fr[i];
+  const float w = inv_s * (inv_s * group_sum<LPR>(tree_sum(dot)));
   if (valid) {
     float* out = dlogits + t * (long long)E;
 #pragma unroll
@@ -426,22 +533,22 @@ __device__ __forceinline__ void bwd_group(const typename DT::Raw (&raw)[VW * NV]
       if (c0 < E) {
         float d[VW];
 #pragma unroll
-        for (int i = 0; i < VW; ++i) d[i] = coef * e[v * VW + i] * (fr[v * VW + i] - dot);
+        for (int i = 0; i < VW; ++i) d[i] = e[v * VW + i] * fmaf(inv_s, Fr[v * VW + i], -w);
         store_vec_f32<VW>(out + c0, d);
       }
     }
   }
 }
 
-// Lane l's f values (zero past E) from a shared-memory copy of f.
+// Lane l's values of coef * f (zero past E) from a shared-memory copy of f.
 template <int LPR, int VW, int NV>
-__device__ __forceinline__ void load_f(const float* s_f, int E, int l, float (&fr)[VW * NV]) {
+__device__ __forceinline__ void load_f(const float* s_f, int E, int l, float coef, float (&Fr)[VW * NV]) {
 #pragma unroll
   for (int v = 0; v < NV; ++v)
 #pragma unroll
     for (int i = 0; i < VW; ++i) {
       const int c = col_of<LPR, VW>(v, l, i);
-      fr[v * VW + i] = c < E ? s_f[c] : 0.f;
+      Fr[v * VW + i] = c < E ? coef * s_f[c] : 0.f;
     }
 }
 
@@ -693,47 +800,52 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
     if (lane == 0) *p.n_dropped = dropped;
   }
   if constexpr ((MODE & kModeFwd) != 0) {
-    const double mean = double(p.T) * k / E;
-    double fp = 0.0, dev = 0.0;
+    // Sums of f*P, of squared count deviations and the extremes.  A deviation
+    // c*E - T*k is exact in 64-bit integers; its square and the sums are fp32
+    // (positive terms, relative error well under 1e-6 at E <= 1024).
+    const long long tk = p.T * k;
+    float fp = 0.f, dev = 0.f;
     int cmax = 0, cmin = 0x7fffffff;
     for (int e = lane; e < E; e += kWarp) {
       const int c = __ldcg(p.counts + e);
-      fp += double(__ldcg(p.f + e)) * double(__ldcg(p.P + e));
-      dev += (double(c) - mean) * (double(c) - mean);
+      fp = fmaf(__ldcg(p.f + e), __ldcg(p.P + e), fp);
+      const float d = float((long long)c * E - tk);
+      dev = fmaf(d, d, dev);
       cmax = max(cmax, c);
       cmin = min(cmin, c);
     }
-    fp = warp_sum_d(fp);
-    dev = warp_sum_d(dev);
+    fp = warp_sum_f(fp);
+    dev = warp_sum_f(dev);
     cmax = __reduce_max_sync(0xffffffffu, cmax);
     cmin = __reduce_min_sync(0xffffffffu, cmin);
     const int R = p.n_ranks;
-    double rdev = 0.0;
+    float rdev = 0.f;
     int rmax = 0;
     if (R > 0) {
       const int per = E / R;
-      const double rmean = double(p.T) * k / R;
       for (int r = lane; r < R; r += kWarp) {
         int load = 0;
         for (int j = 0; j < per; ++j) load += __ldcg(p.counts + r * per + j);
         p.rank_load[r] = load;
-        rdev += (double(load) - rmean) * (double(load) - rmean);
+        const float d = float((long long)load * R - tk);
+        rdev = fmaf(d, d, rdev);
         rmax = max(rmax, load);
       }
-      rdev = warp_sum_d(rdev);
+      rdev = warp_sum_f(rdev);
       rmax = __reduce_max_sync(0xffffffffu, rmax);
     }
     if (lane == 0) {
-      const double balance = double(E) * fp;
-      p.scalars[0] = float(double(p.alpha) * balance);
-      p.scalars[1] = float(balance);
-      p.scalars[2] = float(sqrt(dev / E) / mean);
-      p.scalars[3] = float(cmax / mean);
-      p.scalars[4] = float(cmin / mean);
+      // mean = T*k/E; std/mean = sqrt(sum d^2 / E) / E / mean = sqrt(sum d^2) / (sqrt(E) * T*k)
+      const float ftk = float(tk);
+      const float balance = float(E) * fp;
+      p.scalars[0] = p.alpha * balance;
+      p.scalars[1] = balance;
+      p.scalars[2] = __fdiv_rn(__fsqrt_rn(dev), __fsqrt_rn(float(E)) * ftk);
+      p.scalars[3] = __fdiv_rn(float(cmax) * float(E), ftk);
+      p.scalars[4] = __fdiv_rn(float(cmin) * float(E), ftk);
       if (R > 0) {
-        const double rmean = double(p.T) * k / R;
-        p.scalars[5] = float(sqrt(rdev / R) / rmean);
-        p.scalars[6] = float(rmax / rmean);
+        p.scalars[5] = __fdiv_rn(__fsqrt_rn(rdev), __fsqrt_rn(float(R)) * ftk);
+        p.scalars[6] = __fdiv_rn(float(rmax) * float(R), ftk);
       } else {
         p.scalars[5] = 0.f;
         p.scalars[6] = 0.f;
@@ -812,10 +924,11 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   const int S = STAGED ? p.rows_per_stage : 1;
   const int NS = STAGED ? p.n_slots : 1;
   const int stage_elems = S * E;
-  const SmemLayout L = router_smem_layout(E, STAGED ? NS : 0, stage_elems * int(sizeof(Raw)), p.asg_cap);
+  const SmemLayout L = router_smem_layout(E, int(sizeof(typename DT::Key)), STAGED ? NS : 0, stage_elems * int(sizeof(Raw)),
+                                          p.asg_cap, p.rstat_cap);
   int* s_red = reinterpret_cast<int*>(smem + L.red);
-  int* s_prog = s_red + 40;       // stages finished per consumer warp (forward)
-  int* s_phase = s_red + 48;      // 1 once grid barrier 2 has passed, -1 after an error
+  int* s_prog = s_red + kRedProg;     // stages finished per consumer warp (forward)
+  int* s_phase = s_red + kRedPhase;   // 1 once grid barrier 2 has passed, -1 after an error
   int* s_hist = reinterpret_cast<int*>(smem + L.hist);
   int* s_off = reinterpret_cast<int*>(smem + L.off);
   int* s_rank = reinterpret_cast<int*>(smem + L.rank);
@@ -823,6 +936,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kMaxSlots;
   Raw* ring = reinterpret_cast<Raw*>(smem + L.ring);
+  typename DT::Key* s_pick_w = reinterpret_cast<typename DT::Key*>(smem + L.pick) + warp * kPickSlotsPerWarp;
 
   const long long r0 = p.T * cta / G, r1 = p.T * (cta + 1) / G;
   const long long a0 = r0 * k, a1 = r1 * k;
@@ -834,6 +948,9 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   const bool asg_smem = STAGED && (MODE & kModeFwd) != 0 && (MODE & kModeDispatch) != 0 && a1 - a0 <= p.asg_cap;
   uint16_t* s_aidx = asg_smem ? reinterpret_cast<uint16_t*>(smem + L.asg) : nullptr;
   uint16_t* s_arank = asg_smem ? s_aidx + p.asg_cap : nullptr;
+  // each row's softmax statistics from the forward, for the backward
+  float2* s_rstat = STAGED && (MODE & kModeFwd) != 0 && (MODE & kModeBwd) != 0 && r1 - r0 <= p.rstat_cap
+                        ? reinterpret_cast<float2*>(smem + L.rstat) : nullptr;
   const bool is_producer = STAGED && warp == kProducerWarp && lane == 0;
   int fills[kMaxSlots];          // copies issued per slot (producer thread), drained on an error exit
   bool ranked = true;            // dispatch warp: every in-CTA rank of this CTA has been written
@@ -866,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
         for (int s = 0; s < n_st; ++s) {
           const int q = s % NS;
           if (!mbar_wait(&full[q], (s / NS) & 1, p.timeout_ns)) {
-            atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+            ctrl_set_error(p.ctrl, kErrPipelineTimeout);
             break;
           }
           if (s == 0) trace_point(p, kTrFirstStage);
@@ -883,7 +1000,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
               rows[r] = st + (valids[r] ? ri : 0) * E;
               ts[r] = r0 + (long long)s * S + ri;
             }
-            fwd_groups<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc, s_aidx, a0);
+            fwd_groups<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, s_aidx, a0,
+                                                   s_rstat, r0);
           }
           __syncwarp();
           if (lane == 0) {
@@ -905,10 +1023,11 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
             valids[r] = ts[r] < r1;
             rows[r] = X + (valids[r] ? ts[r] : r0) * (long long)E;
           }
-          fwd_groups<DT, LPR, VW, NV, NR, true>(p, rows, ts, valids, l, s_hist, pacc, nullptr, 0);
+          fwd_groups<DT, LPR, VW, NV, NR, true>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, nullptr, 0, nullptr, 0);
         }
       }
       trace_point(p, kTrFwdRows);
+      trace_last(p, kTrFwdRowsAll);
       // Sum the row groups of the warp; group 0 stores the warp's partials.
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
@@ -929,7 +1048,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
       for (int s = 0; s < n_st; ++s) {
         const int q = s % NS;
         if (s >= NS && !mbar_wait(&empty[q], ((s / NS) - 1) & 1, p.timeout_ns)) {
-          atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+          ctrl_set_error(p.ctrl, kErrPipelineTimeout);
           break;
         }
         const int rows_here = min(S, n_rows - s * S);
@@ -957,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           }
         }
         if (!ready) {
-          if (lane == 0) atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+          if (lane == 0) ctrl_set_error(p.ctrl, kErrPipelineTimeout);
           break;
         }
         __threadfence_block();
@@ -999,7 +1118,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     }
   }
   trace_point(p, kTrFwdDone);
-  if (!grid_barrier(p.ctrl, G, p.barrier_extra, p.timeout_ns, s_red + 63, kBarMain, kMainThreads)) {
+  if (!grid_barrier(p.ctrl, G, p.barrier_extra, 1, false, p.timeout_ns, s_red + kRedFlag, kBarMain, kMainThreads)) {
     if (tid == 0) *reinterpret_cast<volatile int*>(s_phase) = -1;
     if (is_producer)   // let every issued copy land before the CTA exits
       for (int q = 0; q < NS; ++q)
@@ -1013,20 +1132,20 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     float t = 0.f;
     if constexpr ((MODE & kModeFwd) != 0)
       for (int j = tid; j < G; j += kMainThreads) t += __ldcg(p.P_part + (size_t)e * p.G_stride + j);
-    const int total = block_exclusive_scan(p.tile_hist + (size_t)e * p.G_stride, G, s_red, true);
+    const int total = block_exclusive_scan(p.tile_hist + (size_t)e * p.G_stride, G, s_red + kRedScan, true);
     if constexpr ((MODE & kModeFwd) != 0) {
-      const float Ps = block_sum_f(t, reinterpret_cast<float*>(s_red + 16));
+      const float Ps = block_sum_f(t, reinterpret_cast<float*>(s_red + kRedSum));
       if (tid == 0) {
         p.counts[e] = total;
-        p.f[e] = float(double(total) / double(p.T * k));
-        p.P[e] = float(double(Ps) / double(p.T));
+        p.f[e] = __fdiv_rn(float(total), float(p.T * k));
+        p.P[e] = __fdiv_rn(Ps, float(p.T));
       }
     } else {
       if (tid == 0) counts_dst[e] = total;
     }
   }
   trace_point(p, kTrScanDone);
-  if (!grid_barrier(p.ctrl, G, p.barrier_extra, p.timeout_ns, s_red + 63, kBarMain, kMainThreads)) {
+  if (!grid_barrier(p.ctrl, G, p.barrier_extra, 2, true, p.timeout_ns, s_red + kRedFlag, kBarMain, kMainThreads)) {
     if (tid == 0) *reinterpret_cast<volatile int*>(s_phase) = -1;
     return;
   }
@@ -1046,13 +1165,13 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     if (warp < kConsumerWarps) named_barrier(kBarConsumers, kConsumerThreads);
     if (warp < kConsumerWarps) {
       float fr[EPL];
-      load_f<LPR, VW, NV>(s_f, E, l, fr);
+      load_f<LPR, VW, NV>(s_f, E, l, coef, fr);
       if constexpr (STAGED) {
         for (int s = n_st - 1; s >= 0; --s) {
           const int q = s % NS;
           const int rel = (ring_last(q, n_st, NS) - s) / NS;     // 0: still in the ring from the forward
           if (rel > 0 && !mbar_wait(&full[q], (ring_count_a(q, n_st, NS) + rel - 1) & 1, p.timeout_ns)) {
-            atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+            ctrl_set_error(p.ctrl, kErrPipelineTimeout);
             break;
           }
           if (s == n_st - 1) trace_point(p, kTrBwdFirst);
@@ -1063,7 +1182,15 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
             const bool valid = ri < rows_here;
             Raw raw[EPL];
             load_lane<DT, LPR, VW, NV, false>(st + (valid ? ri : 0) * E, E, l, valid, raw);
-            bwd_group<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, coef, p.dlogits);
+            float mL, inv_s;
+            if (s_rstat != nullptr) {
+              const float2 rs = s_rstat[valid ? s * S + ri : 0];
+              mL = rs.x;
+              inv_s = rs.y;
+            } else {
+              bwd_row_stats<DT, LPR, VW, NV>(raw, mL, inv_s);
+            }
+            bwd_group<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, mL, inv_s, p.dlogits);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[q]);
@@ -1075,10 +1202,13 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           const bool valid = t < r1;
           Raw raw[EPL];
           load_lane<DT, LPR, VW, NV, true>(X + (valid ? t : r0) * (long long)E, E, l, valid, raw);
-          bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, E, coef, p.dlogits);
+          float mL, inv_s;
+          bwd_row_stats<DT, LPR, VW, NV>(raw, mL, inv_s);
+          bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, E, mL, inv_s, p.dlogits);
         }
       }
       trace_point(p, kTrBwdRows);
+      trace_last(p, kTrBwdRowsAll);
     } else if (is_producer) {
       const uint64_t pol = l2_policy_evict_first();
       const uint32_t row_bytes = uint32_t(E) * uint32_t(sizeof(Raw));
@@ -1086,7 +1216,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
         const int q = s % NS;
         const int rel = (ring_last(q, n_st, NS) - s) / NS;       // >= 1 here
         if (!mbar_wait(&empty[q], (ring_count_a(q, n_st, NS) + rel - 1) & 1, p.timeout_ns)) {
-          atomicOr(&p.ctrl->error, kErrPipelineTimeout);
+          ctrl_set_error(p.ctrl, kErrPipelineTimeout);
           break;
         }
         const int rows_here = min(S, n_rows - s * S);
@@ -1122,13 +1252,15 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const BwdParams p) {
   const long long nw = (long long)gridDim.x * 8;
   const Raw* X = static_cast<const Raw*>(p.logits);
   float fr[EPL];
-  load_f<LPR, VW, NV>(s_f, p.E, l, fr);
+  load_f<LPR, VW, NV>(s_f, p.E, l, p.coef, fr);
   for (long long base = gw * RPW; base < p.T; base += nw * RPW) {
     const long long t = base + g;
     const bool valid = t < p.T;
     Raw raw[EPL];
     load_lane<DT, LPR, VW, NV, true>(X + (valid ? t : 0) * (long long)p.E, p.E, l, valid, raw);
-    bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, p.E, p.coef, p.dlogits);
+    float mL, inv_s;
+    bwd_row_stats<DT, LPR, VW, NV>(raw, mL, inv_s);
+    bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, p.E, mL, inv_s, p.dlogits);
   }
 }
 

@@ -22,6 +22,6 @@ const RouterVariant* router_variants_fp32_staged(int* n);
 const RouterVariant* router_variants_fp32_direct(int* n);
 // The dispatch-only persistent kernel (compiled for kDispatchMinBlocks CTAs per SM).
 const void* dispatch_kernel();
-constexpr int kDispatchMinBlocks = 2;
+constexpr int kDispatchMinBlocks = 1;
 
 }  // namespace moe

@@ -23,7 +23,8 @@ from .api import Workspace, moe_router_fwd, moe_router_step
 POINTS = ("entry", "first forward stage landed", "forward rows done (warp 0)", "per-CTA partials published",
           "grid barrier 1 passed", "per-expert scans done", "grid barrier 2 passed", "first backward stage",
           "backward rows done (warp 0)", "dispatch + E-sized outputs done", "all warps joined", "exit",
-          "in-CTA dispatch ranks done")
+          "in-CTA dispatch ranks done", "SM id", "forward rows done (all warps)", "backward rows done (all warps)")
+SM_ID = 13
 TRACE_POINTS = 16
 MAX_CTAS = 2048
 
@@ -63,6 +64,7 @@ def phase_timeline(w, mode: str = "step", reps: int = 3) -> tuple[int, np.ndarra
     t = buf.view(-1, TRACE_POINTS).cpu().numpy().astype(np.int64)[:, :len(POINTS)]
     t = t[t[:, 0] > 0]
     rel = np.where(t > 0, (t - t[:, 0].min()) / 1000.0, np.nan)
+    rel[:, SM_ID] = t[:, SM_ID]
     return t.shape[0], rel
 
 
@@ -78,6 +80,8 @@ def main() -> int:
         G, rel = phase_timeline(w, args.mode)
         print(f"{args.mode} {name}: {G} CTAs, last exit {np.nanmax(rel[:, 11]):.2f} us")
         for i in range(1, len(POINTS)):
+            if i == SM_ID:
+                continue
             col = rel[:, i]
             if np.all(np.isnan(col)):
                 continue
