@@ -236,7 +236,8 @@ MOE_API moe_status moe_router_step_static(const void* logits, moe_dtype dt, int6
  * lambda > 0; eps <= 0 means eps = lambda; iters >= 0.
  * u, v [B,R] fp32; plan [B,R,R] fp32 or NULL; status [B] int32:
  * 0 = planned, 1 = nothing to move (no rank above the mean; u = v = plan = 0).
- * One CTA per microbatch; no workspace. */
+ * One warp per microbatch, O(R) work per iteration (M has three distinct
+ * values, so M x needs only x, its per-node sums and its total); no workspace. */
 MOE_API moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t R, int32_t ranks_per_node,
                                  float lambda, float eps, int32_t iters,
                                  float* u, float* v, float* plan, int32_t* status,

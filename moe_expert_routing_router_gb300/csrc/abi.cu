@@ -469,11 +469,16 @@ moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t R, int32
   p.R = R;
   p.ranks_per_node = ranks_per_node;
   p.iters = iters;
-  p.m_node = float(std::exp(-1.0 / e));
-  p.m_cross = float(std::exp(-double(lambda) / e));
+  const double m_node = std::exp(-1.0 / e), m_cross = std::exp(-double(lambda) / e);
+  p.m_node = float(m_node);
+  p.m_cross = float(m_cross);
+  p.c_self = float(1.0 - m_node);
+  p.c_node = float(m_node - m_cross);
+  p.c_all = float(m_cross);
   p.u = u;
   p.v = v;
   p.plan = plan;
+  p.plan_vec4 = plan != nullptr && R % 4 == 0 && reinterpret_cast<uintptr_t>(plan) % 16 == 0 ? 1 : 0;
   p.status = status;
   cudaError_t err = moe::launch_taot_sinkhorn(p, stream);
   if (err != cudaSuccess) return cuda_fail(err, "taot_sinkhorn launch");

@@ -45,7 +45,9 @@ def test_sinkhorn_parity_on_the_ep64_microbatches(mr):
 
 @pytest.mark.parametrize("R,rpn,lam,eps,iters", [(2, 1, 10.0, 0.0, 5), (16, 4, 3.0, 1.5, 50),
                                                   (37, 37, 10.0, 0.0, 20), (64, 8, 10.0, 0.0, 0),
-                                                  (64, 2, 25.0, 5.0, 200), (1, 1, 10.0, 0.0, 50)])
+                                                  (64, 2, 25.0, 5.0, 200), (1, 1, 10.0, 0.0, 50),
+                                                  (48, 6, 10.0, 0.0, 50), (64, 32, 10.0, 0.0, 50),
+                                                  (64, 64, 4.0, 0.0, 30)])
 def test_sinkhorn_shapes_and_edges(mr, R, rpn, lam, eps, iters):
     rng = np.random.default_rng(R * 31 + iters)
     B = 33
@@ -70,3 +72,19 @@ def test_sinkhorn_without_plan_output(mr):
     b = mr.taot_sinkhorn_batched(torch.from_numpy(loads).cuda(), 8, 10.0, with_plan=True)
     torch.cuda.synchronize()
     assert a["plan"] is None and torch.equal(a["u"], b["u"]) and torch.equal(a["v"], b["v"])
+
+
+def test_sinkhorn_plan_into_a_misaligned_view(mr):
+    """A plan pointer that is only 4-byte aligned takes the scalar stores."""
+    loads = np.load(LOADS)[:16].astype(np.float32)
+    B, R = loads.shape
+    x = torch.from_numpy(loads).cuda()
+    backing = torch.zeros(B * R * R + 1, dtype=torch.float32, device="cuda")
+    view = backing[1:].view(B, R, R)
+    assert view.data_ptr() % 16 != 0
+    out = {"u": torch.empty_like(x), "v": torch.empty_like(x), "plan": view,
+           "status": torch.empty(B, dtype=torch.int32, device="cuda")}
+    a = mr.taot_sinkhorn_batched(x, 8, 10.0, out=out)
+    b = mr.taot_sinkhorn_batched(x, 8, 10.0)
+    torch.cuda.synchronize()
+    assert torch.equal(a["plan"], b["plan"]) and backing[0].item() == 0.0
