@@ -23,7 +23,7 @@ namespace {
 using moe::RouterParams;
 using moe::RouterVariant;
 
-constexpr int kGridMax = 1024;                       // CTAs of the persistent kernel
+constexpr int kGridMax = moe::kGridMax;              // CTAs of the persistent kernel
 constexpr size_t kAlign = 256;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};

@@ -45,8 +45,6 @@ constexpr int kConsumerThreads = kConsumerWarps * kWarp;
 constexpr int kMainThreads = (kConsumerWarps + 1) * kWarp;
 static_assert(kMainThreads / kWarp <= 32, "block scans hold one value per warp in 32 slots");
 // Slots of the 128-int scratch area at the start of shared memory.
-constexpr int kRedScan = 0;      // block_exclusive_scan, one int per warp
-constexpr int kRedSum = 32;      // block_sum_f, one float per warp
 constexpr int kRedProg = 64;     // forward stages finished, per consumer warp
 constexpr int kRedPhase = 96;    // 1 once grid barrier 2 has passed, -1 after an error
 constexpr int kRedFlag = 127;    // grid barrier result
@@ -54,6 +52,7 @@ static_assert(kConsumerWarps <= 32, "progress slots");
 constexpr int kBarMain = 2;       // named barrier of the main group
 constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
 constexpr int kMaxK = 8;
+constexpr int kGridMax = 1024;   // CTAs of a persistent launch at most (the per-CTA partial tables' width)
 constexpr int kMaxSlots = 16;
 constexpr int kNumScalars = 7;
 // Limit of the wait for this CTA's own bulk copies before it exits; it does not
@@ -264,7 +263,7 @@ __device__ __forceinline__ void load_lane(const typename DT::Raw* row, int E, in
 // and the row is then redone by exact_topk, which rescans.
 // ---------------------------------------------------------------------------
 template <class DT, int LPR, int VW, int NV, bool GLOBAL>
-__device__ __noinline__ void exact_topk(const typename DT::Raw* row, int E, int k, int l, bool valid,
+__device__ __forceinline__ void exact_topk(const typename DT::Raw* row, int E, int k, int l, bool valid,
                                         typename DT::Key* top_out, typename DT::Key* mine_out) {
   using Key = typename DT::Key;
   constexpr int EPL = VW * NV;
@@ -428,19 +427,33 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
     mL[r] = DT::key_value(top[r]) * kLog2e;
     row_exp<DT, LPR, EPL>(raw[r], mL[r], e[r]);
   }
-#pragma unroll
-  for (int j = 1; j < kMaxK; ++j) {
-    if (j < k) {                                   // uniform across the warp
-#pragma unroll
-      for (int r = 0; r < NR; ++r) w[r] = group_max_key<LPR>(m1[r]);
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        s_pick[(r * GPW + g) * kMaxK + j] = w[r];
-        const bool won = m1[r] == w[r];
-        m1[r] = won ? m2[r] : m1[r];
-        m2[r] = won ? DT::kKeyMin : m2[r];
-      }
+  {
+    // Rounds 1 .. k - 1 in order: the switch enters the run of rounds k - 1
+    // from its end, so no round tests k.
+    Key* pk = s_pick + g * kMaxK + 1;
+#define MOE_TOPK_ROUND                                                              \
+    {                                                                               \
+      _Pragma("unroll") for (int r = 0; r < NR; ++r) w[r] = group_max_key<LPR>(m1[r]); \
+      _Pragma("unroll") for (int r = 0; r < NR; ++r) {                              \
+        pk[r * GPW * kMaxK] = w[r];                                                 \
+        const bool won = m1[r] == w[r];                                             \
+        m1[r] = won ? m2[r] : m1[r];                                                \
+        m2[r] = won ? DT::kKeyMin : m2[r];                                          \
+      }                                                                             \
+      ++pk;                                                                         \
     }
+    static_assert(kMaxK == 8, "one case per k");
+    switch (k) {
+      case 8: MOE_TOPK_ROUND [[fallthrough]];
+      case 7: MOE_TOPK_ROUND [[fallthrough]];
+      case 6: MOE_TOPK_ROUND [[fallthrough]];
+      case 5: MOE_TOPK_ROUND [[fallthrough]];
+      case 4: MOE_TOPK_ROUND [[fallthrough]];
+      case 3: MOE_TOPK_ROUND [[fallthrough]];
+      case 2: MOE_TOPK_ROUND [[fallthrough]];
+      default: break;
+    }
+#undef MOE_TOPK_ROUND
   }
   __syncwarp();
 #pragma unroll
@@ -557,62 +570,40 @@ __device__ __forceinline__ void sync_main() {
 }
 
 // ---------------------------------------------------------------------------
-// Exclusive scan of n ints in place over the main group (n <= 4 * kMainThreads);
-// returns the total.  All kMainThreads threads must call it.
+// Phase B for one expert, by one warp: the exclusive scan in place of the
+// expert's per-CTA counts col[0 .. G) (G <= kGridMax), returning the total.
+// Lane l takes the consecutive CTAs [l * per, (l + 1) * per).  With P_col the
+// per-CTA sums of p are added up as well (*Ps, in a fixed order).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int block_exclusive_scan(int* data, int n, int* s_red, bool global_src) {
-  constexpr int PER = 4;
-  constexpr int NW = kMainThreads / kWarp;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int v[PER];
+constexpr int kScanPerLane = 32;   // kGridMax / 32
+__device__ __forceinline__ int warp_expert_scan(int32_t* col, const float* P_col, int G, float* Ps) {
+  const int lane = threadIdx.x & 31;
+  const int per = (G + kWarp - 1) / kWarp;
+  const int c0 = min(lane * per, G), c1 = min(c0 + per, G);
+  int v[kScanPerLane];
+  float ps = 0.f;
   int sum = 0;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int j = tid * PER + i;
-    v[i] = j < n ? (global_src ? __ldcg(data + j) : data[j]) : 0;
-    sum += v[i];
+  for (int i = 0; i < kScanPerLane; ++i) {
+    v[i] = c0 + i < c1 ? __ldcg(col + c0 + i) : 0;
+    if (P_col != nullptr && c0 + i < c1) ps += __ldcg(P_col + c0 + i);
   }
+#pragma unroll
+  for (int i = 0; i < kScanPerLane; ++i) sum += v[i];
   int incl = sum;
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
+  for (int off = 1; off < kWarp; off <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, incl, off);
     if (lane >= off) incl += y;
   }
-  sync_main();
-  if (lane == 31) s_red[warp] = incl;
-  sync_main();
-  int warp_base = 0, total = 0;
+  int run = incl - sum;
 #pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    const int t = s_red[w];
-    warp_base += w < warp ? t : 0;
-    total += t;
-  }
-  int run = warp_base + incl - sum;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int j = tid * PER + i;
-    if (j < n) data[j] = run;
+  for (int i = 0; i < kScanPerLane; ++i) {
+    if (c0 + i < c1) col[c0 + i] = run;
     run += v[i];
   }
-  sync_main();
-  return total;
-}
-
-// Fixed-order sum of one float per thread over the main group (all call it).
-__device__ __forceinline__ float block_sum_f(float x, float* s_red) {
-  constexpr int NW = kMainThreads / kWarp;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  sync_main();
-  if (lane == 0) s_red[warp] = x;
-  sync_main();
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) t += s_red[w];
-  sync_main();
-  return t;
+  if (P_col != nullptr) *Ps = warp_sum_f(ps);
+  return __shfl_sync(0xffffffffu, incl, kWarp - 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -1127,21 +1118,23 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   }
   trace_point(p, kTrBarrier1);
 
-  // ---- phase B: experts cta, cta + G, ...
-  for (int e = cta; e < E; e += G) {
-    float t = 0.f;
-    if constexpr ((MODE & kModeFwd) != 0)
-      for (int j = tid; j < G; j += kMainThreads) t += __ldcg(p.P_part + (size_t)e * p.G_stride + j);
-    const int total = block_exclusive_scan(p.tile_hist + (size_t)e * p.G_stride, G, s_red + kRedScan, true);
-    if constexpr ((MODE & kModeFwd) != 0) {
-      const float Ps = block_sum_f(t, reinterpret_cast<float*>(s_red + kRedSum));
-      if (tid == 0) {
-        p.counts[e] = total;
-        p.f[e] = __fdiv_rn(float(total), float(p.T * k));
-        p.P[e] = __fdiv_rn(Ps, float(p.T));
+  // ---- phase B: experts cta + G * j, one warp each
+  {
+    constexpr int kMainWarps = kMainThreads / kWarp;
+    static_assert(kGridMax <= kWarp * kScanPerLane, "phase B scan width");
+    for (int e = cta + G * warp; e < E; e += G * kMainWarps) {
+      float Ps = 0.f;
+      const float* P_col = (MODE & kModeFwd) != 0 ? p.P_part + (size_t)e * p.G_stride : nullptr;
+      const int total = warp_expert_scan(p.tile_hist + (size_t)e * p.G_stride, P_col, G, &Ps);
+      if (lane == 0) {
+        if constexpr ((MODE & kModeFwd) != 0) {
+          p.counts[e] = total;
+          p.f[e] = __fdiv_rn(float(total), float(p.T * k));
+          p.P[e] = __fdiv_rn(Ps, float(p.T));
+        } else {
+          counts_dst[e] = total;
+        }
       }
-    } else {
-      if (tid == 0) counts_dst[e] = total;
     }
   }
   trace_point(p, kTrScanDone);
