@@ -188,7 +188,7 @@ struct Geometry {
 
 constexpr size_t kSmemPerSm = 228 * 1024;      // GB300 shared memory per SM
 constexpr size_t kSmemReservedPerCta = 1024;
-constexpr int kStageBytes = 24576;             // target size of one ring stage
+constexpr int kStageBytes = 65536;             // target size of one ring stage (several rows per consumer warp)
 constexpr int kMaxAsgSmem = 12288;             // assignments per CTA kept in shared memory for the dispatch
 constexpr int kMaxRowStats = 4096;             // rows per CTA whose softmax statistics stay in shared memory
 
