@@ -304,6 +304,58 @@ def time_e2e(w, steps: int, warmup: int, torch, device, dist_ctx) -> dict:
             "read_back": "scalars (L_aux, balance, CV, max/min over mean, rank CV, rank max/mean) and counts"}
 
 
+def time_calls(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
+    """The forward, backward and dispatch as separate C-ABI calls (moe_router_fwd,
+    moe_router_bwd, moe_dispatch), each a CUDA graph of `reps` calls over buffer
+    sets rotated at least 3x L2 apart, with its algorithmic bytes per call."""
+    import moe_expert_routing_router_gb300 as mr
+    esize = 2 if w.dtype == "bf16" else 4
+    T, E, k = w.T, w.E, w.k
+    nbytes = {"moe_router_fwd": T * E * esize + T * k * 8,          # logits in; idx, gate out
+              "moe_router_bwd": T * E * (esize + 4),                # logits in; dlogits out
+              "moe_dispatch": T * k * 12}                           # idx in; perm, slot out
+    x0 = to_device(synth.router_logits(w), w.dtype, torch, device)
+    ws = mr.Workspace(device)
+    ref = mr.moe_router_fwd(x0, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, ws=ws)
+    out = {}
+    for name, b in nbytes.items():
+        n_sets = max(2, math.ceil(3 * L2_BYTES / b))
+        xs = [x0] + [x0.clone() for _ in range(n_sets - 1)] if name != "moe_dispatch" else None
+        idxs = [ref["idx"].clone() for _ in range(n_sets)] if name == "moe_dispatch" else None
+        bufs = [out_buffers(w, torch, device) for _ in range(n_sets)]
+        fo = lambda i: {kk: bufs[i][kk] for kk in ("idx", "gate", "counts", "f", "P", "scalars", "rank_load")}
+        def call(i):
+            j = i % n_sets
+            if name == "moe_router_fwd":
+                mr.moe_router_fwd(xs[j], w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, ws=ws, out=fo(j))
+            elif name == "moe_router_bwd":
+                mr.moe_router_bwd(xs[j], ref["f"], w.alpha, 1.0, dlogits=bufs[j]["dlogits"])
+            else:
+                mr.moe_dispatch(idxs[j], w.E, w.capacity_factor, ws=ws,
+                                out={kk: bufs[j][kk] for kk in ("perm", "slot", "offsets", "kept", "n_dropped")})
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps):
+                call(i)
+        stream = torch.cuda.current_stream(device)
+        g.replay()
+        torch.cuda.synchronize(device)
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b2.record(stream)
+        torch.cuda.synchronize(device)
+        us = a.elapsed_time(b2) / reps * 1e3
+        gbs = b / (us * 1e-6) / 1e9
+        out[name] = {"us_per_call": round(us, 2), "algorithmic_bytes": b, "achieved_gbs": round(gbs, 1),
+                     "frac_of_hbm_peak": round(gbs / hbm_gbs, 4)}
+        del xs, idxs, bufs, g
+    return out
+
+
 def time_sinkhorn(torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     """The batched TAOT Sinkhorn call, timed as a CUDA graph of `reps` calls on
     the 1024-microbatch workload.  Its bound is the HBM write of the plan."""
@@ -506,6 +558,8 @@ def run_ours(args) -> dict:
                           "roofline_frac": round(ach / pk["hbm_gbs"], 4), "achieved_gbs": round(ach, 1),
                           "algorithmic_bytes_per_launch": rx["step_bytes"]}
         line["also"] = also
+        line["separate_calls"] = {name: time_calls(synth.ROUTER_WORKLOADS[name], torch, device, pk["hbm_gbs"])
+                                  for name in (w.name, EXTRA_WORKLOADS[-1])}
         line["sinkhorn"] = time_sinkhorn(torch, device, pk["hbm_gbs"])
     if dist_ctx.rank == 0:
         cb = time_oracle(w, budget_s=args.cpu_seconds, min_steps=2)

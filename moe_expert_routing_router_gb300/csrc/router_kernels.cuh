@@ -869,13 +869,12 @@ __device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta,
   }
   if (ph != 1 || !ranked) return;                        // an error (or a lost signal): write nothing
   __threadfence();
-  if constexpr ((MODE & kModeDispatch) != 0) {
+  if constexpr ((MODE & kModeDispatch) != 0 && (MODE & kModeFwd) != 0) {   // given idx: the consumer warps do it
     warp_offsets(counts, E, s_off);
     for (int e = lane; e < E; e += kWarp) s_rank[e] = __ldcg(p.tile_hist + (size_t)e * p.G_stride + cta);
     __syncwarp();
-    constexpr bool kRanked = STAGED || (MODE & kModeFwd) == 0;   // in-CTA ranks already computed
     if (s_aidx != nullptr) dispatch_fixup_smem(p, a0, int(a1 - a0), s_aidx, s_arank, s_off, s_rank);
-    else if constexpr (kRanked) dispatch_fixup(p, (MODE & kModeFwd) ? p.idx : p.idx_in, a0, a1, s_off, s_rank);
+    else if constexpr (STAGED) dispatch_fixup(p, p.idx, a0, a1, s_off, s_rank);
     else dispatch_direct(p, p.idx, a0, a1, s_off, s_rank);
   }
   if (finalize_here) finalize_warp<MODE>(p, counts);
@@ -953,6 +952,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     s_hist[e] = 0;
     s_rank[e] = 0;
   }
+  if constexpr ((MODE & kModeFwd) == 0)       // per-consumer-warp expert counts (dispatch of given idx)
+    for (int i = tid; i < kConsumerWarps * E; i += kThreads) reinterpret_cast<int*>(s_wf)[i] = 0;
   if (tid < kConsumerWarps) s_prog[tid] = 0;
   if (tid == 0) *s_phase = 0;
   if (STAGED && tid == 0) {
@@ -1081,13 +1082,14 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
       trace_point(p, kTrRanked);
     }
   } else {
-    if (warp == kDispatchWarp) {
-      local_ranks<kLoadInput>(p.idx_in, a0, a1, E, s_rank, p.slot);
-    } else {
-      for (long long a = a0 + tid; a < a1; a += kMainThreads) {
-        const int e = min(max(__ldg(p.idx_in + a), 0), E - 1);
-        atomicAdd(&s_hist[e], 1);
-      }
+    // Dispatch of given assignments: consumer warp w ranks the w-th contiguous
+    // chunk of this CTA's assignments (ranks within the chunk into slot[],
+    // counts per expert in its row of s_wcnt); a prefix over the warps then
+    // gives each chunk's base per expert and the CTA's counts.
+    if (warp < kConsumerWarps) {
+      const long long n = a1 - a0;
+      const long long lo = a0 + n * warp / kConsumerWarps, hi = a0 + n * (warp + 1) / kConsumerWarps;
+      local_ranks<kLoadInput>(p.idx_in, lo, hi, E, reinterpret_cast<int*>(s_wf) + warp * E, p.slot);
     }
   }
   // The producer warp is idle in phase C unless it refills the ring for the
@@ -1099,6 +1101,20 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     return;
   }
   sync_main();
+  if constexpr ((MODE & kModeFwd) == 0) {
+    int* s_wcnt = reinterpret_cast<int*>(s_wf);
+    for (int e = tid; e < E; e += kMainThreads) {
+      int tot = 0;
+#pragma unroll 1
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const int c = s_wcnt[w * E + e];
+        s_wcnt[w * E + e] = tot;
+        tot += c;
+      }
+      s_hist[e] = tot;
+    }
+    sync_main();
+  }
   for (int e = tid; e < E; e += kMainThreads) {
     p.tile_hist[(size_t)e * p.G_stride + cta] = s_hist[e];
     if constexpr ((MODE & kModeFwd) != 0) {
@@ -1150,6 +1166,25 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
 
   // ---- phase C
   if (warp == kProducerWarp && cta == 0 && !refills) finalize_warp<MODE>(p, counts_dst);
+  if constexpr ((MODE & kModeFwd) == 0) {
+    // final positions of the given assignments, chunk by chunk
+    if (warp == 0) warp_offsets(counts_dst, E, s_off);
+    for (int e = tid; e < E; e += kMainThreads) s_rank[e] = __ldcg(p.tile_hist + (size_t)e * p.G_stride + cta);
+    sync_main();
+    if (warp < kConsumerWarps) {
+      const int* s_wcnt = reinterpret_cast<const int*>(s_wf) + warp * E;
+      const long long n = a1 - a0;
+      const long long lo = a0 + n * warp / kConsumerWarps, hi = a0 + n * (warp + 1) / kConsumerWarps;
+      for (long long a = lo + lane; a < hi; a += kWarp) {
+        const int e = min(max(__ldg(p.idx_in + a), 0), E - 1);
+        const int r = s_rank[e] + s_wcnt[e] + __ldcg(p.slot + a);
+        if (r >= 0 && r < s_off[e + 1] - s_off[e]) {       // always true for consistent ranks
+          p.perm[s_off[e] + r] = int(a);
+          p.slot[a] = r < p.C ? r : -1;
+        }
+      }
+    }
+  }
   if constexpr ((MODE & kModeBwd) != 0) {
     const float coef = p.grad_scale * p.alpha * float(E) / float(p.T);
     float* s_f = s_wf;            // f, staged once per CTA (the per-warp partials are spent)
