@@ -3,12 +3,15 @@
 // stable dispatch, as one persistent cooperative kernel with grid barriers
 // between the phases, plus a plain streaming kernel for the backward alone.
 //
-// CTA organisation (kThreads = 320):
-//   warps 0..7  consumers: the per-row forward and backward math
-//   warp  8     producer: streams this CTA's contiguous chunk of logit rows
-//               into a shared-memory ring with bulk asynchronous copies (TMA)
-//   warp  9     dispatcher: stable ranks and the scatter of the dispatch, and
-//               (CTA 0) the E-sized outputs, concurrently with the backward
+// CTA organisation (one CTA per SM, kThreads = 640):
+//   warps 0..17 consumers: the per-row forward and backward math (for a
+//               dispatch of given assignments: the ranking and the scatter)
+//   warp  18    producer: streams this CTA's contiguous chunk of logit rows
+//               into a shared-memory ring with bulk asynchronous copies (TMA);
+//               in CTA 0 it writes the E-sized outputs when it has no refills
+//   warp  19    dispatcher: stable ranks of the forward's picks as they are
+//               made, their scatter during the backward, and (CTA 0, when the
+//               producer is refilling) the E-sized outputs
 //
 // Row layout.  A row of E logits is held by a group of LPR consecutive lanes
 // (LPR in {8, 16, 32}; a warp holds 32/LPR rows).  Lane l of the group owns
@@ -113,10 +116,10 @@ enum : int {
   kTrBarrier2,         // warp 0: second grid barrier passed
   kTrBwdFirst,         // warp 0: first backward stage available
   kTrBwdRows,          // warp 0: its backward rows are done
-  kTrDispatchDone,     // warp 9: dispatch (and CTA 0's E-sized outputs) done
+  kTrDispatchDone,     // dispatch warp: dispatch (and CTA 0's E-sized outputs) done
   kTrJoined,           // warp 0: all warps joined
   kTrEnd,              // warp 0: kernel exit
-  kTrRanked,           // warp 9: in-CTA dispatch ranks done
+  kTrRanked,           // dispatch warp: in-CTA dispatch ranks done
   kTrSmId,             // the SM the CTA runs on (an id, not a time)
   kTrFwdRowsAll,       // the last consumer warp's forward rows are done
   kTrBwdRowsAll,       // the last consumer warp's backward rows are done
@@ -1093,7 +1096,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     }
   }
   // The producer warp is idle in phase C unless it refills the ring for the
-  // backward; CTA 0's E-sized outputs go to whichever of warps 8 and 9 is idle.
+  // backward; CTA 0's E-sized outputs go to whichever of the producer and the
+  // dispatch warp is idle.
   const bool refills = STAGED && (MODE & kModeBwd) != 0 && n_st > NS;
   if (warp == kDispatchWarp) {
     dispatch_phase_c<MODE, STAGED>(p, cta, a0, a1, s_off, s_rank, s_phase, counts_dst, cta == 0 && refills, ranked,
@@ -1265,7 +1269,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   trace_point(p, kTrEnd);
 }
 
-// Backward alone: a plain grid-stride streaming kernel (8 warps per CTA).
+// Backward alone: a plain grid-stride streaming kernel (8 warps of 256-thread CTAs).
 template <class DT, int LPR, int VW, int NV>
 __global__ void __launch_bounds__(256) router_bwd_kernel(const BwdParams p) {
   using Raw = typename DT::Raw;
