@@ -403,12 +403,20 @@ moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_t k, dou
   int dev = 0;
   if ((s = device_info(&d, &dev)) != MOE_OK) return s;
   const void* func = moe::dispatch_kernel();
-  const size_t smem = moe::router_smem_layout(E, int(sizeof(moe::Bf16::Key)), 0, 0).total;   // a bf16 instance
+  const int kb = int(sizeof(moe::Bf16::Key));                 // a bf16 instance
+  size_t smem = moe::router_smem_layout(E, kb, 0, 0).total;
   int blocks = 0;
   if ((s = occupancy(func, moe::kThreads, smem, dev, &blocks)) != MOE_OK) return s;
   const int64_t cap = std::min<int64_t>(int64_t(blocks) * d.sms, kGridMax);
   const int64_t want = (T * k + 2047) / 2048;
   p.G = int(std::max<int64_t>(1, std::min(cap, want)));
+  // each CTA's assignments (expert id, rank within the CTA) in shared memory when they fit
+  const int64_t asg = ((T * k + p.G - 1) / p.G + 7) / 8 * 8;
+  const size_t with = moe::router_smem_layout(E, kb, 0, 0, int(std::min<int64_t>(asg, INT32_MAX))).total;
+  if (asg <= kMaxAsgSmem && with <= kSmemPerSm - kSmemReservedPerCta) {
+    p.asg_cap = int(asg);
+    smem = with;
+  }
   return launch_persistent(func, p, smem, stream);
 }
 

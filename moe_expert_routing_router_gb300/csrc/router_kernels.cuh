@@ -55,6 +55,7 @@ static_assert(kConsumerWarps <= 32, "progress slots");
 constexpr int kBarMain = 2;       // named barrier of the main group
 constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
 constexpr int kMaxK = 8;
+constexpr int kCtrlNoExpert = 1 << 16;   // above every expert id (dispatch peer matching)
 constexpr int kGridMax = 1024;   // CTAs of a persistent launch at most (the per-CTA partial tables' width)
 constexpr int kMaxSlots = 16;
 constexpr int kNumScalars = 7;
@@ -612,10 +613,10 @@ __device__ __forceinline__ int warp_expert_scan(int32_t* col, const float* P_col
 // ---------------------------------------------------------------------------
 // Dispatch.  The stable rank of assignment a = t*k + j among the assignments
 // to its expert e is  (count of e in the CTAs before this one)  +  (count of e
-// among this CTA's assignments before a).  One warp walks this CTA's
-// assignments in order, 32 at a time: lanes holding the same expert are found
-// with one ballot per bit of e, and a per-expert running count in shared
-// memory gives the in-CTA rank.  With the rows streamed through the ring this
+// among this CTA's assignments before a).  A warp walks a run of assignments
+// in order, 32 at a time: lanes holding the same expert are found with one
+// match.any, and a per-expert running count in shared memory gives the rank
+// within the run.  With the rows streamed through the ring this
 // runs during the forward, a stage behind the consumer warps, and parks the
 // in-CTA ranks in slot[]; after the global prefix is known a sync-free pass
 // turns them into final ranks and writes perm and slot.
@@ -652,11 +653,8 @@ __device__ __forceinline__ void local_ranks(const int32_t* idx_src, long long a_
       if (base + j * kWarp >= a_hi) continue;             // warp-uniform
       const bool act = base + j * kWarp + lane < a_hi;
       const int e = e_[j];
-      unsigned peers = __ballot_sync(0xffffffffu, act);  // lanes holding the same expert
-      for (int bit = 0; (1 << bit) < E; ++bit) {
-        const unsigned ones = __ballot_sync(0xffffffffu, (e >> bit) & 1);
-        peers &= ((e >> bit) & 1) ? ones : ~ones;
-      }
+      // lanes holding the same expert (an inactive lane matches only itself)
+      const unsigned peers = __match_any_sync(0xffffffffu, act ? e : E + lane);
       const int lower = __popc(peers & lt);
       r_[j] = act ? rank[e] + lower : 0;
       __syncwarp();
@@ -707,12 +705,8 @@ __device__ __forceinline__ void local_ranks_smem(const uint16_t* aidx, int lo, i
     const int a = base + lane;
     const bool act = a < hi;
     const int e = act ? aidx[a] : 0;
-    unsigned peers = __ballot_sync(0xffffffffu, act);   // lanes holding the same expert
-#pragma unroll
-    for (int bit = 0; bit < 10; ++bit) {
-      const unsigned ones = __ballot_sync(0xffffffffu, (e >> bit) & 1);
-      peers &= ((e >> bit) & 1) ? ones : ~ones;
-    }
+    // lanes holding the same expert (an inactive lane matches only itself)
+    const unsigned peers = __match_any_sync(0xffffffffu, act ? e : kCtrlNoExpert + lane);
     const int lower = __popc(peers & lt);
     const int r = act ? rank[e] + lower : 0;
     __syncwarp();
@@ -938,7 +932,9 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   const Raw* X = static_cast<const Raw*>(p.logits);
   int32_t* counts_dst = (MODE & kModeFwd) ? p.counts : p.counts_ws;
   // the CTA's dispatch in shared memory when its assignments fit
-  const bool asg_smem = STAGED && (MODE & kModeFwd) != 0 && (MODE & kModeDispatch) != 0 && a1 - a0 <= p.asg_cap;
+  // (also for a dispatch of given assignments, which loads them there)
+  const bool asg_smem = ((STAGED && (MODE & kModeFwd) != 0) || MODE == kModeDispatch) && (MODE & kModeDispatch) != 0 &&
+                        a1 - a0 <= p.asg_cap;
   uint16_t* s_aidx = asg_smem ? reinterpret_cast<uint16_t*>(smem + L.asg) : nullptr;
   uint16_t* s_arank = asg_smem ? s_aidx + p.asg_cap : nullptr;
   // each row's softmax statistics from the forward, for the backward
@@ -1086,13 +1082,36 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     }
   } else {
     // Dispatch of given assignments: consumer warp w ranks the w-th contiguous
-    // chunk of this CTA's assignments (ranks within the chunk into slot[],
-    // counts per expert in its row of s_wcnt); a prefix over the warps then
-    // gives each chunk's base per expert and the CTA's counts.
+    // chunk of this CTA's assignments (ranks within the chunk into s_arank, or
+    // slot[] when the CTA's assignments do not fit in shared memory; counts per
+    // expert in its row of s_wcnt); a prefix over the warps then gives each
+    // chunk's base per expert and the CTA's counts.
+    if (s_aidx != nullptr && warp != kDispatchWarp) {   // the CTA's expert ids, once, into shared memory
+      constexpr int kB = 8;                          // loads per thread in flight together
+      for (long long b0 = a0 + tid; b0 < a1; b0 += (long long)kB * kMainThreads) {
+        int v[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const long long a = b0 + (long long)j * kMainThreads;
+          v[j] = a < a1 ? __ldg(p.idx_in + a) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const long long a = b0 + (long long)j * kMainThreads;
+          if (a < a1) s_aidx[a - a0] = uint16_t(min(max(v[j], 0), E - 1));
+        }
+      }
+      sync_main();                                   // the main group (the dispatch warp is not in it)
+    }
+    trace_point(p, kTrFirstStage);                   // the assignments are loaded
     if (warp < kConsumerWarps) {
       const long long n = a1 - a0;
       const long long lo = a0 + n * warp / kConsumerWarps, hi = a0 + n * (warp + 1) / kConsumerWarps;
-      local_ranks<kLoadInput>(p.idx_in, lo, hi, E, reinterpret_cast<int*>(s_wf) + warp * E, p.slot);
+      int* wcnt = reinterpret_cast<int*>(s_wf) + warp * E;
+      if (s_aidx != nullptr) local_ranks_smem(s_aidx, int(lo - a0), int(hi - a0), wcnt, s_arank);
+      else local_ranks<kLoadInput>(p.idx_in, lo, hi, E, wcnt, p.slot);
+      trace_point(p, kTrFwdRows);
+      trace_last(p, kTrFwdRowsAll);
     }
   }
   // The producer warp is idle in phase C unless it refills the ring for the
@@ -1179,12 +1198,29 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
       const int* s_wcnt = reinterpret_cast<const int*>(s_wf) + warp * E;
       const long long n = a1 - a0;
       const long long lo = a0 + n * warp / kConsumerWarps, hi = a0 + n * (warp + 1) / kConsumerWarps;
-      for (long long a = lo + lane; a < hi; a += kWarp) {
-        const int e = min(max(__ldg(p.idx_in + a), 0), E - 1);
-        const int r = s_rank[e] + s_wcnt[e] + __ldcg(p.slot + a);
-        if (r >= 0 && r < s_off[e + 1] - s_off[e]) {       // always true for consistent ranks
-          p.perm[s_off[e] + r] = int(a);
-          p.slot[a] = r < p.C ? r : -1;
+      constexpr int kB = 8;                                // assignments per lane in flight together
+      for (long long b0 = lo; b0 < hi; b0 += kB * kWarp) {
+        int e_[kB], loc_[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const long long a = b0 + j * kWarp + lane;
+          if (s_aidx != nullptr) {
+            e_[j] = a < hi ? int(s_aidx[a - a0]) : 0;
+            loc_[j] = a < hi ? int(s_arank[a - a0]) : 0;
+          } else {
+            e_[j] = a < hi ? min(max(__ldg(p.idx_in + a), 0), E - 1) : 0;
+            loc_[j] = a < hi ? __ldcg(p.slot + a) : 0;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const long long a = b0 + j * kWarp + lane;
+          const int e = e_[j];
+          const int r = s_rank[e] + s_wcnt[e] + loc_[j];
+          if (a < hi && r >= 0 && r < s_off[e + 1] - s_off[e]) {   // always true for consistent ranks
+            p.perm[s_off[e] + r] = int(a);
+            p.slot[a] = r < p.C ? r : -1;
+          }
         }
       }
     }

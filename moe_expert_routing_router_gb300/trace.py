@@ -1,8 +1,8 @@
 """Phase timeline of the persistent router kernel (device timestamps per CTA).
 
-    python -m moe_expert_routing_router_gb300.trace [--mode step|fwd] WORKLOAD...
+    python -m moe_expert_routing_router_gb300.trace [--mode step|fwd|dispatch] WORKLOAD...
 
-Runs the fused step (or the forward) on a synthetic workload with the
+Runs the fused step (or the forward, or the dispatch of the forward's picks) on a synthetic workload with the
 library's phase tracing on (moe_set_trace_buffer) and prints, for each phase
 boundary, the median / min / max over CTAs of the time since the first CTA
 started.  Uses only the public ABI.
@@ -18,7 +18,7 @@ import numpy as np
 import torch
 
 from . import _native
-from .api import Workspace, moe_router_fwd, moe_router_step
+from .api import Workspace, moe_dispatch, moe_router_fwd, moe_router_step
 
 POINTS = ("entry", "first forward stage landed", "forward rows done (warp 0)", "per-CTA partials published",
           "grid barrier 1 passed", "per-expert scans done", "grid barrier 2 passed", "first backward stage",
@@ -45,9 +45,14 @@ def phase_timeline(w, mode: str = "step", reps: int = 3) -> tuple[int, np.ndarra
     if mode == "step":
         def run():
             moe_router_step(x, w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks, ws=ws)
-    else:
+    elif mode == "fwd":
         def run():
             moe_router_fwd(x, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, ws=ws)
+    else:                                          # dispatch of the forward's picks
+        idx = moe_router_fwd(x, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, ws=ws)["idx"]
+
+        def run():
+            moe_dispatch(idx, w.E, w.capacity_factor, ws=ws)
     for _ in range(3):
         run()
     torch.cuda.synchronize()
@@ -72,7 +77,7 @@ def main() -> int:
     sys.path.insert(0, str(Path(__file__).resolve().parents[1]))
     import synth
     ap = argparse.ArgumentParser()
-    ap.add_argument("--mode", choices=("step", "fwd"), default="step")
+    ap.add_argument("--mode", choices=("step", "fwd", "dispatch"), default="step")
     ap.add_argument("workloads", nargs="*", default=list(synth.ROUTER_WORKLOADS))
     args = ap.parse_args()
     for name in args.workloads:
