@@ -177,3 +177,39 @@ def test_uniform_routing_gives_unit_balance(mr):
     want = oracle_forward(z, "fp32", 1, 0.01, None, 0)
     assert abs(sc[1] - want["balance"]) <= 1e-5 * want["balance"]
     assert sc[2] == 0.0                             # CV of equal counts
+
+
+# ----------------------------------------------------------------------------- shared-memory fallbacks
+
+# Token counts past what the fused step keeps in shared memory per CTA at 152
+# CTAs: E = 256 / k = 8 with 2.4M assignments (over 12288 per CTA: the dispatch
+# ranks go through global memory), and E = 64 / k = 2 with 700k tokens (over
+# 4096 rows per CTA: the backward recomputes each row's max and sum).
+FALLBACK_CASES = [("zipf-hot-top8-T131072-E256", 300_000), ("zipf-top2-T65536-E64", 700_000)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,T", FALLBACK_CASES)
+def test_step_past_the_shared_memory_buffers(mr, name, T):
+    w, logits = workload_inputs(name, T)
+    x = to_device(logits, w.dtype)
+    st = mr.moe_router_step(x, w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks)
+    torch.cuda.synchronize()
+    want = oracle_forward(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks)
+    check_forward(st, want, w.n_ranks)
+    C = oracle.dispatch.capacity(w.T, w.k, w.E, w.capacity_factor)
+    check_dispatch(st, want["idx"], w.E, C)
+    check_backward(st["dlogits"], logits, w.dtype, want["f"], w.alpha, 1.0)
+
+
+@pytest.mark.slow
+def test_dispatch_past_the_shared_memory_buffer(mr):
+    """Given assignments over 12288 per CTA: the ranks go through global memory."""
+    rng = np.random.default_rng(11)
+    T, E, k = 300_000, 256, 8
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)   # k distinct experts per token
+    C = oracle.dispatch.capacity(T, k, E, 1.0)
+    got = mr.moe_dispatch(torch.from_numpy(idx).cuda(), E, 1.0)
+    torch.cuda.synchronize()
+    assert got["capacity"] == C
+    check_dispatch(got, idx, E, C)
