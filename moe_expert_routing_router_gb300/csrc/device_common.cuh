@@ -198,36 +198,51 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 // ---------------------------------------------------------------------------
 // Element types.  Raw is the storage word of one element; bits() gives its
-// fp32 bit pattern.  key_from_bits() is an order-preserving signed integer: a
-// larger logit gives a larger key, and of equal logits (-0.0 equals +0.0) the
-// lower column gets the larger key.
+// fp32 bit pattern.  key_from_bits(b, lane_bits, elem_bits) is an
+// order-preserving integer key of the value with bit pattern b in column
+// lane_bits | elem_bits (two disjoint bit fields: the lane's share of the
+// column and the element's): a larger logit gives a larger key, and of equal
+// logits the lower column gets the larger key.
 // ---------------------------------------------------------------------------
 struct Bf16 {
   using Raw = uint16_t;
-  using Key = int;          // 16 value bits above 16 column bits
+  // Unsigned: bit 31 set for values from +0 up, bits 16..30 the magnitude
+  // (inverted for negative values), bits 0..15 the column inverted.  Built
+  // with two instructions: a byte permute that replicates the sign into the
+  // upper half and takes the lane's column bits into the lower half, then one
+  // three-input logic op.  The one place where the key order differs from
+  // the value order is -0.0, which ranks just below +0.0; callers that must
+  // treat the two as equal check the picks with is_zero().
+  using Key = uint32_t;
+  static constexpr bool kSplitsZero = true;
   static constexpr Raw kNegInf = 0xff80u;
   static __device__ __forceinline__ uint32_t bits(Raw r) { return uint32_t(r) << 16; }
-  static __device__ __forceinline__ Key key_from_bits(uint32_t b, int col) {
-    const int v = int(b);
-    const int s = v >> 31;                        // 0, or -1 for a negative value
-    const int t = v ^ (s & 0x7fffffff);           // one's complement of negative magnitudes
-    return t - s + (0xffff - col);                // two's complement; the low 16 bits of v are zero
+  static __device__ __forceinline__ Key key_from_bits(uint32_t b, uint32_t lane_bits, uint32_t elem_bits) {
+    uint32_t s, k;
+    asm("prmt.b32 %0, %1, %2, 0xBB54;" : "=r"(s) : "r"(b), "r"(lane_bits));
+    // per bit: b ^ s where the constant is 0 (bits 16..30), s ^ c where b is 0
+    // (bits 0..15), and NOT b at bit 31 (b and s both hold the sign there)
+    asm("lop3.b32 %0, %1, %2, %3, 0x16;" : "=r"(k) : "r"(b), "r"(s), "r"(0x80000000u | (0xffffu ^ elem_bits)));
+    return k;
   }
-  static __device__ __forceinline__ int key_col(Key k) { return 0xffff - (k & 0xffff); }
+  static __device__ __forceinline__ int key_col(Key k) { return int(0xffffu ^ (k & 0xffffu)); }
   static __device__ __forceinline__ float key_value(Key k) {
-    const int v = k & int(0xffff0000u);
-    const uint32_t b = v < 0 ? (0x80000000u | uint32_t(-v)) : uint32_t(v);
-    return __uint_as_float(b);
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fff0000u) : (~k & 0xffff0000u));
   }
-  static constexpr Key kKeyMin = int(0x80000000u);
+  // +0.0 or -0.0
+  static __device__ __forceinline__ bool is_zero(Key k) { return (k >> 16) - 0x7fffu <= 1u; }
+  static __device__ __forceinline__ uint32_t canonical_zero(uint32_t b) { return b == 0x80000000u ? 0u : b; }
+  static constexpr Key kKeyMin = 0u;
 };
 
 struct Fp32 {
   using Raw = uint32_t;
-  using Key = long long;    // 32 value bits above 32 column bits
+  using Key = long long;    // signed: 32 value bits (two's complement of the magnitude) above 32 column bits
+  static constexpr bool kSplitsZero = false;
   static constexpr Raw kNegInf = 0xff800000u;
   static __device__ __forceinline__ uint32_t bits(Raw r) { return r; }
-  static __device__ __forceinline__ Key key_from_bits(uint32_t b, int col) {
+  static __device__ __forceinline__ Key key_from_bits(uint32_t b, uint32_t lane_bits, uint32_t elem_bits) {
+    const uint32_t col = lane_bits | elem_bits;
     const int v = int(b);
     const int s = v >> 31;
     const long long m = (long long)((v ^ (s & 0x7fffffff)) - s);   // two's complement of the magnitude
@@ -239,6 +254,8 @@ struct Fp32 {
     const uint32_t b = v < 0 ? (0x80000000u | uint32_t(-v)) : uint32_t(v);
     return __uint_as_float(b);
   }
+  static __device__ __forceinline__ bool is_zero(Key) { return false; }
+  static __device__ __forceinline__ uint32_t canonical_zero(uint32_t b) { return b; }
   static constexpr Key kKeyMin = (long long)0x8000000000000000ull;
 };
 
@@ -261,7 +278,7 @@ __device__ __forceinline__ float group_max(float x) {
 }
 
 template <int LPR>
-__device__ __forceinline__ int group_max_key(int x) {
+__device__ __forceinline__ uint32_t group_max_key(uint32_t x) {
   if constexpr (LPR == 32) {
     return __reduce_max_sync(0xffffffffu, x);
   } else {

@@ -232,6 +232,12 @@ __device__ __forceinline__ void store_vec_f32(float* dst, const float* src) {
 
 template <int LPR, int VW>
 __device__ __forceinline__ int col_of(int v, int l, int i) { return v * LPR * VW + l * VW + i; }
+// The two disjoint bit fields of col_of (LPR and VW are powers of two): the
+// lane's share, and the element's (a compile-time constant once unrolled).
+template <int LPR, int VW>
+__device__ __forceinline__ uint32_t col_lane_bits(int l) { return uint32_t(l * VW); }
+template <int LPR, int VW>
+__device__ __forceinline__ uint32_t col_elem_bits(int v, int i) { return uint32_t(v * LPR * VW + i); }
 
 // Lane l's EPL elements of one row.  Columns past E read as -inf (their key is
 // below every logit and their exp is 0, so the math needs no column checks);
@@ -277,7 +283,9 @@ __device__ __forceinline__ void exact_topk(const typename DT::Raw* row, int E, i
 #pragma unroll
   for (int v = 0; v < NV; ++v)
 #pragma unroll
-    for (int i = 0; i < VW; ++i) key[v * VW + i] = DT::key_from_bits(DT::bits(raw[v * VW + i]), col_of<LPR, VW>(v, l, i));
+    for (int i = 0; i < VW; ++i)
+      key[v * VW + i] = DT::key_from_bits(DT::canonical_zero(DT::bits(raw[v * VW + i])), col_lane_bits<LPR, VW>(l),
+                                          col_elem_bits<LPR, VW>(v, i));
   Key prev = DT::kKeyMin, top = DT::kKeyMin, mine = DT::kKeyMin;
   for (int j = 0; j < k; ++j) {
     Key local = DT::kKeyMin;
@@ -295,7 +303,7 @@ __device__ __forceinline__ void exact_topk(const typename DT::Raw* row, int E, i
 // Lane-local two largest keys of one row, as a pairwise tree (short dependency
 // chains): merging sorted pairs (h1, l1) and (h2, l2) gives
 // (max(h1, h2), max(min(h1, h2), l1, l2)).
-__device__ __forceinline__ int max3_key(int a, int b, int c) { return __vimax3_s32(a, b, c); }
+__device__ __forceinline__ uint32_t max3_key(uint32_t a, uint32_t b, uint32_t c) { return __vimax3_u32(a, b, c); }
 __device__ __forceinline__ long long max3_key(long long a, long long b, long long c) {
   const long long m = a > b ? a : b;
   return m > c ? m : c;
@@ -310,7 +318,8 @@ __device__ __forceinline__ void lane_top2(const typename DT::Raw (&raw)[VW * NV]
 #pragma unroll
   for (int v = 0; v < NV; ++v)
 #pragma unroll
-    for (int i = 0; i < VW; ++i) key[v * VW + i] = DT::key_from_bits(DT::bits(raw[v * VW + i]), col_of<LPR, VW>(v, l, i));
+    for (int i = 0; i < VW; ++i)
+      key[v * VW + i] = DT::key_from_bits(DT::bits(raw[v * VW + i]), col_lane_bits<LPR, VW>(l), col_elem_bits<LPR, VW>(v, i));
   if constexpr (EPL == 1) {
     m1 = key[0];
     m2 = DT::kKeyMin;
@@ -408,12 +417,13 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
   const int g = (threadIdx.x & 31) / LPR;
 
   Raw raw[NR][EPL];
-  Key m1[NR], m2[NR], top[NR], mine[NR], w[NR];
+  Key m1[NR], m2[NR], second[NR], top[NR], mine[NR], w[NR];
   float mL[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     load_lane<DT, LPR, VW, NV, GLOBAL>(row[r], p.E, l, valid[r], raw[r]);
     lane_top2<DT, LPR, VW, NV>(raw[r], l, m1[r], m2[r]);
+    second[r] = m2[r];
   }
   // Round 0 gives the row max; the exponentials are issued before the other
   // rounds so that their latency hides behind them.  Round j's pick goes to
@@ -463,32 +473,43 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
 #pragma unroll
   for (int r = 0; r < NR; ++r) mine[r] = l < k ? s_pick[(r * GPW + g) * kMaxK + l] : DT::kKeyMin;
 
-  // Only a lane that won twice (its cache is spent: m1 == kKeyMin) can hide an
-  // unpicked key above the k-th pick w; it does iff more than two of its keys
-  // exceed w (its picks account for at most two).  A count on the FMA pipe
-  // screens for that: every key above w has e >= e(w) and adds 1, others add
-  // at most 1, so a lane whose count stays at 2 hides nothing.  Rows that fail
-  // the screen get the exact count, and exact_topk if needed.
-  bool twice = false;
+  // Only a lane that won twice before the last round can hide an unpicked
+  // key above the k-th pick w (its cache is spent: m1 == kKeyMin, and its
+  // second key was not the last pick); it does iff more than two of its keys
+  // exceed w.  A count on the FMA pipe screens for that: every key above w
+  // has e >= e(w) and adds 1, others add at most 1, so a lane whose count
+  // stays at 2 hides nothing.  Rows that fail the screen get the exact count,
+  // and exact_topk if needed.  With keys that rank -0.0 below +0.0, a row
+  // whose picks include a zero is redone by exact_topk as well (the order of
+  // equal logits decides it there).
+  bool early[NR], check = false;
 #pragma unroll
-  for (int r = 0; r < NR; ++r) twice = twice || m1[r] == DT::kKeyMin;
-  if (__any_sync(0xffffffffu, twice)) {
+  for (int r = 0; r < NR; ++r) {
+    early[r] = EPL > 1 && m1[r] == DT::kKeyMin && second[r] != w[r];
+    check = check || early[r];
+    if constexpr (DT::kSplitsZero) check = check || (valid[r] && l < k && DT::is_zero(mine[r]));
+  }
+  if (__any_sync(0xffffffffu, check)) {
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      const float ew = ex2_approx(fmaf(DT::key_value(w[r]), kLog2e, -mL[r]));
-      float est = 0.f;
+      bool redo = DT::kSplitsZero && __any_sync(0xffffffffu, valid[r] && l < k && DT::is_zero(mine[r]));
+      if (!redo && __any_sync(0xffffffffu, early[r])) {
+        const float ew = ex2_approx(fmaf(DT::key_value(w[r]), kLog2e, -mL[r]));
+        float est = 0.f;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) est += fma_sat(e[r][i] - ew, 0x1p100f, 1.f);
-      if (__any_sync(0xffffffffu, m1[r] == DT::kKeyMin && est > 2.f)) {
-        int above = 0;
+        for (int i = 0; i < EPL; ++i) est += fma_sat(e[r][i] - ew, 0x1p100f, 1.f);
+        if (__any_sync(0xffffffffu, early[r] && est > 2.f)) {
+          int above = 0;
 #pragma unroll
-        for (int v = 0; v < NV; ++v)
+          for (int v = 0; v < NV; ++v)
 #pragma unroll
-          for (int i = 0; i < VW; ++i)
-            above += DT::key_from_bits(DT::bits(raw[r][v * VW + i]), col_of<LPR, VW>(v, l, i)) > w[r] ? 1 : 0;
-        if (__any_sync(0xffffffffu, m1[r] == DT::kKeyMin && above > 2))
-          exact_topk<DT, LPR, VW, NV, GLOBAL>(row[r], p.E, k, l, valid[r], &top[r], &mine[r]);
+            for (int i = 0; i < VW; ++i)
+              above += DT::key_from_bits(DT::bits(raw[r][v * VW + i]), col_lane_bits<LPR, VW>(l),
+                                         col_elem_bits<LPR, VW>(v, i)) > w[r] ? 1 : 0;
+          redo = __any_sync(0xffffffffu, early[r] && above > 2);
+        }
       }
+      if (redo) exact_topk<DT, LPR, VW, NV, GLOBAL>(row[r], p.E, k, l, valid[r], &top[r], &mine[r]);
     }
   }
 

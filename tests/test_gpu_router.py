@@ -213,3 +213,21 @@ def test_dispatch_past_the_shared_memory_buffer(mr):
     torch.cuda.synchronize()
     assert got["capacity"] == C
     check_dispatch(got, idx, E, C)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("E,k", [(64, 2), (256, 8), (384, 6), (7, 3)])
+def test_signed_zero_ties(mr, dtype, E, k):
+    """-0.0 and +0.0 are equal logits: the lower column wins between them."""
+    rng = np.random.default_rng(E * 10 + k)
+    T = 1201
+    z = rng.choice(np.array([-0.0, 0.0, -0.0, 0.0, -1.0, -2.5, 0.5]), size=(T, E)).astype(np.float32)
+    z[::7] = rng.choice(np.array([-0.0, 0.0], dtype=np.float32), size=(len(z[::7]), E))   # rows of zeros only
+    logits = z if dtype == "fp32" else synth.f32_to_bf16_bits(z)
+    x = to_device(logits, dtype)
+    st = mr.moe_router_step(x, k, 0.01, 1.0, n_ranks=0, grad_scale=1.0)
+    torch.cuda.synchronize()
+    want = oracle_forward(logits, dtype, k, 0.01, None, 0)
+    check_forward(st, want, 0)
+    check_dispatch(st, want["idx"], E, oracle.dispatch.capacity(T, k, E, 1.0))
+    check_backward(st["dlogits"], logits, dtype, want["f"], 0.01, 1.0)
