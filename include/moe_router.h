@@ -199,7 +199,7 @@ MOE_API moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, 
  * scratch memory: code running where allocation is not allowed or not safe,
  * plugins with a device-memory budget fixed at load time, or runtimes that
  * keep all device memory in their own pool.  Its scratch is a fixed array
- * inside the library image (4 MiB + 64 KiB, held by every GPU that loads the
+ * inside the library image (4.75 MiB, held by every GPU that loads the
  * library until the process exits); the call allocates nothing and frees
  * nothing.
  *   - Arguments and outputs are exactly those of moe_router_step, minus the

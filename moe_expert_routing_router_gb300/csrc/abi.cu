@@ -52,15 +52,22 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Workspace: [Ctrl][tile_hist E x kGridMax][P_part E x kGridMax][counts E]
+// Workspace: [Ctrl][group_hist][tile_hist E x kGridMax][P_part E x kGridMax][counts E].
+// The group sums must be zero when a launch starts, so they have a region of
+// their own at a fixed place and of a fixed size, whatever E: calls with
+// different E on one workspace never write into it with anything but sums
+// that their own CTA 0 clears again.
 struct WsLayout {
-  size_t ctrl = 0, tile_hist = 0, p_part = 0, counts = 0, total = 0;
+  size_t ctrl = 0, group_hist = 0, tile_hist = 0, p_part = 0, counts = 0, total = 0;
 };
+
+constexpr size_t kGroupHistBytes = size_t(moe::kGroupMax) * MOE_MAX_EXPERTS * sizeof(int32_t);
 
 WsLayout ws_layout(int E) {
   WsLayout w;
   w.ctrl = 0;
-  w.tile_hist = align_up(sizeof(moe::Ctrl));
+  w.group_hist = align_up(sizeof(moe::Ctrl));
+  w.tile_hist = w.group_hist + align_up(kGroupHistBytes);
   w.p_part = w.tile_hist + align_up(size_t(E) * kGridMax * sizeof(int32_t));
   w.counts = w.p_part + align_up(size_t(E) * kGridMax * sizeof(float));
   w.total = w.counts + align_up(size_t(E) * sizeof(int32_t));
@@ -164,6 +171,7 @@ void bind_ws(RouterParams& p, void* ws, int E) {
   char* base = static_cast<char*>(ws);
   p.ctrl = reinterpret_cast<moe::Ctrl*>(base + w.ctrl);
   p.tile_hist = reinterpret_cast<int32_t*>(base + w.tile_hist);
+  p.group_hist = reinterpret_cast<int32_t*>(base + w.group_hist);
   p.P_part = reinterpret_cast<float*>(base + w.p_part);
   p.counts_ws = reinterpret_cast<int32_t*>(base + w.counts);
   p.G_stride = kGridMax;
@@ -300,15 +308,15 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream, int32_t* flags) 
   if (!ws || !flags) return fail(MOE_ERR_INVALID, "NULL argument");
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  moe::Ctrl* c = static_cast<moe::Ctrl*>(ws);
-  unsigned long long word = 0;
-  e = cudaMemcpy(&word, &c->sync, sizeof(word), cudaMemcpyDeviceToHost);
+  moe::Ctrl c{};
+  e = cudaMemcpy(&c, ws, sizeof(moe::Ctrl), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
-  const int32_t v = int32_t(word >> 32);
+  const int32_t v = int32_t(c.sync >> 32);
   *flags = v;
   if (v != 0) {
-    // Clear the flags and the barrier state for the next call.
-    e = cudaMemset(ws, 0, sizeof(moe::Ctrl));
+    // Clear the flags, the barrier state and the failed launch's group sums
+    // for the next call.
+    e = cudaMemset(ws, 0, ws_layout(1).tile_hist);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
     return fail(MOE_ERR_TIMEOUT, "device wait expired (flags 0x%x)", unsigned(v));
   }
@@ -340,6 +348,7 @@ moe_status moe_router_fwd(const void* logits, moe_dtype dt, int64_t T, int32_t E
   Geometry geo;
   if ((s = persistent_geometry(v, dt, T, E, k, false, &geo)) != MOE_OK) return s;
   p.G = geo.G;
+  p.n_groups = (p.G + moe::kGroupCtas - 1) / moe::kGroupCtas;
   p.rows_per_stage = geo.rows_per_stage;
   p.n_slots = geo.n_slots;
   p.asg_cap = geo.asg_cap;
@@ -410,6 +419,7 @@ moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_t k, dou
   const int64_t cap = std::min<int64_t>(int64_t(blocks) * d.sms, kGridMax);
   const int64_t want = (T * k + 2047) / 2048;
   p.G = int(std::max<int64_t>(1, std::min(cap, want)));
+  p.n_groups = (p.G + moe::kGroupCtas - 1) / moe::kGroupCtas;
   // each CTA's assignments (expert id, rank within the CTA) in shared memory when they fit
   const int64_t asg = ((T * k + p.G - 1) / p.G + 7) / 8 * 8;
   const size_t with = moe::router_smem_layout(E, kb, 0, 0, int(std::min<int64_t>(asg, INT32_MAX))).total;
@@ -451,6 +461,7 @@ moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t 
   Geometry geo;
   if ((s = persistent_geometry(v, dt, T, E, k, true, &geo)) != MOE_OK) return s;
   p.G = geo.G;
+  p.n_groups = (p.G + moe::kGroupCtas - 1) / moe::kGroupCtas;
   p.rows_per_stage = geo.rows_per_stage;
   p.n_slots = geo.n_slots;
   p.asg_cap = geo.asg_cap;
@@ -535,9 +546,10 @@ int32_t moe_abi_version(void) { return MOE_ROUTER_ABI_VERSION; }
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kStaticScratchBytes = (size_t(4) << 20) + (size_t(64) << 10);   // 4 MiB + 64 KiB
+constexpr size_t kStaticScratchBytes = (size_t(4) << 20) + (size_t(768) << 10);   // 4.75 MiB
 constexpr int kStaticMaxExperts = 512;      // ws_layout(512).total fits in kStaticScratchBytes
-static_assert(kStaticScratchBytes >= 4096 + size_t(kStaticMaxExperts) * 4 * (2 * 1024 + 1), "scratch size");
+static_assert(kStaticScratchBytes >= 4096 + kGroupHistBytes + size_t(kStaticMaxExperts) * 4 * (2 * 1024 + 1),
+              "scratch size");
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
@@ -582,8 +594,9 @@ extern "C" moe_status moe_router_step_static(const void* logits, moe_dtype dt, i
   const size_t need = ws_layout(E).total;
   if (need > kStaticScratchBytes) return fail(MOE_ERR_INVALID, "E = %d needs %zu bytes of scratch", E, need);
   // The array keeps the previous call's contents; the control block (barrier
-  // state, error flags) must start at zero, the rest is written before it is read.
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(moe::Ctrl), stream);
+  // state, error flags) and the group sums must start at zero, the rest is
+  // written before it is read.
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_layout(E).tile_hist, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   return moe_router_step(logits, dt, T, E, k, alpha, renorm, n_ranks, capacity_factor, grad_scale, idx, gate, counts,
                          f, P, scalars, rank_load, perm, slot, offsets, kept, n_dropped, dlogits, ws, need, stream);

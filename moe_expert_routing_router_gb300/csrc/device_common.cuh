@@ -14,6 +14,10 @@ constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
 // ---------------------------------------------------------------------------
 // Workspace control block (first 512 bytes of the caller's workspace).
 //
+// The per-expert counts of each group of kGroupCtas consecutive CTAs are
+// accumulated with integer atomics in the workspace right after this block
+// (zero before a launch; CTA 0 clears them again at the end of the launch).
+//
 // One 64-bit word carries the grid-barrier arrival count (low half) and the
 // sticky error bits (high half), so that an arrival is a single atomic and a
 // waiter learns both "everyone is here" and "someone failed" from one load.
@@ -24,8 +28,9 @@ constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
 // sees the error at its first barrier and writes nothing.
 // ---------------------------------------------------------------------------
 struct Ctrl {
-  unsigned long long sync;   // [31:0] arrivals, [63:32] error bits
-  unsigned long long pad[63];
+  unsigned long long sync;      // [31:0] arrivals, [63:32] error bits
+  unsigned long long done;      // CTAs whose per-expert outputs are written (the launch's CTA 0 resets it)
+  unsigned long long pad[62];
 };
 static_assert(sizeof(Ctrl) == 512, "control block is 512 bytes");
 

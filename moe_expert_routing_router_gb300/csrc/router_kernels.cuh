@@ -49,14 +49,23 @@ constexpr int kMainThreads = (kConsumerWarps + 1) * kWarp;
 static_assert(kMainThreads / kWarp <= 32, "block scans hold one value per warp in 32 slots");
 // Slots of the 128-int scratch area at the start of shared memory.
 constexpr int kRedProg = 64;     // forward stages finished, per consumer warp
-constexpr int kRedPhase = 96;    // 1 once grid barrier 2 has passed, -1 after an error
+constexpr int kRedPhase = 96;    // 1 once the grid barrier has passed, 2 once this CTA's totals, bases and
+                                 // offsets are in shared memory, -1 after an error
+constexpr int kRedRanked = 97;   // 1 once the dispatch warp has ranked every pick of the CTA, -1 if it gave up
+constexpr int kRedFixNext = 98;  // next chunk of the CTA's final dispatch positions to write
 constexpr int kRedFlag = 127;    // grid barrier result
 static_assert(kConsumerWarps <= 32, "progress slots");
 constexpr int kBarMain = 2;       // named barrier of the main group
 constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
 constexpr int kMaxK = 8;
+// The final dispatch positions of a CTA's picks are written in chunks of this
+// many assignments: by the dispatch warp while the consumers run the backward,
+// and by the consumers that have finished it.
+constexpr int kFixupChunk = 256;
 constexpr int kCtrlNoExpert = 1 << 16;   // above every expert id (dispatch peer matching)
 constexpr int kGridMax = 1024;   // CTAs of a persistent launch at most (the per-CTA partial tables' width)
+constexpr int kGroupCtas = 8;    // CTAs per group of the per-group count sums
+constexpr int kGroupMax = kGridMax / kGroupCtas;
 constexpr int kMaxSlots = 16;
 constexpr int kNumScalars = 7;
 // Limit of the wait for this CTA's own bulk copies before it exits; it does not
@@ -91,10 +100,12 @@ struct RouterParams {
   int32_t* n_dropped;          // [1]
   // workspace
   Ctrl* ctrl;
-  int32_t* tile_hist;          // [E][G_stride]: per-CTA counts, then their exclusive prefix over CTAs
+  int32_t* tile_hist;          // [E][G_stride]: per-CTA counts
+  int32_t* group_hist;         // [n_groups][E]: per-group counts (atomics; zero between launches)
   float* P_part;               // [E][G_stride]: per-CTA sums of p
   int32_t* counts_ws;          // [E] counts when `counts` is not an output
   int G;                       // CTAs in the grid
+  int n_groups;                // ceil(G / kGroupCtas)
   int G_stride;
   unsigned long long timeout_ns;
   unsigned barrier_extra;      // 0; 1 makes every grid barrier unreachable (timeout tests)
@@ -113,8 +124,8 @@ enum : int {
   kTrFwdRows,          // warp 0: its forward rows are done
   kTrFwdDone,          // warp 0: per-CTA counts and sums of p published
   kTrBarrier1,         // warp 0: first grid barrier passed
-  kTrScanDone,         // warp 0: per-expert scans done
-  kTrBarrier2,         // warp 0: second grid barrier passed
+  kTrScanDone,         // warp 0: totals, this CTA's bases and the offsets are in shared memory
+  kTrBarrier2,         // (not recorded)
   kTrBwdFirst,         // warp 0: first backward stage available
   kTrBwdRows,          // warp 0: its backward rows are done
   kTrDispatchDone,     // dispatch warp: dispatch (and CTA 0's E-sized outputs) done
@@ -595,40 +606,77 @@ __device__ __forceinline__ void sync_main() {
 }
 
 // ---------------------------------------------------------------------------
-// Phase B for one expert, by one warp: the exclusive scan in place of the
-// expert's per-CTA counts col[0 .. G) (G <= kGridMax), returning the total.
-// Lane l takes the consecutive CTAs [l * per, (l + 1) * per).  With P_col the
-// per-CTA sums of p are added up as well (*Ps, in a fixed order).
+// The sum over the G CTAs of one expert's per-CTA sums of p, by one warp, in a
+// fixed order: lane l adds the consecutive CTAs [l * per, (l + 1) * per), then
+// the lanes are added pairwise.
 // ---------------------------------------------------------------------------
-constexpr int kScanPerLane = 32;   // kGridMax / 32
-__device__ __forceinline__ int warp_expert_scan(int32_t* col, const float* P_col, int G, float* Ps) {
+constexpr int kColPerLane = 32;   // kGridMax / 32
+__device__ __forceinline__ float warp_column_sum_f(const float* col, int G) {
+  static_assert(kGridMax <= kWarp * kColPerLane, "column width");
   const int lane = threadIdx.x & 31;
   const int per = (G + kWarp - 1) / kWarp;
   const int c0 = min(lane * per, G), c1 = min(c0 + per, G);
-  int v[kScanPerLane];
-  float ps = 0.f;
-  int sum = 0;
+  float v[kColPerLane];
 #pragma unroll
-  for (int i = 0; i < kScanPerLane; ++i) {
-    v[i] = c0 + i < c1 ? __ldcg(col + c0 + i) : 0;
-    if (P_col != nullptr && c0 + i < c1) ps += __ldcg(P_col + c0 + i);
+  for (int i = 0; i < kColPerLane; ++i) v[i] = c0 + i < c1 ? __ldcg(col + c0 + i) : 0.f;
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kColPerLane; ++i) s += v[i];
+  return warp_sum_f(s);
+}
+
+// Per-expert totals and this CTA's dispatch bases (the counts of the CTAs
+// before it), by the main group: S consecutive lanes share an expert (S the
+// largest power of two up to 32 with E * S <= kMainThreads), each reads its
+// share of the expert's group sums and of the counts of this CTA's
+// predecessors within its group (all loads in flight together), and the S
+// partial sums are added by shuffles.  Writes total[e] and base[e] for every
+// expert; the caller syncs the main group.
+__device__ __forceinline__ void totals_and_bases(const RouterParams& p, int cta, int* total, int* base) {
+  const int E = p.E, tid = threadIdx.x;
+  const int grp = cta / kGroupCtas;
+  const int n_pre = cta - grp * kGroupCtas;            // predecessors within the group
+  const int n_items = p.n_groups + n_pre;              // per expert: group sums, then predecessors
+  int S = 32;
+  while (S > 1 && E * S > kMainThreads) S >>= 1;
+  const int s = tid & (S - 1);
+  constexpr int kB = 8;
+  static_assert(kMainThreads % kWarp == 0, "whole warps");
+  const int per_trip = kMainThreads / S;               // experts per trip (S divides kMainThreads)
+  const int trips = (E + per_trip - 1) / per_trip;     // the same for every thread: the shuffles need whole warps
+  for (int r = 0; r < trips; ++r) {
+    const int e = r * per_trip + tid / S;
+    const bool on = e < E;
+    int tot = 0, pre = 0;
+    for (int i0 = s; i0 < n_items; i0 += kB * S) {
+      int v[kB];
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int i = i0 + j * S;
+        v[j] = 0;
+        if (on && i < p.n_groups) v[j] = __ldcg(p.group_hist + (size_t)i * E + e);
+        else if (on && i < n_items) v[j] = __ldcg(p.tile_hist + (size_t)e * p.G_stride + grp * kGroupCtas + (i - p.n_groups));
+      }
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int i = i0 + j * S;
+        if (i < p.n_groups) {
+          tot += v[j];
+          pre += i < grp ? v[j] : 0;
+        } else {
+          pre += v[j];
+        }
+      }
+    }
+    for (int o = 1; o < S; o <<= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    }
+    if (on && s == 0) {
+      total[e] = tot;
+      base[e] = pre;
+    }
   }
-#pragma unroll
-  for (int i = 0; i < kScanPerLane; ++i) sum += v[i];
-  int incl = sum;
-#pragma unroll
-  for (int off = 1; off < kWarp; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += y;
-  }
-  int run = incl - sum;
-#pragma unroll
-  for (int i = 0; i < kScanPerLane; ++i) {
-    if (c0 + i < c1) col[c0 + i] = run;
-    run += v[i];
-  }
-  if (P_col != nullptr) *Ps = warp_sum_f(ps);
-  return __shfl_sync(0xffffffffu, incl, kWarp - 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -770,13 +818,14 @@ __device__ __forceinline__ void dispatch_direct(const RouterParams& p, const int
   }
 }
 
-// Exclusive scan of counts[0..E) into off[0..E] (shared or global) by one warp.
-__device__ __forceinline__ void warp_offsets(const int32_t* counts, int E, int* off) {
+// Exclusive scan of src[0..E) (shared memory) into dst[0..E], dst[E] = the
+// total, by one warp; dst may be src.  Lane l takes a contiguous run.
+__device__ __forceinline__ void warp_exclusive_scan(const int* src, int E, int* dst) {
   const int lane = threadIdx.x & 31;
   const int per = (E + 31) / 32;
   const int lo = min(lane * per, E), hi = min(lo + per, E);
   int sum = 0;
-  for (int e = lo; e < hi; ++e) sum += __ldcg(counts + e);
+  for (int e = lo; e < hi; ++e) sum += src[e];
   int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -785,44 +834,65 @@ __device__ __forceinline__ void warp_offsets(const int32_t* counts, int E, int* 
   }
   int run = incl - sum;
   for (int e = lo; e < hi; ++e) {
-    off[e] = run;
-    run += __ldcg(counts + e);
+    const int c = src[e];
+    dst[e] = run;
+    run += c;
   }
-  if (lane == 31) off[E] = incl;
+  if (lane == 31) dst[E] = incl;
   __syncwarp();
 }
 
-// The E-sized outputs, by one warp of CTA 0.
+// The E-sized outputs, by one warp of CTA 0.  The counts (and f, P) are read
+// in batches of eight loads per lane in flight, and the counts kept in the
+// shared-memory scratch s_cnt[0..E) for the offsets and the rank loads.
 template <int MODE>
-__device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32_t* counts) {
+__device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32_t* counts, int* s_cnt) {
   const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
-  if constexpr ((MODE & kModeDispatch) != 0) {
-    warp_offsets(counts, E, p.offsets);
-    int dropped = 0;
-    for (int e = lane; e < E; e += kWarp) {
-      const int c = __ldcg(counts + e);
-      p.kept[e] = min(c, p.C);
-      dropped += max(c - p.C, 0);
+  constexpr bool kFwd = (MODE & kModeFwd) != 0, kDisp = (MODE & kModeDispatch) != 0;
+  // Sums of f*P, of squared count deviations and the extremes.  A deviation
+  // c*E - T*k is exact in 64-bit integers; its square and the sums are fp32
+  // (positive terms, relative error well under 1e-6 at E <= 1024).
+  const long long tk = p.T * k;
+  float fp = 0.f, dev = 0.f;
+  int cmax = 0, cmin = 0x7fffffff, dropped = 0;
+  constexpr int kB = 8;
+  for (int e0 = 0; e0 < E; e0 += kB * kWarp) {
+    int c[kB];
+    float fv[kB], pv[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int e = e0 + j * kWarp + lane;
+      c[j] = e < E ? __ldcg(counts + e) : 0;
+      fv[j] = kFwd && e < E ? __ldcg(p.f + e) : 0.f;
+      pv[j] = kFwd && e < E ? __ldcg(p.P + e) : 0.f;
     }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int e = e0 + j * kWarp + lane;
+      if (e < E) {
+        s_cnt[e] = c[j];
+        if constexpr (kDisp) {
+          p.kept[e] = min(c[j], p.C);
+          dropped += max(c[j] - p.C, 0);
+        }
+        if constexpr (kFwd) {
+          fp = fmaf(fv[j], pv[j], fp);
+          const float d = float((long long)c[j] * E - tk);
+          dev = fmaf(d, d, dev);
+          cmax = max(cmax, c[j]);
+          cmin = min(cmin, c[j]);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  if constexpr (kDisp) {
+    warp_exclusive_scan(s_cnt, E, p.offsets);
     dropped = __reduce_add_sync(0xffffffffu, dropped);
     if (lane == 0) *p.n_dropped = dropped;
   }
-  if constexpr ((MODE & kModeFwd) != 0) {
-    // Sums of f*P, of squared count deviations and the extremes.  A deviation
-    // c*E - T*k is exact in 64-bit integers; its square and the sums are fp32
-    // (positive terms, relative error well under 1e-6 at E <= 1024).
-    const long long tk = p.T * k;
-    float fp = 0.f, dev = 0.f;
-    int cmax = 0, cmin = 0x7fffffff;
-    for (int e = lane; e < E; e += kWarp) {
-      const int c = __ldcg(p.counts + e);
-      fp = fmaf(__ldcg(p.f + e), __ldcg(p.P + e), fp);
-      const float d = float((long long)c * E - tk);
-      dev = fmaf(d, d, dev);
-      cmax = max(cmax, c);
-      cmin = min(cmin, c);
-    }
+  if constexpr (kFwd) {
     fp = warp_sum_f(fp);
     dev = warp_sum_f(dev);
     cmax = __reduce_max_sync(0xffffffffu, cmax);
@@ -834,7 +904,7 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
       const int per = E / R;
       for (int r = lane; r < R; r += kWarp) {
         int load = 0;
-        for (int j = 0; j < per; ++j) load += __ldcg(p.counts + r * per + j);
+        for (int j = 0; j < per; ++j) load += s_cnt[r * per + j];
         p.rank_load[r] = load;
         const float d = float((long long)load * R - tk);
         rdev = fmaf(d, d, rdev);
@@ -864,38 +934,118 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
 }
 
 // ---------------------------------------------------------------------------
-// The dispatch warp after the forward: waits (bounded) until grid barrier 2 has
-// passed for this CTA, then turns the in-CTA ranks into final positions and,
-// in CTA 0 when the producer warp is busy with refills, writes the E-sized
-// outputs.
+// CTA 0, one warp: waits (bounded) until every CTA of the launch has counted
+// itself done (its per-expert outputs are written and it has read the group
+// sums), clears the group sums and the count for the next launch, and writes
+// the E-sized outputs.
 // ---------------------------------------------------------------------------
-template <int MODE, bool STAGED>
-__device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta, long long a0, long long a1, int* s_off,
-                                                 int* s_rank, int* s_phase, const int32_t* counts, bool finalize_here,
-                                                 bool ranked, const uint16_t* s_aidx, const uint16_t* s_arank) {
+template <int MODE>
+__device__ __forceinline__ void finalize_after_all(const RouterParams& p, const int32_t* counts, int* s_cnt) {
   const int lane = threadIdx.x & 31;
-  const int E = p.E;
+  int ok = 1;
+  if (lane == 0) {
+    uint64_t t0 = 0;
+    for (unsigned spin = 0;; ++spin) {
+      if (ld_acquire_u64(&p.ctrl->done) >= (unsigned long long)p.G) break;
+      if ((spin & 15u) == 15u) {
+        if ((ld_acquire_u64(&p.ctrl->sync) >> 32) != 0) {   // another CTA failed: its outputs are missing
+          ok = 0;
+          break;
+        }
+        const uint64_t now = global_ns();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > p.timeout_ns) {
+          ctrl_set_error(p.ctrl, kErrBarrierTimeout);
+          ok = 0;
+          break;
+        }
+      }
+      __nanosleep(64);
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  if (!ok) return;
+  const int n = p.n_groups * p.E;
+  for (int i = lane; i < n; i += kWarp) p.group_hist[i] = 0;
+  if (lane == 0) p.ctrl->done = 0ull;
+  finalize_warp<MODE>(p, counts, s_cnt);
+}
+
+// ---------------------------------------------------------------------------
+// The dispatch warp after the forward: once grid barrier 1 has passed (bounded
+// wait) it adds up the per-CTA sums of p of this CTA's experts (e = cta mod
+// G), counts the CTA done once the CTA's totals and bases are in shared memory,
+// turns the in-CTA ranks into final positions (unless the consumer warps do
+// that: fixup_here false) and, in CTA 0 when the producer warp is busy with
+// refills, writes the E-sized outputs (shared-memory scratch s_cnt).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int wait_phase(const RouterParams& p, const int* s_phase, int at_least) {
   int ph = 0;
   uint64_t t0 = 0;
-  for (unsigned spin = 0; (ph = *reinterpret_cast<volatile int*>(s_phase)) == 0; ++spin) {
+  for (unsigned spin = 0; (ph = *reinterpret_cast<const volatile int*>(s_phase)) >= 0 && ph < at_least; ++spin) {
     if ((spin & 15u) == 15u) {
       const uint64_t now = global_ns();
       if (t0 == 0) t0 = now;
-      else if (now - t0 > p.timeout_ns) break;
+      else if (now - t0 > p.timeout_ns) return -1;
     }
     __nanosleep(64);
   }
-  if (ph != 1 || !ranked) return;                        // an error (or a lost signal): write nothing
-  __threadfence();
-  if constexpr ((MODE & kModeDispatch) != 0 && (MODE & kModeFwd) != 0) {   // given idx: the consumer warps do it
-    warp_offsets(counts, E, s_off);
-    for (int e = lane; e < E; e += kWarp) s_rank[e] = __ldcg(p.tile_hist + (size_t)e * p.G_stride + cta);
-    __syncwarp();
-    if (s_aidx != nullptr) dispatch_fixup_smem(p, a0, int(a1 - a0), s_aidx, s_arank, s_off, s_rank);
-    else if constexpr (STAGED) dispatch_fixup(p, p.idx, a0, a1, s_off, s_rank);
-    else dispatch_direct(p, p.idx, a0, a1, s_off, s_rank);
+  return ph;
+}
+
+// Final dispatch positions of the CTA's picks [a0, a0 + n) in chunks of
+// kFixupChunk taken from the shared counter *s_next, by one warp; every warp
+// that calls it takes chunks until none are left.
+__device__ __forceinline__ void fixup_chunks(const RouterParams& p, long long a0, int n, const uint16_t* s_aidx,
+                                             const uint16_t* s_arank, const int* s_off, const int* s_base, int* s_next) {
+  const int lane = threadIdx.x & 31;
+  const int n_chunks = (n + kFixupChunk - 1) / kFixupChunk;
+  for (;;) {
+    int c = 0;
+    if (lane == 0) c = atomicAdd(s_next, 1);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    if (c >= n_chunks) break;
+    const int lo = c * kFixupChunk, len = min(kFixupChunk, n - lo);
+    dispatch_fixup_smem(p, a0 + lo, len, s_aidx + lo, s_arank + lo, s_off, s_base);
   }
-  if (finalize_here) finalize_warp<MODE>(p, counts);
+}
+
+template <int MODE, bool STAGED>
+__device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta, long long a0, long long a1, int* s_coff,
+                                                 int* s_cbase, int* s_phase, const int32_t* counts, bool finalize_here,
+                                                 bool ranked, const uint16_t* s_aidx, const uint16_t* s_arank, int* s_cnt,
+                                                 int* s_next) {
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+  if (wait_phase(p, s_phase, 1) < 1) return;            // an error (or a lost signal): write nothing
+  if constexpr ((MODE & kModeFwd) != 0) {
+    for (int e = cta; e < E; e += p.G) {
+      const float Ps = warp_column_sum_f(p.P_part + (size_t)e * p.G_stride, p.G);
+      if (lane == 0) p.P[e] = __fdiv_rn(Ps, float(p.T));
+    }
+  }
+  if (wait_phase(p, s_phase, 2) < 2) return;
+  if (lane == 0) {
+    __threadfence();
+    atomicAdd(&p.ctrl->done, 1ull);
+  }
+  __syncwarp();
+  if constexpr ((MODE & kModeDispatch) != 0 && (MODE & kModeFwd) != 0) {   // given idx: the consumer warps do it
+    warp_exclusive_scan(s_coff, E, s_coff);             // totals -> offsets
+    if (lane == 0) {
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(s_phase) = ranked ? 3 : 4;   // 3: the consumers may help with the chunks
+    }
+    __syncwarp();
+    if (ranked) {
+      if (s_aidx != nullptr) fixup_chunks(p, a0, int(a1 - a0), s_aidx, s_arank, s_coff, s_cbase, s_next);
+      else if constexpr (STAGED) dispatch_fixup(p, p.idx, a0, a1, s_coff, s_cbase);
+      else dispatch_direct(p, p.idx, a0, a1, s_coff, s_cbase);
+    }
+  }
+  if (finalize_here) finalize_after_all<MODE>(p, counts, s_cnt);
   trace_point(p, kTrDispatchDone);
 }
 
@@ -936,7 +1086,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
                                           p.asg_cap, p.rstat_cap);
   int* s_red = reinterpret_cast<int*>(smem + L.red);
   int* s_prog = s_red + kRedProg;     // stages finished per consumer warp (forward)
-  int* s_phase = s_red + kRedPhase;   // 1 once grid barrier 2 has passed, -1 after an error
+  int* s_phase = s_red + kRedPhase;
+  int* s_ranked = s_red + kRedRanked;
   int* s_hist = reinterpret_cast<int*>(smem + L.hist);
   int* s_off = reinterpret_cast<int*>(smem + L.off);
   int* s_rank = reinterpret_cast<int*>(smem + L.rank);
@@ -964,6 +1115,11 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   const bool is_producer = STAGED && warp == kProducerWarp && lane == 0;
   int fills[kMaxSlots];          // copies issued per slot (producer thread), drained on an error exit
   bool ranked = true;            // dispatch warp: every in-CTA rank of this CTA has been written
+  // small CTAs: the consumers write the final dispatch positions, before the backward
+  // the fused step's final dispatch positions: shared by the dispatch warp and
+  // the consumers that are done with the backward, when the picks are in
+  // shared memory
+  const bool share_fixup = s_aidx != nullptr && (MODE & kModeFwd) != 0 && (MODE & kModeBwd) != 0;
 #pragma unroll
   for (int q = 0; q < kMaxSlots; ++q) fills[q] = 0;
 
@@ -975,7 +1131,11 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   if constexpr ((MODE & kModeFwd) == 0)       // per-consumer-warp expert counts (dispatch of given idx)
     for (int i = tid; i < kConsumerWarps * E; i += kThreads) reinterpret_cast<int*>(s_wf)[i] = 0;
   if (tid < kConsumerWarps) s_prog[tid] = 0;
-  if (tid == 0) *s_phase = 0;
+  if (tid == 0) {
+    *s_phase = 0;
+    *s_ranked = 0;
+    s_red[kRedFixNext] = 0;
+  }
   if (STAGED && tid == 0) {
     for (int q = 0; q < NS; ++q) {
       mbar_init(&full[q], 1);
@@ -1099,6 +1259,10 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
         if (s == n_st - 1) ranked = true;
       }
       if (n_st == 0) ranked = true;
+      if (lane == 0) {
+        __threadfence_block();                       // the ranks before the flag
+        *reinterpret_cast<volatile int*>(s_ranked) = ranked ? 1 : -1;
+      }
       trace_point(p, kTrRanked);
     }
   } else {
@@ -1139,9 +1303,16 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   // backward; CTA 0's E-sized outputs go to whichever of the producer and the
   // dispatch warp is idle.
   const bool refills = STAGED && (MODE & kModeBwd) != 0 && n_st > NS;
+  // Phase C shared memory: per expert f, the total (then the offsets) and this
+  // CTA's base.  With the forward they take the per-warp partials' space, which
+  // is spent after the publication below; a dispatch of given assignments
+  // keeps its per-warp counts there and uses the offset and rank arrays.
+  float* s_f = s_wf;
+  int* s_coff = (MODE & kModeFwd) != 0 ? reinterpret_cast<int*>(s_wf + E) : s_off;
+  int* s_cbase = (MODE & kModeFwd) != 0 ? s_coff + E + 1 : s_rank;
   if (warp == kDispatchWarp) {
-    dispatch_phase_c<MODE, STAGED>(p, cta, a0, a1, s_off, s_rank, s_phase, counts_dst, cta == 0 && refills, ranked,
-                                   s_aidx, s_arank);
+    dispatch_phase_c<MODE, STAGED>(p, cta, a0, a1, s_coff, s_cbase, s_phase, counts_dst, cta == 0 && refills,
+                                   ranked, s_aidx, s_arank, s_hist, s_red + kRedFixNext);
     return;
   }
   sync_main();
@@ -1159,62 +1330,63 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     }
     sync_main();
   }
-  for (int e = tid; e < E; e += kMainThreads) {
-    p.tile_hist[(size_t)e * p.G_stride + cta] = s_hist[e];
-    if constexpr ((MODE & kModeFwd) != 0) {
-      float t = 0.f;
+  // Publish this CTA's counts (per CTA, and into its group's sums) and sums of p.
+  {
+    int32_t* grp_hist = p.group_hist + (size_t)(cta / kGroupCtas) * E;
+    for (int e = tid; e < E; e += kMainThreads) {
+      const int c = s_hist[e];
+      p.tile_hist[(size_t)e * p.G_stride + cta] = c;
+      if (c != 0) atomicAdd(grp_hist + e, c);
+      if constexpr ((MODE & kModeFwd) != 0) {
+        float t = 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) t += s_wf[w * E + e];
-      p.P_part[(size_t)e * p.G_stride + cta] = t;
+        for (int w = 0; w < kConsumerWarps; ++w) t += s_wf[w * E + e];
+        p.P_part[(size_t)e * p.G_stride + cta] = t;
+      }
     }
   }
   trace_point(p, kTrFwdDone);
-  if (!grid_barrier(p.ctrl, G, p.barrier_extra, 1, false, p.timeout_ns, s_red + kRedFlag, kBarMain, kMainThreads)) {
+  if (!grid_barrier(p.ctrl, G, p.barrier_extra, 1, true, p.timeout_ns, s_red + kRedFlag, kBarMain, kMainThreads)) {
     if (tid == 0) *reinterpret_cast<volatile int*>(s_phase) = -1;
     if (is_producer)   // let every issued copy land before the CTA exits
       for (int q = 0; q < NS; ++q)
         if (fills[q] > 0) mbar_wait(&full[q], (fills[q] - 1) & 1, kDrainNs);
     return;
   }
-  trace_point(p, kTrBarrier1);
-
-  // ---- phase B: experts cta + G * j, one warp each
-  {
-    constexpr int kMainWarps = kMainThreads / kWarp;
-    static_assert(kGridMax <= kWarp * kScanPerLane, "phase B scan width");
-    for (int e = cta + G * warp; e < E; e += G * kMainWarps) {
-      float Ps = 0.f;
-      const float* P_col = (MODE & kModeFwd) != 0 ? p.P_part + (size_t)e * p.G_stride : nullptr;
-      const int total = warp_expert_scan(p.tile_hist + (size_t)e * p.G_stride, P_col, G, &Ps);
-      if (lane == 0) {
-        if constexpr ((MODE & kModeFwd) != 0) {
-          p.counts[e] = total;
-          p.f[e] = __fdiv_rn(float(total), float(p.T * k));
-          p.P[e] = __fdiv_rn(Ps, float(p.T));
-        } else {
-          counts_dst[e] = total;
-        }
-      }
-    }
-  }
-  trace_point(p, kTrScanDone);
-  if (!grid_barrier(p.ctrl, G, p.barrier_extra, 2, true, p.timeout_ns, s_red + kRedFlag, kBarMain, kMainThreads)) {
-    if (tid == 0) *reinterpret_cast<volatile int*>(s_phase) = -1;
-    return;
-  }
   if (tid == 0) {
     __threadfence_block();
-    *reinterpret_cast<volatile int*>(s_phase) = 1;
+    *reinterpret_cast<volatile int*>(s_phase) = 1;      // the dispatch warp may add up its experts' p
   }
-  trace_point(p, kTrBarrier2);
+  trace_point(p, kTrBarrier1);
 
   // ---- phase C
-  if (warp == kProducerWarp && cta == 0 && !refills) finalize_warp<MODE>(p, counts_dst);
+  // Per expert: the total over all CTAs, f, and this CTA's base; the CTA that
+  // owns expert e (e = cta mod G) writes its count and f.
+  totals_and_bases(p, cta, s_coff, s_cbase);
+  sync_main();
+  for (int e = tid; e < E; e += kMainThreads) {
+    const int total = s_coff[e];
+    const float fe = __fdiv_rn(float(total), float(p.T * k));
+    if constexpr ((MODE & kModeFwd) != 0) s_f[e] = fe;
+    if (e % G == cta) {             // ordered before the dispatch warp's done count by the syncs below
+      counts_dst[e] = total;
+      if constexpr ((MODE & kModeFwd) != 0) p.f[e] = fe;
+    }
+  }
+  sync_main();
+  if (warp == 0) {
+    // the offsets: here for a dispatch of given assignments, else by the dispatch warp
+    if constexpr ((MODE & kModeFwd) == 0) warp_exclusive_scan(s_coff, E, s_coff);
+    if (lane == 0) {
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(s_phase) = 2;    // totals (offsets) and bases are in shared memory
+    }
+  }
+  sync_main();
+  trace_point(p, kTrScanDone);
+  if (warp == kProducerWarp && cta == 0 && !refills) finalize_after_all<MODE>(p, counts_dst, s_hist);
   if constexpr ((MODE & kModeFwd) == 0) {
     // final positions of the given assignments, chunk by chunk
-    if (warp == 0) warp_offsets(counts_dst, E, s_off);
-    for (int e = tid; e < E; e += kMainThreads) s_rank[e] = __ldcg(p.tile_hist + (size_t)e * p.G_stride + cta);
-    sync_main();
     if (warp < kConsumerWarps) {
       const int* s_wcnt = reinterpret_cast<const int*>(s_wf) + warp * E;
       const long long n = a1 - a0;
@@ -1237,9 +1409,9 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
         for (int j = 0; j < kB; ++j) {
           const long long a = b0 + j * kWarp + lane;
           const int e = e_[j];
-          const int r = s_rank[e] + s_wcnt[e] + loc_[j];
-          if (a < hi && r >= 0 && r < s_off[e + 1] - s_off[e]) {   // always true for consistent ranks
-            p.perm[s_off[e] + r] = int(a);
+          const int r = s_cbase[e] + s_wcnt[e] + loc_[j];
+          if (a < hi && r >= 0 && r < s_coff[e + 1] - s_coff[e]) {   // always true for consistent ranks
+            p.perm[s_coff[e] + r] = int(a);
             p.slot[a] = r < p.C ? r : -1;
           }
         }
@@ -1248,10 +1420,6 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   }
   if constexpr ((MODE & kModeBwd) != 0) {
     const float coef = p.grad_scale * p.alpha * float(E) / float(p.T);
-    float* s_f = s_wf;            // f, staged once per CTA (the per-warp partials are spent)
-    if (warp < kConsumerWarps)
-      for (int e = tid; e < E; e += kConsumerThreads) s_f[e] = __ldcg(p.f + e);
-    if (warp < kConsumerWarps) named_barrier(kBarConsumers, kConsumerThreads);
     if (warp < kConsumerWarps) {
       float fr[EPL];
       load_f<LPR, VW, NV>(s_f, E, l, coef, fr);
@@ -1298,6 +1466,9 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
       }
       trace_point(p, kTrBwdRows);
       trace_last(p, kTrBwdRowsAll);
+      // then help with the final dispatch positions that remain
+      if (share_fixup && wait_phase(p, s_phase, 3) == 3)
+        fixup_chunks(p, a0, int(a1 - a0), s_aidx, s_arank, s_coff, s_cbase, s_red + kRedFixNext);
     } else if (is_producer) {
       const uint64_t pol = l2_policy_evict_first();
       const uint32_t row_bytes = uint32_t(E) * uint32_t(sizeof(Raw));

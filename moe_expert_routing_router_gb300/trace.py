@@ -21,7 +21,7 @@ from . import _native
 from .api import Workspace, moe_dispatch, moe_router_fwd, moe_router_step
 
 POINTS = ("entry", "first forward stage landed", "forward rows done (warp 0)", "per-CTA partials published",
-          "grid barrier 1 passed", "per-expert scans done", "grid barrier 2 passed", "first backward stage",
+          "grid barrier passed", "totals, bases, offsets in smem", "(unused)", "first backward stage",
           "backward rows done (warp 0)", "dispatch + E-sized outputs done", "all warps joined", "exit",
           "in-CTA dispatch ranks done", "SM id", "forward rows done (all warps)", "backward rows done (all warps)")
 SM_ID = 13
