@@ -268,8 +268,8 @@ MOE_API void moe_set_unreachable_barriers(int32_t enable);
  * %globaltimer (ns) to device_buf[c * MOE_TRACE_POINTS + i] at phase boundary
  * i (points a launch does not pass are left as they were):
  *   0 entry, 1 first forward ring stage landed, 2 forward rows done (warp 0),
- *   3 per-CTA partials published, 4 after grid barrier 1, 5 per-expert scans
- *   done, 6 after grid barrier 2, 7 first backward stage available, 8 backward
+ *   3 per-CTA partials published, 4 after the grid barrier, 5 totals, bases
+ *   and offsets in shared memory, 6 (not recorded), 7 first backward stage available, 8 backward
  *   rows done (warp 0), 9 dispatch and E-sized outputs done (dispatch warp),
  *   10 all warps joined, 11 exit, 12 in-CTA dispatch ranks done (dispatch warp),
  *   13 the SM the CTA ran on (an SM id, not a time), 14 and 15 the time the
