@@ -259,6 +259,30 @@ moe_status launch_persistent(const void* func, const RouterParams& p, size_t sme
     cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
   }
+  // Cooperative (every CTA resident: the grid barrier) and, where the driver
+  // takes it, with programmatic dependent launch: the launch may be scheduled
+  // while the previous kernel of the stream finishes, and waits for it in the
+  // kernel's prologue (griddepcontrol.wait) before touching memory.
+  static std::atomic<int> pdl_ok{1};
+  if (pdl_ok.load(std::memory_order_relaxed)) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.G);
+    cfg.blockDim = dim3(moe::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeCooperative;
+    attrs[0].val.cooperative = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 2;
+    void* args[] = {const_cast<RouterParams*>(&p)};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, func, args);
+    if (e == cudaSuccess) return MOE_OK;
+    (void)cudaGetLastError();                 // not taken: fall back to the plain cooperative launch
+    pdl_ok.store(0, std::memory_order_relaxed);
+  }
   void* args[] = {const_cast<RouterParams*>(&p)};
   cudaError_t e = cudaLaunchCooperativeKernel(func, dim3(p.G), dim3(moe::kThreads), args, smem, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchCooperativeKernel");

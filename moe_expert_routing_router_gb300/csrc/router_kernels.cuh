@@ -1123,7 +1123,6 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
 #pragma unroll
   for (int q = 0; q < kMaxSlots; ++q) fills[q] = 0;
 
-  trace_point(p, kTrStart);
   for (int e = tid; e < E; e += kThreads) {
     s_hist[e] = 0;
     s_rank[e] = 0;
@@ -1143,6 +1142,12 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     }
     mbar_fence_init();
   }
+  // Launched with programmatic dependent launch, this grid may start while the
+  // previous kernel of the stream is finishing: nothing above touches global
+  // memory, and this waits until that kernel has completed and its writes are
+  // visible (it returns at once otherwise).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  trace_point(p, kTrStart);
   __syncthreads();
 
   // ---- phase A
@@ -1356,6 +1361,9 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   if (tid == 0) {
     __threadfence_block();
     *reinterpret_cast<volatile int*>(s_phase) = 1;      // the dispatch warp may add up its experts' p
+    // The next kernel of the stream may be scheduled as SMs free up; it waits
+    // for this grid's completion before it touches memory.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
   trace_point(p, kTrBarrier1);
 
