@@ -7,11 +7,12 @@
 //   warps 0..17 consumers: the per-row forward and backward math (for a
 //               dispatch of given assignments: the ranking and the scatter)
 //   warp  18    producer: streams this CTA's contiguous chunk of logit rows
-//               into a shared-memory ring with bulk asynchronous copies (TMA);
-//               in CTA 0 it writes the E-sized outputs when it has no refills
+//               into a shared-memory ring with bulk asynchronous copies (TMA),
+//               and refills it for the backward
 //   warp  19    dispatcher: stable ranks of the forward's picks as they are
-//               made, their scatter during the backward, and (CTA 0, when the
-//               producer is refilling) the E-sized outputs
+//               made, the sums of p of the CTA's experts, the scatter during
+//               the backward, and (in the CTA that finishes its per-expert
+//               outputs last) the E-sized outputs
 //
 // Row layout.  A row of E logits is held by a group of LPR consecutive lanes
 // (LPR in {8, 16, 32}; a warp holds 32/LPR rows).  Lane l of the group owns
@@ -934,39 +935,13 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
 }
 
 // ---------------------------------------------------------------------------
-// CTA 0, one warp: waits (bounded) until every CTA of the launch has counted
-// itself done (its per-expert outputs are written and it has read the group
-// sums), clears the group sums and the count for the next launch, and writes
-// the E-sized outputs.
+// One warp of the CTA that counted itself done last: every other CTA has
+// written its per-expert outputs and read the group sums.  Clears the group
+// sums and the count for the next launch and writes the E-sized outputs.
 // ---------------------------------------------------------------------------
 template <int MODE>
-__device__ __forceinline__ void finalize_after_all(const RouterParams& p, const int32_t* counts, int* s_cnt) {
+__device__ __forceinline__ void finalize_last(const RouterParams& p, const int32_t* counts, int* s_cnt) {
   const int lane = threadIdx.x & 31;
-  int ok = 1;
-  if (lane == 0) {
-    uint64_t t0 = 0;
-    for (unsigned spin = 0;; ++spin) {
-      if (ld_acquire_u64(&p.ctrl->done) >= (unsigned long long)p.G) break;
-      if ((spin & 15u) == 15u) {
-        if ((ld_acquire_u64(&p.ctrl->sync) >> 32) != 0) {   // another CTA failed: its outputs are missing
-          ok = 0;
-          break;
-        }
-        const uint64_t now = global_ns();
-        if (t0 == 0) {
-          t0 = now;
-        } else if (now - t0 > p.timeout_ns) {
-          ctrl_set_error(p.ctrl, kErrBarrierTimeout);
-          ok = 0;
-          break;
-        }
-      }
-      __nanosleep(64);
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  if (!ok) return;
   const int n = p.n_groups * p.E;
   for (int i = lane; i < n; i += kWarp) p.group_hist[i] = 0;
   if (lane == 0) p.ctrl->done = 0ull;
@@ -974,12 +949,13 @@ __device__ __forceinline__ void finalize_after_all(const RouterParams& p, const 
 }
 
 // ---------------------------------------------------------------------------
-// The dispatch warp after the forward: once grid barrier 1 has passed (bounded
-// wait) it adds up the per-CTA sums of p of this CTA's experts (e = cta mod
-// G), counts the CTA done once the CTA's totals and bases are in shared memory,
-// turns the in-CTA ranks into final positions (unless the consumer warps do
-// that: fixup_here false) and, in CTA 0 when the producer warp is busy with
-// refills, writes the E-sized outputs (shared-memory scratch s_cnt).
+// The dispatch warp after the forward: once the grid barrier has passed
+// (bounded wait) it adds up the per-CTA sums of p of this CTA's experts (e =
+// cta mod G) and counts the CTA done once the CTA's totals and bases are in
+// shared memory; in the CTA that counts itself done last it then writes the
+// E-sized outputs (shared-memory scratch s_cnt).  In the fused step it turns
+// the in-CTA ranks into final positions, in chunks that the consumers done with
+// the backward share.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int wait_phase(const RouterParams& p, const int* s_phase, int at_least) {
   int ph = 0;
@@ -1014,8 +990,8 @@ __device__ __forceinline__ void fixup_chunks(const RouterParams& p, long long a0
 
 template <int MODE, bool STAGED>
 __device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta, long long a0, long long a1, int* s_coff,
-                                                 int* s_cbase, int* s_phase, const int32_t* counts, bool finalize_here,
-                                                 bool ranked, const uint16_t* s_aidx, const uint16_t* s_arank, int* s_cnt,
+                                                 int* s_cbase, int* s_phase, const int32_t* counts, bool ranked,
+                                                 const uint16_t* s_aidx, const uint16_t* s_arank, int* s_cnt,
                                                  int* s_next) {
   const int lane = threadIdx.x & 31;
   const int E = p.E;
@@ -1027,10 +1003,10 @@ __device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta,
     }
   }
   if (wait_phase(p, s_phase, 2) < 2) return;
-  if (lane == 0) {
-    __threadfence();
-    atomicAdd(&p.ctrl->done, 1ull);
-  }
+  // counted done (release: this CTA's outputs; acquire: everyone else's, for the last)
+  unsigned long long before = 0;
+  if (lane == 0) before = atom_add_acq_rel_u64(&p.ctrl->done, 1ull);
+  const bool last = __shfl_sync(0xffffffffu, before, 0) == (unsigned long long)(p.G - 1);
   __syncwarp();
   if constexpr ((MODE & kModeDispatch) != 0 && (MODE & kModeFwd) != 0) {   // given idx: the consumer warps do it
     warp_exclusive_scan(s_coff, E, s_coff);             // totals -> offsets
@@ -1039,13 +1015,15 @@ __device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta,
       *reinterpret_cast<volatile int*>(s_phase) = ranked ? 3 : 4;   // 3: the consumers may help with the chunks
     }
     __syncwarp();
+    if (last) finalize_last<MODE>(p, counts, s_cnt);
     if (ranked) {
       if (s_aidx != nullptr) fixup_chunks(p, a0, int(a1 - a0), s_aidx, s_arank, s_coff, s_cbase, s_next);
       else if constexpr (STAGED) dispatch_fixup(p, p.idx, a0, a1, s_coff, s_cbase);
       else dispatch_direct(p, p.idx, a0, a1, s_coff, s_cbase);
     }
+  } else {
+    if (last) finalize_last<MODE>(p, counts, s_cnt);
   }
-  if (finalize_here) finalize_after_all<MODE>(p, counts, s_cnt);
   trace_point(p, kTrDispatchDone);
 }
 
@@ -1304,10 +1282,6 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
       trace_last(p, kTrFwdRowsAll);
     }
   }
-  // The producer warp is idle in phase C unless it refills the ring for the
-  // backward; CTA 0's E-sized outputs go to whichever of the producer and the
-  // dispatch warp is idle.
-  const bool refills = STAGED && (MODE & kModeBwd) != 0 && n_st > NS;
   // Phase C shared memory: per expert f, the total (then the offsets) and this
   // CTA's base.  With the forward they take the per-warp partials' space, which
   // is spent after the publication below; a dispatch of given assignments
@@ -1316,8 +1290,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   int* s_coff = (MODE & kModeFwd) != 0 ? reinterpret_cast<int*>(s_wf + E) : s_off;
   int* s_cbase = (MODE & kModeFwd) != 0 ? s_coff + E + 1 : s_rank;
   if (warp == kDispatchWarp) {
-    dispatch_phase_c<MODE, STAGED>(p, cta, a0, a1, s_coff, s_cbase, s_phase, counts_dst, cta == 0 && refills,
-                                   ranked, s_aidx, s_arank, s_hist, s_red + kRedFixNext);
+    dispatch_phase_c<MODE, STAGED>(p, cta, a0, a1, s_coff, s_cbase, s_phase, counts_dst, ranked, s_aidx, s_arank,
+                                   s_hist, s_red + kRedFixNext);
     return;
   }
   sync_main();
@@ -1392,7 +1366,6 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   }
   sync_main();
   trace_point(p, kTrScanDone);
-  if (warp == kProducerWarp && cta == 0 && !refills) finalize_after_all<MODE>(p, counts_dst, s_hist);
   if constexpr ((MODE & kModeFwd) == 0) {
     // final positions of the given assignments, chunk by chunk
     if (warp < kConsumerWarps) {

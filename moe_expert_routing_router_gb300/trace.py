@@ -1,6 +1,6 @@
 """Phase timeline of the persistent router kernel (device timestamps per CTA).
 
-    python -m moe_expert_routing_router_gb300.trace [--mode step|fwd|dispatch] WORKLOAD...
+    python -m moe_expert_routing_router_gb300.trace [--mode step|fwd|dispatch] [--cold] WORKLOAD...
 
 Runs the fused step (or the forward, or the dispatch of the forward's picks) on a synthetic workload with the
 library's phase tracing on (moe_set_trace_buffer) and prints, for each phase
@@ -38,8 +38,11 @@ def _device_logits(w, seed: int = 0) -> torch.Tensor:
     return torch.from_numpy(z).cuda()
 
 
-def phase_timeline(w, mode: str = "step", reps: int = 3) -> tuple[int, np.ndarray]:
-    """Returns (CTAs, times [CTAs, points] in microseconds since the first CTA's entry; NaN = not passed)."""
+def phase_timeline(w, mode: str = "step", reps: int = 3, cold: bool = False) -> tuple[int, np.ndarray]:
+    """Returns (CTAs, times [CTAs, points] in microseconds since the first CTA's entry; NaN = not passed).
+
+    cold: before each traced launch, write a buffer of three times the L2 size so
+    that the launch finds its inputs in HBM, as in the benchmark's rotation."""
     x = _device_logits(w)
     ws = Workspace()
     if mode == "step":
@@ -57,11 +60,14 @@ def phase_timeline(w, mode: str = "step", reps: int = 3) -> tuple[int, np.ndarra
         run()
     torch.cuda.synchronize()
     buf = torch.zeros(MAX_CTAS * TRACE_POINTS, dtype=torch.int64, device="cuda")
+    flush = torch.empty(3 * 129 * 2**20, dtype=torch.uint8, device="cuda") if cold else None
     lib = _native.lib()
     lib.moe_set_trace_buffer(buf.data_ptr(), MAX_CTAS)
     try:
         for _ in range(reps):
             buf.zero_()
+            if flush is not None:
+                flush.fill_(1)
             run()
             torch.cuda.synchronize()
     finally:
@@ -78,11 +84,12 @@ def main() -> int:
     import synth
     ap = argparse.ArgumentParser()
     ap.add_argument("--mode", choices=("step", "fwd", "dispatch"), default="step")
+    ap.add_argument("--cold", action="store_true", help="flush L2 before each traced launch")
     ap.add_argument("workloads", nargs="*", default=list(synth.ROUTER_WORKLOADS))
     args = ap.parse_args()
     for name in args.workloads:
         w = synth.ROUTER_WORKLOADS[name]
-        G, rel = phase_timeline(w, args.mode)
+        G, rel = phase_timeline(w, args.mode, cold=args.cold)
         print(f"{args.mode} {name}: {G} CTAs, last exit {np.nanmax(rel[:, 11]):.2f} us")
         for i in range(1, len(POINTS)):
             if i == SM_ID:
