@@ -122,6 +122,9 @@ EDGE = [
     (4096, 8, 1, "fp32", -1, 0, 1.25, 0),      # Switch top-1, E = 8
     (3000, 384, 6, "fp32", -1, 64, 1.0, 0),    # fp32 vector path at E = 384
     (2000, 16, 2, "bf16", -1, 4, 0.25, 0),     # capacity below the mean: most tokens dropped
+    (2048, 64, 8, "bf16", -1, 8, 1.0, 0),      # k = 8 at E = 64
+    (1500, 48, 6, "bf16", 0, 0, 1.25, 2),      # raw gates, ties
+    (999, 40, 5, "bf16", 1, 5, 1.0, 0),        # odd k, renormalised
 ]
 
 
@@ -231,3 +234,24 @@ def test_signed_zero_ties(mr, dtype, E, k):
     check_forward(st, want, 0)
     check_dispatch(st, want["idx"], E, oracle.dispatch.capacity(T, k, E, 1.0))
     check_backward(st["dlogits"], logits, dtype, want["f"], 0.01, 1.0)
+
+
+@pytest.mark.parametrize("E,k", [(64, 8), (64, 3), (56, 7)])
+def test_small_expert_counts_equal_separate_calls(mr, E, k):
+    """At E <= 64 (one or two vectors per lane) the separate calls give the fused step's bits."""
+    logits = synth.random_logits(3001, E, "bf16", seed=E + k, scale=2.0)
+    x = to_device(logits, "bf16")
+    st = mr.moe_router_step(x, k, 0.01, 1.25, n_ranks=0, grad_scale=1.0)
+    fw = mr.moe_router_fwd(x, k, 0.01, n_ranks=0)
+    dp = mr.moe_dispatch(fw["idx"], E, 1.25)
+    dl = mr.moe_router_bwd(x, fw["f"], 0.01, 1.0)
+    torch.cuda.synchronize()
+    want = oracle_forward(logits, "bf16", k, 0.01, None, 0)
+    check_forward(st, want, 0)
+    check_dispatch(st, want["idx"], E, oracle.dispatch.capacity(3001, k, E, 1.25))
+    check_backward(st["dlogits"], logits, "bf16", want["f"], 0.01, 1.0)
+    for key in ("idx", "gate", "counts", "f", "P", "scalars"):
+        assert torch.equal(st[key], fw[key]), key
+    for key in ("perm", "slot", "offsets", "kept", "n_dropped"):
+        assert torch.equal(st[key], dp[key]), key
+    assert torch.equal(st["dlogits"], dl)
