@@ -641,7 +641,7 @@ __device__ __forceinline__ void totals_and_bases(const RouterParams& p, int cta,
   int S = 32;
   while (S > 1 && E * S > kMainThreads) S >>= 1;
   const int s = tid & (S - 1);
-  constexpr int kB = 8;
+  constexpr int kB = 16;                               // loads per lane in flight together
   static_assert(kMainThreads % kWarp == 0, "whole warps");
   const int per_trip = kMainThreads / S;               // experts per trip (S divides kMainThreads)
   const int trips = (E + per_trip - 1) / per_trip;     // the same for every thread: the shuffles need whole warps
