@@ -23,6 +23,15 @@
  *     call returns without synchronising.  Results are valid once the stream
  *     reaches that point.  Calls that share a workspace must be ordered on one
  *     stream; concurrent calls need separate workspaces.
+ *   - The persistent kernels (moe_router_fwd, moe_dispatch, moe_router_step)
+ *     are launched with programmatic dependent launch: a launch may be
+ *     scheduled while the previous kernel of the stream finishes and waits
+ *     for it before touching memory, and each launch lets the next one be
+ *     scheduled once all its CTAs have passed their grid barrier.  A kernel
+ *     of the caller's that is itself launched with programmatic stream
+ *     serialization must wait for its prerequisite grid
+ *     (cudaGridDependencySynchronize) before it reads these outputs; any
+ *     other launch is ordered as usual.
  *   - Errors are returned as moe_status; no exception crosses the ABI.
  *     Argument errors are found on the host before anything is enqueued.
  *     moe_last_error() gives a one-line description of the last failure on

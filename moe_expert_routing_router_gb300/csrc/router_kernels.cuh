@@ -957,14 +957,21 @@ __device__ __forceinline__ void finalize_last(const RouterParams& p, const int32
 // the in-CTA ranks into final positions, in chunks that the consumers done with
 // the backward share.
 // ---------------------------------------------------------------------------
+// Waits (bounded) until this CTA's phase word reaches at_least or turns -1
+// (an error elsewhere in the CTA); returns it, or -1 after recording an
+// expired wait.
 __device__ __forceinline__ int wait_phase(const RouterParams& p, const int* s_phase, int at_least) {
   int ph = 0;
   uint64_t t0 = 0;
   for (unsigned spin = 0; (ph = *reinterpret_cast<const volatile int*>(s_phase)) >= 0 && ph < at_least; ++spin) {
     if ((spin & 15u) == 15u) {
       const uint64_t now = global_ns();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > p.timeout_ns) return -1;
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > p.timeout_ns) {
+        if ((threadIdx.x & 31) == 0) ctrl_set_error(p.ctrl, kErrPipelineTimeout);
+        return -1;
+      }
     }
     __nanosleep(64);
   }
