@@ -959,7 +959,9 @@ __device__ __forceinline__ void finalize_last(const RouterParams& p, const int32
 // ---------------------------------------------------------------------------
 // Waits (bounded) until this CTA's phase word reaches at_least or turns -1
 // (an error elsewhere in the CTA); returns it, or -1 after recording an
-// expired wait.
+// expired wait.  The limit is four times the wait limit: whatever the phase
+// word waits for (the grid barrier, the CTA's own syncs) is bounded by the
+// wait limit itself and reports its own expiry first.
 __device__ __forceinline__ int wait_phase(const RouterParams& p, const int* s_phase, int at_least) {
   int ph = 0;
   uint64_t t0 = 0;
@@ -968,7 +970,7 @@ __device__ __forceinline__ int wait_phase(const RouterParams& p, const int* s_ph
       const uint64_t now = global_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > p.timeout_ns) {
+      } else if (now - t0 > 4 * p.timeout_ns) {
         if ((threadIdx.x & 31) == 0) ctrl_set_error(p.ctrl, kErrPipelineTimeout);
         return -1;
       }
