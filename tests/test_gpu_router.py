@@ -255,3 +255,31 @@ def test_small_expert_counts_equal_separate_calls(mr, E, k):
     for key in ("perm", "slot", "offsets", "kept", "n_dropped"):
         assert torch.equal(st[key], dp[key]), key
     assert torch.equal(st["dlogits"], dl)
+
+
+def test_back_to_back_calls_on_one_workspace(mr):
+    """Launches queued without a host sync on one workspace (each may be scheduled
+    while the previous one finishes): steps, forwards and dispatches of different
+    sizes in turn, every result checked afterwards."""
+    ws = mr.Workspace()
+    ws.ensure(262144, 1024, 8)           # one buffer for every call below, whatever its E
+    cases = [("zipf-top2-T65536-E64", 20001), ("zipf-hot-top8-T131072-E256", 9001), ("switch-top1-T4096-E8", 4096),
+             ("zipf-ep64-top6-T262144-E384", 7001), ("zipf-top2-T65536-E64", 3001)]
+    runs = []
+    for name, T in cases:
+        w, logits = workload_inputs(name, T)
+        x = to_device(logits, w.dtype)
+        st = mr.moe_router_step(x, w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks, ws=ws)
+        fw = mr.moe_router_fwd(x, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, ws=ws)
+        dp = mr.moe_dispatch(fw["idx"], w.E, w.capacity_factor, ws=ws)
+        runs.append((w, logits, st, fw, dp))
+    torch.cuda.synchronize()
+    assert mr.moe_get_device_status(ws) == 0
+    for w, logits, st, fw, dp in runs:
+        want = oracle_forward(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks)
+        check_forward(st, want, w.n_ranks)
+        check_forward(fw, want, w.n_ranks)
+        C = oracle.dispatch.capacity(w.T, w.k, w.E, w.capacity_factor)
+        check_dispatch(st, want["idx"], w.E, C)
+        check_dispatch(dp, want["idx"], w.E, C)
+        check_backward(st["dlogits"], logits, w.dtype, want["f"], w.alpha, 1.0)
