@@ -249,8 +249,9 @@ def time_e2e(w, steps: int, warmup: int, torch, device, dist_ctx) -> dict:
     every step copies its logits host -> device (double-buffered on a copy
     stream, so that step i + 1's copy overlaps step i's kernel) and reads its
     result back to pinned host memory (the scalars -- L_aux, balance, CV,
-    max/min over mean, rank CV -- and the per-expert counts).  Copies and
-    launches are issued eagerly from Python, inside the timed region."""
+    max/min over mean, rank CV -- and the per-expert counts).  Timed twice:
+    the copies and calls issued eagerly from Python, and the same sequence of
+    K steps captured once in a CUDA graph and replayed (the value reported)."""
     import moe_expert_routing_router_gb300 as mr
     logits = synth.router_logits(w)
     host_x = to_device(logits, w.dtype, torch, "cpu").pin_memory()
@@ -259,23 +260,23 @@ def time_e2e(w, steps: int, warmup: int, torch, device, dist_ctx) -> dict:
     result_keys = ("scalars", "counts")
     host_res = {k: torch.empty_like(outs[k], device="cpu").pin_memory() for k in result_keys}
     ws = mr.Workspace(device)
-    compute = torch.cuda.current_stream(device)
     copy = torch.cuda.Stream(device)
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
     h2d = host_x.numel() * host_x.element_size()
     d2h = sum(outs[k].numel() * outs[k].element_size() for k in result_keys)
 
-    def h2d_into(b):
-        with torch.cuda.stream(copy):
-            copy.wait_event(consumed[b])             # the kernel that read this buffer is done
-            dev_x[b].copy_(host_x, non_blocking=True)
-            copied[b].record(copy)
+    def run(n, start):
+        # start: an event on the compute stream that the first copy waits for
+        compute = torch.cuda.current_stream(device)
 
-    def run(n, start=None):
-        if start is not None:
-            copy.wait_event(start)                   # no copy of the timed steps starts before the clock
-        h2d_into(0)
+        def h2d_into(b, after):
+            with torch.cuda.stream(copy):
+                copy.wait_event(after)               # the kernel that read this buffer is done
+                dev_x[b].copy_(host_x, non_blocking=True)
+                copied[b].record(copy)
+
+        h2d_into(0, start)
         for i in range(n):
             b = i & 1
             compute.wait_event(copied[b])
@@ -283,24 +284,42 @@ def time_e2e(w, steps: int, warmup: int, torch, device, dist_ctx) -> dict:
                                n_ranks=w.n_ranks, grad_scale=1.0, ws=ws, out=outs)
             consumed[b].record(compute)
             if i + 1 < n:
-                h2d_into(b ^ 1)
+                h2d_into(b ^ 1, consumed[b ^ 1] if i >= 1 else start)
             for k2 in result_keys:
                 host_res[k2].copy_(outs[k2], non_blocking=True)
 
-    for b in range(2):
-        consumed[b].record(compute)
-    run(max(warmup, 3))
+    def timed(fn):
+        compute = torch.cuda.current_stream(device)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        dist_ctx.barrier()
+        t0.record(compute)
+        fn(t0)
+        t1.record(compute)
+        torch.cuda.synchronize(device)
+        dist_ctx.barrier()
+        return dist_ctx.max(t0.elapsed_time(t1)) / steps
+
+    w0 = torch.cuda.Event()
+    w0.record(torch.cuda.current_stream(device))
+    run(max(warmup, 3), w0)
     torch.cuda.synchronize(device)
-    dist_ctx.barrier()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(compute)
-    run(steps, t0)
-    t1.record(compute)
-    torch.cuda.synchronize(device)
-    dist_ctx.barrier()
-    ms = dist_ctx.max(t0.elapsed_time(t1)) / steps
-    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h,
+    eager_ms = timed(lambda t0: run(steps, t0))
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            s0 = torch.cuda.Event()
+            s0.record(torch.cuda.current_stream(device))
+            run(steps, s0)
+        g.replay()
+        torch.cuda.synchronize(device)
+        graph_ms = timed(lambda t0: g.replay())
+    except Exception as e:  # capture unsupported: report the eager number
+        log(f"CUDA graph capture of the end-to-end steps failed ({e!r}); reporting eager launches")
+    return {"ms_per_step": graph_ms if graph_ms is not None else eager_ms, "eager_ms_per_step": eager_ms,
+            "graph": graph_ms is not None, "h2d": h2d, "d2h": d2h,
             "read_back": "scalars (L_aux, balance, CV, max/min over mean, rank CV, rank max/mean) and counts"}
 
 
@@ -540,9 +559,12 @@ def run_ours(args) -> dict:
                      "launch_us_mean": round(r["launch_ms_mean"] * 1e3, 2), "peak_source": pk["source"]},
         "e2e": {"value": dist_ctx.world * w.T / (e2e["ms_per_step"] * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": e2e["ms_per_step"], "read_back": e2e["read_back"],
-                "timing": "eager API calls; logits copied from pinned host memory every step on a copy "
-                          "stream (double-buffered), the step's result read back every step"},
+                "ms_per_step": e2e["ms_per_step"], "eager_ms_per_step": e2e["eager_ms_per_step"],
+                "read_back": e2e["read_back"],
+                "timing": ("the API calls of K steps captured in one CUDA graph and replayed" if e2e["graph"]
+                           else "eager API calls") +
+                          "; logits copied from pinned host memory every step on a copy stream (double-buffered), "
+                          "the step's result read back every step"},
         "gpu_launches": args.steps,
         "clocks": r["clocks"],
     }
