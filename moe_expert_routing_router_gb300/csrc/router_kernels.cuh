@@ -1,7 +1,8 @@
 // Router kernels: softmax + top-k + Switch balance statistics (forward), the
 // closed-form gradient of the aux loss (backward) and the capacity-limited
-// stable dispatch, as one persistent cooperative kernel with grid barriers
-// between the phases, plus a plain streaming kernel for the backward alone.
+// stable dispatch, as one persistent cooperative kernel with one grid barrier
+// between the forward and the rest, plus a plain streaming kernel for the
+// backward alone.
 //
 // CTA organisation (one CTA per SM, kThreads = 640):
 //   warps 0..17 consumers: the per-row forward and backward math (for a
@@ -44,8 +45,8 @@ constexpr int kDispatchWarp = kConsumerWarps + 1;
 constexpr int kThreads = (kConsumerWarps + 2) * kWarp;
 constexpr int kConsumerThreads = kConsumerWarps * kWarp;
 // Consumers + producer: the CTA-level syncs from the end of the forward to the
-// start of phase C exclude the dispatch warp, whose in-CTA ranking runs on
-// through the grid barriers and the per-expert scans.
+// start of the backward exclude the dispatch warp, whose in-CTA ranking runs
+// on through the grid barrier and the totals.
 constexpr int kMainThreads = (kConsumerWarps + 1) * kWarp;
 static_assert(kMainThreads / kWarp <= 32, "block scans hold one value per warp in 32 slots");
 // Slots of the 128-int scratch area at the start of shared memory.
@@ -1049,10 +1050,12 @@ __device__ __forceinline__ int ring_last(int q, int n, int NS) { return q + (rin
 
 // ---------------------------------------------------------------------------
 // The persistent kernel.  MODE selects the phases:
-//   A: per-CTA counts (and, with kModeFwd, idx/gate and sums of p)
-//   B: per-expert totals, exclusive prefixes over CTAs, f and P
-//   C: dispatch scatter (kModeDispatch), backward (kModeBwd), and the E-sized
-//      outputs written by CTA 0 (scalars, rank loads, offsets, kept, drops).
+//   A: per-CTA counts (and, with kModeFwd, idx/gate and sums of p), published
+//      per CTA and into the group sums; then the launch's one grid barrier
+//   C: per-expert totals, this CTA's dispatch bases and f (one round of L2
+//      reads), P of the CTA's own experts, dispatch scatter (kModeDispatch),
+//      backward (kModeBwd), and the E-sized outputs (scalars, rank loads,
+//      offsets, kept, drops) written by the CTA that finishes its part last.
 // STAGED: logit rows are 16-byte multiples and the producer warp streams them
 // through the ring; otherwise the consumers read global memory directly.
 // Launched cooperatively with p.G CTAs of kThreads threads.
