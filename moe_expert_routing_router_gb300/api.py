@@ -9,6 +9,7 @@ runs in the library's CUDA kernels; nothing here computes on the host.
 from __future__ import annotations
 
 import ctypes as C
+import functools
 
 import torch
 
@@ -140,9 +141,15 @@ def moe_router_bwd(logits: torch.Tensor, f: torch.Tensor, alpha: float, grad_sca
     return dl
 
 
+@functools.lru_cache(maxsize=256)
+def _capacity(T: int, E: int, k: int, capacity_factor: float) -> int:
+    return int(lib().moe_dispatch_capacity(T, E, k, capacity_factor))
+
+
 def moe_dispatch_capacity(T: int, E: int, k: int, capacity_factor: float) -> int:
-    """Expert capacity ceil(ceil(T*k/E) * capacity_factor) (C: moe_dispatch_capacity)."""
-    c = int(lib().moe_dispatch_capacity(T, E, k, float(capacity_factor)))
+    """Expert capacity ceil(ceil(T*k/E) * capacity_factor) (C: moe_dispatch_capacity; the
+    library's answer is remembered per argument tuple)."""
+    c = _capacity(int(T), int(E), int(k), float(capacity_factor))
     if c < 0:
         raise ValueError("invalid capacity arguments")
     return c
