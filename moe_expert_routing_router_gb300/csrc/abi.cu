@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <unordered_map>
@@ -100,6 +101,26 @@ moe_status device_info(DeviceInfo* out, int* dev_out) {
   return MOE_OK;
 }
 
+// Raises a kernel's dynamic shared-memory limit on the current device to at
+// least `smem` (never lowers it), with one driver call per device, kernel and
+// larger size.
+moe_status raise_smem_limit(const void* func, size_t smem) {
+  if (smem <= 48 * 1024) return MOE_OK;
+  int dev = 0;
+  cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) return cuda_fail(ge, "cudaGetDevice");
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> raised;
+  std::lock_guard<std::mutex> lk(mu);
+  size_t& have = raised[{dev, func}];
+  if (have < smem) {
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    have = smem;
+  }
+  return MOE_OK;
+}
+
 moe_status occupancy(const void* func, int threads, size_t smem, int dev, int* blocks) {
   char key[96];
   snprintf(key, sizeof(key), "%d:%p:%d:%zu", dev, func, threads, smem);
@@ -111,13 +132,10 @@ moe_status occupancy(const void* func, int threads, size_t smem, int dev, int* b
       return MOE_OK;
     }
   }
-  cudaError_t e = cudaSuccess;
-  if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-  }
+  moe_status s = raise_smem_limit(func, smem);
+  if (s != MOE_OK) return s;
   int b = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, func, threads, smem);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, func, threads, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   if (b < 1) return fail(MOE_ERR_CUDA, "kernel does not fit on an SM (smem %zu bytes)", smem);
   std::lock_guard<std::mutex> lk(g_mu);
@@ -255,9 +273,9 @@ moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, 
 moe_status launch_persistent(const void* func, const RouterParams& p, size_t smem, cudaStream_t stream) {
   if (p.trace != nullptr && p.G > g_trace_ctas.load(std::memory_order_relaxed))
     return fail(MOE_ERR_INVALID, "trace buffer holds %d CTAs, the launch has %d", g_trace_ctas.load(), p.G);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  {
+    moe_status s = raise_smem_limit(func, smem);
+    if (s != MOE_OK) return s;
   }
   // Cooperative (every CTA resident: the grid barrier) and, where the driver
   // takes it, with programmatic dependent launch: the launch may be scheduled
