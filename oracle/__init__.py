@@ -21,9 +21,10 @@ Modules:
   router    -- softmax, top-k, gates, f_i, P_i, L_aux, CV, per-rank loads, dL_aux/dlogits
   dispatch  -- capacity and the stable capacity-limited token->expert dispatch
   sinkhorn  -- TAOT Phase 1: topology-aware entropic transport plan
+  routing_ext -- aux-loss-free bias routing, masked P_i, the full backward through the gates
 
 Parity status of each function is stated in its docstring ("pinned by ...");
 the pins live in ``tests/test_oracle_*.py``.
 """
 
-from . import router, dispatch, sinkhorn  # noqa: F401
+from . import router, dispatch, sinkhorn, routing_ext  # noqa: F401

@@ -334,3 +334,159 @@ def check_sinkhorn_topology_kernel(sinkhorn) -> None:
     M = sinkhorn.gibbs_kernel(W, 10.0)
     assert M[0, 0] == 1.0 and abs(M[0, 1] / M[0, 8] - math.exp(0.9)) < 1e-14
     assert (W == W.T).all() and W[3, 3] == 0 and W[3, 5] == 1 and W[3, 12] == 10
+
+
+# ----------------------------------------------------------------------------- next steps (bias, masked P, full backward)
+
+def check_biased_topk_bruteforce(ext) -> None:
+    """top_k_biased equals brute force over k-subsets of z + b (integer values:
+    the fp32 sum is exact, ties everywhere); a zero bias gives plain top-k."""
+    rng = np.random.default_rng(31)
+    for E in range(1, 8):
+        for k in range(1, min(E, 3) + 1):
+            z = rng.integers(-2, 3, size=(20, E)).astype(np.float32)
+            b = rng.integers(-2, 3, size=E).astype(np.float32)
+            got = ext.top_k_biased(z, "fp32", b, k)
+            s = z.astype(np.float64) + b.astype(np.float64)[None, :]
+            for t in range(z.shape[0]):
+                assert list(got[t]) == _brute_topk_row(s[t], k), (E, k, t, s[t], got[t])
+            zero = ext.top_k_biased(z, "fp32", np.zeros(E, np.float32), k)
+            for t in range(z.shape[0]):
+                assert list(zero[t]) == _brute_topk_row(z[t].astype(np.float64), k)
+
+
+def check_biased_topk_dominant(ext) -> None:
+    """A bias far above the logits' spread puts its expert first in every row,
+    and the rest of each row's picks are that row's plain top-(k-1) of the others."""
+    rng = np.random.default_rng(32)
+    T, E, k, hot = 50, 9, 3, 6
+    z = rng.standard_normal((T, E)).astype(np.float32)
+    b = np.zeros(E, np.float32)
+    b[hot] = 100.0
+    got = ext.top_k_biased(z, "fp32", b, k)
+    assert (got[:, 0] == hot).all()
+    others = [e for e in range(E) if e != hot]
+    for t in range(T):
+        rest = sorted(others, key=lambda e: (-float(z[t, e]), e))[:k - 1]
+        assert list(got[t, 1:]) == rest
+
+
+def check_biased_sum_is_fp32(ext) -> None:
+    """The selection score is the fp32 sum: 1 + 2^-24 rounds to 1 in fp32, so
+    a logit of 1 with bias 2^-24 ties a logit of 1 with bias 0 and the lower
+    index wins; in float64 the first would win."""
+    z = np.array([[1.0, 1.0]], np.float32)
+    b = np.array([0.0, 2.0 ** -24], np.float32)
+    assert list(ext.top_k_biased(z, "fp32", b, 1)[0]) == [0]
+    b2 = np.array([0.0, 2.0 ** -23], np.float32)       # representable: expert 1 wins
+    assert list(ext.top_k_biased(z, "fp32", b2, 1)[0]) == [1]
+
+
+def check_bias_update_hand(ext) -> None:
+    """T*k = 12 assignments over E = 4 experts (mean 3): counts [5, 3, 0, 4]
+    move the biases by [-g, 0, +g, -g]; with T*k = 10 (mean 2.5, not an
+    integer) no expert sits at the mean."""
+    g = 0.125
+    b = np.array([0.5, -0.25, 0.0, 1.0], np.float32)
+    out = ext.bias_update(b, np.array([5, 3, 0, 4]), T=6, k=2, gamma=g)
+    np.testing.assert_array_equal(out, np.array([0.375, -0.25, 0.125, 0.875], np.float32))
+    assert out.dtype == np.float32
+    out2 = ext.bias_update(np.zeros(4, np.float32), np.array([3, 2, 3, 2]), T=5, k=2, gamma=g)
+    np.testing.assert_array_equal(out2, np.array([-g, g, -g, g], np.float32))
+
+
+def check_bias_update_balances(ext, router) -> None:
+    """Bias routing does what [P1] §4.3 says it is for: on a batch with a
+    strongly preferred expert set, repeated selection + update lowers the load
+    CV (the gate and aux loss are not involved)."""
+    rng = np.random.default_rng(33)
+    T, E, k = 2000, 16, 2
+    z = (rng.standard_normal((T, E)) + np.linspace(2.0, -2.0, E)[None, :]).astype(np.float32)
+    b = np.zeros(E, np.float32)
+    cv0 = router.load_cv(router.expert_counts(ext.top_k_biased(z, "fp32", b, k), E))
+    for _ in range(300):
+        counts = router.expert_counts(ext.top_k_biased(z, "fp32", b, k), E)
+        b = ext.bias_update(b, counts, T, k, gamma=0.02)
+    cv1 = router.load_cv(router.expert_counts(ext.top_k_biased(z, "fp32", b, k), E))
+    assert cv0 > 0.5 and cv1 < 0.1 * cv0, (cv0, cv1)
+    assert b[0] < 0 < b[-1]          # the favoured expert is pushed down, the shunned one up
+
+
+def check_masked_p_closed_forms(ext, router) -> None:
+    """k = E picks every expert, so masked P = unmasked P / k; a per-token loop
+    gives the masked mean for k < E."""
+    rng = np.random.default_rng(34)
+    T, E = 30, 5
+    z = rng.standard_normal((T, E))
+    p = router.softmax(z)
+    idx_all = router.top_k(z, E)
+    np.testing.assert_allclose(ext.mean_router_prob_masked(p, idx_all, E), router.mean_router_prob(p) / E,
+                               rtol=1e-14, atol=0)
+    k = 2
+    idx = router.top_k(z, k)
+    want = np.zeros(E)
+    for t in range(T):
+        for j in range(k):
+            want[idx[t, j]] += p[t, idx[t, j]]
+    want /= T * k
+    np.testing.assert_allclose(ext.mean_router_prob_masked(p, idx, k), want, rtol=1e-14, atol=0)
+
+
+def _full_grad_case(ext, router, renorm: bool, masked: bool, k: int, with_dgate: bool, seed: int):
+    rng = np.random.default_rng(seed)
+    T, E, alpha, g = 4, 6, 0.3, 1.7
+    z32 = rng.standard_normal((T, E)).astype(np.float32)
+    z = z32.astype(np.float64)
+    idx = router.top_k(z, k)
+    f = rng.random(E)
+    f /= f.sum()
+    dgate = rng.standard_normal((T, k)) if with_dgate else None
+    grad = ext.router_backward_full(z32, "fp32", f, alpha, g, idx, dgate, renorm, masked)
+    h = 1e-6
+    fd = np.zeros_like(z)
+    for t in range(T):
+        for j in range(E):
+            zp, zm = z.copy(), z.copy()
+            zp[t, j] += h
+            zm[t, j] -= h
+            fd[t, j] = (ext.full_loss_of_logits(zp, f, alpha, g, idx, dgate, renorm, masked)
+                        - ext.full_loss_of_logits(zm, f, alpha, g, idx, dgate, renorm, masked)) / (2 * h)
+    return grad, fd, idx
+
+
+def check_full_grad_finite_difference(ext, router) -> None:
+    """Central differences of the main-loss gate term plus g * L_aux (picks and
+    f frozen) match router_backward_full, for every combination of
+    renormalised gates, masked P, k and the presence of dgate."""
+    seed = 40
+    for renorm in (False, True):
+        for masked in (False, True):
+            for k in (1, 2, 3):
+                for with_dgate in (False, True):
+                    seed += 1
+                    grad, fd, _ = _full_grad_case(ext, router, renorm, masked, k, with_dgate, seed)
+                    scale = max(np.abs(grad).max(), 1e-12)
+                    err = np.abs(grad - fd).max() / scale
+                    assert err <= 1e-7, (renorm, masked, k, with_dgate, err)
+
+
+def check_full_grad_structure(ext, router) -> None:
+    """Rows sum to zero; no dgate and unmasked P reduce to router.aux_loss_grad;
+    with renormalised gates and no aux loss, the unpicked experts get no gradient
+    (the renormalised gates depend only on the picked logits)."""
+    rng = np.random.default_rng(50)
+    T, E, k, alpha = 6, 7, 3, 0.2
+    z = rng.standard_normal((T, E)).astype(np.float32)
+    idx = router.top_k(z.astype(np.float64), k)
+    f = rng.random(E)
+    f /= f.sum()
+    dgate = rng.standard_normal((T, k))
+    g = ext.router_backward_full(z, "fp32", f, alpha, 1.3, idx, dgate, True, False)
+    assert np.abs(g.sum(axis=1)).max() < 1e-14
+    np.testing.assert_allclose(ext.router_backward_full(z, "fp32", f, alpha, 1.3, idx, None, True, False),
+                               router.aux_loss_grad(z, "fp32", f, alpha, grad_scale=1.3), rtol=1e-12, atol=1e-18)
+    gate_only = ext.router_backward_full(z, "fp32", f, 0.0, 1.0, idx, dgate, True, False)
+    mask = ext.pick_mask(idx, E)
+    # zero up to the rounding of sum_i p_i dp_i, which cancels exactly in real arithmetic
+    assert np.abs(gate_only * (1.0 - mask)).max() <= 1e-14 * np.abs(gate_only).max()
+    assert np.abs(gate_only * mask).max() > 1e-3

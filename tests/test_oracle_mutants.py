@@ -16,6 +16,7 @@ import pins
 import synth
 
 R, D, S = oracle.router, oracle.dispatch, oracle.sinkhorn
+X = oracle.routing_ext
 
 
 def _masked_forward(logits, dtype, k, alpha, renorm=None, n_ranks=0):
@@ -83,7 +84,47 @@ MUTANTS = {
     "cross-node cost and intra-node cost swapped": (
         [(S, "topology_cost", lambda R_, rpn, lam: np.where(_orig_tc(R_, rpn, lam) == 1.0, lam, np.where(_orig_tc(R_, rpn, lam) == lam, 1.0, 0.0)))],
         [lambda: pins.check_sinkhorn_topology_kernel(S)]),
+    "bias added in float64 instead of fp32": (
+        [(X, "selection_scores", lambda logits, dtype, bias: R.widen(logits, dtype) + np.asarray(bias, np.float64)[None, :])],
+        [lambda: pins.check_biased_sum_is_fp32(X)]),
+    "bias subtracted from the logits": (
+        [(X, "selection_scores", lambda logits, dtype, bias: _orig_sel(logits, dtype, -np.asarray(bias, np.float32)))],
+        [lambda: pins.check_biased_topk_bruteforce(X), lambda: pins.check_biased_topk_dominant(X)]),
+    "bias update with the wrong sign": (
+        [(X, "bias_update", lambda bias, counts, T, k, gamma: _orig_bu(bias, counts, T, k, -gamma))],
+        [lambda: pins.check_bias_update_hand(X), lambda: pins.check_bias_update_balances(X, R)]),
+    "bias update against the floor of the mean": (
+        [(X, "bias_update", lambda bias, counts, T, k, gamma: (np.asarray(bias, np.float32) + np.float32(gamma) * np.sign(
+            (T * k) // len(counts) - np.asarray(counts)).astype(np.float32)).astype(np.float32))],
+        [lambda: pins.check_bias_update_hand(X)]),
+    "masked P divided by T instead of T*k": (
+        [(X, "mean_router_prob_masked", lambda p, idx, k: (p * X.pick_mask(idx, p.shape[1])).sum(axis=0) / p.shape[0])],
+        [lambda: pins.check_masked_p_closed_forms(X, R)]),
+    "renormalised gate gradient without the p/S^2 term": (
+        [(X, "grad_wrt_probs", lambda *a: _no_quotient_term(*a))],
+        [lambda: pins.check_full_grad_finite_difference(X, R)]),
+    "masked aux gradient without the mask": (
+        [(X, "grad_wrt_probs", lambda p, idx, f, a, g, T, k, dg, rn, masked: _orig_gwp(p, idx, f, a, g * (1.0 / k if masked else 1.0), T, k, dg, rn, False))],
+        [lambda: pins.check_full_grad_finite_difference(X, R)]),
+    "softmax backward without the row-sum term": (
+        [(X, "softmax_backward", lambda p, dp: p * dp)],
+        [lambda: pins.check_full_grad_finite_difference(X, R), lambda: pins.check_full_grad_structure(X, R)]),
 }
+
+_orig_sel = X.selection_scores
+_orig_bu = X.bias_update
+_orig_gwp = X.grad_wrt_probs
+
+
+def _no_quotient_term(p, idx, f, alpha, grad_scale, T, k, dgate, renorm, masked_p):
+    dp = _orig_gwp(p, idx, f, alpha, grad_scale, T, k, None, renorm, masked_p)
+    if dgate is not None:
+        rows = np.arange(p.shape[0])
+        S = np.take_along_axis(p, idx, axis=1).sum(axis=1) if renorm else 1.0
+        for j in range(idx.shape[1]):
+            dp[rows, idx[:, j]] += dgate[:, j] / S
+    return dp
+
 
 _orig_grad = R.aux_loss_grad
 _orig_dispatch = D.dispatch
