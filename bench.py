@@ -375,6 +375,89 @@ def time_calls(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     return out
 
 
+def _graph_us(torch, device, call, reps: int) -> float:
+    """Mean time of `call(i)` for i in 0..reps-1, as one CUDA graph replayed
+    between two CUDA events (after three eager warm-up calls and one replay)."""
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            call(i)
+    stream = torch.cuda.current_stream(device)
+    g.replay()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    return a.elapsed_time(b) / reps * 1e3
+
+
+def time_next_steps(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
+    """The method's next steps through the C ABI: the forward with bias routing
+    and the in-place bias update, the forward with masked P, the full backward
+    through the gates, and a bias-routed training step (fwd_ex + dispatch +
+    bwd_full).  Each is a CUDA graph of `reps` calls over buffer sets rotated
+    at least 3x L2 apart, with its algorithmic bytes per call."""
+    import moe_expert_routing_router_gb300 as mr
+    esize = 2 if w.dtype == "bf16" else 4
+    T, E, k = w.T, w.E, w.k
+    fwd_b = T * E * esize + T * k * 8                     # logits in; idx, gate out
+    bwd_b = T * E * (esize + 4) + T * k * 8               # logits, idx, dgate in; dlogits out
+    step_b = T * E * (esize + 4) + T * k * 20             # + perm, slot out
+    x0 = to_device(synth.router_logits(w), w.dtype, torch, device)
+    ws = mr.Workspace(device)
+    rng = np.random.default_rng(1)
+    bias = torch.from_numpy((rng.standard_normal(E) * 0.5).astype(np.float32)).to(device)
+    ref = mr.moe_router_fwd_ex(x0, k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, bias=bias, ws=ws)
+    n_sets = max(2, math.ceil(3 * L2_BYTES / fwd_b))
+    xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
+    bufs = [out_buffers(w, torch, device) for _ in range(n_sets)]
+    idxs = [ref["idx"].clone() for _ in range(n_sets)]
+    dgates = [torch.randn(T, k, device=device) for _ in range(n_sets)]
+    fo = lambda j: {kk: bufs[j][kk] for kk in ("idx", "gate", "counts", "f", "P", "scalars", "rank_load")}
+    do = lambda j: {kk: bufs[j][kk] for kk in ("perm", "slot", "offsets", "kept", "n_dropped")}
+
+    def fwd_bias(i):
+        j = i % n_sets
+        mr.moe_router_fwd_ex(xs[j], k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, bias=bias,
+                             bias_gamma=1e-3, bias_out=bias, ws=ws, out=fo(j))
+
+    def fwd_masked(i):
+        j = i % n_sets
+        mr.moe_router_fwd_ex(xs[j], k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, masked_p=True,
+                             ws=ws, out=fo(j))
+
+    def bwd_full(i):
+        j = i % n_sets
+        mr.moe_router_bwd_full(xs[j], ref["f"], w.alpha, 1.0, idx=idxs[j], dgate=dgates[j],
+                               renorm=int(w.renorm), dlogits=bufs[j]["dlogits"])
+
+    def step(i):
+        j = i % n_sets
+        o = fo(j)
+        mr.moe_router_fwd_ex(xs[j], k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, bias=bias,
+                             bias_gamma=1e-3, bias_out=bias, ws=ws, out=o)
+        mr.moe_dispatch(o["idx"], E, w.capacity_factor, ws=ws, out=do(j))
+        mr.moe_router_bwd_full(xs[j], o["f"], w.alpha, 1.0, idx=o["idx"], dgate=dgates[j],
+                               renorm=int(w.renorm), dlogits=bufs[j]["dlogits"])
+
+    out = {"workload": w.name}
+    for name, fn, b in (("moe_router_fwd_ex (bias routing + update)", fwd_bias, fwd_b),
+                        ("moe_router_fwd_ex (masked P)", fwd_masked, fwd_b),
+                        ("moe_router_bwd_full (gates + aux)", bwd_full, bwd_b),
+                        ("bias-routed step (fwd_ex + dispatch + bwd_full)", step, step_b)):
+        us = _graph_us(torch, device, fn, reps)
+        gbs = b / (us * 1e-6) / 1e9
+        out[name] = {"us_per_call": round(us, 2), "tokens_per_s": round(T / (us * 1e-6), 1),
+                     "algorithmic_bytes": b, "achieved_gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm_gbs, 4)}
+    del xs, bufs, idxs, dgates
+    return out
+
+
 def time_sinkhorn(torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     """The batched TAOT Sinkhorn call, timed as a CUDA graph of `reps` calls on
     the 1024-microbatch workload.  Its bound is the HBM write of the plan."""
@@ -583,6 +666,8 @@ def run_ours(args) -> dict:
         line["separate_calls"] = {name: time_calls(synth.ROUTER_WORKLOADS[name], torch, device, pk["hbm_gbs"])
                                   for name in (w.name, EXTRA_WORKLOADS[-1])}
         line["sinkhorn"] = time_sinkhorn(torch, device, pk["hbm_gbs"])
+        line["next_steps"] = {name: time_next_steps(synth.ROUTER_WORKLOADS[name], torch, device, pk["hbm_gbs"])
+                              for name in (w.name, EXTRA_WORKLOADS[-1])}
     if dist_ctx.rank == 0:
         cb = time_oracle(w, budget_s=args.cpu_seconds, min_steps=2)
         line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}

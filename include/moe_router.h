@@ -4,7 +4,9 @@
  * The hot path of MoE expert routing with equal-cost load balancing: router
  * softmax and top-k, the Switch auxiliary balance loss and its closed-form
  * gradient, a capacity-limited stable token->expert dispatch, and the batched
- * topology-aware Sinkhorn-Knopp flow plan of TAOT Phase 1.
+ * topology-aware Sinkhorn-Knopp flow plan of TAOT Phase 1.  Beside them: the
+ * aux-loss-free bias routing, the masked P_i variant and the full router
+ * backward through the gates.
  *
  * Sources (cited by title and section):
  *   [P1] the three-layer load-balancing article (LVS, NIC Teaming, MoE
@@ -228,6 +230,63 @@ MOE_API moe_status moe_router_step_static(const void* logits, moe_dtype dt, int6
                                           float* scalars, int32_t* rank_load,
                                           int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
                                           int32_t* n_dropped, float* dlogits, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Aux-loss-free bias routing, masked P_i, full backward through the gates   */
+/* ------------------------------------------------------------------------ */
+
+/* Router forward with two options of the method that moe_router_fwd does not
+ * take, computed by a plain (non-cooperative) streaming kernel whose last CTA
+ * adds up the per-CTA partials:
+ *
+ *   Bias routing ([P1] §4.3, aux-loss-free balancing): each expert carries a
+ *   scalar bias b_e on its router logit that steers which experts are picked.
+ *   Top-k ranks s[t,e] = fp32(z[t,e]) + b_e (one fp32 addition, round to
+ *   nearest; ties to the lower expert index); softmax, gates, P and the
+ *   backward use the unbiased z.  bias [E] fp32, or NULL for b = 0.
+ *   With bias_out non-NULL the call also writes the updated bias
+ *       bias_out[e] = b_e + bias_gamma * sign(T*k/E - counts[e])
+ *   (the sign from the exact integer comparison of counts[e]*E with T*k,
+ *   sign 0 -> no change; one fp32 addition): an overloaded expert's bias goes
+ *   down, an idle one's up.  bias_out may alias bias (in-place update).
+ *
+ *   Masked P ([P2] §3.1, the code of [P1] §4.4): with masked_p != 0,
+ *       P[e] = (1/(T*k)) * sum_t p[t,e] * [e is one of t's picks]
+ *   instead of the unmasked mean (1/T) sum_t p[t,e] ([P1] §4.2).  balance and
+ *   L_aux use this P.
+ *
+ * Every other argument and output is that of moe_router_fwd (same layout,
+ * same scalars, same workspace size: moe_router_workspace_size; the
+ * workspace must have been zeroed once by moe_workspace_init and is left
+ * reusable).  With bias = NULL and masked_p = 0 the picks and counts equal
+ * moe_router_fwd's bit for bit, the floating outputs to rounding.
+ * bias_gamma must be finite.  Needs no grid barrier and never waits. */
+MOE_API moe_status moe_router_fwd_ex(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                             float alpha, int32_t renorm, int32_t n_ranks,
+                             const float* bias, int32_t masked_p, float bias_gamma, float* bias_out,
+                             int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                             float* scalars, int32_t* rank_load,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Full router backward: the gradient with respect to the logits of
+ *     L = sum_{t,j} dgate[t,j] * gate[t,j](z)  +  grad_scale * L_aux(z),
+ * the picks idx and f held constant (top-k is piecewise constant; f carries
+ * no gradient, [P1] §4.2).  dgate [T,k] fp32 is the main loss's upstream
+ * gradient of the gates written by the forward; gate[t,j] = p[t,idx[t,j]]
+ * (renorm = 0) or that p divided by the sum of the row's picked p (renorm = 1;
+ * -1 = automatic: renorm iff k > 1).  L_aux uses the unmasked P_i, or the
+ * masked P_i with masked_p != 0 (then its gradient reaches the picked logits
+ * only through P).  Per row, with dp the gradient with respect to p:
+ *     dlogits[t,j] = p[t,j] * (dp[t,j] - sum_i p[t,i] dp[t,i]).
+ * dgate may be NULL (aux loss only: with masked_p = 0 this is moe_router_bwd);
+ * idx [T,k] int32 is required when dgate is given or masked_p != 0, else may
+ * be NULL; its values must lie in [0,E) (others give unspecified results but
+ * every access stays in bounds).  dlogits [T,E] fp32 is written, not
+ * accumulated.  No workspace. */
+MOE_API moe_status moe_router_bwd_full(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                               float alpha, const float* f, float grad_scale, int32_t masked_p,
+                               const int32_t* idx, const float* dgate, int32_t renorm,
+                               float* dlogits, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* TAOT Phase 1: batched topology-aware Sinkhorn flow plan                  */

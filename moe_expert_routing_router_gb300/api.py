@@ -18,7 +18,7 @@ from ._native import MOE_DTYPE_BF16, MOE_DTYPE_FP32, MOE_NUM_SCALARS, SCALAR_NAM
 
 __all__ = [
     "Workspace", "moe_router_fwd", "moe_router_bwd", "moe_dispatch", "moe_dispatch_capacity",
-    "moe_router_step", "moe_router_step_static", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
+    "moe_router_step", "moe_router_step_static", "moe_router_fwd_ex", "moe_router_bwd_full", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
 ]
 
 _DTYPES = {torch.float32: MOE_DTYPE_FP32, torch.bfloat16: MOE_DTYPE_BF16}
@@ -138,6 +138,79 @@ def moe_router_bwd(logits: torch.Tensor, f: torch.Tensor, alpha: float, grad_sca
     st = lib().moe_router_bwd(_ptr(logits), _DTYPES[logits.dtype], T, E, float(alpha), _ptr(f), float(grad_scale),
                               _ptr(dl), _stream_handle(stream))
     check(st, "moe_router_bwd")
+    return dl
+
+
+def moe_router_fwd_ex(logits: torch.Tensor, k: int, alpha: float, renorm: int = -1, n_ranks: int = 0,
+                      bias: torch.Tensor | None = None, masked_p: bool = False, bias_gamma: float = 0.0,
+                      bias_out: torch.Tensor | bool | None = None, ws: Workspace | None = None,
+                      out: dict | None = None, stream: torch.cuda.Stream | None = None) -> dict:
+    """Router forward with bias routing and/or masked P (C: moe_router_fwd_ex).
+
+    ``bias`` [E] fp32 steers selection only; ``bias_out`` is a tensor to
+    receive the updated bias (it may be ``bias`` itself), True for a new one,
+    or None for no update.  The result holds the outputs of moe_router_fwd
+    and, with an update, ``bias_out``.
+    """
+    _need_cuda("logits", logits)
+    if logits.dtype not in _DTYPES or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 or bfloat16 tensor")
+    T, E = logits.shape
+    if bias is not None:
+        _need_cuda("bias", bias, torch.float32)
+        if bias.numel() != E:
+            raise ValueError("bias must have E elements")
+    if bias_out is True:
+        bias_out = torch.empty(E, dtype=torch.float32, device=logits.device)
+    elif bias_out is False:
+        bias_out = None
+    if bias_out is not None:
+        _need_cuda("bias_out", bias_out, torch.float32)
+        if bias_out.numel() != E:
+            raise ValueError("bias_out must have E elements")
+    o = _fwd_outputs(T, E, k, n_ranks, logits.device, out)
+    ws = ws or _default_ws(logits.device, stream)
+    wp, wn = ws.ensure(T, E, k, stream)
+    st = lib().moe_router_fwd_ex(_ptr(logits), _DTYPES[logits.dtype], T, E, k, float(alpha), int(renorm),
+                                 int(n_ranks), _ptr(bias), int(bool(masked_p)), float(bias_gamma), _ptr(bias_out),
+                                 _ptr(o["idx"]), _ptr(o["gate"]), _ptr(o["counts"]), _ptr(o["f"]), _ptr(o["P"]),
+                                 _ptr(o["scalars"]), _ptr(o["rank_load"]) if n_ranks > 0 else None,
+                                 wp, wn, _stream_handle(stream))
+    check(st, "moe_router_fwd_ex")
+    if bias_out is not None:
+        o["bias_out"] = bias_out
+    return o
+
+
+def moe_router_bwd_full(logits: torch.Tensor, f: torch.Tensor, alpha: float, grad_scale: float = 1.0,
+                        idx: torch.Tensor | None = None, dgate: torch.Tensor | None = None, renorm: int = -1,
+                        masked_p: bool = False, k: int | None = None, dlogits: torch.Tensor | None = None,
+                        stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Gradient of sum(dgate * gate) + grad_scale * L_aux with respect to the logits,
+    picks and f held constant (C: moe_router_bwd_full)."""
+    _need_cuda("logits", logits)
+    _need_cuda("f", f, torch.float32)
+    if logits.dtype not in _DTYPES or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 or bfloat16 tensor")
+    T, E = logits.shape
+    if f.numel() != E:
+        raise ValueError("f must have E elements")
+    if idx is not None:
+        _need_cuda("idx", idx, torch.int32)
+        if idx.dim() != 2 or idx.shape[0] != T:
+            raise ValueError("idx must be [T, k]")
+        k = idx.shape[1]
+    if dgate is not None:
+        _need_cuda("dgate", dgate, torch.float32)
+        if idx is None or tuple(dgate.shape) != tuple(idx.shape):
+            raise ValueError("dgate needs idx of the same [T, k] shape")
+    if k is None:
+        raise ValueError("k is needed when idx is not given")
+    dl = _out({"dlogits": dlogits}, "dlogits", (T, E), torch.float32, logits.device)
+    st = lib().moe_router_bwd_full(_ptr(logits), _DTYPES[logits.dtype], T, E, int(k), float(alpha), _ptr(f),
+                                   float(grad_scale), int(bool(masked_p)), _ptr(idx), _ptr(dgate), int(renorm),
+                                   _ptr(dl), _stream_handle(stream))
+    check(st, "moe_router_bwd_full")
     return dl
 
 

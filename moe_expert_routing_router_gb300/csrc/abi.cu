@@ -15,6 +15,7 @@
 #include <unordered_map>
 
 #include "moe_router.h"
+#include "router_ext.cuh"
 #include "router_kernels.cuh"
 #include "router_table.h"
 #include "sinkhorn.h"
@@ -330,6 +331,24 @@ moe_status check_fwd_outputs(int32_t k, float alpha, int32_t renorm, int32_t n_r
   return MOE_OK;
 }
 
+// The bias-routing / masked-P forward and full-backward kernels for (dtype, E):
+// the vector-load layout with the smallest coverage when rows are a multiple
+// of 16 bytes and the arrays 16-byte aligned, else the one-element-per-load
+// layout.
+const moe::ExtVariant* pick_ext_variant(moe_dtype dt, int E, bool aligned16) {
+  const int esize = dt == MOE_DTYPE_BF16 ? 2 : 4;
+  const bool vec_ok = aligned16 && (E * esize) % 16 == 0;
+  int n = 0;
+  const moe::ExtVariant* all = dt == MOE_DTYPE_BF16 ? moe::ext_variants_bf16(&n) : moe::ext_variants_fp32(&n);
+  auto cover = [](const moe::ExtVariant* v) { return v->LPR * v->VW * v->NV; };
+  const moe::ExtVariant* best = nullptr;
+  for (int pass = vec_ok ? 1 : 0; pass >= 0 && !best; --pass)
+    for (int i = 0; i < n; ++i)
+      if (all[i].vec == pass && cover(&all[i]) >= E && E % all[i].VW == 0 && (!best || cover(&all[i]) < cover(best)))
+        best = &all[i];
+  return best;
+}
+
 }  // namespace
 
 extern "C" {
@@ -543,6 +562,96 @@ moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t R, int32
   p.status = status;
   cudaError_t err = moe::launch_taot_sinkhorn(p, stream);
   if (err != cudaSuccess) return cuda_fail(err, "taot_sinkhorn launch");
+  return MOE_OK;
+}
+
+moe_status moe_router_fwd_ex(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                             float alpha, int32_t renorm, int32_t n_ranks,
+                             const float* bias, int32_t masked_p, float bias_gamma, float* bias_out,
+                             int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                             float* scalars, int32_t* rank_load,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_router_args(logits, dt, T, E, k);
+  if (s != MOE_OK) return s;
+  if ((s = check_fwd_outputs(k, alpha, renorm, n_ranks, E, idx, gate, counts, f, P, scalars, rank_load)) != MOE_OK) return s;
+  if ((s = check_ws(ws, ws_bytes, E)) != MOE_OK) return s;
+  if (!std::isfinite(bias_gamma)) return fail(MOE_ERR_INVALID, "bias_gamma must be finite");
+  if ((bias && !aligned(bias, 4)) || (bias_out && !aligned(bias_out, 4))) return fail(MOE_ERR_INVALID, "bias is not 4-byte aligned");
+  const moe::ExtVariant* v = pick_ext_variant(dt, E, aligned(logits, 16));
+  if (!v) return fail(MOE_ERR_INVALID, "no kernel variant for E = %d", E);
+  DeviceInfo d;
+  int dev = 0;
+  if ((s = device_info(&d, &dev)) != MOE_OK) return s;
+  int blocks = 0;
+  if ((s = occupancy(v->fwd, moe::kExtFwdThreads, 0, dev, &blocks)) != MOE_OK) return s;
+  const int64_t rows_per_cta = int64_t(moe::kExtFwdWarps) * (moe::kWarp / v->LPR);
+  const int64_t want = (T + rows_per_cta - 1) / rows_per_cta;
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>({want, int64_t(blocks) * d.sms, int64_t(kGridMax)})));
+  const WsLayout w = ws_layout(E);
+  char* base = static_cast<char*>(ws);
+  moe::FwdExParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.logits = logits;
+  p.T = T;
+  p.E = E;
+  p.k = k;
+  p.renorm = renorm < 0 ? (k > 1) : renorm;
+  p.masked_p = masked_p != 0;
+  p.bias = bias;
+  p.alpha = alpha;
+  p.n_ranks = n_ranks;
+  p.gamma = bias_gamma;
+  p.bias_out = bias_out;
+  p.idx = idx; p.gate = gate; p.counts = counts; p.f = f; p.P = P; p.scalars = scalars; p.rank_load = rank_load;
+  p.tile_hist = reinterpret_cast<int32_t*>(base + w.tile_hist);
+  p.P_part = reinterpret_cast<float*>(base + w.p_part);
+  p.G_stride = kGridMax;
+  p.done = &reinterpret_cast<moe::Ctrl*>(base + w.ctrl)->ext_done;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernel(v->fwd, dim3(grid), dim3(moe::kExtFwdThreads), args, 0, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
+  return MOE_OK;
+}
+
+moe_status moe_router_bwd_full(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                               float alpha, const float* f, float grad_scale, int32_t masked_p,
+                               const int32_t* idx, const float* dgate, int32_t renorm,
+                               float* dlogits, moe_stream_t stream) {
+  moe_status s = check_router_args(logits, dt, T, E, k);
+  if (s != MOE_OK) return s;
+  if (!(alpha >= 0.f) || !std::isfinite(alpha)) return fail(MOE_ERR_INVALID, "alpha must be finite and >= 0");
+  if (!std::isfinite(grad_scale)) return fail(MOE_ERR_INVALID, "grad_scale must be finite");
+  if (renorm < -1 || renorm > 1) return fail(MOE_ERR_INVALID, "renorm must be -1, 0 or 1");
+  if (!f || !dlogits) return fail(MOE_ERR_INVALID, "f or dlogits is NULL");
+  if ((dgate || masked_p) && !idx) return fail(MOE_ERR_INVALID, "idx is NULL but dgate or masked_p needs the picks");
+  if (!aligned(dlogits, 4) || !aligned(f, 4) || (idx && !aligned(idx, 4)) || (dgate && !aligned(dgate, 4)))
+    return fail(MOE_ERR_INVALID, "an array is not 4-byte aligned");
+  const moe::ExtVariant* v = pick_ext_variant(dt, E, aligned(logits, 16) && aligned(dlogits, 16));
+  if (!v) return fail(MOE_ERR_INVALID, "no kernel variant for E = %d", E);
+  DeviceInfo d;
+  int dev = 0;
+  if ((s = device_info(&d, &dev)) != MOE_OK) return s;
+  int blocks = 0;
+  if ((s = occupancy(v->bwd, moe::kExtBwdThreads, 0, dev, &blocks)) != MOE_OK) return s;
+  const int64_t rows_per_block = int64_t(moe::kExtBwdThreads / moe::kWarp) * (moe::kWarp / v->LPR);
+  const int64_t want = (T + rows_per_block - 1) / rows_per_block;
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(blocks) * d.sms)));
+  moe::BwdFullParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.logits = logits;
+  p.T = T;
+  p.E = E;
+  p.k = k;
+  p.f = f;
+  p.masked_p = masked_p != 0;
+  p.coef = float(double(grad_scale) * double(alpha) * double(E) / (masked_p ? double(T) * double(k) : double(T)));
+  p.idx = idx;
+  p.dgate = dgate;
+  p.renorm = renorm < 0 ? (k > 1) : renorm;
+  p.dlogits = dlogits;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchKernel(v->bwd, dim3(grid), dim3(moe::kExtBwdThreads), args, 0, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
   return MOE_OK;
 }
 

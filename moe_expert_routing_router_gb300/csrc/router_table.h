@@ -20,6 +20,17 @@ const RouterVariant* router_variants_bf16_staged(int* n);
 const RouterVariant* router_variants_bf16_direct(int* n);
 const RouterVariant* router_variants_fp32_staged(int* n);
 const RouterVariant* router_variants_fp32_direct(int* n);
+// Kernels of the forward with bias routing / masked P and of the full
+// backward, per row layout.  vec: 16-byte rows read VW elements per load.
+struct ExtVariant {
+  int LPR, VW, NV;
+  int vec;
+  const void* fwd;         // router_fwd_ex_kernel
+  const void* bwd;         // router_bwd_full_kernel
+};
+const ExtVariant* ext_variants_bf16(int* n);
+const ExtVariant* ext_variants_fp32(int* n);
+
 // The dispatch-only persistent kernel (compiled for kDispatchMinBlocks CTAs per SM).
 const void* dispatch_kernel();
 constexpr int kDispatchMinBlocks = 1;

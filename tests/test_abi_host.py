@@ -127,3 +127,27 @@ def test_bwd_and_sinkhorn_reject_bad_arguments(native_lib):
 def test_status_strings(native_lib):
     for s in range(6):
         assert native_lib.moe_status_string(s)
+
+
+def test_fwd_ex_and_bwd_full_reject_bad_arguments(native_lib):
+    fx = native_lib.moe_router_fwd_ex
+    args = [FAKE, 1, 16, 8, 2, 0.01, -1, 0, None, 0, 0.0, None] + [FAKE] * 6 + [None, FAKE, 1 << 30, None]
+    for pos, val, want in [(2, 0, 1), (4, 9, 1), (1, 7, 2), (5, -1.0, 1), (6, 3, 1), (7, 3, 1),
+                           (10, float("inf"), 1), (8, FAKE + 2, 1), (11, FAKE + 1, 1), (13, None, 1),
+                           (19, FAKE + 8, 1), (20, 64, 5)]:
+        bad = list(args)
+        bad[pos] = val
+        assert fx(*bad) == want, (pos, val)
+        assert native_lib.moe_last_error()
+    bf = native_lib.moe_router_bwd_full
+    args = [FAKE, 1, 16, 8, 2, 0.01, FAKE, 1.0, 0, FAKE, FAKE, -1, FAKE, None]
+    for pos, val, want in [(6, None, 1), (12, None, 1), (5, float("nan"), 1), (7, float("inf"), 1),
+                           (11, 2, 1), (9, None, 1), (12, FAKE + 2, 1), (10, FAKE + 1, 1), (4, 0, 1)]:
+        bad = list(args)
+        bad[pos] = val
+        assert bf(*bad) == want, (pos, val)
+    bad = list(args)
+    bad[10] = None                                   # no dgate: masked P still needs idx
+    bad[8] = 1
+    bad[9] = None
+    assert bf(*bad) == 1
