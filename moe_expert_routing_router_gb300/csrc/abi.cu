@@ -586,7 +586,8 @@ moe_status moe_router_fwd_ex(const void* logits, moe_dtype dt, int64_t T, int32_
   if ((s = occupancy(v->fwd, moe::kExtFwdThreads, 0, dev, &blocks)) != MOE_OK) return s;
   const int64_t rows_per_cta = int64_t(moe::kExtFwdWarps) * (moe::kWarp / v->LPR);
   const int64_t want = (T + rows_per_cta - 1) / rows_per_cta;
-  const int grid = int(std::max<int64_t>(1, std::min<int64_t>({want, int64_t(blocks) * d.sms, int64_t(kGridMax)})));
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(blocks) * d.sms)));
+  static_assert(kGroupHistBytes >= size_t(MOE_MAX_EXPERTS) * 20, "accumulators fit the group-sum region");
   const WsLayout w = ws_layout(E);
   char* base = static_cast<char*>(ws);
   moe::FwdExParams p;
@@ -603,9 +604,11 @@ moe_status moe_router_fwd_ex(const void* logits, moe_dtype dt, int64_t T, int32_
   p.gamma = bias_gamma;
   p.bias_out = bias_out;
   p.idx = idx; p.gate = gate; p.counts = counts; p.f = f; p.P = P; p.scalars = scalars; p.rank_load = rank_load;
-  p.tile_hist = reinterpret_cast<int32_t*>(base + w.tile_hist);
-  p.P_part = reinterpret_cast<float*>(base + w.p_part);
-  p.G_stride = kGridMax;
+  // The accumulators share the group-sum region: both kernels find it zero at
+  // launch and leave it zero, so calls of either kind can follow each other.
+  p.acc_hi = reinterpret_cast<unsigned long long*>(base + w.group_hist);
+  p.acc_lo = p.acc_hi + E;
+  p.acc_count = reinterpret_cast<int32_t*>(p.acc_lo + E);
   p.done = &reinterpret_cast<moe::Ctrl*>(base + w.ctrl)->ext_done;
   void* args[] = {&p};
   cudaError_t e = cudaLaunchKernel(v->fwd, dim3(grid), dim3(moe::kExtFwdThreads), args, 0, stream);

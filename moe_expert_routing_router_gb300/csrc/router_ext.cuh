@@ -8,18 +8,21 @@
 //     gates (plain p, or p renormalised over the picks) through the gate and
 //     the softmax, added to the closed-form gradient of the aux loss.
 //
-// The forward is one launch: every CTA streams rows of its grid-stride share,
-// publishes its per-expert counts and sums of p, and the CTA that counts
-// itself done last (no waiting: the others have already left) adds the
-// partials up in a fixed order and writes the per-expert outputs, the batch
-// scalars and the updated bias.  The backward is a plain streaming kernel.
+// The forward is one launch: every CTA streams rows of its grid-stride share
+// and adds its per-expert counts and sums of p into workspace accumulators
+// with integer atomics; the CTA that counts itself done last (no waiting: the
+// others have already left) writes the per-expert outputs, the batch scalars
+// and the updated bias, and clears the accumulators.  A CTA's sum of p enters
+// as two integers, its fixed-point value split at 2^-20 and 2^-64, so the
+// total is exact to 2^-64 whatever the order of the atomics: the result does
+// not depend on scheduling.  The backward is a plain streaming kernel.
 #pragma once
 
 #include "router_kernels.cuh"
 
 namespace moe {
 
-constexpr int kExtFwdThreads = 512;                   // one CTA per SM
+constexpr int kExtFwdThreads = 256;                   // two or more CTAs per SM
 constexpr int kExtFwdWarps = kExtFwdThreads / kWarp;
 constexpr int kExtBwdThreads = 256;
 
@@ -41,10 +44,11 @@ struct FwdExParams {
   float* P;                    // [E]
   float* scalars;              // [kNumScalars]
   int32_t* rank_load;          // [n_ranks] or null
-  int32_t* tile_hist;          // workspace [E][G_stride]: per-CTA counts
-  float* P_part;               // workspace [E][G_stride]: per-CTA sums of p
-  int G_stride;
-  unsigned long long* done;    // workspace counter of finished CTAs (zero between launches)
+  // workspace accumulators, zero between launches (the last CTA clears them)
+  int32_t* acc_count;          // [E] counts
+  unsigned long long* acc_hi;  // [E] sums of p: integer parts of (CTA sum) * 2^20
+  unsigned long long* acc_lo;  // [E] and the remaining fraction * 2^44
+  unsigned long long* done;    // counter of finished CTAs
 };
 
 struct BwdFullParams {
@@ -62,92 +66,91 @@ struct BwdFullParams {
 
 // ---------------------------------------------------------------------------
 // Forward, the row part.  Lane l of a row group holds the row's columns
-// col_of(v, l, i) (the layout of router_kernels.cuh).  Selection keys are
-// 64-bit: the order-preserving image of the fp32 score z + b above the
-// inverted column, so the group maximum is the largest score and, among equal
-// scores, the lowest column.  k rounds each take the group maximum of the
-// keys below the previous pick.
+// col_of(v, l, i) (the layout of router_kernels.cuh), in ascending column
+// order along its elements.  Selection works on the order-preserving 32-bit
+// image of the fp32 score z + b; each of the k rounds takes the group maximum
+// of the images, then the lowest column holding it (ties go to the lower
+// expert index), and clears that element's image to 0 (below every score's
+// image, -inf included): afterwards exactly the picked elements read 0.
 // ---------------------------------------------------------------------------
+template <int LPR>
+__device__ __forceinline__ uint32_t group_min_u32(uint32_t x) {
+  if constexpr (LPR == 32) {
+    return __reduce_min_sync(0xffffffffu, x);
+  } else {
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) x = min(x, __shfl_xor_sync(0xffffffffu, x, off));
+    return x;
+  }
+}
+
+// Larger value, larger image; -0 is folded into +0 first.
+__device__ __forceinline__ uint32_t ordered_image(float x) {
+  const uint32_t b = __float_as_uint(__fadd_rn(x, 0.f));
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 template <class DT, int LPR, int VW, int NV>
 struct ExtRow {
   static constexpr int EPL = VW * NV;
   using Raw = typename DT::Raw;
 
-  // Softmax statistics of the unbiased row: e[i] = 2^(z_i log2e - max log2e), inv_s = 1 / sum e.
-  static __device__ __forceinline__ void softmax(const Raw (&raw)[EPL], bool valid, float (&e)[EPL], float& inv_s) {
+  // Softmax statistics of the unbiased row: e[i] = 2^(z_i log2e - mL), inv_s = 1 / sum e.
+  static __device__ __forceinline__ void softmax(const Raw (&raw)[EPL], bool valid, float (&e)[EPL], float& mL,
+                                                 float& inv_s) {
     float m = -3.402823466e38f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) m = fmaxf(m, __uint_as_float(DT::bits(raw[i])));
-    const float mL = group_max<LPR>(m) * kLog2e;
+    mL = group_max<LPR>(m) * kLog2e;
     row_exp<DT, LPR, EPL>(raw, mL, e);
     const float s = group_sum<LPR>(tree_sum(e));
     inv_s = valid ? rcp_approx(s) : 0.f;
   }
 
-  // Top-k on z + b.  Returns the lane's own pick (lane j < k: pick j) with its
-  // e, the sum of the picks' e, and the mask of the lane's picked elements.
-  static __device__ __forceinline__ void select(const Raw (&raw)[EPL], const float (&bl)[EPL], const float (&e)[EPL],
-                                                int k, int l, int& my_col, float& my_e, float& pick_sum,
-                                                uint32_t& taken) {
-    long long key[EPL];
+  // Top-k on z + b: lane j < k receives pick j's column; hv[i] == 0 marks the
+  // lane's picked elements.
+  static __device__ __forceinline__ void select(const Raw (&raw)[EPL], const float (&bl)[EPL], int k, int l,
+                                                uint32_t (&hv)[EPL], int& my_col) {
 #pragma unroll
-    for (int v = 0; v < NV; ++v)
-#pragma unroll
-      for (int i = 0; i < VW; ++i) {
-        const float sv = __fadd_rn(__uint_as_float(DT::bits(raw[v * VW + i])), bl[v * VW + i]);
-        key[v * VW + i] = Fp32::key_from_bits(__float_as_uint(sv), col_lane_bits<LPR, VW>(l), col_elem_bits<LPR, VW>(v, i));
-      }
-    long long prev = 0x7fffffffffffffffll;
-    taken = 0u;
-    pick_sum = 0.f;
+    for (int i = 0; i < EPL; ++i) hv[i] = ordered_image(__fadd_rn(__uint_as_float(DT::bits(raw[i])), bl[i]));
+    const uint32_t lane_bits = col_lane_bits<LPR, VW>(l);
     my_col = 0;
-    my_e = 0.f;
     for (int j = 0; j < k; ++j) {
-      long long lk = Fp32::kKeyMin;
+      uint32_t lm = hv[0];
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) lk = (key[i] < prev && key[i] > lk) ? key[i] : lk;
-      const long long w = group_max_key<LPR>(lk);
-      float le = 0.f;
+      for (int i = 1; i + 1 < EPL; i += 2) lm = __vimax3_u32(lm, hv[i], hv[i + 1]);
+      if constexpr (EPL % 2 == 0) lm = max(lm, hv[EPL - 1]);
+      const uint32_t wv = group_max_key<LPR>(lm);
+      uint32_t lc = 0xffffffffu;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const bool hit = key[i] == w;
-        le = hit ? e[i] : le;
-        taken |= hit ? (1u << i) : 0u;
-      }
-      const float pe = group_sum<LPR>(le);          // the winner's e; every other lane adds 0
-      pick_sum += pe;
-      if (l == j) {
-        my_col = Fp32::key_col(w);
-        my_e = pe;
-      }
-      prev = w;
+      for (int v = NV - 1; v >= 0; --v)
+#pragma unroll
+        for (int i = VW - 1; i >= 0; --i) lc = hv[v * VW + i] == wv ? (lane_bits | col_elem_bits<LPR, VW>(v, i)) : lc;
+      const uint32_t wc = group_min_u32<LPR>(lc);
+      // the column fields are disjoint: wc - lane_bits is the element's field iff this lane holds wc
+      const uint32_t d = wc - lane_bits;
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int i = 0; i < VW; ++i) hv[v * VW + i] = d == col_elem_bits<LPR, VW>(v, i) ? 0u : hv[v * VW + i];
+      if (l == j) my_col = int(wc);
     }
   }
 };
 
 // The per-expert outputs, the batch scalars and the updated bias, by the CTA
-// that finished last.  Warp w adds up experts w, w + warps, ...: lane l the
-// CTAs l, l + 32, ... (a fixed order), then a fixed shuffle tree, so the
-// result does not depend on which CTA finishes last.  s_cnt / s_pe are the
-// CTA's own shared arrays (its partials are already published).
-__device__ __forceinline__ void ext_finalize(const FwdExParams& p, int G, int* s_cnt, float* s_pe) {
+// that finished last: the accumulated totals go to shared memory (s_cnt, and
+// the sums of p in double in s_pe) and the accumulators are cleared for the
+// next launch.
+__device__ __forceinline__ void ext_finalize(const FwdExParams& p, int* s_cnt, double* s_pe) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = int(blockDim.x >> 5);
-  for (int e = warp; e < p.E; e += nwarps) {
-    const int32_t* hc = p.tile_hist + (long long)e * p.G_stride;
-    const float* pc = p.P_part + (long long)e * p.G_stride;
-    int c = 0;
-    float s = 0.f;
-    for (int b = lane; b < G; b += kWarp) {
-      c += __ldcg(hc + b);
-      s += __ldcg(pc + b);
-    }
-    c = __reduce_add_sync(0xffffffffu, c);
-    s = warp_sum_f(s);
-    if (lane == 0) {
-      s_cnt[e] = c;
-      s_pe[e] = s;
-    }
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    s_cnt[e] = __ldcg(p.acc_count + e);
+    const unsigned long long hi = __ldcg(p.acc_hi + e), lo = __ldcg(p.acc_lo + e);
+    s_pe[e] = (double(hi) + double(lo) * 0x1p-44) * 0x1p-20;
+    p.acc_count[e] = 0;
+    p.acc_hi[e] = 0ull;
+    p.acc_lo[e] = 0ull;
   }
   __syncthreads();
   const long long TK = p.T * p.k;
@@ -156,7 +159,7 @@ __device__ __forceinline__ void ext_finalize(const FwdExParams& p, int G, int* s
     const int c = s_cnt[e];
     p.counts[e] = c;
     p.f[e] = float(double(c) / double(TK));
-    p.P[e] = float(double(s_pe[e]) / p_den);
+    p.P[e] = float(s_pe[e] / p_den);
     if (p.bias_out != nullptr) {
       // sign(T*k/E - count) from the exact integer comparison of count * E with T * k
       const long long d = TK - (long long)c * p.E;
@@ -170,7 +173,7 @@ __device__ __forceinline__ void ext_finalize(const FwdExParams& p, int G, int* s
     for (int e = lane; e < p.E; e += kWarp) {
       const int c = s_cnt[e];
       const float fe = float(double(c) / double(TK));
-      const float Pe = float(double(s_pe[e]) / p_den);
+      const float Pe = float(s_pe[e] / p_den);
       fp += double(fe) * double(Pe);
       const double d = double((long long)c * p.E - TK);
       d2 += d * d;
@@ -218,16 +221,16 @@ __device__ __forceinline__ void ext_finalize(const FwdExParams& p, int G, int* s
 }
 
 template <class DT, int LPR, int VW, int NV>
-__global__ void __launch_bounds__(kExtFwdThreads, 1) router_fwd_ex_kernel(const FwdExParams p) {
+__global__ void __launch_bounds__(kExtFwdThreads, 2) router_fwd_ex_kernel(const FwdExParams p) {
   using Row = ExtRow<DT, LPR, VW, NV>;
   using Raw = typename DT::Raw;
   constexpr int EPL = Row::EPL;
   constexpr int GPW = kWarp / LPR;
   constexpr int COLS = LPR * VW * NV;
-  static_assert(EPL <= 32, "taken mask");
   __shared__ float s_bias[COLS];
   __shared__ int s_hist[COLS];
   __shared__ float s_p[COLS];
+  __shared__ double s_pe[COLS];
   __shared__ int s_last;
   for (int c = threadIdx.x; c < COLS; c += blockDim.x) {
     s_bias[c] = (p.bias != nullptr && c < p.E) ? p.bias[c] : 0.f;
@@ -269,21 +272,28 @@ __global__ void __launch_bounds__(kExtFwdThreads, 1) router_fwd_ex_kernel(const 
       const bool ok = rg + nw < n_rg && tn < p.T;
       load_lane<DT, LPR, VW, NV, true>(X + (ok ? tn : 0) * (long long)p.E, p.E, l, ok, nxt);
     }
-    float e[EPL], inv_s;
-    Row::softmax(raw, valid, e, inv_s);
+    float e[EPL], mL, inv_s;
+    Row::softmax(raw, valid, e, mL, inv_s);
+    uint32_t hv[EPL];
     int my_col;
-    float my_e, pick_sum;
-    uint32_t taken;
-    Row::select(raw, bl, e, p.k, l, my_col, my_e, pick_sum, taken);
-    if (valid && l < p.k) {
+    Row::select(raw, bl, p.k, l, hv, my_col);
+    // The pick's e by the formula of row_exp from its logit (the same bits as
+    // its owner's e[i]); the row was just read, so the load hits L1.
+    const bool owner = valid && l < p.k;
+    Raw zr[1] = {DT::kNegInf};
+    if (owner) zr[0] = X[t * (long long)p.E + my_col];
+    float my_e[1];
+    row_exp<DT, LPR, 1>(zr, mL, my_e);
+    const float pick_sum = owners_sum<LPR>(my_e[0]);
+    if (owner) {
       const long long a = t * p.k + l;
       p.idx[a] = my_col;
-      p.gate[a] = p.renorm ? my_e * rcp_approx(pick_sum) : my_e * inv_s;
+      p.gate[a] = p.renorm ? my_e[0] * rcp_approx(pick_sum) : my_e[0] * inv_s;
       atomicAdd(&s_hist[my_col], 1);
     }
     if (p.masked_p) {
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) pacc[i] = ((taken >> i) & 1u) ? fmaf(e[i], inv_s, pacc[i]) : pacc[i];
+      for (int i = 0; i < EPL; ++i) pacc[i] = hv[i] == 0u ? fmaf(e[i], inv_s, pacc[i]) : pacc[i];
     } else {
 #pragma unroll
       for (int i = 0; i < EPL; ++i) pacc[i] = fmaf(e[i], inv_s, pacc[i]);
@@ -308,18 +318,21 @@ __global__ void __launch_bounds__(kExtFwdThreads, 1) router_fwd_ex_kernel(const 
     }
     __syncthreads();
   }
-  const long long G = gridDim.x;
   for (int c = threadIdx.x; c < p.E; c += blockDim.x) {
-    p.tile_hist[(long long)c * p.G_stride + blockIdx.x] = s_hist[c];
-    p.P_part[(long long)c * p.G_stride + blockIdx.x] = s_p[c];
+    if (s_hist[c] != 0) atomicAdd(p.acc_count + c, s_hist[c]);
+    const double q = double(s_p[c]) * 0x1p20;          // s_p >= 0, below 2^31: q < 2^51
+    const double hi = floor(q);
+    const unsigned long long lo = (unsigned long long)((q - hi) * 0x1p44);   // exact for s_p >= 2^-41
+    if (hi != 0.0) atomicAdd(p.acc_hi + c, (unsigned long long)hi);
+    if (lo != 0ull) atomicAdd(p.acc_lo + c, lo);
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(p.done, 1ull) == (unsigned long long)(G - 1);
+  if (threadIdx.x == 0) s_last = atomicAdd(p.done, 1ull) == (unsigned long long)(gridDim.x - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  ext_finalize(p, int(G), s_hist, s_p);
+  ext_finalize(p, s_hist, s_pe);
 }
 
 // ---------------------------------------------------------------------------
@@ -345,20 +358,26 @@ __global__ void __launch_bounds__(kExtBwdThreads) router_bwd_full_kernel(const B
   constexpr int EPL = VW * NV;
   constexpr int RPW = kWarp / LPR;
   constexpr int COLS = LPR * VW * NV;
+  constexpr int WARPS = kExtBwdThreads / kWarp;
   __shared__ float s_f[COLS];
+  // Per warp and row group: the picks' gradient terms scattered to their
+  // columns (zero elsewhere; every pick's slot is cleared after use).
+  __shared__ __align__(16) float s_g[WARPS][RPW][COLS];
   for (int c = threadIdx.x; c < COLS; c += blockDim.x) s_f[c] = c < p.E ? __ldg(p.f + c) : 0.f;
+  for (int c = threadIdx.x; c < WARPS * RPW * COLS; c += blockDim.x) (&s_g[0][0][0])[c] = 0.f;
   __syncthreads();
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane / LPR, l = lane % LPR;
-  const long long gw = (long long)blockIdx.x * (kExtBwdThreads / kWarp) + (threadIdx.x >> 5);
-  const long long nw = (long long)gridDim.x * (kExtBwdThreads / kWarp);
+  const long long gw = (long long)blockIdx.x * WARPS + warp;
+  const long long nw = (long long)gridDim.x * WARPS;
   const Raw* X = static_cast<const Raw*>(p.logits);
   const bool need_picks = p.dgate != nullptr || p.masked_p;
+  float* sg = s_g[warp][g];
   float fr[EPL];
 #pragma unroll
   for (int v = 0; v < NV; ++v)
 #pragma unroll
-    for (int i = 0; i < VW; ++i) fr[v * VW + i] = p.coef * s_f[col_of<LPR, VW>(v, l, i)];
+    for (int i = 0; i < VW; ++i) fr[v * VW + i] = p.masked_p ? 0.f : p.coef * s_f[col_of<LPR, VW>(v, l, i)];
   for (long long base = gw * RPW; base < p.T; base += nw * RPW) {
     const long long t = base + g;
     const bool valid = t < p.T;
@@ -367,12 +386,13 @@ __global__ void __launch_bounds__(kExtBwdThreads) router_bwd_full_kernel(const B
     load_lane<DT, LPR, VW, NV, true>(row, p.E, l, valid, raw);
     // lane j < k of the group loads pick j and its upstream gradient
     const bool owner = need_picks && valid && l < p.k;
-    int my_idx = -1;
+    int my_idx = 0;
     float my_dg = 0.f;
     if (owner) {
       my_idx = __ldg(p.idx + t * p.k + l);
       if (p.dgate != nullptr) my_dg = __ldg(p.dgate + t * p.k + l);
     }
+    const bool in_range = owner && unsigned(my_idx) < unsigned(p.E);   // out-of-range picks touch nothing
     float m = -3.402823466e38f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) m = fmaxf(m, __uint_as_float(DT::bits(raw[i])));
@@ -381,13 +401,13 @@ __global__ void __launch_bounds__(kExtBwdThreads) router_bwd_full_kernel(const B
     row_exp<DT, LPR, EPL>(raw, mL, e);
     const float s = group_sum<LPR>(tree_sum(e));
     const float inv_s = rcp_approx(s);
-    // G of the lane's own pick
+    // The gradient term of the lane's own pick: the masked aux term and G.
     float my_G = 0.f;
     if (p.dgate != nullptr) {
       if (p.renorm) {
         // e of the lane's pick, by the formula of row_exp (the same bits as its owner's e)
         Raw zr[1] = {DT::kNegInf};
-        if (owner && unsigned(my_idx) < unsigned(p.E)) zr[0] = row[my_idx];   // out-of-range picks read nothing
+        if (in_range) zr[0] = row[my_idx];
         float my_e[1];
         row_exp<DT, LPR, 1>(zr, mL, my_e);
         float Se = 0.f, acc = 0.f;
@@ -403,33 +423,32 @@ __global__ void __launch_bounds__(kExtBwdThreads) router_bwd_full_kernel(const B
         my_G = my_dg;
       }
     }
-    // the lane's picked elements (mask) and their G
-    float mk[EPL], gg[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      mk[i] = 0.f;
-      gg[i] = 0.f;
-    }
-    if (need_picks) {
-      for (int j = 0; j < p.k; ++j) {
-        const int cj = __shfl_sync(0xffffffffu, my_idx, g * LPR + j);
-        const float Gj = __shfl_sync(0xffffffffu, my_G, g * LPR + j);
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-          for (int i = 0; i < VW; ++i) {
-            const bool hit = col_of<LPR, VW>(v, l, i) == cj;
-            mk[v * VW + i] = hit ? 1.f : mk[v * VW + i];
-            gg[v * VW + i] = hit ? Gj : gg[v * VW + i];
-          }
-      }
-    }
+    __syncwarp();                                   // the previous row's slots are cleared
+    if (in_range) sg[my_idx] = (p.masked_p ? p.coef * s_f[my_idx] : 0.f) + my_G;
+    __syncwarp();
     float dp[EPL], pd[EPL];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      dp[i] = (p.masked_p ? fr[i] * mk[i] : fr[i]) + gg[i];
-      pd[i] = e[i] * dp[i];
+    for (int v = 0; v < NV; ++v) {
+      const int c0 = col_of<LPR, VW>(v, l, 0);
+      float gv[VW];
+      if constexpr (VW % 4 == 0) {
+#pragma unroll
+        for (int h = 0; h < VW / 4; ++h) {
+          const float4 q = *reinterpret_cast<const float4*>(sg + c0 + 4 * h);
+          gv[4 * h] = q.x; gv[4 * h + 1] = q.y; gv[4 * h + 2] = q.z; gv[4 * h + 3] = q.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < VW; ++i) gv[i] = sg[c0 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < VW; ++i) {
+        dp[v * VW + i] = fr[v * VW + i] + gv[i];
+        pd[v * VW + i] = e[v * VW + i] * dp[v * VW + i];
+      }
     }
+    __syncwarp();
+    if (in_range) sg[my_idx] = 0.f;
     const float w = inv_s * group_sum<LPR>(tree_sum(pd));      // sum_j p_j dp_j
     if (valid) {
       float* out = p.dlogits + t * (long long)p.E;

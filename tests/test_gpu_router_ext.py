@@ -246,3 +246,29 @@ def test_backward_full_without_dgate_matches_moe_router_bwd(mr, name):
     c = 2.0 * w.alpha * w.E / w.T
     scale = c * p * (f[None, :] + (p * f[None, :]).sum(axis=1, keepdims=True))
     assert_close("bwd_full vs bwd", a.cpu().numpy(), bb, 0.0, 4 * RTOL * scale + 1e-30)
+
+
+def test_interleaved_with_the_fused_step_on_one_workspace(mr):
+    """The forward's accumulators share the workspace with the fused step's
+    group sums: calls of both kinds and of different E follow each other on
+    one workspace, without a host sync, and each stays exact."""
+    ws = mr.Workspace()
+    cases = []
+    for name in ("zipf-top2-T65536-E64", "zipf-ep64-top6-T262144-E384"):
+        w, logits = workload_inputs(name, 2047)
+        cases.append((w, logits, to_device(logits, w.dtype), seeded_bias(w.E, 11)))
+    outs = []
+    for rep in range(2):
+        for w, logits, x, bias in cases:
+            st = mr.moe_router_step(x, w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks, ws=ws)
+            fx = mr.moe_router_fwd_ex(x, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks,
+                                      bias=torch.from_numpy(bias).cuda(), masked_p=bool(rep), bias_gamma=GAMMA,
+                                      bias_out=True, ws=ws)
+            outs.append((w, logits, bias, bool(rep), st, fx))
+    torch.cuda.synchronize()
+    for w, logits, bias, masked, st, fx in outs:
+        plain = oracle_forward_ex(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks, None, False, GAMMA)
+        assert_equal("step counts", st["counts"].cpu().numpy(), plain["counts"])
+        assert_equal("step idx", st["idx"].cpu().numpy(), plain["idx"])
+        want = oracle_forward_ex(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks, bias, masked, GAMMA)
+        check_forward(fx, want, w.n_ranks)
