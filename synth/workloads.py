@@ -118,6 +118,42 @@ def _encode(z64: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
+@dataclass(frozen=True)
+class EplbWorkload:
+    """Per-expert token counts of B independent problems (layers or
+    microbatches) for the replication and packing planner."""
+    name: str
+    workload_id: int
+    B: int
+    E: int
+    assignments: int           # T * k per problem
+    zipf_s: float
+    num_phys: int              # physical expert slots
+    num_gpus: int
+    num_nodes: int
+    num_groups: int            # contiguous expert groups (0: none)
+
+
+EPLB_WORKLOADS: dict[str, EplbWorkload] = {
+    "eplb-zipf-E384-B1024": EplbWorkload("eplb-zipf-E384-B1024", 5, B=1024, E=384, assignments=4096 * 6,
+                                         zipf_s=1.3, num_phys=448, num_gpus=64, num_nodes=8, num_groups=32),
+}
+
+
+def eplb_loads(w: EplbWorkload, B: int | None = None) -> np.ndarray:
+    """int64 [B, E] expert token counts: problem b draws a seeded permutation of
+    the experts, Zipf(s) probabilities over it, and a multinomial of
+    ``assignments`` draws."""
+    B = w.B if B is None else B
+    rng = _rng(0, w.workload_id)
+    out = np.empty((B, w.E), dtype=np.int64)
+    for b in range(B):
+        perm = rng.permutation(w.E)
+        p = (perm + 1.0) ** (-w.zipf_s)
+        out[b] = rng.multinomial(w.assignments, p / p.sum())
+    return out
+
+
 def router_logits(w: RouterWorkload, seed: int = 0) -> np.ndarray:
     """Logits of workload ``w``: float32 [T, E] for fp32, uint16 bf16 bits [T, E] for bf16."""
     rng = _rng(seed, w.workload_id)

@@ -490,3 +490,101 @@ def check_full_grad_structure(ext, router) -> None:
     # zero up to the rounding of sum_i p_i dp_i, which cancels exactly in real arithmetic
     assert np.abs(gate_only * (1.0 - mask)).max() <= 1e-14 * np.abs(gate_only).max()
     assert np.abs(gate_only * mask).max() > 1e-3
+
+
+# ----------------------------------------------------------------------------- EPLB (replication, packing)
+
+def check_packing_worked_example(eplb) -> None:
+    """The page's example: [9, 7, 5, 3] onto 2 nodes of 2 groups -> {9, 3} / {7, 5}, 12 / 12,
+    placed in the order 9, 7, 5, 3 (so 5 lands second on node 1 and 3 second on node 0)."""
+    g = golden("p3_s4_1_2_balanced_packing_example.json")
+    bins, pos, totals = eplb.balanced_packing(g["weights"], g["num_bins"])
+    assert list(bins) == g["bin_of_item"], bins
+    assert list(pos) == [0, 0, 1, 1], pos
+    assert list(totals) == g["bin_totals"], totals
+
+
+def check_packing_equal_weights_round_robin(eplb) -> None:
+    """Equal weights: the lightest non-full bin is always the next one in turn,
+    so item i goes to bin i mod G at position i // G."""
+    for N, G in ((12, 4), (8, 8), (6, 1), (64, 16)):
+        bins, pos, totals = eplb.balanced_packing([2.5] * N, G)
+        assert list(bins) == [i % G for i in range(N)]
+        assert list(pos) == [i // G for i in range(N)]
+        assert np.all(totals == 2.5 * (N // G))
+
+
+def check_packing_cardinality_and_mass(eplb) -> None:
+    """Every bin takes exactly N / G items, and the bins' totals hold all the weight;
+    a dominant item fills its bin with the lightest items only once the others are full."""
+    bins, pos, totals = eplb.balanced_packing([10.0, 1.0, 1.0, 1.0], 2)
+    assert list(bins) == [0, 1, 1, 0] and list(totals) == [11.0, 2.0]
+    rng = np.random.default_rng(60)
+    for N, G in ((48, 8), (30, 5), (7, 7), (24, 4)):
+        w = rng.random(N) * 10
+        if N == 24:
+            w[:3] *= 50                          # a few dominant items: the capacity binds
+        bins, pos, totals = eplb.balanced_packing(w, G)
+        assert np.all(np.bincount(bins, minlength=G) == N // G)
+        for b in range(G):
+            assert sorted(pos[bins == b]) == list(range(N // G))
+        assert abs(totals.sum(dtype=np.float64) - w.sum()) < 1e-4 * w.sum()
+
+
+def check_replication_bruteforce(eplb) -> None:
+    """The greedy replication reaches the smallest possible per-replica peak
+    max_e w_e / c_e over all count vectors with sum c = num_phys and c >= 1
+    (brute force on tiny cases)."""
+    rng = np.random.default_rng(61)
+
+    def compositions(total, parts):
+        if parts == 1:
+            yield (total,)
+            return
+        for first in range(1, total - parts + 2):
+            for rest in compositions(total - first, parts - 1):
+                yield (first,) + rest
+
+    for _ in range(40):
+        E = int(rng.integers(1, 5))
+        w = rng.integers(0, 30, size=E)
+        num_phys = E + int(rng.integers(0, 6))
+        _, count = eplb.replicate_experts(w, num_phys)
+        assert count.sum() == num_phys and count.min() >= 1
+        best = min(max(w[e] / c[e] for e in range(E)) for c in compositions(num_phys, E))
+        got = max(w[e] / count[e] for e in range(E))
+        assert abs(got - best) < 1e-12, (w, num_phys, count, got, best)
+
+
+def check_replication_hand_case(eplb) -> None:
+    """w = [6, 2, 1], three extra replicas: 6/1 -> expert 0 (c = 2); 3 > 2 -> expert 0
+    (c = 3); 6/3 = 2/1 ties -> the lower index, expert 0 (c = 4).  num_phys = E: identity."""
+    p2l, c = eplb.replicate_experts([6, 2, 1], 6)
+    assert list(c) == [4, 1, 1] and list(p2l) == [0, 1, 2, 0, 0, 0]
+    p2l, c = eplb.replicate_experts([5, 9, 1, 3], 4)
+    assert list(c) == [1, 1, 1, 1] and list(p2l) == [0, 1, 2, 3]
+
+
+def check_plan_invariants(eplb) -> None:
+    """Both policies: every GPU holds S slots; each expert's copies equal its count;
+    the GPU loads add up to the total load; the hierarchical policy keeps every
+    copy of an expert on the node its group was packed to."""
+    rng = np.random.default_rng(62)
+    E, num_phys, num_gpus, num_nodes, num_groups = 48, 64, 16, 4, 8
+    w = rng.integers(0, 500, size=E)
+    for groups in (0, num_groups):
+        out = eplb.plan(w, num_phys, num_gpus, num_nodes, groups)
+        assert out["hierarchical"] == (groups > 0)
+        p2l, cnt = out["phy2log"], out["log_count"]
+        assert np.array_equal(np.bincount(p2l, minlength=E), cnt) and cnt.sum() == num_phys
+        assert abs(out["gpu_load"].sum(dtype=np.float64) - w.sum()) < 1e-5 * w.sum()
+        S = num_phys // num_gpus
+        loads = [sum(w[e] / cnt[e] for e in p2l[g * S:(g + 1) * S]) for g in range(num_gpus)]
+        np.testing.assert_allclose(loads, out["gpu_load"], rtol=1e-5)
+        if groups:
+            gsize, slots_per_node = E // groups, num_phys // num_nodes
+            for n in range(num_nodes):
+                on_node = set(p2l[n * slots_per_node:(n + 1) * slots_per_node] // gsize)
+                assert len(on_node) == groups // num_nodes
+    out = eplb.plan(w, num_phys, num_gpus, 3, 8)            # 3 nodes do not divide 8 groups: global
+    assert not out["hierarchical"]

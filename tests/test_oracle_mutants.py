@@ -17,6 +17,7 @@ import synth
 
 R, D, S = oracle.router, oracle.dispatch, oracle.sinkhorn
 X = oracle.routing_ext
+B = oracle.eplb
 
 
 def _masked_forward(logits, dtype, k, alpha, renorm=None, n_ranks=0):
@@ -109,7 +110,63 @@ MUTANTS = {
     "softmax backward without the row-sum term": (
         [(X, "softmax_backward", lambda p, dp: p * dp)],
         [lambda: pins.check_full_grad_finite_difference(X, R), lambda: pins.check_full_grad_structure(X, R)]),
+    "packing takes the lightest item first": (
+        [(B, "balanced_packing", lambda w, n: _orig_bp([-x for x in w], n)[:2] + (_totals(w, *_orig_bp([-x for x in w], n)[:2], n),))],
+        [lambda: pins.check_packing_worked_example(B)]),
+    "packing ignores the bins' capacity": (
+        [(B, "balanced_packing", lambda w, n: _uncapped_packing(w, n))],
+        [lambda: pins.check_packing_cardinality_and_mass(B), lambda: pins.check_packing_worked_example(B)]),
+    "replication by weight instead of weight per copy": (
+        [(B, "replicate_experts", lambda w, n: _by_weight(w, n))],
+        [lambda: pins.check_replication_bruteforce(B), lambda: pins.check_replication_hand_case(B)]),
+    "replication ties to the higher index": (
+        [(B, "replicate_experts", lambda w, n: _ties_high(w, n))],
+        [lambda: pins.check_replication_hand_case(B)]),
 }
+
+_orig_bp = B.balanced_packing
+
+
+def _totals(w, bins, pos, n):
+    t = np.zeros(n)
+    for i, b in enumerate(bins):
+        t[b] += w[i]
+    return t
+
+
+def _uncapped_packing(w, n):
+    order = sorted(range(len(w)), key=lambda i: (-w[i], i))
+    t, fill, bins, pos = [0.0] * n, [0] * n, [0] * len(w), [0] * len(w)
+    for i in order:
+        b = min(range(n), key=lambda j: (t[j], j))
+        bins[i], pos[i] = b, fill[b]
+        fill[b] += 1
+        t[b] += w[i]
+    return np.asarray(bins), np.asarray(pos), np.asarray(t)
+
+
+def _by_weight(w, num_phys):
+    E = len(w)
+    count, p2l = [1] * E, list(range(E))
+    for _ in range(num_phys - E):
+        best = max(range(E), key=lambda e: (w[e], -e))
+        count[best] += 1
+        p2l.append(best)
+    return np.asarray(p2l), np.asarray(count)
+
+
+def _ties_high(w, num_phys):
+    E = len(w)
+    count, p2l = [1] * E, list(range(E))
+    for _ in range(num_phys - E):
+        best = 0
+        for e in range(1, E):
+            if w[e] * count[best] >= w[best] * count[e]:
+                best = e
+        count[best] += 1
+        p2l.append(best)
+    return np.asarray(p2l), np.asarray(count)
+
 
 _orig_sel = X.selection_scores
 _orig_bu = X.bias_update
