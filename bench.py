@@ -458,6 +458,30 @@ def time_next_steps(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     return out
 
 
+def time_eplb(torch, device, hbm_gbs: float, reps: int = 10) -> dict:
+    """The batched EPLB planner (moe_eplb_plan) on 1024 problems of 384 experts,
+    both policies, each a CUDA graph of `reps` calls; with the load balance it
+    reaches (CV of the GPU loads against the CV of the expert loads)."""
+    import moe_expert_routing_router_gb300 as mr
+    w = synth.EPLB_WORKLOADS["eplb-zipf-E384-B1024"]
+    loads_np = synth.eplb_loads(w)
+    loads = torch.from_numpy(loads_np.astype(np.int32)).to(device)
+    nbytes = w.B * (w.E * 4 + w.num_phys * 4 + w.E * 4 + w.num_gpus * 4)
+    out = {"workload": w.name, "B": w.B, "E": w.E, "num_phys": w.num_phys, "num_gpus": w.num_gpus,
+           "num_nodes": w.num_nodes, "bound": "latency (two sequential greedy loops per problem, one CTA each)",
+           "expert_load_cv_mean": round(float((loads_np.std(axis=1) / loads_np.mean(axis=1)).mean()), 4)}
+    for policy, groups in (("global", 0), ("hierarchical", w.num_groups)):
+        o = mr.moe_eplb_plan(loads, w.num_phys, w.num_gpus, w.num_nodes, groups)
+        us = _graph_us(torch, device, lambda i: mr.moe_eplb_plan(loads, w.num_phys, w.num_gpus, w.num_nodes, groups,
+                                                                  out=o), reps)
+        gl = o["gpu_load"].double()
+        cv = float((gl.std(dim=1, unbiased=False) / gl.mean(dim=1)).mean())
+        out[policy] = {"num_groups": groups, "us_per_call": round(us, 2), "problems_per_s": round(w.B / (us * 1e-6), 1),
+                       "gpu_load_cv_mean": round(cv, 4), "algorithmic_bytes": nbytes,
+                       "frac_of_hbm_peak": round(nbytes / (us * 1e-6) / 1e9 / hbm_gbs, 5)}
+    return out
+
+
 def time_sinkhorn(torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     """The batched TAOT Sinkhorn call, timed as a CUDA graph of `reps` calls on
     the 1024-microbatch workload.  Its bound is the HBM write of the plan."""
@@ -666,6 +690,7 @@ def run_ours(args) -> dict:
         line["separate_calls"] = {name: time_calls(synth.ROUTER_WORKLOADS[name], torch, device, pk["hbm_gbs"])
                                   for name in (w.name, EXTRA_WORKLOADS[-1])}
         line["sinkhorn"] = time_sinkhorn(torch, device, pk["hbm_gbs"])
+        line["eplb"] = time_eplb(torch, device, pk["hbm_gbs"])
         line["next_steps"] = {name: time_next_steps(synth.ROUTER_WORKLOADS[name], torch, device, pk["hbm_gbs"])
                               for name in (w.name, EXTRA_WORKLOADS[-1])}
     if dist_ctx.rank == 0:

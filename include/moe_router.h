@@ -6,7 +6,7 @@
  * gradient, a capacity-limited stable token->expert dispatch, and the batched
  * topology-aware Sinkhorn-Knopp flow plan of TAOT Phase 1.  Beside them: the
  * aux-loss-free bias routing, the masked P_i variant and the full router
- * backward through the gates.
+ * backward through the gates, and the EPLB replication / packing planner.
  *
  * Sources (cited by title and section):
  *   [P1] the three-layer load-balancing article (LVS, NIC Teaming, MoE
@@ -287,6 +287,40 @@ MOE_API moe_status moe_router_bwd_full(const void* logits, moe_dtype dt, int64_t
                                float alpha, const float* f, float grad_scale, int32_t masked_p,
                                const int32_t* idx, const float* dgate, int32_t renorm,
                                float* dlogits, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* EPLB: expert replication and balanced packing onto GPUs                  */
+/* ------------------------------------------------------------------------ */
+
+/* [P3] §4.1.2, for B independent problems (layers or microbatches) at once,
+ * one CTA each.  loads [B,E] int32: tokens routed to each expert (>= 0; the
+ * counts moe_router_fwd writes).
+ *   replicate_experts: starting from one copy per expert, repeatedly add a
+ *     copy of the expert whose load per copy w/c is largest (compared
+ *     exactly, w_a*c_b against w_b*c_a; ties to the lower index) until there
+ *     are num_phys copies;
+ *   balanced_packing: items heaviest first, each into the currently lightest
+ *     bin that is not yet full, every bin taking the same number of items (in
+ *     fp32: a copy weighs fp32(w)/fp32(c), a bin's total is the fp32 sum of
+ *     its items in placement order; ties to the lower item / bin index).
+ * Policy: hierarchical when num_groups > 0 and num_nodes divides num_groups
+ * (experts form num_groups contiguous groups; groups are packed onto nodes by
+ * their summed load, then each node's experts, in the order its groups were
+ * placed, are replicated onto num_phys/num_nodes slots and packed onto its
+ * num_gpus/num_nodes GPUs, node n owning GPUs [n*G/N, (n+1)*G/N)); global
+ * otherwise (replication over all E experts, packing onto all GPUs).
+ * Outputs:
+ *   phy2log   [B,num_phys] int32: the logical expert in each physical slot;
+ *             GPU g holds slots [g*S, (g+1)*S), S = num_phys/num_gpus, in the
+ *             order the packing placed them
+ *   log_count [B,E] int32: copies of each expert (sums to num_phys)
+ *   gpu_load  [B,num_gpus] fp32: each GPU's load, the sum of w/c over its copies
+ * Limits: E in [1,1024]; num_phys in [E, 4096], a multiple of num_gpus;
+ * num_gpus in [1,256], a multiple of num_nodes >= 1; num_groups 0 or a
+ * divisor of E.  No workspace. */
+MOE_API moe_status moe_eplb_plan(const int32_t* loads, int32_t B, int32_t E, int32_t num_phys,
+                         int32_t num_gpus, int32_t num_nodes, int32_t num_groups,
+                         int32_t* phy2log, int32_t* log_count, float* gpu_load, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* TAOT Phase 1: batched topology-aware Sinkhorn flow plan                  */

@@ -18,7 +18,7 @@ from ._native import MOE_DTYPE_BF16, MOE_DTYPE_FP32, MOE_NUM_SCALARS, SCALAR_NAM
 
 __all__ = [
     "Workspace", "moe_router_fwd", "moe_router_bwd", "moe_dispatch", "moe_dispatch_capacity",
-    "moe_router_step", "moe_router_step_static", "moe_router_fwd_ex", "moe_router_bwd_full", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
+    "moe_router_step", "moe_router_step_static", "moe_router_fwd_ex", "moe_router_bwd_full", "moe_eplb_plan", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
 ]
 
 _DTYPES = {torch.float32: MOE_DTYPE_FP32, torch.bfloat16: MOE_DTYPE_BF16}
@@ -314,6 +314,28 @@ def taot_sinkhorn_batched(loads: torch.Tensor, ranks_per_node: int, lam: float, 
                                      _ptr(o["u"]), _ptr(o["v"]), _ptr(o["plan"]), _ptr(o["status"]),
                                      _stream_handle(stream))
     check(st, "taot_sinkhorn_batched")
+    return o
+
+
+def moe_eplb_plan(loads: torch.Tensor, num_phys: int, num_gpus: int, num_nodes: int = 1, num_groups: int = 0,
+                  out: dict | None = None, stream: torch.cuda.Stream | None = None) -> dict:
+    """EPLB replication and balanced packing of B problems (C: moe_eplb_plan).
+
+    loads [B, E] int32 expert token counts; returns phy2log [B, num_phys],
+    log_count [B, E] and gpu_load [B, num_gpus]."""
+    _need_cuda("loads", loads, torch.int32)
+    if loads.dim() != 2:
+        raise ValueError("loads must be [B, E]")
+    B, E = loads.shape
+    dev = loads.device
+    o = {
+        "phy2log": _out(out, "phy2log", (B, num_phys), torch.int32, dev),
+        "log_count": _out(out, "log_count", (B, E), torch.int32, dev),
+        "gpu_load": _out(out, "gpu_load", (B, num_gpus), torch.float32, dev),
+    }
+    st = lib().moe_eplb_plan(_ptr(loads), B, E, int(num_phys), int(num_gpus), int(num_nodes), int(num_groups),
+                             _ptr(o["phy2log"]), _ptr(o["log_count"]), _ptr(o["gpu_load"]), _stream_handle(stream))
+    check(st, "moe_eplb_plan")
     return o
 
 

@@ -19,6 +19,7 @@
 #include "router_kernels.cuh"
 #include "router_table.h"
 #include "sinkhorn.h"
+#include "eplb.h"
 
 namespace {
 
@@ -562,6 +563,39 @@ moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t R, int32
   p.status = status;
   cudaError_t err = moe::launch_taot_sinkhorn(p, stream);
   if (err != cudaSuccess) return cuda_fail(err, "taot_sinkhorn launch");
+  return MOE_OK;
+}
+
+moe_status moe_eplb_plan(const int32_t* loads, int32_t B, int32_t E, int32_t num_phys,
+                         int32_t num_gpus, int32_t num_nodes, int32_t num_groups,
+                         int32_t* phy2log, int32_t* log_count, float* gpu_load, moe_stream_t stream) {
+  if (!loads || !phy2log || !log_count || !gpu_load) return fail(MOE_ERR_INVALID, "an EPLB argument is NULL");
+  if (B < 1) return fail(MOE_ERR_INVALID, "B = %d must be >= 1", B);
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_INVALID, "E = %d outside [1, %d]", E, MOE_MAX_EXPERTS);
+  if (num_gpus < 1 || num_gpus > moe::kEplbMaxGpus)
+    return fail(MOE_ERR_INVALID, "num_gpus = %d outside [1, %d]", num_gpus, moe::kEplbMaxGpus);
+  if (num_phys < E || num_phys > moe::kEplbMaxPhys || num_phys % num_gpus != 0)
+    return fail(MOE_ERR_INVALID, "num_phys = %d must be in [E, %d] and a multiple of num_gpus", num_phys, moe::kEplbMaxPhys);
+  if (num_nodes < 1 || num_gpus % num_nodes != 0)
+    return fail(MOE_ERR_INVALID, "num_nodes = %d must divide num_gpus = %d", num_nodes, num_gpus);
+  if (num_groups < 0 || (num_groups > 0 && E % num_groups != 0))
+    return fail(MOE_ERR_INVALID, "num_groups = %d must be 0 or divide E = %d", num_groups, E);
+  if (!aligned(loads, 4) || !aligned(phy2log, 4) || !aligned(log_count, 4) || !aligned(gpu_load, 4))
+    return fail(MOE_ERR_INVALID, "an EPLB array is not 4-byte aligned");
+  moe::EplbParams p;
+  p.loads = loads;
+  p.B = B;
+  p.E = E;
+  p.num_phys = num_phys;
+  p.num_gpus = num_gpus;
+  p.num_nodes = num_nodes;
+  p.num_groups = num_groups;
+  p.hier = num_groups > 0 && num_groups % num_nodes == 0;
+  p.phy2log = phy2log;
+  p.log_count = log_count;
+  p.gpu_load = gpu_load;
+  cudaError_t e = moe::launch_eplb_plan(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "eplb_plan launch");
   return MOE_OK;
 }
 

@@ -84,6 +84,24 @@ __device__ __forceinline__ uint32_t group_min_u32(uint32_t x) {
   }
 }
 
+// Maximum / minimum of N values as a tree of three-input operations (short
+// dependency chains).
+template <int N, bool MAX>
+__device__ __forceinline__ uint32_t tree3_u32(const uint32_t (&x)[N]) {
+  uint32_t t[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) t[i] = x[i];
+#pragma unroll
+  for (int n = N; n > 1; n = (n + 2) / 3) {
+#pragma unroll
+    for (int i = 0; i < n / 3; ++i)
+      t[i] = MAX ? __vimax3_u32(t[3 * i], t[3 * i + 1], t[3 * i + 2]) : __vimin3_u32(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+    if (n % 3 == 2) t[n / 3] = MAX ? max(t[n - 2], t[n - 1]) : min(t[n - 2], t[n - 1]);
+    if (n % 3 == 1) t[n / 3] = t[n - 1];
+  }
+  return t[0];
+}
+
 // Larger value, larger image; -0 is folded into +0 first.
 __device__ __forceinline__ uint32_t ordered_image(float x) {
   const uint32_t b = __float_as_uint(__fadd_rn(x, 0.f));
@@ -116,17 +134,14 @@ struct ExtRow {
     const uint32_t lane_bits = col_lane_bits<LPR, VW>(l);
     my_col = 0;
     for (int j = 0; j < k; ++j) {
-      uint32_t lm = hv[0];
+      const uint32_t wv = group_max_key<LPR>(tree3_u32<EPL, true>(hv));
+      uint32_t cand[EPL];
 #pragma unroll
-      for (int i = 1; i + 1 < EPL; i += 2) lm = __vimax3_u32(lm, hv[i], hv[i + 1]);
-      if constexpr (EPL % 2 == 0) lm = max(lm, hv[EPL - 1]);
-      const uint32_t wv = group_max_key<LPR>(lm);
-      uint32_t lc = 0xffffffffu;
+      for (int v = 0; v < NV; ++v)
 #pragma unroll
-      for (int v = NV - 1; v >= 0; --v)
-#pragma unroll
-        for (int i = VW - 1; i >= 0; --i) lc = hv[v * VW + i] == wv ? (lane_bits | col_elem_bits<LPR, VW>(v, i)) : lc;
-      const uint32_t wc = group_min_u32<LPR>(lc);
+        for (int i = 0; i < VW; ++i)
+          cand[v * VW + i] = hv[v * VW + i] == wv ? (lane_bits | col_elem_bits<LPR, VW>(v, i)) : 0xffffffffu;
+      const uint32_t wc = group_min_u32<LPR>(tree3_u32<EPL, false>(cand));
       // the column fields are disjoint: wc - lane_bits is the element's field iff this lane holds wc
       const uint32_t d = wc - lane_bits;
 #pragma unroll

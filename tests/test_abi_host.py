@@ -151,3 +151,14 @@ def test_fwd_ex_and_bwd_full_reject_bad_arguments(native_lib):
     bad[8] = 1
     bad[9] = None
     assert bf(*bad) == 1
+
+
+def test_eplb_rejects_bad_arguments(native_lib):
+    f = native_lib.moe_eplb_plan
+    args = [FAKE, 4, 48, 64, 16, 4, 8, FAKE, FAKE, FAKE, None]
+    for pos, val in [(0, None), (1, 0), (2, 0), (2, 1025), (3, 40), (3, 65), (3, 8192), (4, 0), (4, 257),
+                     (5, 3), (5, 0), (6, 5), (6, -1), (7, None), (9, FAKE + 2)]:
+        bad = list(args)
+        bad[pos] = val
+        assert f(*bad) == 1, (pos, val)
+        assert native_lib.moe_last_error()
