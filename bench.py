@@ -719,10 +719,21 @@ def main() -> int:
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="loaded window before the timed region, for the clock samples")
+    ap.add_argument("--section", choices=("next_steps", "eplb"), default=None,
+                    help="print only this part of the extra lines (for --workload), as JSON; no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warmup raised to 3")
         args.warmup = 3
+    if args.section is not None:
+        import torch
+        device = torch.device("cuda", 0)
+        torch.cuda.set_device(device)
+        hbm = peaks()["hbm_gbs"]
+        part = (time_next_steps(synth.ROUTER_WORKLOADS[args.workload], torch, device, hbm)
+                if args.section == "next_steps" else time_eplb(torch, device, hbm))
+        print(json.dumps(part), flush=True)
+        return 0
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line:
         print(json.dumps(line), flush=True)

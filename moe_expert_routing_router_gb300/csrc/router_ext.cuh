@@ -125,10 +125,11 @@ struct ExtRow {
     inv_s = valid ? rcp_approx(s) : 0.f;
   }
 
-  // Top-k on z + b: lane j < k receives pick j's column; hv[i] == 0 marks the
+  // Top-k on z + b, exact by construction (k passes over the lane's
+  // elements): lane j < k receives pick j's column; hv[i] == 0 marks the
   // lane's picked elements.
-  static __device__ __forceinline__ void select(const Raw (&raw)[EPL], const float (&bl)[EPL], int k, int l,
-                                                uint32_t (&hv)[EPL], int& my_col) {
+  static __device__ __forceinline__ void select_exact(const Raw (&raw)[EPL], const float (&bl)[EPL], int k, int l,
+                                                      uint32_t (&hv)[EPL], int& my_col) {
 #pragma unroll
     for (int i = 0; i < EPL; ++i) hv[i] = ordered_image(__fadd_rn(__uint_as_float(DT::bits(raw[i])), bl[i]));
     const uint32_t lane_bits = col_lane_bits<LPR, VW>(l);
@@ -149,6 +150,114 @@ struct ExtRow {
 #pragma unroll
         for (int i = 0; i < VW; ++i) hv[v * VW + i] = d == col_elem_bits<LPR, VW>(v, i) ? 0u : hv[v * VW + i];
       if (l == j) my_col = int(wc);
+    }
+  }
+
+  // Top-k on z + b with a per-lane cache (the fast path).  A key holds the
+  // score image's upper 22 bits above the inverted 10-bit column, so keys are
+  // distinct and one group maximum per round names the pick.  Each lane keeps
+  // its two largest keys; the lane that wins takes its second key up, and a
+  // lane whose cache runs empty refills it from its keys below the last one
+  // taken.  One more round finds the best key left.  The key order is the
+  // score order except between scores that share their upper 22 bits, so the
+  // row is redone by select_exact when two consecutive keys of the k + 1 have
+  // equal upper bits whose scores differ (for bf16 logits and a zero bias the
+  // upper bits hold the whole score and nothing is redone).  Returns false
+  // when the row must be redone; else lane j < k receives pick j's column
+  // and bit i of `taken` marks the lane's picked elements.
+  static __device__ __forceinline__ bool select_fast(const Raw (&raw)[EPL], const float (&bl)[EPL], int k, int l,
+                                                     int& my_col, uint32_t& taken) {
+    const uint32_t lane_bits = col_lane_bits<LPR, VW>(l);
+    uint32_t key[EPL];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int i = 0; i < VW; ++i) {
+        const uint32_t img = ordered_image(__fadd_rn(__uint_as_float(DT::bits(raw[v * VW + i])), bl[v * VW + i]));
+        key[v * VW + i] = (img & 0xfffffc00u) | (1023u - (lane_bits | col_elem_bits<LPR, VW>(v, i)));
+      }
+    uint32_t h1, h2;
+    top2_keys(key, 0xffffffffu, h1, h2);
+    my_col = 0;
+    uint32_t prev = 0, cv = 0, kth = 0;
+    bool ok = true, have_cv = false;
+    for (int j = 0; j <= k; ++j) {
+      const uint32_t w = group_max_key<LPR>(h1);
+      if (j > 0 && (w >> 10) == (prev >> 10) && w != 0u) {       // equal upper bits: the fine order decides
+        ok = ok && (!have_cv || cv == (w >> 10));
+        have_cv = true;
+        cv = w >> 10;
+      }
+      prev = w;
+      if (j == k) break;
+      kth = w;
+      if (l == j) my_col = int(1023u - (w & 1023u));
+      const bool won = h1 == w;
+      const uint32_t last = w;
+      h1 = won ? h2 : h1;
+      const bool refill = won && h2 == 0u;
+      h2 = won ? 0u : h2;
+      if (__any_sync(0xffffffffu, refill) && refill) top2_keys(key, last, h1, h2);
+    }
+    // Scores sharing the collided upper bits must all be equal (then the
+    // column order is the score order): their smallest and largest image agree.
+    const bool collided = __any_sync(0xffffffffu, have_cv);
+    ok = __all_sync(0xffffffffu, ok);
+    if (collided && ok) {
+      uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const uint32_t img = ordered_image(__fadd_rn(__uint_as_float(DT::bits(raw[i])), bl[i]));
+        const bool in = have_cv && (img >> 10) == cv;
+        lo = in ? min(lo, img) : lo;
+        hi = in ? max(hi, img) : hi;
+      }
+      const uint32_t glo = group_min_u32<LPR>(lo), ghi = group_max_key<LPR>(hi);
+      ok = __all_sync(0xffffffffu, !have_cv || glo == ghi);
+    }
+    taken = 0u;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) taken |= key[i] >= kth ? (1u << i) : 0u;
+    return ok;
+  }
+
+  // The two largest of the lane's keys below `below` (0 where there are none),
+  // as a pairwise tree: merging sorted pairs (h1, l1) and (h2, l2) gives
+  // (max(h1, h2), max(min(h1, h2), l1, l2)).
+  static __device__ __forceinline__ void top2_keys(const uint32_t (&key)[EPL], uint32_t below, uint32_t& m1, uint32_t& m2) {
+    uint32_t k2[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) k2[i] = key[i] < below ? key[i] : 0u;
+    if constexpr (EPL == 1) {
+      m1 = k2[0];
+      m2 = 0u;
+    } else {
+      constexpr int N0 = (EPL + 1) / 2;
+      uint32_t hi[N0], lo[N0];
+#pragma unroll
+      for (int i = 0; i < EPL / 2; ++i) {
+        hi[i] = max(k2[2 * i], k2[2 * i + 1]);
+        lo[i] = min(k2[2 * i], k2[2 * i + 1]);
+      }
+      if constexpr (EPL & 1) {
+        hi[N0 - 1] = k2[EPL - 1];
+        lo[N0 - 1] = 0u;
+      }
+#pragma unroll
+      for (int n = N0; n > 1; n = (n + 1) / 2) {
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+          const uint32_t a = hi[2 * i], b = hi[2 * i + 1];
+          hi[i] = max(a, b);
+          lo[i] = __vimax3_u32(min(a, b), lo[2 * i], lo[2 * i + 1]);
+        }
+        if (n & 1) {
+          hi[n / 2] = hi[n - 1];
+          lo[n / 2] = lo[n - 1];
+        }
+      }
+      m1 = hi[0];
+      m2 = lo[0];
     }
   }
 };
@@ -289,9 +398,17 @@ __global__ void __launch_bounds__(kExtFwdThreads, 2) router_fwd_ex_kernel(const 
     }
     float e[EPL], mL, inv_s;
     Row::softmax(raw, valid, e, mL, inv_s);
-    uint32_t hv[EPL];
+    // The cached selection pays at 12 or more elements per lane (E = 384: 310 -> 276 us); with
+    // fewer, its refills cost more than the passes they save (E = 64: 22 -> 24 us, E = 256: 137 -> 148 us).
     int my_col;
-    Row::select(raw, bl, p.k, l, hv, my_col);
+    uint32_t taken;
+    if (EPL < 12 || !__all_sync(0xffffffffu, Row::select_fast(raw, bl, p.k, l, my_col, taken))) {
+      uint32_t hv[EPL];
+      Row::select_exact(raw, bl, p.k, l, hv, my_col);
+      taken = 0u;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) taken |= hv[i] == 0u ? (1u << i) : 0u;
+    }
     // The pick's e by the formula of row_exp from its logit (the same bits as
     // its owner's e[i]); the row was just read, so the load hits L1.
     const bool owner = valid && l < p.k;
@@ -308,7 +425,7 @@ __global__ void __launch_bounds__(kExtFwdThreads, 2) router_fwd_ex_kernel(const 
     }
     if (p.masked_p) {
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) pacc[i] = hv[i] == 0u ? fmaf(e[i], inv_s, pacc[i]) : pacc[i];
+      for (int i = 0; i < EPL; ++i) pacc[i] = ((taken >> i) & 1u) ? fmaf(e[i], inv_s, pacc[i]) : pacc[i];
     } else {
 #pragma unroll
       for (int i = 0; i < EPL; ++i) pacc[i] = fmaf(e[i], inv_s, pacc[i]);

@@ -138,11 +138,13 @@ def test_bias_update_in_place_over_steps(mr):
 
 
 @pytest.mark.parametrize("E,k,dtype", [(40, 3, "fp32"), (64, 2, "bf16"), (8, 8, "bf16"), (1, 1, "fp32"),
-                                       (96, 5, "bf16"), (200, 8, "fp32")])
+                                       (96, 5, "bf16"), (200, 8, "fp32"), (384, 6, "bf16"), (384, 8, "fp32"),
+                                       (512, 4, "bf16"), (1000, 8, "fp32"), (1023, 7, "bf16")])
 def test_ties_and_edge_shapes(mr, E, k, dtype):
     """Integer logits and integer biases: the fp32 sums tie everywhere, so the
-    lower-index rule decides most picks; E not a multiple of the vector width,
-    k = E and E = 1 are covered."""
+    lower-index rule decides most picks (and, at 12 or more elements per lane,
+    the cached selection hands most rows to the exact one); E not a multiple of
+    the vector width, k = E and E = 1 are covered."""
     rng = np.random.default_rng(E * 10 + k)
     T = 777
     z = rng.integers(-3, 4, size=(T, E)).astype(np.float32)
@@ -272,3 +274,22 @@ def test_interleaved_with_the_fused_step_on_one_workspace(mr):
         assert_equal("step idx", st["idx"].cpu().numpy(), plain["idx"])
         want = oracle_forward_ex(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks, bias, masked, GAMMA)
         check_forward(fx, want, w.n_ranks)
+
+
+@pytest.mark.parametrize("E,dtype", [(384, "fp32"), (512, "fp32"), (384, "bf16")])
+def test_scores_equal_in_their_upper_bits(mr, E, dtype):
+    """Scores that differ only below the upper 22 bits of their image (fp32
+    logits 1.5 + j * 2^-20, or bf16 logits with biases of that size): the
+    cached selection must see the collision and leave the row to the exact one."""
+    rng = np.random.default_rng(E)
+    T, k = 517, 6
+    if dtype == "fp32":
+        z = (np.float32(1.5) + rng.integers(0, 3, size=(T, E)).astype(np.float32) * np.float32(2.0 ** -20))
+        logits, bias = z.astype(np.float32), np.zeros(E, np.float32)
+    else:
+        logits = synth.f32_to_bf16_bits(np.full((T, E), 1.5, np.float32) + rng.integers(0, 2, size=(T, E)).astype(np.float32))
+        bias = (rng.integers(0, 3, size=E) * 2.0 ** -19).astype(np.float32)
+    x = to_device(logits, dtype)
+    got = mr.moe_router_fwd_ex(x, k, 0.01, bias=torch.from_numpy(bias).cuda(), bias_gamma=0.5, bias_out=True)
+    torch.cuda.synchronize()
+    check_forward(got, oracle_forward_ex(logits, dtype, k, 0.01, True, 0, bias, False, 0.5), 0)
