@@ -59,13 +59,13 @@ def algorithmic_bytes(w: synth.RouterWorkload) -> int:
 
 def kernel_source_hash() -> str:
     """Hash of the sources of the router step kernel and its launch (changes
-    whenever that kernel or its launch geometry does; the Sinkhorn files are
-    not part of it)."""
+    whenever that kernel or its launch geometry does; the Sinkhorn, EPLB and
+    bias-routing / full-backward kernel files are not part of it)."""
     import hashlib
     h = hashlib.sha256()
     csrc = ROOT / "moe_expert_routing_router_gb300" / "csrc"
     for f in sorted(csrc.iterdir()):
-        if f.suffix in (".cu", ".cuh", ".h") and not f.name.startswith("sinkhorn"):
+        if f.suffix in (".cu", ".cuh", ".h") and not f.name.startswith(("sinkhorn", "eplb", "router_ext")):
             h.update(f.name.encode())
             h.update(f.read_bytes())
     return h.hexdigest()[:16]
