@@ -23,9 +23,10 @@ Modules:
   sinkhorn  -- TAOT Phase 1: topology-aware entropic transport plan
   routing_ext -- aux-loss-free bias routing, masked P_i, the full backward through the gates
   eplb      -- EPLB expert replication and balanced packing onto GPUs ([P3] §4.1.2)
+  taot_match -- TAOT Phase 2: column-first matching of hot experts to cold ranks ([P4] §2)
 
 Parity status of each function is stated in its docstring ("pinned by ...");
 the pins live in ``tests/test_oracle_*.py``.
 """
 
-from . import router, dispatch, sinkhorn, routing_ext, eplb  # noqa: F401
+from . import router, dispatch, sinkhorn, routing_ext, eplb, taot_match  # noqa: F401

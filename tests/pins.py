@@ -588,3 +588,69 @@ def check_plan_invariants(eplb) -> None:
                 assert len(on_node) == groups // num_nodes
     out = eplb.plan(w, num_phys, num_gpus, 3, 8)            # 3 nodes do not divide 8 groups: global
     assert not out["hierarchical"]
+
+
+# ----------------------------------------------------------------------------- TAOT Phase 2 (column-first matching)
+
+def check_match_hand_single(match) -> None:
+    """Two ranks on one node, experts [5, 3 | 1, 1]: rank loads 8 / 2, mean 5.  The cold
+    rank can take min(w, floor(8 - 5), floor(5 - 2)) = 3 tokens of expert 0 or 1: the tie
+    goes to expert 0; then both ranks sit at the mean and nothing else moves."""
+    out = match.match([5, 3, 1, 1], np.zeros((2, 2), np.float32), R=2, ranks_per_node=2, K=2)
+    assert out["slot_expert"].tolist() == [[-1, -1], [0, -1]]
+    assert out["slot_tokens"].tolist() == [[0, 0], [3, 0]]
+    assert out["rank_load"].tolist() == [5, 5] and out["moved"] == 3
+
+
+def check_match_hand_arbitration(match) -> None:
+    """Four ranks, two per node, one expert each: loads [10, 2, 2, 2], mean 4.  Every cold
+    rank wants expert 0 (2 tokens each).  Round 1: rank 1 shares rank 0's node and wins.
+    Round 2: rank 1 is at the mean; ranks 2 and 3 tie on tokens and topology, and the
+    flow plan prefers rank 3.  Round 3: rank 2.  All four end at the mean."""
+    plan = np.zeros((4, 4), np.float32)
+    plan[0, 2], plan[0, 3] = 0.25, 0.5
+    out = match.match([10, 2, 2, 2], plan, R=4, ranks_per_node=2, K=3)
+    assert out["slot_expert"][:, 0].tolist() == [-1, 0, 0, 0]
+    assert out["slot_tokens"][:, 0].tolist() == [0, 2, 2, 2]
+    assert out["rank_load"].tolist() == [4, 4, 4, 4]
+    one = match.match([10, 2, 2, 2], plan, R=4, ranks_per_node=2, K=1)
+    assert one["slot_expert"][:, 0].tolist() == [-1, 0, -1, -1]
+    flip = plan.copy()
+    flip[0, 2], flip[0, 3] = 0.5, 0.25
+    two = match.match([10, 2, 2, 2], flip, R=4, ranks_per_node=2, K=2)
+    assert two["slot_expert"][:, :2].tolist() == [[-1, -1], [0, -1], [0, -1], [-1, -1]]
+
+
+def check_match_invariants(match) -> None:
+    """On skewed random loads: the total is kept, no hot rank drops below the mean and
+    no cold rank rises above it, a rank holds at most K replicas and an expert once,
+    every slot moves tokens, and an expert never gives away more than its load."""
+    rng = np.random.default_rng(70)
+    for trial in range(30):
+        R, rpn, per, K = (8, 4, 3, 2) if trial % 2 else (16, 8, 2, 3)
+        E = R * per
+        w = rng.multinomial(40 * E, (np.arange(E) + 1.0) ** -1.2 / ((np.arange(E) + 1.0) ** -1.2).sum())
+        w = w[rng.permutation(E)]
+        plan = rng.random((R, R)).astype(np.float32)
+        out = match.match(w, plan, R, rpn, K)
+        before = w.reshape(R, per).sum(axis=1)
+        after = out["rank_load"]
+        total = before.sum()
+        assert after.sum() == total
+        hot, cold = before * R > total, before * R < total
+        assert np.all(after[hot] * R >= total) and np.all(after[cold] * R <= total)
+        assert np.all(after[hot] <= before[hot]) and np.all(after[cold] >= before[cold])
+        se, st = out["slot_expert"], out["slot_tokens"]
+        assert np.all((se >= 0) == (st > 0))
+        for c in range(R):
+            got = [e for e in se[c] if e >= 0]
+            assert len(got) == len(set(got)) <= K
+        given = np.zeros(E, np.int64)
+        for c in range(R):
+            for e, x in zip(se[c], st[c]):
+                if e >= 0:
+                    given[e] += x
+        assert np.all(given <= w)
+        assert out["moved"] == int(st.sum())
+    none = match.match(w, plan, R, rpn, 0)
+    assert none["moved"] == 0 and np.array_equal(none["rank_load"], before)

@@ -18,6 +18,7 @@ import synth
 R, D, S = oracle.router, oracle.dispatch, oracle.sinkhorn
 X = oracle.routing_ext
 B = oracle.eplb
+M = oracle.taot_match
 
 
 def _masked_forward(logits, dtype, k, alpha, renorm=None, n_ranks=0):
@@ -122,8 +123,15 @@ MUTANTS = {
     "replication ties to the higher index": (
         [(B, "replicate_experts", lambda w, n: _ties_high(w, n))],
         [lambda: pins.check_replication_hand_case(B)]),
+    "matching ignores the topology": (
+        [(M, "match", lambda w, plan, R, rpn, K: _orig_match(w, plan, R, R, K))],
+        [lambda: pins.check_match_hand_arbitration(M)]),
+    "matching prefers the smaller flow": (
+        [(M, "match", lambda w, plan, R, rpn, K: _orig_match(w, -np.asarray(plan), R, rpn, K))],
+        [lambda: pins.check_match_hand_arbitration(M)]),
 }
 
+_orig_match = M.match
 _orig_bp = B.balanced_packing
 
 
