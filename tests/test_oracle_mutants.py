@@ -124,10 +124,10 @@ MUTANTS = {
         [(B, "replicate_experts", lambda w, n: _ties_high(w, n))],
         [lambda: pins.check_replication_hand_case(B)]),
     "matching ignores the topology": (
-        [(M, "match", lambda w, plan, R, rpn, K: _orig_match(w, plan, R, R, K))],
+        [(M, "match", lambda w, plan, R, ranks_per_node, K: _orig_match(w, plan, R, R, K))],
         [lambda: pins.check_match_hand_arbitration(M)]),
     "matching prefers the smaller flow": (
-        [(M, "match", lambda w, plan, R, rpn, K: _orig_match(w, -np.asarray(plan), R, rpn, K))],
+        [(M, "match", lambda w, plan, R, ranks_per_node, K: _orig_match(w, -np.asarray(plan), R, ranks_per_node, K))],
         [lambda: pins.check_match_hand_arbitration(M)]),
 }
 
