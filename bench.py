@@ -482,6 +482,37 @@ def time_eplb(torch, device, hbm_gbs: float, reps: int = 10) -> dict:
     return out
 
 
+def time_taot_match(torch, device, hbm_gbs: float, reps: int = 10, K: int = 4) -> dict:
+    """TAOT Phase 2 (taot_match_batched) on 1024 microbatches of 384 experts over
+    64 ranks in 8 nodes, K = 4 replica slots per cold rank, fed by the Phase 1
+    plan of taot_sinkhorn_batched; a CUDA graph of `reps` calls of Phase 1 +
+    Phase 2 and of Phase 2 alone, with the residual imbalance (max - mean) / mean
+    of the rank loads before and after."""
+    import moe_expert_routing_router_gb300 as mr
+    w = synth.EPLB_WORKLOADS["eplb-zipf-E384-B1024"]
+    R, rpn = 64, 8
+    loads = torch.from_numpy(synth.eplb_loads(w).astype(np.int32)).to(device)
+    rank = loads.view(w.B, R, -1).sum(dim=2).float().contiguous()
+    sk = mr.taot_sinkhorn_batched(rank, rpn, 10.0, 0.0, 50)
+    o = mr.taot_match_batched(loads, sk["plan"], rpn, K)
+
+    def both(i):
+        mr.taot_sinkhorn_batched(rank, rpn, 10.0, 0.0, 50, out=sk)
+        mr.taot_match_batched(loads, sk["plan"], rpn, K, out=o)
+
+    us_both = _graph_us(torch, device, both, reps)
+    us_match = _graph_us(torch, device, lambda i: mr.taot_match_batched(loads, sk["plan"], rpn, K, out=o), reps)
+    before, after = rank.double(), o["rank_load"].double()
+    imb = lambda x: float(((x.max(dim=1).values - x.mean(dim=1)) / x.mean(dim=1)).mean())
+    nbytes = w.B * (w.E * 4 + R * R * 4 + 2 * R * K * 4 + R * 4)
+    return {"workload": w.name, "B": w.B, "E": w.E, "R": R, "ranks_per_node": rpn, "K": K,
+            "bound": "latency (K dependent rounds of score, arbitration and commit per microbatch)",
+            "us_per_call_phase2": round(us_match, 2), "us_per_call_phase1_and_2": round(us_both, 2),
+            "microbatches_per_s": round(w.B / (us_match * 1e-6), 1), "algorithmic_bytes_phase2": nbytes,
+            "frac_of_hbm_peak": round(nbytes / (us_match * 1e-6) / 1e9 / hbm_gbs, 5),
+            "residual_imbalance_before": round(imb(before), 4), "residual_imbalance_after": round(imb(after), 4)}
+
+
 def time_sinkhorn(torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     """The batched TAOT Sinkhorn call, timed as a CUDA graph of `reps` calls on
     the 1024-microbatch workload.  Its bound is the HBM write of the plan."""
@@ -691,6 +722,7 @@ def run_ours(args) -> dict:
                                   for name in (w.name, EXTRA_WORKLOADS[-1])}
         line["sinkhorn"] = time_sinkhorn(torch, device, pk["hbm_gbs"])
         line["eplb"] = time_eplb(torch, device, pk["hbm_gbs"])
+        line["taot_match"] = time_taot_match(torch, device, pk["hbm_gbs"])
         line["next_steps"] = {name: time_next_steps(synth.ROUTER_WORKLOADS[name], torch, device, pk["hbm_gbs"])
                               for name in (w.name, EXTRA_WORKLOADS[-1])}
     if dist_ctx.rank == 0:
@@ -719,7 +751,7 @@ def main() -> int:
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="loaded window before the timed region, for the clock samples")
-    ap.add_argument("--section", choices=("next_steps", "eplb"), default=None,
+    ap.add_argument("--section", choices=("next_steps", "eplb", "taot_match"), default=None,
                     help="print only this part of the extra lines (for --workload), as JSON; no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -731,7 +763,8 @@ def main() -> int:
         torch.cuda.set_device(device)
         hbm = peaks()["hbm_gbs"]
         part = (time_next_steps(synth.ROUTER_WORKLOADS[args.workload], torch, device, hbm)
-                if args.section == "next_steps" else time_eplb(torch, device, hbm))
+                if args.section == "next_steps" else
+                time_eplb(torch, device, hbm) if args.section == "eplb" else time_taot_match(torch, device, hbm))
         print(json.dumps(part), flush=True)
         return 0
     line = run_reference(args) if args.impl == "reference" else run_ours(args)

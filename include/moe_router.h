@@ -345,6 +345,30 @@ MOE_API moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t 
                                  float* u, float* v, float* plan, int32_t* status,
                                  moe_stream_t stream);
 
+/* TAOT Phase 2 ([P4] §2, §3): column-first matching of hot experts to cold
+ * ranks, for B microbatches at once (one CTA each).  Experts live on their home
+ * ranks contiguously (E/R per rank); a rank is hot above the mean load, cold
+ * below it.  K rounds: every cold rank with a free slot picks the hot expert
+ * that scores best,
+ *   (tokens moved x, 1 if same node else 0, plan[h,c], then the lower expert),
+ *   x = min(tokens of e still at home, floor(load[h] - mean), floor(mean - load[c])),
+ * skipping experts it already holds; several ranks picking one expert are
+ * arbitrated by the same score (ties to the lower rank); the winners' moves are
+ * applied in ascending rank order, each x taken again against the current
+ * loads.  The page gives the three levels of the score and the arbitration,
+ * not these formulas: they are this library's reading.
+ * expert_loads [B,E] int32 (>= 0, total per microbatch below 2^31);
+ * plan [B,R,R] fp32, the Phase 1 flow (taot_sinkhorn_batched's plan);
+ * R in [1,64] dividing E; ranks_per_node dividing R; K in [0,16]; E <= 1024.
+ * Outputs: slot_expert [B,R,K] int32 (the expert in cold rank r's j-th
+ * replica slot, -1 when empty), slot_tokens [B,R,K] int32 (tokens it takes),
+ * rank_load [B,R] int32 (loads after the moves).  With K = 0 the slot arrays
+ * may be NULL (nothing moves).  No workspace. */
+MOE_API moe_status taot_match_batched(const int32_t* expert_loads, const float* plan, int32_t B, int32_t E,
+                              int32_t R, int32_t ranks_per_node, int32_t K,
+                              int32_t* slot_expert, int32_t* slot_tokens, int32_t* rank_load,
+                              moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Misc                                                                     */
 /* ------------------------------------------------------------------------ */

@@ -18,7 +18,7 @@ from ._native import MOE_DTYPE_BF16, MOE_DTYPE_FP32, MOE_NUM_SCALARS, SCALAR_NAM
 
 __all__ = [
     "Workspace", "moe_router_fwd", "moe_router_bwd", "moe_dispatch", "moe_dispatch_capacity",
-    "moe_router_step", "moe_router_step_static", "moe_router_fwd_ex", "moe_router_bwd_full", "moe_eplb_plan", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
+    "moe_router_step", "moe_router_step_static", "moe_router_fwd_ex", "moe_router_bwd_full", "moe_eplb_plan", "taot_match_batched", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
 ]
 
 _DTYPES = {torch.float32: MOE_DTYPE_FP32, torch.bfloat16: MOE_DTYPE_BF16}
@@ -336,6 +336,31 @@ def moe_eplb_plan(loads: torch.Tensor, num_phys: int, num_gpus: int, num_nodes: 
     st = lib().moe_eplb_plan(_ptr(loads), B, E, int(num_phys), int(num_gpus), int(num_nodes), int(num_groups),
                              _ptr(o["phy2log"]), _ptr(o["log_count"]), _ptr(o["gpu_load"]), _stream_handle(stream))
     check(st, "moe_eplb_plan")
+    return o
+
+
+def taot_match_batched(expert_loads: torch.Tensor, plan: torch.Tensor, ranks_per_node: int, K: int,
+                       out: dict | None = None, stream: torch.cuda.Stream | None = None) -> dict:
+    """TAOT Phase 2 column-first matching of hot experts to cold ranks (C: taot_match_batched).
+
+    expert_loads [B, E] int32, plan [B, R, R] fp32 (the Phase 1 flow); returns
+    slot_expert and slot_tokens [B, R, K] and rank_load [B, R]."""
+    _need_cuda("expert_loads", expert_loads, torch.int32)
+    _need_cuda("plan", plan, torch.float32)
+    if expert_loads.dim() != 2 or plan.dim() != 3 or plan.shape[0] != expert_loads.shape[0] or plan.shape[1] != plan.shape[2]:
+        raise ValueError("expert_loads must be [B, E] and plan [B, R, R]")
+    B, E = expert_loads.shape
+    R = plan.shape[1]
+    dev = expert_loads.device
+    o = {
+        "slot_expert": _out(out, "slot_expert", (B, R, K), torch.int32, dev),
+        "slot_tokens": _out(out, "slot_tokens", (B, R, K), torch.int32, dev),
+        "rank_load": _out(out, "rank_load", (B, R), torch.int32, dev),
+    }
+    st = lib().taot_match_batched(_ptr(expert_loads), _ptr(plan), B, E, R, int(ranks_per_node), int(K),
+                                  _ptr(o["slot_expert"]), _ptr(o["slot_tokens"]), _ptr(o["rank_load"]),
+                                  _stream_handle(stream))
+    check(st, "taot_match_batched")
     return o
 
 

@@ -20,6 +20,7 @@
 #include "router_table.h"
 #include "sinkhorn.h"
 #include "eplb.h"
+#include "taot_match.h"
 
 namespace {
 
@@ -596,6 +597,35 @@ moe_status moe_eplb_plan(const int32_t* loads, int32_t B, int32_t E, int32_t num
   p.gpu_load = gpu_load;
   cudaError_t e = moe::launch_eplb_plan(p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "eplb_plan launch");
+  return MOE_OK;
+}
+
+moe_status taot_match_batched(const int32_t* expert_loads, const float* plan, int32_t B, int32_t E,
+                              int32_t R, int32_t ranks_per_node, int32_t K,
+                              int32_t* slot_expert, int32_t* slot_tokens, int32_t* rank_load,
+                              moe_stream_t stream) {
+  if (!expert_loads || !plan || !rank_load || (K > 0 && (!slot_expert || !slot_tokens)))
+    return fail(MOE_ERR_INVALID, "a matching argument is NULL");
+  if (B < 1) return fail(MOE_ERR_INVALID, "B = %d must be >= 1", B);
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_INVALID, "E = %d outside [1, %d]", E, MOE_MAX_EXPERTS);
+  if (R < 1 || R > MOE_MAX_RANKS || E % R != 0) return fail(MOE_ERR_INVALID, "R = %d must be in [1, %d] and divide E", R, MOE_MAX_RANKS);
+  if (ranks_per_node < 1 || R % ranks_per_node != 0) return fail(MOE_ERR_INVALID, "ranks_per_node = %d must divide R", ranks_per_node);
+  if (K < 0 || K > moe::kMatchMaxRounds) return fail(MOE_ERR_INVALID, "K = %d outside [0, %d]", K, moe::kMatchMaxRounds);
+  if (!aligned(expert_loads, 4) || !aligned(plan, 4) || !aligned(slot_expert, 4) || !aligned(slot_tokens, 4) || !aligned(rank_load, 4))
+    return fail(MOE_ERR_INVALID, "a matching array is not 4-byte aligned");
+  moe::MatchParams p;
+  p.expert_loads = expert_loads;
+  p.plan = plan;
+  p.B = B;
+  p.E = E;
+  p.R = R;
+  p.ranks_per_node = ranks_per_node;
+  p.K = K;
+  p.slot_expert = slot_expert;
+  p.slot_tokens = slot_tokens;
+  p.rank_load = rank_load;
+  cudaError_t e = moe::launch_taot_match(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "taot_match launch");
   return MOE_OK;
 }
 

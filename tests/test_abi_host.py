@@ -162,3 +162,13 @@ def test_eplb_rejects_bad_arguments(native_lib):
         bad[pos] = val
         assert f(*bad) == 1, (pos, val)
         assert native_lib.moe_last_error()
+
+
+def test_taot_match_rejects_bad_arguments(native_lib):
+    f = native_lib.taot_match_batched
+    args = [FAKE, FAKE, 4, 384, 64, 8, 4, FAKE, FAKE, FAKE, None]
+    for pos, val in [(0, None), (1, None), (2, 0), (3, 0), (3, 1025), (4, 0), (4, 65), (4, 5), (5, 3), (6, -1),
+                     (6, 17), (9, None), (7, FAKE + 2), (7, None), (8, None)]:
+        bad = list(args)
+        bad[pos] = val
+        assert f(*bad) == 1, (pos, val)
