@@ -468,7 +468,7 @@ def time_eplb(torch, device, hbm_gbs: float, reps: int = 10) -> dict:
     loads = torch.from_numpy(loads_np.astype(np.int32)).to(device)
     nbytes = w.B * (w.E * 4 + w.num_phys * 4 + w.E * 4 + w.num_gpus * 4)
     out = {"workload": w.name, "B": w.B, "E": w.E, "num_phys": w.num_phys, "num_gpus": w.num_gpus,
-           "num_nodes": w.num_nodes, "bound": "latency (two sequential greedy loops per problem, one CTA each)",
+           "num_nodes": w.num_nodes, "bound": "latency (two sequential greedy loops per problem, one warp each)",
            "expert_load_cv_mean": round(float((loads_np.std(axis=1) / loads_np.mean(axis=1)).mean()), 4)}
     for policy, groups in (("global", 0), ("hierarchical", w.num_groups)):
         o = mr.moe_eplb_plan(loads, w.num_phys, w.num_gpus, w.num_nodes, groups)
