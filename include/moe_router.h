@@ -236,8 +236,9 @@ MOE_API moe_status moe_router_step_static(const void* logits, moe_dtype dt, int6
 /* ------------------------------------------------------------------------ */
 
 /* Router forward with two options of the method that moe_router_fwd does not
- * take, computed by a plain (non-cooperative) streaming kernel whose last CTA
- * adds up the per-CTA partials:
+ * take, computed by a plain (non-cooperative) streaming kernel whose CTAs add
+ * their per-expert partials into the workspace with integer atomics (so the
+ * results do not depend on scheduling) and whose last CTA writes the outputs:
  *
  *   Bias routing ([P1] §4.3, aux-loss-free balancing): each expert carries a
  *   scalar bias b_e on its router logit that steers which experts are picked.
