@@ -289,6 +289,23 @@ MOE_API moe_status moe_router_bwd_full(const void* logits, moe_dtype dt, int64_t
                                const int32_t* idx, const float* dgate, int32_t renorm,
                                float* dlogits, moe_stream_t stream);
 
+/* Data-parallel batch statistics.  Combines the forward statistics of G shards
+ * of one batch -- data-parallel ranks that each routed their own tokens with
+ * moe_router_fwd / moe_router_fwd_ex, or slices routed one after another --
+ * into the whole batch's, as if one call had routed all of it:
+ *   counts = sum_s counts_s (exact),  P = sum_s P_s * T_s / T  (double, then fp32;
+ *   the same for masked P),  f = counts / (T*k),  the scalars and rank loads as
+ *   moe_router_fwd computes them, T = sum_s T_s.
+ * counts [G,E] int32 and P [G,E] fp32 are the shards' outputs stacked (on a
+ * multi-GPU job, the result of an all-gather); T_shard is a HOST array of G
+ * token counts.  G in [1,64].  The batch gradient then comes from each shard's
+ * moe_router_bwd with the combined f and grad_scale * T_s / T (its coefficient
+ * alpha*E/T_s becomes alpha*E/T).  No workspace; one CTA. */
+MOE_API moe_status moe_router_combine(const int32_t* counts, const float* P, const int64_t* T_shard, int32_t G,
+                              int32_t E, int32_t k, float alpha, int32_t n_ranks, int32_t masked_p,
+                              int32_t* counts_out, float* f, float* P_out, float* scalars, int32_t* rank_load,
+                              moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* EPLB: expert replication and balanced packing onto GPUs                  */
 /* ------------------------------------------------------------------------ */

@@ -13,6 +13,7 @@ from .api import (  # noqa: F401
     moe_eplb_plan,
     moe_get_device_status,
     moe_router_bwd,
+    moe_router_combine,
     moe_router_fwd,
     moe_router_fwd_ex,
     moe_router_bwd_full,
@@ -24,5 +25,5 @@ from .api import (  # noqa: F401
 
 __all__ = [
     "SCALAR_NAMES", "Workspace", "moe_dispatch", "moe_dispatch_capacity", "moe_eplb_plan", "moe_get_device_status",
-    "moe_router_bwd", "moe_router_bwd_full", "moe_router_fwd", "moe_router_fwd_ex", "moe_router_step", "moe_router_step_static", "taot_match_batched", "taot_sinkhorn_batched",
+    "moe_router_bwd", "moe_router_bwd_full", "moe_router_combine", "moe_router_fwd", "moe_router_fwd_ex", "moe_router_step", "moe_router_step_static", "taot_match_batched", "taot_sinkhorn_batched",
 ]

@@ -38,6 +38,8 @@ SIGNATURES = {
     "moe_router_bwd_full": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _p, _f32, _i32, _p, _p, _i32, _p, _p]),
     "moe_eplb_plan": (_i32, [_p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p]),
     "taot_match_batched": (_i32, [_p, _p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p]),
+    "moe_router_combine": (_i32, [_p, _p, C.POINTER(_i64), _i32, _i32, _i32, _f32, _i32, _i32,
+                                  _p, _p, _p, _p, _p, _p]),
     "taot_sinkhorn_batched": (_i32, [_p, _i32, _i32, _i32, _f32, _f32, _i32, _p, _p, _p, _p, _p]),
     "moe_set_wait_timeout_ns": (None, [C.c_uint64]),
     "moe_set_unreachable_barriers": (None, [_i32]),

@@ -18,7 +18,7 @@ from ._native import MOE_DTYPE_BF16, MOE_DTYPE_FP32, MOE_NUM_SCALARS, SCALAR_NAM
 
 __all__ = [
     "Workspace", "moe_router_fwd", "moe_router_bwd", "moe_dispatch", "moe_dispatch_capacity",
-    "moe_router_step", "moe_router_step_static", "moe_router_fwd_ex", "moe_router_bwd_full", "moe_eplb_plan", "taot_match_batched", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
+    "moe_router_step", "moe_router_step_static", "moe_router_fwd_ex", "moe_router_bwd_full", "moe_eplb_plan", "taot_match_batched", "moe_router_combine", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
 ]
 
 _DTYPES = {torch.float32: MOE_DTYPE_FP32, torch.bfloat16: MOE_DTYPE_BF16}
@@ -361,6 +361,37 @@ def taot_match_batched(expert_loads: torch.Tensor, plan: torch.Tensor, ranks_per
                                   _ptr(o["slot_expert"]), _ptr(o["slot_tokens"]), _ptr(o["rank_load"]),
                                   _stream_handle(stream))
     check(st, "taot_match_batched")
+    return o
+
+
+def moe_router_combine(counts: torch.Tensor, P: torch.Tensor, T_shard, k: int, alpha: float, n_ranks: int = 0,
+                       masked_p: bool = False, out: dict | None = None,
+                       stream: torch.cuda.Stream | None = None) -> dict:
+    """The whole batch's counts, f, P, scalars and rank loads from G shards'
+    forward statistics (C: moe_router_combine).  counts [G, E] int32, P [G, E]
+    fp32 on the GPU; T_shard: the G shards' token counts (host integers)."""
+    _need_cuda("counts", counts, torch.int32)
+    _need_cuda("P", P, torch.float32)
+    if counts.dim() != 2 or tuple(P.shape) != tuple(counts.shape):
+        raise ValueError("counts and P must both be [G, E]")
+    G, E = counts.shape
+    T_list = [int(t) for t in T_shard]
+    if len(T_list) != G:
+        raise ValueError("T_shard must have G entries")
+    dev = counts.device
+    o = {
+        "counts": _out(out, "counts", (E,), torch.int32, dev),
+        "f": _out(out, "f", (E,), torch.float32, dev),
+        "P": _out(out, "P", (E,), torch.float32, dev),
+        "scalars": _out(out, "scalars", (MOE_NUM_SCALARS,), torch.float32, dev),
+        "rank_load": _out(out, "rank_load", (max(n_ranks, 0),), torch.int32, dev),
+    }
+    tarr = (C.c_int64 * G)(*T_list)
+    st = lib().moe_router_combine(_ptr(counts), _ptr(P), tarr, G, E, int(k), float(alpha), int(n_ranks),
+                                  int(bool(masked_p)), _ptr(o["counts"]), _ptr(o["f"]), _ptr(o["P"]),
+                                  _ptr(o["scalars"]), _ptr(o["rank_load"]) if n_ranks > 0 else None,
+                                  _stream_handle(stream))
+    check(st, "moe_router_combine")
     return o
 
 

@@ -629,6 +629,50 @@ moe_status taot_match_batched(const int32_t* expert_loads, const float* plan, in
   return MOE_OK;
 }
 
+moe_status moe_router_combine(const int32_t* counts, const float* P, const int64_t* T_shard, int32_t G,
+                              int32_t E, int32_t k, float alpha, int32_t n_ranks, int32_t masked_p,
+                              int32_t* counts_out, float* f, float* P_out, float* scalars, int32_t* rank_load,
+                              moe_stream_t stream) {
+  if (!counts || !P || !T_shard) return fail(MOE_ERR_INVALID, "a shard input is NULL");
+  if (G < 1 || G > moe::kMaxShards) return fail(MOE_ERR_INVALID, "G = %d outside [1, %d]", G, moe::kMaxShards);
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_INVALID, "E = %d outside [1, %d]", E, MOE_MAX_EXPERTS);
+  if (k < 1 || k > MOE_MAX_TOPK || k > E) return fail(MOE_ERR_INVALID, "k = %d outside [1, min(E, %d)]", k, MOE_MAX_TOPK);
+  if (!(alpha >= 0.f) || !std::isfinite(alpha)) return fail(MOE_ERR_INVALID, "alpha must be finite and >= 0");
+  if (n_ranks < 0 || n_ranks > MOE_MAX_RANKS || (n_ranks > 0 && E % n_ranks != 0))
+    return fail(MOE_ERR_INVALID, "n_ranks = %d must be 0 or a divisor of E in [1, %d]", n_ranks, MOE_MAX_RANKS);
+  if (!counts_out || !f || !P_out || !scalars || (n_ranks > 0 && !rank_load))
+    return fail(MOE_ERR_INVALID, "a combined output is NULL");
+  if (!aligned(counts, 4) || !aligned(P, 4) || !aligned(counts_out, 4) || !aligned(f, 4) || !aligned(P_out, 4) ||
+      !aligned(scalars, 4) || (rank_load && !aligned(rank_load, 4)))
+    return fail(MOE_ERR_INVALID, "an array is not 4-byte aligned");
+  moe::CombineParams p;
+  std::memset(&p, 0, sizeof(p));
+  long long T = 0;
+  for (int g = 0; g < G; ++g) {
+    if (T_shard[g] < 0 || T_shard[g] >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T_shard[%d] = %lld outside [0, 2^31)", g, (long long)T_shard[g]);
+    T += T_shard[g];
+    p.T_shard[g] = double(T_shard[g]);
+  }
+  if (T < 1 || T * (long long)k >= (1ll << 31)) return fail(MOE_ERR_INVALID, "the shards' total T = %lld must be >= 1 with T*k < 2^31", T);
+  p.counts = counts;
+  p.P = P;
+  p.G = G;
+  p.E = E;
+  p.k = k;
+  p.T = T;
+  p.alpha = alpha;
+  p.n_ranks = n_ranks;
+  p.masked_p = masked_p != 0;
+  p.counts_out = counts_out;
+  p.f = f;
+  p.P_out = P_out;
+  p.scalars = scalars;
+  p.rank_load = rank_load;
+  cudaError_t e = moe::launch_router_combine(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "router_combine launch");
+  return MOE_OK;
+}
+
 moe_status moe_router_fwd_ex(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
                              float alpha, int32_t renorm, int32_t n_ranks,
                              const float* bias, int32_t masked_p, float bias_gamma, float* bias_out,

@@ -266,8 +266,9 @@ struct ExtRow {
 // that finished last: the accumulated totals go to shared memory (s_cnt, and
 // the sums of p in double in s_pe) and the accumulators are cleared for the
 // next launch.
+__device__ __forceinline__ void ext_outputs(const FwdExParams& p, const int* s_cnt, const double* s_pe);
+
 __device__ __forceinline__ void ext_finalize(const FwdExParams& p, int* s_cnt, double* s_pe) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
     s_cnt[e] = __ldcg(p.acc_count + e);
     const unsigned long long hi = __ldcg(p.acc_hi + e), lo = __ldcg(p.acc_lo + e);
@@ -277,6 +278,14 @@ __device__ __forceinline__ void ext_finalize(const FwdExParams& p, int* s_cnt, d
     p.acc_lo[e] = 0ull;
   }
   __syncthreads();
+  ext_outputs(p, s_cnt, s_pe);
+  if (threadIdx.x == 0) *p.done = 0ull;   // every CTA has counted itself: ready for the next launch
+}
+
+// counts, f, P, the scalars, the rank loads and the updated bias from the
+// totals in shared memory (s_cnt, and the sums of p in s_pe).
+__device__ __forceinline__ void ext_outputs(const FwdExParams& p, const int* s_cnt, const double* s_pe) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long TK = p.T * p.k;
   const double p_den = p.masked_p ? double(TK) : double(p.T);
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
@@ -339,10 +348,36 @@ __device__ __forceinline__ void ext_finalize(const FwdExParams& p, int* s_cnt, d
       p.scalars[4] = float(double(cmin) * double(p.E) / double(TK));
       p.scalars[5] = R > 0 ? float(sqrt(rd2 / double(R)) / double(TK)) : 0.f;
       p.scalars[6] = R > 0 ? float(double(rmax) * double(R) / double(TK)) : 0.f;
-      *p.done = 0ull;                      // every CTA has counted itself: ready for the next launch
     }
   }
 }
+
+// ---------------------------------------------------------------------------
+// Combine the forward statistics of G shards of one batch (data-parallel ranks
+// or slices routed one after another) into the batch's: counts summed exactly,
+// P = sum_s P_s * T_s / T in double (the same for masked P, whose shard value
+// divides by T_s * k), then f, the scalars and the rank loads as the forward
+// computes them.  One CTA.
+// ---------------------------------------------------------------------------
+constexpr int kMaxShards = 64;
+
+struct CombineParams {
+  const int32_t* counts;       // [G, E]
+  const float* P;              // [G, E]
+  double T_shard[kMaxShards];  // tokens of each shard (passed by value)
+  int G, E, k;
+  long long T;                 // total tokens
+  float alpha;
+  int n_ranks;
+  int masked_p;
+  int32_t* counts_out;
+  float* f;
+  float* P_out;
+  float* scalars;
+  int32_t* rank_load;
+};
+
+cudaError_t launch_router_combine(const CombineParams& p, cudaStream_t stream);
 
 template <class DT, int LPR, int VW, int NV>
 __global__ void __launch_bounds__(kExtFwdThreads, 2) router_fwd_ex_kernel(const FwdExParams p) {

@@ -172,3 +172,18 @@ def test_taot_match_rejects_bad_arguments(native_lib):
         bad = list(args)
         bad[pos] = val
         assert f(*bad) == 1, (pos, val)
+
+
+def test_combine_rejects_bad_arguments(native_lib):
+    f = native_lib.moe_router_combine
+    T2 = (C.c_int64 * 2)(100, 200)
+    bad_T = (C.c_int64 * 2)(-1, 200)
+    args = [FAKE, FAKE, T2, 2, 8, 2, 0.01, 0, 0, FAKE, FAKE, FAKE, FAKE, None, None]
+    for pos, val in [(0, None), (2, None), (3, 0), (3, 65), (4, 0), (5, 9), (6, -1.0), (7, 3), (9, None),
+                     (12, None), (2, bad_T), (10, FAKE + 2)]:
+        bad = list(args)
+        bad[pos] = val
+        assert f(*bad) == 1, (pos, val)
+    bad = list(args)
+    bad[7] = 4                                        # rank loads requested without a buffer
+    assert f(*bad) == 1
