@@ -2,11 +2,15 @@
 dispatch + backward over one batch (one launch of moe_router_step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-extra]
+                    [--workload NAME] [--no-extra] [--section next_steps|eplb|taot_match]
 
 Prints one JSON line on rank 0.  With --gpus N > 1 (under torchrun) every rank
 routes its own batch (independent replicas, weak scaling); the timed region
-is bracketed by a barrier and the slowest rank's time is reported.
+is bracketed by a barrier and the slowest rank's time is reported.  Unless
+--no-extra, the line also carries the larger router workloads (`also`), the
+separate calls, the Sinkhorn plan, the bias-routing forward / full backward /
+bias-routed step (`next_steps`), the EPLB planner (`eplb`) and TAOT Phase 2
+(`taot_match`); --section prints one of those parts alone.
 
 `--impl reference` times the CPU oracle (fp64 numpy, the only other use of
 ``oracle/`` outside the tests) on a bounded sample of the same workload.
