@@ -654,3 +654,35 @@ def check_match_invariants(match) -> None:
         assert out["moved"] == int(st.sum())
     none = match.match(w, plan, R, rpn, 0)
     assert none["moved"] == 0 and np.array_equal(none["rank_load"], before)
+
+
+def check_plan_hand_cases(eplb) -> None:
+    """Worked by hand from the page's rules.
+    Hierarchical: the page's groups [9, 7, 5, 3] (one expert each) on 2 nodes of one GPU
+    with 3 slots: node 0 takes groups {9, 3}, replicates expert 0 (9 > 3) and packs
+    4.5, 4.5, 3 -> slots [0, 0, 3]; node 1 takes {7, 5}, replicates expert 1 and packs
+    5, 3.5, 3.5 -> slots [2, 1, 1]; both GPUs carry 12.
+    Global: loads [6, 2, 1, 3] onto 6 slots of 2 GPUs: expert 0 gets two more copies
+    (6 > 3, then 6/2 ties 3/1 and the lower index wins); copies weigh 3, 2, 2, 2, 2, 1
+    (items 3, 0, 1, 4, 5, 2) and land 3 -> GPU 0, 2 -> GPU 1, 2 -> GPU 1, 2 -> GPU 0,
+    2 -> GPU 1 (the lighter), 1 -> GPU 0 (the only open one): 6 / 6."""
+    h = eplb.plan([9, 7, 5, 3], 6, 2, 2, 4)
+    assert h["hierarchical"] and h["phy2log"].tolist() == [0, 0, 3, 2, 1, 1]
+    assert h["log_count"].tolist() == [2, 2, 1, 1] and h["gpu_load"].tolist() == [12.0, 12.0]
+    g = eplb.plan([6, 2, 1, 3], 6, 2, 1, 0)
+    assert not g["hierarchical"] and g["phy2log"].tolist() == [3, 0, 2, 0, 1, 0]
+    assert g["log_count"].tolist() == [3, 1, 1, 1] and g["gpu_load"].tolist() == [6.0, 6.0]
+
+
+def check_masked_p_hand(ext, router) -> None:
+    """Two tokens, three experts, top-1, by hand: z = [0, ln 2, 0] gives p = [1/4, 1/2, 1/4]
+    and picks expert 1; z = [ln 3, 0, 0] gives p = [3/5, 1/5, 1/5] and picks expert 0.
+    Masked P = [3/5, 1/2, 0] / 2 = [0.3, 0.25, 0], balance 3 * (0.5*0.3 + 0.5*0.25) = 0.825;
+    unmasked P = [0.425, 0.35, 0.225], balance 1.1625."""
+    z = np.array([[0.0, math.log(2.0), 0.0], [math.log(3.0), 0.0, 0.0]])
+    m = ext.router_forward_ex(z.astype(np.float32), "fp32", 1, 1.0, masked_p=True)
+    u = ext.router_forward_ex(z.astype(np.float32), "fp32", 1, 1.0, masked_p=False)
+    assert m["idx"][:, 0].tolist() == [1, 0]
+    np.testing.assert_allclose(m["P"], [0.3, 0.25, 0.0], rtol=1e-7, atol=1e-9)
+    np.testing.assert_allclose(u["P"], [0.425, 0.35, 0.225], rtol=1e-7)
+    assert abs(m["balance"] - 0.825) < 1e-7 and abs(u["balance"] - 1.1625) < 1e-7

@@ -27,3 +27,7 @@ def test_replication_hand_case():
 
 def test_plan_invariants():
     pins.check_plan_invariants(eplb)
+
+
+def test_plan_hand_cases():
+    pins.check_plan_hand_cases(eplb)

@@ -132,6 +132,7 @@ MUTANTS = {
 }
 
 _orig_match = M.match
+_orig_pg = B.plan_global
 _orig_bp = B.balanced_packing
 
 

@@ -36,3 +36,7 @@ def test_full_backward_finite_differences():
 
 def test_full_backward_structure():
     pins.check_full_grad_structure(X, R)
+
+
+def test_masked_p_hand_case():
+    pins.check_masked_p_hand(X, R)
