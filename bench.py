@@ -488,7 +488,7 @@ def time_eplb(torch, device, hbm_gbs: float, reps: int = 10) -> dict:
 
 def time_taot_match(torch, device, hbm_gbs: float, reps: int = 10, K: int = 4) -> dict:
     """TAOT Phase 2 (taot_match_batched) on 1024 microbatches of 384 experts over
-    64 ranks in 8 nodes, K = 4 replica slots per cold rank, fed by the Phase 1
+    64 ranks in 8 nodes, up to K = 4 replicas per cold rank, fed by the Phase 1
     plan of taot_sinkhorn_batched; a CUDA graph of `reps` calls of Phase 1 +
     Phase 2 and of Phase 2 alone, with the residual imbalance (max - mean) / mean
     of the rank loads before and after."""
@@ -510,7 +510,7 @@ def time_taot_match(torch, device, hbm_gbs: float, reps: int = 10, K: int = 4) -
     imb = lambda x: float(((x.max(dim=1).values - x.mean(dim=1)) / x.mean(dim=1)).mean())
     nbytes = w.B * (w.E * 4 + R * R * 4 + 2 * R * K * 4 + R * 4)
     return {"workload": w.name, "B": w.B, "E": w.E, "R": R, "ranks_per_node": rpn, "K": K,
-            "bound": "latency (K dependent rounds of score, arbitration and commit per microbatch)",
+            "bound": "latency (dependent rounds of score, arbitration and commit per microbatch, until no cold rank matches)",
             "us_per_call_phase2": round(us_match, 2), "us_per_call_phase1_and_2": round(us_both, 2),
             "microbatches_per_s": round(w.B / (us_match * 1e-6), 1), "algorithmic_bytes_phase2": nbytes,
             "frac_of_hbm_peak": round(nbytes / (us_match * 1e-6) / 1e9 / hbm_gbs, 5),

@@ -366,7 +366,8 @@ MOE_API moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t 
 /* TAOT Phase 2 ([P4] §2, §3): column-first matching of hot experts to cold
  * ranks, for B microbatches at once (one CTA each).  Experts live on their home
  * ranks contiguously (E/R per rank); a rank is hot above the mean load, cold
- * below it.  K rounds: every cold rank with a free slot picks the hot expert
+ * below it.  Rounds repeat until no cold rank finds a match (at most R*K + 1):
+ * every cold rank with a free slot (at most K replicas each) picks the hot expert
  * that scores best,
  *   (tokens moved x, 1 if same node else 0, plan[h,c], then the lower expert),
  *   x = min(tokens of e still at home, floor(load[h] - mean), floor(mean - load[c])),

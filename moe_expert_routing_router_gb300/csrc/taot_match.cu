@@ -1,8 +1,9 @@
 // Batched TAOT Phase 2: column-first iterative matching of hot experts to cold
 // ranks, as section 2 of the LoongForge TAOT article describes it ("MoE 训练端到端
-// 加速 1.43 倍 ..."): K rounds in which every cold rank picks its best hot expert
-// on its own, conflicts over one expert are arbitrated, and a rank that lost
-// picks again in the next round; each cold rank hosts at most K replicas.
+// 加速 1.43 倍 ..."): rounds in which every cold rank picks its best hot expert on
+// its own, conflicts over one expert are arbitrated, and a rank that lost picks
+// again in the next round, until no cold rank finds a match; each cold rank
+// hosts at most K replicas.
 //
 // The pair score is (tokens moved, same node, Phase 1 flow plan[h, c]), then the
 // lower expert index; arbitration uses the same score, then the lower rank
@@ -49,6 +50,7 @@ struct MatchSmem {
   int32_t* win;        // [E] winning rank of each expert this round, or -1
   int32_t* cand;       // [E] this round's candidates: experts on hot ranks with tokens left
   int32_t* n_cand;     // [1]
+  int32_t* any;        // [1] the round had a choice (another round follows)
   long long* total;    // [1]
 };
 
@@ -70,7 +72,9 @@ __host__ __device__ inline size_t match_layout(int E, int R, MatchSmem* s, char*
   char* win = take(4u * E);
   char* cand = take(4u * E);
   char* n_cand = take(4u);
+  char* any = take(4u);
   if (s) {
+    s->any = reinterpret_cast<int32_t*>(any);
     s->cand = reinterpret_cast<int32_t*>(cand);
     s->n_cand = reinterpret_cast<int32_t*>(n_cand);
     s->load = reinterpret_cast<long long*>(load);
@@ -135,7 +139,11 @@ __global__ void __launch_bounds__(kMatchThreads) taot_match_kernel(const MatchPa
     *s.total = t;
   }
   __syncthreads();
-  for (int round = 0; round < K; ++round) {
+  // Rounds repeat while some cold rank still finds a positive match.  A round
+  // with a choice commits at least its lowest-ranked winner (no earlier move of
+  // the round changed its numbers), and a rank holds at most K replicas, so
+  // there are at most R * K + 1 rounds.
+  for (int round = 0; round <= R * K; ++round) {
     // This round's candidates: experts whose home rank is hot and that still
     // have tokens at home (in any order: the score breaks ties by index).
     if (threadIdx.x == 0) *s.n_cand = 0;
@@ -202,10 +210,16 @@ __global__ void __launch_bounds__(kMatchThreads) taot_match_kernel(const MatchPa
           s.n_slots[c] += 1;
         }
       }
+      int chosen = 0;
       for (int c = 0; c < R; ++c)
-        if (s.choice[c] >= 0) s.win[s.choice[c]] = -1;
+        if (s.choice[c] >= 0) {
+          s.win[s.choice[c]] = -1;
+          ++chosen;
+        }
+      *s.any = chosen;
     }
     __syncthreads();
+    if (*s.any == 0) break;                   // written before the barrier, rewritten only after the next two
   }
   for (int r = threadIdx.x; r < R; r += blockDim.x) p.rank_load[(long long)b * R + r] = int32_t(s.load[r]);
 }

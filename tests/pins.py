@@ -603,22 +603,32 @@ def check_match_hand_single(match) -> None:
 
 
 def check_match_hand_arbitration(match) -> None:
-    """Four ranks, two per node, one expert each: loads [10, 2, 2, 2], mean 4.  Every cold
-    rank wants expert 0 (2 tokens each).  Round 1: rank 1 shares rank 0's node and wins.
-    Round 2: rank 1 is at the mean; ranks 2 and 3 tie on tokens and topology, and the
-    flow plan prefers rank 3.  Round 3: rank 2.  All four end at the mean."""
+    """Four ranks, two per node, one expert each.
+    (a) Loads [10, 2, 2, 2], mean 4: every cold rank wants expert 0 (2 tokens each); rank 1
+        shares rank 0's node and wins round 1, then the larger flow (rank 3), then rank 2:
+        all end at the mean, whatever K >= 1.
+    (b) Loads [2, 6, 8, 8], mean 6, K = 1: cold rank 0 can take 2 tokens of expert 2 or of
+        expert 3, both across nodes: the flow decides (plan[3, 0] > plan[2, 0]: expert 3).
+    (c) Loads [8, 4, 4, 8], mean 6, K = 1: cold rank 1 takes rank 0's expert (same node)
+        and cold rank 2 rank 3's, although the flow prefers the cross-node pairs."""
     plan = np.zeros((4, 4), np.float32)
     plan[0, 2], plan[0, 3] = 0.25, 0.5
-    out = match.match([10, 2, 2, 2], plan, R=4, ranks_per_node=2, K=3)
-    assert out["slot_expert"][:, 0].tolist() == [-1, 0, 0, 0]
-    assert out["slot_tokens"][:, 0].tolist() == [0, 2, 2, 2]
-    assert out["rank_load"].tolist() == [4, 4, 4, 4]
-    one = match.match([10, 2, 2, 2], plan, R=4, ranks_per_node=2, K=1)
-    assert one["slot_expert"][:, 0].tolist() == [-1, 0, -1, -1]
-    flip = plan.copy()
-    flip[0, 2], flip[0, 3] = 0.5, 0.25
-    two = match.match([10, 2, 2, 2], flip, R=4, ranks_per_node=2, K=2)
-    assert two["slot_expert"][:, :2].tolist() == [[-1, -1], [0, -1], [0, -1], [-1, -1]]
+    for K in (1, 3):
+        out = match.match([10, 2, 2, 2], plan, R=4, ranks_per_node=2, K=K)
+        assert out["slot_expert"][:, 0].tolist() == [-1, 0, 0, 0]
+        assert out["slot_tokens"][:, 0].tolist() == [0, 2, 2, 2]
+        assert out["rank_load"].tolist() == [4, 4, 4, 4]
+    pb = np.zeros((4, 4), np.float32)
+    pb[2, 0], pb[3, 0] = 0.25, 0.5
+    out = match.match([2, 6, 8, 8], pb, R=4, ranks_per_node=2, K=1)
+    assert out["slot_expert"][:, 0].tolist() == [3, -1, -1, -1] and out["rank_load"].tolist() == [4, 6, 8, 6]
+    pb[2, 0], pb[3, 0] = 0.5, 0.25
+    out = match.match([2, 6, 8, 8], pb, R=4, ranks_per_node=2, K=1)
+    assert out["slot_expert"][:, 0].tolist() == [2, -1, -1, -1] and out["rank_load"].tolist() == [4, 6, 6, 8]
+    pc = np.zeros((4, 4), np.float32)
+    pc[0, 1], pc[3, 1], pc[0, 2], pc[3, 2] = 0.1, 0.9, 0.9, 0.1
+    out = match.match([8, 4, 4, 8], pc, R=4, ranks_per_node=2, K=1)
+    assert out["slot_expert"][:, 0].tolist() == [-1, 0, 3, -1] and out["rank_load"].tolist() == [6, 6, 6, 6]
 
 
 def check_match_invariants(match) -> None:
