@@ -696,3 +696,57 @@ def check_masked_p_hand(ext, router) -> None:
     np.testing.assert_allclose(m["P"], [0.3, 0.25, 0.0], rtol=1e-7, atol=1e-9)
     np.testing.assert_allclose(u["P"], [0.425, 0.35, 0.225], rtol=1e-7)
     assert abs(m["balance"] - 0.825) < 1e-7 and abs(u["balance"] - 1.1625) < 1e-7
+
+
+def _row_first_match(w, plan, R, rpn, K):
+    """An expert-major greedy for comparison (the "row-first" order the TAOT page
+    argues against): hot experts heaviest first, each placing replicas on the
+    best-scoring cold ranks until its home rank or the cold ranks are spent."""
+    w = [int(x) for x in w]
+    E = len(w)
+    per = E // R
+    load = [sum(w[r * per:(r + 1) * per]) for r in range(R)]
+    total = sum(load)
+    w_rem, used, n_slots = list(w), set(), [0] * R
+    P = np.asarray(plan, np.float32)
+    for e in sorted(range(E), key=lambda e: (-w[e], e)):
+        h = e // per
+        while load[h] * R > total and w_rem[e] > 0:
+            best = None
+            for c in range(R):
+                if n_slots[c] >= K or load[c] * R >= total or (c, e) in used:
+                    continue
+                x = min(w_rem[e], (load[h] * R - total) // R, (total - load[c] * R) // R)
+                if x > 0:
+                    s = (x, 1 if h // rpn == c // rpn else 0, float(P[h, c]), -c)
+                    if best is None or s > best[0]:
+                        best = (s, c, x)
+            if best is None:
+                break
+            _, c, x = best
+            load[h] -= x
+            load[c] += x
+            w_rem[e] -= x
+            used.add((c, e))
+            n_slots[c] += 1
+    return np.asarray(load)
+
+
+def check_match_column_first_claim(match, sinkhorn) -> None:
+    """[P4] §2: the column-first matching leaves less residual imbalance than a
+    row-first (expert-major) order, 1-2 % against 7-10 % on the page's loads.  On
+    seeded Zipf loads (s 0.6-1.0, 16-64 ranks, K 2-4) the column-first plan's mean
+    residual is below the expert-major greedy's and below 5 %."""
+    rng = np.random.default_rng(80)
+    col, row = [], []
+    for s_exp, R, per, K in ((0.6, 16, 4, 2), (0.8, 32, 6, 2), (0.5, 64, 6, 4), (1.0, 16, 4, 3)):
+        for _ in range(8):
+            E = R * per
+            p = (np.arange(E) + 1.0) ** -s_exp
+            w = rng.multinomial(200 * E, p[rng.permutation(E)] / p.sum())
+            rl = w.reshape(R, per).sum(axis=1).astype(np.float64)
+            plan = np.asarray(sinkhorn.taot_phase1(rl[None, :], 8, 10.0, None, 50)["plan"][0], np.float32)
+            col.append(match.residual_imbalance(match.match(w, plan, R, 8, K)["rank_load"]))
+            row.append(match.residual_imbalance(_row_first_match(w, plan, R, 8, K)))
+    assert np.mean(col) < np.mean(row), (np.mean(col), np.mean(row))
+    assert np.mean(col) < 0.05, np.mean(col)

@@ -126,12 +126,64 @@ MUTANTS = {
     "matching ignores the topology": (
         [(M, "match", lambda w, plan, R, ranks_per_node, K: _orig_match(w, plan, R, R, K))],
         [lambda: pins.check_match_hand_arbitration(M)]),
+    "matching stops after K rounds": (
+        [(M, "match", lambda w, plan, R, ranks_per_node, K: _k_rounds_match(w, plan, R, ranks_per_node, K))],
+        [lambda: pins.check_match_column_first_claim(M, S), lambda: pins.check_match_hand_arbitration(M)]),
     "matching prefers the smaller flow": (
         [(M, "match", lambda w, plan, R, ranks_per_node, K: _orig_match(w, -np.asarray(plan), R, ranks_per_node, K))],
         [lambda: pins.check_match_hand_arbitration(M)]),
 }
 
 _orig_match = M.match
+
+
+def _k_rounds_match(w, plan, R, rpn, K):
+    """The matching cut to exactly K rounds (a rank that lost does not get its slot back)."""
+    w = [int(x) for x in w]
+    E = len(w)
+    per = E // R
+    load = [sum(w[r * per:(r + 1) * per]) for r in range(R)]
+    total = sum(load)
+    w_rem, used, n = list(w), set(), [0] * R
+    se, st = np.full((R, K), -1), np.zeros((R, K), np.int64)
+    P = np.asarray(plan, np.float32)
+
+    def mv(c, e):
+        h = e // per
+        if load[h] * R <= total or load[c] * R >= total or (c, e) in used or w_rem[e] <= 0:
+            return 0
+        return max(0, min(w_rem[e], (load[h] * R - total) // R, (total - load[c] * R) // R))
+
+    for _ in range(K):
+        ch = {}
+        for c in range(R):
+            if n[c] >= K:
+                continue
+            best = None
+            for e in range(E):
+                x = mv(c, e)
+                if x > 0:
+                    sc = (x, 1 if (e // per) // rpn == c // rpn else 0, float(P[e // per, c]))
+                    if best is None or sc > best[0]:
+                        best = (sc, e)
+            if best:
+                ch[c] = best
+        win = {}
+        for c in sorted(ch):
+            sc, e = ch[c]
+            if e not in win or sc > win[e][0]:
+                win[e] = (sc, c)
+        for c in sorted(c for _, c in win.values()):
+            e = ch[c][1]
+            x = mv(c, e)
+            if x > 0:
+                load[e // per] -= x
+                load[c] += x
+                w_rem[e] -= x
+                used.add((c, e))
+                se[c, n[c]], st[c, n[c]] = e, x
+                n[c] += 1
+    return {"slot_expert": se, "slot_tokens": st, "rank_load": np.asarray(load), "moved": int(st.sum())}
 _orig_pg = B.plan_global
 _orig_bp = B.balanced_packing
 

@@ -16,3 +16,8 @@ def test_hand_arbitration_topology_and_flow():
 
 def test_invariants():
     pins.check_match_invariants(taot_match)
+
+
+def test_column_first_beats_row_first():
+    from oracle import sinkhorn
+    pins.check_match_column_first_claim(taot_match, sinkhorn)
