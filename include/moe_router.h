@@ -6,7 +6,9 @@
  * gradient, a capacity-limited stable token->expert dispatch, and the batched
  * topology-aware Sinkhorn-Knopp flow plan of TAOT Phase 1.  Beside them: the
  * aux-loss-free bias routing, the masked P_i variant and the full router
- * backward through the gates, and the EPLB replication / packing planner.
+ * backward through the gates, the batch statistics of data-parallel shards,
+ * the EPLB replication / packing planner, and TAOT Phase 2 (column-first
+ * matching of hot experts to cold ranks).
  *
  * Sources (cited by title and section):
  *   [P1] the three-layer load-balancing article (LVS, NIC Teaming, MoE
