@@ -61,17 +61,28 @@ def algorithmic_bytes(w: synth.RouterWorkload) -> int:
     return w.T * (w.E * (esize + 4) + 16 * w.k)
 
 
+STEP_KERNEL_SOURCES = ("router_kernels.cuh", "device_common.cuh", "router_instances.cuh", "router_table.h",
+                       "router_bf16_staged.cu", "router_bf16_direct.cu", "router_fp32_staged.cu",
+                       "router_fp32_direct.cu", "router_dispatch.cu")
+
+
 def kernel_source_hash() -> str:
-    """Hash of the sources of the router step kernel and its launch (changes
-    whenever that kernel or its launch geometry does; the Sinkhorn, EPLB and
-    bias-routing / full-backward kernel files are not part of it)."""
+    """Hash of the sources of the router step kernel and its launch: the files
+    that build router_persistent_kernel, and the part of abi.cu that lays out
+    the workspace, picks the variant, sizes and launches the grid, plus the
+    moe_router_step entry point.  It changes whenever that kernel or its launch
+    does, and not when other entry points of the library do."""
     import hashlib
     h = hashlib.sha256()
     csrc = ROOT / "moe_expert_routing_router_gb300" / "csrc"
-    for f in sorted(csrc.iterdir()):
-        if f.suffix in (".cu", ".cuh", ".h") and not f.name.startswith(("sinkhorn", "eplb", "router_ext")):
-            h.update(f.name.encode())
-            h.update(f.read_bytes())
+    for name in STEP_KERNEL_SOURCES:
+        h.update(name.encode())
+        h.update((csrc / name).read_bytes())
+    abi = (csrc / "abi.cu").read_text()
+    a = abi.index("moe_status moe_router_step(")
+    part = abi[:abi.index("moe_status check_fwd_outputs(")] + abi[a:abi.index("\n}\n", a) + 3]
+    h.update(b"abi.cu")
+    h.update(part.encode())
     return h.hexdigest()[:16]
 
 
