@@ -110,14 +110,22 @@ def load_cv(loads: np.ndarray) -> float:
 def rank_loads(counts: np.ndarray, n_ranks: int) -> np.ndarray:
     """Token load of each simulated expert-parallel rank; experts are mapped
     contiguously, E / n_ranks per rank ([P4] introduction: a rank's load is the
-    tokens routed to the experts it hosts)."""
+    tokens routed to the experts it hosts).
+    Pinned by: a hand-worked 12-expert, 4-rank case; one expert per rank gives
+    the counts back, one rank the total."""
     E = len(counts)
     return np.asarray(counts).reshape(n_ranks, E // n_ranks).sum(axis=1)
 
 
 def batch_statistics(counts: np.ndarray, P: np.ndarray, T: int, k: int, alpha: float,
                      n_ranks: int = 0) -> dict:
-    """f and the batch scalars from the expert counts and P of a whole batch."""
+    """f and the batch scalars from the expert counts and P of a whole batch.
+
+    max/mean and min/mean divide by the mean assignments per expert T*k/E;
+    the rank max/mean by the mean per rank T*k/n_ranks ([P3] §5.1: max load
+    over mean load); both CVs use the population deviation.
+    Pinned by: a hand-worked 4-expert, 2-rank case (every scalar); the [P1]
+    §5.3 log line (8192 tokens, 4320 on one expert: max/mean 4.21875)."""
     E = len(counts)
     f = token_fraction(counts, T, k)
     mean = T * k / E

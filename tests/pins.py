@@ -157,14 +157,64 @@ def check_cv_closed_forms(router) -> None:
 
 
 def check_log_example(router) -> None:
-    """[P1] §5.3's log line: 8192 tokens over 8 experts, one expert receiving
-    4320; [P1] §5.4 calls max/mean above 2 imbalanced."""
+    """[P1] §5.3's log line: 8192 tokens over 8 experts, expert 3 receiving
+    4320 and expert 7 receiving 312; [P1] §5.4 calls max/mean above 2
+    imbalanced.  The oracle's batch statistics of a count vector with those
+    entries (top-1, the other six experts sharing the rest) must give the
+    printed max/mean and 312 over the mean of 1024 as min/mean."""
     g = golden("p1_s5_3_tokens_per_expert_log.json")
-    mean = g["total_tokens"] / g["num_experts"]
-    ratio = g["max_expert_tokens"] / mean
-    assert abs(ratio - g["max_over_mean"]) < 1e-12
-    assert router.is_ratio_imbalanced(ratio)
+    E, T = g["num_experts"], g["total_tokens"]
+    counts = np.zeros(E, dtype=np.int64)
+    counts[3], counts[7] = g["max_expert_tokens"], g["min_expert_tokens_shown"]
+    rest = T - counts[3] - counts[7]
+    others = [e for e in range(E) if e not in (3, 7)]
+    for i, e in enumerate(others):                    # 593 or 594 each: all above 312, below 4320
+        counts[e] = rest // len(others) + (1 if i < rest % len(others) else 0)
+    assert counts.sum() == T
+    out = router.batch_statistics(counts, np.full(E, 1.0 / E), T, 1, 0.01)
+    assert out["max_over_mean"] == g["max_over_mean"], out["max_over_mean"]
+    assert out["min_over_mean"] == g["min_expert_tokens_shown"] / (T / E), out["min_over_mean"]
+    assert router.is_ratio_imbalanced(out["max_over_mean"])
     assert not router.is_ratio_imbalanced(1.9)
+
+
+def check_rank_loads_contiguous(router) -> None:
+    """A rank's load is the tokens routed to the experts it hosts ([P4]
+    introduction), the experts laid out contiguously: with 12 experts on 4
+    ranks, rank 0 hosts experts 0-2, rank 1 experts 3-5, and so on.  Worked
+    by hand for counts 1..12: 1+2+3, 4+5+6, 7+8+9, 10+11+12.  One expert per
+    rank gives the counts back, one rank gives the total."""
+    counts = np.arange(1, 13, dtype=np.int64)
+    assert list(router.rank_loads(counts, 4)) == [6, 15, 24, 33]
+    assert list(router.rank_loads(counts, 2)) == [21, 57]
+    assert list(router.rank_loads(counts, 12)) == list(counts)
+    assert list(router.rank_loads(counts, 1)) == [78]
+
+
+def check_batch_scalars_hand(router) -> None:
+    """The scalars of batch_statistics on a case worked by hand.
+
+    T = 6 tokens, top-2, E = 4 experts, counts [6, 3, 2, 1] (12 = T*k
+    assignments, mean 3 per expert): max/mean = 6/3 = 2, min/mean = 1/3
+    ([P3] §5.1: max load over mean load), CV = pop-std / mean with
+    std = sqrt(((6-3)^2 + 0 + 1 + 4) / 4) = sqrt(14)/2.  On 2 EP ranks the
+    loads are [9, 3] (experts 0-1, 2-3), mean 6: rank max/mean = 1.5 and
+    rank CV = 3/6 = 0.5 (population std 3).  With P uniform the balance is
+    E * sum f/E = 1 and L_aux = alpha.
+    """
+    counts = np.array([6, 3, 2, 1], dtype=np.int64)
+    out = router.batch_statistics(counts, np.full(4, 0.25), 6, 2, alpha=0.5, n_ranks=2)
+    assert out["max_over_mean"] == 2.0, out["max_over_mean"]
+    assert abs(out["min_over_mean"] - 1.0 / 3.0) < 1e-15, out["min_over_mean"]
+    assert abs(out["cv"] - math.sqrt(14.0) / 2.0 / 3.0) < 1e-15, out["cv"]
+    assert list(out["rank_load"]) == [9, 3]
+    assert out["rank_max_over_mean"] == 1.5, out["rank_max_over_mean"]
+    assert abs(out["rank_cv"] - 0.5) < 1e-15, out["rank_cv"]
+    assert abs(out["balance"] - 1.0) < 1e-15 and abs(out["l_aux"] - 0.5) < 1e-15
+    np.testing.assert_array_equal(out["f"], counts / 12.0)
+    # no ranks: the rank outputs stay empty / zero
+    out0 = router.batch_statistics(counts, np.full(4, 0.25), 6, 2, alpha=0.5, n_ranks=0)
+    assert len(out0["rank_load"]) == 0 and out0["rank_cv"] == 0.0 and out0["rank_max_over_mean"] == 0.0
 
 
 def check_cv_grades(router) -> None:

@@ -65,6 +65,18 @@ MUTANTS = {
     "CV with the sample (n-1) deviation": (
         [(R, "load_cv", lambda x: float(np.std(np.asarray(x, float), ddof=1) / np.mean(x)))],
         [lambda: pins.check_cv_closed_forms(R)]),
+    "rank loads from a strided expert mapping (e mod R)": (
+        [(R, "rank_loads", lambda counts, n: np.asarray(counts).reshape(len(counts) // n, n).sum(axis=0))],
+        [lambda: pins.check_rank_loads_contiguous(R), lambda: pins.check_batch_scalars_hand(R)]),
+    "max/min over mean divided by T instead of T*k": (
+        [(R, "batch_statistics", lambda *a, **kw: _stats_over_T(*a, **kw))],
+        [lambda: pins.check_batch_scalars_hand(R), lambda: pins.check_log_example(R)]),
+    "rank max/mean over the per-expert mean": (
+        [(R, "batch_statistics", lambda *a, **kw: _stats_rank_mean_per_expert(*a, **kw))],
+        [lambda: pins.check_batch_scalars_hand(R)]),
+    "rank CV with the sample (n-1) deviation": (
+        [(R, "batch_statistics", lambda *a, **kw: _stats_rank_cv_ddof1(*a, **kw))],
+        [lambda: pins.check_batch_scalars_hand(R)]),
     "dispatch keeps the last C instead of the first": (
         [(D, "dispatch", lambda idx, E, C: _reverse_dispatch(idx, E, C))],
         [lambda: pins.check_dispatch_bruteforce(D, R)]),
@@ -249,6 +261,31 @@ _orig_dispatch = D.dispatch
 _orig_sk = S.sinkhorn_knopp
 _orig_sd = S.supply_demand
 _orig_tc = S.topology_cost
+
+
+_orig_stats = R.batch_statistics
+
+
+def _stats_over_T(counts, P, T, k, alpha, n_ranks=0):
+    out = _orig_stats(counts, P, T, k, alpha, n_ranks)
+    out["max_over_mean"] = counts.max() / (T / len(counts))
+    out["min_over_mean"] = counts.min() / (T / len(counts))
+    return out
+
+
+def _stats_rank_mean_per_expert(counts, P, T, k, alpha, n_ranks=0):
+    out = _orig_stats(counts, P, T, k, alpha, n_ranks)
+    if n_ranks > 0:
+        out["rank_max_over_mean"] = out["rank_load"].max() / (T * k / len(counts))
+    return out
+
+
+def _stats_rank_cv_ddof1(counts, P, T, k, alpha, n_ranks=0):
+    out = _orig_stats(counts, P, T, k, alpha, n_ranks)
+    if n_ranks > 0:
+        rl = np.asarray(out["rank_load"], dtype=np.float64)
+        out["rank_cv"] = float(rl.std(ddof=1) / rl.mean())
+    return out
 
 
 def _reverse_dispatch(idx, E, C):

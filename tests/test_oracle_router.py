@@ -49,6 +49,14 @@ def test_tokens_per_expert_log_example():
     pins.check_log_example(oracle.router)
 
 
+def test_rank_loads_contiguous_hand_case():
+    pins.check_rank_loads_contiguous(oracle.router)
+
+
+def test_batch_scalars_hand_case():
+    pins.check_batch_scalars_hand(oracle.router)
+
+
 def test_cv_grade_bands():
     pins.check_cv_grades(oracle.router)
 
