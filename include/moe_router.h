@@ -108,7 +108,10 @@ MOE_API moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t st
 
 /* Reads and clears the device error flags of a workspace (synchronises
  * `stream`).  *flags = 0 when every bounded wait completed; otherwise
- * returns MOE_ERR_TIMEOUT and sets bits: 1 = grid barrier wait expired. */
+ * returns MOE_ERR_TIMEOUT and sets bits: 1 = grid barrier wait expired,
+ * 2 = a wait of the kernel's internal pipeline expired.  With ws = NULL it
+ * reads and clears the flags of moe_router_step_static's fixed scratch on
+ * the current device instead. */
 MOE_API moe_status moe_get_device_status(void* ws, moe_stream_t stream, int32_t* flags);
 
 /* ------------------------------------------------------------------------ */
@@ -216,15 +219,25 @@ MOE_API moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, 
  * library until the process exits); the call allocates nothing and frees
  * nothing.
  *   - Arguments and outputs are exactly those of moe_router_step, minus the
- *     workspace; the results are the same.
+ *     workspace; the results are the same, bit for bit.
  *   - E must be <= 512 (MOE_ERR_INVALID otherwise, with a message naming the
- *     limit).
+ *     limit).  Every argument is checked before anything is queued, so a
+ *     refused call leaves the shared array untouched.
  *   - The first call on a device looks up the array's device address (a
- *     cudaGetSymbolAddress, with that device current) and caches it; make that
- *     first call before any stream capture.
+ *     cudaGetSymbolAddress, with that device current) and caches it for the
+ *     life of the process; make that first call before any stream capture.
+ *     The cache assumes the device's primary context is never reset: after a
+ *     cudaDeviceReset the library's module, and the array with it, may be
+ *     loaded at another address, so do not call this entry point again in
+ *     that process.
  *   - All calls on a device share the one array: calls that may overlap on the
  *     GPU (different streams, or different host threads) race.  Each call
- *     clears the array's control block on `stream` before its kernel. */
+ *     clears the array's barrier count, counters and group sums on `stream`
+ *     before its kernel.
+ *   - An expired device wait (MOE_ERR_TIMEOUT in moe_router_step's terms)
+ *     leaves its error bits set in the array; later calls then write nothing
+ *     until moe_get_device_status(NULL, stream, &flags) reads the bits,
+ *     returns MOE_ERR_TIMEOUT and clears them. */
 MOE_API moe_status moe_router_step_static(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
                                           float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
                                           float grad_scale,

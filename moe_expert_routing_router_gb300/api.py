@@ -395,12 +395,14 @@ def moe_router_combine(counts: torch.Tensor, P: torch.Tensor, T_shard, k: int, a
     return o
 
 
-def moe_get_device_status(ws: Workspace, stream: torch.cuda.Stream | None = None) -> int:
-    """Reads and clears the device error flags of a workspace (synchronises)."""
-    if ws.buf is None:
+def moe_get_device_status(ws: Workspace | None, stream: torch.cuda.Stream | None = None) -> int:
+    """Reads and clears the device error flags of a workspace (synchronises);
+    ws=None reads those of moe_router_step_static's fixed scratch on the
+    current device."""
+    if ws is not None and ws.buf is None:
         return 0
     flags = C.c_int32(0)
-    st = lib().moe_get_device_status(_ptr(ws.buf), _stream_handle(stream), C.byref(flags))
+    st = lib().moe_get_device_status(None if ws is None else _ptr(ws.buf), _stream_handle(stream), C.byref(flags))
     if st not in (_native.MOE_OK, _native.MOE_ERR_TIMEOUT):
         check(st, "moe_get_device_status")
     return int(flags.value)

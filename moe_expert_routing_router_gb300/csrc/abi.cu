@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -77,6 +78,10 @@ WsLayout ws_layout(int E) {
   w.total = w.counts + align_up(size_t(E) * sizeof(int32_t));
   return w;
 }
+
+// Device address of the fixed scratch array of moe_router_step_static on the
+// current device (defined with that entry point at the end of this file).
+moe_status static_scratch(void** out);
 
 // Per-device, per-kernel occupancy (blocks per SM) and SM count.
 struct DeviceInfo {
@@ -368,7 +373,11 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
 }
 
 moe_status moe_get_device_status(void* ws, moe_stream_t stream, int32_t* flags) {
-  if (!ws || !flags) return fail(MOE_ERR_INVALID, "NULL argument");
+  if (!flags) return fail(MOE_ERR_INVALID, "NULL argument");
+  if (!ws) {                       // the fixed scratch of moe_router_step_static on this device
+    moe_status s = static_scratch(&ws);
+    if (s != MOE_OK) return s;
+  }
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   moe::Ctrl c{};
@@ -493,6 +502,30 @@ moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_t k, dou
   return launch_persistent(func, p, smem, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Every check of the fused step's arguments except the workspace's.
+moe_status check_step_args(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k, float alpha,
+                           int32_t renorm, int32_t n_ranks, double capacity_factor, float grad_scale,
+                           int32_t* idx, float* gate, int32_t* counts, float* f, float* P, float* scalars,
+                           int32_t* rank_load, int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                           int32_t* n_dropped, float* dlogits) {
+  moe_status s = check_router_args(logits, dt, T, E, k);
+  if (s != MOE_OK) return s;
+  if ((s = check_fwd_outputs(k, alpha, renorm, n_ranks, E, idx, gate, counts, f, P, scalars, rank_load)) != MOE_OK) return s;
+  if (!(capacity_factor > 0.0) || !std::isfinite(capacity_factor)) return fail(MOE_ERR_INVALID, "capacity_factor must be > 0");
+  if (!std::isfinite(grad_scale)) return fail(MOE_ERR_INVALID, "grad_scale must be finite");
+  if (!perm || !slot || !offsets || !kept || !n_dropped || !dlogits) return fail(MOE_ERR_INVALID, "a dispatch or backward output is NULL");
+  if (!aligned(dlogits, 4)) return fail(MOE_ERR_INVALID, "dlogits is not 4-byte aligned");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
                            float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
                            float grad_scale,
@@ -501,13 +534,9 @@ moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t 
                            int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
                            int32_t* n_dropped, float* dlogits,
                            void* ws, size_t ws_bytes, moe_stream_t stream) {
-  moe_status s = check_router_args(logits, dt, T, E, k);
+  moe_status s = check_step_args(logits, dt, T, E, k, alpha, renorm, n_ranks, capacity_factor, grad_scale, idx, gate,
+                                 counts, f, P, scalars, rank_load, perm, slot, offsets, kept, n_dropped, dlogits);
   if (s != MOE_OK) return s;
-  if ((s = check_fwd_outputs(k, alpha, renorm, n_ranks, E, idx, gate, counts, f, P, scalars, rank_load)) != MOE_OK) return s;
-  if (!(capacity_factor > 0.0) || !std::isfinite(capacity_factor)) return fail(MOE_ERR_INVALID, "capacity_factor must be > 0");
-  if (!std::isfinite(grad_scale)) return fail(MOE_ERR_INVALID, "grad_scale must be finite");
-  if (!perm || !slot || !offsets || !kept || !n_dropped || !dlogits) return fail(MOE_ERR_INVALID, "a dispatch or backward output is NULL");
-  if (!aligned(dlogits, 4)) return fail(MOE_ERR_INVALID, "dlogits is not 4-byte aligned");
   if ((s = check_ws(ws, ws_bytes, E)) != MOE_OK) return s;
   const RouterVariant* v = pick_variant(dt, E, aligned(logits, 16) && aligned(dlogits, 16));
   if (!v) return fail(MOE_ERR_INVALID, "no kernel variant for E = %d", E);
@@ -850,15 +879,26 @@ extern "C" moe_status moe_router_step_static(const void* logits, moe_dtype dt, i
   if (E > kStaticMaxExperts)
     return fail(MOE_ERR_INVALID, "moe_router_step_static serves at most %d experts (E = %d); use moe_router_step",
                 kStaticMaxExperts, E);
-  void* ws = nullptr;
-  moe_status s = static_scratch(&ws);
+  // Every argument is checked before anything is queued on the stream, so a
+  // refused call leaves the shared array as it was.
+  moe_status s = check_step_args(logits, dt, T, E, k, alpha, renorm, n_ranks, capacity_factor, grad_scale, idx, gate,
+                                 counts, f, P, scalars, rank_load, perm, slot, offsets, kept, n_dropped, dlogits);
   if (s != MOE_OK) return s;
+  void* ws = nullptr;
+  if ((s = static_scratch(&ws)) != MOE_OK) return s;
   const size_t need = ws_layout(E).total;
   if (need > kStaticScratchBytes) return fail(MOE_ERR_INVALID, "E = %d needs %zu bytes of scratch", E, need);
-  // The array keeps the previous call's contents; the control block (barrier
-  // state, error flags) and the group sums must start at zero, the rest is
-  // written before it is read.
-  cudaError_t e = cudaMemsetAsync(ws, 0, ws_layout(E).tile_hist, stream);
+  // The array keeps the previous call's contents.  The barrier's arrival
+  // count (the low half of the control block's first word), the other
+  // counters and the group sums must start at zero; the rest is written
+  // before it is read.  The error bits (the first word's high half) are left
+  // as they are: after an expired wait they stay set, later calls write
+  // nothing, and moe_get_device_status(NULL, ...) reads and clears them.
+  static_assert(offsetof(moe::Ctrl, sync) == 0 && offsetof(moe::Ctrl, done) == 8, "control block layout");
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(static_cast<unsigned char*>(ws) + offsetof(moe::Ctrl, done), 0,
+                        ws_layout(E).tile_hist - offsetof(moe::Ctrl, done), stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   return moe_router_step(logits, dt, T, E, k, alpha, renorm, n_ranks, capacity_factor, grad_scale, idx, gate, counts,
                          f, P, scalars, rank_load, perm, slot, offsets, kept, n_dropped, dlogits, ws, need, stream);

@@ -25,7 +25,7 @@ constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
 // arrive at the launch's final barrier takes it back to 0.  A failed launch
 // leaves the count wherever it stopped and the error bits set; the host reads
 // and clears both (moe_get_device_status), and until then every later launch
-// sees the error at its first barrier and writes nothing.
+// sees the error at its first barrier and writes nothing after it.
 // ---------------------------------------------------------------------------
 struct Ctrl {
   unsigned long long sync;      // [31:0] arrivals, [63:32] error bits
