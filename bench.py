@@ -7,7 +7,7 @@ dispatch + backward over one batch (one launch of moe_router_step).
 Prints one JSON line on rank 0.  With --gpus N > 1 (under torchrun) every rank
 routes its own batch (independent replicas, weak scaling); the timed region
 is bracketed by a barrier and the slowest rank's time is reported.  Unless
---no-extra, the line also carries the larger router workloads (`also`), the
+--no-extra, the line also carries the other router workloads (`also`), the
 separate calls, the Sinkhorn plan, the bias-routing forward / full backward /
 bias-routed step (`next_steps`), the EPLB planner (`eplb`) and TAOT Phase 2
 (`taot_match`); --section prints one of those parts alone.
@@ -41,8 +41,9 @@ sys.path.insert(0, str(ROOT))
 import synth  # noqa: E402
 
 METRIC = "router fwd+bwd+dispatch tokens/s; achieved HBM GB/s vs GB300 peak"
-DEFAULT_WORKLOAD = "zipf-top2-T65536-E64"
-EXTRA_WORKLOADS = ("zipf-hot-top8-T131072-E256", "zipf-ep64-top6-T262144-E384")
+DEFAULT_WORKLOAD = "zipf-ep64-top6-T262144-E384"
+EXTRA_WORKLOADS = ("zipf-top2-T65536-E64", "zipf-hot-top8-T131072-E256")
+DETAIL_WORKLOADS = ("zipf-top2-T65536-E64", "zipf-ep64-top6-T262144-E384")   # separate calls, next steps
 SINKHORN_WORKLOAD = "taot-sinkhorn-B1024-R64"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
@@ -190,13 +191,42 @@ def out_buffers(w, torch, device) -> dict:
     }
 
 
+def replay_plan(steps: int, n_min: int) -> tuple[int, int, int]:
+    """(steps per graph S, replays R, buffer sets) for K = steps timed steps:
+    R * S = K with R >= 10 where K allows, and the buffer sets (at least
+    n_min) dividing S, so that every replay rotates through them the same way.
+    When no divisor of S reaches n_min, one graph of all K steps is replayed
+    once."""
+    S = 1
+    for d in range(max(1, steps // 10), 0, -1):
+        if steps % d == 0:
+            S = d
+            break
+    for n in range(n_min, S + 1):
+        if S % n == 0:
+            return S, steps // S, n
+    return steps, 1, n_min
+
+
+def percentile(xs: list[float], q: float) -> float:
+    ys = sorted(xs)
+    if len(ys) == 1:
+        return ys[0]
+    pos = q * (len(ys) - 1)
+    lo = int(math.floor(pos))
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
+
+
 def time_router(w, steps: int, warmup: int, torch, device, dist_ctx, soak_s: float = 0.0, sampler=None) -> dict:
-    """Device-timed steps of moe_router_step with buffers rotated so that the
-    working set of consecutive steps exceeds L2 several times over."""
+    """Device-timed steps of moe_router_step: K steps as R replays of one CUDA
+    graph of S steps (R >= 10 where K allows), each replay between two CUDA
+    events on the launching stream; buffers rotated so that a set is reused
+    only after at least 3x the L2 of other traffic."""
     import moe_expert_routing_router_gb300 as mr
     logits = synth.router_logits(w)
     step_bytes = algorithmic_bytes(w)
-    n_sets = max(2, math.ceil(3 * L2_BYTES / step_bytes))
+    S, R, n_sets = replay_plan(steps, max(2, math.ceil(3 * L2_BYTES / step_bytes)))
     x0 = to_device(logits, w.dtype, torch, device)
     xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
     outs = [out_buffers(w, torch, device) for _ in range(n_sets)]
@@ -210,132 +240,95 @@ def time_router(w, steps: int, warmup: int, torch, device, dist_ctx, soak_s: flo
     for i in range(max(warmup, 3)):
         step(i)
     torch.cuda.synchronize(device)
-    # The K timed steps are captured once into a CUDA graph so that the device
-    # time is measured, not the Python-side launch rate.
-    graph = None
-    try:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for s in range(steps):
-                step(s)
-        graph = g
-    except Exception as e:  # capture unsupported: time eager launches instead
-        log(f"CUDA graph capture failed ({e!r}); timing eager launches")
-        torch.cuda.synchronize(device)
-
-    def run_steps():
-        if graph is not None:
-            graph.replay()
-        else:
-            for s in range(steps):
-                step(s)
-
-    run_steps()
+    # S steps captured once into a CUDA graph, so that the device time is
+    # measured, not the Python-side launch rate.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(S):
+            step(i)
+    graph.replay()
     torch.cuda.synchronize(device)
     if sampler is not None:
         sampler.start()
     t_end = time.time() + soak_s
     while time.time() < t_end:                      # loaded window for the clock samples
-        run_steps()
+        graph.replay()
         torch.cuda.synchronize(device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(R + 1)]
     dist_ctx.barrier()
     torch.cuda.synchronize(device)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    run_steps()
-    t1.record(stream)
+    ev[0].record(stream)
+    for r in range(R):
+        graph.replay()
+        ev[r + 1].record(stream)
     torch.cuda.synchronize(device)
     dist_ctx.barrier()
     clocks = sampler.stop() if sampler is not None else None
-    total_ms = t0.elapsed_time(t1)
+    total_ms = ev[0].elapsed_time(ev[R])
+    per_step = [ev[r].elapsed_time(ev[r + 1]) / S for r in range(R)]
     flags = mr.moe_get_device_status(ws)
     if flags:
         raise RuntimeError(f"device wait expired during the benchmark (flags {flags})")
-    # one kernel per step: its mean launch duration is the device time per step
+    # one kernel per step: the mean step time is its mean launch duration
     return {"total_ms": dist_ctx.max(total_ms), "launch_ms_mean": total_ms / steps, "n_sets": n_sets,
             "clocks": clocks, "step_bytes": step_bytes,
-            "timing": ("CUDA graph of the timed steps replayed once between two CUDA events" if graph is not None
-                       else "eager launches between two CUDA events")}
+            "spread": {"replays": R, "steps_per_replay": S, "ms_per_step_median": statistics.median(per_step),
+                       "ms_per_step_p10": percentile(per_step, 0.1), "ms_per_step_p90": percentile(per_step, 0.9)},
+            "timing": f"{R} replays of a CUDA graph of {S} steps, each between two CUDA events on the launching stream"}
 
 
 def time_e2e(w, steps: int, warmup: int, torch, device, dist_ctx) -> dict:
-    """The step through the public API with its input in pinned HOST memory:
-    every step copies its logits host -> device (double-buffered on a copy
-    stream, so that step i + 1's copy overlaps step i's kernel) and reads its
-    result back to pinned host memory (the scalars -- L_aux, balance, CV,
-    max/min over mean, rank CV -- and the per-expert counts).  Timed twice:
-    the copies and calls issued eagerly from Python, and the same sequence of
-    K steps captured once in a CUDA graph and replayed (the value reported)."""
+    """The step through the C ABI on HOST buffers (moe_router_step_host):
+    every step copies its logits from pinned host memory into device staging,
+    runs the step, and copies every output back to pinned host memory (idx,
+    gate, counts, f, P, scalars, rank loads, perm, slot, offsets, kept,
+    n_dropped, dlogits).  Consecutive steps alternate between two streams,
+    each with its own staging buffer, workspace and host outputs, so that one
+    step's copies overlap the other's kernel; the kernels run one after the
+    other (each waits for the previous step's kernel_done event)."""
     import moe_expert_routing_router_gb300 as mr
     logits = synth.router_logits(w)
     host_x = to_device(logits, w.dtype, torch, "cpu").pin_memory()
-    dev_x = [torch.empty_like(host_x, device=device) for _ in range(2)]
-    outs = out_buffers(w, torch, device)
-    result_keys = ("scalars", "counts")
-    host_res = {k: torch.empty_like(outs[k], device="cpu").pin_memory() for k in result_keys}
-    ws = mr.Workspace(device)
-    copy = torch.cuda.Stream(device)
-    copied = [torch.cuda.Event() for _ in range(2)]
-    consumed = [torch.cuda.Event() for _ in range(2)]
+    streams = [torch.cuda.Stream(device) for _ in range(2)]
+    wss = [mr.Workspace(device) for _ in range(2)]
+    dev_bytes = mr.moe_router_step_host_device_size(host_x.dtype, w.T, w.E, w.k, w.n_ranks)
+    devs = [torch.empty(dev_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    outs = [mr.host_step_outputs(w.T, w.E, w.k, w.n_ranks) for _ in range(2)]
     h2d = host_x.numel() * host_x.element_size()
-    d2h = sum(outs[k].numel() * outs[k].element_size() for k in result_keys)
+    d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
 
-    def run(n, start):
-        # start: an event on the compute stream that the first copy waits for
-        compute = torch.cuda.current_stream(device)
+    compute = torch.cuda.current_stream(device)
+    done = [torch.cuda.Event() for _ in range(2)]
+    for e in done:                                   # creates the events' CUDA handles
+        e.record(compute)
 
-        def h2d_into(b, after):
-            with torch.cuda.stream(copy):
-                copy.wait_event(after)               # the kernel that read this buffer is done
-                dev_x[b].copy_(host_x, non_blocking=True)
-                copied[b].record(copy)
-
-        h2d_into(0, start)
+    def run(n):
         for i in range(n):
             b = i & 1
-            compute.wait_event(copied[b])
-            mr.moe_router_step(dev_x[b], w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm),
-                               n_ranks=w.n_ranks, grad_scale=1.0, ws=ws, out=outs)
-            consumed[b].record(compute)
-            if i + 1 < n:
-                h2d_into(b ^ 1, consumed[b ^ 1] if i >= 1 else start)
-            for k2 in result_keys:
-                host_res[k2].copy_(outs[k2], non_blocking=True)
+            mr.moe_router_step_host(host_x, w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm),
+                                    n_ranks=w.n_ranks, grad_scale=1.0, ws=wss[b], dev=devs[b], out=outs[b],
+                                    stream=streams[b], device=device, kernel_after=done[b ^ 1],
+                                    kernel_done=done[b])
 
-    def timed(fn):
-        compute = torch.cuda.current_stream(device)
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(device)
-        dist_ctx.barrier()
-        t0.record(compute)
-        fn(t0)
-        t1.record(compute)
-        torch.cuda.synchronize(device)
-        dist_ctx.barrier()
-        return dist_ctx.max(t0.elapsed_time(t1)) / steps
-
-    w0 = torch.cuda.Event()
-    w0.record(torch.cuda.current_stream(device))
-    run(max(warmup, 3), w0)
+    run(max(warmup, 3))
     torch.cuda.synchronize(device)
-    eager_ms = timed(lambda t0: run(steps, t0))
-    graph_ms = None
-    try:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            s0 = torch.cuda.Event()
-            s0.record(torch.cuda.current_stream(device))
-            run(steps, s0)
-        g.replay()
-        torch.cuda.synchronize(device)
-        graph_ms = timed(lambda t0: g.replay())
-    except Exception as e:  # capture unsupported: report the eager number
-        log(f"CUDA graph capture of the end-to-end steps failed ({e!r}); reporting eager launches")
-    return {"ms_per_step": graph_ms if graph_ms is not None else eager_ms, "eager_ms_per_step": eager_ms,
-            "graph": graph_ms is not None, "h2d": h2d, "d2h": d2h,
-            "read_back": "scalars (L_aux, balance, CV, max/min over mean, rank CV, rank max/mean) and counts"}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    dist_ctx.barrier()
+    t0.record(compute)
+    for s in streams:
+        s.wait_event(t0)
+    run(steps)
+    for s in streams:
+        compute.wait_stream(s)
+    t1.record(compute)
+    torch.cuda.synchronize(device)
+    dist_ctx.barrier()
+    ms = dist_ctx.max(t0.elapsed_time(t1)) / steps
+    for b in range(2):
+        if mr.moe_get_device_status(wss[b]):
+            raise RuntimeError("device wait expired during the end-to-end benchmark")
+    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h, "steps": steps}
 
 
 def time_calls(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
@@ -704,6 +697,7 @@ def run_ours(args) -> dict:
         "config": config_of(w, {"l2": f"inputs and outputs rotated over {r['n_sets']} buffer sets "
                                       f"(>= 3x the 129 MB L2 between reuses)",
                                 "parallelism": f"replicas x{dist_ctx.world}", "timing": r["timing"]}),
+        "spread": r["spread"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / pk["hbm_gbs"], 4),
                      "traffic": (lambda t: None if t is None else t["read"] + t["write"])(measured_traffic(w.name)),
@@ -712,12 +706,13 @@ def run_ours(args) -> dict:
                      "launch_us_mean": round(r["launch_ms_mean"] * 1e3, 2), "peak_source": pk["source"]},
         "e2e": {"value": dist_ctx.world * w.T / (e2e["ms_per_step"] * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": e2e["ms_per_step"], "eager_ms_per_step": e2e["eager_ms_per_step"],
-                "read_back": e2e["read_back"],
-                "timing": ("the API calls of K steps captured in one CUDA graph and replayed" if e2e["graph"]
-                           else "eager API calls") +
-                          "; logits copied from pinned host memory every step on a copy stream (double-buffered), "
-                          "the step's result read back every step"},
+                "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"],
+                "read_back": "every output of the step: idx, gate, counts, f, P, scalars, rank_load, perm, slot, "
+                             "offsets, kept, n_dropped, dlogits",
+                "timing": "C-ABI moe_router_step_host calls issued eagerly, alternating over two streams (each "
+                          "with its own staging buffer and workspace; kernels ordered one after the other); the "
+                          "logits copied from pinned host memory and every output copied back to pinned host "
+                          "memory each step; CUDA events around all K steps"},
         "gpu_launches": args.steps,
         "clocks": r["clocks"],
     }
@@ -725,21 +720,24 @@ def run_ours(args) -> dict:
         also = {}
         for name in EXTRA_WORKLOADS:
             wx = synth.ROUTER_WORKLOADS[name]
-            rx = time_router(wx, max(10, min(args.steps, 50)), args.warmup, torch, device, _Solo())
-            msx = rx["total_ms"] / max(10, min(args.steps, 50))
+            kx = max(args.steps, 10)
+            rx = time_router(wx, kx, args.warmup, torch, device, _Solo())
+            msx = rx["total_ms"] / kx
             ach = rx["step_bytes"] / (rx["launch_ms_mean"] * 1e-3) / 1e9
             also[name] = {"value": wx.T / (msx * 1e-3), "unit": "tokens/s", "ms_per_step": msx,
                           "launch_us_mean": round(rx["launch_ms_mean"] * 1e3, 2),
                           "roofline_frac": round(ach / pk["hbm_gbs"], 4), "achieved_gbs": round(ach, 1),
-                          "algorithmic_bytes_per_launch": rx["step_bytes"]}
+                          "algorithmic_bytes_per_launch": rx["step_bytes"], "spread": rx["spread"],
+                          "traffic": (lambda t: None if t is None else t["read"] + t["write"])(
+                              measured_traffic(wx.name))}
         line["also"] = also
         line["separate_calls"] = {name: time_calls(synth.ROUTER_WORKLOADS[name], torch, device, pk["hbm_gbs"])
-                                  for name in (w.name, EXTRA_WORKLOADS[-1])}
+                                  for name in DETAIL_WORKLOADS}
         line["sinkhorn"] = time_sinkhorn(torch, device, pk["hbm_gbs"])
         line["eplb"] = time_eplb(torch, device, pk["hbm_gbs"])
         line["taot_match"] = time_taot_match(torch, device, pk["hbm_gbs"])
         line["next_steps"] = {name: time_next_steps(synth.ROUTER_WORKLOADS[name], torch, device, pk["hbm_gbs"])
-                              for name in (w.name, EXTRA_WORKLOADS[-1])}
+                              for name in DETAIL_WORKLOADS}
     if dist_ctx.rank == 0:
         cb = time_oracle(w, budget_s=args.cpu_seconds, min_steps=2)
         line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}

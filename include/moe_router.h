@@ -208,6 +208,41 @@ MOE_API moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, 
                            int32_t* n_dropped, float* dlogits,
                            void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_router_step for inputs and outputs in HOST memory.
+ *
+ * One call queues, on `stream`: the copy of the logits from host memory into
+ * a caller-owned device staging buffer, moe_router_step on it, and the copy
+ * of every output of the step (idx, gate, counts, f, P, scalars, rank_load,
+ * perm, slot, offsets, kept, n_dropped, dlogits) back to the host arrays.
+ * It is asynchronous: the host arrays hold the results once the stream has
+ * reached the end of the call.  The host arrays should be page-locked
+ * (cudaHostAlloc / cudaHostRegister); with pageable memory CUDA stages the
+ * copies and the call blocks the host.
+ *   - logits and every output pointer are HOST pointers with the layouts of
+ *     moe_router_step (rank_load may be NULL when n_ranks == 0).
+ *   - dev: a caller-owned device buffer of at least
+ *     moe_router_step_host_device_size(dt, T, E, k, n_ranks) bytes, 256-byte
+ *     aligned (MOE_ERR_WORKSPACE if smaller).  It is overwritten.
+ *   - ws, ws_bytes: the step's workspace, as for moe_router_step.
+ *   - kernel_after, kernel_done: cudaEvent_t handles or NULL.  The step's
+ *     kernel waits for kernel_after (cudaStreamWaitEvent, after the logits'
+ *     copy has been queued) and kernel_done is recorded right after it, so
+ *     that calls alternating between streams can overlap one call's copies
+ *     with another's kernel while the kernels themselves run one at a time.
+ *   - Calls that overlap in time (several streams) need their own dev and ws.
+ * Errors: those of moe_router_step, MOE_ERR_INVALID for a NULL host pointer,
+ * MOE_ERR_CUDA when a copy cannot be queued. */
+MOE_API size_t moe_router_step_host_device_size(moe_dtype dt, int64_t T, int32_t E, int32_t k, int32_t n_ranks);
+MOE_API moe_status moe_router_step_host(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                                        float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
+                                        float grad_scale,
+                                        int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                                        float* scalars, int32_t* rank_load,
+                                        int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                                        int32_t* n_dropped, float* dlogits,
+                                        void* dev, size_t dev_bytes, void* ws, size_t ws_bytes,
+                                        void* kernel_after, void* kernel_done, moe_stream_t stream);
+
 /* moe_router_step for callers that cannot allocate device memory.
  *
  * Not a step of the method: the source pages have no counterpart.  It exists

@@ -33,6 +33,10 @@ SIGNATURES = {
                                _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_router_step_static": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _i32, _i32, _f64, _f32,
                                       _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
+    "moe_router_step_host_device_size": (_sz, [_i32, _i64, _i32, _i32, _i32]),
+    "moe_router_step_host": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _i32, _i32, _f64, _f32,
+                                    _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p, _sz, _p, _p,
+                                    _p]),
     "moe_router_fwd_ex": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _i32, _i32, _p, _i32, _f32, _p,
                                  _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_router_bwd_full": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _p, _f32, _i32, _p, _p, _i32, _p, _p]),

@@ -29,6 +29,16 @@ def _stream_handle(stream: torch.cuda.Stream | None) -> int:
     return int(s.cuda_stream)
 
 
+def _event_handle(ev: torch.cuda.Event | None) -> int | None:
+    """The cudaEvent_t of a torch event (created on first record), or None."""
+    if ev is None:
+        return None
+    h = int(ev.cuda_event)
+    if h == 0:
+        raise ValueError("the event has not been recorded yet, so it has no CUDA handle")
+    return h
+
+
 def _ptr(t: torch.Tensor | None) -> int | None:
     return None if t is None else int(t.data_ptr())
 
@@ -269,6 +279,58 @@ def moe_router_step(logits: torch.Tensor, k: int, alpha: float, capacity_factor:
                                _ptr(o["n_dropped"]), _ptr(o["dlogits"]), wp, wn, _stream_handle(stream))
     check(st, "moe_router_step")
     o["capacity"] = moe_dispatch_capacity(T, E, k, capacity_factor)
+    return o
+
+
+def moe_router_step_host_device_size(dtype: torch.dtype, T: int, E: int, k: int, n_ranks: int = 0) -> int:
+    """Bytes of the device staging buffer moe_router_step_host needs (C: moe_router_step_host_device_size)."""
+    return int(lib().moe_router_step_host_device_size(_DTYPES[dtype], T, E, k, n_ranks))
+
+
+def host_step_outputs(T: int, E: int, k: int, n_ranks: int = 0, pin: bool = True) -> dict:
+    """Page-locked host arrays for every output of moe_router_step_host."""
+    i32, f32 = torch.int32, torch.float32
+    shapes = {"idx": ((T, k), i32), "gate": ((T, k), f32), "counts": ((E,), i32), "f": ((E,), f32),
+              "P": ((E,), f32), "scalars": ((_native.MOE_NUM_SCALARS,), f32), "rank_load": ((max(n_ranks, 0),), i32),
+              "perm": ((T * k,), i32), "slot": ((T * k,), i32), "offsets": ((E + 1,), i32), "kept": ((E,), i32),
+              "n_dropped": ((1,), i32), "dlogits": ((T, E), f32)}
+    return {name: torch.empty(shape, dtype=dt, pin_memory=pin) for name, (shape, dt) in shapes.items()}
+
+
+def moe_router_step_host(logits: torch.Tensor, k: int, alpha: float, capacity_factor: float, renorm: int = -1,
+                         n_ranks: int = 0, grad_scale: float = 1.0, ws: Workspace | None = None,
+                         dev: torch.Tensor | None = None, out: dict | None = None,
+                         stream: torch.cuda.Stream | None = None, device: torch.device | int | None = None,
+                         kernel_after: torch.cuda.Event | None = None,
+                         kernel_done: torch.cuda.Event | None = None) -> dict:
+    """The step on HOST logits with every output copied back to HOST arrays
+    (C: moe_router_step_host).  logits: a contiguous CPU tensor (pinned for
+    asynchronous copies); out: host arrays as from host_step_outputs; dev: the
+    device staging buffer (uint8, moe_router_step_host_device_size bytes);
+    kernel_after / kernel_done: events the step's kernel waits for / records.
+    Asynchronous on `stream`: synchronise before reading the outputs."""
+    if logits.device.type != "cpu" or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous CPU tensor")
+    if logits.dtype not in _DTYPES or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 or bfloat16 tensor")
+    T, E = logits.shape
+    d = torch.device("cuda", torch.cuda.current_device() if device is None else
+                     (device.index if isinstance(device, torch.device) else device))
+    o = out if out is not None else host_step_outputs(T, E, k, n_ranks)
+    need = moe_router_step_host_device_size(logits.dtype, T, E, k, n_ranks)
+    if dev is None:
+        dev = torch.empty(need, dtype=torch.uint8, device=d)
+    ws = ws or _default_ws(d, stream)
+    wp, wn = ws.ensure(T, E, k, stream)
+    st = lib().moe_router_step_host(_ptr(logits), _DTYPES[logits.dtype], T, E, k, float(alpha), int(renorm),
+                                    int(n_ranks), float(capacity_factor), float(grad_scale),
+                                    _ptr(o["idx"]), _ptr(o["gate"]), _ptr(o["counts"]), _ptr(o["f"]), _ptr(o["P"]),
+                                    _ptr(o["scalars"]), _ptr(o["rank_load"]) if n_ranks > 0 else None,
+                                    _ptr(o["perm"]), _ptr(o["slot"]), _ptr(o["offsets"]), _ptr(o["kept"]),
+                                    _ptr(o["n_dropped"]), _ptr(o["dlogits"]), _ptr(dev), int(dev.numel()),
+                                    wp, wn, _event_handle(kernel_after), _event_handle(kernel_done),
+                                    _stream_handle(stream))
+    check(st, "moe_router_step_host")
     return o
 
 

@@ -561,6 +561,107 @@ moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t 
   return launch_persistent(v->step, p, geo.smem, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Device staging layout of moe_router_step_host: the logits, then every
+// output of the step, each 256-byte aligned.
+struct HostStepLayout {
+  size_t logits, idx, gate, counts, f, P, scalars, rank_load, perm, slot, offsets, kept, n_dropped, dlogits, total;
+};
+
+HostStepLayout host_step_layout(moe_dtype dt, int64_t T, int32_t E, int32_t k, int32_t n_ranks) {
+  const size_t esize = dt == MOE_DTYPE_BF16 ? 2 : 4;
+  const size_t tk = size_t(T) * size_t(k), te = size_t(T) * size_t(E);
+  HostStepLayout L;
+  size_t at = 0;
+  auto take = [&at](size_t bytes) { const size_t o = at; at += align_up(bytes); return o; };
+  L.logits = take(te * esize);
+  L.idx = take(tk * 4);
+  L.gate = take(tk * 4);
+  L.counts = take(size_t(E) * 4);
+  L.f = take(size_t(E) * 4);
+  L.P = take(size_t(E) * 4);
+  L.scalars = take(size_t(moe::kNumScalars) * 4);
+  L.rank_load = take(size_t(n_ranks > 0 ? n_ranks : 0) * 4);
+  L.perm = take(tk * 4);
+  L.slot = take(tk * 4);
+  L.offsets = take(size_t(E + 1) * 4);
+  L.kept = take(size_t(E) * 4);
+  L.n_dropped = take(4);
+  L.dlogits = take(te * 4);
+  L.total = at;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_router_step_host_device_size(moe_dtype dt, int64_t T, int32_t E, int32_t k, int32_t n_ranks) {
+  if (T < 1 || E < 1 || k < 1 || n_ranks < 0) return 0;
+  return host_step_layout(dt, T, E, k, n_ranks).total;
+}
+
+moe_status moe_router_step_host(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                                float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
+                                float grad_scale,
+                                int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                                float* scalars, int32_t* rank_load,
+                                int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                                int32_t* n_dropped, float* dlogits,
+                                void* dev, size_t dev_bytes, void* ws, size_t ws_bytes,
+                                void* kernel_after, void* kernel_done, moe_stream_t stream) {
+  // The host pointers are only checked for NULL here; the device staging
+  // pointers handed to the step are checked by moe_router_step itself.
+  if (!logits || !idx || !gate || !counts || !f || !P || !scalars || (n_ranks > 0 && !rank_load) || !perm ||
+      !slot || !offsets || !kept || !n_dropped || !dlogits)
+    return fail(MOE_ERR_INVALID, "a host input or output is NULL");
+  if (dt != MOE_DTYPE_BF16 && dt != MOE_DTYPE_FP32) return fail(MOE_ERR_UNSUPPORTED, "dtype %d", int(dt));
+  if (T < 1 || E < 1 || k < 1 || n_ranks < 0) return fail(MOE_ERR_INVALID, "T, E, k must be >= 1 and n_ranks >= 0");
+  if (!dev || !aligned(dev, kAlign)) return fail(MOE_ERR_INVALID, "device staging buffer is NULL or not 256-byte aligned");
+  const HostStepLayout L = host_step_layout(dt, T, E, k, n_ranks);
+  if (dev_bytes < L.total)
+    return fail(MOE_ERR_WORKSPACE, "device staging buffer of %zu bytes, %zu needed", dev_bytes, L.total);
+  unsigned char* d = static_cast<unsigned char*>(dev);
+  const size_t esize = dt == MOE_DTYPE_BF16 ? 2 : 4;
+  const size_t tk = size_t(T) * size_t(k), te = size_t(T) * size_t(E);
+  cudaError_t e = cudaMemcpyAsync(d + L.logits, logits, te * esize, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (logits in)");
+  if (kernel_after) {
+    e = cudaStreamWaitEvent(stream, static_cast<cudaEvent_t>(kernel_after), 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+  }
+  moe_status s = moe_router_step(d + L.logits, dt, T, E, k, alpha, renorm, n_ranks, capacity_factor, grad_scale,
+                                 reinterpret_cast<int32_t*>(d + L.idx), reinterpret_cast<float*>(d + L.gate),
+                                 reinterpret_cast<int32_t*>(d + L.counts), reinterpret_cast<float*>(d + L.f),
+                                 reinterpret_cast<float*>(d + L.P), reinterpret_cast<float*>(d + L.scalars),
+                                 n_ranks > 0 ? reinterpret_cast<int32_t*>(d + L.rank_load) : nullptr,
+                                 reinterpret_cast<int32_t*>(d + L.perm), reinterpret_cast<int32_t*>(d + L.slot),
+                                 reinterpret_cast<int32_t*>(d + L.offsets), reinterpret_cast<int32_t*>(d + L.kept),
+                                 reinterpret_cast<int32_t*>(d + L.n_dropped), reinterpret_cast<float*>(d + L.dlogits),
+                                 ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (kernel_done) {
+    e = cudaEventRecord(static_cast<cudaEvent_t>(kernel_done), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  }
+  struct Back { void* dst; size_t off, bytes; };
+  const Back back[] = {
+      {idx, L.idx, tk * 4}, {gate, L.gate, tk * 4}, {counts, L.counts, size_t(E) * 4}, {f, L.f, size_t(E) * 4},
+      {P, L.P, size_t(E) * 4}, {scalars, L.scalars, size_t(moe::kNumScalars) * 4},
+      {rank_load, L.rank_load, size_t(n_ranks) * 4}, {perm, L.perm, tk * 4}, {slot, L.slot, tk * 4},
+      {offsets, L.offsets, size_t(E + 1) * 4}, {kept, L.kept, size_t(E) * 4}, {n_dropped, L.n_dropped, 4},
+      {dlogits, L.dlogits, te * 4}};
+  for (const Back& b : back) {
+    if (b.bytes == 0) continue;
+    e = cudaMemcpyAsync(b.dst, d + b.off, b.bytes, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (outputs back)");
+  }
+  return MOE_OK;
+}
+
 moe_status taot_sinkhorn_batched(const float* loads, int32_t B, int32_t R, int32_t ranks_per_node,
                                  float lambda, float eps, int32_t iters,
                                  float* u, float* v, float* plan, int32_t* status,

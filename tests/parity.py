@@ -9,6 +9,10 @@ Tolerances (fp32 arithmetic on the GPU against the fp64 oracle):
                           c * p_tj * (f_j - s_t) is a difference that cancels, so 1e-5
                           relative is taken against the magnitude of its two terms
   * Sinkhorn u, v, plan:  |x - o| <= 1e-4 * |o| + 1e-4 * max|o| per microbatch
+  * every floating comparison of the router outputs also admits an absolute
+    error of FLT_MIN = 2^-126: fp32 results below the smallest normal number
+    carry no relative precision, and the kernels' exponentials flush them to
+    zero (a row whose logits spread by more than about 87 gives such p)
 """
 
 from __future__ import annotations
@@ -21,6 +25,7 @@ import synth
 
 RTOL = 1e-5
 SK_RTOL = 1e-4
+FLT_MIN = 2.0 ** -126
 SCALARS = ("l_aux", "balance", "cv", "max_over_mean", "min_over_mean", "rank_cv", "rank_max_over_mean")
 
 
@@ -77,10 +82,10 @@ def oracle_forward(logits: np.ndarray, dtype: str, k: int, alpha: float, renorm:
 
 def check_forward(got: dict, want: dict, n_ranks: int) -> None:
     assert_equal("idx", got["idx"].cpu().numpy(), want["idx"])
-    assert_close("gate", got["gate"].cpu().numpy(), want["gate"], RTOL)
+    assert_close("gate", got["gate"].cpu().numpy(), want["gate"], RTOL, FLT_MIN)
     assert_equal("counts", got["counts"].cpu().numpy(), want["counts"])
     assert_close("f", got["f"].cpu().numpy(), want["f"], RTOL)
-    assert_close("P", got["P"].cpu().numpy(), want["P"], RTOL)
+    assert_close("P", got["P"].cpu().numpy(), want["P"], RTOL, FLT_MIN)
     sc = got["scalars"].cpu().numpy()
     for j, name in enumerate(SCALARS):
         assert_close(f"scalar {name}", sc[j], want[name], RTOL)
@@ -99,7 +104,7 @@ def check_backward(dlogits: torch.Tensor, logits: np.ndarray, dtype: str, f: np.
         p = oracle.router.softmax(oracle.router.widen(sl, dtype))
         s = (p * f[None, :]).sum(axis=1)
         scale = abs(c) * p * (np.abs(f)[None, :] + np.abs(s)[:, None])
-        assert_close(f"dlogits rows {r0}..", got[r0:r0 + chunk], want, RTOL, RTOL * scale)
+        assert_close(f"dlogits rows {r0}..", got[r0:r0 + chunk], want, RTOL, RTOL * scale + FLT_MIN)
 
 
 def check_dispatch(got: dict, idx: np.ndarray, E: int, C: int) -> None:

@@ -187,3 +187,29 @@ def test_combine_rejects_bad_arguments(native_lib):
     bad = list(args)
     bad[7] = 4                                        # rank loads requested without a buffer
     assert f(*bad) == 1
+
+
+def test_host_step_staging_size_and_argument_checks(native_lib):
+    # logits 256 x 64 bf16 (32 KiB); idx, gate, perm, slot 2 KiB each; counts, f, P, scalars, kept, n_dropped one
+    # 256-byte region each; offsets (65 ints) two; 64 KiB of dlogits: every region 256-byte aligned
+    T, E, k = 256, 64, 2
+    want = 32768 + 4 * 2048 + 6 * 256 + 512 + 65536
+    assert native_lib.moe_router_step_host_device_size(1, T, E, k, 0) == want
+    assert native_lib.moe_router_step_host_device_size(1, T, E, k, 8) == want + 256
+    assert native_lib.moe_router_step_host_device_size(0, T, E, k, 0) == want + 32768
+    assert native_lib.moe_router_step_host_device_size(1, 0, E, k, 0) == 0
+    host = [FAKE] * 13
+    args = [FAKE, 1, T, E, k, 0.01, -1, 0, 1.25, 1.0]
+    # a NULL host output
+    st = native_lib.moe_router_step_host(*args, *([None] + host[1:]), FAKE, want, FAKE, 1 << 20, None, None, None)
+    assert st == _native.MOE_ERR_INVALID
+    # a staging buffer one byte short
+    st = native_lib.moe_router_step_host(*args, *host, FAKE, want - 1, FAKE, 1 << 20, None, None, None)
+    assert st == _native.MOE_ERR_WORKSPACE
+    # a misaligned staging buffer
+    st = native_lib.moe_router_step_host(*args, *host, FAKE + 16, want, FAKE, 1 << 20, None, None, None)
+    assert st == _native.MOE_ERR_INVALID
+    # an unknown dtype
+    args_bad = [FAKE, 7, T, E, k, 0.01, -1, 0, 1.25, 1.0]
+    st = native_lib.moe_router_step_host(*args_bad, *host, FAKE, want, FAKE, 1 << 20, None, None, None)
+    assert st == _native.MOE_ERR_UNSUPPORTED

@@ -31,3 +31,26 @@ def test_traffic_table_parses_and_matches_its_hash():
     for f in lines:
         got = bench.measured_traffic(f[1])
         assert (got is not None) == (f[7] == cur)
+
+
+def test_replay_plan_times_exactly_k_steps():
+    # (steps per graph, replays, buffer sets): replays * steps per graph == K, >= 10 replays where K allows,
+    # and the buffer sets divide the steps per graph
+    assert bench.replay_plan(200, 2) == (20, 10, 2)
+    assert bench.replay_plan(200, 15) == (20, 10, 20)
+    assert bench.replay_plan(20, 2) == (2, 10, 2)
+    assert bench.replay_plan(200, 1184) == (200, 1, 1184)
+    assert bench.replay_plan(7, 2) == (7, 1, 2)
+    for K in (10, 12, 50, 97, 200, 256):
+        for n_min in (1, 2, 3, 15):
+            S, R, n = bench.replay_plan(K, n_min)
+            assert S * R == K and n >= n_min
+            assert R == 1 or S % n == 0
+
+
+def test_percentile_interpolates():
+    xs = [5.0, 1.0, 3.0, 2.0, 4.0]
+    assert bench.percentile(xs, 0.5) == 3.0
+    assert bench.percentile(xs, 0.0) == 1.0 and bench.percentile(xs, 1.0) == 5.0
+    assert abs(bench.percentile(xs, 0.1) - 1.4) < 1e-12
+    assert bench.percentile([2.5], 0.9) == 2.5

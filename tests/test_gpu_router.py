@@ -141,6 +141,49 @@ def test_edge_cases(mr, T, E, k, dtype, renorm, n_ranks, cf, levels):
     check_backward(st["dlogits"], logits, dtype, want["f"], 0.01, 0.5)
 
 
+SATURATED = [
+    # (T, E, k, dtype): staged bf16 at E = 64 and E = 384, fp32 at E = 64
+    (3001, 64, 2, "bf16"), (3007, 384, 6, "bf16"), (2001, 64, 2, "fp32"),
+]
+
+
+def _saturated_logits(T, E, dtype, seed):
+    """N(0, 1) logits where every third row has one logit raised to +100 (a
+    spread above 87, so that the other probabilities of the row fall below the
+    smallest normal fp32 number), every seventh row two such logits (a tie at
+    the top), and every eleventh row one at +88 (p near 2^-126)."""
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal((T, E)).astype(np.float32)
+    cols = rng.integers(0, E, size=T)
+    z[0::3][np.arange(len(z[0::3])), cols[0::3]] = 100.0
+    r7 = np.arange(0, T, 7)
+    z[r7, cols[r7]] = 100.0
+    z[r7, (cols[r7] + 5) % E] = 100.0
+    r11 = np.arange(5, T, 11)
+    z[r11, cols[r11]] = 88.0
+    return synth.f32_to_bf16_bits(z) if dtype == "bf16" else z
+
+
+@pytest.mark.parametrize("T,E,k,dtype", SATURATED)
+def test_saturated_rows(mr, T, E, k, dtype):
+    """Rows whose logits spread by more than about 87: the kernels flush p
+    below 2^-126 to zero, the oracle keeps it in fp64; everything else must
+    match as usual (the parity rules admit FLT_MIN of absolute error)."""
+    logits = _saturated_logits(T, E, dtype, seed=T + E)
+    x = to_device(logits, dtype)
+    st = mr.moe_router_step(x, k, 0.01, 1.25, n_ranks=8, grad_scale=1.0)
+    fw = mr.moe_router_fwd(x, k, 0.01, n_ranks=8)
+    torch.cuda.synchronize()
+    want = oracle_forward(logits, dtype, k, 0.01, None, 8)
+    check_forward(st, want, 8)
+    check_forward(fw, want, 8)
+    check_dispatch(st, want["idx"], E, oracle.dispatch.capacity(T, k, E, 1.25))
+    check_backward(st["dlogits"], logits, dtype, want["f"], 0.01, 1.0)
+    dl = mr.moe_router_bwd(x, st["f"], 0.01, 1.0)
+    torch.cuda.synchronize()
+    assert torch.equal(dl, st["dlogits"])
+
+
 def test_misaligned_views_take_the_scalar_path(mr):
     T, E, k = 1500, 64, 2
     base = synth.random_logits(T + 1, E, "bf16", seed=3)
