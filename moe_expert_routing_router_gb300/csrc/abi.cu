@@ -57,22 +57,28 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Workspace: [Ctrl][group_hist][tile_hist E x kGridMax][P_part E x kGridMax][counts E].
+// Workspace: [Ctrl][group_hist][pfix][tile_hist E x kGridMax][P_part E x kGridMax][counts E].
 // The group sums must be zero when a launch starts, so they have a region of
 // their own at a fixed place and of a fixed size, whatever E: calls with
 // different E on one workspace never write into it with anything but sums
 // that their own CTA 0 clears again.
 struct WsLayout {
-  size_t ctrl = 0, group_hist = 0, tile_hist = 0, p_part = 0, counts = 0, total = 0;
+  size_t ctrl = 0, group_hist = 0, pfix = 0, tile_hist = 0, p_part = 0, counts = 0, total = 0;
 };
 
 constexpr size_t kGroupHistBytes = size_t(moe::kGroupMax) * MOE_MAX_EXPERTS * sizeof(int32_t);
+// A split fused step's sums of p in fixed point: two 64-bit integers per
+// expert, zero between launches like the group sums (so both sit before
+// tile_hist, in the part moe_get_device_status clears after a failure).
+constexpr size_t kPfixBytes = size_t(2) * moe::kMaxExperts * sizeof(unsigned long long);
+static_assert(moe::kMaxExperts == MOE_MAX_EXPERTS, "expert limit");
 
 WsLayout ws_layout(int E) {
   WsLayout w;
   w.ctrl = 0;
   w.group_hist = align_up(sizeof(moe::Ctrl));
-  w.tile_hist = w.group_hist + align_up(kGroupHistBytes);
+  w.pfix = w.group_hist + align_up(kGroupHistBytes);
+  w.tile_hist = w.pfix + align_up(kPfixBytes);
   w.p_part = w.tile_hist + align_up(size_t(E) * kGridMax * sizeof(int32_t));
   w.counts = w.p_part + align_up(size_t(E) * kGridMax * sizeof(float));
   w.total = w.counts + align_up(size_t(E) * sizeof(int32_t));
@@ -198,6 +204,7 @@ void bind_ws(RouterParams& p, void* ws, int E) {
   p.ctrl = reinterpret_cast<moe::Ctrl*>(base + w.ctrl);
   p.tile_hist = reinterpret_cast<int32_t*>(base + w.tile_hist);
   p.group_hist = reinterpret_cast<int32_t*>(base + w.group_hist);
+  p.pfix = reinterpret_cast<unsigned long long*>(base + w.pfix);
   p.P_part = reinterpret_cast<float*>(base + w.p_part);
   p.counts_ws = reinterpret_cast<int32_t*>(base + w.counts);
   p.G_stride = kGridMax;
@@ -252,6 +259,11 @@ moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, 
   int bf = 0, bs = 0;
   if ((s = occupancy(v->fwd, moe::kThreads, smem, dev, &bf)) != MOE_OK) return s;
   if ((s = occupancy(v->step, moe::kThreads, smem, dev, &bs)) != MOE_OK) return s;
+  if (v->step_split != nullptr) {
+    int bss = 0;
+    if ((s = occupancy(v->step_split, moe::kThreads, smem, dev, &bss)) != MOE_OK) return s;
+    bs = std::min(bs, bss);
+  }
   const int64_t cap = std::min<int64_t>(int64_t(std::min(bf, bs)) * d.sms, kGridMax);
   const int64_t want = (T + group_rows - 1) / group_rows;
   g.G = int(std::max<int64_t>(1, std::min(cap, want)));
@@ -558,7 +570,12 @@ moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t 
   p.n_slots = geo.n_slots;
   p.asg_cap = geo.asg_cap;
   p.rstat_cap = geo.rstat_cap;
-  return launch_persistent(v->step, p, geo.smem, stream);
+  // With renormalised gates the split kernel forms the softmax sums and P in
+  // the backward; it keeps its per-warp sums of p in the ring's memory at the end.
+  const size_t ring_bytes = size_t(geo.n_slots) * size_t(geo.rows_per_stage) * size_t(E) * (dt == MOE_DTYPE_BF16 ? 2 : 4);
+  const bool split = p.renorm != 0 && v->step_split != nullptr &&
+                     ring_bytes >= size_t(moe::kConsumerWarps) * size_t(E) * sizeof(float);
+  return launch_persistent(split ? v->step_split : v->step, p, geo.smem, stream);
 }
 
 }  // extern "C"
@@ -940,7 +957,7 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = (size_t(4) << 20) + (size_t(768) << 10);   // 4.75 MiB
 constexpr int kStaticMaxExperts = 512;      // ws_layout(512).total fits in kStaticScratchBytes
-static_assert(kStaticScratchBytes >= 4096 + kGroupHistBytes + size_t(kStaticMaxExperts) * 4 * (2 * 1024 + 1),
+static_assert(kStaticScratchBytes >= 4096 + kGroupHistBytes + kPfixBytes + size_t(kStaticMaxExperts) * 4 * (2 * 1024 + 1),
               "scratch size");
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];

@@ -113,14 +113,14 @@ struct ExtRow {
   static constexpr int EPL = VW * NV;
   using Raw = typename DT::Raw;
 
-  // Softmax statistics of the unbiased row: e[i] = 2^(z_i log2e - mL), inv_s = 1 / sum e.
-  static __device__ __forceinline__ void softmax(const Raw (&raw)[EPL], bool valid, float (&e)[EPL], float& mL,
+  // Softmax statistics of the unbiased row: e[i] = 2^((z_i - mx) log2e), inv_s = 1 / sum e.
+  static __device__ __forceinline__ void softmax(const Raw (&raw)[EPL], bool valid, float (&e)[EPL], float& mx,
                                                  float& inv_s) {
     float m = -3.402823466e38f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) m = fmaxf(m, __uint_as_float(DT::bits(raw[i])));
-    mL = group_max<LPR>(m) * kLog2e;
-    row_exp<DT, LPR, EPL>(raw, mL, e);
+    mx = group_max<LPR>(m);
+    row_exp<DT, LPR, EPL>(raw, mx, e);
     const float s = group_sum<LPR>(tree_sum(e));
     inv_s = valid ? rcp_approx(s) : 0.f;
   }
@@ -431,8 +431,8 @@ __global__ void __launch_bounds__(kExtFwdThreads, 2) router_fwd_ex_kernel(const 
       const bool ok = rg + nw < n_rg && tn < p.T;
       load_lane<DT, LPR, VW, NV, true>(X + (ok ? tn : 0) * (long long)p.E, p.E, l, ok, nxt);
     }
-    float e[EPL], mL, inv_s;
-    Row::softmax(raw, valid, e, mL, inv_s);
+    float e[EPL], mx, inv_s;
+    Row::softmax(raw, valid, e, mx, inv_s);
     // The cached selection pays at 12 or more elements per lane (E = 384: 310 -> 276 us); with
     // fewer, its refills cost more than the passes they save (E = 64: 22 -> 24 us, E = 256: 137 -> 148 us).
     int my_col;
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kExtFwdThreads, 2) router_fwd_ex_kernel(const 
     Raw zr[1] = {DT::kNegInf};
     if (owner) zr[0] = X[t * (long long)p.E + my_col];
     float my_e[1];
-    row_exp<DT, LPR, 1>(zr, mL, my_e);
+    row_exp<DT, LPR, 1>(zr, mx, my_e);
     const float pick_sum = owners_sum<LPR>(my_e[0]);
     if (owner) {
       const long long a = t * p.k + l;
@@ -582,9 +582,9 @@ __global__ void __launch_bounds__(kExtBwdThreads, (VW * NV <= 8 ? 5 : (VW * NV <
     float m = -3.402823466e38f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) m = fmaxf(m, __uint_as_float(DT::bits(raw[i])));
-    const float mL = group_max<LPR>(m) * kLog2e;
+    const float mx = group_max<LPR>(m);
     float e[EPL];
-    row_exp<DT, LPR, EPL>(raw, mL, e);
+    row_exp<DT, LPR, EPL>(raw, mx, e);
     const float s = group_sum<LPR>(tree_sum(e));
     const float inv_s = rcp_approx(s);
     // The gradient term of the lane's own pick: the masked aux term and G.
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(kExtBwdThreads, (VW * NV <= 8 ? 5 : (VW * NV <
         Raw zr[1] = {DT::kNegInf};
         if (in_range) zr[0] = row[my_idx];
         float my_e[1];
-        row_exp<DT, LPR, 1>(zr, mL, my_e);
+        row_exp<DT, LPR, 1>(zr, mx, my_e);
         float Se = 0.f, acc = 0.f;
         for (int j = 0; j < p.k; ++j) {
           const float ej = __shfl_sync(0xffffffffu, my_e[0], g * LPR + j);

@@ -4,11 +4,23 @@
 #include "router_kernels.cuh"
 #include "router_table.h"
 
+namespace moe {
+// The split step kernel of a variant, where it has one.
+template <class DT, int LPR, int VW, int NV, int NR, bool STAGED, int MINB>
+constexpr const void* split_step_kernel() {
+  if constexpr (STAGED && kFastTopk<DT, LPR, VW, NV>)
+    return reinterpret_cast<const void*>(&router_persistent_kernel<DT, LPR, VW, NV, NR, kModeStepSplit, STAGED, MINB>);
+  else
+    return nullptr;
+}
+}  // namespace moe
+
 #define MOE_ROUTER_VARIANT(DT, LPR, VW, NV, NR, STAGED, MINB)                                                       \
   {LPR, VW, NV, NR, STAGED, MINB,                                                                                    \
    reinterpret_cast<const void*>(&::moe::router_persistent_kernel<DT, LPR, VW, NV, NR, ::moe::kModeFwd, STAGED, MINB>), \
    reinterpret_cast<const void*>(&::moe::router_persistent_kernel<DT, LPR, VW, NV, NR, ::moe::kModeStep, STAGED, MINB>), \
-   reinterpret_cast<const void*>(&::moe::router_bwd_kernel<DT, LPR, VW, NV>)}
+   reinterpret_cast<const void*>(&::moe::router_bwd_kernel<DT, LPR, VW, NV>),                                        \
+   ::moe::split_step_kernel<DT, LPR, VW, NV, NR, STAGED, MINB>()}
 
 #define MOE_VARIANT_TABLE(NAME, ARRAY)                       \
   const RouterVariant* NAME(int* n) {                        \

@@ -56,6 +56,14 @@ constexpr int kRedPhase = 96;    // 1 once the grid barrier has passed, 2 once t
 constexpr int kRedRanked = 97;   // 1 once the dispatch warp has ranked every pick of the CTA, -1 if it gave up
 constexpr int kRedFixNext = 98;  // next chunk of the CTA's final dispatch positions to write
 constexpr int kRedFlag = 127;    // grid barrier result
+// The candidate set of the fast top-k path (see fwd_groups_fast): 64 columns
+// in the 128-int scratch (two per lane, 16 bits each in 32 ints), their
+// membership bitmap (E <= 1024 bits) and a flag set once both are written.
+constexpr int kRedCand = 0;
+constexpr int kRedCandBits = 32;
+constexpr int kRedCandReady = 99;
+constexpr int kRedBwdLast = 100;  // a split step: 1 in the CTA that added its sums of p last
+constexpr int kRedCandDone = 101; // consumer warps that have added their columns of the first stage
 static_assert(kConsumerWarps <= 32, "progress slots");
 constexpr int kBarMain = 2;       // named barrier of the main group
 constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
@@ -69,12 +77,18 @@ constexpr int kGridMax = 1024;   // CTAs of a persistent launch at most (the per
 constexpr int kGroupCtas = 8;    // CTAs per group of the per-group count sums
 constexpr int kGroupMax = kGridMax / kGroupCtas;
 constexpr int kMaxSlots = 16;
+constexpr int kMaxExperts = 1024;
 constexpr int kNumScalars = 7;
 // Limit of the wait for this CTA's own bulk copies before it exits; it does not
 // follow RouterParams::timeout_ns, which tests shorten.
 constexpr unsigned long long kDrainNs = 1000000000ull;
 
-enum : int { kModeFwd = 1, kModeDispatch = 2, kModeBwd = 4, kModeStep = kModeFwd | kModeDispatch | kModeBwd };
+// kModeSplit (with kModeStep, renormalised gates): the forward takes only the
+// top-k and the gates; the backward forms each row's softmax sum and P.
+enum : int {
+  kModeFwd = 1, kModeDispatch = 2, kModeBwd = 4, kModeSplit = 8,
+  kModeStep = kModeFwd | kModeDispatch | kModeBwd, kModeStepSplit = kModeStep | kModeSplit
+};
 
 struct RouterParams {
   const void* logits;          // [T, E] fp32 or bf16
@@ -105,6 +119,7 @@ struct RouterParams {
   int32_t* tile_hist;          // [E][G_stride]: per-CTA counts
   int32_t* group_hist;         // [n_groups][E]: per-group counts (atomics; zero between launches)
   float* P_part;               // [E][G_stride]: per-CTA sums of p
+  unsigned long long* pfix;    // [2][kMaxExperts]: a split step's sums of p in fixed point (zero between launches)
   int32_t* counts_ws;          // [E] counts when `counts` is not an output
   int G;                       // CTAs in the grid
   int n_groups;                // ceil(G / kGroupCtas)
@@ -178,7 +193,7 @@ __host__ __device__ inline unsigned align_to(unsigned x, unsigned a) { return (x
 
 // asg_cap: capacity of the two uint16 arrays (expert id and in-CTA rank of each
 // of the CTA's assignments) that keep the dispatch in shared memory.
-// rstat_cap: rows of (max * log2e, 1 / sum) kept from the forward for the backward.
+// rstat_cap: rows of (max, 1 / sum) kept from the forward for the backward.
 // key_bytes: size of a top-k key (4 for bf16 logits, 8 for fp32).
 __host__ __device__ inline SmemLayout router_smem_layout(int E, int key_bytes, int n_slots, int stage_bytes,
                                                          int asg_cap = 0, int rstat_cap = 0) {
@@ -367,18 +382,40 @@ __device__ __forceinline__ void lane_top2(const typename DT::Raw (&raw)[VW * NV]
   }
 }
 
+// Sum of x[0..N) in a fixed order: the pairs (x[2i], x[2i+1]) are added as
+// packed fp32 pairs in a tree, then the pair's two halves, then the odd last
+// element.
 template <int N>
 __device__ __forceinline__ float tree_sum(const float (&x)[N]) {
-  float t[N];
+  if constexpr (N == 1) {
+    return x[0];
+  } else {
+    constexpr int P = N / 2;
+    float2 t[P];
 #pragma unroll
-  for (int i = 0; i < N; ++i) t[i] = x[i];
+    for (int i = 0; i < P; ++i) t[i] = make_float2(x[2 * i], x[2 * i + 1]);
 #pragma unroll
-  for (int n = N; n > 1; n = (n + 1) / 2) {
+    for (int n = P; n > 1; n = (n + 1) / 2) {
 #pragma unroll
-    for (int i = 0; i < n / 2; ++i) t[i] = t[2 * i] + t[2 * i + 1];
-    if (n & 1) t[n / 2] = t[n - 1];
+      for (int i = 0; i < n / 2; ++i) t[i] = add2(t[2 * i], t[2 * i + 1]);
+      if (n & 1) t[n / 2] = t[n - 1];
+    }
+    float r = t[0].x + t[0].y;
+    if constexpr (N & 1) r += x[N - 1];
+    return r;
   }
-  return t[0];
+}
+
+// acc[i] += a[i] * b, two lanes at a time.
+template <int N>
+__device__ __forceinline__ void axpy2(float (&acc)[N], const float (&a)[N], float b) {
+#pragma unroll
+  for (int i = 0; i + 1 < N; i += 2) {
+    const float2 r = fma2(make_float2(a[i], a[i + 1]), make_float2(b, b), make_float2(acc[i], acc[i + 1]));
+    acc[i] = r.x;
+    acc[i + 1] = r.y;
+  }
+  if constexpr (N & 1) acc[N - 1] = fmaf(a[N - 1], b, acc[N - 1]);
 }
 
 // Sum over the first min(LPR, 8) lanes of each row group (the owners of the k
@@ -390,21 +427,261 @@ __device__ __forceinline__ float owners_sum(float x) {
   return x;
 }
 
-// Softmax statistics of one row from lane l's share: e[i] = 2^(x log2e - mL)
-// and the row sum s of e (a fixed tree per lane, then across the group).  The
-// forward and both backward paths use this one definition, so a row's p is the
-// same bits wherever it is recomputed.
+// Softmax numerators of lane l's share of a row against the row max m:
+// e[i] = 2^(z_i * log2 e - mL) with mL = m * log2 e rounded once (one FFMA per
+// element, ex2.approx, flush to zero).  The forward, both backward paths and
+// the extension kernels use this one definition (and elem_exp for a single
+// logit in fp32), so a row's p is the same bits wherever it is recomputed.
 template <class DT, int LPR, int EPL>
-__device__ __forceinline__ void row_exp(const typename DT::Raw (&raw)[EPL], float mL, float (&e)[EPL]) {
+__device__ __forceinline__ void row_exp(const typename DT::Raw (&raw)[EPL], float m, float (&e)[EPL]) {
+  const float mL = m * kLog2e;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) e[i] = ex2_approx(fmaf(__uint_as_float(DT::bits(raw[i])), kLog2e, -mL));
 }
+
+// The numerator of one logit already in fp32, by the formula of row_exp.
+__device__ __forceinline__ float elem_exp(float z, float m) { return ex2_approx(fmaf(z, kLog2e, -(m * kLog2e))); }
 
 // d = a * b + c, clamped to [0, 1].
 __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   float d;
   asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// ---------------------------------------------------------------------------
+// Fast top-k path for rows of 256 or more bf16 logits (32 lanes per row).
+//
+// Routing is skewed: most picks fall on a few experts.  Each CTA takes as
+// candidates the 64 experts whose logits summed over the rows of its first
+// ring stage are largest (an estimate of each expert's mean logit, which sets
+// how often it lands in a row's top-k; choose_candidates).  For each later row
+// every lane builds the keys of its two candidates' logits, k warp-wide rounds
+// give the exact top-k among the 64, and a packed bf16 max over every other
+// element of the row checks that none of them reaches the k-th pick's value.
+// If one does (or ties it), the row is redone by the full path (lane_top2 and
+// its rounds), so the result is exact for any input; the candidate set only
+// decides how often the short path is enough.  A warp whose rows fail the
+// check often stops trying.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// The halves of w outside `keep` (0 there) replaced by -inf: (w & keep) | (~keep & -inf).
+__device__ __forceinline__ uint32_t bf16x2_keep(uint32_t w, uint32_t keep) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xE2;" : "=r"(d) : "r"(w), "r"(keep), "r"(0xff80ff80u));
+  return d;
+}
+
+// Order-preserving key of the bf16 value with fp32 bit pattern b (low half 0)
+// in the column whose complement (0xffff - column) is inv: the key layout of
+// Bf16::key_from_bits, for a column held in one register.
+__device__ __forceinline__ uint32_t bf16_key_for(uint32_t b, uint32_t inv) {
+  uint32_t s, k;
+  asm("prmt.b32 %0, %1, %2, 0xBB54;" : "=r"(s) : "r"(b), "r"(inv));
+  asm("lop3.b32 %0, %1, %2, %3, 0x16;" : "=r"(k) : "r"(b), "r"(s), "r"(0x80000000u));
+  return k;
+}
+
+// Variants whose forward takes the fast path: bf16, 32 lanes per row, an even
+// number of at most 16 elements per lane (E from 129 to 512).
+template <class DT, int LPR, int VW, int NV>
+constexpr bool kFastTopk = LPR == 32 && sizeof(typename DT::Raw) == 2 && VW % 2 == 0 && VW * NV <= 16;
+
+// A consumer warp's share of the candidate set: one candidate per lane.
+template <int NW>
+struct FastTopk {
+  int state;           // 0: candidates not chosen yet, 1: in use, 2: given up (warp-uniform)
+  int tries, fails;    // rows tried and rows the check sent to the full path, since the last review
+  uint32_t col0, col1; // this lane's two candidate columns
+  uint32_t inv0, inv1; // 0xffff - col
+  uint32_t keep[NW];   // per word of the lane's elements: 0xffff in each half whose column is not a candidate
+};
+
+// Adds column c of the rows [0, n) of a ring stage (bf16) into score[c]: the
+// consumer warps split the columns between them, one per lane.
+__device__ __forceinline__ void stage_column_sums(const uint16_t* st, int n, int E, int warp, float* score) {
+  const int per = (E + kConsumerWarps - 1) / kConsumerWarps;    // <= 32 for E <= 576
+  const int c = warp * per + (threadIdx.x & 31);
+  if ((threadIdx.x & 31) < per && c < E) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int r = 0;
+    for (; r + 4 <= n; r += 4)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] += __uint_as_float(uint32_t(st[(r + j) * E + c]) << 16);
+    for (; r < n; ++r) acc[0] += __uint_as_float(uint32_t(st[r * E + c]) << 16);
+    score[c] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  }
+}
+
+// Chooses the candidate set: the 64 columns with the largest scores (the
+// columns' sums of the first stage's logits), by the upper 16 bits of their
+// order-preserving images: those above the largest threshold th that at least
+// 64 columns reach, then those at th in increasing column order.  Writes them
+// as 16-bit pairs (lane l's two candidates in int l of the scratch), their
+// membership bitmap, then the flag.  One warp; 64 < E <= 1024.
+__device__ __forceinline__ void choose_candidates(const float* score, int E, int* s_red) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  constexpr int kCand = 2 * kWarp;
+  auto key_of = [&](int e) -> uint32_t {
+    const uint32_t b = __float_as_uint(score[e]);
+    return ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) >> 16;
+  };
+  int lo_t = 0, hi_t = 0xffff;                   // #{key >= lo_t} >= 64 holds at lo_t = 0
+  while (lo_t < hi_t) {
+    const int mid = (lo_t + hi_t + 1) >> 1;
+    int n = 0;
+    for (int e = lane; e < E; e += kWarp) n += int(key_of(e)) >= mid ? 1 : 0;
+    n = __reduce_add_sync(0xffffffffu, n);
+    if (n >= kCand) lo_t = mid;
+    else hi_t = mid - 1;
+  }
+  uint16_t* cand = reinterpret_cast<uint16_t*>(s_red + kRedCand);
+  unsigned* bits = reinterpret_cast<unsigned*>(s_red + kRedCandBits);
+  int base = 0;
+  for (int pass = 0; pass < 2; ++pass) {         // above the threshold, then at it
+    for (int e0 = 0; e0 < E && base < kCand; e0 += kWarp) {
+      const int e = e0 + lane;
+      const bool sel = e < E && (pass == 0 ? int(key_of(e)) > lo_t : int(key_of(e)) == lo_t);
+      const unsigned b = __ballot_sync(0xffffffffu, sel);
+      const int pos = base + __popc(b & lt);
+      if (sel && pos < kCand) cand[pos] = uint16_t(e);
+      base += __popc(b);
+    }
+  }
+  bits[lane] = 0u;
+  __syncwarp();
+  for (int j = 0; j < 2; ++j) {
+    const int c = cand[2 * lane + j];
+    atomicOr(&bits[c >> 5], 1u << (c & 31));
+  }
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(s_red + kRedCandReady) = 1;
+  }
+}
+
+// Loads the candidate set into a consumer warp's FastTopk (after the flag).
+template <int LPR, int VW, int NV>
+__device__ __forceinline__ void fast_setup(FastTopk<VW * NV / 2>& fs, const int* s_red, int E, int l) {
+  const unsigned* bits = reinterpret_cast<const unsigned*>(s_red + kRedCandBits);
+  const uint16_t* cand = reinterpret_cast<const uint16_t*>(s_red + kRedCand);
+  fs.col0 = cand[2 * (threadIdx.x & 31)];
+  fs.col1 = cand[2 * (threadIdx.x & 31) + 1];
+  fs.inv0 = 0xffffu - fs.col0;
+  fs.inv1 = 0xffffu - fs.col1;
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < VW; i += 2) {
+      const int c = col_of<LPR, VW>(v, l, i);
+      const bool in0 = c < E && ((bits[c >> 5] >> (c & 31)) & 1u);
+      const bool in1 = c + 1 < E && ((bits[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u);
+      fs.keep[(v * VW + i) / 2] = (in0 ? 0u : 0x0000ffffu) | (in1 ? 0u : 0xffff0000u);
+    }
+  fs.state = 1;
+  fs.tries = 0;
+  fs.fails = 0;
+}
+
+// Lane l's EPL bf16 elements of one row (from a ring stage) as 32-bit words
+// of two, columns past E as -inf, an invalid row as zeros.
+template <int LPR, int VW, int NV>
+__device__ __forceinline__ void load_lane_words(const uint16_t* row, int E, int l, bool valid,
+                                                uint32_t (&wd)[VW * NV / 2]) {
+  static_assert(VW == 2 || VW == 4 || VW == 8, "vector width");
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int c0 = col_of<LPR, VW>(v, l, 0);
+    if (valid && c0 < E) {
+      if constexpr (VW == 2) {
+        wd[v] = *reinterpret_cast<const uint32_t*>(row + c0);
+      } else if constexpr (VW == 4) {
+        const uint2 q = *reinterpret_cast<const uint2*>(row + c0);
+        wd[2 * v] = q.x;
+        wd[2 * v + 1] = q.y;
+      } else {
+        const uint4 q = *reinterpret_cast<const uint4*>(row + c0);
+        wd[4 * v] = q.x;
+        wd[4 * v + 1] = q.y;
+        wd[4 * v + 2] = q.z;
+        wd[4 * v + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < VW / 2; ++h) wd[v * VW / 2 + h] = valid ? 0xff80ff80u : 0u;
+    }
+  }
+}
+
+// The top key and lane l's pick (l < k) of one row.
+template <class Key>
+struct TopPick {
+  Key top, mine;
+};
+
+// The full top-k of one row from a ring stage (32 lanes per row), out of
+// line: lane_top2 and k rounds, then the exactness check of fwd_groups (a
+// lane that spent both cached keys before the last round is counted exactly,
+// and a row with a hidden key or a zero among its picks goes to exact_topk).
+// It serves the rows of the fast path's first stage, the rows its check
+// rejects and the warps that stopped trying it; kept out of line so that the
+// fast path compiles lean.  Writes the picks to s_pick_row[0..k).
+template <class DT, int VW, int NV>
+__device__ __noinline__ TopPick<typename DT::Key> full_topk_row(const typename DT::Raw* row, int E, int k, int l,
+                                                                 bool valid, typename DT::Key* s_pick_row) {
+  using Key = typename DT::Key;
+  constexpr int LPR = kWarp;
+  constexpr int EPL = VW * NV;
+  typename DT::Raw raw[EPL];
+  load_lane<DT, LPR, VW, NV, false>(row, E, l, valid, raw);
+  Key m1, m2;
+  lane_top2<DT, LPR, VW, NV>(raw, l, m1, m2);
+  const Key second = m2;
+  __syncwarp();
+  Key w = group_max_key<LPR>(m1);
+  TopPick<Key> r;
+  r.top = w;
+  for (int j = 0;;) {
+    s_pick_row[j] = w;
+    const bool won = m1 == w;
+    m1 = won ? m2 : m1;
+    m2 = won ? DT::kKeyMin : m2;
+    if (++j >= k) break;
+    w = group_max_key<LPR>(m1);
+  }
+  __syncwarp();
+  r.mine = l < k ? s_pick_row[l] : DT::kKeyMin;
+  const bool early = EPL > 1 && m1 == DT::kKeyMin && second != w;
+  bool redo = DT::kSplitsZero && __any_sync(0xffffffffu, valid && l < k && DT::is_zero(r.mine));
+  if (!redo && __any_sync(0xffffffffu, early)) {
+    int above = 0;
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int i = 0; i < VW; ++i)
+        above += DT::key_from_bits(DT::bits(raw[v * VW + i]), col_lane_bits<LPR, VW>(l), col_elem_bits<LPR, VW>(v, i)) > w
+                     ? 1 : 0;
+    redo = __any_sync(0xffffffffu, early && above > 2);
+  }
+  if (redo) exact_topk<DT, LPR, VW, NV, false>(row, E, k, l, valid, &r.top, &r.mine);
+  return r;
+}
+
+// exact_topk of one row from a ring stage, out of line (a row of the fast
+// path with a zero among its picks).
+template <class DT, int VW, int NV>
+__device__ __noinline__ TopPick<typename DT::Key> exact_topk_row(const typename DT::Raw* row, int E, int k, int l,
+                                                                  bool valid) {
+  TopPick<typename DT::Key> r;
+  exact_topk<DT, kWarp, VW, NV, false>(row, E, k, l, valid, &r.top, &r.mine);
+  return r;
 }
 
 // Shared-memory slots for one warp's picks: NR rows x (32 / LPR) groups x kMaxK.
@@ -415,7 +692,7 @@ constexpr int kPickSlotsPerWarp = 64;
 // gates; idx/gate stores, pick counts into s_hist, p into pacc.  s_pick is the
 // warp's kPickSlotsPerWarp slots.  With s_aidx the expert ids also go to this
 // CTA's shared-memory dispatch buffer (index a - a_base); with s_rstat each
-// row's (max * log2e, 1 / sum) goes to s_rstat[t - r_base] for the backward.
+// row's (max, 1 / sum) goes to s_rstat[t - r_base] for the backward.
 template <class DT, int LPR, int VW, int NV, int NR, bool GLOBAL>
 __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename DT::Raw* const (&row)[NR],
                                            const long long (&t)[NR], const bool (&valid)[NR], int l, int* s_hist,
@@ -431,7 +708,7 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
 
   Raw raw[NR][EPL];
   Key m1[NR], m2[NR], second[NR], top[NR], mine[NR], w[NR];
-  float mL[NR];
+  float mx[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     load_lane<DT, LPR, VW, NV, GLOBAL>(row[r], p.E, l, valid[r], raw[r]);
@@ -451,8 +728,8 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
     const bool won = m1[r] == w[r];
     m1[r] = won ? m2[r] : m1[r];
     m2[r] = won ? DT::kKeyMin : m2[r];
-    mL[r] = DT::key_value(top[r]) * kLog2e;
-    row_exp<DT, LPR, EPL>(raw[r], mL[r], e[r]);
+    mx[r] = DT::key_value(top[r]);
+    row_exp<DT, LPR, EPL>(raw[r], mx[r], e[r]);
   }
   {
     // Rounds 1 .. k - 1 in order: the switch enters the run of rounds k - 1
@@ -507,7 +784,7 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
     for (int r = 0; r < NR; ++r) {
       bool redo = DT::kSplitsZero && __any_sync(0xffffffffu, valid[r] && l < k && DT::is_zero(mine[r]));
       if (!redo && __any_sync(0xffffffffu, early[r])) {
-        const float ew = ex2_approx(fmaf(DT::key_value(w[r]), kLog2e, -mL[r]));
+        const float ew = elem_exp(DT::key_value(w[r]), mx[r]);
         float est = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) est += fma_sat(e[r][i] - ew, 0x1p100f, 1.f);
@@ -530,10 +807,9 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
   for (int r = 0; r < NR; ++r) {
     const float s = group_sum<LPR>(tree_sum(e[r]));
     const float inv_s = valid[r] ? rcp_approx(s) : 0.f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) pacc[i] = fmaf(e[r][i], inv_s, pacc[i]);
+    axpy2(pacc, e[r], inv_s);
     const bool owner = l < k;
-    const float ej = owner ? ex2_approx(fmaf(DT::key_value(mine[r]), kLog2e, -mL[r])) : 0.f;
+    const float ej = owner ? elem_exp(DT::key_value(mine[r]), mx[r]) : 0.f;
     const float denom = p.renorm ? owners_sum<LPR>(ej) : s;
     if (valid[r] && owner) {
       const int col = DT::key_col(mine[r]);
@@ -543,7 +819,233 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
       atomicAdd(&s_hist[col], 1);
       if (s_aidx != nullptr) s_aidx[a - a_base] = uint16_t(col);
     }
-    if (s_rstat != nullptr && valid[r] && l == 0) s_rstat[t[r] - r_base] = make_float2(mL[r], inv_s);
+    if (s_rstat != nullptr && valid[r] && l == 0) s_rstat[t[r] - r_base] = make_float2(mx[r], inv_s);
+  }
+}
+
+// The forward of the large-E bf16 variants (32 lanes per row, rows in a ring
+// stage), in three parts: fast_topk_rows (the candidate path for K picks),
+// full_topk_row (the full path, out of line) and row_tail (gates, idx and
+// gate stores, pick counts, dispatch ids, row statistics).  A stage's rows
+// take the candidate path one after the other and the ones it rejects are
+// redone by the full path after the loop, so the per-row code has no rare
+// branch in it.  SOFTMAX: the forward also forms the row's softmax (p into
+// pacc, (max, 1 / sum) into s_rstat); without it (the fused step with
+// renormalised gates, whose backward forms them) only the row max goes to
+// s_rstat and the gates come from the picks' numerators alone.
+
+// The candidate path for NR row groups: K rounds over the 64 candidates, then
+// the check.  Returns (uniformly) whether every row passed; then top and
+// mine hold each row's top key and lane l's pick.  A row whose picks include
+// a zero does not pass (the order of equal logits decides it: the full path).
+template <class DT, int VW, int NV, int NR, int K>
+__device__ __forceinline__ bool fast_topk_rows(const typename DT::Raw* const (&row)[NR], const bool (&valid)[NR],
+                                               int E, int l, typename DT::Key* s_pick, const FastTopk<(VW * NV) / 2>& fs,
+                                               typename DT::Key (&top)[NR], typename DT::Key (&mine)[NR]) {
+  using Key = typename DT::Key;
+  constexpr int LPR = kWarp;
+  constexpr int NW = VW * NV / 2;
+  uint32_t wd[NR][NW];
+  Key c1[NR], c2[NR], w[NR];                       // the lane's two candidate keys, larger first
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    load_lane_words<LPR, VW, NV>(row[r], E, l, valid[r], wd[r]);
+    const uint32_t za = valid[r] ? uint32_t(row[r][fs.col0]) : 0u;
+    const uint32_t zb = valid[r] ? uint32_t(row[r][fs.col1]) : 0u;
+    const Key ka = bf16_key_for(za << 16, fs.inv0), kb = bf16_key_for(zb << 16, fs.inv1);
+    c1[r] = ka > kb ? ka : kb;
+    c2[r] = ka > kb ? kb : ka;
+  }
+  __syncwarp();                                    // the previous rows' picks have been read
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) w[r] = group_max_key<LPR>(c1[r]);
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      if (j == 0) top[r] = w[r];
+      s_pick[r * kMaxK + j] = w[r];
+      const bool won = c1[r] == w[r];
+      c1[r] = won ? c2[r] : c1[r];
+      c2[r] = won ? DT::kKeyMin : c2[r];
+    }
+  }
+  // Every element outside the candidates must lie below the k-th pick's value.
+  bool ok = true;
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    uint32_t mw = bf16x2_keep(wd[r][0], fs.keep[0]);
+#pragma unroll
+    for (int j = 1; j < NW; ++j) mw = bf16x2_max(mw, bf16x2_keep(wd[r][j], fs.keep[j]));
+    mw = bf16x2_max(mw, __byte_perm(mw, 0u, 0x1032));
+    ok = ok && (!valid[r] || __uint_as_float(mw << 16) < DT::key_value(w[r]));
+  }
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    mine[r] = l < K ? s_pick[r * kMaxK + l] : DT::kKeyMin;
+    ok = ok && !(valid[r] && l < K && DT::is_zero(mine[r]));
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
+// The rest of the forward of NR row groups once their picks are known.
+template <class DT, int VW, int NV, int NR, bool SOFTMAX>
+__device__ __forceinline__ void row_tail(const RouterParams& p, const typename DT::Raw* const (&row)[NR],
+                                         const long long (&t)[NR], const bool (&valid)[NR], int l, int* s_hist,
+                                         float (&pacc)[VW * NV], uint16_t* s_aidx, long long a_base, float2* s_rstat,
+                                         long long r_base, const typename DT::Key (&top)[NR],
+                                         const typename DT::Key (&mine)[NR]) {
+  using Raw = typename DT::Raw;
+  constexpr int LPR = kWarp;
+  constexpr int EPL = VW * NV;
+  const int k = p.k;
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const float mx = DT::key_value(top[r]);
+    const bool owner = l < k;
+    const float ej = owner ? elem_exp(DT::key_value(mine[r]), mx) : 0.f;
+    float denom, inv_s = 0.f;
+    if constexpr (SOFTMAX) {
+      Raw raw[EPL];
+      load_lane<DT, LPR, VW, NV, false>(row[r], p.E, l, valid[r], raw);
+      float e[EPL];
+      row_exp<DT, LPR, EPL>(raw, mx, e);
+      const float s = group_sum<LPR>(tree_sum(e));
+      inv_s = valid[r] ? rcp_approx(s) : 0.f;
+      axpy2(pacc, e, inv_s);
+      denom = p.renorm ? owners_sum<LPR>(ej) : s;
+    } else {
+      denom = owners_sum<LPR>(ej);
+    }
+    if (valid[r] && owner) {
+      const int col = DT::key_col(mine[r]);
+      const long long a = t[r] * k + l;
+      p.idx[a] = col;
+      p.gate[a] = ej * rcp_approx(denom);
+      atomicAdd(&s_hist[col], 1);
+      if (s_aidx != nullptr) s_aidx[a - a_base] = uint16_t(col);
+    }
+    if (s_rstat != nullptr && valid[r] && l == 0) s_rstat[t[r] - r_base] = make_float2(mx, inv_s);
+  }
+}
+
+// The full path for NR row groups, then the tail.
+template <class DT, int VW, int NV, int NR, bool SOFTMAX>
+__device__ __forceinline__ void slow_rows(const RouterParams& p, const typename DT::Raw* const (&row)[NR],
+                                          const long long (&t)[NR], const bool (&valid)[NR], int l, int* s_hist,
+                                          float (&pacc)[VW * NV], typename DT::Key* s_pick, uint16_t* s_aidx,
+                                          long long a_base, float2* s_rstat, long long r_base) {
+  typename DT::Key top[NR], mine[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const TopPick<typename DT::Key> tp = full_topk_row<DT, VW, NV>(row[r], p.E, p.k, l, valid[r], s_pick + r * kMaxK);
+    top[r] = tp.top;
+    mine[r] = tp.mine;
+  }
+  row_tail<DT, VW, NV, NR, SOFTMAX>(p, row, t, valid, l, s_hist, pacc, s_aidx, a_base, s_rstat, r_base, top, mine);
+}
+
+// The rest of a ring stage of a consumer warp on the candidate path with K
+// picks: its row groups sg = sg0, sg0 + kConsumerWarps, ... take
+// fast_topk_rows and the tail; the groups the check rejects are redone by the
+// full path after the loop.  Returns the number of row groups tried; *failed
+// gets the count rejected.
+template <class DT, int VW, int NV, int NR, int K, bool SOFTMAX>
+__device__ __forceinline__ int fast_stage(const RouterParams& p, const typename DT::Raw* st, int rows_here,
+                                          long long t0, int sg0, int l, int* s_hist, float (&pacc)[VW * NV],
+                                          typename DT::Key* s_pick, uint16_t* s_aidx, long long a_base,
+                                          float2* s_rstat, long long r_base, const FastTopk<(VW * NV) / 2>& fs,
+                                          int* failed_out) {
+  using Raw = typename DT::Raw;
+  const int E = p.E;
+  unsigned failed = 0u;
+  int n = 0;
+  for (int sg = sg0; sg * NR < rows_here; sg += kConsumerWarps, ++n) {
+    const Raw* rows[NR];
+    long long ts[NR];
+    bool valids[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const int ri = sg * NR + r;
+      valids[r] = ri < rows_here;
+      rows[r] = st + (valids[r] ? ri : 0) * E;
+      ts[r] = t0 + ri;
+    }
+    typename DT::Key top[NR], mine[NR];
+    if (fast_topk_rows<DT, VW, NV, NR, K>(rows, valids, E, l, s_pick, fs, top, mine))
+      row_tail<DT, VW, NV, NR, SOFTMAX>(p, rows, ts, valids, l, s_hist, pacc, s_aidx, a_base, s_rstat, r_base, top, mine);
+    else
+      failed |= 1u << n;
+  }
+  *failed_out = __popc(failed);
+  while (failed != 0u) {
+    const int b = __ffs(failed) - 1;
+    failed &= failed - 1u;
+    const int sg = sg0 + b * kConsumerWarps;
+    const Raw* rows[NR];
+    long long ts[NR];
+    bool valids[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const int ri = sg * NR + r;
+      valids[r] = ri < rows_here;
+      rows[r] = st + (valids[r] ? ri : 0) * E;
+      ts[r] = t0 + ri;
+    }
+    slow_rows<DT, VW, NV, NR, SOFTMAX>(p, rows, ts, valids, l, s_hist, pacc, s_pick, s_aidx, a_base, s_rstat, r_base);
+  }
+  return n;
+}
+
+// A whole ring stage of a consumer warp in the large-E bf16 variants: the
+// candidate path (k fixed per instantiation) while fs is in use, the full path
+// otherwise.  A warp still waiting for the candidate set looks for it before
+// each row group and switches as soon as it is published.
+template <class DT, int VW, int NV, int NR, bool SOFTMAX>
+__device__ __forceinline__ void fwd_stage_fast(const RouterParams& p, const typename DT::Raw* st, int rows_here,
+                                               long long t0, int warp, int l, int* s_hist, float (&pacc)[VW * NV],
+                                               typename DT::Key* s_pick, uint16_t* s_aidx, long long a_base,
+                                               float2* s_rstat, long long r_base, FastTopk<(VW * NV) / 2>& fs,
+                                               const int* s_red) {
+  using Raw = typename DT::Raw;
+  int sg = warp;
+  for (; sg * NR < rows_here; sg += kConsumerWarps) {
+    if (fs.state == 0 && *reinterpret_cast<const volatile int*>(s_red + kRedCandReady) != 0) {
+      __threadfence_block();                       // the set itself after its flag
+      fast_setup<kWarp, VW, NV>(fs, s_red, p.E, l);
+    }
+    if (fs.state == 1) break;
+    const Raw* rows[NR];
+    long long ts[NR];
+    bool valids[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const int ri = sg * NR + r;
+      valids[r] = ri < rows_here;
+      rows[r] = st + (valids[r] ? ri : 0) * p.E;
+      ts[r] = t0 + ri;
+    }
+    slow_rows<DT, VW, NV, NR, SOFTMAX>(p, rows, ts, valids, l, s_hist, pacc, s_pick, s_aidx, a_base, s_rstat, r_base);
+  }
+  if (fs.state == 1 && sg * NR < rows_here) {
+    int n = 0, failed = 0;
+#define MOE_FAST_STAGE(K)                                                                                        \
+    n = fast_stage<DT, VW, NV, NR, K, SOFTMAX>(p, st, rows_here, t0, sg, l, s_hist, pacc, s_pick, s_aidx, a_base, \
+                                               s_rstat, r_base, fs, &failed)
+    switch (p.k) {
+      case 1: MOE_FAST_STAGE(1); break;
+      case 2: MOE_FAST_STAGE(2); break;
+      case 3: MOE_FAST_STAGE(3); break;
+      case 4: MOE_FAST_STAGE(4); break;
+      case 5: MOE_FAST_STAGE(5); break;
+      case 6: MOE_FAST_STAGE(6); break;
+      case 7: MOE_FAST_STAGE(7); break;
+      default: MOE_FAST_STAGE(8); break;
+    }
+#undef MOE_FAST_STAGE
+    fs.tries += n;
+    fs.fails += failed;
   }
 }
 
@@ -552,29 +1054,34 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
 //   dlogits[t,j] = coef * p[t,j] * (f[j] - sum_i p[t,i] f[i])
 // With F = coef * f (held per lane), p = e / s and w = (1/s)^2 * sum_i e_i F_i:
 //   dlogits[t,j] = e_j * ((1/s) * F_j - w).
-// mL (max * log2e) and inv_s come from the forward (bwd_row_stats otherwise).
+// The row max mx and inv_s come from the forward (bwd_row_stats otherwise).
 // ---------------------------------------------------------------------------
 template <class DT, int LPR, int VW, int NV>
-__device__ __forceinline__ void bwd_row_stats(const typename DT::Raw (&raw)[VW * NV], float& mL, float& inv_s) {
+__device__ __forceinline__ void bwd_row_stats(const typename DT::Raw (&raw)[VW * NV], float& mx, float& inv_s) {
   constexpr int EPL = VW * NV;
   float m = -3.402823466e38f;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) m = fmaxf(m, __uint_as_float(DT::bits(raw[i])));
-  mL = group_max<LPR>(m) * kLog2e;
+  mx = group_max<LPR>(m);
   float e[EPL];
-  row_exp<DT, LPR, EPL>(raw, mL, e);
+  row_exp<DT, LPR, EPL>(raw, mx, e);
   inv_s = rcp_approx(group_sum<LPR>(tree_sum(e)));
 }
 
 template <class DT, int LPR, int VW, int NV>
 __device__ __forceinline__ void bwd_group(const typename DT::Raw (&raw)[VW * NV], const float (&Fr)[VW * NV], long long t,
-                                          bool valid, int l, int E, float mL, float inv_s, float* dlogits) {
+                                          bool valid, int l, int E, float mx, float inv_s, float* dlogits) {
   constexpr int EPL = VW * NV;
   float e[EPL];
-  row_exp<DT, LPR, EPL>(raw, mL, e);
+  row_exp<DT, LPR, EPL>(raw, mx, e);
   float dot[EPL];
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) dot[i] = e[i] * Fr[i];
+  for (int i = 0; i + 1 < EPL; i += 2) {
+    const float2 q = mul2(make_float2(e[i], e[i + 1]), make_float2(Fr[i], Fr[i + 1]));
+    dot[i] = q.x;
+    dot[i + 1] = q.y;
+  }
+  if constexpr (EPL & 1) dot[EPL - 1] = e[EPL - 1] * Fr[EPL - 1];
   const float w = inv_s * (inv_s * group_sum<LPR>(tree_sum(dot)));
   if (valid) {
     float* out = dlogits + t * (long long)E;
@@ -583,12 +1090,88 @@ __device__ __forceinline__ void bwd_group(const typename DT::Raw (&raw)[VW * NV]
       const int c0 = col_of<LPR, VW>(v, l, 0);
       if (c0 < E) {
         float d[VW];
+        if constexpr (VW % 2 == 0) {
 #pragma unroll
-        for (int i = 0; i < VW; ++i) d[i] = e[v * VW + i] * fmaf(inv_s, Fr[v * VW + i], -w);
+          for (int i = 0; i < VW; i += 2) {
+            const int j = v * VW + i;
+            const float2 h = fma2(make_float2(inv_s, inv_s), make_float2(Fr[j], Fr[j + 1]), make_float2(-w, -w));
+            const float2 q = mul2(make_float2(e[j], e[j + 1]), h);
+            d[i] = q.x;
+            d[i + 1] = q.y;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < VW; ++i) d[i] = e[v * VW + i] * fmaf(inv_s, Fr[v * VW + i], -w);
+        }
         store_vec_f32<VW>(out + c0, d);
       }
     }
   }
+}
+
+// Backward of one row group in a split step: the softmax sum comes here, not
+// from the forward.  e, s = sum e and sum e * F are formed in one pass (the
+// same arithmetic and order as bwd_row_stats and bwd_group, so dlogits is the
+// same bits as the separate backward's); p = e / s is added into pacc.
+template <class DT, int LPR, int VW, int NV>
+__device__ __forceinline__ void bwd_group_split(const typename DT::Raw (&raw)[VW * NV], const float (&Fr)[VW * NV],
+                                                long long t, bool valid, int l, int E, float mx, float (&pacc)[VW * NV],
+                                                float* dlogits) {
+  constexpr int EPL = VW * NV;
+  float e[EPL];
+  row_exp<DT, LPR, EPL>(raw, mx, e);
+  float dot[EPL];
+#pragma unroll
+  for (int i = 0; i + 1 < EPL; i += 2) {
+    const float2 q = mul2(make_float2(e[i], e[i + 1]), make_float2(Fr[i], Fr[i + 1]));
+    dot[i] = q.x;
+    dot[i + 1] = q.y;
+  }
+  if constexpr (EPL & 1) dot[EPL - 1] = e[EPL - 1] * Fr[EPL - 1];
+  float sum = tree_sum(e), sdot = tree_sum(dot);
+#pragma unroll
+  for (int off = LPR / 2; off > 0; off >>= 1) {
+    sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    sdot += __shfl_xor_sync(0xffffffffu, sdot, off);
+  }
+  const float inv_s = rcp_approx(sum);
+  if (valid) axpy2(pacc, e, inv_s);
+  const float w = inv_s * (inv_s * sdot);
+  if (valid) {
+    float* out = dlogits + t * (long long)E;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int c0 = col_of<LPR, VW>(v, l, 0);
+      if (c0 < E) {
+        float d[VW];
+#pragma unroll
+        for (int i = 0; i < VW; i += 2) {
+          const int j = v * VW + i;
+          const float2 h = fma2(make_float2(inv_s, inv_s), make_float2(Fr[j], Fr[j + 1]), make_float2(-w, -w));
+          const float2 q = mul2(make_float2(e[j], e[j + 1]), h);
+          d[i] = q.x;
+          d[i + 1] = q.y;
+        }
+        store_vec_f32<VW>(out + c0, d);
+      }
+    }
+  }
+}
+
+// A CTA's sum of p of one expert (x >= 0) into the fixed-point totals: its
+// value split at 2^-20 and 2^-64 into two 64-bit integers, so the totals are
+// exact whatever the order of the atomics.
+__device__ __forceinline__ void pfix_add(unsigned long long* hi_acc, unsigned long long* lo_acc, float x) {
+  const double q = double(x) * 0x1p20;                 // x < 2^31: q < 2^51
+  const double hi = floor(q);
+  const unsigned long long lo = (unsigned long long)((q - hi) * 0x1p44);   // exact for x >= 2^-41
+  if (hi != 0.0) atomicAdd(hi_acc, (unsigned long long)hi);
+  if (lo != 0ull) atomicAdd(lo_acc, lo);
+}
+
+// The value of a fixed-point total.
+__device__ __forceinline__ double pfix_value(unsigned long long hi, unsigned long long lo) {
+  return double(hi) * 0x1p-20 + double(lo) * 0x1p-64;
 }
 
 // Lane l's values of coef * f (zero past E) from a shared-memory copy of f.
@@ -852,6 +1435,7 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
   const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
   constexpr bool kFwd = (MODE & kModeFwd) != 0, kDisp = (MODE & kModeDispatch) != 0;
+  constexpr bool kHasP = kFwd && (MODE & kModeSplit) == 0;   // a split step writes P and the balance at its end
   // Sums of f*P, of squared count deviations and the extremes.  A deviation
   // c*E - T*k is exact in 64-bit integers; its square and the sums are fp32
   // (positive terms, relative error well under 1e-6 at E <= 1024).
@@ -866,8 +1450,8 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
     for (int j = 0; j < kB; ++j) {
       const int e = e0 + j * kWarp + lane;
       c[j] = e < E ? __ldcg(counts + e) : 0;
-      fv[j] = kFwd && e < E ? __ldcg(p.f + e) : 0.f;
-      pv[j] = kFwd && e < E ? __ldcg(p.P + e) : 0.f;
+      fv[j] = kHasP && e < E ? __ldcg(p.f + e) : 0.f;
+      pv[j] = kHasP && e < E ? __ldcg(p.P + e) : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < kB; ++j) {
@@ -918,9 +1502,11 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
     if (lane == 0) {
       // mean = T*k/E; std/mean = sqrt(sum d^2 / E) / E / mean = sqrt(sum d^2) / (sqrt(E) * T*k)
       const float ftk = float(tk);
-      const float balance = float(E) * fp;
-      p.scalars[0] = p.alpha * balance;
-      p.scalars[1] = balance;
+      if constexpr (kHasP) {
+        const float balance = float(E) * fp;
+        p.scalars[0] = p.alpha * balance;
+        p.scalars[1] = balance;
+      }
       p.scalars[2] = __fdiv_rn(__fsqrt_rn(dev), __fsqrt_rn(float(E)) * ftk);
       p.scalars[3] = __fdiv_rn(float(cmax) * float(E), ftk);
       p.scalars[4] = __fdiv_rn(float(cmin) * float(E), ftk);
@@ -1006,7 +1592,7 @@ __device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta,
   const int lane = threadIdx.x & 31;
   const int E = p.E;
   if (wait_phase(p, s_phase, 1) < 1) return;            // an error (or a lost signal): write nothing
-  if constexpr ((MODE & kModeFwd) != 0) {
+  if constexpr ((MODE & kModeFwd) != 0 && (MODE & kModeSplit) == 0) {
     for (int e = cta; e < E; e += p.G) {
       const float Ps = warp_column_sum_f(p.P_part + (size_t)e * p.G_stride, p.G);
       if (lane == 0) p.P[e] = __fdiv_rn(Ps, float(p.T));
@@ -1124,6 +1710,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     *s_phase = 0;
     *s_ranked = 0;
     s_red[kRedFixNext] = 0;
+    s_red[kRedCandReady] = 0;
+    s_red[kRedCandDone] = 0;
   }
   if (STAGED && tid == 0) {
     for (int q = 0; q < NS; ++q) {
@@ -1147,6 +1735,12 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
 #pragma unroll
       for (int i = 0; i < EPL; ++i) pacc[i] = 0.f;
       if constexpr (STAGED) {
+        // The fast top-k path (bf16 rows of 32 lanes, at most 16 elements per lane).
+        constexpr bool kFast = kFastTopk<DT, LPR, VW, NV>;
+        FastTopk<(EPL / 2 > 0 ? EPL / 2 : 1)> fs;
+        fs.state = kFast && n_st > 1 ? 0 : 2;
+        fs.tries = 0;
+        fs.fails = 0;
         for (int s = 0; s < n_st; ++s) {
           const int q = s % NS;
           if (!mbar_wait(&full[q], (s / NS) & 1, p.timeout_ns)) {
@@ -1156,19 +1750,47 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           if (s == 0) trace_point(p, kTrFirstStage);
           const Raw* st = ring + q * stage_elems;
           const int rows_here = min(S, n_rows - s * S);
-          for (int sg = warp; sg * NR * RPW < rows_here; sg += kConsumerWarps) {
-            const Raw* rows[NR];
-            long long ts[NR];
-            bool valids[NR];
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-              const int ri = (sg * NR + r) * RPW + g;
-              valids[r] = ri < rows_here;
-              rows[r] = st + (valids[r] ? ri : 0) * E;
-              ts[r] = r0 + (long long)s * S + ri;
+          if constexpr (kFast) {
+            if (fs.state == 1 && fs.tries >= 64) {
+              if (fs.fails * 8 > fs.tries) fs.state = 2;      // more than one row in eight fails: stop trying
+              fs.tries = 0;
+              fs.fails = 0;
             }
-            fwd_groups<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, s_aidx, a0,
-                                                   s_rstat, r0);
+            // The first stage's column sums choose the candidate set: each warp
+            // adds its slice of the columns (into warp 0's slot of the per-warp
+            // partials, unused until warp 0's rows are done) and the last warp
+            // to finish chooses, while the others go on with their rows.
+            if (s == 0 && n_st > 1) {
+              stage_column_sums(reinterpret_cast<const uint16_t*>(st), rows_here, E, warp, reinterpret_cast<float*>(s_wf));
+              __syncwarp();
+              int last = 0;
+              if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(&s_red[kRedCandDone], 1) == kConsumerWarps - 1;
+              }
+              if (__shfl_sync(0xffffffffu, last, 0)) {
+                __threadfence_block();
+                choose_candidates(reinterpret_cast<const float*>(s_wf), E, s_red);
+              }
+            }
+            fwd_stage_fast<DT, VW, NV, NR, (MODE & kModeSplit) == 0>(p, st, rows_here, r0 + (long long)s * S, warp, l,
+                                                                     s_hist, pacc, s_pick_w, s_aidx, a0, s_rstat, r0, fs,
+                                                                     s_red);
+          } else {
+            for (int sg = warp; sg * NR * RPW < rows_here; sg += kConsumerWarps) {
+              const Raw* rows[NR];
+              long long ts[NR];
+              bool valids[NR];
+#pragma unroll
+              for (int r = 0; r < NR; ++r) {
+                const int ri = (sg * NR + r) * RPW + g;
+                valids[r] = ri < rows_here;
+                rows[r] = st + (valids[r] ? ri : 0) * E;
+                ts[r] = r0 + (long long)s * S + ri;
+              }
+              fwd_groups<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, s_aidx, a0,
+                                                     s_rstat, r0);
+            }
           }
           __syncwarp();
           if (lane == 0) {
@@ -1178,6 +1800,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
               *reinterpret_cast<volatile int*>(&s_prog[warp]) = s + 1;
             }
           }
+
         }
       } else {
         for (long long base = r0 + (long long)warp * NR * RPW; base < r1; base += (long long)kConsumerWarps * NR * RPW) {
@@ -1195,12 +1818,13 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
       }
       trace_point(p, kTrFwdRows);
       trace_last(p, kTrFwdRowsAll);
-      // Sum the row groups of the warp; group 0 stores the warp's partials.
+      // Sum the row groups of the warp; group 0 stores the warp's partials
+      // (a split step forms p in the backward instead).
 #pragma unroll
       for (int i = 0; i < EPL; ++i)
 #pragma unroll
         for (int off = LPR; off < kWarp; off <<= 1) pacc[i] += __shfl_xor_sync(0xffffffffu, pacc[i], off);
-      if (g == 0) {
+      if ((MODE & kModeSplit) == 0 && g == 0) {
 #pragma unroll
         for (int v = 0; v < NV; ++v)
 #pragma unroll
@@ -1328,7 +1952,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
       const int c = s_hist[e];
       p.tile_hist[(size_t)e * p.G_stride + cta] = c;
       if (c != 0) atomicAdd(grp_hist + e, c);
-      if constexpr ((MODE & kModeFwd) != 0) {
+      if constexpr ((MODE & kModeFwd) != 0 && (MODE & kModeSplit) == 0) {
         float t = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) t += s_wf[w * E + e];
@@ -1416,6 +2040,11 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     if (warp < kConsumerWarps) {
       float fr[EPL];
       load_f<LPR, VW, NV>(s_f, E, l, coef, fr);
+      constexpr bool kSplit = (MODE & kModeSplit) != 0;
+      static_assert(!kSplit || (STAGED && kFastTopk<DT, LPR, VW, NV>), "split steps run on the fast variants");
+      float pacc_b[EPL];                           // a split step's sums of p over the warp's rows
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) pacc_b[i] = 0.f;
       if constexpr (STAGED) {
         for (int s = n_st - 1; s >= 0; --s) {
           const int q = s % NS;
@@ -1432,15 +2061,28 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
             const bool valid = ri < rows_here;
             Raw raw[EPL];
             load_lane<DT, LPR, VW, NV, false>(st + (valid ? ri : 0) * E, E, l, valid, raw);
-            float mL, inv_s;
-            if (s_rstat != nullptr) {
-              const float2 rs = s_rstat[valid ? s * S + ri : 0];
-              mL = rs.x;
-              inv_s = rs.y;
+            if constexpr (kSplit) {
+              float mx;
+              if (s_rstat != nullptr) {
+                mx = s_rstat[valid ? s * S + ri : 0].x;
+              } else {
+                float m = -3.402823466e38f;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) m = fmaxf(m, __uint_as_float(DT::bits(raw[i])));
+                mx = group_max<LPR>(m);
+              }
+              bwd_group_split<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, mx, pacc_b, p.dlogits);
             } else {
-              bwd_row_stats<DT, LPR, VW, NV>(raw, mL, inv_s);
+              float mx, inv_s;
+              if (s_rstat != nullptr) {
+                const float2 rs = s_rstat[valid ? s * S + ri : 0];
+                mx = rs.x;
+                inv_s = rs.y;
+              } else {
+                bwd_row_stats<DT, LPR, VW, NV>(raw, mx, inv_s);
+              }
+              bwd_group<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, mx, inv_s, p.dlogits);
             }
-            bwd_group<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, mL, inv_s, p.dlogits);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[q]);
@@ -1452,13 +2094,62 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           const bool valid = t < r1;
           Raw raw[EPL];
           load_lane<DT, LPR, VW, NV, true>(X + (valid ? t : r0) * (long long)E, E, l, valid, raw);
-          float mL, inv_s;
-          bwd_row_stats<DT, LPR, VW, NV>(raw, mL, inv_s);
-          bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, E, mL, inv_s, p.dlogits);
+          float mx, inv_s;
+          bwd_row_stats<DT, LPR, VW, NV>(raw, mx, inv_s);
+          bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, E, mx, inv_s, p.dlogits);
         }
       }
       trace_point(p, kTrBwdRows);
       trace_last(p, kTrBwdRowsAll);
+      if constexpr (kSplit) {
+        // This CTA's sums of p: each warp's into the ring's memory (free once
+        // every consumer is past the backward), added over the warps in a
+        // fixed order, then into the fixed-point totals.  The CTA that adds
+        // its sums last writes P, the balance and L_aux, and clears the totals.
+        float* s_pw = reinterpret_cast<float*>(ring);      // [kConsumerWarps][E]
+        named_barrier(kBarConsumers, kConsumerThreads);
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+          for (int i = 0; i < VW; ++i) {
+            const int c = col_of<LPR, VW>(v, l, i);
+            if (c < E) s_pw[warp * E + c] = pacc_b[v * VW + i];
+          }
+        named_barrier(kBarConsumers, kConsumerThreads);
+        for (int c = tid; c < E; c += kConsumerThreads) {
+          float t = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) t += s_pw[w * E + c];
+          pfix_add(p.pfix + c, p.pfix + kMaxExperts + c, t);
+        }
+        __threadfence();
+        named_barrier(kBarConsumers, kConsumerThreads);
+        if (tid == 0) s_red[kRedBwdLast] = atom_add_acq_rel_u64(&p.ctrl->bwd_done, 1ull) == (unsigned long long)(G - 1);
+        named_barrier(kBarConsumers, kConsumerThreads);
+        if (s_red[kRedBwdLast]) {
+          __threadfence();
+          for (int c = tid; c < E; c += kConsumerThreads) {
+            const double tot = pfix_value(__ldcg(p.pfix + c), __ldcg(p.pfix + kMaxExperts + c));
+            const float Pc = float(tot / double(p.T));
+            p.P[c] = Pc;
+            s_pw[c] = Pc;
+            p.pfix[c] = 0ull;
+            p.pfix[kMaxExperts + c] = 0ull;
+          }
+          named_barrier(kBarConsumers, kConsumerThreads);
+          if (warp == 0) {
+            float fp = 0.f;
+            for (int c = lane; c < E; c += kWarp) fp = fmaf(__ldcg(p.f + c), s_pw[c], fp);
+            fp = warp_sum_f(fp);
+            if (lane == 0) {
+              const float balance = float(E) * fp;
+              p.scalars[0] = p.alpha * balance;
+              p.scalars[1] = balance;
+              p.ctrl->bwd_done = 0ull;
+            }
+          }
+        }
+      }
       // then help with the final dispatch positions that remain
       if (share_fixup && wait_phase(p, s_phase, 3) == 3)
         fixup_chunks(p, a0, int(a1 - a0), s_aidx, s_arank, s_coff, s_cbase, s_red + kRedFixNext);
@@ -1511,9 +2202,9 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const BwdParams p) {
     const bool valid = t < p.T;
     Raw raw[EPL];
     load_lane<DT, LPR, VW, NV, true>(X + (valid ? t : 0) * (long long)p.E, p.E, l, valid, raw);
-    float mL, inv_s;
-    bwd_row_stats<DT, LPR, VW, NV>(raw, mL, inv_s);
-    bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, p.E, mL, inv_s, p.dlogits);
+    float mx, inv_s;
+    bwd_row_stats<DT, LPR, VW, NV>(raw, mx, inv_s);
+    bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, p.E, mx, inv_s, p.dlogits);
   }
 }
 

@@ -13,6 +13,8 @@ struct RouterVariant {
   const void* fwd;         // persistent kernel, forward phases
   const void* step;        // persistent kernel, forward + dispatch + backward
   const void* bwd;         // streaming backward kernel
+  const void* step_split;  // the step with the softmax sum and P formed in the backward (renormalised
+                           // gates; bf16 rows of 32 lanes only, else null)
 };
 
 // Variants compiled for bf16 / fp32 logits; *n receives the count.

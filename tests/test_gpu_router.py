@@ -10,8 +10,8 @@ import torch
 
 import oracle
 import synth
-from parity import (assert_equal, check_backward, check_dispatch, check_forward, oracle_forward,
-                    to_device, workload_inputs)
+from parity import (FLT_MIN, RTOL, assert_close, assert_equal, check_backward, check_dispatch, check_forward,
+                    oracle_forward, to_device, workload_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -82,13 +82,22 @@ def test_step_parity_and_equals_separate_calls(mr, name, size):
     C = oracle.dispatch.capacity(w.T, w.k, w.E, w.capacity_factor)
     check_dispatch(st, want["idx"], w.E, C)
     check_backward(st["dlogits"], logits, w.dtype, want["f"], w.alpha, 1.0)
-    # the three separate calls give the same bits
+    # the three separate calls give the same bits, except P and the two scalars
+    # built from it, which a split step forms in its backward (exact fixed-point
+    # totals of other partial sums): those agree to rounding
     fw = mr.moe_router_fwd(x, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks)
     dp = mr.moe_dispatch(fw["idx"], w.E, w.capacity_factor)
     dl = mr.moe_router_bwd(x, fw["f"], w.alpha, 1.0)
     torch.cuda.synchronize()
-    for key in ("idx", "gate", "counts", "f", "P", "scalars", "rank_load"):
+    check_step_equals_separate(st, fw, dp, dl)
+
+
+def check_step_equals_separate(st, fw, dp, dl):
+    for key in ("idx", "gate", "counts", "f", "rank_load"):
         assert torch.equal(st[key], fw[key]), key
+    assert torch.equal(st["scalars"][2:], fw["scalars"][2:])
+    assert_close("P", st["P"].cpu().numpy(), fw["P"].double().cpu().numpy(), 2 * RTOL, FLT_MIN)
+    assert_close("L_aux, balance", st["scalars"][:2].cpu().numpy(), fw["scalars"][:2].double().cpu().numpy(), 2 * RTOL)
     for key in ("perm", "slot", "offsets", "kept", "n_dropped"):
         assert torch.equal(st[key], dp[key]), key
     assert torch.equal(st["dlogits"], dl)
@@ -125,6 +134,11 @@ EDGE = [
     (2048, 64, 8, "bf16", -1, 8, 1.0, 0),      # k = 8 at E = 64
     (1500, 48, 6, "bf16", 0, 0, 1.25, 2),      # raw gates, ties
     (999, 40, 5, "bf16", 1, 5, 1.0, 0),        # odd k, renormalised
+    (30011, 384, 6, "bf16", -1, 64, 1.25, 3),  # 32 lanes per row: candidate path with heavy ties
+    (30011, 200, 4, "bf16", -1, 8, 1.0, 0),    # candidate path, columns past E in the last lanes
+    (20011, 512, 8, "bf16", -1, 64, 1.0, 0),   # candidate path at E = 512
+    (20011, 256, 1, "bf16", 1, 0, 1.0, 0),     # candidate path, top-1 renormalised
+    (20011, 384, 6, "bf16", 0, 0, 1.25, 0),    # raw gates: the step keeps the softmax in its forward
 ]
 
 
@@ -182,6 +196,31 @@ def test_saturated_rows(mr, T, E, k, dtype):
     dl = mr.moe_router_bwd(x, st["f"], 0.01, 1.0)
     torch.cuda.synchronize()
     assert torch.equal(dl, st["dlogits"])
+
+
+def test_candidate_path_when_the_hot_experts_change(mr):
+    """The fast top-k path takes its candidates from each CTA's first rows.
+    Here the first half of the batch favours one set of experts and the second
+    half another, so the candidates go stale and rows fall back to the full
+    path; unskewed rows at the end make the check fail outright.  Every result
+    must still match the oracle."""
+    T, E, k = 40000, 384, 6
+    rng = np.random.default_rng(21)
+    z = rng.standard_normal((T, E)).astype(np.float32)
+    hot_a = rng.choice(E, 24, replace=False)
+    hot_b = rng.choice(np.setdiff1d(np.arange(E), hot_a), 24, replace=False)
+    z[: T // 2, hot_a] += 3.0
+    z[T // 2: 3 * T // 4, hot_b] += 3.0
+    logits = synth.f32_to_bf16_bits(z)
+    x = to_device(logits, "bf16")
+    st = mr.moe_router_step(x, k, 0.001, 1.25, n_ranks=64, grad_scale=1.0)
+    fw = mr.moe_router_fwd(x, k, 0.001, n_ranks=64)
+    torch.cuda.synchronize()
+    want = oracle_forward(logits, "bf16", k, 0.001, None, 64)
+    check_forward(st, want, 64)
+    check_forward(fw, want, 64)
+    check_dispatch(st, want["idx"], E, oracle.dispatch.capacity(T, k, E, 1.25))
+    check_backward(st["dlogits"], logits, "bf16", want["f"], 0.001, 1.0)
 
 
 def test_misaligned_views_take_the_scalar_path(mr):
@@ -293,11 +332,7 @@ def test_small_expert_counts_equal_separate_calls(mr, E, k):
     check_forward(st, want, 0)
     check_dispatch(st, want["idx"], E, oracle.dispatch.capacity(3001, k, E, 1.25))
     check_backward(st["dlogits"], logits, "bf16", want["f"], 0.01, 1.0)
-    for key in ("idx", "gate", "counts", "f", "P", "scalars"):
-        assert torch.equal(st[key], fw[key]), key
-    for key in ("perm", "slot", "offsets", "kept", "n_dropped"):
-        assert torch.equal(st[key], dp[key]), key
-    assert torch.equal(st["dlogits"], dl)
+    check_step_equals_separate(st, fw, dp, dl)
 
 
 def test_back_to_back_calls_on_one_workspace(mr):
