@@ -198,7 +198,12 @@ MOE_API moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_
  * moe_router_fwd, then moe_dispatch on the idx it produced, then
  * moe_router_bwd with its f, computed by one persistent cooperative kernel
  * (grid-wide barriers separate the global reductions).  Outputs are
- * bit-identical to the three separate calls.  Arguments as above. */
+ * bit-identical to the three separate calls, with one exception: for bf16
+ * logits with 129 <= E <= 512 and renormalised gates the step forms the
+ * rows' softmax sums and P in its backward, and P (with L_aux and the
+ * balance, which use it) is then the exact sum of other partial sums, equal
+ * to moe_router_fwd's to rounding (both within the stated tolerance of the
+ * exact value) and bit-identical from run to run.  Arguments as above. */
 MOE_API moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
                            float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
                            float grad_scale,
