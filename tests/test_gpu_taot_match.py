@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle_pool
 import synth
 from oracle import sinkhorn, taot_match
 
@@ -42,14 +43,18 @@ def check(got, loads, plans, R, rpn, k, rows):
         assert np.array_equal(got["rank_load"][b], want["rank_load"]), f"rank_load of microbatch {b}"
 
 
-def test_full_workload_sampled(mr):
-    """All 1024 microbatches on the GPU, as the benchmark runs them; 96 sampled
-    microbatches against the oracle, and the plan's invariants on all of them."""
+def test_full_workload_every_microbatch(mr):
+    """All 1024 microbatches on the GPU, as the benchmark runs them, each
+    against the oracle (run in a process pool across the host's cores), and the
+    plan's invariants on all of them."""
     loads = synth.eplb_loads(W)
     plans = oracle_plans(loads, R, RPN)
     got = run(mr, loads, plans, RPN, K)
-    rows = np.random.default_rng(0).choice(W.B, size=96, replace=False)
-    check(got, loads, plans, R, RPN, K, sorted(rows))
+    want = oracle_pool.match_all(loads, plans, R, RPN, K)
+    for b, (se, st, rl) in enumerate(want):
+        assert np.array_equal(got["slot_expert"][b], se), f"slot_expert of microbatch {b}"
+        assert np.array_equal(got["slot_tokens"][b], st), f"slot_tokens of microbatch {b}"
+        assert np.array_equal(got["rank_load"][b], rl), f"rank_load of microbatch {b}"
     before = loads.reshape(W.B, R, -1).sum(axis=2)
     total = before.sum(axis=1, keepdims=True)
     after = got["rank_load"]
