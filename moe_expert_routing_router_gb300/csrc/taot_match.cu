@@ -13,43 +13,54 @@
 // loads as they stand then.  Loads are compared with the mean exactly, as
 // load * R against the total.
 //
-// One CTA per microbatch.  Each round first gathers the candidate experts
-// (home rank hot, tokens left); a warp per cold rank scores them (lanes stride
-// over the candidates, a shuffle tree picks the best).  The arbitration is two
-// shared-memory atomic maxima per expert over its choosers' keys, (tokens,
-// same node) and then (flow, inverted rank), so the best chooser and, among
-// equal ones, the lowest rank wins.  The winners' moves are committed in
-// ascending rank order within each hot home rank (the only quantity two
-// winners of a round share is the load of the hot rank they both draw on) and
-// in parallel across home ranks.  floor((load * R - total) / R) is
-// load - ceil(total / R) and floor((total - load * R) / R) is
+// One CTA per microbatch.  Same node and flow depend only on the pair of ranks
+// (h, c), so the best expert of c splits into a best per home rank h, by tokens
+// and then the lower index, and a best over h by (tokens, same node, flow, lower
+// index).  The CTA keeps the table best[h][c] in shared memory.  An entry
+// changes only when a move touches h (its load and its experts' tokens left) or
+// c (its load, its slots, the experts it already hosts), so after the first
+// round only the rows and columns of the ranks that moved tokens are
+// recomputed.  Each round then has three parts, separated by block barriers:
+// the table update; the per-rank choice, eight warps each taking a quarter of
+// the home ranks for 32 cold ranks; and, in warp 0 alone with warp-level
+// synchronisation, the merge of the quarters, the arbitration and the commits.
+// The arbitration is two shared-memory atomic maxima per expert over its
+// choosers' keys, (tokens, same node) and then (flow, inverted rank), so the
+// best chooser and, among equal ones, the lowest rank wins.  The winners' moves
+// are committed in ascending rank order within each hot home rank (the only
+// quantity two winners of a round share is the load of the hot rank they both
+// draw on) and in parallel across home ranks.  floor((load * R - total) / R)
+// is load - ceil(total / R) and floor((total - load * R) / R) is
 // floor(total / R) - load, so no division is left in the scoring.
 #include "taot_match.h"
 
 namespace moe {
 namespace {
 
-constexpr int kMatchThreads = 256;
+constexpr int kMatchThreads = 256;   // eight warps: two blocks of 32 cold ranks x four quarters of the home ranks
+constexpr int kParts = 4;
 
 struct MatchSmem {
   long long* load;     // [R]
+  long long* total;    // [1]
+  unsigned long long* win2;   // [E] best key2 among the choosers with the best key1
+  unsigned long long* hmask;  // [R] this round's winners drawing on hot home rank h, one bit per rank
   int32_t* w_rem;      // [E]
   uint32_t* used;      // [R][E / 32 rounded up]
   int32_t* n_slots;    // [R]
-  int32_t* choice;     // [R] chosen expert or -1
-  uint32_t* key1;      // [R] the choice's (tokens << 1) | same node
-  unsigned long long* key2;   // [R] the choice's (flow image << 6) | (63 - rank)
   uint32_t* win1;      // [E] best key1 among the expert's choosers this round (0: none)
-  unsigned long long* win2;   // [E] best key2 among the choosers with the best key1
-  unsigned long long* hmask;  // [R] this round's winners drawing on hot home rank h, one bit per rank
-  int32_t* cand;       // [E] this round's candidates: experts on hot ranks with tokens left
-  int32_t* give;       // [E] per candidate: min(tokens left at home, floor(home load - mean))
-  int32_t* hnode;      // [E] node of each expert's home rank
-  float* plan;         // [R][R] this microbatch's Phase 1 flow
-  int32_t* n_cand;     // [1]
+  uint32_t* fimg;      // [R][R] order-preserving image of this microbatch's Phase 1 flow, [h][c]
+  uint32_t* bk;        // [R][64] best (tokens << 1 | same node) of cold rank c on home rank h (0: none), at tab(h, c)
+  uint16_t* be;        // [R][64] the expert of that entry
+  uint32_t* pk;        // [kParts][R] per quarter of the home ranks: best key of cold rank c
+  uint32_t* pf;        // [kParts][R] its flow image
+  int32_t* pe;         // [kParts][R] its expert
+  uint8_t* hl;         // [R] home ranks whose table rows are recomputed this round
+  uint8_t* cl;         // [R] cold ranks whose table columns are recomputed this round
+  int32_t* nh;         // [1] entries of hl
+  int32_t* nc;         // [1] entries of cl
   int32_t* any;        // [1] the round had a choice (another round follows)
-  int32_t* steps;      // [1] the most winners on one home rank this round
-  long long* total;    // [1]
+  unsigned long long* dh;     // [1] bit h: home rank h is in hl
 };
 
 __host__ __device__ inline size_t a16(size_t x) { return (x + 15) / 16 * 16; }
@@ -60,44 +71,53 @@ __host__ __device__ inline size_t match_layout(int E, int R, MatchSmem* s, char*
   auto take = [&](size_t bytes) { const size_t o = off; off += a16(bytes); return base ? base + o : nullptr; };
   char* load = take(8u * R);
   char* total = take(8u);
-  char* key2 = take(8u * R);
   char* win2 = take(8u * E);
   char* hmask = take(8u * R);
   char* w_rem = take(4u * E);
   char* used = take(4u * R * words);
   char* n_slots = take(4u * R);
-  char* choice = take(4u * R);
-  char* key1 = take(4u * R);
   char* win1 = take(4u * E);
-  char* cand = take(4u * E);
-  char* give = take(4u * E);
-  char* hnode = take(4u * E);
-  char* plan = take(4u * R * R);
-  char* n_cand = take(4u);
+  char* fimg = take(4u * R * R);
+  char* bk = take(4u * R * 64);
+  char* be = take(2u * R * 64);
+  char* pk = take(4u * kParts * R);
+  char* pf = take(4u * kParts * R);
+  char* pe = take(4u * kParts * R);
+  char* hl = take(1u * R);
+  char* cl = take(1u * R);
+  char* nh = take(4u);
+  char* nc = take(4u);
   char* any = take(4u);
-  char* steps = take(4u);
+  char* dh = take(8u);
   if (s) {
-    s->any = reinterpret_cast<int32_t*>(any);
-    s->steps = reinterpret_cast<int32_t*>(steps);
-    s->cand = reinterpret_cast<int32_t*>(cand);
-    s->give = reinterpret_cast<int32_t*>(give);
-    s->hnode = reinterpret_cast<int32_t*>(hnode);
-    s->plan = reinterpret_cast<float*>(plan);
-    s->n_cand = reinterpret_cast<int32_t*>(n_cand);
     s->load = reinterpret_cast<long long*>(load);
     s->total = reinterpret_cast<long long*>(total);
+    s->win2 = reinterpret_cast<unsigned long long*>(win2);
+    s->hmask = reinterpret_cast<unsigned long long*>(hmask);
     s->w_rem = reinterpret_cast<int32_t*>(w_rem);
     s->used = reinterpret_cast<uint32_t*>(used);
     s->n_slots = reinterpret_cast<int32_t*>(n_slots);
-    s->choice = reinterpret_cast<int32_t*>(choice);
-    s->key1 = reinterpret_cast<uint32_t*>(key1);
-    s->key2 = reinterpret_cast<unsigned long long*>(key2);
     s->win1 = reinterpret_cast<uint32_t*>(win1);
-    s->win2 = reinterpret_cast<unsigned long long*>(win2);
-    s->hmask = reinterpret_cast<unsigned long long*>(hmask);
+    s->fimg = reinterpret_cast<uint32_t*>(fimg);
+    s->bk = reinterpret_cast<uint32_t*>(bk);
+    s->be = reinterpret_cast<uint16_t*>(be);
+    s->pk = reinterpret_cast<uint32_t*>(pk);
+    s->pf = reinterpret_cast<uint32_t*>(pf);
+    s->pe = reinterpret_cast<int32_t*>(pe);
+    s->hl = reinterpret_cast<uint8_t*>(hl);
+    s->cl = reinterpret_cast<uint8_t*>(cl);
+    s->nh = reinterpret_cast<int32_t*>(nh);
+    s->nc = reinterpret_cast<int32_t*>(nc);
+    s->any = reinterpret_cast<int32_t*>(any);
+    s->dh = reinterpret_cast<unsigned long long*>(dh);
   }
   return off;
 }
+
+// Position of the table entry (h, c): rows of 64, columns swizzled by the row so
+// that a warp reads or writes conflict-free both along a row (fixed h) and along
+// a column (fixed c).
+__device__ __forceinline__ int tab(int h, int c) { return h * 64 + (c ^ (h & 31)); }
 
 // Tokens the match (c, e) would move now (0: none).  fl = floor(total / R),
 // cl = ceil(total / R).
@@ -118,11 +138,50 @@ __device__ __forceinline__ uint32_t flow_image(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Best expert of home rank h for cold rank c as the state stands: the most
+// tokens moved, then the lower index; the key is (tokens << 1) | same node.
+__device__ __forceinline__ void update_entry(const MatchSmem& s, int R, int per, int words, int K, int rpn,
+                                             long long total, long long fl, long long cl, int h, int c) {
+  uint32_t bkey = 0u;
+  int bexp = 0;
+  const long long Lh = s.load[h], Lc = s.load[c];
+  if (Lh * R > total && Lc * R < total && s.n_slots[c] < K) {
+    const long long lim = Lh - cl < fl - Lc ? Lh - cl : fl - Lc;
+    if (lim > 0) {
+      const uint32_t same = h / rpn == c / rpn ? 1u : 0u;
+      const uint32_t* urow = s.used + c * words;
+      for (int e = h * per; e < (h + 1) * per; ++e) {
+        const int wr = s.w_rem[e];
+        if (wr <= 0 || ((urow[e >> 5] >> (e & 31)) & 1u)) continue;
+        const long long x = wr < lim ? wr : lim;
+        const uint32_t key = (uint32_t(x) << 1) | same;
+        if (key > bkey) {
+          bkey = key;
+          bexp = e;
+        }
+      }
+    }
+  }
+  s.bk[tab(h, c)] = bkey;
+  s.be[tab(h, c)] = uint16_t(bexp);
+}
+
+// Keeps (k, f, e) if it beats the best so far: larger key, then larger flow
+// image, then lower expert.
+__device__ __forceinline__ void better(uint32_t k, uint32_t f, int e, uint32_t& k1, uint32_t& f1, int& e1) {
+  if (k == 0u || k < k1) return;
+  if (k > k1 || f > f1 || (f == f1 && e < e1)) {
+    k1 = k;
+    f1 = f;
+    e1 = e;
+  }
+}
+
 __global__ void __launch_bounds__(kMatchThreads) taot_match_kernel(const MatchParams p) {
   extern __shared__ __align__(16) char smem[];
   MatchSmem s;
   match_layout(p.E, p.R, &s, smem);
-  const int b = blockIdx.x, R = p.R, E = p.E, K = p.K, per = E / R, words = (E + 31) / 32;
+  const int b = blockIdx.x, R = p.R, E = p.E, K = p.K, per = E / R, words = (E + 31) / 32, rpn = p.ranks_per_node;
   const int32_t* w = p.expert_loads + (long long)b * E;
   const float* plan = p.plan + (long long)b * R * R;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = kMatchThreads / 32;
@@ -130,13 +189,13 @@ __global__ void __launch_bounds__(kMatchThreads) taot_match_kernel(const MatchPa
     s.w_rem[e] = w[e];
     s.win1[e] = 0u;
     s.win2[e] = 0ull;
-    s.hnode[e] = (e / per) / p.ranks_per_node;
   }
-  for (int i = tid; i < R * R; i += blockDim.x) s.plan[i] = plan[i];
+  for (int i = tid; i < R * R; i += blockDim.x) s.fimg[i] = flow_image(plan[i]);
   for (int i = tid; i < R * words; i += blockDim.x) s.used[i] = 0u;
   for (int r = tid; r < R; r += blockDim.x) {
     s.n_slots[r] = 0;
     s.hmask[r] = 0ull;
+    s.hl[r] = uint8_t(r);                          // the first round computes every row
   }
   int32_t* se = p.slot_expert + (long long)b * R * K;
   int32_t* st = p.slot_tokens + (long long)b * R * K;
@@ -157,126 +216,157 @@ __global__ void __launch_bounds__(kMatchThreads) taot_match_kernel(const MatchPa
     long long t = 0;
     for (int r = 0; r < R; ++r) t += s.load[r];
     *s.total = t;
+    *s.nh = R;
+    *s.nc = 0;
+    *s.dh = R == 64 ? ~0ull : (1ull << R) - 1ull;
   }
   __syncthreads();
   const long long total = *s.total;
   const long long fl = total >= 0 ? total / R : -((-total + R - 1) / R);
   const long long cl = total >= 0 ? (total + R - 1) / R : -((-total) / R);
+  const int hq = (R + kParts - 1) / kParts;
   // Rounds repeat while some cold rank still finds a positive match.  A round
   // with a choice commits at least its lowest-ranked winner (no earlier move of
   // the round changed its numbers), and a rank holds at most K replicas, so
   // there are at most R * K + 1 rounds.
   for (int round = 0; round <= R * K; ++round) {
-    // This round's candidates: experts whose home rank is hot and that still
-    // have tokens at home (in any order: the score breaks ties by index).
-    if (tid == 0) {
-      *s.n_cand = 0;
-      *s.any = 0;
-      *s.steps = 0;
-    }
-    __syncthreads();
-    for (int e0 = warp * 32; e0 < E; e0 += kMatchThreads) {   // whole warps: the ballot needs every lane
-      const int e = e0 + lane;
-      long long g = 0;
-      if (e < E) {
-        const long long Lh = s.load[e / per];
-        if (Lh * R > total && s.w_rem[e] > 0) g = Lh - cl < s.w_rem[e] ? Lh - cl : s.w_rem[e];
-      }
-      const unsigned m = __ballot_sync(0xffffffffu, g > 0);
-      int base = 0;
-      if (lane == 0 && m != 0u) base = atomicAdd(s.n_cand, __popc(m));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (g > 0) {
-        const int q = base + __popc(m & ((1u << lane) - 1u));
-        s.cand[q] = e;
-        s.give[q] = int(g);
+    // Table update: the rows of the home ranks that gave tokens last round (all
+    // of them before the first), then the columns of the cold ranks that took
+    // tokens, without the entries the rows already covered.
+    {
+      const int nh = *s.nh, nc = *s.nc;
+      const unsigned long long dh = *s.dh;
+      for (int i = tid; i < (nh + nc) * 64; i += kMatchThreads) {
+        int h, c;
+        if (i < nh * 64) {
+          h = s.hl[i >> 6];
+          c = i & 63;
+        } else {
+          const int j = i - nh * 64;
+          c = s.cl[j >> 6];
+          h = j & 63;
+          if (h < R && ((dh >> h) & 1ull)) continue;
+        }
+        if (h < R && c < R) update_entry(s, R, per, words, K, rpn, total, fl, cl, h, c);
       }
     }
     __syncthreads();
-    const int n_cand = *s.n_cand;
-    // Every cold rank with a free slot picks its best expert: the largest
-    // (tokens << 1 | same node), then the largest flow, then the lowest expert:
-    // each lane keeps its best in that order over its share of the candidates,
-    // and three warp reductions settle the warp's.  A match moves
-    // min(give, floor(mean - load_c)).
-    for (int c = warp; c < R; c += nwarps) {
-      uint32_t k1 = 0u, fimg = 0u;
-      int be = 0x7fffffff;
-      const long long Lc = s.load[c];
-      if (s.n_slots[c] < K && Lc * R < total) {
-        const long long spare = fl - Lc;
-        const int node_c = c / p.ranks_per_node;
-        for (int q = lane; q < n_cand; q += 32) {
-          const int e = s.cand[q];
-          if ((s.used[c * words + (e >> 5)] >> (e & 31)) & 1u) continue;
-          const long long x = s.give[q] < spare ? s.give[q] : spare;
-          if (x <= 0) continue;
-          const uint32_t k = (uint32_t(x) << 1) | uint32_t(s.hnode[e] == node_c ? 1 : 0);
-          if (k < k1) continue;
-          const uint32_t fi = flow_image(s.plan[(e / per) * R + c]);
-          if (k > k1 || fi > fimg || (fi == fimg && e < be)) {
-            k1 = k;
-            fimg = fi;
-            be = e;
+    // Per-rank choice over a quarter of the home ranks: warp w takes cold ranks
+    // 32 (w & 1) + lane and home ranks [hq (w >> 1), hq (w >> 1 + 1)).
+    {
+      const int c = (warp & 1) * 32 + lane, part = warp >> 1;
+      if (c < R) {
+        uint32_t k1 = 0u, f1 = 0u;
+        int e1 = 0x7fffffff;
+        const int h1 = (part + 1) * hq < R ? (part + 1) * hq : R;
+        for (int h = part * hq; h < h1; ++h) {
+          const uint32_t k = s.bk[tab(h, c)];
+          if (k != 0u && k >= k1) better(k, s.fimg[h * R + c], s.be[tab(h, c)], k1, f1, e1);
+        }
+        s.pk[part * R + c] = k1;
+        s.pf[part * R + c] = f1;
+        s.pe[part * R + c] = e1;
+      }
+    }
+    __syncthreads();
+    // Warp 0 alone (lane l holds ranks l and l + 32): the merge of the quarters
+    // into each rank's choice; the arbitration, per expert the best (tokens,
+    // same node), then among those the best (flow, lower rank), by shared-memory
+    // atomic maxima; the winners' moves, in ascending rank order on each hot
+    // home rank and in parallel across home ranks; the lists of ranks whose
+    // table entries change; the clearing of the round's arbitration state.
+    if (warp == 0) {
+      int ce[2], hh[2], pos[2];
+      uint32_t ck1[2];
+      unsigned long long ck2[2];
+      bool win[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = lane + 32 * j;
+        uint32_t k1 = 0u, f1 = 0u;
+        int e1 = 0x7fffffff;
+        if (c < R) {
+#pragma unroll
+          for (int q = 0; q < kParts; ++q) better(s.pk[q * R + c], s.pf[q * R + c], s.pe[q * R + c], k1, f1, e1);
+        }
+        ce[j] = k1 != 0u ? e1 : -1;
+        ck1[j] = k1;
+        ck2[j] = ((unsigned long long)f1 << 6) | (unsigned long long)(63 - c);
+        if (ce[j] >= 0) atomicMax(&s.win1[ce[j]], k1);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        if (ce[j] >= 0 && s.win1[ce[j]] == ck1[j]) atomicMax(&s.win2[ce[j]], ck2[j]);
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = lane + 32 * j;
+        win[j] = ce[j] >= 0 && s.win1[ce[j]] == ck1[j] && s.win2[ce[j]] == ck2[j];
+        hh[j] = ce[j] >= 0 ? ce[j] / per : 0;
+        if (win[j]) atomicOr(&s.hmask[hh[j]], 1ull << c);
+      }
+      __syncwarp();
+      int steps = 0;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = lane + 32 * j;
+        pos[j] = 0;
+        if (win[j]) {
+          const unsigned long long m = s.hmask[hh[j]];
+          pos[j] = __popcll(m & ((1ull << c) - 1ull));
+          steps = max(steps, __popcll(m));
+        }
+      }
+      steps = int(__reduce_max_sync(0xffffffffu, uint32_t(steps)));
+      unsigned long long gave = 0ull, took = 0ull;   // this lane's commits: home ranks and cold ranks
+      for (int step = 0; step < steps; ++step) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = lane + 32 * j;
+          if (win[j] && pos[j] == step) {
+            const int x = moved(s, R, per, words, total, fl, cl, c, ce[j]);
+            if (x > 0) {
+              s.load[hh[j]] -= x;
+              s.load[c] += x;
+              s.w_rem[ce[j]] -= x;
+              s.used[c * words + (ce[j] >> 5)] |= 1u << (ce[j] & 31);
+              se[c * K + s.n_slots[c]] = ce[j];
+              st[c * K + s.n_slots[c]] = x;
+              s.n_slots[c] += 1;
+              gave |= 1ull << hh[j];
+              took |= 1ull << c;
+            }
           }
         }
+        __syncwarp();
       }
-      const uint32_t m1 = __reduce_max_sync(0xffffffffu, k1);
-      const uint32_t mf = __reduce_max_sync(0xffffffffu, k1 == m1 ? fimg : 0u);
-      const int me = int(__reduce_min_sync(0xffffffffu, k1 == m1 && fimg == mf ? uint32_t(be) : 0x7fffffffu));
-      if (lane == 0) {
-        s.choice[c] = m1 != 0u ? me : -1;
-        s.key1[c] = m1;
-        s.key2[c] = ((unsigned long long)mf << 6) | (unsigned long long)(63 - c);
-      }
-    }
-    __syncthreads();
-    // Arbitration: per expert the best (tokens, same node), then among those
-    // the best (flow, lower rank).
-    const int c = tid;
-    const int ce = c < R ? s.choice[c] : -1;
-    if (ce >= 0) atomicMax(&s.win1[ce], s.key1[c]);
-    __syncthreads();
-    if (ce >= 0 && s.win1[ce] == s.key1[c]) atomicMax(&s.win2[ce], s.key2[c]);
-    __syncthreads();
-    const bool winner = ce >= 0 && s.win1[ce] == s.key1[c] && s.win2[ce] == s.key2[c];
-    const int h = ce >= 0 ? ce / per : 0;
-    if (winner) atomicOr(&s.hmask[h], 1ull << c);
-    if (ce >= 0) atomicAdd(s.any, 1);
-    __syncthreads();
-    // The winners' moves: ascending rank order on each home rank, home ranks in parallel.
-    int pos = 0;
-    if (winner) {
-      const unsigned long long m = s.hmask[h];
-      pos = __popcll(m & ((1ull << c) - 1ull));
-      atomicMax(s.steps, __popcll(m));
-    }
-    __syncthreads();
-    const int steps = *s.steps;
-    for (int j = 0; j < steps; ++j) {
-      if (winner && pos == j) {
-        const int x = moved(s, R, per, words, total, fl, cl, c, ce);
-        if (x > 0) {
-          s.load[h] -= x;
-          s.load[c] += x;
-          s.w_rem[ce] -= x;
-          s.used[c * words + (ce >> 5)] |= 1u << (ce & 31);
-          se[c * K + s.n_slots[c]] = ce;
-          st[c * K + s.n_slots[c]] = x;
-          s.n_slots[c] += 1;
+      const bool any = __any_sync(0xffffffffu, ce[0] >= 0 || ce[1] >= 0);
+      gave = (unsigned long long)__reduce_or_sync(0xffffffffu, uint32_t(gave)) |
+             ((unsigned long long)__reduce_or_sync(0xffffffffu, uint32_t(gave >> 32)) << 32);
+      took = (unsigned long long)__reduce_or_sync(0xffffffffu, uint32_t(took)) |
+             ((unsigned long long)__reduce_or_sync(0xffffffffu, uint32_t(took >> 32)) << 32);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (ce[j] >= 0) {
+          s.win1[ce[j]] = 0u;
+          s.win2[ce[j]] = 0ull;
         }
+        const int r = lane + 32 * j;
+        if (r < R) s.hmask[r] = 0ull;
+        const unsigned long long below = (1ull << r) - 1ull;
+        if ((gave >> r) & 1ull) s.hl[__popcll(gave & below)] = uint8_t(r);
+        if ((took >> r) & 1ull) s.cl[__popcll(took & below)] = uint8_t(r);
       }
-      __syncthreads();
+      if (lane == 0) {
+        *s.any = any ? 1 : 0;
+        *s.nh = __popcll(gave);
+        *s.nc = __popcll(took);
+        *s.dh = gave;
+      }
     }
-    // clear this round's arbitration state
-    if (ce >= 0) {
-      s.win1[ce] = 0u;
-      s.win2[ce] = 0ull;
-    }
-    if (c < R) s.hmask[c] = 0ull;
-    const bool any = *s.any != 0;
     __syncthreads();
-    if (!any) break;
+    if (*s.any == 0) break;                        // written before the barrier, rewritten only after the next two
   }
   for (int r = tid; r < R; r += blockDim.x) p.rank_load[(long long)b * R + r] = int32_t(s.load[r]);
 }
