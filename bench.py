@@ -3,10 +3,15 @@ dispatch + backward over one batch (one launch of moe_router_step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-extra] [--section next_steps|eplb|taot_match]
+                    [--parallelism auto|dp|replicas]
 
-Prints one JSON line on rank 0.  With --gpus N > 1 (under torchrun) every rank
-routes its own batch (independent replicas, weak scaling); the timed region
-is bracketed by a barrier and the slowest rank's time is reported.  Unless
+Prints one JSON line on rank 0.  With --gpus N > 1 (under torchrun) the ranks
+hold one batch of N * T rows, T per rank (weak scaling), and run the
+data-parallel step: each routes its rows, the ranks all-gather their counts
+and P, combine them, dispatch with the whole batch's capacity and run the
+backward of the batch's loss (--parallelism replicas instead runs the fused
+single-launch step on every rank independently).  The timed region is
+bracketed by a barrier and the slowest rank's time is reported.  Unless
 --no-extra, the line also carries the other router workloads (`also`), the
 separate calls, the Sinkhorn plan, the bias-routing forward / full backward /
 bias-routed step (`next_steps`), the EPLB planner (`eplb`) and TAOT Phase 2
@@ -329,6 +334,65 @@ def time_e2e(w, steps: int, warmup: int, torch, device, dist_ctx) -> dict:
         if mr.moe_get_device_status(wss[b]):
             raise RuntimeError("device wait expired during the end-to-end benchmark")
     return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h, "steps": steps}
+
+
+def time_dp(w, steps: int, warmup: int, torch, device, dist_ctx, e2e: bool = False, sampler=None) -> dict:
+    """Device-timed data-parallel steps (dp.data_parallel_step): each rank routes
+    its own w.T rows of a batch of world * w.T rows (its logits a row rotation
+    of the workload's by the rank), exchanges counts and P in one all-gather,
+    combines them, dispatches with the whole batch's capacity and runs the
+    backward of the batch's loss.  Five library launches and one collective per
+    step, issued eagerly; the logits (201 MB at E = 384) exceed the L2.  With
+    e2e, every step also copies its logits from pinned host memory and every
+    output of the rank (idx, gate, perm, slot, offsets, kept, n_dropped,
+    dlogits and the batch's counts, f, P, scalars, rank loads) back to pinned
+    host memory."""
+    import moe_expert_routing_router_gb300 as mr
+    from moe_expert_routing_router_gb300 import dp
+    logits = np.roll(synth.router_logits(w), dist_ctx.rank * 97, axis=0)
+    x = to_device(logits, w.dtype, torch, device)
+    host_x = to_device(logits, w.dtype, torch, "cpu").pin_memory() if e2e else None
+    ws = mr.Workspace(device)
+    T_shard = [w.T] * dist_ctx.world
+    keys = ("idx", "gate", "perm", "slot", "offsets", "kept", "n_dropped", "dlogits", "counts", "f", "P",
+            "scalars", "rank_load")
+    host_out: dict = {}
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        if e2e:
+            x.copy_(host_x, non_blocking=True)
+        o = dp.data_parallel_step(x, w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks,
+                                  ws=ws, T_shard=T_shard)
+        if e2e:
+            for k in keys:
+                if k not in host_out:
+                    host_out[k] = torch.empty(o[k].shape, dtype=o[k].dtype, pin_memory=True)
+                host_out[k].copy_(o[k], non_blocking=True)
+        return o
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize(device)
+    if sampler is not None:
+        sampler.start()
+    dist_ctx.barrier()
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    dist_ctx.barrier()
+    clocks = sampler.stop() if sampler is not None else None
+    ms = dist_ctx.max(t0.elapsed_time(t1)) / steps
+    if mr.moe_get_device_status(ws):
+        raise RuntimeError("device wait expired during the data-parallel benchmark")
+    h2d = host_x.numel() * host_x.element_size() if e2e else 0
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values()) if e2e else 0
+    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h, "steps": steps, "clocks": clocks}
 
 
 def time_calls(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
@@ -677,6 +741,52 @@ def run_reference(args) -> dict:
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_dp(args, torch, dist_ctx, device, pk, w) -> dict:
+    """The data-parallel partition of one batch over the ranks (weak scaling: w.T
+    rows per rank), timed as dp.data_parallel_step."""
+    sampler = ClockSampler(dist_ctx.local)
+    r = time_dp(w, args.steps, args.warmup, torch, device, dist_ctx, sampler=sampler)
+    e = time_dp(w, max(5, min(args.steps, 50)), args.warmup, torch, device, dist_ctx, e2e=True)
+    ms = r["ms_per_step"]
+    step_bytes = algorithmic_bytes(w)
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    kernels = ("moe_router_fwd", "moe_router_combine", "moe_shard_capacity_base", "moe_dispatch_sharded",
+               "moe_router_bwd")
+    line = {
+        "metric": METRIC, "value": dist_ctx.world * w.T / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": dist_ctx.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w, {"parallelism": f"dp{dist_ctx.world}", "global_batch": dist_ctx.world * w.T,
+                                "l2": "each rank's logits exceed the 129 MB L2",
+                                "timing": f"{args.steps} eager data-parallel steps between two CUDA events, "
+                                          f"barrier and synchronize on both sides, slowest rank"}),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "the whole step per rank: " + ", ".join(kernels) + " and one all-gather",
+                     "algorithmic_bytes_per_launch": step_bytes, "peak_source": pk["source"]},
+        "e2e": {"value": dist_ctx.world * w.T / (e["ms_per_step"] * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e["ms_per_step"],
+                "steps": e["steps"],
+                "timing": "the data-parallel step on pinned host buffers: logits copied in and every output "
+                          "of the rank copied out each step"},
+        "gpu_launches": len(kernels) * args.steps,
+        "clocks": r["clocks"],
+    }
+    if dist_ctx.rank == 0:
+        cb = time_oracle(w, budget_s=args.cpu_seconds, min_steps=2)
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    return line
+
+
+def parallelism_of(choice: str, world: int) -> str:
+    """dp (one batch split over the ranks) by default with several ranks,
+    replicas (the fused step on every rank, or the single GPU) otherwise."""
+    par = choice if choice != "auto" else ("dp" if world > 1 else "replicas")
+    if par == "dp" and world < 2:
+        raise SystemExit("--parallelism dp needs at least two ranks (torchrun)")
+    return par
+
+
 def run_ours(args) -> dict:
     import torch
     dist_ctx = DistCtx(torch)
@@ -684,6 +794,10 @@ def run_ours(args) -> dict:
     torch.cuda.set_device(device)
     pk = peaks()
     w = synth.ROUTER_WORKLOADS[args.workload]
+    if parallelism_of(args.parallelism, dist_ctx.world) == "dp":
+        line = run_dp(args, torch, dist_ctx, device, pk, w)
+        dist_ctx.close()
+        return line if dist_ctx.rank == 0 else {}
     sampler = ClockSampler(dist_ctx.local)
     r = time_router(w, args.steps, args.warmup, torch, device, dist_ctx, soak_s=args.soak_seconds, sampler=sampler)
     ms_step = r["total_ms"] / args.steps
@@ -764,6 +878,9 @@ def main() -> int:
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="loaded window before the timed region, for the clock samples")
+    ap.add_argument("--parallelism", choices=("auto", "dp", "replicas"), default="auto",
+                    help="with N > 1 ranks: dp (default) splits one batch over the ranks (dp.data_parallel_step); "
+                         "replicas runs the fused step independently on every rank")
     ap.add_argument("--section", choices=("next_steps", "eplb", "taot_match"), default=None,
                     help="print only this part of the extra lines (for --workload), as JSON; no bench line")
     args = ap.parse_args()

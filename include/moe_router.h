@@ -190,6 +190,40 @@ MOE_API moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_
                         int32_t* n_dropped, int64_t* capacity_out,
                         void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Global capacity across data-parallel ranks.  The capacity of [P1] §4.5 is
+ * that of the whole batch, and a batch split over G data-parallel ranks (rank
+ * g holding the rows after those of ranks 0..g-1) is dispatched as if one
+ * call had taken all of it: an assignment's position in its expert's buffer
+ * counts the expert's assignments on the lower ranks first.
+ *
+ * moe_shard_capacity_base writes cap_base[e] = sum over ranks g < rank of
+ * counts[g][e] (summed in 64 bits, clamped to INT32_MAX): the exclusive scan
+ * across ranks of every expert's count.  counts [G,E] int32 device, the ranks'
+ * per-expert counts stacked in rank order (on a multi-GPU job the result of an
+ * all-gather of moe_router_fwd's counts); cap_base [E] int32 device.  G in
+ * [1,64], rank in [0,G).  One small launch, no workspace. */
+MOE_API moe_status moe_shard_capacity_base(const int32_t* counts, int32_t G, int32_t E, int32_t rank,
+                                   int32_t* cap_base, moe_stream_t stream);
+
+/* moe_dispatch of one rank's T rows of a batch of T_total rows, with the
+ * batch's capacity C = moe_dispatch_capacity(T_total, E, k, capacity_factor)
+ * and cap_base [E] (device) from moe_shard_capacity_base:
+ *   perm, offsets: as moe_dispatch, over this rank's assignments (local ids)
+ *   slot [T*k]:    cap_base[e] + r when that is below C, else -1, r the
+ *                  assignment's rank among this rank's assignments to e
+ *   kept [E]:      min(count_e, max(C - cap_base[e], 0)), count_e this rank's
+ *   n_dropped [1]: T*k - sum(kept)
+ * Over all ranks, the slots (concatenated in rank order) are moe_dispatch's
+ * slots of the whole batch, the kept sum to its kept, the n_dropped to its
+ * n_dropped.  Errors: T_total < T, T_total*k >= 2^31, cap_base NULL or not
+ * 4-byte aligned, and everything moe_dispatch rejects.  ws as for
+ * moe_router_fwd. */
+MOE_API moe_status moe_dispatch_sharded(const int32_t* idx, int64_t T, int32_t E, int32_t k, double capacity_factor,
+                                int64_t T_total, const int32_t* cap_base,
+                                int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                                int32_t* n_dropped, int64_t* capacity_out,
+                                void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Fused step: forward + dispatch + backward in one launch                  */
 /* ------------------------------------------------------------------------ */

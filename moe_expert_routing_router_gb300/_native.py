@@ -29,6 +29,9 @@ SIGNATURES = {
     "moe_router_bwd": (_i32, [_p, _i32, _i64, _i32, _f32, _p, _f32, _p, _p]),
     "moe_dispatch_capacity": (_i64, [_i64, _i32, _i32, _f64]),
     "moe_dispatch": (_i32, [_p, _i64, _i32, _i32, _f64, _p, _p, _p, _p, _p, C.POINTER(_i64), _p, _sz, _p]),
+    "moe_shard_capacity_base": (_i32, [_p, _i32, _i32, _i32, _p, _p]),
+    "moe_dispatch_sharded": (_i32, [_p, _i64, _i32, _i32, _f64, _i64, _p, _p, _p, _p, _p, _p, C.POINTER(_i64),
+                                    _p, _sz, _p]),
     "moe_router_step": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _i32, _i32, _f64, _f32,
                                _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_router_step_static": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _i32, _i32, _f64, _f32,

@@ -18,6 +18,7 @@ from ._native import MOE_DTYPE_BF16, MOE_DTYPE_FP32, MOE_NUM_SCALARS, SCALAR_NAM
 
 __all__ = [
     "Workspace", "moe_router_fwd", "moe_router_bwd", "moe_dispatch", "moe_dispatch_capacity",
+    "moe_shard_capacity_base", "moe_dispatch_sharded",
     "moe_router_step", "moe_router_step_static", "moe_router_fwd_ex", "moe_router_bwd_full", "moe_eplb_plan", "taot_match_batched", "moe_router_combine", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
 ]
 
@@ -253,6 +254,47 @@ def moe_dispatch(idx: torch.Tensor, E: int, capacity_factor: float, ws: Workspac
                             _ptr(o["offsets"]), _ptr(o["kept"]), _ptr(o["n_dropped"]), C.byref(cap),
                             wp, wn, _stream_handle(stream))
     check(st, "moe_dispatch")
+    o["capacity"] = int(cap.value)
+    return o
+
+
+def moe_shard_capacity_base(counts: torch.Tensor, rank: int, out: torch.Tensor | None = None,
+                            stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """cap_base [E] int32: every expert's assignments on the ranks below `rank`,
+    from the ranks' counts stacked [G, E] in rank order (C: moe_shard_capacity_base)."""
+    _need_cuda("counts", counts, torch.int32)
+    if counts.dim() != 2:
+        raise ValueError("counts must be [G, E]")
+    G, E = counts.shape
+    base = out if out is not None else torch.empty(E, dtype=torch.int32, device=counts.device)
+    _need_cuda("out", base, torch.int32)
+    if tuple(base.shape) != (E,):
+        raise ValueError("out must be [E]")
+    st = lib().moe_shard_capacity_base(_ptr(counts), G, E, int(rank), _ptr(base), _stream_handle(stream))
+    check(st, "moe_shard_capacity_base")
+    return base
+
+
+def moe_dispatch_sharded(idx: torch.Tensor, E: int, capacity_factor: float, T_total: int, cap_base: torch.Tensor,
+                         ws: Workspace | None = None, out: dict | None = None,
+                         stream: torch.cuda.Stream | None = None) -> dict:
+    """Dispatch of this rank's idx [T, k] with the capacity of the whole batch of
+    T_total rows and slots offset by cap_base [E] (C: moe_dispatch_sharded)."""
+    _need_cuda("idx", idx, torch.int32)
+    _need_cuda("cap_base", cap_base, torch.int32)
+    if idx.dim() != 2:
+        raise ValueError("idx must be [T, k]")
+    if tuple(cap_base.shape) != (E,):
+        raise ValueError("cap_base must be [E]")
+    T, k = idx.shape
+    o = _dispatch_outputs(T, E, k, idx.device, out)
+    ws = ws or _default_ws(idx.device, stream)
+    wp, wn = ws.ensure(T, E, k, stream)
+    cap = C.c_int64(0)
+    st = lib().moe_dispatch_sharded(_ptr(idx), T, E, k, float(capacity_factor), int(T_total), _ptr(cap_base),
+                                    _ptr(o["perm"]), _ptr(o["slot"]), _ptr(o["offsets"]), _ptr(o["kept"]),
+                                    _ptr(o["n_dropped"]), C.byref(cap), wp, wn, _stream_handle(stream))
+    check(st, "moe_dispatch_sharded")
     o["capacity"] = int(cap.value)
     return o
 

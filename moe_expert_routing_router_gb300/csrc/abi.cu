@@ -370,6 +370,53 @@ const moe::ExtVariant* pick_ext_variant(moe_dtype dt, int E, bool aligned16) {
 
 }  // namespace
 
+// moe_dispatch and moe_dispatch_sharded: the capacity is that of T_cap tokens
+// (the whole batch), cap_base null for a batch on one rank.
+static moe_status dispatch_impl(const int32_t* idx, int64_t T, int32_t E, int32_t k, double capacity_factor,
+                                int64_t T_cap, const int32_t* cap_base,
+                                int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                                int32_t* n_dropped, int64_t* capacity_out,
+                                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!idx) return fail(MOE_ERR_INVALID, "idx is NULL");
+  if (T < 1 || T >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T = %lld outside [1, 2^31)", (long long)T);
+  if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_INVALID, "E = %d outside [1, %d]", E, MOE_MAX_EXPERTS);
+  if (k < 1 || k > MOE_MAX_TOPK || k > E) return fail(MOE_ERR_INVALID, "k = %d outside [1, min(E, %d)]", k, MOE_MAX_TOPK);
+  if (T * (int64_t)k >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T*k does not fit int32");
+  if (!(capacity_factor > 0.0) || !std::isfinite(capacity_factor)) return fail(MOE_ERR_INVALID, "capacity_factor must be > 0");
+  if (!perm || !slot || !offsets || !kept || !n_dropped) return fail(MOE_ERR_INVALID, "a dispatch output is NULL");
+  moe_status s = check_ws(ws, ws_bytes, E);
+  if (s != MOE_OK) return s;
+  const int64_t C = capacity_of(T_cap, E, k, capacity_factor);
+  if (capacity_out) *capacity_out = C;
+  RouterParams p = base_params(nullptr, T, E, k);
+  p.idx_in = idx;
+  p.cap_base = cap_base;
+  p.C = int(std::min<int64_t>(C, INT32_MAX));
+  p.perm = perm; p.slot = slot; p.offsets = offsets; p.kept = kept; p.n_dropped = n_dropped;
+  bind_ws(p, ws, E);
+  DeviceInfo d;
+  int dev = 0;
+  if ((s = device_info(&d, &dev)) != MOE_OK) return s;
+  const void* func = moe::dispatch_kernel();
+  const int kb = int(sizeof(moe::Bf16::Key));                 // a bf16 instance
+  size_t smem = moe::router_smem_layout(E, kb, 0, 0).total;
+  int blocks = 0;
+  if ((s = occupancy(func, moe::kThreads, smem, dev, &blocks)) != MOE_OK) return s;
+  const int64_t cap = std::min<int64_t>(int64_t(blocks) * d.sms, kGridMax);
+  const int64_t want = (T * k + 2047) / 2048;
+  p.G = int(std::max<int64_t>(1, std::min(cap, want)));
+  p.n_groups = (p.G + moe::kGroupCtas - 1) / moe::kGroupCtas;
+  // each CTA's assignments (expert id, rank within the CTA) in shared memory when they fit
+  const int64_t asg = ((T * k + p.G - 1) / p.G + 7) / 8 * 8;
+  const size_t with = moe::router_smem_layout(E, kb, 0, 0, int(std::min<int64_t>(asg, INT32_MAX))).total;
+  if (asg <= kMaxAsgSmem && with <= kSmemPerSm - kSmemReservedPerCta) {
+    p.asg_cap = int(asg);
+    smem = with;
+  }
+  return launch_persistent(func, p, smem, stream);
+}
+
+
 extern "C" {
 
 size_t moe_router_workspace_size(int64_t T, int32_t E, int32_t k) {
@@ -476,42 +523,33 @@ moe_status moe_dispatch(const int32_t* idx, int64_t T, int32_t E, int32_t k, dou
                         int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
                         int32_t* n_dropped, int64_t* capacity_out,
                         void* ws, size_t ws_bytes, moe_stream_t stream) {
-  if (!idx) return fail(MOE_ERR_INVALID, "idx is NULL");
-  if (T < 1 || T >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T = %lld outside [1, 2^31)", (long long)T);
+  return dispatch_impl(idx, T, E, k, capacity_factor, T, nullptr, perm, slot, offsets, kept, n_dropped, capacity_out,
+                       ws, ws_bytes, stream);
+}
+
+moe_status moe_dispatch_sharded(const int32_t* idx, int64_t T, int32_t E, int32_t k, double capacity_factor,
+                                int64_t T_total, const int32_t* cap_base,
+                                int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                                int32_t* n_dropped, int64_t* capacity_out,
+                                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!cap_base) return fail(MOE_ERR_INVALID, "cap_base is NULL");
+  if (!aligned(cap_base, 4)) return fail(MOE_ERR_INVALID, "cap_base is not 4-byte aligned");
+  if (T_total < T) return fail(MOE_ERR_INVALID, "T_total = %lld is below this rank's T = %lld", (long long)T_total, (long long)T);
+  if (k >= 1 && T_total * (int64_t)k >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T_total*k does not fit int32");
+  return dispatch_impl(idx, T, E, k, capacity_factor, T_total, cap_base, perm, slot, offsets, kept, n_dropped,
+                       capacity_out, ws, ws_bytes, stream);
+}
+
+moe_status moe_shard_capacity_base(const int32_t* counts, int32_t G, int32_t E, int32_t rank, int32_t* cap_base,
+                                   moe_stream_t stream) {
+  if (!counts || !cap_base) return fail(MOE_ERR_INVALID, "counts or cap_base is NULL");
+  if (G < 1 || G > moe::kMaxShards) return fail(MOE_ERR_INVALID, "G = %d outside [1, %d]", G, moe::kMaxShards);
   if (E < 1 || E > MOE_MAX_EXPERTS) return fail(MOE_ERR_INVALID, "E = %d outside [1, %d]", E, MOE_MAX_EXPERTS);
-  if (k < 1 || k > MOE_MAX_TOPK || k > E) return fail(MOE_ERR_INVALID, "k = %d outside [1, min(E, %d)]", k, MOE_MAX_TOPK);
-  if (T * (int64_t)k >= (int64_t(1) << 31)) return fail(MOE_ERR_INVALID, "T*k does not fit int32");
-  if (!(capacity_factor > 0.0) || !std::isfinite(capacity_factor)) return fail(MOE_ERR_INVALID, "capacity_factor must be > 0");
-  if (!perm || !slot || !offsets || !kept || !n_dropped) return fail(MOE_ERR_INVALID, "a dispatch output is NULL");
-  moe_status s = check_ws(ws, ws_bytes, E);
-  if (s != MOE_OK) return s;
-  const int64_t C = capacity_of(T, E, k, capacity_factor);
-  if (capacity_out) *capacity_out = C;
-  RouterParams p = base_params(nullptr, T, E, k);
-  p.idx_in = idx;
-  p.C = int(std::min<int64_t>(C, INT32_MAX));
-  p.perm = perm; p.slot = slot; p.offsets = offsets; p.kept = kept; p.n_dropped = n_dropped;
-  bind_ws(p, ws, E);
-  DeviceInfo d;
-  int dev = 0;
-  if ((s = device_info(&d, &dev)) != MOE_OK) return s;
-  const void* func = moe::dispatch_kernel();
-  const int kb = int(sizeof(moe::Bf16::Key));                 // a bf16 instance
-  size_t smem = moe::router_smem_layout(E, kb, 0, 0).total;
-  int blocks = 0;
-  if ((s = occupancy(func, moe::kThreads, smem, dev, &blocks)) != MOE_OK) return s;
-  const int64_t cap = std::min<int64_t>(int64_t(blocks) * d.sms, kGridMax);
-  const int64_t want = (T * k + 2047) / 2048;
-  p.G = int(std::max<int64_t>(1, std::min(cap, want)));
-  p.n_groups = (p.G + moe::kGroupCtas - 1) / moe::kGroupCtas;
-  // each CTA's assignments (expert id, rank within the CTA) in shared memory when they fit
-  const int64_t asg = ((T * k + p.G - 1) / p.G + 7) / 8 * 8;
-  const size_t with = moe::router_smem_layout(E, kb, 0, 0, int(std::min<int64_t>(asg, INT32_MAX))).total;
-  if (asg <= kMaxAsgSmem && with <= kSmemPerSm - kSmemReservedPerCta) {
-    p.asg_cap = int(asg);
-    smem = with;
-  }
-  return launch_persistent(func, p, smem, stream);
+  if (rank < 0 || rank >= G) return fail(MOE_ERR_INVALID, "rank = %d outside [0, %d)", rank, G);
+  if (!aligned(counts, 4) || !aligned(cap_base, 4)) return fail(MOE_ERR_INVALID, "counts or cap_base is not 4-byte aligned");
+  cudaError_t e = moe::launch_shard_capacity_base(counts, G, E, rank, cap_base, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "shard_capacity_base launch");
+  return MOE_OK;
 }
 
 }  // extern "C"

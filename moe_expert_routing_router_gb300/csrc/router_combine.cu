@@ -1,5 +1,5 @@
-// The shard-combine kernel of the data-parallel statistics (declared in
-// router_ext.cuh).
+// The shard-combine kernel of the data-parallel statistics and the cross-rank
+// exclusive scan of the expert counts (both declared in router_ext.cuh).
 #include "router_ext.cuh"
 
 namespace moe {
@@ -35,7 +35,24 @@ __global__ void __launch_bounds__(256) router_combine_kernel(const CombineParams
   ext_outputs(q, s_cnt, s_pe);
 }
 
+// base[e] = sum over ranks g < rank of counts[g][e]: every expert's exclusive
+// scan across the data-parallel ranks, summed in 64 bits and clamped to int32.
+__global__ void __launch_bounds__(256) shard_capacity_base_kernel(const int32_t* counts, int G, int E, int rank,
+                                                                  int32_t* base) {
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+    long long c = 0;
+    for (int g = 0; g < rank && g < G; ++g) c += counts[(long long)g * E + e];
+    base[e] = int32_t(c < 0x7fffffffLL ? c : 0x7fffffffLL);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_shard_capacity_base(const int32_t* counts, int G, int E, int rank, int32_t* base,
+                                       cudaStream_t stream) {
+  shard_capacity_base_kernel<<<(E + 255) / 256, 256, 0, stream>>>(counts, G, E, rank, base);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_router_combine(const CombineParams& p, cudaStream_t stream) {
   router_combine_kernel<<<1, 256, 0, stream>>>(p);

@@ -378,6 +378,8 @@ struct CombineParams {
 };
 
 cudaError_t launch_router_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_shard_capacity_base(const int32_t* counts, int G, int E, int rank, int32_t* base,
+                                       cudaStream_t stream);
 
 template <class DT, int LPR, int VW, int NV>
 __global__ void __launch_bounds__(kExtFwdThreads, 2) router_fwd_ex_kernel(const FwdExParams p) {

@@ -99,6 +99,7 @@ struct RouterParams {
   int renorm;
   int n_ranks;
   int C;                       // expert capacity
+  const int32_t* cap_base;     // [E] assignments of each expert on lower data-parallel ranks, or null (none)
   float grad_scale;
   // outputs (null when the mode does not produce them)
   int32_t* idx;                // [T, k]
@@ -1323,6 +1324,15 @@ __device__ __forceinline__ void local_ranks(const int32_t* idx_src, long long a_
   }
 }
 
+// Slot of an assignment with rank r among this batch's assignments to expert
+// e: its position r + cap_base[e] in the expert's buffer when that is below
+// the capacity, else -1 (dropped).  cap_base (the expert's assignments on the
+// lower data-parallel ranks) is null for a batch on one rank.
+__device__ __forceinline__ int slot_of(const RouterParams& p, int e, int r) {
+  const int g = p.cap_base != nullptr ? r + __ldg(p.cap_base + e) : r;
+  return g < p.C ? g : -1;
+}
+
 // Final ranks from the parked in-CTA ranks: r = base[e] + local; perm and slot.
 __device__ __forceinline__ void dispatch_fixup(const RouterParams& p, const int32_t* idx_src, long long a0, long long a1,
                                                const int* off, const int* base) {
@@ -1343,7 +1353,7 @@ __device__ __forceinline__ void dispatch_fixup(const RouterParams& p, const int3
       const int r = base[e] + l_[j];
       if (a < a1 && r >= 0 && r < off[e + 1] - off[e]) {   // always true for consistent ranks
         p.perm[off[e] + r] = int(a);
-        p.slot[a] = r < p.C ? r : -1;
+        p.slot[a] = slot_of(p, e, r);
       }
     }
   }
@@ -1380,7 +1390,7 @@ __device__ __forceinline__ void dispatch_fixup_smem(const RouterParams& p, long 
     const long long a = a0 + i;
     if (r >= 0 && r < off[e + 1] - off[e]) {                // always true for consistent ranks
       p.perm[off[e] + r] = int(a);
-      p.slot[a] = r < p.C ? r : -1;
+      p.slot[a] = slot_of(p, e, r);
     }
   }
 }
@@ -1398,7 +1408,7 @@ __device__ __forceinline__ void dispatch_direct(const RouterParams& p, const int
     const int r = p.slot[a];
     if (r >= 0 && r < off[e + 1] - off[e]) {                // always true for consistent ranks
       p.perm[off[e] + r] = int(a);
-      p.slot[a] = r < p.C ? r : -1;
+      p.slot[a] = slot_of(p, e, r);
     }
   }
 }
@@ -1459,8 +1469,10 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
       if (e < E) {
         s_cnt[e] = c[j];
         if constexpr (kDisp) {
-          p.kept[e] = min(c[j], p.C);
-          dropped += max(c[j] - p.C, 0);
+          const int lower = p.cap_base != nullptr ? __ldg(p.cap_base + e) : 0;
+          const int kept = min(c[j], max(p.C - lower, 0));
+          p.kept[e] = kept;
+          dropped += c[j] - kept;
         }
         if constexpr (kFwd) {
           fp = fmaf(fv[j], pv[j], fp);
@@ -2029,7 +2041,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           const int r = s_cbase[e] + s_wcnt[e] + loc_[j];
           if (a < hi && r >= 0 && r < s_coff[e + 1] - s_coff[e]) {   // always true for consistent ranks
             p.perm[s_coff[e] + r] = int(a);
-            p.slot[a] = r < p.C ? r : -1;
+            p.slot[a] = slot_of(p, e, r);
           }
         }
       }

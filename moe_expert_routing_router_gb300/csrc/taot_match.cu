@@ -252,17 +252,23 @@ __global__ void __launch_bounds__(kMatchThreads) taot_match_kernel(const MatchPa
     }
     __syncthreads();
     // Per-rank choice over a quarter of the home ranks: warp w takes cold ranks
-    // 32 (w & 1) + lane and home ranks [hq (w >> 1), hq (w >> 1 + 1)).
+    // 32 (w & 1) + lane and the hot ones among home ranks
+    // [hq (w >> 1), hq (w >> 1 + 1)) (a home rank that is not hot has no entry).
     {
       const int c = (warp & 1) * 32 + lane, part = warp >> 1;
+      const unsigned hot_lo = __ballot_sync(0xffffffffu, lane < R && s.load[lane] * R > total);
+      const unsigned hot_hi = __ballot_sync(0xffffffffu, lane + 32 < R && s.load[lane + 32] * R > total);
+      const int h0 = part * hq, h1 = (part + 1) * hq < R ? (part + 1) * hq : R;
+      unsigned long long m = ((unsigned long long)hot_hi << 32) | hot_lo;
+      m &= (h1 == 64 ? ~0ull : (1ull << h1) - 1ull) & ~((1ull << h0) - 1ull);
+      uint32_t k1 = 0u, f1 = 0u;
+      int e1 = 0x7fffffff;
+      for (; m != 0ull; m &= m - 1ull) {
+        const int h = __ffsll((long long)m) - 1;
+        const uint32_t k = c < R ? s.bk[tab(h, c)] : 0u;
+        if (k != 0u && k >= k1) better(k, s.fimg[h * R + c], s.be[tab(h, c)], k1, f1, e1);
+      }
       if (c < R) {
-        uint32_t k1 = 0u, f1 = 0u;
-        int e1 = 0x7fffffff;
-        const int h1 = (part + 1) * hq < R ? (part + 1) * hq : R;
-        for (int h = part * hq; h < h1; ++h) {
-          const uint32_t k = s.bk[tab(h, c)];
-          if (k != 0u && k >= k1) better(k, s.fimg[h * R + c], s.be[tab(h, c)], k1, f1, e1);
-        }
         s.pk[part * R + c] = k1;
         s.pf[part * R + c] = f1;
         s.pe[part * R + c] = e1;

@@ -110,6 +110,25 @@ def test_dispatch_and_step_reject_bad_arguments(native_lib):
     assert s(*bad) == 1
 
 
+def test_sharded_dispatch_rejects_bad_arguments(native_lib):
+    cap = C.c_int64(0)
+    d = native_lib.moe_dispatch_sharded
+    args = [FAKE, 16, 8, 2, 1.0, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, C.byref(cap), FAKE, 1 << 30, None]
+    for pos, val in [(6, None), (6, FAKE + 2), (5, 15), (5, 2 ** 30), (4, 0.0), (7, None), (0, None), (2, 0)]:
+        bad = list(args)
+        bad[pos] = val
+        assert d(*bad) == 1, (pos, val)
+    bad = list(args)
+    bad[14] = 8                                       # workspace too small
+    assert d(*bad) == 5
+    b = native_lib.moe_shard_capacity_base
+    args = [FAKE, 4, 8, 1, FAKE, None]
+    for pos, val in [(0, None), (4, None), (1, 0), (1, 65), (2, 0), (2, 1025), (3, -1), (3, 4), (4, FAKE + 2)]:
+        bad = list(args)
+        bad[pos] = val
+        assert b(*bad) == 1, (pos, val)
+
+
 def test_bwd_and_sinkhorn_reject_bad_arguments(native_lib):
     b = native_lib.moe_router_bwd
     assert b(FAKE, 1, 16, 8, 0.01, None, 1.0, FAKE, None) == 1

@@ -1,7 +1,7 @@
 """Host logic of bench.py under torch.distributed, as two gloo ranks on the CPU.
 
-Each rank times its own replica (weak scaling); the job's time is the maximum
-over ranks, and only rank 0 prints.  These tests run that logic without a GPU.
+With several ranks the job's time is the maximum over ranks and only rank 0
+prints; the ranks split one batch (dp) unless replicas are asked for.  These tests run that logic without a GPU.
 """
 
 from __future__ import annotations
@@ -87,3 +87,16 @@ def test_single_process_context():
 
 if __name__ == "__main__":
     sys.exit(pytest.main([__file__, "-q"]))
+
+
+def test_parallelism_choice():
+    """Several ranks split one batch (dp) unless replicas are asked for; one GPU
+    runs the fused step, and dp on one rank is refused."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    assert bench.parallelism_of("auto", 1) == "replicas"
+    assert bench.parallelism_of("auto", 4) == "dp"
+    assert bench.parallelism_of("replicas", 8) == "replicas"
+    assert bench.parallelism_of("dp", 2) == "dp"
+    with pytest.raises(SystemExit):
+        bench.parallelism_of("dp", 1)

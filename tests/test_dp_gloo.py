@@ -40,7 +40,15 @@ def _rank_main(rank: int, world: int, port: int, out) -> None:
     try:
         counts, P, T = _shard(rank)
         c_all, p_all, t_all = dp.gather_shard_stats(torch.from_numpy(counts), torch.from_numpy(P), T)
-        out.put((rank, c_all.numpy(), p_all.numpy(), t_all))
+        known = [_shard(r)[2] for r in range(world)]
+        c2, p2, t2 = dp.gather_shard_stats(torch.from_numpy(counts), torch.from_numpy(P), T, T_shard=known)
+        same = (torch.equal(c2, c_all) and torch.equal(p2.view(torch.int32), p_all.view(torch.int32)) and t2 == t_all)
+        try:
+            dp.gather_shard_stats(torch.from_numpy(counts), torch.from_numpy(P), T, T_shard=known[::-1])
+            rejected = False
+        except ValueError:
+            rejected = True
+        out.put((rank, c_all.numpy(), p_all.numpy(), t_all, same, rejected))
     finally:
         dist.destroy_process_group()
 
@@ -57,7 +65,8 @@ def test_gather_shard_stats_gloo():
         p.join(timeout=60)
     assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
     want = [_shard(r) for r in range(world)]
-    for rank, c_all, p_all, t_all in got:
+    for rank, c_all, p_all, t_all, same, rejected in got:
+        assert same and rejected
         assert c_all.shape == (world, E) and c_all.dtype == np.int32
         for r in range(world):
             assert np.array_equal(c_all[r], want[r][0])
@@ -71,3 +80,74 @@ def test_shard_grad_scale():
     # alpha*E/T_local * g * T_local/T_total = alpha*E/T_total * g
     assert dp.shard_grad_scale(2.0, 300, 1200) == 0.5
     assert dp.shard_grad_scale(1.0, 4096, 4096) == 1.0
+
+
+# Global-capacity dispatch over two gloo ranks.  The exchange and the choice of
+# rank and batch size are dp's host logic; the two kernel calls are replaced by
+# stand-ins built from the oracle (cap_base = the counts of the lower ranks;
+# slot = cap_base + the rank-local order, dropped at the batch's capacity), so
+# that a wrong rank, rank order or token count changes the slots.
+E_D, K_D, CF_D = 7, 2, 0.8
+
+
+def _dispatch_shard(rank: int):
+    rng = np.random.default_rng(300 + rank)
+    T = 90 + 41 * rank
+    idx = np.stack([rng.choice(E_D, size=K_D, replace=False) for _ in range(T)]).astype(np.int32)
+    return idx
+
+
+def _rank_dispatch_main(rank: int, world: int, port: int, out) -> None:
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, str(ROOT))
+    import torch.distributed as dist
+    import oracle
+    from moe_expert_routing_router_gb300 import dp
+
+    def fake_base(counts, r, out=None, stream=None):
+        c = counts.numpy()
+        return torch.from_numpy(c[:r].sum(axis=0).astype(np.int32))
+
+    def fake_dispatch(idx, E, cf, T_total, base, ws=None, out=None, stream=None):
+        i = idx.numpy()
+        C = oracle.dispatch.capacity(int(T_total), i.shape[1], E, cf)
+        local = oracle.dispatch.dispatch(i, E, 10 ** 9)["slot"]
+        g = base.numpy()[i.ravel()] + local
+        return {"slot": np.where(g < C, g, -1), "capacity": C}
+
+    dp.api.moe_shard_capacity_base = fake_base
+    dp.api.moe_dispatch_sharded = fake_dispatch
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        idx = _dispatch_shard(rank)
+        counts = torch.from_numpy(np.bincount(idx.ravel(), minlength=E_D).astype(np.int32))
+        c_all, _, T_shard = dp.gather_shard_stats(counts, torch.zeros(E_D), idx.shape[0])
+        batch = {"counts_all": c_all, "rank": dist.get_rank(), "T_total": sum(T_shard)}
+        got = dp.data_parallel_dispatch(torch.from_numpy(idx), batch, E_D, CF_D)
+        out.put((rank, got["slot"], got["cap_base"].numpy(), got["capacity"]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_global_capacity_dispatch_gloo():
+    sys.path.insert(0, str(ROOT))
+    import oracle
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    world, port = 2, _free_port()
+    procs = [ctx.Process(target=_rank_dispatch_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = sorted((q.get(timeout=120) for _ in range(world)), key=lambda x: x[0])
+    for p in procs:
+        p.join(timeout=60)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    shards = [_dispatch_shard(r) for r in range(world)]
+    whole_idx = np.concatenate(shards)
+    C = oracle.dispatch.capacity(whole_idx.shape[0], K_D, E_D, CF_D)
+    whole = oracle.dispatch.dispatch(whole_idx, E_D, C)
+    assert all(g[3] == C for g in got)
+    assert np.array_equal(got[0][2], np.zeros(E_D, np.int32))
+    assert np.array_equal(got[1][2], np.bincount(shards[0].ravel(), minlength=E_D))
+    assert np.array_equal(np.concatenate([g[1] for g in got]), whole["slot"])
+    assert (whole["slot"] < 0).any() and (whole["slot"] >= 0).any()    # the capacity binds

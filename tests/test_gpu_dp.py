@@ -84,3 +84,93 @@ def test_sharded_masked_p_and_bias(mr, masked):
     assert_equal("counts", got["counts"].cpu().numpy(), whole["counts"].cpu().numpy())
     for key in ("f", "P", "scalars"):
         assert_close(key, got[key].cpu().numpy(), whole[key].cpu().numpy().astype(np.float64), 2 * RTOL)
+
+
+def _global_dispatch_case(mr, name: str, cuts, cf: float):
+    """Routes the shards [cuts[s], cuts[s+1]) of one batch separately, takes each
+    shard's cap_base from the stacked counts and dispatches it with the batch's
+    capacity; checks everything against one oracle dispatch of the whole batch."""
+    w, logits = workload_inputs(name, int(cuts[-1]))
+    G = len(cuts) - 1
+    x = to_device(logits, w.dtype)
+    want = oracle_forward(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks)
+    C = oracle.dispatch.capacity(w.T, w.k, w.E, cf)
+    whole = oracle.dispatch.dispatch(want["idx"], w.E, C)
+    outs = [mr.moe_router_fwd(x[cuts[s]:cuts[s + 1]], w.k, w.alpha, renorm=int(w.renorm)) for s in range(G)]
+    stacked = torch.stack([o["counts"] for o in outs])
+    for s in range(G):
+        a, b = int(cuts[s]), int(cuts[s + 1])
+        idx_ref = want["idx"][a:b]
+        base = mr.moe_shard_capacity_base(stacked, s)
+        got = mr.moe_dispatch_sharded(outs[s]["idx"], w.E, cf, w.T, base)
+        torch.cuda.synchronize()
+        assert_equal(f"shard {s} idx", outs[s]["idx"].cpu().numpy(), idx_ref)
+        lower = np.bincount(want["idx"][:a].ravel(), minlength=w.E) if a > 0 else np.zeros(w.E, np.int64)
+        assert_equal(f"shard {s} cap_base", base.cpu().numpy(), lower)
+        local = oracle.dispatch.dispatch(idx_ref, w.E, C)
+        assert_equal(f"shard {s} perm", got["perm"].cpu().numpy(), local["perm"])
+        assert_equal(f"shard {s} offsets", got["offsets"].cpu().numpy(), local["offsets"])
+        slot_ref = whole["slot"][a * w.k:b * w.k]
+        assert_equal(f"shard {s} slot", got["slot"].cpu().numpy(), slot_ref)
+        kept_ref = np.bincount(idx_ref.ravel()[slot_ref >= 0], minlength=w.E)
+        assert_equal(f"shard {s} kept", got["kept"].cpu().numpy(), kept_ref)
+        assert int(got["n_dropped"].item()) == int((slot_ref < 0).sum())
+        assert got["capacity"] == C
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+@pytest.mark.parametrize("G", [2, 3, 8])
+@pytest.mark.parametrize("cf", [0.5, 1.25])
+def test_global_capacity_dispatch(mr, name, G, cf):
+    """Dispatch with the capacity of the whole batch across G emulated ranks: the
+    ranks' slots, concatenated in rank order, are one dispatch's slots of the
+    whole batch, bit for bit; each rank's perm and offsets are its own."""
+    T = 20011 if large(name) else synth.ROUTER_WORKLOADS[name].T
+    cuts = np.linspace(0, T, G + 1).astype(int)
+    cuts[1] -= 7                                          # ranks of unequal size
+    _global_dispatch_case(mr, name, cuts, cf)
+
+
+def test_global_capacity_dispatch_edges(mr):
+    """A rank of one row; a second rank that finds most experts' buffers already
+    filled by the first (a capacity of 7 per expert); a single rank."""
+    name = "zipf-top2-T65536-E64"
+    _global_dispatch_case(mr, name, [0, 1, 2, 5000], 1.0)
+    _global_dispatch_case(mr, name, [0, 4000, 4100], 0.05)
+    _global_dispatch_case(mr, name, [0, 3001], 1.25)
+
+
+def test_data_parallel_step_single_rank(mr):
+    """dp.data_parallel_step end to end in a one-rank gloo group: the exchange
+    degenerates to the rank's own statistics, so routing, counts and the
+    dispatch with cap_base = 0 must equal the oracle's whole-batch results bit
+    for bit, and f, P, the scalars and the gradient match within tolerance."""
+    import os
+    import socket
+    import torch.distributed as dist
+    from moe_expert_routing_router_gb300 import dp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=0, world_size=1)
+    try:
+        w, logits = workload_inputs("zipf-top2-T65536-E64", 30011)
+        x = to_device(logits, w.dtype)
+        got = dp.data_parallel_step(x, w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    want = oracle_forward(logits, w.dtype, w.k, w.alpha, w.renorm, w.n_ranks)
+    C = oracle.dispatch.capacity(w.T, w.k, w.E, w.capacity_factor)
+    disp = oracle.dispatch.dispatch(want["idx"], w.E, C)
+    assert_equal("idx", got["idx"].cpu().numpy(), want["idx"])
+    assert_equal("counts", got["counts"].cpu().numpy(), want["counts"])
+    assert_equal("cap_base", got["cap_base"].cpu().numpy(), np.zeros(w.E, np.int64))
+    for key in ("perm", "slot", "offsets", "kept"):
+        assert_equal(key, got[key].cpu().numpy(), disp[key])
+    assert int(got["n_dropped"].item()) == disp["n_dropped"]
+    assert got["capacity"] == C
+    assert_close("f", got["f"].cpu().numpy(), want["f"], RTOL)
+    assert_close("P", got["P"].cpu().numpy(), want["P"], RTOL, FLT_MIN)
+    check_backward(got["dlogits"], logits, w.dtype, want["f"].astype(np.float32).astype(np.float64), w.alpha, 1.0)
