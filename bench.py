@@ -471,8 +471,8 @@ def _graph_us(torch, device, call, reps: int) -> float:
 def time_next_steps(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     """The method's next steps through the C ABI: the forward with bias routing
     and the in-place bias update, the forward with masked P, the full backward
-    through the gates, and a bias-routed training step (fwd_ex + dispatch +
-    bwd_full).  Each is a CUDA graph of `reps` calls over buffer sets rotated
+    through the gates, and a bias-routed training step, as three calls (fwd_ex
+    + dispatch + bwd_full) and as one launch (moe_router_step_ex).  Each is a CUDA graph of `reps` calls over buffer sets rotated
     at least 3x L2 apart, with its algorithmic bytes per call."""
     import moe_expert_routing_router_gb300 as mr
     esize = 2 if w.dtype == "bf16" else 4
@@ -517,11 +517,18 @@ def time_next_steps(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
         mr.moe_router_bwd_full(xs[j], o["f"], w.alpha, 1.0, idx=o["idx"], dgate=dgates[j],
                                renorm=int(w.renorm), dlogits=bufs[j]["dlogits"])
 
+    def step_one(i):
+        j = i % n_sets
+        mr.moe_router_step_ex(xs[j], k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks,
+                              bias=bias, bias_gamma=1e-3, bias_out=bias, dgate=dgates[j], ws=ws,
+                              out={**fo(j), **do(j), "dlogits": bufs[j]["dlogits"]})
+
     out = {"workload": w.name}
     for name, fn, b in (("moe_router_fwd_ex (bias routing + update)", fwd_bias, fwd_b),
                         ("moe_router_fwd_ex (masked P)", fwd_masked, fwd_b),
                         ("moe_router_bwd_full (gates + aux)", bwd_full, bwd_b),
-                        ("bias-routed step (fwd_ex + dispatch + bwd_full)", step, step_b)):
+                        ("bias-routed step (fwd_ex + dispatch + bwd_full)", step, step_b),
+                        ("bias-routed step in one launch (moe_router_step_ex)", step_one, step_b)):
         us = _graph_us(torch, device, fn, reps)
         gbs = b / (us * 1e-6) / 1e9
         out[name] = {"us_per_call": round(us, 2), "tokens_per_s": round(T / (us * 1e-6), 1),

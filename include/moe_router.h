@@ -247,6 +247,37 @@ MOE_API moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, 
                            int32_t* n_dropped, float* dlogits,
                            void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* The extended training step in one launch: the outputs of moe_router_fwd_ex
+ * (bias routing with the bias update, masked P), then moe_dispatch on its idx,
+ * then moe_router_bwd_full with its f and the given upstream gradient of the
+ * gates, computed by one persistent cooperative kernel:
+ *   - selection on s = fp32(z) + bias_e ([P1] §4.3: the bias moves the choice
+ *     of experts only); softmax, gates and P from the unbiased z; bias NULL
+ *     means zero bias;
+ *   - masked_p != 0: P_i = (1/(T*k)) sum_t p[t,i] [i picked by t] ([P2] §3.1)
+ *     in P, the balance and L_aux, and in the gradient of the aux loss;
+ *   - bias_out != NULL: bias_out[e] = bias[e] + bias_gamma * sign(T*k/E -
+ *     counts[e]) in fp32 (sign(0) = 0); bias_out may alias bias;
+ *   - dlogits = dL/dlogits of L = sum_{t,j} dgate[t,j] * gate[t,j] +
+ *     grad_scale * L_aux, the picks and f held fixed; dgate [T,k] fp32 may be
+ *     NULL (the aux loss alone).
+ * The other arguments, the outputs and the workspace are those of
+ * moe_router_step.  idx, counts, perm, slot, offsets, kept, n_dropped and
+ * bias_out are bit-identical to the three separate calls'; gate, f, P, the
+ * scalars and dlogits agree within fp32 rounding (the separate forward sums p
+ * in fixed point, this step in fp32 per CTA).  Errors: those of
+ * moe_router_step, and INVALID for a bias, bias_out or dgate that is not
+ * 4-byte aligned or a non-finite bias_gamma with bias_out given. */
+MOE_API moe_status moe_router_step_ex(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                              float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
+                              float grad_scale, const float* bias, float bias_gamma, float* bias_out,
+                              int32_t masked_p, const float* dgate,
+                              int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                              float* scalars, int32_t* rank_load,
+                              int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                              int32_t* n_dropped, float* dlogits,
+                              void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* moe_router_step for inputs and outputs in HOST memory.
  *
  * One call queues, on `stream`: the copy of the logits from host memory into

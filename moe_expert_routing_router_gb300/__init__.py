@@ -19,6 +19,7 @@ from .api import (  # noqa: F401
     moe_router_fwd_ex,
     moe_router_bwd_full,
     moe_router_step,
+    moe_router_step_ex,
     moe_router_step_host,
     moe_router_step_host_device_size,
     moe_router_step_static,
@@ -30,5 +31,5 @@ from .api import (  # noqa: F401
 
 __all__ = [
     "SCALAR_NAMES", "Workspace", "moe_dispatch", "moe_dispatch_capacity", "moe_dispatch_sharded", "moe_eplb_plan", "moe_get_device_status",
-    "moe_router_bwd", "moe_router_bwd_full", "moe_router_combine", "moe_router_fwd", "moe_router_fwd_ex", "moe_router_step", "moe_router_step_host", "moe_router_step_host_device_size", "host_step_outputs", "moe_router_step_static", "moe_shard_capacity_base", "taot_match_batched", "taot_sinkhorn_batched",
+    "moe_router_bwd", "moe_router_bwd_full", "moe_router_combine", "moe_router_fwd", "moe_router_fwd_ex", "moe_router_step", "moe_router_step_ex", "moe_router_step_host", "moe_router_step_host_device_size", "host_step_outputs", "moe_router_step_static", "moe_shard_capacity_base", "taot_match_batched", "taot_sinkhorn_batched",
 ]

@@ -34,6 +34,8 @@ SIGNATURES = {
                                     _p, _sz, _p]),
     "moe_router_step": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _i32, _i32, _f64, _f32,
                                _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_router_step_ex": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _i32, _i32, _f64, _f32, _p, _f32, _p, _i32, _p,
+                                  _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_router_step_static": (_i32, [_p, _i32, _i64, _i32, _i32, _f32, _i32, _i32, _f64, _f32,
                                       _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
     "moe_router_step_host_device_size": (_sz, [_i32, _i64, _i32, _i32, _i32]),

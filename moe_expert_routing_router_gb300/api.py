@@ -18,7 +18,7 @@ from ._native import MOE_DTYPE_BF16, MOE_DTYPE_FP32, MOE_NUM_SCALARS, SCALAR_NAM
 
 __all__ = [
     "Workspace", "moe_router_fwd", "moe_router_bwd", "moe_dispatch", "moe_dispatch_capacity",
-    "moe_shard_capacity_base", "moe_dispatch_sharded",
+    "moe_shard_capacity_base", "moe_dispatch_sharded", "moe_router_step_ex",
     "moe_router_step", "moe_router_step_static", "moe_router_fwd_ex", "moe_router_bwd_full", "moe_eplb_plan", "taot_match_batched", "moe_router_combine", "taot_sinkhorn_batched", "moe_get_device_status", "SCALAR_NAMES",
 ]
 
@@ -321,6 +321,55 @@ def moe_router_step(logits: torch.Tensor, k: int, alpha: float, capacity_factor:
                                _ptr(o["n_dropped"]), _ptr(o["dlogits"]), wp, wn, _stream_handle(stream))
     check(st, "moe_router_step")
     o["capacity"] = moe_dispatch_capacity(T, E, k, capacity_factor)
+    return o
+
+
+def moe_router_step_ex(logits: torch.Tensor, k: int, alpha: float, capacity_factor: float, renorm: int = -1,
+                       n_ranks: int = 0, grad_scale: float = 1.0, bias: torch.Tensor | None = None,
+                       bias_gamma: float = 0.0, bias_out: torch.Tensor | bool | None = None, masked_p: bool = False,
+                       dgate: torch.Tensor | None = None, ws: Workspace | None = None, out: dict | None = None,
+                       stream: torch.cuda.Stream | None = None) -> dict:
+    """The extended step in one launch: bias routing with its update and masked
+    P in the forward, dispatch, and the backward of the gates' upstream
+    gradient dgate [T, k] added to the aux loss's (C: moe_router_step_ex).
+    ``bias`` / ``bias_out`` as for moe_router_fwd_ex."""
+    _need_cuda("logits", logits)
+    if logits.dtype not in _DTYPES or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D float32 or bfloat16 tensor")
+    T, E = logits.shape
+    dev = logits.device
+    if bias is not None:
+        _need_cuda("bias", bias, torch.float32)
+        if bias.numel() != E:
+            raise ValueError("bias must have E elements")
+    if bias_out is True:
+        bias_out = torch.empty(E, dtype=torch.float32, device=dev)
+    elif bias_out is False:
+        bias_out = None
+    if bias_out is not None:
+        _need_cuda("bias_out", bias_out, torch.float32)
+        if bias_out.numel() != E:
+            raise ValueError("bias_out must have E elements")
+    if dgate is not None:
+        _need_cuda("dgate", dgate, torch.float32)
+        if tuple(dgate.shape) != (T, k):
+            raise ValueError("dgate must be [T, k]")
+    o = _fwd_outputs(T, E, k, n_ranks, dev, out)
+    o.update(_dispatch_outputs(T, E, k, dev, out))
+    o["dlogits"] = _out(out, "dlogits", (T, E), torch.float32, dev)
+    ws = ws or _default_ws(dev, stream)
+    wp, wn = ws.ensure(T, E, k, stream)
+    st = lib().moe_router_step_ex(_ptr(logits), _DTYPES[logits.dtype], T, E, k, float(alpha), int(renorm),
+                                  int(n_ranks), float(capacity_factor), float(grad_scale), _ptr(bias),
+                                  float(bias_gamma), _ptr(bias_out), int(bool(masked_p)), _ptr(dgate),
+                                  _ptr(o["idx"]), _ptr(o["gate"]), _ptr(o["counts"]), _ptr(o["f"]), _ptr(o["P"]),
+                                  _ptr(o["scalars"]), _ptr(o["rank_load"]) if n_ranks > 0 else None,
+                                  _ptr(o["perm"]), _ptr(o["slot"]), _ptr(o["offsets"]), _ptr(o["kept"]),
+                                  _ptr(o["n_dropped"]), _ptr(o["dlogits"]), wp, wn, _stream_handle(stream))
+    check(st, "moe_router_step_ex")
+    o["capacity"] = moe_dispatch_capacity(T, E, k, capacity_factor)
+    if bias_out is not None:
+        o["bias_out"] = bias_out
     return o
 
 

@@ -24,6 +24,8 @@ LIBNAME = "libmoerouter.so"
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 SOURCES = ["router_bf16_staged.cu", "router_bf16_direct.cu", "router_fp32_staged.cu", "router_fp32_direct.cu",
+           "router_step_ext_bf16_staged.cu", "router_step_ext_bf16_direct.cu", "router_step_ext_fp32_staged.cu",
+           "router_step_ext_fp32_direct.cu",
            "router_dispatch.cu", "router_ext_bf16.cu", "router_ext_fp32.cu", "router_combine.cu", "sinkhorn.cu", "taot_match.cu", "eplb.cu", "abi.cu"]
 
 

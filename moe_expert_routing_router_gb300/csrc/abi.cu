@@ -179,6 +179,19 @@ const RouterVariant* pick_variant(moe_dtype dt, int E, bool aligned16) {
   return best;
 }
 
+// The extended step's kernel of a plain variant (the same row layout), or null.
+const void* step_ext_kernel(moe_dtype dt, const RouterVariant* v) {
+  int n = 0;
+  const moe::StepExtVariant* t =
+      dt == MOE_DTYPE_BF16 ? (v->staged ? moe::step_ext_bf16_staged(&n) : moe::step_ext_bf16_direct(&n))
+                           : (v->staged ? moe::step_ext_fp32_staged(&n) : moe::step_ext_fp32_direct(&n));
+  for (int i = 0; i < n; ++i)
+    if (t[i].LPR == v->LPR && t[i].VW == v->VW && t[i].NV == v->NV && t[i].NR == v->NR &&
+        t[i].min_blocks == v->min_blocks)
+      return t[i].step_ext;
+  return nullptr;
+}
+
 moe_status check_router_args(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k) {
   if (dt != MOE_DTYPE_FP32 && dt != MOE_DTYPE_BF16) return fail(MOE_ERR_UNSUPPORTED, "dtype %d is not fp32 (0) or bf16 (1)", int(dt));
   if (!logits) return fail(MOE_ERR_INVALID, "logits is NULL");
@@ -236,14 +249,17 @@ constexpr int kMaxRowStats = 4096;             // rows per CTA whose softmax sta
 // fused: the launch runs the fused step (forward, dispatch and backward), whose
 // CTAs keep their dispatch and the rows' softmax statistics in shared memory
 // when these fit beside at least two ring slots.
+// ext: the extended step's kernel of the variant (its pick slots hold 64-bit
+// keys and its occupancy sets the grid), or null for the plain kernels.
 moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, int E, int k, bool fused,
-                               Geometry* out) {
+                               Geometry* out, const void* ext = nullptr) {
   DeviceInfo d;
   int dev = 0;
   moe_status s = device_info(&d, &dev);
   if (s != MOE_OK) return s;
   const int esize = dt == MOE_DTYPE_BF16 ? 2 : 4;
-  const int kb = dt == MOE_DTYPE_BF16 ? int(sizeof(moe::Bf16::Key)) : int(sizeof(moe::Fp32::Key));
+  const int kb = ext != nullptr ? int(sizeof(long long))
+                 : dt == MOE_DTYPE_BF16 ? int(sizeof(moe::Bf16::Key)) : int(sizeof(moe::Fp32::Key));
   const int group_rows = moe::kConsumerWarps * (moe::kWarp / v->LPR) * v->NR;
   Geometry g;
   const size_t fixed = moe::router_smem_layout(E, kb, 0, 0).total;
@@ -257,9 +273,14 @@ moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, 
   }
   size_t smem = moe::router_smem_layout(E, kb, g.n_slots, int(stage_bytes)).total;
   int bf = 0, bs = 0;
-  if ((s = occupancy(v->fwd, moe::kThreads, smem, dev, &bf)) != MOE_OK) return s;
-  if ((s = occupancy(v->step, moe::kThreads, smem, dev, &bs)) != MOE_OK) return s;
-  if (v->step_split != nullptr) {
+  if (ext != nullptr) {
+    if ((s = occupancy(ext, moe::kThreads, smem, dev, &bs)) != MOE_OK) return s;
+    bf = bs;
+  } else {
+    if ((s = occupancy(v->fwd, moe::kThreads, smem, dev, &bf)) != MOE_OK) return s;
+    if ((s = occupancy(v->step, moe::kThreads, smem, dev, &bs)) != MOE_OK) return s;
+  }
+  if (ext == nullptr && v->step_split != nullptr) {
     int bss = 0;
     if ((s = occupancy(v->step_split, moe::kThreads, smem, dev, &bss)) != MOE_OK) return s;
     bs = std::min(bs, bss);
@@ -614,6 +635,52 @@ moe_status moe_router_step(const void* logits, moe_dtype dt, int64_t T, int32_t 
   const bool split = p.renorm != 0 && v->step_split != nullptr &&
                      ring_bytes >= size_t(moe::kConsumerWarps) * size_t(E) * sizeof(float);
   return launch_persistent(split ? v->step_split : v->step, p, geo.smem, stream);
+}
+
+moe_status moe_router_step_ex(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
+                              float alpha, int32_t renorm, int32_t n_ranks, double capacity_factor,
+                              float grad_scale, const float* bias, float bias_gamma, float* bias_out,
+                              int32_t masked_p, const float* dgate,
+                              int32_t* idx, float* gate, int32_t* counts, float* f, float* P,
+                              float* scalars, int32_t* rank_load,
+                              int32_t* perm, int32_t* slot, int32_t* offsets, int32_t* kept,
+                              int32_t* n_dropped, float* dlogits,
+                              void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_step_args(logits, dt, T, E, k, alpha, renorm, n_ranks, capacity_factor, grad_scale, idx, gate,
+                                 counts, f, P, scalars, rank_load, perm, slot, offsets, kept, n_dropped, dlogits);
+  if (s != MOE_OK) return s;
+  if (!aligned(bias, 4) || !aligned(bias_out, 4) || !aligned(dgate, 4))
+    return fail(MOE_ERR_INVALID, "bias, bias_out or dgate is not 4-byte aligned");
+  if (bias_out != nullptr && !std::isfinite(bias_gamma)) return fail(MOE_ERR_INVALID, "bias_gamma must be finite");
+  if ((s = check_ws(ws, ws_bytes, E)) != MOE_OK) return s;
+  const RouterVariant* v = pick_variant(dt, E, aligned(logits, 16) && aligned(dlogits, 16));
+  if (!v) return fail(MOE_ERR_INVALID, "no kernel variant for E = %d", E);
+  const void* func = step_ext_kernel(dt, v);
+  if (!func) return fail(MOE_ERR_INVALID, "no extended step kernel for E = %d", E);
+  RouterParams p = base_params(logits, T, E, k);
+  p.alpha = alpha;
+  p.renorm = renorm < 0 ? (k > 1) : renorm;
+  p.n_ranks = n_ranks;
+  p.grad_scale = grad_scale;
+  p.C = int(std::min<int64_t>(capacity_of(T, E, k, capacity_factor), INT32_MAX));
+  p.bias = bias;
+  p.bias_gamma = bias_gamma;
+  p.bias_out = bias_out;
+  p.masked_p = masked_p != 0;
+  p.dgate = dgate;
+  p.idx = idx; p.gate = gate; p.counts = counts; p.f = f; p.P = P; p.scalars = scalars; p.rank_load = rank_load;
+  p.perm = perm; p.slot = slot; p.offsets = offsets; p.kept = kept; p.n_dropped = n_dropped;
+  p.dlogits = dlogits;
+  bind_ws(p, ws, E);
+  Geometry geo;
+  if ((s = persistent_geometry(v, dt, T, E, k, true, &geo, func)) != MOE_OK) return s;
+  p.G = geo.G;
+  p.n_groups = (p.G + moe::kGroupCtas - 1) / moe::kGroupCtas;
+  p.rows_per_stage = geo.rows_per_stage;
+  p.n_slots = geo.n_slots;
+  p.asg_cap = geo.asg_cap;
+  p.rstat_cap = geo.rstat_cap;
+  return launch_persistent(func, p, geo.smem, stream);
 }
 
 }  // extern "C"

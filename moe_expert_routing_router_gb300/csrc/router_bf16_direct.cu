@@ -1,17 +1,10 @@
 // bf16 logits of any E, read from global memory one element per load.
 #include "router_instances.cuh"
+#include "router_variant_lists.h"
 
 namespace moe {
 
-static const RouterVariant kVariants[] = {
-    MOE_ROUTER_VARIANT(Bf16, 8, 1, 1, 1, false, 1),    // E <= 8
-    MOE_ROUTER_VARIANT(Bf16, 32, 1, 1, 1, false, 1),   // E <= 32
-    MOE_ROUTER_VARIANT(Bf16, 32, 1, 2, 1, false, 1),
-    MOE_ROUTER_VARIANT(Bf16, 32, 1, 4, 1, false, 1),
-    MOE_ROUTER_VARIANT(Bf16, 32, 1, 8, 1, false, 1),
-    MOE_ROUTER_VARIANT(Bf16, 32, 1, 16, 1, false, 1),
-    MOE_ROUTER_VARIANT(Bf16, 32, 1, 32, 1, false, 1),  // E <= 1024
-};
+static const RouterVariant kVariants[] = {MOE_BF16_DIRECT_LIST(MOE_ROUTER_VARIANT_ITEM)};
 
 MOE_VARIANT_TABLE(router_variants_bf16_direct, kVariants)
 

@@ -22,6 +22,18 @@ constexpr const void* split_step_kernel() {
    reinterpret_cast<const void*>(&::moe::router_bwd_kernel<DT, LPR, VW, NV>),                                        \
    ::moe::split_step_kernel<DT, LPR, VW, NV, NR, STAGED, MINB>()}
 
+#define MOE_ROUTER_VARIANT_ITEM(DT, LPR, VW, NV, NR, STAGED, MINB) MOE_ROUTER_VARIANT(DT, LPR, VW, NV, NR, STAGED, MINB),
+
+#define MOE_STEP_EXT_VARIANT_ITEM(DT, LPR, VW, NV, NR, STAGED, MINB)                                                  \
+  {LPR, VW, NV, NR, STAGED, MINB,                                                                                     \
+   reinterpret_cast<const void*>(&::moe::router_persistent_kernel<DT, LPR, VW, NV, NR, ::moe::kModeStepExt, STAGED, MINB>)},
+
+#define MOE_STEP_EXT_TABLE(NAME, ARRAY)                      \
+  const StepExtVariant* NAME(int* n) {                       \
+    *n = int(sizeof(ARRAY) / sizeof(ARRAY[0]));              \
+    return ARRAY;                                            \
+  }
+
 #define MOE_VARIANT_TABLE(NAME, ARRAY)                       \
   const RouterVariant* NAME(int* n) {                        \
     *n = int(sizeof(ARRAY) / sizeof(ARRAY[0]));              \

@@ -85,10 +85,19 @@ constexpr unsigned long long kDrainNs = 1000000000ull;
 
 // kModeSplit (with kModeStep, renormalised gates): the forward takes only the
 // top-k and the gates; the backward forms each row's softmax sum and P.
+// kModeExt (with kModeStep): the extended step -- selection on fp32(z) + b,
+// masked P when asked, the bias update, and the backward of the gates' upstream
+// gradient added to the aux loss's.
 enum : int {
-  kModeFwd = 1, kModeDispatch = 2, kModeBwd = 4, kModeSplit = 8,
-  kModeStep = kModeFwd | kModeDispatch | kModeBwd, kModeStepSplit = kModeStep | kModeSplit
+  kModeFwd = 1, kModeDispatch = 2, kModeBwd = 4, kModeSplit = 8, kModeExt = 16,
+  kModeStep = kModeFwd | kModeDispatch | kModeBwd, kModeStepSplit = kModeStep | kModeSplit,
+  kModeStepExt = kModeStep | kModeExt
 };
+
+// The type of the pick slots: 64-bit keys of the biased scores in the
+// extended step, the element type's keys otherwise.
+template <bool EXT, class Key> struct PickKeyOf { using type = Key; };
+template <class Key> struct PickKeyOf<true, Key> { using type = long long; };
 
 struct RouterParams {
   const void* logits;          // [T, E] fp32 or bf16
@@ -100,6 +109,12 @@ struct RouterParams {
   int n_ranks;
   int C;                       // expert capacity
   const int32_t* cap_base;     // [E] assignments of each expert on lower data-parallel ranks, or null (none)
+  // extended step (kModeExt)
+  const float* bias;           // [E] selection bias, or null (all zero)
+  float bias_gamma;            // bias step
+  float* bias_out;             // [E] updated bias (may alias bias), or null
+  int masked_p;                // P over the picked experts only, divided by T*k
+  const float* dgate;          // [T, k] upstream gradient of the gates, or null
   float grad_scale;
   // outputs (null when the mode does not produce them)
   int32_t* idx;                // [T, k]
@@ -338,20 +353,11 @@ __device__ __forceinline__ long long max3_key(long long a, long long b, long lon
   return m > c ? m : c;
 }
 
-template <class DT, int LPR, int VW, int NV>
-__device__ __forceinline__ void lane_top2(const typename DT::Raw (&raw)[VW * NV], int l, typename DT::Key& m1,
-                                          typename DT::Key& m2) {
-  using Key = typename DT::Key;
-  constexpr int EPL = VW * NV;
-  Key key[EPL];
-#pragma unroll
-  for (int v = 0; v < NV; ++v)
-#pragma unroll
-    for (int i = 0; i < VW; ++i)
-      key[v * VW + i] = DT::key_from_bits(DT::bits(raw[v * VW + i]), col_lane_bits<LPR, VW>(l), col_elem_bits<LPR, VW>(v, i));
+template <class Key, int EPL>
+__device__ __forceinline__ void keys_top2(const Key (&key)[EPL], Key kmin, Key& m1, Key& m2) {
   if constexpr (EPL == 1) {
     m1 = key[0];
-    m2 = DT::kKeyMin;
+    m2 = kmin;
   } else {
     constexpr int N0 = (EPL + 1) / 2;
     Key hi[N0], lo[N0];
@@ -363,7 +369,7 @@ __device__ __forceinline__ void lane_top2(const typename DT::Raw (&raw)[VW * NV]
     }
     if constexpr (EPL & 1) {
       hi[N0 - 1] = key[EPL - 1];
-      lo[N0 - 1] = DT::kKeyMin;
+      lo[N0 - 1] = kmin;
     }
 #pragma unroll
     for (int n = N0; n > 1; n = (n + 1) / 2) {
@@ -381,6 +387,36 @@ __device__ __forceinline__ void lane_top2(const typename DT::Raw (&raw)[VW * NV]
     m1 = hi[0];
     m2 = lo[0];
   }
+}
+
+template <class DT, int LPR, int VW, int NV>
+__device__ __forceinline__ void lane_top2(const typename DT::Raw (&raw)[VW * NV], int l, typename DT::Key& m1,
+                                          typename DT::Key& m2) {
+  using Key = typename DT::Key;
+  constexpr int EPL = VW * NV;
+  Key key[EPL];
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < VW; ++i)
+      key[v * VW + i] = DT::key_from_bits(DT::bits(raw[v * VW + i]), col_lane_bits<LPR, VW>(l), col_elem_bits<LPR, VW>(v, i));
+  keys_top2<Key, EPL>(key, DT::kKeyMin, m1, m2);
+}
+
+// Selection keys of the biased scores s = fp32(z) + b of lane l's elements
+// ([P1] §4.3: the bias moves the choice of experts only): the fp32 keys of
+// s (equal values tie, -0.0 with +0.0, and go to the lower column).  Columns
+// past E hold -inf, whose score stays -inf whatever the bias there (zero).
+template <class DT, int LPR, int VW, int NV>
+__device__ __forceinline__ void biased_keys(const typename DT::Raw (&raw)[VW * NV], const float (&bl)[VW * NV], int l,
+                                            long long (&key)[VW * NV]) {
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int i = 0; i < VW; ++i) {
+      const float sc = __uint_as_float(DT::bits(raw[v * VW + i])) + bl[v * VW + i];
+      key[v * VW + i] = Fp32::key_from_bits(__float_as_uint(sc), col_lane_bits<LPR, VW>(l), col_elem_bits<LPR, VW>(v, i));
+    }
 }
 
 // Sum of x[0..N) in a fixed order: the pairs (x[2i], x[2i+1]) are added as
@@ -824,6 +860,129 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
   }
 }
 
+// ---------------------------------------------------------------------------
+// Forward of one row group of the extended step: top-k on the biased scores
+// fp32(z) + b ([P1] §4.3; 64-bit keys, the rounds of fwd_groups, and for a lane
+// that won twice the exact count of its keys above the k-th pick), softmax,
+// gates and P from the unbiased z.  With masked P ([P2] §3.1) each pick adds
+// its p into the warp's per-expert sums s_pm instead of pacc.  bl: the bias of
+// the lane's columns.
+// ---------------------------------------------------------------------------
+template <class DT, int LPR, int VW, int NV, bool GLOBAL>
+__device__ __noinline__ long long exact_topk_ext(const typename DT::Raw* row, const float (&bl)[VW * NV], int E, int k,
+                                                int l, bool valid) {
+  constexpr int EPL = VW * NV;
+  typename DT::Raw raw[EPL];
+  load_lane<DT, LPR, VW, NV, GLOBAL>(row, E, l, valid, raw);
+  long long key[EPL];
+  biased_keys<DT, LPR, VW, NV>(raw, bl, l, key);
+  long long prev = Fp32::kKeyMin, mine = Fp32::kKeyMin;
+  for (int j = 0; j < k; ++j) {
+    long long local = Fp32::kKeyMin;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) local = ((j == 0 || key[i] < prev) && key[i] > local) ? key[i] : local;
+    const long long w = group_max_key<LPR>(local);
+    if (l == j) mine = w;
+    prev = w;
+  }
+  return mine;
+}
+
+template <class DT, int LPR, int VW, int NV, int NR, bool GLOBAL>
+__device__ __forceinline__ void fwd_groups_ext(const RouterParams& p, const typename DT::Raw* const (&row)[NR],
+                                               const long long (&t)[NR], const bool (&valid)[NR], int l, int* s_hist,
+                                               float (&pacc)[VW * NV], long long* s_pick, uint16_t* s_aidx,
+                                               long long a_base, float2* s_rstat, long long r_base,
+                                               const float (&bl)[VW * NV], float* s_pm) {
+  using Raw = typename DT::Raw;
+  using Key = long long;
+  constexpr int EPL = VW * NV;
+  constexpr int GPW = kWarp / LPR;
+  static_assert(NR * GPW * kMaxK <= kPickSlotsPerWarp, "pick slots");
+  const int k = p.k, E = p.E;
+  const int g = (threadIdx.x & 31) / LPR;
+
+  Raw raw[NR][EPL];
+  Key m1[NR], m2[NR], second[NR], mine[NR], w[NR];
+  float mx[NR], e[NR][EPL];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    load_lane<DT, LPR, VW, NV, GLOBAL>(row[r], E, l, valid[r], raw[r]);
+    Key key[EPL];
+    biased_keys<DT, LPR, VW, NV>(raw[r], bl, l, key);
+    keys_top2<Key, EPL>(key, Fp32::kKeyMin, m1[r], m2[r]);
+    second[r] = m2[r];
+    float m = -3.402823466e38f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) m = fmaxf(m, __uint_as_float(DT::bits(raw[r][i])));
+    mx[r] = group_max<LPR>(m);
+    row_exp<DT, LPR, EPL>(raw[r], mx[r], e[r]);
+  }
+  __syncwarp();                                    // the previous rows' picks have been read
+  for (int j = 0; j < k; ++j) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) w[r] = group_max_key<LPR>(m1[r]);
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      s_pick[(r * GPW + g) * kMaxK + j] = w[r];
+      const bool won = m1[r] == w[r];
+      m1[r] = won ? m2[r] : m1[r];
+      m2[r] = won ? Fp32::kKeyMin : m2[r];
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < NR; ++r) mine[r] = l < k ? s_pick[(r * GPW + g) * kMaxK + l] : Fp32::kKeyMin;
+  // A lane that won twice before the last round hides a pick iff more than
+  // two of its keys exceed the k-th pick w (the reasoning of fwd_groups).
+  bool early[NR], check = false;
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    early[r] = EPL > 1 && m1[r] == Fp32::kKeyMin && second[r] != w[r];
+    check = check || early[r];
+  }
+  if (__any_sync(0xffffffffu, check)) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      if (__any_sync(0xffffffffu, early[r])) {
+        Key key[EPL];
+        biased_keys<DT, LPR, VW, NV>(raw[r], bl, l, key);
+        int above = 0;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) above += key[i] > w[r] ? 1 : 0;
+        if (__any_sync(0xffffffffu, early[r] && above > 2))
+          mine[r] = exact_topk_ext<DT, LPR, VW, NV, GLOBAL>(row[r], bl, E, k, l, valid[r]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const float s = group_sum<LPR>(tree_sum(e[r]));
+    const float inv_s = valid[r] ? rcp_approx(s) : 0.f;
+    if (!p.masked_p) axpy2(pacc, e[r], inv_s);
+    const bool owner = l < k;
+    int col = 0;
+    float ej = 0.f;
+    if (owner) {
+      col = min(Fp32::key_col(mine[r]), E - 1);
+      Raw zr;
+      if constexpr (GLOBAL) zr = __ldg(row[r] + col);
+      else zr = row[r][col];
+      ej = elem_exp(__uint_as_float(DT::bits(zr)), mx[r]);   // the unbiased numerator, as row_exp forms it
+    }
+    const float denom = p.renorm ? owners_sum<LPR>(ej) : s;
+    if (valid[r] && owner) {
+      const long long a = t[r] * k + l;
+      p.idx[a] = col;
+      p.gate[a] = ej * rcp_approx(denom);
+      atomicAdd(&s_hist[col], 1);
+      if (s_aidx != nullptr) s_aidx[a - a_base] = uint16_t(col);
+      if (p.masked_p) atomicAdd(&s_pm[col], ej * inv_s);
+    }
+    if (s_rstat != nullptr && valid[r] && l == 0) s_rstat[t[r] - r_base] = make_float2(mx[r], inv_s);
+  }
+}
+
 // The forward of the large-E bf16 variants (32 lanes per row, rows in a ring
 // stage), in three parts: fast_topk_rows (the candidate path for K picks),
 // full_topk_row (the full path, out of line) and row_tail (gates, idx and
@@ -1156,6 +1315,86 @@ __device__ __forceinline__ void bwd_group_split(const typename DT::Raw (&raw)[VW
         store_vec_f32<VW>(out + c0, d);
       }
     }
+  }
+}
+
+// Backward of one row group of the extended step: dlogits = p * (dp - sum p dp)
+// for L = sum_j dgate_j * gate_j + grad_scale * L_aux (picks and f fixed).  Fr
+// holds coef * f on the lane's columns (zero with masked P).  Lane j < k of the
+// group takes pick j: its column (the forward's idx), its numerator ec (the
+// bits row_exp gives it) and gp = p_j * gamma_j, gamma_j its extra dL/dp: the
+// gate term (renormalised: (dgate_j - sum_m dgate_m gate_m) / sum_m p_m,
+// formed as sum_m e_m (dgate_j - dgate_m) * s / Se^2 times p_j; plain:
+// dgate_j) and with masked P the aux term coef_m * f_j.  Every lane stores
+// p * (F - S) with S = sum p F + sum gp; then, after a warp sync, lane j
+// stores its pick's element again with gp added.
+template <class DT, int LPR, int VW, int NV, bool GLOBAL>
+__device__ __forceinline__ void bwd_group_ext(const RouterParams& p, const typename DT::Raw (&raw)[VW * NV],
+                                              const typename DT::Raw* row, const float (&Fr)[VW * NV], long long t,
+                                              bool valid, int l, int E, float mx, float inv_s, float coef_f,
+                                              float coef_m, const float* s_f, const uint16_t* s_aidx, long long a_base) {
+  constexpr int EPL = VW * NV;
+  const int k = p.k;
+  float e[EPL];
+  row_exp<DT, LPR, EPL>(raw, mx, e);
+  float dot[EPL];
+#pragma unroll
+  for (int i = 0; i + 1 < EPL; i += 2) {
+    const float2 q = mul2(make_float2(e[i], e[i + 1]), make_float2(Fr[i], Fr[i + 1]));
+    dot[i] = q.x;
+    dot[i + 1] = q.y;
+  }
+  if constexpr (EPL & 1) dot[EPL - 1] = e[EPL - 1] * Fr[EPL - 1];
+  const float wa = inv_s * (inv_s * group_sum<LPR>(tree_sum(dot)));
+  const bool owner = valid && l < k;
+  int col = 0;
+  float ec = 0.f, dg = 0.f;
+  if (owner) {
+    const long long a = t * k + l;
+    col = s_aidx != nullptr ? int(s_aidx[a - a_base]) : __ldcg(p.idx + a);
+    col = min(max(col, 0), E - 1);
+    typename DT::Raw zr;
+    if constexpr (GLOBAL) zr = __ldg(row + col);
+    else zr = row[col];
+    ec = elem_exp(__uint_as_float(DT::bits(zr)), mx);
+    if (p.dgate != nullptr) dg = __ldg(p.dgate + a);
+  }
+  float gp = 0.f;
+  if (p.dgate != nullptr) {
+    if (p.renorm) {
+      const int base = (threadIdx.x & 31) - l;    // lane 0 of the group
+      float Se = 0.f, acc = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const float ej = __shfl_sync(0xffffffffu, ec, base + j);
+        const float dj = __shfl_sync(0xffffffffu, dg, base + j);
+        Se += ej;
+        acc = fmaf(ej, dg - dj, acc);
+      }
+      const float inv_Se = rcp_approx(Se);
+      gp = owner ? ec * (acc * inv_Se) * inv_Se : 0.f;
+    } else {
+      gp = owner ? ec * inv_s * dg : 0.f;
+    }
+  }
+  if (p.masked_p && owner) gp = fmaf(ec * inv_s, coef_m * s_f[col], gp);
+  const float w = fmaf(inv_s, group_sum<LPR>(gp), wa);
+  if (valid) {
+    float* out = p.dlogits + t * (long long)E;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int c0 = col_of<LPR, VW>(v, l, 0);
+      if (c0 < E) {
+        float d[VW];
+#pragma unroll
+        for (int i = 0; i < VW; ++i) d[i] = e[v * VW + i] * fmaf(inv_s, Fr[v * VW + i], -w);
+        store_vec_f32<VW>(out + c0, d);
+      }
+    }
+  }
+  __syncwarp();                                    // the pick's element above is stored first
+  if (owner) {
+    const float F = coef_f * s_f[col];
+    __stcs(p.dlogits + t * (long long)E + col, fmaf(ec, fmaf(inv_s, F, -w), gp));
   }
 }
 
@@ -1531,6 +1770,18 @@ __device__ __forceinline__ void finalize_warp(const RouterParams& p, const int32
       }
     }
   }
+  // The extended step's bias update ([P1] §4.3): b_e + gamma * sign(T*k/E -
+  // count_e), the sign taken exactly as sign(T*k - count_e * E), in fp32.
+  // Every CTA read the bias before the grid barrier, so bias_out may alias it.
+  if constexpr ((MODE & kModeExt) != 0) {
+    if (p.bias_out != nullptr) {
+      for (int e = lane; e < E; e += kWarp) {
+        const long long d = tk - (long long)s_cnt[e] * E;
+        const float dir = d > 0 ? 1.f : (d < 0 ? -1.f : 0.f);
+        p.bias_out[e] = (p.bias != nullptr ? p.bias[e] : 0.f) + p.bias_gamma * dir;
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1607,7 +1858,7 @@ __device__ __forceinline__ void dispatch_phase_c(const RouterParams& p, int cta,
   if constexpr ((MODE & kModeFwd) != 0 && (MODE & kModeSplit) == 0) {
     for (int e = cta; e < E; e += p.G) {
       const float Ps = warp_column_sum_f(p.P_part + (size_t)e * p.G_stride, p.G);
-      if (lane == 0) p.P[e] = __fdiv_rn(Ps, float(p.T));
+      if (lane == 0) p.P[e] = __fdiv_rn(Ps, (MODE & kModeExt) != 0 && p.masked_p ? float(p.T * p.k) : float(p.T));
     }
   }
   if (wait_phase(p, s_phase, 2) < 2) return;
@@ -1670,7 +1921,9 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   const int S = STAGED ? p.rows_per_stage : 1;
   const int NS = STAGED ? p.n_slots : 1;
   const int stage_elems = S * E;
-  const SmemLayout L = router_smem_layout(E, int(sizeof(typename DT::Key)), STAGED ? NS : 0, stage_elems * int(sizeof(Raw)),
+  constexpr bool kExt = (MODE & kModeExt) != 0;
+  using PKey = typename PickKeyOf<kExt, typename DT::Key>::type;
+  const SmemLayout L = router_smem_layout(E, int(sizeof(PKey)), STAGED ? NS : 0, stage_elems * int(sizeof(Raw)),
                                           p.asg_cap, p.rstat_cap);
   int* s_red = reinterpret_cast<int*>(smem + L.red);
   int* s_prog = s_red + kRedProg;     // stages finished per consumer warp (forward)
@@ -1683,7 +1936,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kMaxSlots;
   Raw* ring = reinterpret_cast<Raw*>(smem + L.ring);
-  typename DT::Key* s_pick_w = reinterpret_cast<typename DT::Key*>(smem + L.pick) + warp * kPickSlotsPerWarp;
+  PKey* s_pick_w = reinterpret_cast<PKey*>(smem + L.pick) + warp * kPickSlotsPerWarp;
 
   const long long r0 = p.T * cta / G, r1 = p.T * (cta + 1) / G;
   const long long a0 = r0 * k, a1 = r1 * k;
@@ -1715,7 +1968,9 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
     s_hist[e] = 0;
     s_rank[e] = 0;
   }
-  if constexpr ((MODE & kModeFwd) == 0)       // per-consumer-warp expert counts (dispatch of given idx)
+  // per-consumer-warp expert counts (dispatch of given idx), or sums of the
+  // picks' p (extended step with masked P)
+  if constexpr ((MODE & kModeFwd) == 0 || kExt)
     for (int i = tid; i < kConsumerWarps * E; i += kThreads) reinterpret_cast<int*>(s_wf)[i] = 0;
   if (tid < kConsumerWarps) s_prog[tid] = 0;
   if (tid == 0) {
@@ -1746,9 +2001,19 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
       float pacc[EPL];
 #pragma unroll
       for (int i = 0; i < EPL; ++i) pacc[i] = 0.f;
+      // the selection bias of the lane's columns (extended step; zero past E)
+      float bl[EPL];
+#pragma unroll
+      for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int i = 0; i < VW; ++i) {
+          const int c = col_of<LPR, VW>(v, l, i);
+          bl[v * VW + i] = kExt && p.bias != nullptr && c < E ? __ldg(p.bias + c) : 0.f;
+        }
+      float* s_pm = s_wf + warp * E;                 // masked P: this warp's sums of the picks' p
       if constexpr (STAGED) {
         // The fast top-k path (bf16 rows of 32 lanes, at most 16 elements per lane).
-        constexpr bool kFast = kFastTopk<DT, LPR, VW, NV>;
+        constexpr bool kFast = kFastTopk<DT, LPR, VW, NV> && !kExt;
         FastTopk<(EPL / 2 > 0 ? EPL / 2 : 1)> fs;
         fs.state = kFast && n_st > 1 ? 0 : 2;
         fs.tries = 0;
@@ -1800,8 +2065,12 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
                 rows[r] = st + (valids[r] ? ri : 0) * E;
                 ts[r] = r0 + (long long)s * S + ri;
               }
-              fwd_groups<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, s_aidx, a0,
-                                                     s_rstat, r0);
+              if constexpr (kExt)
+                fwd_groups_ext<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, s_aidx, a0,
+                                                           s_rstat, r0, bl, s_pm);
+              else
+                fwd_groups<DT, LPR, VW, NV, NR, false>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, s_aidx, a0,
+                                                       s_rstat, r0);
             }
           }
           __syncwarp();
@@ -1825,7 +2094,11 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
             valids[r] = ts[r] < r1;
             rows[r] = X + (valids[r] ? ts[r] : r0) * (long long)E;
           }
-          fwd_groups<DT, LPR, VW, NV, NR, true>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, nullptr, 0, nullptr, 0);
+          if constexpr (kExt)
+            fwd_groups_ext<DT, LPR, VW, NV, NR, true>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, nullptr, 0,
+                                                      nullptr, 0, bl, s_pm);
+          else
+            fwd_groups<DT, LPR, VW, NV, NR, true>(p, rows, ts, valids, l, s_hist, pacc, s_pick_w, nullptr, 0, nullptr, 0);
         }
       }
       trace_point(p, kTrFwdRows);
@@ -1836,7 +2109,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
       for (int i = 0; i < EPL; ++i)
 #pragma unroll
         for (int off = LPR; off < kWarp; off <<= 1) pacc[i] += __shfl_xor_sync(0xffffffffu, pacc[i], off);
-      if ((MODE & kModeSplit) == 0 && g == 0) {
+      if ((MODE & kModeSplit) == 0 && !(kExt && p.masked_p) && g == 0) {
 #pragma unroll
         for (int v = 0; v < NV; ++v)
 #pragma unroll
@@ -2049,9 +2322,13 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
   }
   if constexpr ((MODE & kModeBwd) != 0) {
     const float coef = p.grad_scale * p.alpha * float(E) / float(p.T);
+    // extended step: the dense aux coefficient (zero with masked P, whose aux
+    // term reaches the picks only) and the picks' one, g*alpha*E/(T*k)
+    const float coef_f = kExt && p.masked_p ? 0.f : coef;
+    const float coef_m = p.grad_scale * p.alpha * float(E) / float(p.T * k);
     if (warp < kConsumerWarps) {
       float fr[EPL];
-      load_f<LPR, VW, NV>(s_f, E, l, coef, fr);
+      load_f<LPR, VW, NV>(s_f, E, l, coef_f, fr);
       constexpr bool kSplit = (MODE & kModeSplit) != 0;
       static_assert(!kSplit || (STAGED && kFastTopk<DT, LPR, VW, NV>), "split steps run on the fast variants");
       float pacc_b[EPL];                           // a split step's sums of p over the warp's rows
@@ -2093,7 +2370,11 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
               } else {
                 bwd_row_stats<DT, LPR, VW, NV>(raw, mx, inv_s);
               }
-              bwd_group<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, mx, inv_s, p.dlogits);
+              if constexpr (kExt)
+                bwd_group_ext<DT, LPR, VW, NV, false>(p, raw, st + (valid ? ri : 0) * E, fr, r0 + (long long)s * S + ri,
+                                                      valid, l, E, mx, inv_s, coef_f, coef_m, s_f, s_aidx, a0);
+              else
+                bwd_group<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, mx, inv_s, p.dlogits);
             }
           }
           __syncwarp();
@@ -2108,7 +2389,11 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           load_lane<DT, LPR, VW, NV, true>(X + (valid ? t : r0) * (long long)E, E, l, valid, raw);
           float mx, inv_s;
           bwd_row_stats<DT, LPR, VW, NV>(raw, mx, inv_s);
-          bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, E, mx, inv_s, p.dlogits);
+          if constexpr (kExt)
+            bwd_group_ext<DT, LPR, VW, NV, true>(p, raw, X + (valid ? t : r0) * (long long)E, fr, t, valid, l, E, mx,
+                                                 inv_s, coef_f, coef_m, s_f, nullptr, 0);
+          else
+            bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, E, mx, inv_s, p.dlogits);
         }
       }
       trace_point(p, kTrBwdRows);

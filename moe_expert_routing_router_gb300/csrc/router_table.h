@@ -22,6 +22,17 @@ const RouterVariant* router_variants_bf16_staged(int* n);
 const RouterVariant* router_variants_bf16_direct(int* n);
 const RouterVariant* router_variants_fp32_staged(int* n);
 const RouterVariant* router_variants_fp32_direct(int* n);
+// The extended step (bias selection, masked P, gate gradients) of the same row
+// layouts, in tables of their own (compiled in separate units).
+struct StepExtVariant {
+  int LPR, VW, NV, NR, staged, min_blocks;
+  const void* step_ext;    // persistent kernel, the extended step
+};
+const StepExtVariant* step_ext_bf16_staged(int* n);
+const StepExtVariant* step_ext_bf16_direct(int* n);
+const StepExtVariant* step_ext_fp32_staged(int* n);
+const StepExtVariant* step_ext_fp32_direct(int* n);
+
 // Kernels of the forward with bias routing / masked P and of the full
 // backward, per row layout.  vec: 16-byte rows read VW elements per load.
 struct ExtVariant {
