@@ -249,8 +249,8 @@ constexpr int kMaxRowStats = 4096;             // rows per CTA whose softmax sta
 // fused: the launch runs the fused step (forward, dispatch and backward), whose
 // CTAs keep their dispatch and the rows' softmax statistics in shared memory
 // when these fit beside at least two ring slots.
-// ext: the extended step's kernel of the variant (its pick slots hold 64-bit
-// keys and its occupancy sets the grid), or null for the plain kernels.
+// ext: the extended step's kernel of the variant (its pick slots hold 32-bit
+// selection keys and its occupancy sets the grid), or null for the plain kernels.
 moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, int E, int k, bool fused,
                                Geometry* out, const void* ext = nullptr) {
   DeviceInfo d;
@@ -258,7 +258,7 @@ moe_status persistent_geometry(const RouterVariant* v, moe_dtype dt, int64_t T, 
   moe_status s = device_info(&d, &dev);
   if (s != MOE_OK) return s;
   const int esize = dt == MOE_DTYPE_BF16 ? 2 : 4;
-  const int kb = ext != nullptr ? int(sizeof(long long))
+  const int kb = ext != nullptr ? int(sizeof(uint32_t))
                  : dt == MOE_DTYPE_BF16 ? int(sizeof(moe::Bf16::Key)) : int(sizeof(moe::Fp32::Key));
   const int group_rows = moe::kConsumerWarps * (moe::kWarp / v->LPR) * v->NR;
   Geometry g;

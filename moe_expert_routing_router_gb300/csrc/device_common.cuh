@@ -321,14 +321,25 @@ __device__ __forceinline__ uint32_t group_max_key(uint32_t x) {
   }
 }
 
+// 64-bit keys (Fp32: signed value word above the column word).  Over a whole
+// warp: the largest value word, as an unsigned number with the sign bit
+// flipped (the same order), by one warp reduction, then the largest column
+// word among the lanes holding it by a second one.
 template <int LPR>
 __device__ __forceinline__ long long group_max_key(long long x) {
+  if constexpr (LPR == 32) {
+    const uint32_t hi = uint32_t((unsigned long long)x >> 32) ^ 0x80000000u;
+    const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, hi == mh ? uint32_t((unsigned long long)x) : 0u);
+    return (long long)(((unsigned long long)(mh ^ 0x80000000u) << 32) | lo);
+  } else {
 #pragma unroll
-  for (int off = LPR / 2; off > 0; off >>= 1) {
-    const long long y = __shfl_xor_sync(0xffffffffu, x, off);
-    x = y > x ? y : x;
+    for (int off = LPR / 2; off > 0; off >>= 1) {
+      const long long y = __shfl_xor_sync(0xffffffffu, x, off);
+      x = y > x ? y : x;
+    }
+    return x;
   }
-  return x;
 }
 
 __device__ __forceinline__ float warp_sum_f(float x) {

@@ -94,10 +94,10 @@ enum : int {
   kModeStepExt = kModeStep | kModeExt
 };
 
-// The type of the pick slots: 64-bit keys of the biased scores in the
-// extended step, the element type's keys otherwise.
+// The type of the pick slots: the 32-bit selection keys of the biased scores
+// in the extended step, the element type's keys otherwise.
 template <bool EXT, class Key> struct PickKeyOf { using type = Key; };
-template <class Key> struct PickKeyOf<true, Key> { using type = long long; };
+template <class Key> struct PickKeyOf<true, Key> { using type = uint32_t; };
 
 struct RouterParams {
   const void* logits;          // [T, E] fp32 or bf16
@@ -888,34 +888,74 @@ __device__ __noinline__ long long exact_topk_ext(const typename DT::Raw* row, co
   return mine;
 }
 
+// 32-bit selection key of a biased score s in column col < 1024: the
+// order-preserving image of fp32 s (-0.0 taken as +0.0) with its low 10 bits
+// replaced by 1023 - col, so equal images go to the lower column.  Scores whose
+// images differ only in those 10 bits compare by column here: the row's picks
+// are kept only when no such pair decides them (see fwd_groups_ext).
+__device__ __forceinline__ uint32_t sel_key32(float sc, uint32_t col) {
+  const uint32_t u = __float_as_uint(__fadd_rn(sc, 0.f));
+  const uint32_t m = uint32_t(int(u) >> 31) | 0x80000000u;
+  return ((u ^ m) | 0x3ffu) - col;
+}
+constexpr uint32_t kSelValueMask = 0xfffffc00u;
+
+// Row max of finite-or-infinite floats: over 32 lanes by one warp reduction of
+// the order-preserving images, else by shuffles.
+template <int LPR>
+__device__ __forceinline__ float group_max_img(float x) {
+  if constexpr (LPR == 32) {
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t img = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t r = __reduce_max_sync(0xffffffffu, img);
+    return __uint_as_float((r & 0x80000000u) ? (r & 0x7fffffffu) : ~r);
+  } else {
+    return group_max<LPR>(x);
+  }
+}
+
+template <int LPR>
+__device__ __forceinline__ int group_sum_int(int x) {
+  if constexpr (LPR == 32) {
+    return int(__reduce_add_sync(0xffffffffu, uint32_t(x)));
+  } else {
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+  }
+}
+
 template <class DT, int LPR, int VW, int NV, int NR, bool GLOBAL>
 __device__ __forceinline__ void fwd_groups_ext(const RouterParams& p, const typename DT::Raw* const (&row)[NR],
                                                const long long (&t)[NR], const bool (&valid)[NR], int l, int* s_hist,
-                                               float (&pacc)[VW * NV], long long* s_pick, uint16_t* s_aidx,
+                                               float (&pacc)[VW * NV], uint32_t* s_pick, uint16_t* s_aidx,
                                                long long a_base, float2* s_rstat, long long r_base,
                                                const float (&bl)[VW * NV], float* s_pm) {
   using Raw = typename DT::Raw;
-  using Key = long long;
   constexpr int EPL = VW * NV;
   constexpr int GPW = kWarp / LPR;
   static_assert(NR * GPW * kMaxK <= kPickSlotsPerWarp, "pick slots");
   const int k = p.k, E = p.E;
   const int g = (threadIdx.x & 31) / LPR;
+  const uint32_t lane_cols = col_lane_bits<LPR, VW>(l);
 
   Raw raw[NR][EPL];
-  Key m1[NR], m2[NR], second[NR], mine[NR], w[NR];
+  uint32_t key[NR][EPL], m1[NR], m2[NR], w[NR];
   float mx[NR], e[NR][EPL];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     load_lane<DT, LPR, VW, NV, GLOBAL>(row[r], E, l, valid[r], raw[r]);
-    Key key[EPL];
-    biased_keys<DT, LPR, VW, NV>(raw[r], bl, l, key);
-    keys_top2<Key, EPL>(key, Fp32::kKeyMin, m1[r], m2[r]);
-    second[r] = m2[r];
     float m = -3.402823466e38f;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) m = fmaxf(m, __uint_as_float(DT::bits(raw[r][i])));
-    mx[r] = group_max<LPR>(m);
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int i = 0; i < VW; ++i) {
+        const float z = __uint_as_float(DT::bits(raw[r][v * VW + i]));
+        m = fmaxf(m, z);
+        key[r][v * VW + i] = sel_key32(z + bl[v * VW + i], lane_cols + col_elem_bits<LPR, VW>(v, i));
+      }
+    keys_top2<uint32_t, EPL>(key[r], 0u, m1[r], m2[r]);
+    mx[r] = group_max_img<LPR>(m);
     row_exp<DT, LPR, EPL>(raw[r], mx[r], e[r]);
   }
   __syncwarp();                                    // the previous rows' picks have been read
@@ -927,32 +967,30 @@ __device__ __forceinline__ void fwd_groups_ext(const RouterParams& p, const type
       s_pick[(r * GPW + g) * kMaxK + j] = w[r];
       const bool won = m1[r] == w[r];
       m1[r] = won ? m2[r] : m1[r];
-      m2[r] = won ? Fp32::kKeyMin : m2[r];
+      m2[r] = won ? 0u : m2[r];
     }
   }
   __syncwarp();
-#pragma unroll
-  for (int r = 0; r < NR; ++r) mine[r] = l < k ? s_pick[(r * GPW + g) * kMaxK + l] : Fp32::kKeyMin;
-  // A lane that won twice before the last round hides a pick iff more than
-  // two of its keys exceed the k-th pick w (the reasoning of fwd_groups).
-  bool early[NR], check = false;
+  // The picks stand iff exactly k elements have a value image at or above the
+  // k-th pick's (then they are the picks: a lane that ran out of cached keys
+  // hid none, and no other score shares the k-th one's image) and the picks'
+  // images are all different (then their order is the scores' order).  Else
+  // the row is redone on the full 64-bit keys.
+  int col[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
-    early[r] = EPL > 1 && m1[r] == Fp32::kKeyMin && second[r] != w[r];
-    check = check || early[r];
-  }
-  if (__any_sync(0xffffffffu, check)) {
+    const uint32_t thr = w[r] & kSelValueMask;
+    int cnt = 0;
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      if (__any_sync(0xffffffffu, early[r])) {
-        Key key[EPL];
-        biased_keys<DT, LPR, VW, NV>(raw[r], bl, l, key);
-        int above = 0;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) above += key[i] > w[r] ? 1 : 0;
-        if (__any_sync(0xffffffffu, early[r] && above > 2))
-          mine[r] = exact_topk_ext<DT, LPR, VW, NV, GLOBAL>(row[r], bl, E, k, l, valid[r]);
-      }
+    for (int i = 0; i < EPL; ++i) cnt += key[r][i] >= thr ? 1 : 0;
+    cnt = group_sum_int<LPR>(cnt);
+    const uint32_t mine = l < k ? s_pick[(r * GPW + g) * kMaxK + l] : 0u;
+    const uint32_t next = l + 1 < k ? s_pick[(r * GPW + g) * kMaxK + l + 1] : 0u;
+    const bool dup = l + 1 < k && (mine & kSelValueMask) == (next & kSelValueMask);
+    col[r] = int(1023u - (mine & 0x3ffu));
+    if (__any_sync(0xffffffffu, valid[r] && (cnt != k || dup))) {
+      const long long m64 = exact_topk_ext<DT, LPR, VW, NV, GLOBAL>(row[r], bl, E, k, l, valid[r]);
+      col[r] = l < k ? Fp32::key_col(m64) : 0;
     }
   }
 #pragma unroll
@@ -961,23 +999,23 @@ __device__ __forceinline__ void fwd_groups_ext(const RouterParams& p, const type
     const float inv_s = valid[r] ? rcp_approx(s) : 0.f;
     if (!p.masked_p) axpy2(pacc, e[r], inv_s);
     const bool owner = l < k;
-    int col = 0;
+    int c = 0;
     float ej = 0.f;
     if (owner) {
-      col = min(Fp32::key_col(mine[r]), E - 1);
+      c = min(max(col[r], 0), E - 1);
       Raw zr;
-      if constexpr (GLOBAL) zr = __ldg(row[r] + col);
-      else zr = row[r][col];
+      if constexpr (GLOBAL) zr = __ldg(row[r] + c);
+      else zr = row[r][c];
       ej = elem_exp(__uint_as_float(DT::bits(zr)), mx[r]);   // the unbiased numerator, as row_exp forms it
     }
     const float denom = p.renorm ? owners_sum<LPR>(ej) : s;
     if (valid[r] && owner) {
       const long long a = t[r] * k + l;
-      p.idx[a] = col;
+      p.idx[a] = c;
       p.gate[a] = ej * rcp_approx(denom);
-      atomicAdd(&s_hist[col], 1);
-      if (s_aidx != nullptr) s_aidx[a - a_base] = uint16_t(col);
-      if (p.masked_p) atomicAdd(&s_pm[col], ej * inv_s);
+      atomicAdd(&s_hist[c], 1);
+      if (s_aidx != nullptr) s_aidx[a - a_base] = uint16_t(c);
+      if (p.masked_p) atomicAdd(&s_pm[c], ej * inv_s);
     }
     if (s_rstat != nullptr && valid[r] && l == 0) s_rstat[t[r] - r_base] = make_float2(mx[r], inv_s);
   }
@@ -1318,23 +1356,44 @@ __device__ __forceinline__ void bwd_group_split(const typename DT::Raw (&raw)[VW
   }
 }
 
+// Lane l's upstream gradient of gate l of row t (zero off the picks' lanes,
+// past the batch, or without dgate).
+__device__ __forceinline__ float dgate_of(const RouterParams& p, long long t, int l, bool valid) {
+  return valid && l < p.k && p.dgate != nullptr ? __ldg(p.dgate + t * p.k + l) : 0.f;
+}
+
 // Backward of one row group of the extended step: dlogits = p * (dp - sum p dp)
 // for L = sum_j dgate_j * gate_j + grad_scale * L_aux (picks and f fixed).  Fr
 // holds coef * f on the lane's columns (zero with masked P).  Lane j < k of the
 // group takes pick j: its column (the forward's idx), its numerator ec (the
 // bits row_exp gives it) and gp = p_j * gamma_j, gamma_j its extra dL/dp: the
-// gate term (renormalised: (dgate_j - sum_m dgate_m gate_m) / sum_m p_m,
-// formed as sum_m e_m (dgate_j - dgate_m) * s / Se^2 times p_j; plain:
-// dgate_j) and with masked P the aux term coef_m * f_j.  Every lane stores
-// p * (F - S) with S = sum p F + sum gp; then, after a warp sync, lane j
-// stores its pick's element again with gp added.
+// gate term (renormalised: (dgate_j - G) / sum_m p_m with G = sum_m dgate_m
+// gate_m, so gp = gate_j (dgate_j - G), formed from the differences dgate_j -
+// dgate_m; plain: dgate_j) and with masked P the
+// aux term coef_m * f_j.  Every lane stores p * (F - S) with S = sum p F +
+// sum gp; then, after a warp sync, lane j stores its pick's element again with
+// gp added.  dg_in: lane j's upstream
+// gradient of gate j of this row (loaded ahead by the caller).
 template <class DT, int LPR, int VW, int NV, bool GLOBAL>
 __device__ __forceinline__ void bwd_group_ext(const RouterParams& p, const typename DT::Raw (&raw)[VW * NV],
                                               const typename DT::Raw* row, const float (&Fr)[VW * NV], long long t,
                                               bool valid, int l, int E, float mx, float inv_s, float coef_f,
-                                              float coef_m, const float* s_f, const uint16_t* s_aidx, long long a_base) {
+                                              float coef_m, const float* s_f, const uint16_t* s_aidx, long long a_base,
+                                              float dg_in) {
   constexpr int EPL = VW * NV;
   const int k = p.k;
+  // the pick's loads first: their latency hides behind the row's arithmetic
+  const bool owner = valid && l < k;
+  int col = 0;
+  const float dg = owner ? dg_in : 0.f;
+  typename DT::Raw zr = DT::kNegInf;
+  if (owner) {
+    const long long a = t * k + l;
+    col = s_aidx != nullptr ? int(s_aidx[a - a_base]) : __ldcg(p.idx + a);
+    col = min(max(col, 0), E - 1);
+    if constexpr (GLOBAL) zr = __ldg(row + col);
+    else zr = row[col];
+  }
   float e[EPL];
   row_exp<DT, LPR, EPL>(raw, mx, e);
   float dot[EPL];
@@ -1346,29 +1405,22 @@ __device__ __forceinline__ void bwd_group_ext(const RouterParams& p, const typen
   }
   if constexpr (EPL & 1) dot[EPL - 1] = e[EPL - 1] * Fr[EPL - 1];
   const float wa = inv_s * (inv_s * group_sum<LPR>(tree_sum(dot)));
-  const bool owner = valid && l < k;
-  int col = 0;
-  float ec = 0.f, dg = 0.f;
-  if (owner) {
-    const long long a = t * k + l;
-    col = s_aidx != nullptr ? int(s_aidx[a - a_base]) : __ldcg(p.idx + a);
-    col = min(max(col, 0), E - 1);
-    typename DT::Raw zr;
-    if constexpr (GLOBAL) zr = __ldg(row + col);
-    else zr = row[col];
-    ec = elem_exp(__uint_as_float(DT::bits(zr)), mx);
-    if (p.dgate != nullptr) dg = __ldg(p.dgate + a);
-  }
+  const float ec = owner ? elem_exp(__uint_as_float(DT::bits(zr)), mx) : 0.f;
   float gp = 0.f;
   if (p.dgate != nullptr) {
     if (p.renorm) {
+      // gate_j (dgate_j - G) as e_j sum_m e_m (dgate_j - dgate_m) / Se^2: the
+      // differences term by term, which do not cancel as dgate_j - G can
       const int base = (threadIdx.x & 31) - l;    // lane 0 of the group
       float Se = 0.f, acc = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const float ej = __shfl_sync(0xffffffffu, ec, base + j);
-        const float dj = __shfl_sync(0xffffffffu, dg, base + j);
-        Se += ej;
-        acc = fmaf(ej, dg - dj, acc);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+          const float ej = __shfl_sync(0xffffffffu, ec, base + j);
+          const float dj = __shfl_sync(0xffffffffu, dg, base + j);
+          Se += ej;
+          acc = fmaf(ej, dg - dj, acc);
+        }
       }
       const float inv_Se = rcp_approx(Se);
       gp = owner ? ec * (acc * inv_Se) * inv_Se : 0.f;
@@ -1377,7 +1429,11 @@ __device__ __forceinline__ void bwd_group_ext(const RouterParams& p, const typen
     }
   }
   if (p.masked_p && owner) gp = fmaf(ec * inv_s, coef_m * s_f[col], gp);
-  const float w = fmaf(inv_s, group_sum<LPR>(gp), wa);
+  // S = sum p F + sum gp.  With renormalised gates and no masked term the gate
+  // part sums to zero over the picks (sum_j gate_j (dgate_j - G) = 0), so it
+  // is left out rather than added as rounding noise.
+  const bool gate_sum = p.masked_p || (p.dgate != nullptr && !p.renorm);
+  const float w = gate_sum ? fmaf(inv_s, group_sum<LPR>(gp), wa) : wa;
   if (valid) {
     float* out = p.dlogits + t * (long long)E;
 #pragma unroll
@@ -1385,8 +1441,19 @@ __device__ __forceinline__ void bwd_group_ext(const RouterParams& p, const typen
       const int c0 = col_of<LPR, VW>(v, l, 0);
       if (c0 < E) {
         float d[VW];
+        if constexpr (VW % 2 == 0) {
 #pragma unroll
-        for (int i = 0; i < VW; ++i) d[i] = e[v * VW + i] * fmaf(inv_s, Fr[v * VW + i], -w);
+          for (int i = 0; i < VW; i += 2) {
+            const int j = v * VW + i;
+            const float2 h = fma2(make_float2(inv_s, inv_s), make_float2(Fr[j], Fr[j + 1]), make_float2(-w, -w));
+            const float2 q = mul2(make_float2(e[j], e[j + 1]), h);
+            d[i] = q.x;
+            d[i + 1] = q.y;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < VW; ++i) d[i] = e[v * VW + i] * fmaf(inv_s, Fr[v * VW + i], -w);
+        }
         store_vec_f32<VW>(out + c0, d);
       }
     }
@@ -2345,9 +2412,19 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           if (s == n_st - 1) trace_point(p, kTrBwdFirst);
           const Raw* st = ring + q * stage_elems;
           const int rows_here = min(S, n_rows - s * S);
+          // extended step: each row group's upstream gate gradients are loaded one group ahead
+          float dg_next = 0.f;
+          if constexpr (kExt)
+            dg_next = dgate_of(p, r0 + (long long)s * S + warp * RPW + g, l, warp * RPW + g < rows_here);
           for (int gi = warp; gi * RPW < rows_here; gi += kConsumerWarps) {
             const int ri = gi * RPW + g;
             const bool valid = ri < rows_here;
+            float dg_cur = 0.f;
+            if constexpr (kExt) {
+              dg_cur = dg_next;
+              const int rn = (gi + kConsumerWarps) * RPW + g;
+              dg_next = dgate_of(p, r0 + (long long)s * S + rn, l, rn < rows_here);
+            }
             Raw raw[EPL];
             load_lane<DT, LPR, VW, NV, false>(st + (valid ? ri : 0) * E, E, l, valid, raw);
             if constexpr (kSplit) {
@@ -2372,7 +2449,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
               }
               if constexpr (kExt)
                 bwd_group_ext<DT, LPR, VW, NV, false>(p, raw, st + (valid ? ri : 0) * E, fr, r0 + (long long)s * S + ri,
-                                                      valid, l, E, mx, inv_s, coef_f, coef_m, s_f, s_aidx, a0);
+                                                      valid, l, E, mx, inv_s, coef_f, coef_m, s_f, s_aidx, a0, dg_cur);
               else
                 bwd_group<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, mx, inv_s, p.dlogits);
             }
@@ -2391,7 +2468,7 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           bwd_row_stats<DT, LPR, VW, NV>(raw, mx, inv_s);
           if constexpr (kExt)
             bwd_group_ext<DT, LPR, VW, NV, true>(p, raw, X + (valid ? t : r0) * (long long)E, fr, t, valid, l, E, mx,
-                                                 inv_s, coef_f, coef_m, s_f, nullptr, 0);
+                                                 inv_s, coef_f, coef_m, s_f, nullptr, 0, dgate_of(p, t, l, valid));
           else
             bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, E, mx, inv_s, p.dlogits);
         }

@@ -1,7 +1,8 @@
 """Phase timeline of the persistent router kernel (device timestamps per CTA).
 
-``phase_timeline`` runs the fused step (or the forward, or the dispatch of the
-forward's picks) on logits the caller supplies, with the library's phase
+``phase_timeline`` runs the fused step (or the extended step with a seeded
+bias and upstream gradient of the gates, or the forward, or the dispatch of
+the forward's picks) on logits the caller supplies, with the library's phase
 tracing on (moe_set_trace_buffer), and returns for each CTA the time of each
 phase boundary since the first CTA started.  ``summary`` turns that into the
 median / min / max over CTAs per boundary.  Uses only the public ABI.
@@ -13,7 +14,7 @@ import numpy as np
 import torch
 
 from . import _native
-from .api import Workspace, moe_dispatch, moe_router_fwd, moe_router_step
+from .api import Workspace, moe_dispatch, moe_router_fwd, moe_router_step, moe_router_step_ex
 
 POINTS = ("entry", "first forward stage landed", "forward rows done (warp 0)", "per-CTA partials published",
           "grid barrier passed", "totals, bases, offsets in smem", "(unused)", "first backward stage",
@@ -37,6 +38,15 @@ def phase_timeline(x: torch.Tensor, k: int, alpha: float, capacity_factor: float
     if mode == "step":
         def run():
             moe_router_step(x, k, alpha, capacity_factor, renorm=renorm, n_ranks=n_ranks, ws=ws)
+    elif mode == "step_ex":
+        T = x.shape[0]
+        gen = torch.Generator(device=x.device).manual_seed(7)
+        bias = torch.randn(E, generator=gen, device=x.device) * 0.5
+        dgate = torch.randn(T, k, generator=gen, device=x.device)
+
+        def run():
+            moe_router_step_ex(x, k, alpha, capacity_factor, renorm=renorm, n_ranks=n_ranks, bias=bias,
+                               dgate=dgate, ws=ws)
     elif mode == "fwd":
         def run():
             moe_router_fwd(x, k, alpha, renorm=renorm, n_ranks=n_ranks, ws=ws)
