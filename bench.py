@@ -3,7 +3,7 @@ dispatch + backward over one batch (one launch of moe_router_step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-extra] [--section next_steps|eplb|taot_match]
-                    [--parallelism auto|dp|replicas]
+                    [--parallelism auto|dp|replicas] [--section step_ex [--tokens T]]
 
 Prints one JSON line on rank 0.  With --gpus N > 1 (under torchrun) the ranks
 hold one batch of N * T rows, T per rank (weak scaling), and run the
@@ -537,6 +537,34 @@ def time_next_steps(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     return out
 
 
+def time_step_ex(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
+    """The bias-routed step in one launch alone (moe_router_step_ex: bias routing
+    with the bias updated in place, dispatch, and the backward of a seeded
+    upstream gradient of the gates), as a CUDA graph of `reps` calls over buffer
+    sets rotated at least 3x L2 apart; the first three calls run eagerly."""
+    import moe_expert_routing_router_gb300 as mr
+    esize = 2 if w.dtype == "bf16" else 4
+    step_b = w.T * w.E * (esize + 4) + w.T * w.k * 20
+    x0 = to_device(synth.router_logits(w), w.dtype, torch, device)
+    n_sets = max(2, math.ceil(3 * L2_BYTES / (w.T * w.E * esize)))
+    xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
+    bufs = [out_buffers(w, torch, device) for _ in range(n_sets)]
+    rng = np.random.default_rng(1)
+    bias = torch.from_numpy((rng.standard_normal(w.E) * 0.5).astype(np.float32)).to(device)
+    dgates = [torch.from_numpy(rng.standard_normal((w.T, w.k)).astype(np.float32)).to(device) for _ in range(n_sets)]
+    ws = mr.Workspace(device)
+
+    def call(i):
+        j = i % n_sets
+        mr.moe_router_step_ex(xs[j], w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks,
+                              bias=bias, bias_gamma=1e-3, bias_out=bias, dgate=dgates[j], ws=ws, out=bufs[j])
+
+    us = _graph_us(torch, device, call, reps)
+    gbs = step_b / (us * 1e-6) / 1e9
+    return {"workload": w.name, "T": w.T, "us_per_call": round(us, 2), "tokens_per_s": round(w.T / (us * 1e-6), 1),
+            "algorithmic_bytes": step_b, "achieved_gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm_gbs, 4)}
+
+
 def time_eplb(torch, device, hbm_gbs: float, reps: int = 10) -> dict:
     """The batched EPLB planner (moe_eplb_plan) on 1024 problems of 384 experts,
     both policies, each a CUDA graph of `reps` calls; with the load balance it
@@ -888,7 +916,9 @@ def main() -> int:
     ap.add_argument("--parallelism", choices=("auto", "dp", "replicas"), default="auto",
                     help="with N > 1 ranks: dp (default) splits one batch over the ranks (dp.data_parallel_step); "
                          "replicas runs the fused step independently on every rank")
-    ap.add_argument("--section", choices=("next_steps", "eplb", "taot_match"), default=None,
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="with --section next_steps or step_ex: the workload cut to this many rows")
+    ap.add_argument("--section", choices=("next_steps", "step_ex", "eplb", "taot_match"), default=None,
                     help="print only this part of the extra lines (for --workload), as JSON; no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -899,8 +929,12 @@ def main() -> int:
         device = torch.device("cuda", 0)
         torch.cuda.set_device(device)
         hbm = peaks()["hbm_gbs"]
-        part = (time_next_steps(synth.ROUTER_WORKLOADS[args.workload], torch, device, hbm)
+        wsec = synth.ROUTER_WORKLOADS[args.workload]
+        if args.tokens is not None and args.tokens != wsec.T:
+            wsec = wsec.with_tokens(args.tokens)
+        part = (time_next_steps(wsec, torch, device, hbm)
                 if args.section == "next_steps" else
+                time_step_ex(wsec, torch, device, hbm) if args.section == "step_ex" else
                 time_eplb(torch, device, hbm) if args.section == "eplb" else time_taot_match(torch, device, hbm))
         print(json.dumps(part), flush=True)
         return 0
