@@ -356,9 +356,9 @@ MOE_API moe_status moe_router_step_static(const void* logits, moe_dtype dt, int6
 /* ------------------------------------------------------------------------ */
 
 /* Router forward with two options of the method that moe_router_fwd does not
- * take, computed by a plain (non-cooperative) streaming kernel whose CTAs add
- * their per-expert partials into the workspace with integer atomics (so the
- * results do not depend on scheduling) and whose last CTA writes the outputs:
+ * take, computed by the persistent cooperative kernel of moe_router_fwd (the
+ * forward phases of moe_router_step_ex; per-expert sums added in a fixed
+ * order, so repeated calls give the same bits):
  *
  *   Bias routing ([P1] §4.3, aux-loss-free balancing): each expert carries a
  *   scalar bias b_e on its router logit that steers which experts are picked.
@@ -381,7 +381,8 @@ MOE_API moe_status moe_router_step_static(const void* logits, moe_dtype dt, int6
  * workspace must have been zeroed once by moe_workspace_init and is left
  * reusable).  With bias = NULL and masked_p = 0 the picks and counts equal
  * moe_router_fwd's bit for bit, the floating outputs to rounding.
- * bias_gamma must be finite.  Needs no grid barrier and never waits. */
+ * bias_gamma must be finite.  Its one grid barrier waits with the bounded
+ * wait of moe_router_fwd (an expired wait: moe_get_device_status). */
 MOE_API moe_status moe_router_fwd_ex(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,
                              float alpha, int32_t renorm, int32_t n_ranks,
                              const float* bias, int32_t masked_p, float bias_gamma, float* bias_out,

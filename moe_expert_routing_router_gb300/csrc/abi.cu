@@ -179,8 +179,8 @@ const RouterVariant* pick_variant(moe_dtype dt, int E, bool aligned16) {
   return best;
 }
 
-// The extended step's kernel of a plain variant (the same row layout), or null.
-const void* step_ext_kernel(moe_dtype dt, const RouterVariant* v) {
+// The extended step's kernels of a plain variant (the same row layout), or null.
+const moe::StepExtVariant* step_ext_variant(moe_dtype dt, const RouterVariant* v) {
   int n = 0;
   const moe::StepExtVariant* t =
       dt == MOE_DTYPE_BF16 ? (v->staged ? moe::step_ext_bf16_staged(&n) : moe::step_ext_bf16_direct(&n))
@@ -188,7 +188,7 @@ const void* step_ext_kernel(moe_dtype dt, const RouterVariant* v) {
   for (int i = 0; i < n; ++i)
     if (t[i].LPR == v->LPR && t[i].VW == v->VW && t[i].NV == v->NV && t[i].NR == v->NR &&
         t[i].min_blocks == v->min_blocks)
-      return t[i].step_ext;
+      return &t[i];
   return nullptr;
 }
 
@@ -655,8 +655,9 @@ moe_status moe_router_step_ex(const void* logits, moe_dtype dt, int64_t T, int32
   if ((s = check_ws(ws, ws_bytes, E)) != MOE_OK) return s;
   const RouterVariant* v = pick_variant(dt, E, aligned(logits, 16) && aligned(dlogits, 16));
   if (!v) return fail(MOE_ERR_INVALID, "no kernel variant for E = %d", E);
-  const void* func = step_ext_kernel(dt, v);
-  if (!func) return fail(MOE_ERR_INVALID, "no extended step kernel for E = %d", E);
+  const moe::StepExtVariant* xv = step_ext_variant(dt, v);
+  if (!xv) return fail(MOE_ERR_INVALID, "no extended step kernel for E = %d", E);
+  const void* func = xv->step_ext;
   RouterParams p = base_params(logits, T, E, k);
   p.alpha = alpha;
   p.renorm = renorm < 0 ? (k > 1) : renorm;
@@ -937,43 +938,30 @@ moe_status moe_router_fwd_ex(const void* logits, moe_dtype dt, int64_t T, int32_
   if ((s = check_ws(ws, ws_bytes, E)) != MOE_OK) return s;
   if (!std::isfinite(bias_gamma)) return fail(MOE_ERR_INVALID, "bias_gamma must be finite");
   if ((bias && !aligned(bias, 4)) || (bias_out && !aligned(bias_out, 4))) return fail(MOE_ERR_INVALID, "bias is not 4-byte aligned");
-  const moe::ExtVariant* v = pick_ext_variant(dt, E, aligned(logits, 16));
+  // the extended step's forward alone: the persistent kernel in mode kModeFwdExt
+  const RouterVariant* v = pick_variant(dt, E, aligned(logits, 16));
   if (!v) return fail(MOE_ERR_INVALID, "no kernel variant for E = %d", E);
-  DeviceInfo d;
-  int dev = 0;
-  if ((s = device_info(&d, &dev)) != MOE_OK) return s;
-  int blocks = 0;
-  if ((s = occupancy(v->fwd, moe::kExtFwdThreads, 0, dev, &blocks)) != MOE_OK) return s;
-  const int64_t rows_per_cta = int64_t(moe::kExtFwdWarps) * (moe::kWarp / v->LPR);
-  const int64_t want = (T + rows_per_cta - 1) / rows_per_cta;
-  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(blocks) * d.sms)));
-  static_assert(kGroupHistBytes >= size_t(MOE_MAX_EXPERTS) * 20, "accumulators fit the group-sum region");
-  const WsLayout w = ws_layout(E);
-  char* base = static_cast<char*>(ws);
-  moe::FwdExParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.logits = logits;
-  p.T = T;
-  p.E = E;
-  p.k = k;
-  p.renorm = renorm < 0 ? (k > 1) : renorm;
-  p.masked_p = masked_p != 0;
-  p.bias = bias;
+  const moe::StepExtVariant* xv = step_ext_variant(dt, v);
+  if (!xv) return fail(MOE_ERR_INVALID, "no extended forward kernel for E = %d", E);
+  RouterParams p = base_params(logits, T, E, k);
   p.alpha = alpha;
+  p.renorm = renorm < 0 ? (k > 1) : renorm;
   p.n_ranks = n_ranks;
-  p.gamma = bias_gamma;
+  p.bias = bias;
+  p.bias_gamma = bias_gamma;
   p.bias_out = bias_out;
+  p.masked_p = masked_p != 0;
   p.idx = idx; p.gate = gate; p.counts = counts; p.f = f; p.P = P; p.scalars = scalars; p.rank_load = rank_load;
-  // The accumulators share the group-sum region: both kernels find it zero at
-  // launch and leave it zero, so calls of either kind can follow each other.
-  p.acc_hi = reinterpret_cast<unsigned long long*>(base + w.group_hist);
-  p.acc_lo = p.acc_hi + E;
-  p.acc_count = reinterpret_cast<int32_t*>(p.acc_lo + E);
-  p.done = &reinterpret_cast<moe::Ctrl*>(base + w.ctrl)->ext_done;
-  void* args[] = {&p};
-  cudaError_t e = cudaLaunchKernel(v->fwd, dim3(grid), dim3(moe::kExtFwdThreads), args, 0, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
-  return MOE_OK;
+  bind_ws(p, ws, E);
+  Geometry geo;
+  if ((s = persistent_geometry(v, dt, T, E, k, false, &geo, xv->fwd_ext)) != MOE_OK) return s;
+  p.G = geo.G;
+  p.n_groups = (p.G + moe::kGroupCtas - 1) / moe::kGroupCtas;
+  p.rows_per_stage = geo.rows_per_stage;
+  p.n_slots = geo.n_slots;
+  p.asg_cap = geo.asg_cap;
+  p.rstat_cap = geo.rstat_cap;
+  return launch_persistent(xv->fwd_ext, p, geo.smem, stream);
 }
 
 moe_status moe_router_bwd_full(const void* logits, moe_dtype dt, int64_t T, int32_t E, int32_t k,

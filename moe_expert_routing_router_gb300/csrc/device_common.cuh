@@ -30,9 +30,8 @@ constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
 struct Ctrl {
   unsigned long long sync;      // [31:0] arrivals, [63:32] error bits
   unsigned long long done;      // CTAs whose per-expert outputs are written (the launch's CTA 0 resets it)
-  unsigned long long ext_done;  // CTAs of a bias-routing / masked-P forward that have published their partials
   unsigned long long bwd_done;  // CTAs of a split fused step that have added their sums of p (the last resets it)
-  unsigned long long pad[60];
+  unsigned long long pad[61];
 };
 static_assert(sizeof(Ctrl) == 512, "control block is 512 bytes");
 

@@ -1,10 +1,9 @@
-// fp32 instances of the bias-routing / masked-P forward and the full backward.
+// fp32 instances of the full backward.
 #include "router_ext.cuh"
 #include "router_table.h"
 
 #define MOE_EXT_VARIANT(DT, LPR, VW, NV, VEC)                                         \
-  {LPR, VW, NV, VEC, reinterpret_cast<const void*>(&::moe::router_fwd_ex_kernel<DT, LPR, VW, NV>), \
-   reinterpret_cast<const void*>(&::moe::router_bwd_full_kernel<DT, LPR, VW, NV>)}
+  {LPR, VW, NV, VEC, reinterpret_cast<const void*>(&::moe::router_bwd_full_kernel<DT, LPR, VW, NV>)}
 
 namespace moe {
 

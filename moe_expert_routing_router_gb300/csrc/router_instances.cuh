@@ -26,7 +26,8 @@ constexpr const void* split_step_kernel() {
 
 #define MOE_STEP_EXT_VARIANT_ITEM(DT, LPR, VW, NV, NR, STAGED, MINB)                                                  \
   {LPR, VW, NV, NR, STAGED, MINB,                                                                                     \
-   reinterpret_cast<const void*>(&::moe::router_persistent_kernel<DT, LPR, VW, NV, NR, ::moe::kModeStepExt, STAGED, MINB>)},
+   reinterpret_cast<const void*>(&::moe::router_persistent_kernel<DT, LPR, VW, NV, NR, ::moe::kModeStepExt, STAGED, MINB>), \
+   reinterpret_cast<const void*>(&::moe::router_persistent_kernel<DT, LPR, VW, NV, NR, ::moe::kModeFwdExt, STAGED, MINB>)},
 
 #define MOE_STEP_EXT_TABLE(NAME, ARRAY)                      \
   const StepExtVariant* NAME(int* n) {                       \

@@ -85,13 +85,13 @@ constexpr unsigned long long kDrainNs = 1000000000ull;
 
 // kModeSplit (with kModeStep, renormalised gates): the forward takes only the
 // top-k and the gates; the backward forms each row's softmax sum and P.
-// kModeExt (with kModeStep): the extended step -- selection on fp32(z) + b,
+// kModeExt: the extended step (with kModeStep) -- selection on fp32(z) + b,
 // masked P when asked, the bias update, and the backward of the gates' upstream
-// gradient added to the aux loss's.
+// gradient added to the aux loss's -- or its forward alone (with kModeFwd).
 enum : int {
   kModeFwd = 1, kModeDispatch = 2, kModeBwd = 4, kModeSplit = 8, kModeExt = 16,
   kModeStep = kModeFwd | kModeDispatch | kModeBwd, kModeStepSplit = kModeStep | kModeSplit,
-  kModeStepExt = kModeStep | kModeExt
+  kModeStepExt = kModeStep | kModeExt, kModeFwdExt = kModeFwd | kModeExt
 };
 
 // The type of the pick slots: the 32-bit selection keys of the biased scores
@@ -971,23 +971,30 @@ __device__ __forceinline__ void fwd_groups_ext(const RouterParams& p, const type
     }
   }
   __syncwarp();
-  // The picks stand iff exactly k elements have a value image at or above the
-  // k-th pick's (then they are the picks: a lane that ran out of cached keys
-  // hid none, and no other score shares the k-th one's image) and the picks'
-  // images are all different (then their order is the scores' order).  Else
-  // the row is redone on the full 64-bit keys.
+  // With bf16 logits and no bias the scores are bf16 values, whose images have
+  // 16 zero low bits: the keys hold the whole scores and the rounds are exact
+  // up to a lane that ran out of cached keys.  Otherwise the picks stand iff
+  // exactly k elements have a value image at or above the k-th pick's (then
+  // they are the picks: a lane that ran out of cached keys hid none, and no
+  // other score shares the k-th one's image) and the picks' images are all
+  // different (then their order is the scores' order).  Rows that fail are
+  // redone on the full 64-bit keys.
   int col[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
-    const uint32_t thr = w[r] & kSelValueMask;
+    const uint32_t mine = l < k ? s_pick[(r * GPW + g) * kMaxK + l] : 0u;
+    col[r] = int(1023u - (mine & 0x3ffu));
+    const bool whole = sizeof(Raw) == 2 && p.bias == nullptr;
+    const uint32_t thr = whole ? w[r] : (w[r] & kSelValueMask);
     int cnt = 0;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) cnt += key[r][i] >= thr ? 1 : 0;
     cnt = group_sum_int<LPR>(cnt);
-    const uint32_t mine = l < k ? s_pick[(r * GPW + g) * kMaxK + l] : 0u;
-    const uint32_t next = l + 1 < k ? s_pick[(r * GPW + g) * kMaxK + l + 1] : 0u;
-    const bool dup = l + 1 < k && (mine & kSelValueMask) == (next & kSelValueMask);
-    col[r] = int(1023u - (mine & 0x3ffu));
+    bool dup = false;
+    if (!whole) {
+      const uint32_t next = l + 1 < k ? s_pick[(r * GPW + g) * kMaxK + l + 1] : 0u;
+      dup = l + 1 < k && (mine & kSelValueMask) == (next & kSelValueMask);
+    }
     if (__any_sync(0xffffffffu, valid[r] && (cnt != k || dup))) {
       const long long m64 = exact_topk_ext<DT, LPR, VW, NV, GLOBAL>(row[r], bl, E, k, l, valid[r]);
       col[r] = l < k ? Fp32::key_col(m64) : 0;

@@ -27,18 +27,18 @@ const RouterVariant* router_variants_fp32_direct(int* n);
 struct StepExtVariant {
   int LPR, VW, NV, NR, staged, min_blocks;
   const void* step_ext;    // persistent kernel, the extended step
+  const void* fwd_ext;     // persistent kernel, the extended step's forward alone (moe_router_fwd_ex)
 };
 const StepExtVariant* step_ext_bf16_staged(int* n);
 const StepExtVariant* step_ext_bf16_direct(int* n);
 const StepExtVariant* step_ext_fp32_staged(int* n);
 const StepExtVariant* step_ext_fp32_direct(int* n);
 
-// Kernels of the forward with bias routing / masked P and of the full
-// backward, per row layout.  vec: 16-byte rows read VW elements per load.
+// Kernels of the full backward, per row layout.  vec: 16-byte rows read VW
+// elements per load.
 struct ExtVariant {
   int LPR, VW, NV;
   int vec;
-  const void* fwd;         // router_fwd_ex_kernel
   const void* bwd;         // router_bwd_full_kernel
 };
 const ExtVariant* ext_variants_bf16(int* n);
