@@ -172,15 +172,13 @@ __device__ void pack_warp_bpl(const EplbSmem& s, int N, int G, float* tot_out, P
         bb = b;
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ot = __shfl_xor_sync(0xffffffffu, bt, off);
-      const int ob = __shfl_xor_sync(0xffffffffu, bb, off);
-      if (ob != 0x7fffffff && (bb == 0x7fffffff || ot < bt || (ot == bt && ob < bb))) {
-        bt = ot;
-        bb = ob;
-      }
-    }
+    // The warp's lightest open bin by two warp reductions: the smallest total
+    // (totals are sums of non-negative weights, so their bit patterns order as
+    // their values; a lane with no open bin offers the largest pattern), then
+    // the lowest bin index holding it.
+    const uint32_t img = bb == 0x7fffffff ? 0xffffffffu : __float_as_uint(bt);
+    const uint32_t mt = __reduce_min_sync(0xffffffffu, img);
+    bb = int(__reduce_min_sync(0xffffffffu, img == mt ? uint32_t(bb) : 0xffffffffu));
     if ((bb & 31) == lane) {
       const float xi = s.x[item];
 #pragma unroll
