@@ -29,6 +29,7 @@ namespace moe {
 namespace {
 
 constexpr int kEplbThreads = 256;
+constexpr int kEplbCountSort = 128;   // sets of up to this many items are sorted by counting
 
 struct EplbSmem {
   int32_t* w;        // [E]  weights of the current sub-problem's experts (local order)
@@ -36,15 +37,24 @@ struct EplbSmem {
   int32_t* cnt;      // [E]  copies per local expert
   int32_t* p2l;      // [num_phys] item -> local expert (item < n: first copy)
   float* x;          // [max(num_phys, num_groups)] item weights of a packing
-  int32_t* order;    // [max(num_phys, num_groups)] sorted position -> item
+  int32_t* order;    // [max(num_phys, num_groups), for the global policy rounded up to a power of two] sorted position -> item
   int32_t* gbin;     // [num_groups] node of each group
   int32_t* ginv;     // [num_groups] node-major: (node, position) -> group
+  int order_cap;     // entries of order
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) / 16 * 16; }
 
 __host__ __device__ inline size_t eplb_layout(int E, int num_phys, int num_groups, EplbSmem* s, char* base) {
   const int items = num_phys > num_groups ? num_phys : num_groups;
+  // the global policy sorts all num_phys items at once, padded to a power of
+  // two for the bitonic network; the hierarchical policy's sets are sorted by
+  // counting (sort_items falls back to it wherever the padding is missing)
+  int items_p2 = items;
+  if (num_groups == 0 && items > kEplbCountSort) {
+    items_p2 = 1;
+    while (items_p2 < items) items_p2 <<= 1;
+  }
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off += align16(bytes); return base ? base + o : nullptr; };
   char* w = take(4u * E);
@@ -52,7 +62,7 @@ __host__ __device__ inline size_t eplb_layout(int E, int num_phys, int num_group
   char* cnt = take(4u * E);
   char* p2l = take(4u * num_phys);
   char* x = take(4u * items);
-  char* order = take(4u * items);
+  char* order = take(4u * items_p2);
   char* gbin = take(4u * (num_groups > 0 ? num_groups : 1));
   char* ginv = take(4u * (num_groups > 0 ? num_groups : 1));
   if (s) {
@@ -64,6 +74,7 @@ __host__ __device__ inline size_t eplb_layout(int E, int num_phys, int num_group
     s->order = reinterpret_cast<int32_t*>(order);
     s->gbin = reinterpret_cast<int32_t*>(gbin);
     s->ginv = reinterpret_cast<int32_t*>(ginv);
+    s->order_cap = items_p2;
   }
   return off;
 }
@@ -125,22 +136,64 @@ struct EplbCta {
   }
 };
 
+// Item a comes before item b in the packing order: the larger weight first,
+// ties to the lower index; the padding (indices >= N) last.
+__device__ __forceinline__ bool packs_before(const float* x, int N, int a, int b) {
+  if (a >= N) return false;
+  if (b >= N) return true;
+  const float xa = x[a], xb = x[b];
+  return xa > xb || (xa == xb && a < b);
+}
+
+// order[0..P) = the indices 0..N-1 in packing order, then the padding: a
+// bitonic network by one warp (out of line, so that it does not weigh on the
+// register allocation of the kernel's greedy loops).
+__device__ __noinline__ void bitonic_order(const float* x, int32_t* order, int N, int P, int lane) {
+  for (int i = lane; i < P; i += 32) order[i] = i;
+  __syncwarp();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = lane; t < P / 2; t += 32) {
+        const int i = 2 * t - (t & (stride - 1));            // the pair (i, i + stride)
+        const int j = i + stride;
+        const int a = order[i], b = order[j];
+        const bool up = (i & size) == 0;                     // this block sorts in packing order
+        if (up ? packs_before(x, N, b, a) : packs_before(x, N, a, b)) {
+          order[i] = b;
+          order[j] = a;
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
 // The packing order of every active problem's N items in s.x (weight
-// descending, ties to the lower index): each item counts the items that sort
-// before it.  All threads of the CTA take part.
+// descending, ties to the lower index).  Up to kEplbCountSort items, or where
+// the order array has no room for the padding, each item counts the items
+// that sort before it (all threads of the CTA, problem by problem); beyond,
+// warp q sorts problem q's item indices, padded to a power of two, with a
+// bitonic network in shared memory.  Called by all threads of the CTA.
 __device__ void sort_items(const EplbCta& cta, int N) {
   __syncthreads();
-  for (int q = 0; q < cta.n_active; ++q) {
-    const EplbSmem s = cta.at(q);
-    for (int i = threadIdx.x; i < N; i += blockDim.x) {
-      const float xi = s.x[i];
-      int r = 0;
-      for (int j = 0; j < N; ++j) {
-        const float xj = s.x[j];
-        r += (xj > xi || (xj == xi && j < i)) ? 1 : 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int P = 1;
+  while (P < N) P <<= 1;
+  if (N <= kEplbCountSort || P > cta.at(0).order_cap) {
+    for (int q = 0; q < cta.n_active; ++q) {
+      const EplbSmem s = cta.at(q);
+      for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        const float xi = s.x[i];
+        int r = 0;
+        for (int j = 0; j < N; ++j) {
+          const float xj = s.x[j];
+          r += (xj > xi || (xj == xi && j < i)) ? 1 : 0;
+        }
+        s.order[r] = i;
       }
-      s.order[r] = i;
     }
+  } else if (warp < cta.n_active) {
+    bitonic_order(cta.at(warp).x, cta.at(warp).order, N, P, lane);
   }
   __syncthreads();
 }
