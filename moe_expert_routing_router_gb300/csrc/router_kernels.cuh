@@ -1028,16 +1028,24 @@ __device__ __forceinline__ void fwd_groups_ext(const RouterParams& p, const type
   }
 }
 
+// Where a split step forms its renormalised gates: in the backward from 12
+// elements per lane (E > 256: the forward is bound by instruction issue, the
+// backward by memory, and the step at E = 384 is about 1 % faster), in the
+// forward below (at E = 256, whose shorter backward carries k = 8, the
+// backward's gates made the step 6 % slower).
+template <int EPL>
+constexpr bool kSplitGatesInBwd = EPL >= 12;
+
 // The forward of the large-E bf16 variants (32 lanes per row, rows in a ring
 // stage), in three parts: fast_topk_rows (the candidate path for K picks),
-// full_topk_row (the full path, out of line) and row_tail (gates, idx and
-// gate stores, pick counts, dispatch ids, row statistics).  A stage's rows
+// full_topk_row (the full path, out of line) and row_tail (idx and, unless
+// split, gate stores, pick counts, dispatch ids, row statistics).  A stage's rows
 // take the candidate path one after the other and the ones it rejects are
 // redone by the full path after the loop, so the per-row code has no rare
 // branch in it.  SOFTMAX: the forward also forms the row's softmax (p into
-// pacc, (max, 1 / sum) into s_rstat); without it (the fused step with
-// renormalised gates, whose backward forms them) only the row max goes to
-// s_rstat and the gates come from the picks' numerators alone.
+// pacc, (max, 1 / sum) into s_rstat) and the gates; without it (the fused step
+// with renormalised gates, whose backward forms the softmax sums and the
+// gates) only the picks and the row max are kept.
 
 // The candidate path for NR row groups: K rounds over the 64 candidates, then
 // the check.  Returns (uniformly) whether every row passed; then top and
@@ -1109,9 +1117,9 @@ __device__ __forceinline__ void row_tail(const RouterParams& p, const typename D
   for (int r = 0; r < NR; ++r) {
     const float mx = DT::key_value(top[r]);
     const bool owner = l < k;
-    const float ej = owner ? elem_exp(DT::key_value(mine[r]), mx) : 0.f;
-    float denom, inv_s = 0.f;
+    float inv_s = 0.f;
     if constexpr (SOFTMAX) {
+      const float ej = owner ? elem_exp(DT::key_value(mine[r]), mx) : 0.f;
       Raw raw[EPL];
       load_lane<DT, LPR, VW, NV, false>(row[r], p.E, l, valid[r], raw);
       float e[EPL];
@@ -1119,15 +1127,18 @@ __device__ __forceinline__ void row_tail(const RouterParams& p, const typename D
       const float s = group_sum<LPR>(tree_sum(e));
       inv_s = valid[r] ? rcp_approx(s) : 0.f;
       axpy2(pacc, e, inv_s);
-      denom = p.renorm ? owners_sum<LPR>(ej) : s;
-    } else {
-      denom = owners_sum<LPR>(ej);
+      const float denom = p.renorm ? owners_sum<LPR>(ej) : s;
+      if (valid[r] && owner) p.gate[t[r] * k + l] = ej * rcp_approx(denom);
+    } else if constexpr (!kSplitGatesInBwd<EPL>) {
+      const float ej = owner ? elem_exp(DT::key_value(mine[r]), mx) : 0.f;
+      const float denom = owners_sum<LPR>(ej);
+      if (valid[r] && owner) p.gate[t[r] * k + l] = ej * rcp_approx(denom);
     }
+    // (otherwise a split step's renormalised gates are formed in its backward: split_gates)
     if (valid[r] && owner) {
       const int col = DT::key_col(mine[r]);
       const long long a = t[r] * k + l;
       p.idx[a] = col;
-      p.gate[a] = ej * rcp_approx(denom);
       atomicAdd(&s_hist[col], 1);
       if (s_aidx != nullptr) s_aidx[a - a_base] = uint16_t(col);
     }
@@ -1470,6 +1481,27 @@ __device__ __forceinline__ void bwd_group_ext(const RouterParams& p, const typen
     const float F = coef_f * s_f[col];
     __stcs(p.dlogits + t * (long long)E + col, fmaf(ec, fmaf(inv_s, F, -w), gp));
   }
+}
+
+// A split step's renormalised gates of one row, in its backward (the forward
+// is bound by instruction issue, the backward by memory): lane j < k takes
+// pick j from the dispatch ids in shared memory (or the idx the forward
+// wrote), its logit from the row, and forms gate_j = e_j / sum_m e_m with the
+// arithmetic the forward would have used (the same row max, elem_exp).
+template <class DT, int LPR>
+__device__ __forceinline__ void split_gates(const RouterParams& p, const typename DT::Raw* row, long long t, bool valid,
+                                            int l, float mx, const uint16_t* s_aidx, long long a_base) {
+  const int k = p.k;
+  const bool owner = valid && l < k;
+  float ej = 0.f;
+  if (owner) {
+    const long long a = t * k + l;
+    int col = s_aidx != nullptr ? int(s_aidx[a - a_base]) : __ldcg(p.idx + a);
+    col = min(max(col, 0), p.E - 1);
+    ej = elem_exp(__uint_as_float(DT::bits(row[col])), mx);
+  }
+  const float denom = owners_sum<LPR>(ej);
+  if (owner) p.gate[t * k + l] = ej * rcp_approx(denom);
 }
 
 // A CTA's sum of p of one expert (x >= 0) into the fixed-point totals: its
@@ -2445,6 +2477,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
                 mx = group_max<LPR>(m);
               }
               bwd_group_split<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, mx, pacc_b, p.dlogits);
+              if constexpr (kSplitGatesInBwd<EPL>)
+                split_gates<DT, LPR>(p, st + (valid ? ri : 0) * E, r0 + (long long)s * S + ri, valid, l, mx, s_aidx, a0);
             } else {
               float mx, inv_s;
               if (s_rstat != nullptr) {
