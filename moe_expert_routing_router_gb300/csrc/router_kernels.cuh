@@ -865,7 +865,7 @@ __device__ __forceinline__ void fwd_groups(const RouterParams& p, const typename
 // fp32(z) + b ([P1] §4.3; 64-bit keys, the rounds of fwd_groups, and for a lane
 // that won twice the exact count of its keys above the k-th pick), softmax,
 // gates and P from the unbiased z.  With masked P ([P2] §3.1) each pick adds
-// its p into the warp's per-expert sums s_pm instead of pacc.  bl: the bias of
+// its p into the warp's per-expert sums s_pm instead of pacc, in a fixed order.  bl: the bias of
 // the lane's columns.
 // ---------------------------------------------------------------------------
 template <class DT, int LPR, int VW, int NV, bool GLOBAL>
@@ -1022,7 +1022,16 @@ __device__ __forceinline__ void fwd_groups_ext(const RouterParams& p, const type
       p.gate[a] = ej * rcp_approx(denom);
       atomicAdd(&s_hist[c], 1);
       if (s_aidx != nullptr) s_aidx[a - a_base] = uint16_t(c);
-      if (p.masked_p) atomicAdd(&s_pm[c], ej * inv_s);
+    }
+    // Masked P: the picks' p into the warp's sums, one row group after the
+    // other (two groups' picks may share an expert), so the order of the
+    // fp32 additions, and the result, is the same on every call.
+    if (p.masked_p) {
+#pragma unroll
+      for (int gg = 0; gg < GPW; ++gg) {
+        if (g == gg && valid[r] && owner) s_pm[c] += ej * inv_s;
+        __syncwarp();
+      }
     }
     if (s_rstat != nullptr && valid[r] && l == 0) s_rstat[t[r] - r_base] = make_float2(mx[r], inv_s);
   }

@@ -293,3 +293,23 @@ def test_scores_equal_in_their_upper_bits(mr, E, dtype):
     got = mr.moe_router_fwd_ex(x, k, 0.01, bias=torch.from_numpy(bias).cuda(), bias_gamma=0.5, bias_out=True)
     torch.cuda.synchronize()
     check_forward(got, oracle_forward_ex(logits, dtype, k, 0.01, True, 0, bias, False, 0.5), 0)
+
+
+@pytest.mark.parametrize("name", ["zipf-top2-T65536-E64", "zipf-ep64-top6-T262144-E384"])
+def test_repeated_calls_are_bit_identical(mr, name):
+    """The per-expert sums are added in a fixed order (masked P included, whose
+    picks from several rows of a warp may share an expert): two calls give the
+    same bits in every output."""
+    w, logits = workload_inputs(name, 20011)
+    x = to_device(logits, w.dtype)
+    bias = torch.from_numpy(seeded_bias(w.E)).cuda()
+    for masked in (False, True):
+        a = mr.moe_router_fwd_ex(x, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, bias=bias, masked_p=masked,
+                                 bias_gamma=GAMMA, bias_out=True)
+        b = mr.moe_router_fwd_ex(x, w.k, w.alpha, renorm=int(w.renorm), n_ranks=w.n_ranks, bias=bias, masked_p=masked,
+                                 bias_gamma=GAMMA, bias_out=True)
+        torch.cuda.synchronize()
+        for key in ("idx", "gate", "counts", "f", "P", "scalars", "bias_out"):
+            ta, tb = a[key].cpu(), b[key].cpu()
+            assert torch.equal(ta.view(torch.int32) if ta.dtype == torch.float32 else ta,
+                               tb.view(torch.int32) if tb.dtype == torch.float32 else tb), (key, masked)
