@@ -53,7 +53,13 @@
 extern "C" {
 #endif
 
-#define MOE_ROUTER_ABI_VERSION 1
+/* Version of this interface (moe_abi_version returns it).
+ *   1: the router step, its parts, the Sinkhorn plan, bias routing, the full
+ *      backward, EPLB, TAOT Phase 2 and the shard combine;
+ *   2: adds moe_router_step_ex (the bias-routed step in one launch),
+ *      moe_shard_capacity_base and moe_dispatch_sharded (the capacity of a
+ *      batch split over data-parallel ranks).  Version 1 calls are unchanged. */
+#define MOE_ROUTER_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(native_lib):
 
 
 def test_abi_version(native_lib):
-    assert native_lib.moe_abi_version() == 1
+    assert native_lib.moe_abi_version() == 2
 
 
 def test_capacity_worked_example_through_the_abi(native_lib):
