@@ -1389,6 +1389,61 @@ __device__ __forceinline__ float dgate_of(const RouterParams& p, long long t, in
   return valid && l < p.k && p.dgate != nullptr ? __ldg(p.dgate + t * p.k + l) : 0.f;
 }
 
+// The extended backward's gate terms of a warp's rows of one ring stage, ahead
+// of the rows (pre-pass): 8 lanes per row and 4 rows at a time, lane j of a
+// row taking pick j (its column, its numerator from the row, its upstream
+// gradient: the loads of 4 rows in flight together), and gp_j = p_j gamma_j as
+// bwd_group_ext forms it (renormalised gates: the differences dgate_j -
+// dgate_m over the row's 8-lane segment).  gp_out[slot * kMaxK + j], slot =
+// n * RPW + g for the warp's n-th row group of the stage, its group g.  Needs
+// the forward's row statistics in shared memory.
+template <class DT, int LPR>
+__device__ __forceinline__ void ext_gate_prepass(const RouterParams& p, const typename DT::Raw* st, long long t0,
+                                                 int rs0, int rows_here, int warp, int n_rows, const float2* s_rstat,
+                                                 const uint16_t* s_aidx, long long a_base, float coef_m,
+                                                 const float* s_f, float* gp_out) {
+  constexpr int RPW = kWarp / LPR;
+  const int lane = threadIdx.x & 31;
+  const int k = p.k, E = p.E;
+  for (int base = 0; base < n_rows; base += kWarp / kMaxK) {
+    const int slot = base + lane / kMaxK, j = lane % kMaxK;
+    const int n = slot / RPW, g = slot % RPW;
+    const int ri = (warp + n * kConsumerWarps) * RPW + g;
+    const bool owner = slot < n_rows && ri < rows_here && j < k;
+    float ec = 0.f, dg = 0.f, inv_s = 0.f;
+    int col = 0;
+    if (owner) {
+      const long long a = (t0 + ri) * k + j;
+      col = s_aidx != nullptr ? int(s_aidx[a - a_base]) : __ldcg(p.idx + a);
+      col = min(max(col, 0), E - 1);
+      const float2 rs = s_rstat[rs0 + ri];
+      inv_s = rs.y;
+      ec = elem_exp(__uint_as_float(DT::bits(st[ri * E + col])), rs.x);
+      if (p.dgate != nullptr) dg = __ldg(p.dgate + a);
+    }
+    float gp = 0.f;
+    if (p.dgate != nullptr) {
+      if (p.renorm) {
+        float Se = ec, acc = 0.f;
+#pragma unroll
+        for (int o = 1; o < kMaxK; ++o) {
+          const float ep = __shfl_xor_sync(0xffffffffu, ec, o);
+          const float dp = __shfl_xor_sync(0xffffffffu, dg, o);
+          Se += ep;
+          acc = fmaf(ep, dg - dp, acc);
+        }
+        const float inv_Se = rcp_approx(Se);
+        gp = owner ? ec * (acc * inv_Se) * inv_Se : 0.f;
+      } else {
+        gp = owner ? ec * inv_s * dg : 0.f;
+      }
+    }
+    if (p.masked_p && owner) gp = fmaf(ec * inv_s, coef_m * s_f[col], gp);
+    if (slot < n_rows) gp_out[slot * kMaxK + j] = gp;
+  }
+  __syncwarp();
+}
+
 // Backward of one row group of the extended step: dlogits = p * (dp - sum p dp)
 // for L = sum_j dgate_j * gate_j + grad_scale * L_aux (picks and f fixed).  Fr
 // holds coef * f on the lane's columns (zero with masked P).  Lane j < k of the
@@ -1406,7 +1461,7 @@ __device__ __forceinline__ void bwd_group_ext(const RouterParams& p, const typen
                                               const typename DT::Raw* row, const float (&Fr)[VW * NV], long long t,
                                               bool valid, int l, int E, float mx, float inv_s, float coef_f,
                                               float coef_m, const float* s_f, const uint16_t* s_aidx, long long a_base,
-                                              float dg_in) {
+                                              float dg_in, const float* gp_pre, int slot) {
   constexpr int EPL = VW * NV;
   const int k = p.k;
   // the pick's loads first: their latency hides behind the row's arithmetic
@@ -1434,7 +1489,9 @@ __device__ __forceinline__ void bwd_group_ext(const RouterParams& p, const typen
   const float wa = inv_s * (inv_s * group_sum<LPR>(tree_sum(dot)));
   const float ec = owner ? elem_exp(__uint_as_float(DT::bits(zr)), mx) : 0.f;
   float gp = 0.f;
-  if (p.dgate != nullptr) {
+  if (gp_pre != nullptr) {
+    gp = owner ? gp_pre[slot * kMaxK + l] : 0.f;   // formed ahead by ext_gate_prepass
+  } else if (p.dgate != nullptr) {
     if (p.renorm) {
       // gate_j (dgate_j - G) as e_j sum_m e_m (dgate_j - dgate_m) / Se^2: the
       // differences term by term, which do not cancel as dgate_j - G can
@@ -1455,7 +1512,7 @@ __device__ __forceinline__ void bwd_group_ext(const RouterParams& p, const typen
       gp = owner ? ec * inv_s * dg : 0.f;
     }
   }
-  if (p.masked_p && owner) gp = fmaf(ec * inv_s, coef_m * s_f[col], gp);
+  if (gp_pre == nullptr && p.masked_p && owner) gp = fmaf(ec * inv_s, coef_m * s_f[col], gp);
   // S = sum p F + sum gp.  With renormalised gates and no masked term the gate
   // part sums to zero over the picks (sum_j gate_j (dgate_j - G) = 0), so it
   // is left out rather than added as rounding noise.
@@ -2460,18 +2517,36 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           if (s == n_st - 1) trace_point(p, kTrBwdFirst);
           const Raw* st = ring + q * stage_elems;
           const int rows_here = min(S, n_rows - s * S);
-          // extended step: each row group's upstream gate gradients are loaded one group ahead
+          // extended step: with one row per warp (32 lanes per row) the gate
+          // terms of the warp's rows of the stage are formed ahead into its pick
+          // slots when they fit (E = 384: 296 -> 286 us per step); else, and
+          // with several rows per warp, whose per-row work is shared anyway,
+          // each row group's upstream gate gradients are loaded one group ahead
+          const float* gp_pre = nullptr;
           float dg_next = 0.f;
-          if constexpr (kExt)
-            dg_next = dgate_of(p, r0 + (long long)s * S + warp * RPW + g, l, warp * RPW + g < rows_here);
+          if constexpr (kExt) {
+            const int per = kConsumerWarps * RPW;
+            const int n_rows_w = rows_here > warp * RPW ? (rows_here - warp * RPW + per - 1) / per * RPW : 0;
+            if (LPR == kWarp && s_rstat != nullptr && n_rows_w * kMaxK <= kPickSlotsPerWarp) {
+              float* gp_buf = reinterpret_cast<float*>(s_pick_w);
+              __syncwarp();
+              ext_gate_prepass<DT, LPR>(p, st, r0 + (long long)s * S, s * S, rows_here, warp, n_rows_w, s_rstat,
+                                        s_aidx, a0, coef_m, s_f, gp_buf);
+              gp_pre = gp_buf;
+            } else {
+              dg_next = dgate_of(p, r0 + (long long)s * S + warp * RPW + g, l, warp * RPW + g < rows_here);
+            }
+          }
           for (int gi = warp; gi * RPW < rows_here; gi += kConsumerWarps) {
             const int ri = gi * RPW + g;
             const bool valid = ri < rows_here;
             float dg_cur = 0.f;
             if constexpr (kExt) {
-              dg_cur = dg_next;
-              const int rn = (gi + kConsumerWarps) * RPW + g;
-              dg_next = dgate_of(p, r0 + (long long)s * S + rn, l, rn < rows_here);
+              if (gp_pre == nullptr) {
+                dg_cur = dg_next;
+                const int rn = (gi + kConsumerWarps) * RPW + g;
+                dg_next = dgate_of(p, r0 + (long long)s * S + rn, l, rn < rows_here);
+              }
             }
             Raw raw[EPL];
             load_lane<DT, LPR, VW, NV, false>(st + (valid ? ri : 0) * E, E, l, valid, raw);
@@ -2499,7 +2574,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
               }
               if constexpr (kExt)
                 bwd_group_ext<DT, LPR, VW, NV, false>(p, raw, st + (valid ? ri : 0) * E, fr, r0 + (long long)s * S + ri,
-                                                      valid, l, E, mx, inv_s, coef_f, coef_m, s_f, s_aidx, a0, dg_cur);
+                                                      valid, l, E, mx, inv_s, coef_f, coef_m, s_f, s_aidx, a0, dg_cur,
+                                                      gp_pre, (gi - warp) / kConsumerWarps * RPW + g);
               else
                 bwd_group<DT, LPR, VW, NV>(raw, fr, r0 + (long long)s * S + ri, valid, l, E, mx, inv_s, p.dlogits);
             }
@@ -2518,7 +2594,8 @@ __global__ void __launch_bounds__(kThreads, MINB) router_persistent_kernel(const
           bwd_row_stats<DT, LPR, VW, NV>(raw, mx, inv_s);
           if constexpr (kExt)
             bwd_group_ext<DT, LPR, VW, NV, true>(p, raw, X + (valid ? t : r0) * (long long)E, fr, t, valid, l, E, mx,
-                                                 inv_s, coef_f, coef_m, s_f, nullptr, 0, dgate_of(p, t, l, valid));
+                                                 inv_s, coef_f, coef_m, s_f, nullptr, 0, dgate_of(p, t, l, valid),
+                                                 nullptr, 0);
           else
             bwd_group<DT, LPR, VW, NV>(raw, fr, t, valid, l, E, mx, inv_s, p.dlogits);
         }
