@@ -142,9 +142,9 @@ def test_bias_update_in_place_over_steps(mr):
                                        (512, 4, "bf16"), (1000, 8, "fp32"), (1023, 7, "bf16")])
 def test_ties_and_edge_shapes(mr, E, k, dtype):
     """Integer logits and integer biases: the fp32 sums tie everywhere, so the
-    lower-index rule decides most picks (and, at 12 or more elements per lane,
-    the cached selection hands most rows to the exact one); E not a multiple of
-    the vector width, k = E and E = 1 are covered."""
+    lower-index rule decides most picks (and the collision check hands many
+    rows to the 64-bit keys); E not a multiple of the vector width, k = E and
+    E = 1 are covered."""
     rng = np.random.default_rng(E * 10 + k)
     T = 777
     z = rng.integers(-3, 4, size=(T, E)).astype(np.float32)
@@ -280,7 +280,8 @@ def test_interleaved_with_the_fused_step_on_one_workspace(mr):
 def test_scores_equal_in_their_upper_bits(mr, E, dtype):
     """Scores that differ only below the upper 22 bits of their image (fp32
     logits 1.5 + j * 2^-20, or bf16 logits with biases of that size): the
-    cached selection must see the collision and leave the row to the exact one."""
+    32-bit selection keys must see the collision and leave the row to the
+    64-bit keys."""
     rng = np.random.default_rng(E)
     T, k = 517, 6
     if dtype == "fp32":
