@@ -106,7 +106,11 @@ def _place(phy2log_local, bins, pos, gpu0: int, S: int, out: np.ndarray) -> None
 
 
 def plan_global(weights, num_phys: int, num_gpus: int) -> dict:
-    """Global policy: replicate over all experts, pack the replicas onto all GPUs."""
+    """Global policy: replicate over all experts, pack the replicas onto all GPUs.
+
+    Pinned by: the hand case [6, 2, 1, 3] onto 6 slots of 2 GPUs (6 / 6); the
+    plan invariants (S slots per GPU, copies equal counts, loads add up).
+    """
     E = len(weights)
     S = num_phys // num_gpus
     p2l, count = replicate_experts(weights, num_phys)
@@ -118,7 +122,11 @@ def plan_global(weights, num_phys: int, num_gpus: int) -> dict:
 
 
 def plan_hierarchical(weights, num_phys: int, num_gpus: int, num_nodes: int, num_groups: int) -> dict:
-    """Hierarchical policy: groups onto nodes, then replication and packing within each node."""
+    """Hierarchical policy: groups onto nodes, then replication and packing within each node.
+
+    Pinned by: the page's groups [9, 7, 5, 3] on 2 nodes worked by hand (12 / 12);
+    the plan invariants, with every copy on the node its group went to.
+    """
     w = [int(x) for x in weights]
     E = len(w)
     gsize = E // num_groups
@@ -145,7 +153,8 @@ def plan_hierarchical(weights, num_phys: int, num_gpus: int, num_nodes: int, num
 
 def plan(weights, num_phys: int, num_gpus: int, num_nodes: int, num_groups: int) -> dict:
     """The page's choice of policy: hierarchical when num_groups > 0 and the node
-    count divides the group count, global otherwise."""
+    count divides the group count, global otherwise.  Pinned by: both branches
+    taken in the plan pins (3 nodes do not divide 8 groups: global)."""
     if num_groups > 0 and num_groups % num_nodes == 0:
         return plan_hierarchical(weights, num_phys, num_gpus, num_nodes, num_groups)
     return plan_global(weights, num_phys, num_gpus)

@@ -33,7 +33,11 @@ SCALAR_NAMES = ("l_aux", "balance", "cv", "max_over_mean", "min_over_mean",
 
 
 def widen(logits: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact float64 copy of fp32 logits or of bf16 bit patterns (uint16)."""
+    """Exact float64 copy of fp32 logits or of bf16 bit patterns (uint16).
+
+    Pinned by: torch's bfloat16 -> float32 conversion over every finite bf16
+    pattern (subnormals, -0.0); hand values (0x3F80 = 1, 0xC040 = -3).
+    """
     if dtype == "bf16":
         return bf16_bits_to_f32(logits).astype(np.float64)
     if dtype == "fp32":
@@ -64,7 +68,11 @@ def top_k(z: np.ndarray, k: int) -> np.ndarray:
 
 
 def gates(p: np.ndarray, idx: np.ndarray, renorm: bool) -> np.ndarray:
-    """Gate weights of the selected experts: p, or p / sum of the picked p."""
+    """Gate weights of the selected experts: p, or p / sum of the picked p.
+
+    [P1] §4.4; [P2] §3.1.  Pinned by: hand examples (z = [0, ln 3]: top-1 gate
+    3/4, renormalised top-2 [3/4, 1/4]; z = [ln 2, 0, ln 6]: [6/9, 2/9] plain).
+    """
     g = np.take_along_axis(p, idx, axis=1)
     if renorm:
         g = g / g.sum(axis=1, keepdims=True)
@@ -91,17 +99,27 @@ def mean_router_prob(p: np.ndarray) -> np.ndarray:
 
 
 def balance(f: np.ndarray, P: np.ndarray) -> float:
-    """N * sum_i f_i P_i: equals 1 under uniform routing ([P2] §2.2)."""
+    """N * sum_i f_i P_i: equals 1 under uniform routing ([P2] §2.2).
+
+    Pinned by: uniform P and uniform f both give 1; the two-token hand example 5/4.
+    """
     return float(len(f) * np.sum(f * P))
 
 
 def aux_loss(f: np.ndarray, P: np.ndarray, alpha: float) -> float:
-    """L_aux = alpha * N * sum_i f_i P_i.  [P2] §2.2; [P1] §4.2."""
+    """L_aux = alpha * N * sum_i f_i P_i.  [P2] §2.2; [P1] §4.2.
+
+    Pinned by: alpha at balance 1; the two-token hand example (0.0125 at alpha 0.01);
+    the finite differences of the gradient, which differentiate it.
+    """
     return alpha * balance(f, P)
 
 
 def load_cv(loads: np.ndarray) -> float:
-    """Coefficient of variation std/mean (population std) of a load vector.  [P3] §3.1, §5.1."""
+    """Coefficient of variation std/mean (population std) of a load vector.  [P3] §3.1, §5.1.
+
+    Pinned by: closed forms ([1, 3] -> 1/2, [0, 0, 0, 4] -> sqrt 3, equal loads -> 0).
+    """
     loads = np.asarray(loads, dtype=np.float64)
     mean = loads.mean()
     return float(loads.std() / mean) if mean > 0 else 0.0
@@ -151,6 +169,8 @@ def router_forward(logits: np.ndarray, dtype: str, k: int, alpha: float,
     Returns idx [T,k], gate [T,k], counts [E], f [E], P [E], the scalars
     (l_aux, balance, cv, max_over_mean, min_over_mean, rank_cv,
     rank_max_over_mean) and rank_load [n_ranks].
+    Pinned by its parts' pins and, whole, by the two-token hand example, the
+    uniform-P and uniform-f cases and sum f = sum P = 1 on every workload recipe.
     """
     z = widen(logits, dtype)
     T, E = z.shape
@@ -166,7 +186,8 @@ def router_forward(logits: np.ndarray, dtype: str, k: int, alpha: float,
 
 def aux_loss_of_logits(z: np.ndarray, f: np.ndarray, alpha: float, grad_scale: float = 1.0) -> float:
     """g * L_aux as a function of the logits with f held fixed (f carries no gradient,
-    [P1] §4.2, [P2] §2.2).  Used by the finite-difference pin of ``aux_loss_grad``."""
+    [P1] §4.2, [P2] §2.2).  Used by the finite-difference pin of ``aux_loss_grad``;
+    it composes softmax, mean_router_prob and aux_loss, each pinned on its own."""
     return grad_scale * aux_loss(f, mean_router_prob(softmax(z)), alpha)
 
 
@@ -190,7 +211,7 @@ def aux_loss_grad(logits: np.ndarray, dtype: str, f: np.ndarray, alpha: float,
 
 def cv_grade(cv: float) -> str:
     """CV bands of [P3] §5.1: below 0.1 excellent, [0.1, 0.3) good, [0.3, 0.5) fair,
-    0.5 and above severely imbalanced."""
+    0.5 and above severely imbalanced.  Pinned by: the band edges as golden cases."""
     if cv < 0.1:
         return "excellent"
     if cv < 0.3:
@@ -201,11 +222,17 @@ def cv_grade(cv: float) -> str:
 
 
 def balance_degree(max_over_mean: float) -> float:
-    """[P3] §5.1: 1 - (max load - mean load) / mean load."""
+    """[P3] §5.1: 1 - (max load - mean load) / mean load.
+
+    Pinned by: 1 at the mean, 0 at twice the mean, 1/4 at 1.75.
+    """
     return 1.0 - (max_over_mean - 1.0)
 
 
 def is_ratio_imbalanced(max_over_mean: float) -> bool:
-    """[P1] §5.4: max_tokens_per_expert / mean_tokens_per_expert above 2 means imbalance."""
+    """[P1] §5.4: max_tokens_per_expert / mean_tokens_per_expert above 2 means imbalance.
+
+    Pinned by: the [P1] §5.3 log line is flagged; a ratio of exactly 2 is not.
+    """
     return max_over_mean > 2.0
 

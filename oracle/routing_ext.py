@@ -42,6 +42,8 @@ def selection_scores(logits: np.ndarray, dtype: str, bias: np.ndarray) -> np.nda
 
     The logits widen exactly to fp32 (bf16 and fp32 inputs both do); the sum
     is one fp32 addition, rounded to nearest even.
+    Pinned by: 1 + 2^-24 rounds to 1 (a tie the lower expert wins), 1 + 2^-23
+    does not; brute-force top-k of z + b on integer inputs.
     """
     z32 = R.widen(logits, dtype).astype(np.float32)
     b32 = np.asarray(bias, dtype=np.float32)
@@ -76,7 +78,10 @@ def bias_update(bias: np.ndarray, counts: np.ndarray, T: int, k: int, gamma: flo
 
 
 def pick_mask(idx: np.ndarray, E: int) -> np.ndarray:
-    """m[t, i] = 1 if expert i is one of token t's picks, else 0."""
+    """m[t, i] = 1 if expert i is one of token t's picks, else 0.
+
+    Pinned by: the masked-P hand case and the k == E closed form, which go through it.
+    """
     m = np.zeros((idx.shape[0], E), dtype=np.float64)
     np.put_along_axis(m, np.asarray(idx), 1.0, axis=1)
     return m
@@ -100,6 +105,9 @@ def router_forward_ex(logits: np.ndarray, dtype: str, k: int, alpha: float,
 
     Same outputs as ``router.router_forward``; with ``gamma`` also
     ``bias_out`` = ``bias_update(bias, counts, T, k, gamma)``.
+    Pinned by: a zero bias with unmasked P reproduces router.router_forward
+    exactly; with a bias P and the gates stay those of the unbiased softmax
+    ([P1] §4.3: the bias moves the choice only); the masked-P hand case.
     """
     z = R.widen(logits, dtype)
     T, E = z.shape
@@ -127,6 +135,8 @@ def grad_wrt_probs(p: np.ndarray, idx: np.ndarray, f: np.ndarray, alpha: float, 
     Gate part: gate_j = p[t, i_j] (no renormalisation) or p[t, i_j] / S_t with
     S_t = sum_m p[t, i_m]; by the quotient rule
         d gate_j / d p[t, i_m] = [j == m] / S_t - p[t, i_j] / S_t^2.
+    Pinned by: central differences in p of the gate and aux terms (picks fixed),
+    for plain and renormalised gates, with masked and unmasked P.
     """
     E = p.shape[1]
     f = np.asarray(f, dtype=np.float64)
@@ -151,7 +161,11 @@ def grad_wrt_probs(p: np.ndarray, idx: np.ndarray, f: np.ndarray, alpha: float, 
 
 
 def softmax_backward(p: np.ndarray, dp: np.ndarray) -> np.ndarray:
-    """dz[t, j] = sum_i dp[t, i] * p[t, i] * (delta_ij - p[t, j]) (the softmax Jacobian)."""
+    """dz[t, j] = sum_i dp[t, i] * p[t, i] * (delta_ij - p[t, j]) (the softmax Jacobian).
+
+    Pinned by: torch autograd through torch.softmax in float64 (random rows and
+    a saturated one).
+    """
     return p * (dp - (p * dp).sum(axis=1, keepdims=True))
 
 
@@ -178,7 +192,8 @@ def full_loss_of_logits(z: np.ndarray, f: np.ndarray, alpha: float, grad_scale: 
                         idx: np.ndarray, dgate: np.ndarray | None, renorm: bool,
                         masked_p: bool = False) -> float:
     """sum_{t,j} dgate[t,j] * gate[t,j](z) + grad_scale * alpha * E * sum_i f_i P_i(z),
-    picks and f held fixed.  Used by the finite-difference pin of ``router_backward_full``."""
+    picks and f held fixed.  Used by the finite-difference pin of ``router_backward_full``;
+    it composes softmax, gates and the (masked) P, each pinned on its own."""
     T, E = z.shape
     k = idx.shape[1]
     p = R.softmax(z)

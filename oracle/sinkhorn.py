@@ -31,7 +31,11 @@ STATUS_NO_MASS = 1
 
 
 def supply_demand(load: np.ndarray) -> tuple[np.ndarray, np.ndarray, bool]:
-    """Unit-mass supply a (overloaded ranks) and demand b (idle ranks) of one load vector."""
+    """Unit-mass supply a (overloaded ranks) and demand b (idle ranks) of one load vector.
+
+    Pinned by: hand cases ([3, 1, 1, 3] -> a = [1, 0, 0, 1] / 2, b = [0, 1, 1, 0] / 2;
+    [5, 1, 0, 2] -> b = [0, 1, 2, 0] / 3); equal loads carry no mass.
+    """
     load = np.asarray(load, dtype=np.float64)
     mean = load.mean()
     a = np.maximum(load - mean, 0.0)
@@ -43,7 +47,11 @@ def supply_demand(load: np.ndarray) -> tuple[np.ndarray, np.ndarray, bool]:
 
 
 def topology_cost(R: int, ranks_per_node: int, lam: float) -> np.ndarray:
-    """W[r, s]: 0 on the same rank, 1 within a node, ``lam`` across nodes."""
+    """W[r, s]: 0 on the same rank, 1 within a node, ``lam`` across nodes.
+
+    Pinned by: the 4-rank, 2-per-node matrix written out by hand; the intra- to
+    cross-node kernel ratio at eps = lambda.
+    """
     node = np.arange(R) // ranks_per_node
     W = np.where(node[:, None] == node[None, :], 1.0, float(lam))
     np.fill_diagonal(W, 0.0)
@@ -51,7 +59,7 @@ def topology_cost(R: int, ranks_per_node: int, lam: float) -> np.ndarray:
 
 
 def gibbs_kernel(W: np.ndarray, eps: float) -> np.ndarray:
-    """M = exp(-W / eps)."""
+    """M = exp(-W / eps).  Pinned by: exp(-1/2) and exp(-5) at eps = 2 by hand; the kernel ratio."""
     return np.exp(-W / float(eps))
 
 
@@ -73,13 +81,17 @@ def sinkhorn_knopp(a: np.ndarray, b: np.ndarray, M: np.ndarray, iters: int) -> t
 
 
 def transport_plan(u: np.ndarray, M: np.ndarray, v: np.ndarray) -> np.ndarray:
-    """T = diag(u) M diag(v)."""
+    """T = diag(u) M diag(v).  Pinned by: the plan's marginals a and b; the independent dual solve."""
     return u[:, None] * M * v[None, :]
 
 
 def taot_phase1(loads: np.ndarray, ranks_per_node: int, lam: float, eps: float | None = None,
                 iters: int = 50) -> dict:
-    """Batched Phase 1 over microbatches: loads [B, R] -> u, v [B, R], plan [B, R, R], status [B]."""
+    """Batched Phase 1 over microbatches: loads [B, R] -> u, v [B, R], plan [B, R, R], status [B].
+
+    Pinned by its parts' pins; 50 iterations reach the 10,000-iteration plan;
+    equal loads give status 1 and an empty plan.
+    """
     loads = np.atleast_2d(np.asarray(loads, dtype=np.float64))
     B, R = loads.shape
     if eps is None or eps <= 0:

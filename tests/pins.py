@@ -800,3 +800,142 @@ def check_match_column_first_claim(match, sinkhorn) -> None:
             row.append(match.residual_imbalance(_row_first_match(w, plan, R, 8, K)))
     assert np.mean(col) < np.mean(row), (np.mean(col), np.mean(row))
     assert np.mean(col) < 0.05, np.mean(col)
+
+
+# ----------------------------------------------------------------------------- conversions, helpers, measures
+
+def check_widen_library(router) -> None:
+    """bf16 bit patterns widen to the values torch's own bfloat16 -> float32
+    conversion gives, for every finite pattern (subnormals and -0.0 included),
+    and fp32 logits pass through unchanged.  By hand: 0x3F80 is 1.0, 0xC040 is
+    -3.0, 0x0001 is 2^-133, 0x7F7F is (2 - 2^-7) * 2^127."""
+    import torch
+
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):                     # the NaN patterns, left out below
+        want = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).float().numpy().astype(np.float64)
+        got = router.widen(bits.reshape(256, 256), "bf16").ravel()
+    fin = np.isfinite(want)
+    assert fin.sum() == (1 << 16) - 2 * 128                   # 2 infinities and 254 NaNs left out
+    np.testing.assert_array_equal(got[fin], want[fin])
+    assert np.array_equal(np.signbit(got[fin]), np.signbit(want[fin]))
+    hand = router.widen(np.array([[0x3F80, 0xC040, 0x0001, 0x7F7F]], dtype=np.uint16), "bf16")[0]
+    assert list(hand) == [1.0, -3.0, 2.0 ** -133, (2.0 - 2.0 ** -7) * 2.0 ** 127]
+    x = np.random.default_rng(19).standard_normal((3, 5)).astype(np.float32)
+    np.testing.assert_array_equal(router.widen(x, "fp32"), x.astype(np.float64))
+
+
+def check_balance_degree_hand(router) -> None:
+    """[P3] §5.1's balance degree 1 - (max - mean) / mean: 1 when the peak is the
+    mean, 0 when it is twice the mean, 0.25 at 1.75; [P1] §5.4's ratio flag is
+    strictly above 2."""
+    assert router.balance_degree(1.0) == 1.0
+    assert router.balance_degree(2.0) == 0.0
+    assert router.balance_degree(1.75) == 0.25
+    assert router.balance_degree(4.21875) == -2.21875         # the [P1] §5.3 log line's max/mean
+    assert not router.is_ratio_imbalanced(2.0) and router.is_ratio_imbalanced(2.0 + 2.0 ** -40)
+
+
+def check_softmax_backward_autograd(ext) -> None:
+    """The softmax Jacobian-vector product equals torch's autograd through
+    torch.softmax in float64, on random rows and on a saturated row."""
+    import torch
+
+    rng = np.random.default_rng(21)
+    z = rng.standard_normal((6, 7)) * 3.0
+    z[0, 2] = 60.0                                            # one dominant logit
+    dp = rng.standard_normal((6, 7))
+    zt = torch.tensor(z, dtype=torch.float64, requires_grad=True)
+    torch.softmax(zt, dim=1).backward(torch.tensor(dp, dtype=torch.float64))
+    p = np.exp(z - z.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(ext.softmax_backward(p, dp), zt.grad.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def check_grad_wrt_probs_finite_difference(ext, router) -> None:
+    """dL/dp of L(p) = sum dgate * gate(p) + g * alpha * E * sum_i f_i P_i(p), picks
+    fixed, against central differences of that loss evaluated through
+    router.gates and the (masked or unmasked) P, p treated as free variables."""
+    rng = np.random.default_rng(22)
+    T, E, k, alpha, g = 4, 5, 3, 0.3, 1.3
+    p = rng.random((T, E)) + 0.1
+    idx = np.array([rng.permutation(E)[:k] for _ in range(T)])
+    f = rng.random(E)
+    f /= f.sum()
+    dgate = rng.standard_normal((T, k))
+
+    def loss(q, renorm, masked):
+        P = ext.mean_router_prob_masked(q, idx, k) if masked else router.mean_router_prob(q)
+        return float((dgate * router.gates(q, idx, renorm)).sum()) + g * alpha * E * float((f * P).sum())
+
+    h = 1e-6
+    for renorm in (False, True):
+        for masked in (False, True):
+            got = ext.grad_wrt_probs(p, idx, f, alpha, g, T, k, dgate, renorm, masked)
+            fd = np.zeros_like(p)
+            for t in range(T):
+                for i in range(E):
+                    qp, qm = p.copy(), p.copy()
+                    qp[t, i] += h
+                    qm[t, i] -= h
+                    fd[t, i] = (loss(qp, renorm, masked) - loss(qm, renorm, masked)) / (2 * h)
+            np.testing.assert_allclose(got, fd, rtol=1e-7, atol=1e-8)
+
+
+def check_supply_demand_hand(sinkhorn) -> None:
+    """loads [3, 1, 1, 3]: mean 2, supply [1, 0, 0, 1] / 2, demand [0, 1, 1, 0] / 2;
+    [5, 1, 0, 2]: mean 2, supply [3, 0, 0, 0] / 3, demand [0, 1, 2, 0] / 3; equal
+    loads have no mass."""
+    a, b, ok = sinkhorn.supply_demand(np.array([3.0, 1.0, 1.0, 3.0]))
+    assert ok and list(a) == [0.5, 0.0, 0.0, 0.5] and list(b) == [0.0, 0.5, 0.5, 0.0]
+    a, b, ok = sinkhorn.supply_demand(np.array([5.0, 1.0, 0.0, 2.0]))
+    assert ok and list(a) == [1.0, 0.0, 0.0, 0.0]
+    np.testing.assert_allclose(b, [0.0, 1.0 / 3.0, 2.0 / 3.0, 0.0], rtol=1e-15)
+    _, _, ok = sinkhorn.supply_demand(np.full(5, 7.0))
+    assert not ok
+
+
+def check_topology_cost_hand(sinkhorn) -> None:
+    """Four ranks, two per node, lambda = 10: W written out by hand; its Gibbs
+    kernel at eps = 2 is exp(-W / 2) element by element."""
+    W = sinkhorn.topology_cost(4, 2, 10.0)
+    want = np.array([[0, 1, 10, 10], [1, 0, 10, 10], [10, 10, 0, 1], [10, 10, 1, 0]], dtype=np.float64)
+    np.testing.assert_array_equal(W, want)
+    M = sinkhorn.gibbs_kernel(W, 2.0)
+    assert M[0, 0] == 1.0 and M[0, 1] == math.exp(-0.5) and M[1, 3] == math.exp(-5.0)
+
+
+def check_residual_imbalance_hand(match) -> None:
+    """(max - mean) / mean: [6, 4, 5, 5] -> 0.2, equal loads -> 0, [9, 1] -> 0.8."""
+    assert abs(match.residual_imbalance([6, 4, 5, 5]) - 0.2) < 1e-15
+    assert match.residual_imbalance([3, 3, 3]) == 0.0
+    assert abs(match.residual_imbalance([9, 1]) - 0.8) < 1e-15
+
+
+def check_forward_ex_reductions(ext, router) -> None:
+    """router_forward_ex reduces to the plain forward: with a zero bias and
+    unmasked P every output equals router.router_forward's.  With a bias only
+    the choice of experts moves ([P1] §4.3): P stays the plain mean of the
+    unbiased softmax, and each gate is the unbiased p of its pick (k = 1), or
+    those p renormalised over the picks (k > 1)."""
+    rng = np.random.default_rng(35)
+    T, E = 40, 7
+    z = rng.standard_normal((T, E)).astype(np.float32)
+    for k in (1, 3):
+        plain = router.router_forward(z, "fp32", k, 0.1, n_ranks=7)
+        ex = ext.router_forward_ex(z, "fp32", k, 0.1, n_ranks=7, bias=np.zeros(E, np.float32))
+        for key in ("idx", "gate", "counts", "f", "P", "rank_load"):
+            np.testing.assert_array_equal(ex[key], plain[key], err_msg=key)
+        for key in ("l_aux", "balance", "cv", "max_over_mean", "rank_cv"):
+            assert ex[key] == plain[key], key
+        b = np.zeros(E, np.float32)
+        b[2], b[5] = 3.0, -3.0
+        biased = ext.router_forward_ex(z, "fp32", k, 0.1, bias=b)
+        np.testing.assert_array_equal(biased["P"], plain["P"])
+        assert (biased["idx"] != plain["idx"]).any()
+        p = np.exp(z.astype(np.float64) - z.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        for t in range(T):
+            picked = p[t, biased["idx"][t]]
+            want = picked if k == 1 else picked / picked.sum()
+            np.testing.assert_allclose(biased["gate"][t], want, rtol=1e-14)

@@ -62,6 +62,20 @@ MUTANTS = {
         [(R, "aux_loss_grad", lambda logits, dtype, f, alpha, grad_scale=1.0:
           grad_scale * (alpha * len(f) / R.widen(logits, dtype).shape[0]) * R.softmax(R.widen(logits, dtype)) * f[None, :])],
         [lambda: pins.check_grad_finite_difference(R), lambda: pins.check_grad_structure(R)]),
+    "bf16 bit patterns read as IEEE half precision": (
+        [(R, "widen", lambda logits, dtype: np.asarray(logits).view(np.float16).astype(np.float64)
+          if dtype == "bf16" else _orig_widen(logits, dtype))],
+        [lambda: pins.check_widen_library(R)]),
+    "bf16 widened without the 16-bit shift": (
+        [(R, "widen", lambda logits, dtype: np.asarray(logits).astype(np.uint32).view(np.float32).astype(np.float64)
+          if dtype == "bf16" else _orig_widen(logits, dtype))],
+        [lambda: pins.check_widen_library(R)]),
+    "balance degree over the max instead of the mean": (
+        [(R, "balance_degree", lambda r: 1.0 - (r - 1.0) / r)],
+        [lambda: pins.check_balance_degree_hand(R)]),
+    "imbalance flag at a ratio of 2 and above": (
+        [(R, "is_ratio_imbalanced", lambda r: r >= 2.0)],
+        [lambda: pins.check_balance_degree_hand(R), lambda: pins.check_log_example(R)]),
     "CV with the sample (n-1) deviation": (
         [(R, "load_cv", lambda x: float(np.std(np.asarray(x, float), ddof=1) / np.mean(x)))],
         [lambda: pins.check_cv_closed_forms(R)]),
@@ -94,16 +108,26 @@ MUTANTS = {
         [lambda: pins.check_sinkhorn_topology_kernel(S)]),
     "supply and demand swapped": (
         [(S, "supply_demand", lambda load: _orig_sd(load)[1::-1] + (_orig_sd(load)[2],))],
-        [lambda: pins.check_sinkhorn_marginals(S, _loads()), lambda: pins.check_sinkhorn_two_rank(S)]),
+        [lambda: pins.check_supply_demand_hand(S), lambda: pins.check_sinkhorn_marginals(S, _loads()),
+         lambda: pins.check_sinkhorn_two_rank(S)]),
+    "supply and demand left unnormalised": (
+        [(S, "supply_demand", lambda load: _unnormalised_sd(load))],
+        [lambda: pins.check_supply_demand_hand(S)]),
     "cross-node cost and intra-node cost swapped": (
         [(S, "topology_cost", lambda R_, rpn, lam: np.where(_orig_tc(R_, rpn, lam) == 1.0, lam, np.where(_orig_tc(R_, rpn, lam) == lam, 1.0, 0.0)))],
-        [lambda: pins.check_sinkhorn_topology_kernel(S)]),
+        [lambda: pins.check_topology_cost_hand(S), lambda: pins.check_sinkhorn_topology_kernel(S)]),
+    "topology cost 1 on the diagonal (a rank's own slot priced as intra-node)": (
+        [(S, "topology_cost", lambda R_, rpn, lam: np.where(np.eye(R_, dtype=bool), 1.0, _orig_tc(R_, rpn, lam)))],
+        [lambda: pins.check_topology_cost_hand(S)]),
     "bias added in float64 instead of fp32": (
         [(X, "selection_scores", lambda logits, dtype, bias: R.widen(logits, dtype) + np.asarray(bias, np.float64)[None, :])],
         [lambda: pins.check_biased_sum_is_fp32(X)]),
     "bias subtracted from the logits": (
         [(X, "selection_scores", lambda logits, dtype, bias: _orig_sel(logits, dtype, -np.asarray(bias, np.float32)))],
         [lambda: pins.check_biased_topk_bruteforce(X), lambda: pins.check_biased_topk_dominant(X)]),
+    "softmax and gates taken on the biased scores": (
+        [(X, "router_forward_ex", lambda *a, **kw: _softmax_on_biased(*a, **kw))],
+        [lambda: pins.check_forward_ex_reductions(X, R)]),
     "bias update with the wrong sign": (
         [(X, "bias_update", lambda bias, counts, T, k, gamma: _orig_bu(bias, counts, T, k, -gamma))],
         [lambda: pins.check_bias_update_hand(X), lambda: pins.check_bias_update_balances(X, R)]),
@@ -116,13 +140,17 @@ MUTANTS = {
         [lambda: pins.check_masked_p_closed_forms(X, R)]),
     "renormalised gate gradient without the p/S^2 term": (
         [(X, "grad_wrt_probs", lambda *a: _no_quotient_term(*a))],
-        [lambda: pins.check_full_grad_finite_difference(X, R)]),
+        [lambda: pins.check_grad_wrt_probs_finite_difference(X, R), lambda: pins.check_full_grad_finite_difference(X, R)]),
     "masked aux gradient without the mask": (
         [(X, "grad_wrt_probs", lambda p, idx, f, a, g, T, k, dg, rn, masked: _orig_gwp(p, idx, f, a, g * (1.0 / k if masked else 1.0), T, k, dg, rn, False))],
-        [lambda: pins.check_full_grad_finite_difference(X, R)]),
+        [lambda: pins.check_grad_wrt_probs_finite_difference(X, R), lambda: pins.check_full_grad_finite_difference(X, R)]),
     "softmax backward without the row-sum term": (
         [(X, "softmax_backward", lambda p, dp: p * dp)],
-        [lambda: pins.check_full_grad_finite_difference(X, R), lambda: pins.check_full_grad_structure(X, R)]),
+        [lambda: pins.check_softmax_backward_autograd(X), lambda: pins.check_full_grad_finite_difference(X, R),
+         lambda: pins.check_full_grad_structure(X, R)]),
+    "softmax backward with the row sum of dp instead of p*dp": (
+        [(X, "softmax_backward", lambda p, dp: p * (dp - dp.sum(axis=1, keepdims=True)))],
+        [lambda: pins.check_softmax_backward_autograd(X)]),
     "packing takes the lightest item first": (
         [(B, "balanced_packing", lambda w, n: _orig_bp([-x for x in w], n)[:2] + (_totals(w, *_orig_bp([-x for x in w], n)[:2], n),))],
         [lambda: pins.check_packing_worked_example(B)]),
@@ -135,6 +163,9 @@ MUTANTS = {
     "replication ties to the higher index": (
         [(B, "replicate_experts", lambda w, n: _ties_high(w, n))],
         [lambda: pins.check_replication_hand_case(B)]),
+    "residual imbalance over the max instead of the mean": (
+        [(M, "residual_imbalance", lambda rl: float((np.max(rl) - np.mean(rl)) / np.max(rl)))],
+        [lambda: pins.check_residual_imbalance_hand(M)]),
     "matching ignores the topology": (
         [(M, "match", lambda w, plan, R, ranks_per_node, K: _orig_match(w, plan, R, R, K))],
         [lambda: pins.check_match_hand_arbitration(M)]),
@@ -242,6 +273,15 @@ def _ties_high(w, num_phys):
 
 
 _orig_sel = X.selection_scores
+_orig_fwd_ex = X.router_forward_ex
+
+
+def _softmax_on_biased(logits, dtype, k, alpha, renorm=None, n_ranks=0, bias=None, masked_p=False, gamma=None):
+    if bias is None:
+        return _orig_fwd_ex(logits, dtype, k, alpha, renorm, n_ranks, bias, masked_p, gamma)
+    s = X.selection_scores(logits, dtype, bias)             # the biased scores feed the softmax too
+    return _orig_fwd_ex(s, "fp32", k, alpha, renorm, n_ranks, np.zeros_like(np.asarray(bias, np.float32)),
+                        masked_p, gamma)
 _orig_bu = X.bias_update
 _orig_gwp = X.grad_wrt_probs
 
@@ -257,10 +297,18 @@ def _no_quotient_term(p, idx, f, alpha, grad_scale, T, k, dgate, renorm, masked_
 
 
 _orig_grad = R.aux_loss_grad
+_orig_widen = R.widen
 _orig_dispatch = D.dispatch
 _orig_sk = S.sinkhorn_knopp
 _orig_sd = S.supply_demand
 _orig_tc = S.topology_cost
+
+
+def _unnormalised_sd(load):
+    a, b, ok = _orig_sd(load)
+    load = np.asarray(load, dtype=np.float64)
+    mean = load.mean()
+    return (np.maximum(load - mean, 0.0), np.maximum(mean - load, 0.0), ok)
 
 
 _orig_stats = R.batch_statistics

@@ -67,3 +67,11 @@ def test_grad_matches_finite_differences():
 
 def test_grad_rows_sum_to_zero_and_uniform_case():
     pins.check_grad_structure(oracle.router)
+
+
+def test_widen_matches_torch_bf16():
+    pins.check_widen_library(oracle.router)
+
+
+def test_balance_degree_and_ratio_flag():
+    pins.check_balance_degree_hand(oracle.router)

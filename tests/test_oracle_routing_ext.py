@@ -40,3 +40,15 @@ def test_full_backward_structure():
 
 def test_masked_p_hand_case():
     pins.check_masked_p_hand(X, R)
+
+
+def test_softmax_backward_matches_autograd():
+    pins.check_softmax_backward_autograd(X)
+
+
+def test_grad_wrt_probs_finite_differences():
+    pins.check_grad_wrt_probs_finite_difference(X, R)
+
+
+def test_forward_ex_reduces_to_the_plain_forward():
+    pins.check_forward_ex_reductions(X, R)

@@ -40,3 +40,11 @@ def test_fifty_iterations_reach_the_fixed_point():
 def test_zero_mass_status():
     out = oracle.sinkhorn.taot_phase1(np.full((2, 16), 7.0), 8, 10.0)
     assert list(out["status"]) == [1, 1] and not out["plan"].any() and not out["u"].any()
+
+
+def test_supply_demand_hand_cases():
+    pins.check_supply_demand_hand(oracle.sinkhorn)
+
+
+def test_topology_cost_hand_case():
+    pins.check_topology_cost_hand(oracle.sinkhorn)

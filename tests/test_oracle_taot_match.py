@@ -21,3 +21,7 @@ def test_invariants():
 def test_column_first_beats_row_first():
     from oracle import sinkhorn
     pins.check_match_column_first_claim(taot_match, sinkhorn)
+
+
+def test_residual_imbalance_hand_cases():
+    pins.check_residual_imbalance_hand(taot_match)
