@@ -2,8 +2,8 @@
 dispatch + backward over one batch (one launch of moe_router_step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-extra] [--section next_steps|eplb|taot_match]
-                    [--parallelism auto|dp|replicas] [--section step_ex [--tokens T]]
+                    [--workload NAME] [--no-extra] [--parallelism auto|dp|replicas]
+                    [--section step|next_steps|step_ex|eplb|taot_match [--tokens T]]
 
 Prints one JSON line on rank 0.  With --gpus N > 1 (under torchrun) the ranks
 hold one batch of N * T rows, T per rank (weak scaling), and run the
@@ -537,6 +537,34 @@ def time_next_steps(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     return out
 
 
+def time_step(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
+    """The fused step alone (moe_router_step: forward, dispatch and the aux-loss
+    backward in one launch), as a CUDA graph of `reps` calls over buffer sets
+    rotated at least 3x L2 apart; the first three calls run eagerly.  With
+    --tokens this is a smaller case of the same kernel instantiation."""
+    import moe_expert_routing_router_gb300 as mr
+    step_b = algorithmic_bytes(w)
+    x0 = to_device(synth.router_logits(w), w.dtype, torch, device)
+    n_sets = max(2, math.ceil(3 * L2_BYTES / step_b))
+    xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
+    bufs = [out_buffers(w, torch, device) for _ in range(n_sets)]
+    ws = mr.Workspace(device)
+
+    def call(i):
+        j = i % n_sets
+        mr.moe_router_step(xs[j], w.k, w.alpha, w.capacity_factor, renorm=int(w.renorm), n_ranks=w.n_ranks,
+                           grad_scale=1.0, ws=ws, out=bufs[j])
+
+    us = _graph_us(torch, device, call, reps)
+    flags = mr.moe_get_device_status(ws)
+    if flags:
+        raise RuntimeError(f"device wait expired during the benchmark (flags {flags})")
+    gbs = step_b / (us * 1e-6) / 1e9
+    return {"workload": w.name, "T": w.T, "n_sets": n_sets, "us_per_call": round(us, 2),
+            "tokens_per_s": round(w.T / (us * 1e-6), 1), "algorithmic_bytes": step_b,
+            "achieved_gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / hbm_gbs, 4)}
+
+
 def time_step_ex(w, torch, device, hbm_gbs: float, reps: int = 20) -> dict:
     """The bias-routed step in one launch alone (moe_router_step_ex: bias routing
     with the bias updated in place, dispatch, and the backward of a seeded
@@ -917,8 +945,8 @@ def main() -> int:
                     help="with N > 1 ranks: dp (default) splits one batch over the ranks (dp.data_parallel_step); "
                          "replicas runs the fused step independently on every rank")
     ap.add_argument("--tokens", type=int, default=None,
-                    help="with --section next_steps or step_ex: the workload cut to this many rows")
-    ap.add_argument("--section", choices=("next_steps", "step_ex", "eplb", "taot_match"), default=None,
+                    help="with --section step, next_steps or step_ex: the workload cut to this many rows")
+    ap.add_argument("--section", choices=("step", "next_steps", "step_ex", "eplb", "taot_match"), default=None,
                     help="print only this part of the extra lines (for --workload), as JSON; no bench line")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -932,7 +960,8 @@ def main() -> int:
         wsec = synth.ROUTER_WORKLOADS[args.workload]
         if args.tokens is not None and args.tokens != wsec.T:
             wsec = wsec.with_tokens(args.tokens)
-        part = (time_next_steps(wsec, torch, device, hbm)
+        part = (time_step(wsec, torch, device, hbm) if args.section == "step" else
+                time_next_steps(wsec, torch, device, hbm)
                 if args.section == "next_steps" else
                 time_step_ex(wsec, torch, device, hbm) if args.section == "step_ex" else
                 time_eplb(torch, device, hbm) if args.section == "eplb" else time_taot_match(torch, device, hbm))
