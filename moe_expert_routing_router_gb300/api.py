@@ -8,8 +8,10 @@ runs in the library's CUDA kernels; nothing here computes on the host.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import functools
+import inspect
 
 import torch
 
@@ -28,6 +30,28 @@ _DTYPES = {torch.float32: MOE_DTYPE_FP32, torch.bfloat16: MOE_DTYPE_BF16}
 def _stream_handle(stream: torch.cuda.Stream | None) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(s.cuda_stream)
+
+
+def _on(stream: torch.cuda.Stream | None):
+    """`stream` as torch's current stream while a call allocates (or nothing
+    when the caller gives none: the current stream is the kernels' stream)."""
+    return torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+
+
+def _on_stream(fn):
+    """Runs an entry point with its `stream` argument, when given, as torch's
+    current stream.  The outputs and workspaces it allocates then belong to the
+    stream its kernels write them on, so the caching allocator neither hands
+    the kernels memory that other streams' pending work still uses nor reuses
+    an output before that stream is done with it."""
+    pos = list(inspect.signature(fn).parameters).index("stream")
+
+    @functools.wraps(fn)
+    def call(*args, **kwargs):
+        stream = args[pos] if len(args) > pos else kwargs.get("stream")
+        with _on(stream):
+            return fn(*args, **kwargs)
+    return call
 
 
 def _event_handle(ev: torch.cuda.Event | None) -> int | None:
@@ -69,7 +93,8 @@ class Workspace:
         if need == 0:
             raise ValueError(f"invalid sizes for a workspace: T={T}, E={E}, k={k}")
         if self.buf is None or self.buf.numel() < need:
-            self.buf = torch.empty(need, dtype=torch.uint8, device=self.device)
+            with _on(stream):
+                self.buf = torch.empty(need, dtype=torch.uint8, device=self.device)
             check(lib().moe_workspace_init(_ptr(self.buf), need, _stream_handle(stream)), "moe_workspace_init")
         return _ptr(self.buf), int(self.buf.numel())
 
@@ -116,6 +141,7 @@ def _dispatch_outputs(T: int, E: int, k: int, device, out: dict | None) -> dict:
     }
 
 
+@_on_stream
 def moe_router_fwd(logits: torch.Tensor, k: int, alpha: float, renorm: int = -1, n_ranks: int = 0,
                    ws: Workspace | None = None, out: dict | None = None,
                    stream: torch.cuda.Stream | None = None) -> dict:
@@ -135,6 +161,7 @@ def moe_router_fwd(logits: torch.Tensor, k: int, alpha: float, renorm: int = -1,
     return o
 
 
+@_on_stream
 def moe_router_bwd(logits: torch.Tensor, f: torch.Tensor, alpha: float, grad_scale: float = 1.0,
                    dlogits: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """dL_aux/dlogits with f held constant (C: moe_router_bwd)."""
@@ -152,6 +179,7 @@ def moe_router_bwd(logits: torch.Tensor, f: torch.Tensor, alpha: float, grad_sca
     return dl
 
 
+@_on_stream
 def moe_router_fwd_ex(logits: torch.Tensor, k: int, alpha: float, renorm: int = -1, n_ranks: int = 0,
                       bias: torch.Tensor | None = None, masked_p: bool = False, bias_gamma: float = 0.0,
                       bias_out: torch.Tensor | bool | None = None, ws: Workspace | None = None,
@@ -193,6 +221,7 @@ def moe_router_fwd_ex(logits: torch.Tensor, k: int, alpha: float, renorm: int = 
     return o
 
 
+@_on_stream
 def moe_router_bwd_full(logits: torch.Tensor, f: torch.Tensor, alpha: float, grad_scale: float = 1.0,
                         idx: torch.Tensor | None = None, dgate: torch.Tensor | None = None, renorm: int = -1,
                         masked_p: bool = False, k: int | None = None, dlogits: torch.Tensor | None = None,
@@ -239,6 +268,7 @@ def moe_dispatch_capacity(T: int, E: int, k: int, capacity_factor: float) -> int
     return c
 
 
+@_on_stream
 def moe_dispatch(idx: torch.Tensor, E: int, capacity_factor: float, ws: Workspace | None = None,
                  out: dict | None = None, stream: torch.cuda.Stream | None = None) -> dict:
     """Stable capacity-limited dispatch of idx [T, k] (C: moe_dispatch)."""
@@ -258,6 +288,7 @@ def moe_dispatch(idx: torch.Tensor, E: int, capacity_factor: float, ws: Workspac
     return o
 
 
+@_on_stream
 def moe_shard_capacity_base(counts: torch.Tensor, rank: int, out: torch.Tensor | None = None,
                             stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """cap_base [E] int32: every expert's assignments on the ranks below `rank`,
@@ -275,6 +306,7 @@ def moe_shard_capacity_base(counts: torch.Tensor, rank: int, out: torch.Tensor |
     return base
 
 
+@_on_stream
 def moe_dispatch_sharded(idx: torch.Tensor, E: int, capacity_factor: float, T_total: int, cap_base: torch.Tensor,
                          ws: Workspace | None = None, out: dict | None = None,
                          stream: torch.cuda.Stream | None = None) -> dict:
@@ -299,6 +331,7 @@ def moe_dispatch_sharded(idx: torch.Tensor, E: int, capacity_factor: float, T_to
     return o
 
 
+@_on_stream
 def moe_router_step(logits: torch.Tensor, k: int, alpha: float, capacity_factor: float, renorm: int = -1,
                     n_ranks: int = 0, grad_scale: float = 1.0, ws: Workspace | None = None,
                     out: dict | None = None, stream: torch.cuda.Stream | None = None) -> dict:
@@ -324,6 +357,7 @@ def moe_router_step(logits: torch.Tensor, k: int, alpha: float, capacity_factor:
     return o
 
 
+@_on_stream
 def moe_router_step_ex(logits: torch.Tensor, k: int, alpha: float, capacity_factor: float, renorm: int = -1,
                        n_ranks: int = 0, grad_scale: float = 1.0, bias: torch.Tensor | None = None,
                        bias_gamma: float = 0.0, bias_out: torch.Tensor | bool | None = None, masked_p: bool = False,
@@ -388,6 +422,7 @@ def host_step_outputs(T: int, E: int, k: int, n_ranks: int = 0, pin: bool = True
     return {name: torch.empty(shape, dtype=dt, pin_memory=pin) for name, (shape, dt) in shapes.items()}
 
 
+@_on_stream
 def moe_router_step_host(logits: torch.Tensor, k: int, alpha: float, capacity_factor: float, renorm: int = -1,
                          n_ranks: int = 0, grad_scale: float = 1.0, ws: Workspace | None = None,
                          dev: torch.Tensor | None = None, out: dict | None = None,
@@ -425,6 +460,7 @@ def moe_router_step_host(logits: torch.Tensor, k: int, alpha: float, capacity_fa
     return o
 
 
+@_on_stream
 def moe_router_step_static(logits: torch.Tensor, k: int, alpha: float, capacity_factor: float, renorm: int = -1,
                            n_ranks: int = 0, grad_scale: float = 1.0, out: dict | None = None,
                            stream: torch.cuda.Stream | None = None) -> dict:
@@ -448,6 +484,7 @@ def moe_router_step_static(logits: torch.Tensor, k: int, alpha: float, capacity_
     return o
 
 
+@_on_stream
 def taot_sinkhorn_batched(loads: torch.Tensor, ranks_per_node: int, lam: float, eps: float = 0.0,
                           iters: int = 50, with_plan: bool = True, out: dict | None = None,
                           stream: torch.cuda.Stream | None = None) -> dict:
@@ -470,6 +507,7 @@ def taot_sinkhorn_batched(loads: torch.Tensor, ranks_per_node: int, lam: float, 
     return o
 
 
+@_on_stream
 def moe_eplb_plan(loads: torch.Tensor, num_phys: int, num_gpus: int, num_nodes: int = 1, num_groups: int = 0,
                   out: dict | None = None, stream: torch.cuda.Stream | None = None) -> dict:
     """EPLB replication and balanced packing of B problems (C: moe_eplb_plan).
@@ -492,6 +530,7 @@ def moe_eplb_plan(loads: torch.Tensor, num_phys: int, num_gpus: int, num_nodes: 
     return o
 
 
+@_on_stream
 def taot_match_batched(expert_loads: torch.Tensor, plan: torch.Tensor, ranks_per_node: int, K: int,
                        out: dict | None = None, stream: torch.cuda.Stream | None = None) -> dict:
     """TAOT Phase 2 column-first matching of hot experts to cold ranks (C: taot_match_batched).
@@ -517,6 +556,7 @@ def taot_match_batched(expert_loads: torch.Tensor, plan: torch.Tensor, ranks_per
     return o
 
 
+@_on_stream
 def moe_router_combine(counts: torch.Tensor, P: torch.Tensor, T_shard, k: int, alpha: float, n_ranks: int = 0,
                        masked_p: bool = False, out: dict | None = None,
                        stream: torch.cuda.Stream | None = None) -> dict:

@@ -61,7 +61,11 @@ def data_parallel_forward(logits: torch.Tensor, k: int, alpha: float, renorm: in
     """This rank's routing (idx, gate) and the whole batch's counts, f, P,
     scalars and rank loads; also the batch's T and this rank's T."""
     local = api.moe_router_fwd(logits, k, alpha, renorm=renorm, n_ranks=n_ranks, ws=ws, stream=stream)
-    c_all, p_all, T_shard = gather_shard_stats(local["counts"], local["P"], logits.shape[0], group, T_shard)
+    # The torch side of the exchange (packing copies, collectives, slices) on the
+    # stream of the library's calls: after the forward that wrote counts and P,
+    # before the combine that reads them.
+    with api._on(stream):
+        c_all, p_all, T_shard = gather_shard_stats(local["counts"], local["P"], logits.shape[0], group, T_shard)
     batch = api.moe_router_combine(c_all, p_all, T_shard, k, alpha, n_ranks=n_ranks, stream=stream)
     batch.update(idx=local["idx"], gate=local["gate"], T_total=sum(T_shard), T_local=int(logits.shape[0]),
                  counts_all=c_all, rank=dist.get_rank(group))

@@ -64,3 +64,43 @@ def test_a_missing_library_raises(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "_lib", None)
     with pytest.raises(RuntimeError, match="is not built"):
         _native.lib()
+
+
+class _FakeStream:
+    pass
+
+
+def _recording_stream_ctx(monkeypatch):
+    import contextlib
+    entered = []
+
+    @contextlib.contextmanager
+    def fake(stream):
+        entered.append(stream)
+        yield
+
+    monkeypatch.setattr(torch.cuda, "stream", fake)
+    monkeypatch.setattr(api, "lib", _library_reached)
+    return entered
+
+
+def test_a_given_stream_is_current_while_the_call_allocates(monkeypatch):
+    """With a stream given (by keyword or by position), the call runs with it as
+    torch's current stream, so that what it allocates belongs to the stream its
+    kernels write on; with none given, the current stream is left alone."""
+    entered = _recording_stream_ctx(monkeypatch)
+    s = _FakeStream()
+    with pytest.raises(ValueError):
+        mr.moe_router_step(x, k, 0.01, 1.25, stream=s)
+    with pytest.raises(ValueError):
+        mr.moe_router_bwd(x, f, 0.01, 1.0, None, s)                 # stream by position
+    with pytest.raises(ValueError):
+        mr.moe_router_fwd(x, k, 0.01)
+    assert entered == [s, s]
+
+
+def test_every_device_entry_point_takes_its_stream():
+    """Every device entry point (and the host-buffer step) is wrapped so."""
+    for name in sorted(CALLS) + ["moe_router_step_host"]:
+        fn = getattr(mr, name)
+        assert hasattr(fn, "__wrapped__") and "stream" in fn.__wrapped__.__code__.co_varnames, name
