@@ -724,7 +724,7 @@ def time_oracle(w, budget_s: float, min_steps: int = 1, rows: int | None = None)
     sec = statistics.median(times)
     return {"value": rows / sec, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows} of {w.T} tokens of {w.name} (same E, k, recipe); median of {len(times)} "
-                      f"oracle steps (fwd + dispatch + bwd, fp64 numpy, single thread)",
+                      f"oracle steps (fwd + dispatch + bwd, fp64 numpy, single thread; host nproc {os.cpu_count()})",
             "sec_per_step": sec, "rows": rows}
 
 
@@ -795,7 +795,7 @@ def run_reference(args) -> dict:
     sec = (time.perf_counter() - t0) / args.steps
     value = rows / sec
     desc = (f"{rows} of {w.T} tokens of {w.name} per step; oracle fwd + dispatch + bwd "
-            f"(fp64 numpy, single thread)")
+            f"(fp64 numpy, single thread; host nproc {os.cpu_count()})")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
