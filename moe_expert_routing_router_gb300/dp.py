@@ -15,6 +15,10 @@ rank's ``moe_shard_capacity_base`` is the exclusive scan of the counts across
 the ranks below it, and ``moe_dispatch_sharded`` places the rank's assignments
 after them in each expert's buffer, so the ranks' slots together are those of
 one dispatch over the whole batch.
+
+A rank that holds no rows of the batch still takes part in the exchange, with
+zero counts and P and a token count of 0, so that the other ranks' collectives
+complete; its per-row outputs are empty.
 """
 
 from __future__ import annotations
@@ -60,14 +64,22 @@ def data_parallel_forward(logits: torch.Tensor, k: int, alpha: float, renorm: in
                           group=None, ws=None, stream=None, T_shard=None) -> dict:
     """This rank's routing (idx, gate) and the whole batch's counts, f, P,
     scalars and rank loads; also the batch's T and this rank's T."""
-    local = api.moe_router_fwd(logits, k, alpha, renorm=renorm, n_ranks=n_ranks, ws=ws, stream=stream)
+    T_local, E = int(logits.shape[0]), int(logits.shape[1])
+    if T_local > 0:
+        local = api.moe_router_fwd(logits, k, alpha, renorm=renorm, n_ranks=n_ranks, ws=ws, stream=stream)
+    else:
+        with api._on(stream):
+            local = {"idx": torch.empty((0, k), dtype=torch.int32, device=logits.device),
+                     "gate": torch.empty((0, k), dtype=torch.float32, device=logits.device),
+                     "counts": torch.zeros(E, dtype=torch.int32, device=logits.device),
+                     "P": torch.zeros(E, dtype=torch.float32, device=logits.device)}
     # The torch side of the exchange (packing copies, collectives, slices) on the
     # stream of the library's calls: after the forward that wrote counts and P,
     # before the combine that reads them.
     with api._on(stream):
-        c_all, p_all, T_shard = gather_shard_stats(local["counts"], local["P"], logits.shape[0], group, T_shard)
+        c_all, p_all, T_shard = gather_shard_stats(local["counts"], local["P"], T_local, group, T_shard)
     batch = api.moe_router_combine(c_all, p_all, T_shard, k, alpha, n_ranks=n_ranks, stream=stream)
-    batch.update(idx=local["idx"], gate=local["gate"], T_total=sum(T_shard), T_local=int(logits.shape[0]),
+    batch.update(idx=local["idx"], gate=local["gate"], T_total=sum(T_shard), T_local=T_local,
                  counts_all=c_all, rank=dist.get_rank(group))
     return batch
 
@@ -78,7 +90,17 @@ def data_parallel_dispatch(idx: torch.Tensor, batch: dict, E: int, capacity_fact
     lower ranks' assignments to each expert, from the counts the forward's
     exchange gathered (``batch`` as data_parallel_forward returns it)."""
     base = api.moe_shard_capacity_base(batch["counts_all"], batch["rank"], stream=stream)
-    out = api.moe_dispatch_sharded(idx, E, capacity_factor, batch["T_total"], base, ws=ws, stream=stream)
+    if idx.shape[0] == 0:
+        k, dev = int(idx.shape[1]), idx.device
+        with api._on(stream):
+            out = {"perm": torch.empty(0, dtype=torch.int32, device=dev),
+                   "slot": torch.empty(0, dtype=torch.int32, device=dev),
+                   "offsets": torch.zeros(E + 1, dtype=torch.int32, device=dev),
+                   "kept": torch.zeros(E, dtype=torch.int32, device=dev),
+                   "n_dropped": torch.zeros(1, dtype=torch.int32, device=dev)}
+        out["capacity"] = api.moe_dispatch_capacity(batch["T_total"], E, k, capacity_factor)
+    else:
+        out = api.moe_dispatch_sharded(idx, E, capacity_factor, batch["T_total"], base, ws=ws, stream=stream)
     out["cap_base"] = base
     return out
 
@@ -99,5 +121,10 @@ def data_parallel_step(logits: torch.Tensor, k: int, alpha: float, capacity_fact
 def data_parallel_backward(logits: torch.Tensor, batch: dict, alpha: float, grad_scale: float = 1.0,
                            dlogits=None, stream=None) -> torch.Tensor:
     """dL_aux/dlogits of this rank's rows for the whole batch's loss."""
+    if batch["T_local"] == 0:
+        if dlogits is not None:
+            return dlogits
+        with api._on(stream):
+            return torch.empty((0, logits.shape[1]), dtype=torch.float32, device=logits.device)
     g = shard_grad_scale(grad_scale, batch["T_local"], batch["T_total"])
     return api.moe_router_bwd(logits, batch["f"], alpha, g, dlogits=dlogits, stream=stream)

@@ -151,3 +151,89 @@ def test_global_capacity_dispatch_gloo():
     assert np.array_equal(got[1][2], np.bincount(shards[0].ravel(), minlength=E_D))
     assert np.array_equal(np.concatenate([g[1] for g in got]), whole["slot"])
     assert (whole["slot"] < 0).any() and (whole["slot"] >= 0).any()    # the capacity binds
+
+
+# A rank with no rows of the batch (a ragged split): it must still take part in
+# the exchange, so that the other rank's collectives complete, and return empty
+# per-row outputs; the batch's statistics and capacity are those of the rows
+# that exist.  The kernel calls are stand-ins built from the oracle, and each
+# records that it ran, so that the empty rank is seen to launch none of them.
+E_Z, K_Z, CF_Z, T_Z = 6, 2, 1.0, 40
+
+
+def _rank_empty_main(rank: int, world: int, port: int, out) -> None:
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, str(ROOT))
+    import torch.distributed as dist
+    import oracle
+    from moe_expert_routing_router_gb300 import dp
+    ran = []
+
+    def fake_fwd(logits, k, alpha, renorm=-1, n_ranks=0, ws=None, stream=None):
+        ran.append("fwd")
+        fw = oracle.router.router_forward(logits.numpy(), "fp32", k, alpha)
+        return {"idx": torch.from_numpy(fw["idx"].astype(np.int32)), "gate": torch.from_numpy(fw["gate"]),
+                "counts": torch.from_numpy(fw["counts"].astype(np.int32)),
+                "P": torch.from_numpy(fw["P"].astype(np.float32))}
+
+    def fake_combine(c_all, p_all, T_shard, k, alpha, n_ranks=0, stream=None):
+        T = sum(T_shard)
+        counts = c_all.numpy().sum(axis=0)
+        P = (p_all.numpy().astype(np.float64) * np.asarray(T_shard, np.float64)[:, None]).sum(axis=0) / T
+        return {"counts": counts, "P": P, "f": torch.from_numpy((counts / (T * k)).astype(np.float32))}
+
+    def fake_base(counts, r, out=None, stream=None):
+        return torch.from_numpy(counts.numpy()[:r].sum(axis=0).astype(np.int32))
+
+    def fake_dispatch(idx, E, cf, T_total, base, ws=None, out=None, stream=None):
+        ran.append("dispatch")
+        i = idx.numpy()
+        C = oracle.dispatch.capacity(int(T_total), i.shape[1], E, cf)
+        g = base.numpy()[i.ravel()] + oracle.dispatch.dispatch(i, E, 10 ** 9)["slot"]
+        return {"slot": np.where(g < C, g, -1), "capacity": C}
+
+    def fake_bwd(logits, f, alpha, g, dlogits=None, stream=None):
+        ran.append("bwd")
+        return torch.zeros(logits.shape, dtype=torch.float32)
+
+    dp.api.moe_router_fwd = fake_fwd
+    dp.api.moe_router_combine = fake_combine
+    dp.api.moe_shard_capacity_base = fake_base
+    dp.api.moe_dispatch_sharded = fake_dispatch
+    dp.api.moe_dispatch_capacity = lambda T, E, k, cf: oracle.dispatch.capacity(int(T), k, E, cf)
+    dp.api.moe_router_bwd = fake_bwd
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        rows = T_Z if rank == 0 else 0
+        x = torch.from_numpy(np.random.default_rng(7).standard_normal((T_Z, E_Z)).astype(np.float32)[:rows].copy())
+        b = dp.data_parallel_step(x, K_Z, 0.01, CF_Z)
+        out.put((rank, ran, tuple(b["idx"].shape), np.asarray(b["slot"]), tuple(b["dlogits"].shape),
+                 b["T_local"], b["T_total"], b["capacity"], np.asarray(b["counts"])))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_a_rank_without_rows_gloo():
+    sys.path.insert(0, str(ROOT))
+    import oracle
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    world, port = 2, _free_port()
+    procs = [ctx.Process(target=_rank_empty_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    got = sorted((q.get(timeout=120) for _ in range(world)), key=lambda x: x[0])
+    for p in procs:
+        p.join(timeout=60)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    x = np.random.default_rng(7).standard_normal((T_Z, E_Z)).astype(np.float32)
+    fw = oracle.router.router_forward(x, "fp32", K_Z, 0.01)
+    C = oracle.dispatch.capacity(T_Z, K_Z, E_Z, CF_Z)
+    whole = oracle.dispatch.dispatch(fw["idx"], E_Z, C)
+    (_, ran0, idx0, slot0, dl0, tl0, tt0, c0, n0), (_, ran1, idx1, slot1, dl1, tl1, tt1, c1, n1) = got
+    assert ran0 == ["fwd", "dispatch", "bwd"] and ran1 == []
+    assert idx0 == (T_Z, K_Z) and dl0 == (T_Z, E_Z) and tl0 == T_Z
+    assert idx1 == (0, K_Z) and slot1.shape == (0,) and dl1 == (0, E_Z) and tl1 == 0
+    assert tt0 == tt1 == T_Z and c0 == c1 == C
+    assert np.array_equal(n0, fw["counts"]) and np.array_equal(n1, fw["counts"])
+    assert np.array_equal(slot0, whole["slot"])
